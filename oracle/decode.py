@@ -1,0 +1,294 @@
+"""One denoising step of block-wise masked-diffusion decoding, in plain NumPy fp32.
+
+Test infrastructure only (see the package docstring).  Every function states
+the passage it follows.  Sources:
+
+* prednext.com "拡散言語モデル (diffusion language model)" explainer, section
+  "拡散言語モデルで推論するには": the decoding procedure -- feed [MASK]s,
+  adopt the positions whose output passes a threshold, return the rest to
+  [MASK], repeat until no [MASK] is left.
+* poko-everyday.com Nemotron-TwoTower article, section "技術/ビジネス面": the
+  denoising tower attends bidirectionally inside the block and, by
+  cross-attention, to the frozen context tower's state.
+* dzen.guru Nemotron TwoTower news, "Что нового" / "Как попробовать?": block of
+  16, threshold gamma = 0.8 (higher gamma = more quality), the mock-AR mode
+  that commits one token per step through the diffusion tower.
+
+Where the pages are silent the readings are fixed here (and listed in the
+design notes):
+
+* denoiser = pre-norm dense transformer: RMSNorm -> GQA attention -> residual
+  -> RMSNorm -> SwiGLU -> residual, L layers, final RMSNorm, untied LM head;
+* one softmax per query over [T context keys | S in-block keys], no mask,
+  scale 1/sqrt(D); query head h reads kv head h // (Hq/Hkv);
+* a learned position table Pos[S,H] is added at the embedding; the [MASK]
+  id is V (row V of the embedding); the LM head has V outputs;
+* confidence = the largest softmax probability over the V logits
+  (temperature 1); argmax ties go to the lowest vocab id;
+* commit every masked position with confidence >= gamma; if none qualifies,
+  commit the single most confident masked position (lowest position on
+  ties); mock-AR commits the leftmost masked position;
+* RMSNorm eps = 1e-5, gains from the weights (ones in the synthetic set),
+  silu(x) = x / (1 + exp(-x));
+* activations are stored in bf16 where a bf16 model stores them -- the
+  normalised GEMM inputs, q/k/v, the attention output and the SwiGLU
+  product -- when `act_bf16` is true (the default); the residual stream,
+  scores, softmax and logits stay fp32.  `act_bf16=False` keeps every
+  activation in fp32.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+
+import numpy as np
+
+MODE_THRESHOLD = 0
+MODE_MOCK_AR = 1
+
+F32 = np.float32
+
+# Near-tie thresholds: a position whose top-2 logit gap or whose distance from
+# gamma is below these is reported rather than compared bit-exactly.
+TIE_LOGIT_GAP = 1e-2
+TIE_GAMMA_GAP = 1e-3
+TIE_CONF_GAP = 1e-3
+
+
+def round_bf16(x: np.ndarray) -> np.ndarray:
+    """fp32 -> nearest bf16 (ties to even) -> fp32, elementwise."""
+    a = np.ascontiguousarray(x, dtype=F32)
+    bits = a.view(np.uint32).astype(np.uint64)
+    lsb = (bits >> np.uint64(16)) & np.uint64(1)
+    rounded = ((bits + np.uint64(0x7FFF) + lsb) >> np.uint64(16)) << np.uint64(16)
+    return rounded.astype(np.uint32).view(F32).reshape(a.shape)
+
+
+def rmsnorm(x: np.ndarray, g: np.ndarray, eps: float) -> np.ndarray:
+    """y = x / sqrt(mean(x^2) + eps) * g over the last axis (reading c1/c14)."""
+    x = x.astype(F32, copy=False)
+    ms = np.mean(x * x, axis=-1, keepdims=True, dtype=F32)
+    return (x / np.sqrt(ms + F32(eps))) * g.astype(F32)
+
+
+def silu(x: np.ndarray) -> np.ndarray:
+    """silu(x) = x / (1 + e^-x)."""
+    x = x.astype(F32, copy=False)
+    return x / (F32(1.0) + np.exp(-x))
+
+
+def block_attention(q, k_blk, v_blk, k_ctx, v_ctx):
+    """Block attention for one sequence.
+
+    Bidirectional over the block plus cross-attention to the context
+    (TwoTower article, "技術/ビジネス面"), as one softmax per query over the
+    concatenated keys [context | block].  No mask.
+
+    q      [S, Hq, D]      k_blk, v_blk [S, Hkv, D]
+    k_ctx, v_ctx [Hkv, T, D] (T may be 0)
+    returns [S, Hq, D] fp32
+    """
+    S, Hq, D = q.shape
+    Hkv = k_blk.shape[1]
+    G = Hq // Hkv
+    scale = F32(1.0 / np.sqrt(D))
+    out = np.empty((S, Hq, D), F32)
+    for h in range(Hq):
+        kvh = h // G
+        keys = np.concatenate([k_ctx[kvh], k_blk[:, kvh, :]], axis=0).astype(F32)
+        vals = np.concatenate([v_ctx[kvh], v_blk[:, kvh, :]], axis=0).astype(F32)
+        s = (q[:, h, :].astype(F32) @ keys.T) * scale          # [S, T+S]
+        s = s - s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        p = p / p.sum(axis=1, keepdims=True, dtype=F32)
+        out[:, h, :] = p @ vals
+    return out
+
+
+def linear(x: np.ndarray, w: np.ndarray) -> np.ndarray:
+    """y = x W^T in fp32 for a weight stored [out, in]."""
+    return x.astype(F32, copy=False) @ w.astype(F32, copy=False).T
+
+
+def select_from_logits(logits: np.ndarray):
+    """Per row: confidence = max softmax probability, argmax (lowest id on ties).
+
+    The explainer adopts positions by the size of the network's output
+    ("出力値の大きさ"); the reading here is the top softmax probability at
+    temperature 1: conf = 1 / sum_v exp(l_v - l_max).
+    Returns (conf fp32 [R], argmax int32 [R]).
+    """
+    logits = logits.astype(F32, copy=False)
+    arg = np.argmax(logits, axis=1).astype(np.int32)           # first maximum
+    m = logits.max(axis=1, keepdims=True)
+    s = np.exp(logits - m).sum(axis=1, dtype=F32)
+    conf = (F32(1.0) / s).astype(F32)
+    return conf, arg
+
+
+def lm_head_select(h: np.ndarray, w_lm: np.ndarray):
+    """logits = h W_lm^T (fp32), then `select_from_logits`.  Returns (conf, arg, logits)."""
+    logits = h.astype(F32) @ w_lm.astype(F32).T
+    conf, arg = select_from_logits(logits)
+    return conf, arg, logits
+
+
+def near_tie_flags(logits: np.ndarray, conf: np.ndarray, gamma: float):
+    """Rows whose committed id or commit decision is fragile under rounding.
+
+    A row is flagged when its top-2 logit gap is below TIE_LOGIT_GAP or its
+    confidence lies within TIE_GAMMA_GAP of gamma.
+    """
+    top2 = -np.partition(-logits, 1, axis=1)[:, :2]
+    gap = top2[:, 0] - top2[:, 1]
+    return (gap < TIE_LOGIT_GAP) | (np.abs(conf.astype(np.float64) - gamma) < TIE_GAMMA_GAP)
+
+
+def commit(conf, arg, tokens, mask, gamma: float, mode: int, block: int):
+    """Commit rule for one step, per sequence (explainer steps 3-4; mock-AR from
+    the TwoTower news page).
+
+    conf, arg  [B, S]       tokens [B, S] int32 (updated copy returned)
+    mask       [B] uint32, bit i set = position i still [MASK]
+    Returns (tokens, mask, n_committed [B] int32, fallback [B] bool) where
+    fallback marks sequences where no position reached gamma.
+    """
+    tokens = np.array(tokens, dtype=np.int32, copy=True)
+    mask = np.array(mask, dtype=np.uint32, copy=True)
+    B = tokens.shape[0]
+    n = np.zeros(B, np.int32)
+    fallback = np.zeros(B, bool)
+    g = F32(gamma)
+    for b in range(B):
+        masked = [i for i in range(block) if (int(mask[b]) >> i) & 1]
+        if not masked:
+            continue
+        if mode == MODE_MOCK_AR:
+            chosen = [masked[0]]
+        else:
+            chosen = [i for i in masked if F32(conf[b, i]) >= g]
+            if not chosen:
+                fallback[b] = True
+                best = masked[0]
+                for i in masked[1:]:
+                    if F32(conf[b, i]) > F32(conf[b, best]):
+                        best = i
+                chosen = [best]
+        bits = int(mask[b])
+        for i in chosen:
+            tokens[b, i] = arg[b, i]
+            bits &= ~(1 << i)
+        mask[b] = bits
+        n[b] = len(chosen)
+    return tokens, mask, n, fallback
+
+
+@dataclass
+class OracleModel:
+    """Weights as fp32 arrays holding bf16-rounded values.
+
+    w: dict with embed [V+1,H], pos [S,H], per layer wq/wk/wv/wo/wg/wu/wd
+       ([out,in]) and g_attn/g_mlp [H], g_final [H], lm_head [V,H].
+    k_ctx, v_ctx: [L][B][Hkv][T][D] (only the first `ctx_len` positions are read).
+    """
+
+    cfg: object
+    w: dict
+    k_ctx: np.ndarray
+    v_ctx: np.ndarray
+    ctx_len: int
+
+    @staticmethod
+    def from_bits(cfg, w_bits: dict, k_bits, v_bits, widen):
+        w = {k: widen(v) for k, v in w_bits.items()}
+        return OracleModel(cfg, w, widen(k_bits), widen(v_bits), int(k_bits.shape[3]))
+
+
+@dataclass
+class StepResult:
+    tokens: np.ndarray
+    mask: np.ndarray
+    n_committed: np.ndarray
+    conf: np.ndarray             # [B,S]
+    arg: np.ndarray              # [B,S]
+    logits: np.ndarray           # [B*S, V]
+    near_tie: np.ndarray         # [B,S] bool (position flags)
+    fallback: np.ndarray         # [B] bool
+    attn_out: list = field(default_factory=list)   # per layer [B*S, Hq*D]
+    hidden_final: np.ndarray | None = None          # [B*S, H] final-norm output
+
+
+def denoise_step(model: OracleModel, tokens, mask, gamma: float, mode: int = MODE_THRESHOLD,
+                 act_bf16: bool = True, keep_intermediates: bool = False) -> StepResult:
+    """One reverse-process application over the block, then the commit rule.
+
+    Explainer step 2 ("逆過程ネットワークに入力する") with the TwoTower denoiser
+    reading; steps 3-4 via `commit`.
+    """
+    cfg, w = model.cfg, model.w
+    B, S, H = cfg.batch, cfg.block, cfg.hidden
+    Hq, Hkv, D, V = cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.vocab
+    T = model.ctx_len
+    st = round_bf16 if act_bf16 else (lambda a: a.astype(F32, copy=False))
+    tokens = np.asarray(tokens, np.int32)
+    mask = np.asarray(mask, np.uint32)
+
+    # embedding: [MASK] positions read row V (reading c3/c4)
+    ids = np.array([[V if (int(mask[b]) >> i) & 1 else int(tokens[b, i]) for i in range(S)]
+                    for b in range(B)], np.int64)
+    x = (w["embed"][ids] + w["pos"][None, :, :]).reshape(B * S, H).astype(F32)
+
+    attn_outs = []
+    for l in range(cfg.n_layers):
+        y = st(rmsnorm(x, w[f"g_attn{l}"], cfg.rms_eps))
+        q = st(y @ w[f"wq{l}"].T).reshape(B, S, Hq, D)
+        k = st(y @ w[f"wk{l}"].T).reshape(B, S, Hkv, D)
+        v = st(y @ w[f"wv{l}"].T).reshape(B, S, Hkv, D)
+        o = np.empty((B, S, Hq, D), F32)
+        for b in range(B):
+            o[b] = block_attention(q[b], k[b], v[b], model.k_ctx[l, b, :, :T], model.v_ctx[l, b, :, :T])
+        o = st(o.reshape(B * S, Hq * D))
+        if keep_intermediates:
+            attn_outs.append(o.copy())
+        x = x + o @ w[f"wo{l}"].T
+        y = st(rmsnorm(x, w[f"g_mlp{l}"], cfg.rms_eps))
+        hmid = st(silu(y @ w[f"wg{l}"].T) * (y @ w[f"wu{l}"].T))
+        x = x + hmid @ w[f"wd{l}"].T
+
+    hf = st(rmsnorm(x, w["g_final"], cfg.rms_eps))
+    conf, arg, logits = lm_head_select(hf, w["lm_head"])
+    conf = conf.reshape(B, S)
+    arg = arg.reshape(B, S)
+    new_tok, new_mask, n, fallback = commit(conf, arg, tokens, mask, gamma, mode, S)
+    tie = near_tie_flags(logits, conf.reshape(-1), gamma).reshape(B, S)
+    # In a fallback step the choice between two masked positions whose
+    # confidences nearly tie is fragile too: flag both.
+    for b in np.nonzero(fallback)[0]:
+        masked = [i for i in range(S) if (int(mask[b]) >> i) & 1]
+        c = sorted((float(conf[b, i]) for i in masked), reverse=True)
+        if len(c) > 1 and c[0] - c[1] < TIE_CONF_GAP:
+            for i in masked:
+                if c[0] - float(conf[b, i]) < TIE_CONF_GAP:
+                    tie[b, i] = True
+    return StepResult(new_tok, new_mask, n, conf, arg, logits if keep_intermediates else None,
+                      tie, fallback, attn_outs, hf if keep_intermediates else None)
+
+
+def decode_block(model: OracleModel, gamma: float, mode: int = MODE_THRESHOLD,
+                 max_steps: int | None = None, act_bf16: bool = True):
+    """Fill one block: start all-[MASK], step until no position is masked
+    (explainer step 5).  Returns (tokens [B,S], steps, per-step commit counts)."""
+    cfg = model.cfg
+    S = cfg.block
+    max_steps = 4 * S if max_steps is None else max_steps
+    tokens = np.full((cfg.batch, S), cfg.vocab, np.int32)
+    mask = np.full(cfg.batch, (1 << S) - 1, np.uint32)
+    history = []
+    steps = 0
+    while int(mask.max()) != 0:
+        if steps >= max_steps:
+            raise RuntimeError("step limit reached before the block filled")
+        r = denoise_step(model, tokens, mask, gamma, mode, act_bf16)
+        tokens, mask = r.tokens, r.mask
+        history.append(r.n_committed)
+        steps += 1
+    return tokens, steps, history

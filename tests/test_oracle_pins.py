@@ -1,0 +1,317 @@
+"""Pins for the CPU oracle: brute force, closed forms and invariants (no GPU)."""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests import bruteforce as bf
+
+F32 = np.float32
+
+# A micro workload small enough for the pure-Python brute force.
+MICRO = synth.Config("micro", batch=2, block=4, hidden=16, n_q_heads=4, n_kv_heads=2,
+                     head_dim=4, n_layers=2, mlp=24, vocab=32, ctx_len=5, max_ctx=5)
+
+
+def _micro_model(cfg=MICRO, seed=3, lm_std=None):
+    wb = synth.make_weights(cfg, seed)
+    kb, vb = synth.make_context_kv(cfg, seed)
+    return oracle.OracleModel.from_bits(cfg, wb, kb, vb, synth.bf16_bits_to_f32)
+
+
+# ---------------------------------------------------------------- attention
+
+@pytest.mark.parametrize("T,Hq,Hkv", [(0, 4, 4), (1, 4, 2), (17, 4, 1), (40, 2, 2)])
+def test_attention_vs_bruteforce(T, Hq, Hkv):
+    rng = np.random.default_rng(T * 7 + Hkv)
+    S, D = 16, 8
+    q = rng.standard_normal((S, Hq, D)).astype(F32) * 2
+    kb = rng.standard_normal((S, Hkv, D)).astype(F32)
+    vb = rng.standard_normal((S, Hkv, D)).astype(F32)
+    kc = rng.standard_normal((Hkv, T, D)).astype(F32)
+    vc = rng.standard_normal((Hkv, T, D)).astype(F32)
+    got = oracle.block_attention(q, kb, vb, kc, vc)
+    ref = np.array(bf.block_attention(q.tolist(), kb.tolist(), vb.tolist(), kc.tolist(), vc.tolist()))
+    np.testing.assert_allclose(got, ref, rtol=2e-5, atol=2e-6)
+
+
+def test_attention_constant_values():
+    """Constant value rows give that constant whatever the scores."""
+    rng = np.random.default_rng(1)
+    S, Hq, Hkv, D, T = 16, 4, 2, 8, 33
+    q = rng.standard_normal((S, Hq, D)).astype(F32) * 3
+    kb = rng.standard_normal((S, Hkv, D)).astype(F32)
+    kc = rng.standard_normal((Hkv, T, D)).astype(F32)
+    c = rng.standard_normal((Hkv, D)).astype(F32)
+    vb = np.broadcast_to(c[None], (S, Hkv, D)).copy()
+    vc = np.broadcast_to(c[:, None], (Hkv, T, D)).copy()
+    out = oracle.block_attention(q, kb, vb, kc, vc)
+    for h in range(Hq):
+        np.testing.assert_allclose(out[:, h], np.broadcast_to(c[h // 2], (S, D)), rtol=1e-5, atol=1e-6)
+
+
+def test_attention_zero_query_is_uniform_mean():
+    """q = 0 makes every score equal: the output is the mean of all T+S values."""
+    rng = np.random.default_rng(2)
+    S, Hq, Hkv, D, T = 16, 2, 1, 8, 9
+    q = np.zeros((S, Hq, D), F32)
+    kb = rng.standard_normal((S, Hkv, D)).astype(F32)
+    vb = rng.standard_normal((S, Hkv, D)).astype(F32)
+    kc = rng.standard_normal((Hkv, T, D)).astype(F32)
+    vc = rng.standard_normal((Hkv, T, D)).astype(F32)
+    out = oracle.block_attention(q, kb, vb, kc, vc)
+    mean = np.concatenate([vc[0], vb[:, 0]]).mean(axis=0)
+    np.testing.assert_allclose(out[:, 0], np.broadcast_to(mean, (S, D)), rtol=1e-5, atol=1e-6)
+
+
+def test_attention_gqa_equals_repeated_mha():
+    """GQA with G query heads per kv head equals MHA with each kv head repeated G times."""
+    rng = np.random.default_rng(3)
+    S, Hq, Hkv, D, T = 16, 8, 2, 8, 12
+    q = rng.standard_normal((S, Hq, D)).astype(F32)
+    kb = rng.standard_normal((S, Hkv, D)).astype(F32)
+    vb = rng.standard_normal((S, Hkv, D)).astype(F32)
+    kc = rng.standard_normal((Hkv, T, D)).astype(F32)
+    vc = rng.standard_normal((Hkv, T, D)).astype(F32)
+    gqa = oracle.block_attention(q, kb, vb, kc, vc)
+    rep = lambda a, ax: np.repeat(a, Hq // Hkv, axis=ax)
+    mha = oracle.block_attention(q, rep(kb, 1), rep(vb, 1), rep(kc, 0), rep(vc, 0))
+    np.testing.assert_allclose(gqa, mha, rtol=1e-6, atol=1e-7)
+
+
+def test_attention_is_bidirectional_and_sees_context():
+    """Changing the LAST block key changes the FIRST query's output (no causal
+    mask), and changing one context value changes every query's output."""
+    rng = np.random.default_rng(4)
+    S, Hq, Hkv, D, T = 16, 2, 2, 8, 6
+    q = rng.standard_normal((S, Hq, D)).astype(F32)
+    kb = rng.standard_normal((S, Hkv, D)).astype(F32)
+    vb = rng.standard_normal((S, Hkv, D)).astype(F32)
+    kc = rng.standard_normal((Hkv, T, D)).astype(F32)
+    vc = rng.standard_normal((Hkv, T, D)).astype(F32)
+    base = oracle.block_attention(q, kb, vb, kc, vc)
+    vb2 = vb.copy()
+    vb2[-1] += 5
+    assert np.abs(oracle.block_attention(q, kb, vb2, kc, vc)[0] - base[0]).max() > 1e-4
+    vc2 = vc.copy()
+    vc2[:, 0] += 5
+    assert np.all(np.abs(oracle.block_attention(q, kb, vb, kc, vc2) - base).max(axis=2) > 1e-5)
+
+
+# ---------------------------------------------------------- confidence select
+
+def test_select_equal_logits():
+    V = 4096
+    conf, arg = oracle.select_from_logits(np.full((3, V), 1.25, F32))
+    np.testing.assert_allclose(conf, 1.0 / V, rtol=1e-5)
+    assert (arg == 0).all()
+
+
+@pytest.mark.parametrize("delta", [0.5, 3.0, 9.0])
+def test_select_single_lead_closed_form(delta):
+    V, lead = 1000, 417
+    lg = np.zeros((1, V), F32)
+    lg[0, lead] = delta
+    conf, arg = oracle.select_from_logits(lg)
+    assert arg[0] == lead
+    np.testing.assert_allclose(conf[0], 1.0 / (1.0 + (V - 1) * math.exp(-delta)), rtol=1e-5)
+
+
+def test_select_vs_bruteforce_and_first_max():
+    rng = np.random.default_rng(5)
+    lg = (rng.standard_normal((6, 300)) * 8).astype(F32)
+    lg[2, 10] = lg[2, 250] = lg[2].max() + 1.0            # tie: lowest id wins
+    conf, arg = oracle.select_from_logits(lg)
+    for r in range(lg.shape[0]):
+        c, a = bf.confidence_argmax(lg[r].astype(np.float64).tolist())
+        assert arg[r] == a
+        assert abs(conf[r] - c) <= 1e-5 * c
+    assert arg[2] == 10
+
+
+# ---------------------------------------------------------------- norm / MLP
+
+def test_rmsnorm_closed_forms():
+    H = 64
+    g = np.linspace(0.5, 1.5, H).astype(F32)
+    x = np.full((1, H), 3.0, F32)
+    np.testing.assert_allclose(oracle.rmsnorm(x, g, 1e-5)[0], 3.0 / math.sqrt(9.0 + 1e-5) * g, rtol=1e-6)
+    rng = np.random.default_rng(6)
+    x = rng.standard_normal((4, H)).astype(F32)
+    y1 = oracle.rmsnorm(x, g, 0.0)
+    y2 = oracle.rmsnorm(x * 37.0, g, 0.0)
+    np.testing.assert_allclose(y1, y2, rtol=1e-5, atol=1e-6)
+    for r in range(4):
+        np.testing.assert_allclose(y1[r], bf.rmsnorm(x[r].tolist(), g.tolist(), 0.0), rtol=1e-5, atol=1e-6)
+
+
+def test_silu_values():
+    x = np.array([0.0, 1.0, -1.0, 20.0, -20.0], F32)
+    ref = np.array([0.0, 1 / (1 + math.exp(-1)), -1 / (1 + math.exp(1)), 20.0, -20 / (1 + math.exp(20))])
+    np.testing.assert_allclose(oracle.silu(x), ref, rtol=1e-6, atol=1e-12)
+
+
+def test_round_bf16_matches_bruteforce():
+    rng = np.random.default_rng(7)
+    x = (rng.standard_normal(2000) * np.exp(rng.uniform(-20, 20, 2000))).astype(F32)
+    x[:4] = [1.00390625, 1.01171875, -1.00390625, 0.0]      # exact ties -> even
+    got = oracle.round_bf16(x)
+    ref = np.array([bf.bf16(float(v)) for v in x], F32)
+    assert np.array_equal(got.view(np.uint32), ref.view(np.uint32))
+    assert got[0] == 1.0 and got[1] == 1.015625
+
+
+# ---------------------------------------------------------------- full step
+
+def _nested(a):
+    return a.tolist()
+
+
+@pytest.mark.parametrize("round_act", [False, True])
+def test_full_step_vs_bruteforce(round_act):
+    cfg = MICRO
+    m = _micro_model(cfg)
+    tok, mask = synth.make_tokens(cfg, seed=1, masked_frac=0.6)
+    r = oracle.denoise_step(m, tok, mask, 0.8, act_bf16=round_act, keep_intermediates=True)
+    w = {k: _nested(v) for k, v in m.w.items()}
+    logits, conf, arg = bf.denoise_step(cfg, w, _nested(m.k_ctx), _nested(m.v_ctx),
+                                        tok.tolist(), [int(v) for v in mask], round_act)
+    tol = 1e-2 if round_act else 2e-4
+    np.testing.assert_allclose(r.logits, np.array(logits), rtol=tol, atol=tol * 0.1)
+    np.testing.assert_allclose(r.conf.reshape(-1), np.array(conf), rtol=tol, atol=1e-6)
+    assert (r.arg.reshape(-1) == np.array(arg)).all()
+
+
+def test_full_step_linear_in_lm_head_scale():
+    """Scaling the LM head by c scales the logits by c exactly up to rounding."""
+    m = _micro_model()
+    tok, mask = synth.make_tokens(MICRO, seed=2)
+    r1 = oracle.denoise_step(m, tok, mask, 0.8, act_bf16=False, keep_intermediates=True)
+    m.w["lm_head"] = m.w["lm_head"] * F32(4.0)
+    r2 = oracle.denoise_step(m, tok, mask, 0.8, act_bf16=False, keep_intermediates=True)
+    np.testing.assert_allclose(r2.logits, 4 * r1.logits, rtol=1e-6, atol=1e-6)
+
+
+# ------------------------------------------------------------- commit rule
+
+def test_commit_exhaustive_masks():
+    """Every mask of a 16-position block, two crafted confidence rows, both modes,
+    against the set-based statement of the rule."""
+    S = 16
+    rows = [np.array([0.1, 0.85, 0.3, 0.8, 0.79, 0.95, 0.2, 0.8, 0.5, 0.99, 0.01, 0.6,
+                      0.7, 0.81, 0.4, 0.3], F32),
+            np.array([0.5, 0.7, 0.7, 0.1, 0.2, 0.7, 0.3, 0.6, 0.1, 0.2, 0.3, 0.4,
+                      0.5, 0.6, 0.7, 0.05], F32)]
+    masks = np.arange(1, 1 << S, dtype=np.uint32)
+    for conf in rows:
+        arg = (np.arange(S, dtype=np.int32) * 97 + 5)[None]
+        for mode in (oracle.MODE_THRESHOLD, oracle.MODE_MOCK_AR):
+            B = len(masks)
+            toks = np.full((B, S), 4096, np.int32)
+            new_tok, new_mask, n, _ = oracle.commit(np.broadcast_to(conf, (B, S)),
+                                                    np.broadcast_to(arg, (B, S)), toks, masks,
+                                                    0.8, mode, S)
+            for b in range(0, B, 7):             # every 7th mask keeps this to seconds
+                mk = int(masks[b])
+                masked = [i for i in range(S) if (mk >> i) & 1]
+                want = bf.commit_sets(conf.tolist(), masked, F32(0.8), mode == oracle.MODE_MOCK_AR)
+                got = {i for i in range(S) if (mk >> i) & 1 and not (int(new_mask[b]) >> i) & 1}
+                assert got == want, (mk, mode)
+                assert n[b] == len(want)
+                for i in range(S):
+                    assert new_tok[b, i] == (arg[0, i] if i in want else 4096)
+
+
+def test_commit_gamma_zero_and_above_one():
+    rng = np.random.default_rng(8)
+    conf = rng.uniform(0, 1, (5, 16)).astype(F32)
+    arg = rng.integers(0, 100, (5, 16)).astype(np.int32)
+    tok = np.full((5, 16), 100, np.int32)
+    mask = np.array([0xFFFF, 0x0F0F, 0x8001, 0x1, 0x7FFE], np.uint32)
+    _, m0, n0, _ = oracle.commit(conf, arg, tok, mask, 0.0, oracle.MODE_THRESHOLD, 16)
+    assert (m0 == 0).all() and list(n0) == [bin(int(v)).count("1") for v in mask]
+    _, m2, n2, fb = oracle.commit(conf, arg, tok, mask, 1.5, oracle.MODE_THRESHOLD, 16)
+    assert (n2 == 1).all() and fb.all()
+    for b in range(5):
+        gone = int(mask[b]) & ~int(m2[b])
+        i = gone.bit_length() - 1
+        masked = [j for j in range(16) if (int(mask[b]) >> j) & 1]
+        assert conf[b, i] == max(conf[b, j] for j in masked)
+
+
+def test_commit_monotone_in_gamma():
+    rng = np.random.default_rng(9)
+    conf = rng.uniform(0, 1, (64, 16)).astype(F32)
+    arg = np.zeros((64, 16), np.int32)
+    tok = np.zeros((64, 16), np.int32)
+    mask = rng.integers(1, 1 << 16, 64).astype(np.uint32)
+    prev = None
+    for g in (0.1, 0.3, 0.5, 0.8, 0.95):
+        _, m, _, fb = oracle.commit(conf, arg, tok, mask, g, oracle.MODE_THRESHOLD, 16)
+        done = mask & ~m
+        if prev is not None:
+            # a larger gamma commits a subset, unless the fallback picked its one position
+            ok = ((done & ~prev) == 0) | fb
+            assert ok.all()
+        prev = done
+
+
+# ------------------------------------------------------- decode invariants
+
+@pytest.fixture(scope="module")
+def tiny_model():
+    cfg = synth.TINY.replace(batch=2, ctx_len=64, max_ctx=64)
+    wb = synth.make_weights(cfg, 0)
+    kb, vb = synth.make_context_kv(cfg, 0)
+    return oracle.OracleModel.from_bits(cfg, wb, kb, vb, synth.bf16_bits_to_f32)
+
+
+def test_decode_gamma_zero_fills_in_one_step(tiny_model):
+    tok, steps, hist = oracle.decode_block(tiny_model, 0.0)
+    assert steps == 1 and (hist[0] == 16).all()
+
+
+def test_decode_gamma_above_one_takes_block_steps(tiny_model):
+    tok, steps, hist = oracle.decode_block(tiny_model, 1.01)
+    assert steps == 16 and all((h == 1).all() for h in hist)
+
+
+def test_decode_mock_ar_is_left_to_right(tiny_model):
+    cfg = tiny_model.cfg
+    tokens = np.full((cfg.batch, 16), cfg.vocab, np.int32)
+    mask = np.full(cfg.batch, 0xFFFF, np.uint32)
+    for step in range(16):
+        r = oracle.denoise_step(tiny_model, tokens, mask, 0.8, oracle.MODE_MOCK_AR)
+        assert (r.mask == (0xFFFF & ~((1 << (step + 1)) - 1))).all()
+        tokens, mask = r.tokens, r.mask
+
+
+def test_decode_committed_never_change_and_progress(tiny_model):
+    cfg = tiny_model.cfg
+    tokens = np.full((cfg.batch, 16), cfg.vocab, np.int32)
+    mask = np.full(cfg.batch, 0xFFFF, np.uint32)
+    while mask.max():
+        r = oracle.denoise_step(tiny_model, tokens, mask, 0.8)
+        for b in range(cfg.batch):
+            if mask[b]:
+                assert r.n_committed[b] >= 1
+            for i in range(16):
+                if not (int(mask[b]) >> i) & 1:
+                    assert r.tokens[b, i] == tokens[b, i]
+            assert int(r.mask[b]) & ~int(mask[b]) == 0
+        tokens, mask = r.tokens, r.mask
+    assert (tokens < cfg.vocab).all()
+
+
+def test_batch_independence(tiny_model):
+    """Sequence b decoded in a batch equals sequence b decoded alone."""
+    cfg = tiny_model.cfg
+    tok_all, _, _ = oracle.decode_block(tiny_model, 0.8)
+    for b in range(cfg.batch):
+        one = oracle.OracleModel(cfg.replace(batch=1), tiny_model.w,
+                                 tiny_model.k_ctx[:, b:b + 1], tiny_model.v_ctx[:, b:b + 1],
+                                 tiny_model.ctx_len)
+        tok_one, _, _ = oracle.decode_block(one, 0.8)
+        assert (tok_one[0] == tok_all[b]).all()
