@@ -1,0 +1,718 @@
+// C-ABI of libdd: context and workspace management, tensor maps, the
+// per-step launch sequence (captured once into a CUDA graph), the decode
+// loop, and the single-kernel entry points.  See include/dd.h.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <string>
+#include <vector>
+
+#include "../../include/dd.h"
+#include "kernels.h"
+
+namespace {
+
+thread_local std::string g_last_error;
+
+dd_status fail(dd_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_last_error = buf;
+  return s;
+}
+
+#define DD_CUDA(call)                                                                                   \
+  do {                                                                                                  \
+    cudaError_t e_ = (call);                                                                            \
+    if (e_ != cudaSuccess) return fail(DD_ERR_CUDA, "%s failed: %s", #call, cudaGetErrorString(e_));   \
+  } while (0)
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  if (!fn) {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  }
+  return fn;
+}
+
+}  // namespace
+
+namespace dd {
+
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_map_3d(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {cols, rows, planes};
+  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  cuuint32_t box[3] = {64, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace dd
+
+// ---------------------------------------------------------------------------
+// Context
+// ---------------------------------------------------------------------------
+
+struct Layout {
+  size_t kc, vc, x, y, qkv, attn, hmid, part, attn_part, sel_m, sel_s, sel_a, conf, arg, tok, mask, ncommit, small,
+      params, total;
+  size_t part_elems;
+  int alloc_ctx;
+  dd::GemmPlan p_qkv, p_o, p_gu, p_d, p_lm, p_store;
+  dd::AttnPlan p_attn;
+};
+
+struct dd_ctx {
+  dd_config cfg;
+  int R, G, qkvw, HqD;
+  Layout L;
+  uint8_t* ws;
+  int ctx_len;
+  bool have_weights;
+  dd_weights w;
+  std::vector<CUtensorMap> m_wqkv, m_wo, m_wgu, m_wd;
+  CUtensorMap m_lm, m_y_b, m_attn_b, m_h_b, m_y_a, m_kc, m_vc;
+  cudaStream_t cap_stream;
+  cudaGraphExec_t exec;
+  int32_t* hpin;  // pinned host: [0] remaining, [1] status
+  uint64_t timeout_ns;
+  int device;
+};
+
+namespace {
+
+template <typename T>
+T* at(uint8_t* ws, size_t off) {
+  return reinterpret_cast<T*>(ws + off);
+}
+
+dd_status check_config(const dd_config* c) {
+  if (!c) return fail(DD_ERR_INVALID_ARG, "config is NULL");
+  if (c->batch < 1 || c->block < 1 || c->block > 32)
+    return fail(DD_ERR_INVALID_ARG, "batch must be >= 1 and block in [1, 32] (got %d, %d)", c->batch, c->block);
+  if ((c->batch * c->block) % 16)
+    return fail(DD_ERR_UNSUPPORTED, "batch*block must be a multiple of 16 (got %d)", c->batch * c->block);
+  if (c->head_dim != 64 && c->head_dim != 128)
+    return fail(DD_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", c->head_dim);
+  if (c->n_q_heads < 1 || c->n_kv_heads < 1 || c->n_q_heads % c->n_kv_heads)
+    return fail(DD_ERR_INVALID_ARG, "n_kv_heads must divide n_q_heads (got %d, %d)", c->n_q_heads, c->n_kv_heads);
+  const int G = c->n_q_heads / c->n_kv_heads;
+  if ((G * c->block) % 16 || G * c->block > 128)
+    return fail(DD_ERR_UNSUPPORTED, "(n_q_heads/n_kv_heads)*block must be a multiple of 16 and <= 128 (got %d)",
+                G * c->block);
+  if (c->hidden < 128 || c->hidden % 128)
+    return fail(DD_ERR_UNSUPPORTED, "hidden must be a multiple of 128 (got %d)", c->hidden);
+  if (c->mlp < 128 || c->mlp % 128) return fail(DD_ERR_UNSUPPORTED, "mlp must be a multiple of 128 (got %d)", c->mlp);
+  if (((c->n_q_heads + 2 * c->n_kv_heads) * c->head_dim) % 128)
+    return fail(DD_ERR_UNSUPPORTED, "(n_q_heads+2*n_kv_heads)*head_dim must be a multiple of 128");
+  if ((c->n_q_heads * c->head_dim) % 64) return fail(DD_ERR_UNSUPPORTED, "n_q_heads*head_dim must be a multiple of 64");
+  if (c->vocab < 256 || c->vocab % 256)
+    return fail(DD_ERR_UNSUPPORTED, "vocab must be a multiple of 256 (got %d)", c->vocab);
+  if (c->n_layers < 1) return fail(DD_ERR_INVALID_ARG, "n_layers must be >= 1");
+  if (c->max_ctx < 0) return fail(DD_ERR_INVALID_ARG, "max_ctx must be >= 0");
+  if (!(c->rms_eps >= 0.f)) return fail(DD_ERR_INVALID_ARG, "rms_eps must be >= 0");
+  return DD_OK;
+}
+
+Layout make_layout(const dd_config& c) {
+  Layout L{};
+  const int R = c.batch * c.block;
+  const int qkvw = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
+  const int HqD = c.n_q_heads * c.head_dim;
+  L.alloc_ctx = c.max_ctx < 64 ? 64 : c.max_ctx;
+  L.p_qkv = dd::plan_gemm(dd::kEpiPartial, R, qkvw, c.hidden);
+  L.p_o = dd::plan_gemm(dd::kEpiPartial, R, c.hidden, HqD);
+  L.p_gu = dd::plan_gemm(dd::kEpiPartial, R, 2 * c.mlp, c.hidden);
+  L.p_d = dd::plan_gemm(dd::kEpiPartial, R, c.hidden, c.mlp);
+  L.p_lm = dd::plan_gemm(dd::kEpiSelect, R, c.vocab, c.hidden);
+  L.p_store = dd::plan_gemm(dd::kEpiStore, R, c.vocab, c.hidden);
+  L.p_attn = dd::plan_attention(c.batch, c.block, c.n_q_heads, c.n_kv_heads, c.head_dim, c.max_ctx);
+  size_t pe = 0;
+  auto upd = [&](const dd::GemmPlan& p, int N) {
+    size_t e = (size_t)p.splits * R * N;
+    if (e > pe) pe = e;
+  };
+  upd(L.p_qkv, qkvw);
+  upd(L.p_o, c.hidden);
+  upd(L.p_gu, 2 * c.mlp);
+  upd(L.p_d, c.hidden);
+  L.part_elems = pe;
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align_up(off + bytes, 256);
+    return o;
+  };
+  const size_t kv = (size_t)c.n_layers * c.batch * c.n_kv_heads * L.alloc_ctx * c.head_dim * 2;
+  L.kc = take(kv);
+  L.vc = take(kv);
+  L.x = take((size_t)R * c.hidden * 4);
+  L.y = take((size_t)R * c.hidden * 2);
+  L.qkv = take((size_t)R * qkvw * 2);
+  L.attn = take((size_t)R * HqD * 2);
+  L.hmid = take((size_t)R * c.mlp * 2);
+  L.part = take(pe * 4);
+  L.attn_part = take(dd::attention_partial_bytes(L.p_attn, c.batch, c.n_kv_heads));
+  const size_t sel = (size_t)L.p_lm.n_tiles * R * 4;
+  L.sel_m = take(sel);
+  L.sel_s = take(sel);
+  L.sel_a = take(sel);
+  L.conf = take((size_t)R * 4);
+  L.arg = take((size_t)R * 4);
+  L.tok = take((size_t)R * 4);
+  L.mask = take((size_t)c.batch * 4);
+  L.ncommit = take((size_t)c.batch * 4);
+  L.small = take(16);   // [0] remaining, [1] status, [2] ctx_len
+  L.params = take(8);   // gamma, mode
+  L.total = off;
+  return L;
+}
+
+int32_t* small_ptr(dd_ctx* c) { return at<int32_t>(c->ws, c->L.small); }
+
+dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe) {
+  const dd_config& cf = c->cfg;
+  const Layout& L = c->L;
+  uint8_t* ws = c->ws;
+  const int R = c->R, H = cf.hidden, F = cf.mlp;
+  float* x = at<float>(ws, L.x);
+  void* y = ws + L.y;
+  float* part = at<float>(ws, L.part);
+  int* status = small_ptr(c) + 1;
+  const uint8_t* g_attn = static_cast<const uint8_t*>(c->w.g_attn);
+  const uint8_t* g_mlp = static_cast<const uint8_t*>(c->w.g_mlp);
+
+  DD_CUDA(dd::launch_embed_norm(at<int32_t>(ws, L.tok), at<uint32_t>(ws, L.mask), c->w.embed, c->w.pos, g_attn,
+                                x, y, cf.batch, cf.block, H, cf.vocab, cf.rms_eps, st));
+  for (int l = 0; l < cf.n_layers; ++l) {
+    dd::GemmOut o{};
+    o.partial = part;
+    o.rows_valid = R;
+    // q|k|v = y Wqkv^T
+    o.ld = c->qkvw;
+    o.split_stride = (long long)R * c->qkvw;
+    DD_CUDA(dd::launch_gemm(L.p_qkv, c->m_wqkv[l], c->m_y_b, o, status, c->timeout_ns, st));
+    DD_CUDA(dd::launch_reduce_bf16(part, L.p_qkv.splits, o.split_stride, R, c->qkvw, ws + L.qkv, st));
+    // block attention
+    dd::AttnArgs a{};
+    a.qkv = ws + L.qkv;
+    a.ld_qkv = c->qkvw;
+    a.B = cf.batch;
+    a.S = cf.block;
+    a.Hq = cf.n_q_heads;
+    a.Hkv = cf.n_kv_heads;
+    a.G = c->G;
+    a.ctx_len = small_ptr(c) + 2;
+    a.z0 = l * cf.batch * cf.n_kv_heads;
+    a.out = ws + L.attn;
+    a.ld_out = c->HqD;
+    a.part_o = at<float>(ws, L.attn_part);
+    a.part_ml = reinterpret_cast<float2*>(
+        ws + L.attn_part +
+        align_up((size_t)cf.batch * cf.n_kv_heads * L.p_attn.n_splits * L.p_attn.rows * cf.head_dim * 4, 16));
+    a.scale_log2 = 1.4426950408889634f / sqrtf((float)cf.head_dim);
+    a.status = status;
+    a.timeout_ns = c->timeout_ns;
+    DD_CUDA(dd::launch_attention(L.p_attn, a, c->m_kc, c->m_vc, st));
+    if (probe && probe->attn_out)
+      DD_CUDA(cudaMemcpyAsync(static_cast<uint8_t*>(probe->attn_out) + (size_t)l * R * c->HqD * 2, ws + L.attn,
+                              (size_t)R * c->HqD * 2, cudaMemcpyDeviceToDevice, st));
+    // x += attn Wo^T ; y = norm(x) g_mlp
+    o.ld = H;
+    o.split_stride = (long long)R * H;
+    DD_CUDA(dd::launch_gemm(L.p_o, c->m_wo[l], c->m_attn_b, o, status, c->timeout_ns, st));
+    DD_CUDA(dd::launch_reduce_residual_norm(part, L.p_o.splits, o.split_stride, x, g_mlp + (size_t)l * H * 2, y, R, H,
+                                            cf.rms_eps, st));
+    // h = silu(y Wg^T) * (y Wu^T)
+    o.ld = 2 * F;
+    o.split_stride = (long long)R * 2 * F;
+    DD_CUDA(dd::launch_gemm(L.p_gu, c->m_wgu[l], c->m_y_b, o, status, c->timeout_ns, st));
+    DD_CUDA(dd::launch_reduce_swiglu(part, L.p_gu.splits, o.split_stride, ws + L.hmid, R, F, st));
+    // x += h Wd^T ; y = norm(x) g (next layer's attention norm, or the final norm)
+    o.ld = H;
+    o.split_stride = (long long)R * H;
+    DD_CUDA(dd::launch_gemm(L.p_d, c->m_wd[l], c->m_h_b, o, status, c->timeout_ns, st));
+    const void* gn = (l + 1 < cf.n_layers) ? (const void*)(g_attn + (size_t)(l + 1) * H * 2) : c->w.g_final;
+    DD_CUDA(dd::launch_reduce_residual_norm(part, L.p_d.splits, o.split_stride, x, gn, y, R, H, cf.rms_eps, st));
+  }
+  // LM head + fused select
+  dd::GemmOut so{};
+  so.rows_valid = R;
+  so.sel_m = at<float>(ws, L.sel_m);
+  so.sel_s = at<float>(ws, L.sel_s);
+  so.sel_a = at<int>(ws, L.sel_a);
+  DD_CUDA(dd::launch_gemm(L.p_lm, c->m_y_a, c->m_lm, so, status, c->timeout_ns, st));
+  DD_CUDA(dd::launch_select_combine(so.sel_m, so.sel_s, so.sel_a, L.p_lm.n_tiles, R, at<float>(ws, L.conf),
+                                    at<int>(ws, L.arg), st));
+  if (probe) {
+    if (probe->hidden)
+      DD_CUDA(cudaMemcpyAsync(probe->hidden, y, (size_t)R * H * 2, cudaMemcpyDeviceToDevice, st));
+    if (probe->conf) DD_CUDA(cudaMemcpyAsync(probe->conf, ws + L.conf, (size_t)R * 4, cudaMemcpyDeviceToDevice, st));
+    if (probe->arg) DD_CUDA(cudaMemcpyAsync(probe->arg, ws + L.arg, (size_t)R * 4, cudaMemcpyDeviceToDevice, st));
+    if (probe->logits) {
+      dd::GemmOut lo{};
+      lo.partial = probe->logits;
+      lo.ld = cf.vocab;
+      lo.rows_valid = R;
+      DD_CUDA(dd::launch_gemm(L.p_store, c->m_y_a, c->m_lm, lo, status, c->timeout_ns, st));
+    }
+  }
+  DD_CUDA(dd::launch_commit(at<float>(ws, L.conf), at<int>(ws, L.arg), at<int32_t>(ws, L.tok),
+                            at<uint32_t>(ws, L.mask), at<float>(ws, L.params), 0.f, 0,
+                            at<int32_t>(ws, L.ncommit), small_ptr(c), cf.batch, cf.block, st));
+  return DD_OK;
+}
+
+dd_status ensure_graph(dd_ctx* c) {
+  if (c->exec) return DD_OK;
+  cudaGraph_t g = nullptr;
+  DD_CUDA(cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
+  dd_status s = enqueue_step(c, c->cap_stream, nullptr);
+  cudaError_t e = cudaStreamEndCapture(c->cap_stream, &g);
+  if (s != DD_OK) {
+    if (g) cudaGraphDestroy(g);
+    return s;
+  }
+  if (e != cudaSuccess) return fail(DD_ERR_CUDA, "graph capture failed: %s", cudaGetErrorString(e));
+  e = cudaGraphInstantiate(&c->exec, g, 0);
+  cudaGraphDestroy(g);
+  if (e != cudaSuccess) {
+    c->exec = nullptr;
+    return fail(DD_ERR_CUDA, "graph instantiate failed: %s", cudaGetErrorString(e));
+  }
+  return DD_OK;
+}
+
+dd_status check_ctx(dd_ctx* c) {
+  if (!c) return fail(DD_ERR_INVALID_ARG, "ctx is NULL");
+  if (!c->have_weights) return fail(DD_ERR_NOT_READY, "weights not set (call dd_init_weights)");
+  int dev = -1;
+  DD_CUDA(cudaGetDevice(&dev));
+  if (dev != c->device) return fail(DD_ERR_INVALID_ARG, "current device %d is not the context's device %d", dev, c->device);
+  return DD_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* dd_status_string(dd_status s) {
+  switch (s) {
+    case DD_OK: return "ok";
+    case DD_ERR_INVALID_ARG: return "invalid argument";
+    case DD_ERR_CUDA: return "CUDA error";
+    case DD_ERR_NOT_READY: return "not ready";
+    case DD_ERR_STEP_LIMIT: return "step limit reached";
+    case DD_ERR_DEVICE_TIMEOUT: return "device wait timed out";
+    case DD_ERR_UNSUPPORTED: return "unsupported shape";
+  }
+  return "unknown status";
+}
+
+const char* dd_last_error(void) { return g_last_error.c_str(); }
+
+dd_status dd_workspace_size(const dd_config* cfg, size_t* bytes) {
+  dd_status s = check_config(cfg);
+  if (s != DD_OK) return s;
+  if (!bytes) return fail(DD_ERR_INVALID_ARG, "bytes is NULL");
+  *bytes = make_layout(*cfg).total;
+  return DD_OK;
+}
+
+dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_bytes, dd_ctx** out) {
+  dd_status s = check_config(cfg);
+  if (s != DD_OK) return s;
+  if (!out) return fail(DD_ERR_INVALID_ARG, "out is NULL");
+  *out = nullptr;
+  if (!workspace) return fail(DD_ERR_INVALID_ARG, "workspace is NULL");
+  if (reinterpret_cast<uintptr_t>(workspace) % 256) return fail(DD_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  Layout L = make_layout(*cfg);
+  if (workspace_bytes < L.total)
+    return fail(DD_ERR_INVALID_ARG, "workspace too small: %zu < %zu bytes", workspace_bytes, L.total);
+  if (!encode_fn()) return fail(DD_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+  dd_ctx* c = new dd_ctx();
+  c->cfg = *cfg;
+  c->R = cfg->batch * cfg->block;
+  c->G = cfg->n_q_heads / cfg->n_kv_heads;
+  c->qkvw = (cfg->n_q_heads + 2 * cfg->n_kv_heads) * cfg->head_dim;
+  c->HqD = cfg->n_q_heads * cfg->head_dim;
+  c->L = L;
+  c->ws = static_cast<uint8_t*>(workspace);
+  c->timeout_ns = dd::kDefaultTimeoutNs;
+  cudaError_t e = cudaGetDevice(&c->device);
+  if (e == cudaSuccess) e = dd::prepare_kernels();
+  if (e == cudaSuccess) e = cudaMemset(workspace, 0, L.total);
+  if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking);
+  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&c->hpin), 16, cudaHostAllocDefault);
+  if (e == cudaSuccess) e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) {
+    dd_destroy(c);
+    return fail(DD_ERR_CUDA, "dd_create: %s", cudaGetErrorString(e));
+  }
+  const dd_config& cf = *cfg;
+  const uint64_t planes = (uint64_t)cf.n_layers * cf.batch * cf.n_kv_heads;
+  bool ok = dd::make_map_3d(&c->m_kc, c->ws + L.kc, planes, L.alloc_ctx, cf.head_dim, 64) &&
+            dd::make_map_3d(&c->m_vc, c->ws + L.vc, planes, L.alloc_ctx, cf.head_dim, 64) &&
+            dd::make_map_2d(&c->m_y_b, c->ws + L.y, c->R, cf.hidden, L.p_qkv.BN) &&
+            dd::make_map_2d(&c->m_attn_b, c->ws + L.attn, c->R, c->HqD, L.p_o.BN) &&
+            dd::make_map_2d(&c->m_h_b, c->ws + L.hmid, c->R, cf.mlp, L.p_d.BN) &&
+            dd::make_map_2d(&c->m_y_a, c->ws + L.y, c->R, cf.hidden, 128);
+  if (!ok) {
+    dd_destroy(c);
+    return fail(DD_ERR_CUDA, "tensor map encoding failed for the workspace buffers");
+  }
+  *out = c;
+  return DD_OK;
+}
+
+void dd_destroy(dd_ctx* c) {
+  if (!c) return;
+  if (c->exec) cudaGraphExecDestroy(c->exec);
+  if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
+  if (c->hpin) cudaFreeHost(c->hpin);
+  delete c;
+}
+
+dd_status dd_init_weights(dd_ctx* c, const dd_weights* w) {
+  if (!c) return fail(DD_ERR_INVALID_ARG, "ctx is NULL");
+  if (!w) return fail(DD_ERR_INVALID_ARG, "weights is NULL");
+  const void* ptrs[] = {w->embed, w->pos, w->wqkv, w->wo, w->wgu, w->wd, w->g_attn, w->g_mlp, w->g_final, w->lm_head};
+  const char* names[] = {"embed", "pos", "wqkv", "wo", "wgu", "wd", "g_attn", "g_mlp", "g_final", "lm_head"};
+  for (int i = 0; i < 10; ++i) {
+    if (!ptrs[i]) return fail(DD_ERR_INVALID_ARG, "weight '%s' is NULL", names[i]);
+    if (reinterpret_cast<uintptr_t>(ptrs[i]) % 16) return fail(DD_ERR_INVALID_ARG, "weight '%s' is not 16-byte aligned", names[i]);
+  }
+  const dd_config& cf = c->cfg;
+  const int H = cf.hidden, F = cf.mlp;
+  c->m_wqkv.assign(cf.n_layers, CUtensorMap{});
+  c->m_wo.assign(cf.n_layers, CUtensorMap{});
+  c->m_wgu.assign(cf.n_layers, CUtensorMap{});
+  c->m_wd.assign(cf.n_layers, CUtensorMap{});
+  bool ok = true;
+  for (int l = 0; l < cf.n_layers && ok; ++l) {
+    ok = dd::make_map_2d(&c->m_wqkv[l], (const uint8_t*)w->wqkv + (size_t)l * c->qkvw * H * 2, c->qkvw, H, 128) &&
+         dd::make_map_2d(&c->m_wo[l], (const uint8_t*)w->wo + (size_t)l * H * c->HqD * 2, H, c->HqD, 128) &&
+         dd::make_map_2d(&c->m_wgu[l], (const uint8_t*)w->wgu + (size_t)l * 2 * F * H * 2, 2 * F, H, 128) &&
+         dd::make_map_2d(&c->m_wd[l], (const uint8_t*)w->wd + (size_t)l * H * F * 2, H, F, 128);
+  }
+  ok = ok && dd::make_map_2d(&c->m_lm, w->lm_head, cf.vocab, H, c->L.p_lm.BN);
+  if (!ok) return fail(DD_ERR_CUDA, "tensor map encoding failed for the weights");
+  c->w = *w;
+  c->have_weights = true;
+  if (c->exec) {
+    cudaGraphExecDestroy(c->exec);
+    c->exec = nullptr;
+  }
+  return DD_OK;
+}
+
+dd_status dd_set_context_kv(dd_ctx* c, const void* k, const void* v, int32_t t0, int32_t n, void* stream) {
+  if (!c) return fail(DD_ERR_INVALID_ARG, "ctx is NULL");
+  const dd_config& cf = c->cfg;
+  if (t0 < 0 || n < 0 || (long long)t0 + n > cf.max_ctx)
+    return fail(DD_ERR_INVALID_ARG, "need 0 <= t0, 0 <= n, t0+n <= max_ctx (t0=%d n=%d max_ctx=%d)", t0, n, cf.max_ctx);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (n > 0) {
+    if (!k || !v) return fail(DD_ERR_INVALID_ARG, "k/v is NULL");
+    const size_t row = (size_t)cf.head_dim * 2;
+    const size_t planes = (size_t)cf.n_layers * cf.batch * cf.n_kv_heads;
+    DD_CUDA(cudaMemcpy2DAsync(c->ws + c->L.kc + (size_t)t0 * row, (size_t)c->L.alloc_ctx * row, k, (size_t)n * row,
+                              (size_t)n * row, planes, cudaMemcpyDefault, st));
+    DD_CUDA(cudaMemcpy2DAsync(c->ws + c->L.vc + (size_t)t0 * row, (size_t)c->L.alloc_ctx * row, v, (size_t)n * row,
+                              (size_t)n * row, planes, cudaMemcpyDefault, st));
+  }
+  DD_CUDA(dd::launch_set_int(small_ptr(c) + 2, t0 + n, st));
+  c->ctx_len = t0 + n;
+  return DD_OK;
+}
+
+dd_status dd_denoise_step(dd_ctx* c, int32_t* tokens, uint32_t* mask, float gamma, int32_t mode,
+                          int32_t* n_committed, void* stream) {
+  dd_status s = check_ctx(c);
+  if (s != DD_OK) return s;
+  if (!tokens || !mask) return fail(DD_ERR_INVALID_ARG, "tokens/mask is NULL");
+  if (mode != DD_MODE_THRESHOLD && mode != DD_MODE_MOCK_AR) return fail(DD_ERR_INVALID_ARG, "bad mode %d", mode);
+  if (!(gamma == gamma)) return fail(DD_ERR_INVALID_ARG, "gamma is NaN");
+  s = ensure_graph(c);
+  if (s != DD_OK) return s;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const dd_config& cf = c->cfg;
+  uint8_t* ws = c->ws;
+  DD_CUDA(cudaMemcpyAsync(ws + c->L.tok, tokens, (size_t)c->R * 4, cudaMemcpyDefault, st));
+  DD_CUDA(cudaMemcpyAsync(ws + c->L.mask, mask, (size_t)cf.batch * 4, cudaMemcpyDefault, st));
+  DD_CUDA(dd::launch_set_params(at<float>(ws, c->L.params), gamma, mode, st));
+  DD_CUDA(cudaGraphLaunch(c->exec, st));
+  DD_CUDA(cudaMemcpyAsync(tokens, ws + c->L.tok, (size_t)c->R * 4, cudaMemcpyDefault, st));
+  DD_CUDA(cudaMemcpyAsync(mask, ws + c->L.mask, (size_t)cf.batch * 4, cudaMemcpyDefault, st));
+  if (n_committed)
+    DD_CUDA(cudaMemcpyAsync(n_committed, ws + c->L.ncommit, (size_t)cf.batch * 4, cudaMemcpyDefault, st));
+  return DD_OK;
+}
+
+dd_status dd_denoise_step_probe(dd_ctx* c, int32_t* tokens, uint32_t* mask, float gamma, int32_t mode,
+                                int32_t* n_committed, const dd_probe* probe, void* stream) {
+  dd_status s = check_ctx(c);
+  if (s != DD_OK) return s;
+  if (!tokens || !mask) return fail(DD_ERR_INVALID_ARG, "tokens/mask is NULL");
+  if (mode != DD_MODE_THRESHOLD && mode != DD_MODE_MOCK_AR) return fail(DD_ERR_INVALID_ARG, "bad mode %d", mode);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const dd_config& cf = c->cfg;
+  uint8_t* ws = c->ws;
+  DD_CUDA(cudaMemcpyAsync(ws + c->L.tok, tokens, (size_t)c->R * 4, cudaMemcpyDeviceToDevice, st));
+  DD_CUDA(cudaMemcpyAsync(ws + c->L.mask, mask, (size_t)cf.batch * 4, cudaMemcpyDeviceToDevice, st));
+  DD_CUDA(dd::launch_set_params(at<float>(ws, c->L.params), gamma, mode, st));
+  s = enqueue_step(c, st, probe);
+  if (s != DD_OK) return s;
+  DD_CUDA(cudaMemcpyAsync(tokens, ws + c->L.tok, (size_t)c->R * 4, cudaMemcpyDeviceToDevice, st));
+  DD_CUDA(cudaMemcpyAsync(mask, ws + c->L.mask, (size_t)cf.batch * 4, cudaMemcpyDeviceToDevice, st));
+  if (n_committed)
+    DD_CUDA(cudaMemcpyAsync(n_committed, ws + c->L.ncommit, (size_t)cf.batch * 4, cudaMemcpyDeviceToDevice, st));
+  return DD_OK;
+}
+
+dd_status dd_decode_block(dd_ctx* c, int32_t* tokens, float gamma, int32_t mode, int32_t max_steps,
+                          int32_t* steps_out, void* stream) {
+  dd_status s = check_ctx(c);
+  if (s != DD_OK) return s;
+  if (!tokens) return fail(DD_ERR_INVALID_ARG, "tokens is NULL");
+  if (mode != DD_MODE_THRESHOLD && mode != DD_MODE_MOCK_AR) return fail(DD_ERR_INVALID_ARG, "bad mode %d", mode);
+  if (!(gamma == gamma)) return fail(DD_ERR_INVALID_ARG, "gamma is NaN");
+  s = ensure_graph(c);
+  if (s != DD_OK) return s;
+  const dd_config& cf = c->cfg;
+  if (max_steps <= 0) max_steps = 4 * cf.block;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = c->ws;
+  DD_CUDA(dd::launch_init_block(at<int32_t>(ws, c->L.tok), at<uint32_t>(ws, c->L.mask), cf.batch, cf.block, cf.vocab, st));
+  DD_CUDA(dd::launch_set_params(at<float>(ws, c->L.params), gamma, mode, st));
+  int steps = 0;
+  bool done = false;
+  while (steps < max_steps) {
+    DD_CUDA(cudaGraphLaunch(c->exec, st));
+    ++steps;
+    DD_CUDA(cudaMemcpyAsync(c->hpin, small_ptr(c), 8, cudaMemcpyDeviceToHost, st));
+    DD_CUDA(cudaStreamSynchronize(st));
+    if (c->hpin[1] != 0) {
+      if (steps_out) *steps_out = steps;
+      return fail(DD_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired during step %d", steps);
+    }
+    if (c->hpin[0] == 0) {
+      done = true;
+      break;
+    }
+  }
+  DD_CUDA(cudaMemcpyAsync(tokens, ws + c->L.tok, (size_t)c->R * 4, cudaMemcpyDefault, st));
+  if (steps_out) *steps_out = steps;
+  if (!done) return fail(DD_ERR_STEP_LIMIT, "%d steps without filling the block", max_steps);
+  return DD_OK;
+}
+
+dd_status dd_device_status(dd_ctx* c, void* stream) {
+  if (!c) return fail(DD_ERR_INVALID_ARG, "ctx is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DD_CUDA(cudaMemcpyAsync(c->hpin, small_ptr(c), 8, cudaMemcpyDeviceToHost, st));
+  DD_CUDA(cudaStreamSynchronize(st));
+  if (c->hpin[1] != 0) {
+    DD_CUDA(cudaMemsetAsync(small_ptr(c) + 1, 0, 4, st));
+    DD_CUDA(cudaStreamSynchronize(st));
+    return fail(DD_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired");
+  }
+  return DD_OK;
+}
+
+// ----------------------------------------------------------- single kernels
+
+static dd_status attn_check(const dd_attn_problem* p) {
+  if (!p) return fail(DD_ERR_INVALID_ARG, "problem is NULL");
+  if (p->batch < 1 || p->block < 1 || p->block > 32) return fail(DD_ERR_INVALID_ARG, "bad batch/block");
+  if (p->head_dim != 64 && p->head_dim != 128) return fail(DD_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
+  if (p->n_q_heads < 1 || p->n_kv_heads < 1 || p->n_q_heads % p->n_kv_heads)
+    return fail(DD_ERR_INVALID_ARG, "n_kv_heads must divide n_q_heads");
+  const int G = p->n_q_heads / p->n_kv_heads;
+  if ((G * p->block) % 16 || G * p->block > 128)
+    return fail(DD_ERR_UNSUPPORTED, "(n_q_heads/n_kv_heads)*block must be a multiple of 16 and <= 128");
+  if (p->ctx_len < 0 || p->ctx_stride < p->ctx_len || p->ctx_stride < 1)
+    return fail(DD_ERR_INVALID_ARG, "need 0 <= ctx_len <= ctx_stride, ctx_stride >= 1");
+  return DD_OK;
+}
+
+static size_t attn_ws_bytes(const dd_attn_problem* p, dd::AttnPlan* plan) {
+  *plan = dd::plan_attention(p->batch, p->block, p->n_q_heads, p->n_kv_heads, p->head_dim, p->ctx_len);
+  return 256 + dd::attention_partial_bytes(*plan, p->batch, p->n_kv_heads);
+}
+
+dd_status dd_block_attention_workspace_size(const dd_attn_problem* p, size_t* bytes) {
+  dd_status s = attn_check(p);
+  if (s != DD_OK) return s;
+  if (!bytes) return fail(DD_ERR_INVALID_ARG, "bytes is NULL");
+  dd::AttnPlan plan;
+  *bytes = attn_ws_bytes(p, &plan);
+  return DD_OK;
+}
+
+dd_status dd_block_attention(const dd_attn_problem* p, void* stream) {
+  dd_status s = attn_check(p);
+  if (s != DD_OK) return s;
+  if (!p->qkv || !p->k_ctx || !p->v_ctx || !p->out || !p->workspace)
+    return fail(DD_ERR_INVALID_ARG, "null pointer in attention problem");
+  dd::AttnPlan plan;
+  const size_t need = attn_ws_bytes(p, &plan);
+  if (p->workspace_bytes < need) return fail(DD_ERR_INVALID_ARG, "workspace too small: %zu < %zu", p->workspace_bytes, need);
+  if (!encode_fn()) return fail(DD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  DD_CUDA(dd::prepare_kernels());
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(p->workspace);
+  CUtensorMap mk, mv;
+  const uint64_t planes = (uint64_t)p->batch * p->n_kv_heads;
+  if (!dd::make_map_3d(&mk, p->k_ctx, planes, p->ctx_stride, p->head_dim, 64) ||
+      !dd::make_map_3d(&mv, p->v_ctx, planes, p->ctx_stride, p->head_dim, 64))
+    return fail(DD_ERR_CUDA, "tensor map encoding failed for k_ctx/v_ctx");
+  int* small = reinterpret_cast<int*>(ws);  // [0] ctx_len, [1] status
+  DD_CUDA(dd::launch_set_int(small, p->ctx_len, st));
+  dd::AttnArgs a{};
+  a.qkv = p->qkv;
+  a.ld_qkv = (p->n_q_heads + 2 * p->n_kv_heads) * p->head_dim;
+  a.B = p->batch;
+  a.S = p->block;
+  a.Hq = p->n_q_heads;
+  a.Hkv = p->n_kv_heads;
+  a.G = p->n_q_heads / p->n_kv_heads;
+  a.ctx_len = small;
+  a.z0 = 0;
+  a.out = p->out;
+  a.ld_out = p->n_q_heads * p->head_dim;
+  a.part_o = reinterpret_cast<float*>(ws + 256);
+  a.part_ml = reinterpret_cast<float2*>(
+      ws + 256 + align_up((size_t)p->batch * p->n_kv_heads * plan.n_splits * plan.rows * p->head_dim * 4, 16));
+  a.scale_log2 = 1.4426950408889634f / sqrtf((float)p->head_dim);
+  a.status = small + 1;
+  a.timeout_ns = dd::kDefaultTimeoutNs;
+  DD_CUDA(dd::launch_attention(plan, a, mk, mv, st));
+  return DD_OK;
+}
+
+dd_status dd_lmhead_select_workspace_size(int32_t rows, int32_t hidden, int32_t vocab, size_t* bytes) {
+  if (rows < 1 || hidden < 64 || hidden % 64 || vocab < 256 || vocab % 256)
+    return fail(DD_ERR_UNSUPPORTED, "need rows >= 1, hidden %% 64 == 0, vocab %% 256 == 0");
+  if (!bytes) return fail(DD_ERR_INVALID_ARG, "bytes is NULL");
+  const size_t n = (size_t)(vocab / 256) * rows * 4;
+  *bytes = 256 + 3 * align_up(n, 256);
+  return DD_OK;
+}
+
+dd_status dd_lmhead_select(int32_t rows, int32_t hidden, int32_t vocab, const void* x, const void* w, float* conf,
+                           int32_t* arg, void* workspace, size_t workspace_bytes, void* stream) {
+  size_t need = 0;
+  dd_status s = dd_lmhead_select_workspace_size(rows, hidden, vocab, &need);
+  if (s != DD_OK) return s;
+  if (!x || !w || !conf || !arg || !workspace) return fail(DD_ERR_INVALID_ARG, "null pointer");
+  if (workspace_bytes < need) return fail(DD_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes, need);
+  if (!encode_fn()) return fail(DD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  DD_CUDA(dd::prepare_kernels());
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  dd::GemmPlan p = dd::plan_gemm(dd::kEpiSelect, rows, vocab, hidden);
+  CUtensorMap mx, mw;
+  if (!dd::make_map_2d(&mx, x, rows, hidden, 128) || !dd::make_map_2d(&mw, w, vocab, hidden, p.BN))
+    return fail(DD_ERR_CUDA, "tensor map encoding failed");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  const size_t n = align_up((size_t)p.n_tiles * rows * 4, 256);
+  dd::GemmOut o{};
+  o.rows_valid = rows;
+  o.sel_m = reinterpret_cast<float*>(ws + 256);
+  o.sel_s = reinterpret_cast<float*>(ws + 256 + n);
+  o.sel_a = reinterpret_cast<int*>(ws + 256 + 2 * n);
+  DD_CUDA(dd::launch_gemm(p, mx, mw, o, reinterpret_cast<int*>(ws), dd::kDefaultTimeoutNs, st));
+  DD_CUDA(dd::launch_select_combine(o.sel_m, o.sel_s, o.sel_a, p.n_tiles, rows, conf, arg, st));
+  return DD_OK;
+}
+
+dd_status dd_gemm_workspace_size(int32_t rows, int32_t n, int32_t k, size_t* bytes) {
+  if (rows < 16 || rows % 16 || n < 128 || n % 128 || k < 64 || k % 64)
+    return fail(DD_ERR_UNSUPPORTED, "need rows %% 16 == 0, n %% 128 == 0, k %% 64 == 0");
+  if (!bytes) return fail(DD_ERR_INVALID_ARG, "bytes is NULL");
+  dd::GemmPlan p = dd::plan_gemm(dd::kEpiPartial, rows, n, k);
+  *bytes = 256 + (size_t)p.splits * rows * n * 4;
+  return DD_OK;
+}
+
+dd_status dd_gemm(int32_t rows, int32_t n, int32_t k, const void* x, const void* w, float* y, void* workspace,
+                  size_t workspace_bytes, void* stream) {
+  size_t need = 0;
+  dd_status s = dd_gemm_workspace_size(rows, n, k, &need);
+  if (s != DD_OK) return s;
+  if (!x || !w || !y || !workspace) return fail(DD_ERR_INVALID_ARG, "null pointer");
+  if (workspace_bytes < need) return fail(DD_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes, need);
+  if (!encode_fn()) return fail(DD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  DD_CUDA(dd::prepare_kernels());
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  dd::GemmPlan p = dd::plan_gemm(dd::kEpiPartial, rows, n, k);
+  CUtensorMap mw, mx;
+  if (!dd::make_map_2d(&mw, w, n, k, 128) || !dd::make_map_2d(&mx, x, rows, k, p.BN))
+    return fail(DD_ERR_CUDA, "tensor map encoding failed");
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  dd::GemmOut o{};
+  o.partial = reinterpret_cast<float*>(ws + 256);
+  o.split_stride = (long long)rows * n;
+  o.ld = n;
+  o.rows_valid = rows;
+  DD_CUDA(dd::launch_gemm(p, mw, mx, o, reinterpret_cast<int*>(ws), dd::kDefaultTimeoutNs, st));
+  DD_CUDA(dd::launch_reduce_f32(o.partial, p.splits, o.split_stride, rows, n, y, st));
+  return DD_OK;
+}
+
+dd_status dd_commit(int32_t batch, int32_t block, const float* conf, const int32_t* arg, int32_t* tokens,
+                    uint32_t* mask, float gamma, int32_t mode, int32_t* n_committed, int32_t* remaining,
+                    void* stream) {
+  if (batch < 1 || block < 1 || block > 32) return fail(DD_ERR_INVALID_ARG, "bad batch/block");
+  if (!conf || !arg || !tokens || !mask || !remaining) return fail(DD_ERR_INVALID_ARG, "null pointer");
+  if (mode != DD_MODE_THRESHOLD && mode != DD_MODE_MOCK_AR) return fail(DD_ERR_INVALID_ARG, "bad mode %d", mode);
+  DD_CUDA(dd::launch_commit(conf, arg, tokens, mask, nullptr, gamma, mode, n_committed, remaining, batch, block,
+                            static_cast<cudaStream_t>(stream)));
+  return DD_OK;
+}
+
+dd_status dd_test_wait_timeout(int32_t timeout_us, int32_t* status, void* stream) {
+  if (timeout_us < 1 || timeout_us > 10000000) return fail(DD_ERR_INVALID_ARG, "timeout_us must be in [1, 1e7]");
+  if (!status) return fail(DD_ERR_INVALID_ARG, "status is NULL");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  DD_CUDA(cudaMemsetAsync(status, 0, 4, st));
+  DD_CUDA(dd::launch_wait_forever_bounded(status, (uint64_t)timeout_us * 1000ull, st));
+  int h = 0;
+  DD_CUDA(cudaMemcpyAsync(&h, status, 4, cudaMemcpyDeviceToHost, st));
+  DD_CUDA(cudaStreamSynchronize(st));
+  if (h != 0) return fail(DD_ERR_DEVICE_TIMEOUT, "bounded wait expired after %d us", timeout_us);
+  return DD_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,371 @@
+// Block attention of the denoising tower (TwoTower article, "技術/ビジネス面":
+// bidirectional attention inside the block plus cross-attention to the frozen
+// context tower's state), as one softmax per query over
+// [ctx_len context keys | S block keys], scale 1/sqrt(D), no mask.
+//
+// One CTA serves one (sequence, kv head, context split): all G query heads
+// that share the kv head (G*S query rows, 16 per compute warp) read each
+// context K/V tile once.  A producer warp streams the tiles from HBM with
+// TMA (3D tensor map over the [planes][positions][D] cache, 128-byte
+// swizzle) into a ring of shared-memory stages; the compute warps run
+// QK^T and PV on the tensor cores (mma.sync m16n8k16, bf16 in, fp32 out)
+// with an online softmax in base 2 (quad shuffles for the row max/sum).
+// The S block keys/values come from the packed q|k|v activation rows and
+// are staged once, by split 0.  With several splits per (sequence, kv head)
+// each CTA writes an unnormalised partial (o, m, l) and a combine kernel
+// merges them.
+#include <math.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dd {
+
+namespace {
+
+constexpr int kKT = 64;      // context keys per tile
+constexpr int kKTB = 32;     // block-key tile (S <= 32)
+
+// Byte offset of element (row, col) in a tile of `rows` rows x D columns
+// stored as D/64 boxes of [rows][128 B] with the TMA 128-byte swizzle
+// (16-byte chunk c of row r lives at chunk c ^ (r & 7)).
+template <int D>
+__device__ __forceinline__ uint32_t swz_off(int rows, int r, int col) {
+  const int box = col >> 6;
+  const int chunk = (col & 63) >> 3;
+  return box * rows * 128 + r * 128 + ((chunk ^ (r & 7)) << 4) + (col & 7) * 2;
+}
+
+template <int D>
+struct Tile {
+  static constexpr int kBytes = kKT * D * 2;
+  static constexpr int kBlkBytes = kKTB * D * 2;
+};
+
+// Process one tile of NK keys (NK = 64 context keys, or 32 block keys).
+template <int D, int NK>
+__device__ __forceinline__ void attend_tile(uint32_t k_base, uint32_t v_base, int n_valid, const uint32_t (&qf)[D / 16][4],
+                                            float (&o)[D / 8][4], float& m0, float& m1, float& l0, float& l1,
+                                            float scale_log2, int lane) {
+  // S = Q K^T : 16 rows x NK keys
+  float s[NK / 8][4];
+#pragma unroll
+  for (int j = 0; j < NK / 8; ++j) {
+    s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
+  }
+#pragma unroll
+  for (int j = 0; j < NK / 8; ++j) {
+    const int key = j * 8 + (lane & 7);
+#pragma unroll
+    for (int kk = 0; kk < D / 16; kk += 2) {
+      const int col = kk * 16 + (lane >> 3) * 8;
+      uint32_t b0, b1, b2, b3;
+      ldmatrix_x4(k_base + swz_off<D>(NK, key, col), b0, b1, b2, b3);
+      mma_bf16_16816(s[j], qf[kk], b0, b1);
+      mma_bf16_16816(s[j], qf[kk + 1], b2, b3);
+    }
+  }
+  // scale to base-2 units and mask keys beyond n_valid
+  float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < NK / 8; ++j) {
+    const int key = j * 8 + (lane & 3) * 2;
+#pragma unroll
+    for (int e = 0; e < 2; ++e) {
+      const bool valid = (key + e) < n_valid;
+      s[j][e] = valid ? s[j][e] * scale_log2 : -INFINITY;
+      s[j][2 + e] = valid ? s[j][2 + e] * scale_log2 : -INFINITY;
+      mx0 = fmaxf(mx0, s[j][e]);
+      mx1 = fmaxf(mx1, s[j][2 + e]);
+    }
+  }
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+  mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+  mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+  const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+  const float base0 = mn0 == -INFINITY ? 0.f : mn0;
+  const float base1 = mn1 == -INFINITY ? 0.f : mn1;
+  const float alpha0 = exp2f(m0 - base0), alpha1 = exp2f(m1 - base1);
+  m0 = mn0;
+  m1 = mn1;
+  float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+  for (int j = 0; j < NK / 8; ++j) {
+    s[j][0] = exp2f(s[j][0] - base0);
+    s[j][1] = exp2f(s[j][1] - base0);
+    s[j][2] = exp2f(s[j][2] - base1);
+    s[j][3] = exp2f(s[j][3] - base1);
+    ps0 += s[j][0] + s[j][1];
+    ps1 += s[j][2] + s[j][3];
+  }
+  l0 = l0 * alpha0 + ps0;
+  l1 = l1 * alpha1 + ps1;
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) {
+    o[n][0] *= alpha0;
+    o[n][1] *= alpha0;
+    o[n][2] *= alpha1;
+    o[n][3] *= alpha1;
+  }
+  // O += P V
+#pragma unroll
+  for (int kk = 0; kk < NK / 16; ++kk) {
+    uint32_t pa[4];
+    pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
+    pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
+    pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
+    pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+    const int mi = lane >> 3;
+    const int key = kk * 16 + (lane & 7) + (mi & 1) * 8;
+#pragma unroll
+    for (int jj = 0; jj < D / 16; ++jj) {
+      const int col = jj * 16 + (mi >> 1) * 8;
+      uint32_t b0, b1, b2, b3;
+      ldmatrix_x4_trans(v_base + swz_off<D>(NK, key, col), b0, b1, b2, b3);
+      mma_bf16_16816(o[2 * jj], pa, b0, b1);
+      mma_bf16_16816(o[2 * jj + 1], pa, b2, b3);
+    }
+  }
+}
+
+template <int D, int STAGES>
+__global__ void __launch_bounds__(288) k_block_attn(const __grid_constant__ CUtensorMap map_k,
+                                                    const __grid_constant__ CUtensorMap map_v, const AttnArgs a,
+                                                    int n_splits, int warps_c) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  constexpr int kTileB = Tile<D>::kBytes;
+  constexpr int kBlkB = Tile<D>::kBlkBytes;
+  uint8_t* kv_stages = smem;                                  // STAGES x (K tile, V tile)
+  uint8_t* blk_k = smem + STAGES * 2 * kTileB;                // block keys
+  uint8_t* blk_v = blk_k + kBlkB;
+  uint64_t* full = reinterpret_cast<uint64_t*>(blk_v + kBlkB);
+  uint64_t* empty = full + STAGES;
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = warp_id(), lane = lane_id();
+  const int T = *a.ctx_len;
+  const int ntiles = (T + kKT - 1) / kKT;
+  const int per = (ntiles + n_splits - 1) / n_splits;
+  const int tile0 = split * per;
+  const int tile1 = min(ntiles, tile0 + per);
+  const int z = a.z0 + b * a.Hkv + kvh;
+  const __nv_bfloat16* qkv = reinterpret_cast<const __nv_bfloat16*>(a.qkv);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], warps_c);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (split == 0) {
+    // Stage the block keys/values of this kv head (rows >= S zero-filled).
+    const int chunks = kKTB * (D / 8);
+    for (int c = threadIdx.x; c < 2 * chunks; c += blockDim.x) {
+      const int which = c / chunks;  // 0 = k, 1 = v
+      const int cc = c % chunks;
+      const int r = cc / (D / 8), col = (cc % (D / 8)) * 8;
+      uint4 val = make_uint4(0, 0, 0, 0);
+      if (r < a.S) {
+        const long long off = (long long)(b * a.S + r) * a.ld_qkv + (a.Hq + which * a.Hkv + kvh) * D + col;
+        val = *reinterpret_cast<const uint4*>(qkv + off);
+      }
+      uint8_t* dst = (which == 0 ? blk_k : blk_v) + swz_off<D>(kKTB, r, col);
+      *reinterpret_cast<uint4*>(dst) = val;
+    }
+  }
+  __syncthreads();
+
+  if (warp == warps_c) {
+    // ---------------------------------------------------------- producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t phase = 0;
+      for (int t = tile0; t < tile1; ++t) {
+        if (!mbar_wait_bounded(&empty[s], phase ^ 1, a.timeout_ns, abort_flag, a.status)) break;
+        uint8_t* kd = kv_stages + s * 2 * kTileB;
+        uint8_t* vd = kd + kTileB;
+        mbar_arrive_expect_tx(&full[s], 2 * kTileB);
+#pragma unroll
+        for (int box = 0; box < D / 64; ++box) {
+          tma_load_3d(kd + box * kKT * 128, &map_k, &full[s], box * 64, t * kKT, z);
+          tma_load_3d(vd + box * kKT * 128, &map_v, &full[s], box * 64, t * kKT, z);
+        }
+        if (++s == STAGES) { s = 0; phase ^= 1; }
+      }
+    }
+    __syncwarp();
+    return;
+  }
+
+  // ------------------------------------------------------------ compute
+  // Rows of this warp: r = warp*16 + lane/4 (+8); row r = (g, i) with
+  // g = r / S (query head within the group) and i = r % S (block position).
+  const int r0 = warp * 16 + (lane >> 2);
+  const int r1 = r0 + 8;
+  const int g0 = r0 / a.S, i0 = r0 % a.S;
+  const int g1 = r1 / a.S, i1 = r1 % a.S;
+  const int h0 = kvh * a.G + g0, h1 = kvh * a.G + g1;
+  uint32_t qf[D / 16][4];
+  {
+    const __nv_bfloat16* q0 = qkv + (long long)(b * a.S + i0) * a.ld_qkv + h0 * D + (lane & 3) * 2;
+    const __nv_bfloat16* q1 = qkv + (long long)(b * a.S + i1) * a.ld_qkv + h1 * D + (lane & 3) * 2;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qf[kk][0] = *reinterpret_cast<const uint32_t*>(q0 + kk * 16);
+      qf[kk][1] = *reinterpret_cast<const uint32_t*>(q1 + kk * 16);
+      qf[kk][2] = *reinterpret_cast<const uint32_t*>(q0 + kk * 16 + 8);
+      qf[kk][3] = *reinterpret_cast<const uint32_t*>(q1 + kk * 16 + 8);
+    }
+  }
+  float o[D / 8][4];
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+
+  if (split == 0) {
+    attend_tile<D, kKTB>(smem_u32(blk_k), smem_u32(blk_v), a.S, qf, o, m0, m1, l0, l1, a.scale_log2, lane);
+  }
+  {
+    int s = 0;
+    uint32_t phase = 0;
+    for (int t = tile0; t < tile1; ++t) {
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait_bounded(&full[s], phase, a.timeout_ns, abort_flag, a.status);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      const uint32_t kb = smem_u32(kv_stages + s * 2 * kTileB);
+      attend_tile<D, kKT>(kb, kb + kTileB, min(kKT, T - t * kKT), qf, o, m0, m1, l0, l1, a.scale_log2, lane);
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[s]);
+      if (++s == STAGES) { s = 0; phase ^= 1; }
+    }
+  }
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+  if (n_splits == 1) {
+    __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+    const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+    __nv_bfloat16* d0 = out + (long long)(b * a.S + i0) * a.ld_out + h0 * D + (lane & 3) * 2;
+    __nv_bfloat16* d1 = out + (long long)(b * a.S + i1) * a.ld_out + h1 * D + (lane & 3) * 2;
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      *reinterpret_cast<uint32_t*>(d0 + n * 8) = pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
+      *reinterpret_cast<uint32_t*>(d1 + n * 8) = pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
+    }
+  } else {
+    const long long prow = ((long long)(b * a.Hkv + kvh) * n_splits + split) * (a.G * a.S);
+    float* p0 = a.part_o + (prow + r0) * D + (lane & 3) * 2;
+    float* p1 = a.part_o + (prow + r1) * D + (lane & 3) * 2;
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      *reinterpret_cast<float2*>(p0 + n * 8) = make_float2(o[n][0], o[n][1]);
+      *reinterpret_cast<float2*>(p1 + n * 8) = make_float2(o[n][2], o[n][3]);
+    }
+    if ((lane & 3) == 0) {
+      a.part_ml[prow + r0] = make_float2(m0, l0);
+      a.part_ml[prow + r1] = make_float2(m1, l1);
+    }
+  }
+}
+
+// Merge split partials: o = sum_s 2^(m_s - M) o_s / sum_s 2^(m_s - M) l_s.
+// One warp per (sequence, kv head, row).
+template <int D>
+__global__ void k_attn_combine(const AttnArgs a, int n_splits) {
+  const int rows = a.G * a.S;
+  const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  const long long total = (long long)a.B * a.Hkv * rows;
+  if (gw >= total) return;
+  const int lane = threadIdx.x & 31;
+  const int r = (int)(gw % rows);
+  const long long bk = gw / rows;  // b * Hkv + kvh
+  const int kvh = (int)(bk % a.Hkv), b = (int)(bk / a.Hkv);
+  float M = -INFINITY;
+  for (int s = 0; s < n_splits; ++s) M = fmaxf(M, a.part_ml[(bk * n_splits + s) * rows + r].x);
+  float L = 0.f;
+  float acc[D / 32];
+#pragma unroll
+  for (int k = 0; k < D / 32; ++k) acc[k] = 0.f;
+  for (int s = 0; s < n_splits; ++s) {
+    const float2 ml = a.part_ml[(bk * n_splits + s) * rows + r];
+    const float w = ml.x == -INFINITY ? 0.f : exp2f(ml.x - M);
+    L += w * ml.y;
+    const float* po = a.part_o + ((bk * n_splits + s) * rows + r) * D;
+#pragma unroll
+    for (int k = 0; k < D / 32; ++k) acc[k] += w * po[lane + 32 * k];
+  }
+  const int g = r / a.S, i = r % a.S;
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + (long long)(b * a.S + i) * a.ld_out +
+                       (kvh * a.G + g) * D;
+  const float inv = 1.f / L;
+#pragma unroll
+  for (int k = 0; k < D / 32; ++k) out[lane + 32 * k] = __float2bfloat16_rn(acc[k] * inv);
+}
+
+template <int D>
+constexpr int attn_stages() {
+  return D == 128 ? 3 : 4;
+}
+
+}  // namespace
+
+AttnPlan plan_attention(int B, int S, int Hq, int Hkv, int D, int max_ctx) {
+  AttnPlan p{};
+  p.D = D;
+  p.rows = (Hq / Hkv) * S;
+  p.warps_c = p.rows / 16;
+  p.stages = D == 128 ? attn_stages<128>() : attn_stages<64>();
+  const int tile_b = kKT * D * 2, blk_b = kKTB * D * 2;
+  p.smem_bytes = 1024 + p.stages * 2 * tile_b + 2 * blk_b + 2 * p.stages * 8 + 16;
+  const int pairs = B * Hkv;
+  const int ntiles = (max_ctx + kKT - 1) / kKT;
+  // Enough CTAs for ~4 resident waves (2 CTAs per SM), at least 4 tiles per split.
+  const int want = (4 * 2 * kNumSMs + pairs - 1) / pairs;
+  int max_splits = (ntiles + 3) / 4;
+  if (max_splits < 1) max_splits = 1;
+  p.n_splits = want < max_splits ? want : max_splits;
+  if (p.n_splits < 1) p.n_splits = 1;
+  return p;
+}
+
+size_t attention_partial_bytes(const AttnPlan& p, int B, int Hkv) {
+  if (p.n_splits <= 1) return 0;
+  const size_t n = (size_t)B * Hkv * p.n_splits * p.rows;
+  return n * p.D * sizeof(float) + n * sizeof(float2) + 256;
+}
+
+cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a, const CUtensorMap& map_k, const CUtensorMap& map_v,
+                             cudaStream_t st) {
+  dim3 grid(p.n_splits, a.Hkv, a.B);
+  const int threads = (p.warps_c + 1) * 32;
+  if (p.D == 128)
+    k_block_attn<128, attn_stages<128>()><<<grid, threads, p.smem_bytes, st>>>(map_k, map_v, a, p.n_splits, p.warps_c);
+  else
+    k_block_attn<64, attn_stages<64>()><<<grid, threads, p.smem_bytes, st>>>(map_k, map_v, a, p.n_splits, p.warps_c);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || p.n_splits == 1) return e;
+  const long long warps = (long long)a.B * a.Hkv * p.rows;
+  const int blocks = (int)((warps + 7) / 8);
+  if (p.D == 128) k_attn_combine<128><<<blocks, 256, 0, st>>>(a, p.n_splits);
+  else k_attn_combine<64><<<blocks, 256, 0, st>>>(a, p.n_splits);
+  return cudaGetLastError();
+}
+
+cudaError_t prepare_attention_kernels() {
+  const int lim = 227 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(k_block_attn<128, attn_stages<128>()>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_block_attn<64, attn_stages<64>()>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  return e;
+}
+
+}  // namespace dd

@@ -1,0 +1,337 @@
+// Tensor-core GEMM for sm_103a: TMA -> shared memory (128-byte swizzle) ->
+// tcgen05.mma (bf16 in, fp32 accumulate in TMEM) -> epilogue warps reading
+// TMEM with tcgen05.ld.
+//
+// One warp-specialised kernel serves every dense contraction of the
+// denoising step:
+//   * linear layers (QKV, O, gate|up, down): the weight tile sits on the MMA
+//     M side (128 output features per tile) and the B*S activation rows on
+//     the N side, so a 128-row decode batch still fills the 128-lane
+//     accumulator; K may be split across CTAs, each writing an fp32 partial
+//     that a reduce kernel sums and post-processes (bias-free epilogues:
+//     bf16 store, residual + RMSNorm, SwiGLU);
+//   * the LM head: activation rows on the M side (one TMEM lane per row) and
+//     256 vocab entries per tile on the N side; the epilogue folds each
+//     row's 256 logits into a running (max, sum of exp, first argmax) so the
+//     logits never reach global memory.
+//
+// Roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues
+// MMAs, warps 2-5 run the epilogue (TMEM lane quarter = warp % 4).  Two
+// accumulator buffers let the epilogue of one tile overlap the MMAs of the
+// next.  Every mbarrier wait is bounded; on expiry the kernel records a
+// timeout in the status word and unwinds.
+#include <math.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dd {
+
+namespace {
+
+constexpr int kBM = 128;
+constexpr int kBK = 64;
+constexpr int kThreads = 192;
+constexpr int kStageA = kBM * kBK * 2;  // 16 KB
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct KArgs {
+  int m_tiles, n_tiles, splits, kb_total, kb_per_split, BN, stages, tiles_total;
+  uint32_t tmem_half;
+  GemmOut out;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+template <int EPI>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_gemm_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, const KArgs args) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const int stage_b = args.BN * kBK * 2;
+  const int stage_bytes = kStageA + stage_b;
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + args.stages * stage_bytes);
+  uint64_t* empty = full + args.stages;
+  uint64_t* acc_full = empty + args.stages;
+  uint64_t* acc_empty = acc_full + 2;
+  uint64_t* drain = acc_empty + 2;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id();
+  const int lane = lane_id();
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < args.stages; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&acc_full[a], 1);
+      mbar_init(&acc_empty[a], 4);
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, 2 * args.tmem_half);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int per_split = args.m_tiles * args.n_tiles;
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      int s = 0;
+      uint32_t phase = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < args.tiles_total && ok; t += gridDim.x) {
+        const int split = t / per_split, r = t % per_split;
+        int mt, nt;
+        if (EPI == kEpiPartial) { nt = r % args.n_tiles; mt = r / args.n_tiles; }
+        else { mt = r % args.m_tiles; nt = r / args.m_tiles; }
+        const int kb0 = split * args.kb_per_split;
+        const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait_bounded(&empty[s], phase ^ 1, args.timeout_ns, abort_flag, args.status)) { ok = false; break; }
+          uint8_t* sa = smem + s * stage_bytes;
+          mbar_arrive_expect_tx(&full[s], stage_bytes);
+          tma_load_2d(sa, &map_a, &full[s], kb * kBK, mt * kBM);
+          tma_load_2d(sa + kStageA, &map_b, &full[s], kb * kBK, nt * args.BN);
+          if (++s == args.stages) { s = 0; phase ^= 1; }
+        }
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16_f32(kBM, args.BN);
+      int s = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < args.tiles_total && ok; t += gridDim.x, ++it) {
+        const int split = t / per_split;
+        const int kb0 = split * args.kb_per_split;
+        const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
+        const int ab = it & 1;
+        const uint32_t aphase = (it >> 1) & 1;
+        if (!mbar_wait_bounded(&acc_empty[ab], aphase ^ 1, args.timeout_ns, abort_flag, args.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + ab * args.tmem_half;
+        for (int kb = kb0; kb < kb1; ++kb) {
+          if (!mbar_wait_bounded(&full[s], phase, args.timeout_ns, abort_flag, args.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(smem + s * stage_bytes);
+          const uint32_t b_addr = a_addr + kStageA;
+#pragma unroll
+          for (int k = 0; k < kBK / 16; ++k) {
+            tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
+                        (kb > kb0 || k > 0) ? 1u : 0u);
+          }
+          tc_commit(&empty[s]);
+          if (++s == args.stages) { s = 0; phase ^= 1; }
+        }
+        if (ok) tc_commit(&acc_full[ab]);
+      }
+      // Drain: wait until every MMA issued by this thread has completed, so
+      // TMEM can be released safely on every exit path.
+      tc_commit(drain);
+      mbar_wait_bounded(drain, 0, args.timeout_ns, abort_flag, args.status);
+    }
+    __syncwarp();
+  } else {
+    // ---------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    int it = 0;
+    for (int t = blockIdx.x; t < args.tiles_total; t += gridDim.x, ++it) {
+      const int split = t / per_split, r = t % per_split;
+      int mt, nt;
+      if (EPI == kEpiPartial) { nt = r % args.n_tiles; mt = r / args.n_tiles; }
+      else { mt = r % args.m_tiles; nt = r / args.m_tiles; }
+      const int ab = it & 1;
+      const uint32_t aphase = (it >> 1) & 1;
+      bool ok = true;
+      if (lane == 0) ok = mbar_wait_bounded(&acc_full[ab], aphase, args.timeout_ns, abort_flag, args.status);
+      ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+      if (!ok) break;
+      tc_fence_after();
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + ab * args.tmem_half;
+      const int lrow = mt * kBM + q * 32 + lane;  // accumulator row owned by this thread
+
+      if (EPI == kEpiPartial) {
+        // lrow = output feature, columns = activation rows.
+        float* dst = args.out.partial + (long long)split * args.out.split_stride + lrow;
+        for (int c = 0; c < args.BN; c += 16) {
+          float v[16];
+          tmem_ld16(tbase + c, v);
+          const int row0 = nt * args.BN + c;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            if (row0 + j < args.out.rows_valid) dst[(long long)(row0 + j) * args.out.ld] = v[j];
+          }
+        }
+      } else if (EPI == kEpiSelect) {
+        // lrow = activation row, columns = vocab ids nt*BN + c.
+        float m = -INFINITY, ssum = 0.f;
+        int arg = 0;
+        for (int c = 0; c < args.BN; c += 16) {
+          float v[16];
+          tmem_ld16(tbase + c, v);
+          float cm = v[0];
+          int ci = 0;
+#pragma unroll
+          for (int j = 1; j < 16; ++j) {
+            if (v[j] > cm) { cm = v[j]; ci = j; }
+          }
+          if (cm > m) {
+            ssum *= exp2f((m - cm) * kLog2e);
+            m = cm;
+            arg = nt * args.BN + c + ci;
+          }
+          const float mb = m * kLog2e;
+#pragma unroll
+          for (int j = 0; j < 16; ++j) ssum += exp2f(fmaf(v[j], kLog2e, -mb));
+        }
+        if (lrow < args.out.rows_valid) {
+          const long long o = (long long)nt * args.out.rows_valid + lrow;
+          args.out.sel_m[o] = m;
+          args.out.sel_s[o] = ssum;
+          args.out.sel_a[o] = arg;
+        }
+      } else {
+        // Plain fp32 store of the tile: row lrow, columns nt*BN + c.
+        float* dst = args.out.partial + (long long)lrow * args.out.ld + nt * args.BN;
+        for (int c = 0; c < args.BN; c += 16) {
+          float v[16];
+          tmem_ld16(tbase + c, v);
+          if (lrow < args.out.rows_valid) {
+#pragma unroll
+            for (int j = 0; j < 16; j += 4)
+              *reinterpret_cast<float4*>(dst + c + j) = make_float4(v[j], v[j + 1], v[j + 2], v[j + 3]);
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&acc_empty[ab]);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, 2 * args.tmem_half);
+  }
+}
+
+uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
+  uint32_t p = lo;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+}  // namespace
+
+GemmPlan plan_gemm(int epi, int rows, int N, int K) {
+  GemmPlan p{};
+  p.epi = epi;
+  p.kb_total = K / kBK;
+  if (epi == kEpiPartial) {
+    // features on M, activation rows on N
+    p.m_tiles = N / kBM;
+    p.BN = rows <= 256 ? ((rows + 15) / 16) * 16 : 256;
+    p.n_tiles = (rows + p.BN - 1) / p.BN;
+  } else {
+    // activation rows on M, vocab on N (256 per tile)
+    p.m_tiles = (rows + kBM - 1) / kBM;
+    p.BN = 256;
+    p.n_tiles = N / p.BN;
+  }
+  const int stage_bytes = kStageA + p.BN * kBK * 2;
+  p.stages = (200 * 1024) / stage_bytes;
+  if (p.stages > 8) p.stages = 8;
+  if (p.stages < 2) p.stages = 2;
+  p.smem_bytes = 1024 + p.stages * stage_bytes + 256;
+  p.tmem_half = pow2_at_least(p.BN, 32);
+
+  const int base = p.m_tiles * p.n_tiles;
+  if (epi == kEpiPartial) {
+    // Split K so that the tile count fills the SMs: pick the split count that
+    // minimises (waves x K-blocks per split), preferring fewer splits.
+    int best_s = 1;
+    long long best_cost = -1;
+    const int max_s = p.kb_total < 16 ? p.kb_total : 16;
+    for (int s = 1; s <= max_s; ++s) {
+      const int kbps = (p.kb_total + s - 1) / s;
+      const int real_s = (p.kb_total + kbps - 1) / kbps;
+      if (real_s != s) continue;
+      const long long ctas = (long long)base * s;
+      const long long waves = (ctas + kNumSMs - 1) / kNumSMs;
+      const long long cost = waves * kbps * 100 + s;  // tie-break: fewer splits
+      if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_s = s; }
+    }
+    p.kb_per_split = (p.kb_total + best_s - 1) / best_s;
+    p.splits = best_s;
+    p.tiles_total = base * p.splits;
+    p.grid = p.tiles_total;
+  } else {
+    p.splits = 1;
+    p.kb_per_split = p.kb_total;
+    p.tiles_total = base;
+    p.grid = p.tiles_total < kNumSMs ? p.tiles_total : kNumSMs;
+  }
+  return p;
+}
+
+cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmOut& out,
+                        int* status, uint64_t timeout_ns, cudaStream_t st) {
+  KArgs a;
+  a.m_tiles = p.m_tiles;
+  a.n_tiles = p.n_tiles;
+  a.splits = p.splits;
+  a.kb_total = p.kb_total;
+  a.kb_per_split = p.kb_per_split;
+  a.BN = p.BN;
+  a.stages = p.stages;
+  a.tiles_total = p.tiles_total;
+  a.tmem_half = p.tmem_half;
+  a.out = out;
+  a.status = status;
+  a.timeout_ns = timeout_ns;
+  switch (p.epi) {
+    case kEpiPartial: k_gemm_tc<kEpiPartial><<<p.grid, kThreads, p.smem_bytes, st>>>(map_a, map_b, a); break;
+    case kEpiSelect: k_gemm_tc<kEpiSelect><<<p.grid, kThreads, p.smem_bytes, st>>>(map_a, map_b, a); break;
+    default: k_gemm_tc<kEpiStore><<<p.grid, kThreads, p.smem_bytes, st>>>(map_a, map_b, a); break;
+  }
+  return cudaGetLastError();
+}
+
+cudaError_t prepare_gemm_kernels() {
+  const int lim = 227 * 1024;
+  cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<kEpiPartial>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_gemm_tc<kEpiSelect>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_gemm_tc<kEpiStore>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  return e;
+}
+
+cudaError_t prepare_kernels() {
+  static cudaError_t done = cudaErrorNotReady;
+  if (done == cudaSuccess) return done;
+  cudaError_t e = prepare_gemm_kernels();
+  if (e == cudaSuccess) e = prepare_attention_kernels();
+  done = e;
+  return e;
+}
+
+}  // namespace dd

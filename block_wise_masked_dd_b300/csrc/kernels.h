@@ -1,0 +1,113 @@
+// Host-side launch interfaces of the CUDA kernels (internal to libdd).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace dd {
+
+constexpr int kNumSMs = 148;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per bounded wait
+
+// ------------------------------------------------------------ tcgen05 GEMM
+
+enum GemmEpi : int {
+  kEpiPartial = 0,   // D = W_tile * X_tile^T (features on lanes), fp32 partial [split][row][feature]
+  kEpiSelect = 1,    // D = X_tile * W_tile^T (rows on lanes), per-row (max, sumexp, argmax) per vocab tile
+  kEpiStore = 2,     // D = X_tile * W_tile^T, fp32 store [row][col] (logit probe)
+};
+
+struct GemmPlan {
+  int epi;
+  int m_tiles, n_tiles, splits;   // tile grid (M = 128 per tile)
+  int kb_total, kb_per_split;     // K blocks of 64
+  int BN;                         // MMA N (multiple of 16, <= 256)
+  int stages;
+  int tiles_total;
+  int grid;
+  int smem_bytes;
+  uint32_t tmem_half;             // TMEM columns per accumulator buffer (power of two >= BN)
+};
+
+struct GemmOut {
+  float* partial;          // kEpiPartial: [splits][rows][ld]; kEpiStore: [rows][ld]
+  long long split_stride;  // elements between splits
+  int ld;
+  int rows_valid;          // rows of the activation operand
+  float* sel_m;            // kEpiSelect: [n_tiles][rows_valid]
+  float* sel_s;
+  int* sel_a;
+};
+
+// Plan a GEMM over activations [rows][K] and weights [N][K].
+GemmPlan plan_gemm(int epi, int rows, int N, int K);
+// Enqueue.  map_w / map_x: 2D bf16 tensor maps with 128-byte swizzle, box
+// {64, 128} for the operand on the MMA M side and {64, BN} for the other.
+cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmOut& out,
+                        int* status, uint64_t timeout_ns, cudaStream_t st);
+
+// ------------------------------------------------------------- attention
+
+struct AttnPlan {
+  int D, rows, warps_c, n_splits, stages, smem_bytes;
+};
+
+struct AttnArgs {
+  const void* qkv;     // bf16 [B*S][ld_qkv]
+  int ld_qkv;
+  int B, S, Hq, Hkv, G;
+  const int* ctx_len;  // device int (context length)
+  int z0;              // tensor-map z offset of (b=0, kvh=0) for this layer
+  void* out;           // bf16 [B*S][ld_out]
+  int ld_out;
+  float* part_o;       // [B][Hkv][n_splits][rows][D]
+  float2* part_ml;     // [B][Hkv][n_splits][rows]
+  float scale_log2;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+AttnPlan plan_attention(int B, int S, int Hq, int Hkv, int D, int max_ctx);
+size_t attention_partial_bytes(const AttnPlan& p, int B, int Hkv);
+cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a, const CUtensorMap& map_k, const CUtensorMap& map_v,
+                             cudaStream_t st);
+
+// --------------------------------------------------- elementwise / small
+
+cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const void* embed, const void* pos,
+                              const void* g, float* x, void* y, int B, int S, int H, int V, float eps,
+                              cudaStream_t st);
+cudaError_t launch_reduce_bf16(const float* part, int splits, long long split_stride, int rows, int N, void* out,
+                               cudaStream_t st);
+cudaError_t launch_reduce_f32(const float* part, int splits, long long split_stride, int rows, int N, float* out,
+                              cudaStream_t st);
+cudaError_t launch_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
+                                        const void* g, void* y, int rows, int H, float eps, cudaStream_t st);
+cudaError_t launch_reduce_swiglu(const float* part, int splits, long long split_stride, void* h, int rows, int F,
+                                 cudaStream_t st);
+cudaError_t launch_select_combine(const float* sel_m, const float* sel_s, const int* sel_a, int n_tiles, int rows,
+                                  float* conf, int* arg, cudaStream_t st);
+// params: device float[2] {gamma, mode-as-float}, read at run time so one
+// captured graph serves every gamma; when NULL, `gamma` and `mode` are used.
+cudaError_t launch_commit(const float* conf, const int* arg, int32_t* tokens, uint32_t* mask, const float* params,
+                          float gamma, int mode, int32_t* n_committed, int32_t* remaining, int B, int S,
+                          cudaStream_t st);
+// Set the dynamic shared-memory limits of every pipelined kernel (once per process).
+cudaError_t prepare_kernels();
+cudaError_t prepare_gemm_kernels();
+cudaError_t prepare_attention_kernels();
+cudaError_t launch_set_params(float* params, float gamma, int mode, cudaStream_t st);
+cudaError_t launch_set_int(int* dst, int value, cudaStream_t st);
+cudaError_t launch_init_block(int32_t* tokens, uint32_t* mask, int B, int S, int V, cudaStream_t st);
+cudaError_t launch_copy_i32(int32_t* dst, const int32_t* src, int n, cudaStream_t st);
+cudaError_t launch_wait_forever_bounded(int* status, uint64_t timeout_ns, cudaStream_t st);
+
+// ------------------------------------------------------------ tensor maps
+
+// 2D bf16 map over a row-major [rows][cols] matrix, box {64 cols, box_rows}.
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// 3D bf16 map over [planes][rows][cols] (cols = head dim), box {64, box_rows, 1}.
+bool make_map_3d(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t cols, uint32_t box_rows);
+
+}  // namespace dd

@@ -1,0 +1,247 @@
+/*
+ * dd.h -- block-wise masked-diffusion decoding on one B300 (sm_103a).
+ *
+ * The library runs the denoising step of a TwoTower-style block diffusion
+ * decoder: a block of S [MASK]-initialised positions per sequence attends
+ * bidirectionally within the block and, by cross-attention, to a fixed
+ * context KV cache (the frozen context tower's state); a dense SwiGLU MLP and
+ * an LM head follow; every masked position whose softmax confidence reaches
+ * gamma is committed (the single most confident one if none does), and the
+ * step repeats until the block is full.
+ *
+ * Sources (web pages on the method):
+ *  - poko-everyday.com, "Nemotron-TwoTower" article, section "技術/ビジネス面":
+ *    frozen causal context tower; denoising tower with bidirectional block
+ *    attention and cross-attention to the context.
+ *  - prednext.com, "拡散言語モデル" explainer, section "拡散言語モデルで推論するには":
+ *    steps 1-5 of decoding (feed [MASK]s, adopt positions whose output passes
+ *    a threshold, return the others to [MASK], repeat until none is left).
+ *  - dzen.guru, Nemotron TwoTower news, "Что нового" and "Как попробовать?":
+ *    block size 16, confidence threshold gamma = 0.8, the mock-AR mode.
+ *
+ * Conventions for every entry point:
+ *  - Device memory is owned by the caller.  The library allocates no device
+ *    memory: `dd_create` receives a caller-allocated workspace (size from
+ *    `dd_workspace_size`), and weights are borrowed device pointers that must
+ *    stay valid until `dd_destroy`.
+ *  - bf16 = IEEE bfloat16 stored as 2 bytes; all matrices are row-major and
+ *    linear weights are stored [out_features][in_features].
+ *  - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls are
+ *    asynchronous on `stream` unless stated otherwise.
+ *  - Return value: DD_OK, or an error code; `dd_last_error()` then gives a
+ *    one-line message (thread-local).  Argument errors are detected on the
+ *    host before anything is enqueued.
+ *  - A dd_ctx is not thread-safe; one context serves one host thread at a time.
+ *  - The [MASK] input id is V (vocab size).  The LM head has V outputs, so
+ *    [MASK] is never predicted.
+ */
+#ifndef DD_H
+#define DD_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct dd_ctx dd_ctx;
+
+typedef enum dd_status {
+  DD_OK = 0,
+  DD_ERR_INVALID_ARG = 1,    /* null pointer, bad size or unsupported shape */
+  DD_ERR_CUDA = 2,           /* a CUDA runtime/driver call failed */
+  DD_ERR_NOT_READY = 3,      /* weights not set */
+  DD_ERR_STEP_LIMIT = 4,     /* dd_decode_block hit max_steps with positions still masked */
+  DD_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait expired; results are invalid */
+  DD_ERR_UNSUPPORTED = 6     /* shape outside what the kernels implement */
+} dd_status;
+
+enum {
+  DD_MODE_THRESHOLD = 0, /* commit masked positions with confidence >= gamma (fallback: the most confident one) */
+  DD_MODE_MOCK_AR = 1    /* commit the leftmost masked position each step (one token per step) */
+};
+
+/* Model and batch shape.  Supported: 1 <= block <= 32 with batch*block a
+ * multiple of 16; head_dim 64 or 128; (n_q_heads/n_kv_heads)*block a multiple
+ * of 16 and at most 128; hidden, mlp and (n_q_heads+2*n_kv_heads)*head_dim
+ * multiples of 128; n_q_heads*head_dim a multiple of 64; vocab a multiple of
+ * 256; max_ctx >= 0. */
+typedef struct dd_config {
+  int32_t batch;      /* B: sequences decoded together */
+  int32_t block;      /* S: positions per block */
+  int32_t hidden;     /* H */
+  int32_t n_q_heads;  /* Hq */
+  int32_t n_kv_heads; /* Hkv, divides Hq; query head h reads kv head h / (Hq/Hkv) */
+  int32_t head_dim;   /* D */
+  int32_t n_layers;   /* L >= 1 */
+  int32_t mlp;        /* F: SwiGLU width */
+  int32_t vocab;      /* V */
+  int32_t max_ctx;    /* capacity of the context KV cache, in positions */
+  float rms_eps;      /* RMSNorm epsilon (1e-5 in the synthetic workloads) */
+} dd_config;
+
+/* Borrowed device pointers to bf16 weights (stacked over layers). */
+typedef struct dd_weights {
+  const void* embed;   /* [V+1][H]; row V is the [MASK] embedding */
+  const void* pos;     /* [S][H]; in-block position embedding added to every token */
+  const void* wqkv;    /* [L][(Hq+2*Hkv)*D][H]: q rows (head-major), then k rows, then v rows */
+  const void* wo;      /* [L][H][Hq*D] */
+  const void* wgu;     /* [L][2*F][H]: gate rows 0..F-1, then up rows */
+  const void* wd;      /* [L][H][F] */
+  const void* g_attn;  /* [L][H] RMSNorm gain before attention */
+  const void* g_mlp;   /* [L][H] RMSNorm gain before the MLP */
+  const void* g_final; /* [H] final RMSNorm gain */
+  const void* lm_head; /* [V][H] */
+} dd_weights;
+
+/* ---------------------------------------------------------------- context */
+
+/* Bytes of device workspace `dd_create` needs for `cfg` (KV cache included:
+ * 2 * L*B*Hkv*max_ctx*D bf16).  Fails with DD_ERR_INVALID_ARG/UNSUPPORTED on
+ * a shape the kernels do not implement. */
+dd_status dd_workspace_size(const dd_config* cfg, size_t* bytes);
+
+/* Create a context over a caller-allocated device workspace of at least
+ * dd_workspace_size() bytes, 256-byte aligned, on the current device.  The
+ * workspace must outlive the context.  The KV cache is zero-filled and the
+ * context length is 0.  Synchronous. */
+dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_bytes, dd_ctx** out);
+
+/* Destroy a context (host state only; the workspace stays the caller's). */
+void dd_destroy(dd_ctx* ctx);
+
+/* Set the weights (borrowed; see dd_weights).  Every pointer must be non-null
+ * and 16-byte aligned.  The decoder weights follow the pre-norm dense
+ * transformer reading of the TwoTower denoising tower (attention, then
+ * SwiGLU MLP, per layer; final RMSNorm; untied LM head).  Synchronous on the
+ * host; enqueues nothing. */
+dd_status dd_init_weights(dd_ctx* ctx, const dd_weights* w);
+
+/* Write context K/V for positions [t0, t0+n) of every layer and sequence and
+ * set the context length to t0+n (positions >= t0+n are no longer attended).
+ * k, v: bf16 [L][B][Hkv][n][D], device or host memory (copied on `stream`).
+ * n = 0 only sets the length.  Requires 0 <= t0, t0+n <= max_ctx.  This is the
+ * frozen context tower's output (TwoTower article, "技術/ビジネス面"); the
+ * library takes it as given. */
+dd_status dd_set_context_kv(dd_ctx* ctx, const void* k, const void* v, int32_t t0, int32_t n,
+                            void* stream);
+
+/* ------------------------------------------------------------------ decode */
+
+/* One denoising step (explainer steps 2-4).  tokens: int32 [B][S], mask:
+ * uint32 [B] (bit i set = position i is [MASK]); both device or host memory,
+ * read and updated in place.  Masked positions are fed as [MASK] whatever
+ * their id.  For each sequence it commits every masked position with softmax
+ * confidence >= gamma, or, if none qualifies, the single most confident one
+ * (lowest position on ties); DD_MODE_MOCK_AR commits the leftmost masked
+ * position.  A committed position gets the argmax id (lowest id on ties) and
+ * its mask bit cleared; committed positions never change.  n_committed:
+ * int32 [B] (device or host, may be NULL) receives the count per sequence.
+ * Asynchronous on `stream` (host pointers make the copies synchronous). */
+dd_status dd_denoise_step(dd_ctx* ctx, int32_t* tokens, uint32_t* mask, float gamma, int32_t mode,
+                          int32_t* n_committed, void* stream);
+
+/* Decode one block (explainer step 5): set every position to [MASK] and run
+ * denoising steps until no position is masked.  tokens: int32 [B][S], device
+ * or host memory, receives the committed ids.  max_steps <= 0 means 4*S.
+ * Synchronises `stream` once per step to read the number of masked positions
+ * left.  steps_out (host, may be NULL) receives the step count.  Returns
+ * DD_ERR_STEP_LIMIT if positions are still masked after max_steps and
+ * DD_ERR_DEVICE_TIMEOUT if a kernel's bounded wait expired. */
+dd_status dd_decode_block(dd_ctx* ctx, int32_t* tokens, float gamma, int32_t mode, int32_t max_steps,
+                          int32_t* steps_out, void* stream);
+
+/* Synchronise `stream` and return DD_ERR_DEVICE_TIMEOUT if any kernel of this
+ * context recorded an expired wait since the last call (the flag is then
+ * cleared), else DD_OK. */
+dd_status dd_device_status(dd_ctx* ctx, void* stream);
+
+const char* dd_status_string(dd_status s);
+const char* dd_last_error(void);
+
+/* ------------------------------------------------------ step probes (tests) */
+
+/* Optional device outputs of one step, for parity checks.  Any pointer may be
+ * NULL.  attn_out: bf16 [L][B*S][Hq*D], the attention output of every layer
+ * (before the O projection); hidden: bf16 [B*S][H], the final RMSNorm output;
+ * logits: fp32 [B*S][V], computed by the same tensor-core LM-head mainloop with
+ * a plain store instead of the fused select; conf: fp32 [B*S]; arg: int32 [B*S]. */
+typedef struct dd_probe {
+  void* attn_out;
+  void* hidden;
+  float* logits;
+  float* conf;
+  int32_t* arg;
+} dd_probe;
+
+/* dd_denoise_step, and also fill `probe`.  Runs eagerly (not from the cached
+ * CUDA graph).  tokens/mask/n_committed must be device memory here. */
+dd_status dd_denoise_step_probe(dd_ctx* ctx, int32_t* tokens, uint32_t* mask, float gamma, int32_t mode,
+                                int32_t* n_committed, const dd_probe* probe, void* stream);
+
+/* ------------------------------------------- single-kernel entry points */
+
+/* Block attention for one layer (TwoTower article, "技術/ビジネス面"): for
+ * every sequence b, query head h and block position i, one softmax over the
+ * ctx_len context keys and the S block keys of kv head h/(Hq/Hkv), scale
+ * 1/sqrt(D), no mask.
+ *   qkv:   bf16 [B*S][(Hq+2*Hkv)*D], row b*S+i holds q (Hq heads), k, v of position i
+ *   k_ctx, v_ctx: bf16 [B][Hkv][ctx_stride][D] (positions >= ctx_len not read
+ *          for their values; they must hold finite numbers)
+ *   out:   bf16 [B*S][Hq*D]
+ *   workspace: device scratch of dd_block_attention_workspace_size() bytes
+ *          (split-context partials), 256-byte aligned.
+ * All pointers device memory, 16-byte aligned. */
+typedef struct dd_attn_problem {
+  int32_t batch, block, n_q_heads, n_kv_heads, head_dim;
+  int32_t ctx_len, ctx_stride;
+  const void* qkv;
+  const void* k_ctx;
+  const void* v_ctx;
+  void* out;
+  void* workspace;
+  size_t workspace_bytes;
+} dd_attn_problem;
+
+dd_status dd_block_attention_workspace_size(const dd_attn_problem* p, size_t* bytes);
+dd_status dd_block_attention(const dd_attn_problem* p, void* stream);
+
+/* LM head fused with the confidence select: logits = x W^T (fp32 accumulate on
+ * the tensor cores, never written to memory), then per row conf = 1/sum_v
+ * exp(l_v - max) and arg = the lowest id of the maximum logit.
+ *   x: bf16 [rows][hidden], w: bf16 [vocab][hidden], conf: fp32 [rows], arg: int32 [rows]
+ *   workspace: dd_lmhead_select_workspace_size() bytes (per-tile partials).
+ * hidden a multiple of 64, vocab a multiple of 256, rows >= 1. */
+dd_status dd_lmhead_select_workspace_size(int32_t rows, int32_t hidden, int32_t vocab, size_t* bytes);
+dd_status dd_lmhead_select(int32_t rows, int32_t hidden, int32_t vocab, const void* x, const void* w,
+                           float* conf, int32_t* arg, void* workspace, size_t workspace_bytes, void* stream);
+
+/* Plain tensor-core GEMM y = x w^T with fp32 output, through the same kernel
+ * the linear layers use.  x: bf16 [rows][k], w: bf16 [n][k], y: fp32 [rows][n].
+ * n a multiple of 128, k a multiple of 64, rows a multiple of 16.  workspace:
+ * dd_gemm_workspace_size() bytes (split-K partials). */
+dd_status dd_gemm_workspace_size(int32_t rows, int32_t n, int32_t k, size_t* bytes);
+dd_status dd_gemm(int32_t rows, int32_t n, int32_t k, const void* x, const void* w, float* y,
+                  void* workspace, size_t workspace_bytes, void* stream);
+
+/* The commit rule alone (explainer steps 3-4) on given confidences and ids.
+ * conf: fp32 [B][S], arg: int32 [B][S], tokens: int32 [B][S] (updated),
+ * mask: uint32 [B] (updated), n_committed: int32 [B], remaining: int32 [1]
+ * (masked positions left over all sequences).  Device memory. */
+dd_status dd_commit(int32_t batch, int32_t block, const float* conf, const int32_t* arg, int32_t* tokens,
+                    uint32_t* mask, float gamma, int32_t mode, int32_t* n_committed, int32_t* remaining,
+                    void* stream);
+
+/* Launch a kernel that waits on a barrier nothing will ever complete, with a
+ * wait limit of `timeout_us` microseconds (1..1e7), and report what it
+ * recorded: DD_ERR_DEVICE_TIMEOUT when the bounded wait expired as designed.
+ * status: one device int32 used as the kernel's status word.  For testing the
+ * timeout path; synchronous. */
+dd_status dd_test_wait_timeout(int32_t timeout_us, int32_t* status, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DD_H */

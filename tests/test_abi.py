@@ -1,0 +1,97 @@
+"""The C-ABI library loads, exports every symbol include/dd.h declares, and
+rejects bad arguments on the host (no GPU needed)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import synth
+from block_wise_masked_dd_b300 import binding as B
+from block_wise_masked_dd_b300 import build as libbuild
+from block_wise_masked_dd_b300.decoder import config_struct
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    libbuild.build()
+    return B.load()
+
+
+def declared_symbols():
+    text = open(os.path.join(ROOT, "include", "dd.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(dd_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_four_core_calls():
+    syms = declared_symbols()
+    for s in ("dd_init_weights", "dd_set_context_kv", "dd_denoise_step", "dd_decode_block"):
+        assert s in syms
+
+
+def test_library_exports_every_declared_symbol(lib):
+    syms = declared_symbols()
+    assert len(syms) >= 19
+    for s in syms:
+        assert hasattr(lib, s), s
+    assert set(syms) <= set(B._SIGS), "binding misses a declared symbol"
+
+
+def test_status_strings(lib):
+    assert B.dd_status_string(0) == "ok"
+    assert B.dd_status_string(B.DD_ERR_DEVICE_TIMEOUT) == "device wait timed out"
+
+
+def test_workspace_size_host_only(lib):
+    for cfg in (synth.TINY, synth.SMALL, synth.LARGE):
+        n = B.dd_workspace_size(config_struct(cfg))
+        kv = 2 * cfg.n_layers * cfg.batch * cfg.n_kv_heads * max(cfg.max_ctx, 64) * cfg.head_dim * 2
+        assert kv <= n < kv + 2 ** 31
+
+
+@pytest.mark.parametrize("bad,code", [
+    (dict(block=33), B.DD_ERR_INVALID_ARG),
+    (dict(head_dim=96), B.DD_ERR_UNSUPPORTED),
+    (dict(n_kv_heads=3), B.DD_ERR_INVALID_ARG),
+    (dict(vocab=1000), B.DD_ERR_UNSUPPORTED),
+    (dict(hidden=200), B.DD_ERR_UNSUPPORTED),
+    (dict(batch=1, block=8), B.DD_ERR_UNSUPPORTED),
+    (dict(max_ctx=-1), B.DD_ERR_INVALID_ARG),
+])
+def test_bad_configs_rejected(lib, bad, code):
+    cfg = synth.TINY.replace(**bad)
+    with pytest.raises(B.DDError) as e:
+        B.dd_workspace_size(config_struct(cfg))
+    assert e.value.status == code
+    assert B.dd_last_error()
+
+
+def test_null_pointers_rejected_before_cuda(lib):
+    with pytest.raises(B.DDError) as e:
+        B.dd_create(config_struct(synth.TINY), 0, 1 << 30)
+    assert e.value.status == B.DD_ERR_INVALID_ARG
+    with pytest.raises(B.DDError):
+        B.dd_init_weights(0, B.dd_weights())
+    with pytest.raises(B.DDError):
+        B.dd_decode_block(0, 0, 0.8, 0)
+    p = B.dd_attn_problem(1, 16, 4, 3, 64, 10, 10, 0, 0, 0, 0, 0, 0)
+    with pytest.raises(B.DDError):
+        B.dd_block_attention_workspace_size(p)
+    with pytest.raises(B.DDError) as e:
+        B.dd_lmhead_select_workspace_size(16, 100, 4096)
+    assert e.value.status == B.DD_ERR_UNSUPPORTED
+    with pytest.raises(B.DDError):
+        B.dd_commit(0, 16, 0, 0, 0, 0, 0.8, 0, 0, 0)
+    with pytest.raises(B.DDError):
+        B.dd_test_wait_timeout(0, 0)
+
+
+def test_kernel_workspace_sizes(lib):
+    p = B.dd_attn_problem(64, 16, 32, 8, 128, 8192, 8192, 0, 0, 0, 0, 0, 0)
+    n = B.dd_block_attention_workspace_size(p)
+    assert n >= 256
+    assert B.dd_lmhead_select_workspace_size(1024, 4096, 131072) >= 3 * 512 * 1024 * 4
+    assert B.dd_gemm_workspace_size(128, 2048, 2048) >= 128 * 2048 * 4
