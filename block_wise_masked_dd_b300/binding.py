@@ -83,7 +83,13 @@ _SIGS = {
     "dd_commit": ([c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_float, c_int32, c_void_p, c_void_p,
                    c_void_p], c_int32),
     "dd_test_wait_timeout": ([c_int32, c_void_p, c_void_p], c_int32),
+    "dd_step_launch_count": ([c_void_p, ctypes.POINTER(c_int32)], c_int32),
+    "dd_profile_step": ([c_void_p, c_void_p, c_void_p, c_float, c_int32, c_void_p, c_void_p, c_int32,
+                         ctypes.POINTER(c_int32), c_void_p], c_int32),
 }
+
+KIND_NAMES = ["embed_norm", "gemm_qkv", "reduce_qkv", "block_attention", "attn_combine", "gemm_o", "norm_o",
+              "gemm_gate_up", "swiglu", "gemm_down", "norm_down", "lm_head_select", "select_combine", "commit"]
 
 _lib = None
 
@@ -204,3 +210,19 @@ def dd_commit(batch: int, block: int, conf: int, arg: int, tokens: int, mask: in
 
 def dd_test_wait_timeout(timeout_us: int, status: int, stream: int = 0):
     _check(load().dd_test_wait_timeout(timeout_us, status, stream))
+
+
+def dd_step_launch_count(ctx: int) -> int:
+    n = c_int32(0)
+    _check(load().dd_step_launch_count(ctx, ctypes.byref(n)))
+    return n.value
+
+
+def dd_profile_step(ctx: int, tokens: int, mask: int, gamma: float, mode: int, cap: int = 512, stream: int = 0):
+    """Returns a list of (kind name, milliseconds) for every launch of one step."""
+    times = (c_float * cap)()
+    kinds = (c_int32 * cap)()
+    n = c_int32(0)
+    _check(load().dd_profile_step(ctx, tokens, mask, gamma, mode, ctypes.cast(times, c_void_p),
+                                  ctypes.cast(kinds, c_void_p), cap, ctypes.byref(n), stream))
+    return [(KIND_NAMES[kinds[i]], float(times[i])) for i in range(n.value)]

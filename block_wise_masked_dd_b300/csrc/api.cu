@@ -108,6 +108,7 @@ struct dd_ctx {
   int32_t* hpin;  // pinned host: [0] remaining, [1] status
   uint64_t timeout_ns;
   int device;
+  int step_launches;  // kernels one denoising step launches
 };
 
 namespace {
@@ -201,7 +202,33 @@ Layout make_layout(const dd_config& c) {
 
 int32_t* small_ptr(dd_ctx* c) { return at<int32_t>(c->ws, c->L.small); }
 
-dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe) {
+// Kinds of launches in one step (for the per-kernel profile).
+enum LaunchKind : int {
+  kKEmbed = 0, kKGemmQkv, kKReduceQkv, kKAttention, kKAttnCombine, kKGemmO, kKNormO, kKGemmGu, kKSwiglu,
+  kKGemmDown, kKNormDown, kKLmSelect, kKSelectCombine, kKCommit, kKNumKinds
+};
+
+// Records an event after each launch when profiling; counts launches always.
+struct Marker {
+  cudaStream_t st;
+  cudaEvent_t* ev = nullptr;
+  int32_t* kinds = nullptr;
+  int cap = 0;
+  int n = 0;
+  cudaError_t err = cudaSuccess;
+  void operator()(int kind) {
+    if (ev && n < cap) {
+      kinds[n] = kind;
+      cudaError_t e = cudaEventRecord(ev[n + 1], st);
+      if (e != cudaSuccess) err = e;
+    }
+    ++n;
+  }
+};
+
+dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker* mk_in = nullptr) {
+  Marker local{st};
+  Marker& mk = mk_in ? *mk_in : local;
   const dd_config& cf = c->cfg;
   const Layout& L = c->L;
   uint8_t* ws = c->ws;
@@ -215,6 +242,7 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe) {
 
   DD_CUDA(dd::launch_embed_norm(at<int32_t>(ws, L.tok), at<uint32_t>(ws, L.mask), c->w.embed, c->w.pos, g_attn,
                                 x, y, cf.batch, cf.block, H, cf.vocab, cf.rms_eps, st));
+  mk(kKEmbed);
   for (int l = 0; l < cf.n_layers; ++l) {
     dd::GemmOut o{};
     o.partial = part;
@@ -223,7 +251,9 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe) {
     o.ld = c->qkvw;
     o.split_stride = (long long)R * c->qkvw;
     DD_CUDA(dd::launch_gemm(L.p_qkv, c->m_wqkv[l], c->m_y_b, o, status, c->timeout_ns, st));
+    mk(kKGemmQkv);
     DD_CUDA(dd::launch_reduce_bf16(part, L.p_qkv.splits, o.split_stride, R, c->qkvw, ws + L.qkv, st));
+    mk(kKReduceQkv);
     // block attention
     dd::AttnArgs a{};
     a.qkv = ws + L.qkv;
@@ -245,6 +275,11 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe) {
     a.status = status;
     a.timeout_ns = c->timeout_ns;
     DD_CUDA(dd::launch_attention(L.p_attn, a, c->m_kc, c->m_vc, st));
+    mk(kKAttention);
+    if (L.p_attn.n_splits > 1) {
+      DD_CUDA(dd::launch_attention_combine(L.p_attn, a, st));
+      mk(kKAttnCombine);
+    }
     if (probe && probe->attn_out)
       DD_CUDA(cudaMemcpyAsync(static_cast<uint8_t*>(probe->attn_out) + (size_t)l * R * c->HqD * 2, ws + L.attn,
                               (size_t)R * c->HqD * 2, cudaMemcpyDeviceToDevice, st));
@@ -252,19 +287,25 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe) {
     o.ld = H;
     o.split_stride = (long long)R * H;
     DD_CUDA(dd::launch_gemm(L.p_o, c->m_wo[l], c->m_attn_b, o, status, c->timeout_ns, st));
+    mk(kKGemmO);
     DD_CUDA(dd::launch_reduce_residual_norm(part, L.p_o.splits, o.split_stride, x, g_mlp + (size_t)l * H * 2, y, R, H,
                                             cf.rms_eps, st));
+    mk(kKNormO);
     // h = silu(y Wg^T) * (y Wu^T)
     o.ld = 2 * F;
     o.split_stride = (long long)R * 2 * F;
     DD_CUDA(dd::launch_gemm(L.p_gu, c->m_wgu[l], c->m_y_b, o, status, c->timeout_ns, st));
+    mk(kKGemmGu);
     DD_CUDA(dd::launch_reduce_swiglu(part, L.p_gu.splits, o.split_stride, ws + L.hmid, R, F, st));
+    mk(kKSwiglu);
     // x += h Wd^T ; y = norm(x) g (next layer's attention norm, or the final norm)
     o.ld = H;
     o.split_stride = (long long)R * H;
     DD_CUDA(dd::launch_gemm(L.p_d, c->m_wd[l], c->m_h_b, o, status, c->timeout_ns, st));
+    mk(kKGemmDown);
     const void* gn = (l + 1 < cf.n_layers) ? (const void*)(g_attn + (size_t)(l + 1) * H * 2) : c->w.g_final;
     DD_CUDA(dd::launch_reduce_residual_norm(part, L.p_d.splits, o.split_stride, x, gn, y, R, H, cf.rms_eps, st));
+    mk(kKNormDown);
   }
   // LM head + fused select
   dd::GemmOut so{};
@@ -273,8 +314,10 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe) {
   so.sel_s = at<float>(ws, L.sel_s);
   so.sel_a = at<int>(ws, L.sel_a);
   DD_CUDA(dd::launch_gemm(L.p_lm, c->m_y_a, c->m_lm, so, status, c->timeout_ns, st));
+  mk(kKLmSelect);
   DD_CUDA(dd::launch_select_combine(so.sel_m, so.sel_s, so.sel_a, L.p_lm.n_tiles, R, at<float>(ws, L.conf),
                                     at<int>(ws, L.arg), st));
+  mk(kKSelectCombine);
   if (probe) {
     if (probe->hidden)
       DD_CUDA(cudaMemcpyAsync(probe->hidden, y, (size_t)R * H * 2, cudaMemcpyDeviceToDevice, st));
@@ -291,14 +334,18 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe) {
   DD_CUDA(dd::launch_commit(at<float>(ws, L.conf), at<int>(ws, L.arg), at<int32_t>(ws, L.tok),
                             at<uint32_t>(ws, L.mask), at<float>(ws, L.params), 0.f, 0,
                             at<int32_t>(ws, L.ncommit), small_ptr(c), cf.batch, cf.block, st));
+  mk(kKCommit);
+  if (mk.err != cudaSuccess) return fail(DD_ERR_CUDA, "event record failed: %s", cudaGetErrorString(mk.err));
   return DD_OK;
 }
 
 dd_status ensure_graph(dd_ctx* c) {
   if (c->exec) return DD_OK;
   cudaGraph_t g = nullptr;
+  Marker counter{c->cap_stream};
   DD_CUDA(cudaStreamBeginCapture(c->cap_stream, cudaStreamCaptureModeThreadLocal));
-  dd_status s = enqueue_step(c, c->cap_stream, nullptr);
+  dd_status s = enqueue_step(c, c->cap_stream, nullptr, &counter);
+  c->step_launches = counter.n;
   cudaError_t e = cudaStreamEndCapture(c->cap_stream, &g);
   if (s != DD_OK) {
     if (g) cudaGraphDestroy(g);
@@ -551,6 +598,50 @@ dd_status dd_device_status(dd_ctx* c, void* stream) {
   return DD_OK;
 }
 
+dd_status dd_step_launch_count(dd_ctx* c, int32_t* n) {
+  dd_status s = check_ctx(c);
+  if (s != DD_OK) return s;
+  if (!n) return fail(DD_ERR_INVALID_ARG, "n is NULL");
+  s = ensure_graph(c);
+  if (s != DD_OK) return s;
+  *n = c->step_launches;
+  return DD_OK;
+}
+
+dd_status dd_profile_step(dd_ctx* c, int32_t* tokens, uint32_t* mask, float gamma, int32_t mode, float* times_ms,
+                          int32_t* kinds, int32_t cap, int32_t* n, void* stream) {
+  dd_status s = check_ctx(c);
+  if (s != DD_OK) return s;
+  if (!tokens || !mask || !times_ms || !kinds || !n || cap < 1) return fail(DD_ERR_INVALID_ARG, "bad profile arguments");
+  if (mode != DD_MODE_THRESHOLD && mode != DD_MODE_MOCK_AR) return fail(DD_ERR_INVALID_ARG, "bad mode %d", mode);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const dd_config& cf = c->cfg;
+  uint8_t* ws = c->ws;
+  std::vector<cudaEvent_t> ev(cap + 1);
+  for (auto& e : ev) DD_CUDA(cudaEventCreate(&e));
+  DD_CUDA(cudaMemcpyAsync(ws + c->L.tok, tokens, (size_t)c->R * 4, cudaMemcpyDefault, st));
+  DD_CUDA(cudaMemcpyAsync(ws + c->L.mask, mask, (size_t)cf.batch * 4, cudaMemcpyDefault, st));
+  DD_CUDA(dd::launch_set_params(at<float>(ws, c->L.params), gamma, mode, st));
+  Marker mk{st, ev.data(), kinds, cap};
+  DD_CUDA(cudaEventRecord(ev[0], st));
+  s = enqueue_step(c, st, nullptr, &mk);
+  if (s == DD_OK) {
+    cudaError_t e = cudaStreamSynchronize(st);
+    if (e != cudaSuccess) s = fail(DD_ERR_CUDA, "profile step: %s", cudaGetErrorString(e));
+  }
+  const int m = mk.n < cap ? mk.n : cap;
+  for (int i = 0; s == DD_OK && i < m; ++i) {
+    cudaError_t e = cudaEventElapsedTime(&times_ms[i], ev[i], ev[i + 1]);
+    if (e != cudaSuccess) s = fail(DD_ERR_CUDA, "event timing: %s", cudaGetErrorString(e));
+  }
+  for (auto& e : ev) cudaEventDestroy(e);
+  if (s != DD_OK) return s;
+  *n = m;
+  DD_CUDA(cudaMemcpyAsync(tokens, ws + c->L.tok, (size_t)c->R * 4, cudaMemcpyDefault, st));
+  DD_CUDA(cudaMemcpyAsync(mask, ws + c->L.mask, (size_t)cf.batch * 4, cudaMemcpyDefault, st));
+  return DD_OK;
+}
+
 // ----------------------------------------------------------- single kernels
 
 static dd_status attn_check(const dd_attn_problem* p) {
@@ -619,6 +710,7 @@ dd_status dd_block_attention(const dd_attn_problem* p, void* stream) {
   a.status = small + 1;
   a.timeout_ns = dd::kDefaultTimeoutNs;
   DD_CUDA(dd::launch_attention(plan, a, mk, mv, st));
+  DD_CUDA(dd::launch_attention_combine(plan, a, st));
   return DD_OK;
 }
 

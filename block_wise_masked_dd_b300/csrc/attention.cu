@@ -108,14 +108,17 @@ __device__ __forceinline__ void attend_tile(uint32_t k_base, uint32_t v_base, in
     o[n][2] *= alpha1;
     o[n][3] *= alpha1;
   }
-  // O += P V
+  // O += P V.  P is split into a bf16 head and a bf16 remainder
+  // (p = hi + lo to ~2^-17 relative) and both are multiplied by the same V
+  // fragment: a bf16-rounded P alone perturbs the output by ~2^-9 relative,
+  // which the residual stream and RMSNorm amplify into visible logit error.
 #pragma unroll
   for (int kk = 0; kk < NK / 16; ++kk) {
-    uint32_t pa[4];
-    pa[0] = pack_bf16(s[2 * kk][0], s[2 * kk][1]);
-    pa[1] = pack_bf16(s[2 * kk][2], s[2 * kk][3]);
-    pa[2] = pack_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1]);
-    pa[3] = pack_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3]);
+    uint32_t ph[4], pl[4];
+    split_bf16(s[2 * kk][0], s[2 * kk][1], ph[0], pl[0]);
+    split_bf16(s[2 * kk][2], s[2 * kk][3], ph[1], pl[1]);
+    split_bf16(s[2 * kk + 1][0], s[2 * kk + 1][1], ph[2], pl[2]);
+    split_bf16(s[2 * kk + 1][2], s[2 * kk + 1][3], ph[3], pl[3]);
     const int mi = lane >> 3;
     const int key = kk * 16 + (lane & 7) + (mi & 1) * 8;
 #pragma unroll
@@ -123,8 +126,10 @@ __device__ __forceinline__ void attend_tile(uint32_t k_base, uint32_t v_base, in
       const int col = jj * 16 + (mi >> 1) * 8;
       uint32_t b0, b1, b2, b3;
       ldmatrix_x4_trans(v_base + swz_off<D>(NK, key, col), b0, b1, b2, b3);
-      mma_bf16_16816(o[2 * jj], pa, b0, b1);
-      mma_bf16_16816(o[2 * jj + 1], pa, b2, b3);
+      mma_bf16_16816(o[2 * jj], ph, b0, b1);
+      mma_bf16_16816(o[2 * jj + 1], ph, b2, b3);
+      mma_bf16_16816(o[2 * jj], pl, b0, b1);
+      mma_bf16_16816(o[2 * jj + 1], pl, b2, b3);
     }
   }
 }
@@ -350,8 +355,11 @@ cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a, const CUtenso
     k_block_attn<128, attn_stages<128>()><<<grid, threads, p.smem_bytes, st>>>(map_k, map_v, a, p.n_splits, p.warps_c);
   else
     k_block_attn<64, attn_stages<64>()><<<grid, threads, p.smem_bytes, st>>>(map_k, map_v, a, p.n_splits, p.warps_c);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || p.n_splits == 1) return e;
+  return cudaGetLastError();
+}
+
+cudaError_t launch_attention_combine(const AttnPlan& p, const AttnArgs& a, cudaStream_t st) {
+  if (p.n_splits == 1) return cudaSuccess;
   const long long warps = (long long)a.B * a.Hkv * p.rows;
   const int blocks = (int)((warps + 7) / 8);
   if (p.D == 128) k_attn_combine<128><<<blocks, 256, 0, st>>>(a, p.n_splits);

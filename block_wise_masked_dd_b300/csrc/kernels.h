@@ -72,6 +72,8 @@ AttnPlan plan_attention(int B, int S, int Hq, int Hkv, int D, int max_ctx);
 size_t attention_partial_bytes(const AttnPlan& p, int B, int Hkv);
 cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a, const CUtensorMap& map_k, const CUtensorMap& map_v,
                              cudaStream_t st);
+// Merge the split partials (no-op with one split).
+cudaError_t launch_attention_combine(const AttnPlan& p, const AttnArgs& a, cudaStream_t st);
 
 // --------------------------------------------------- elementwise / small
 

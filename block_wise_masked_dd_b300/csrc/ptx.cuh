@@ -204,6 +204,13 @@ DD_DEV uint32_t pack_bf16(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&p);
 }
 
-DD_DEV float fast_exp2(float x) { return exp2f(x); }
+// Split two fp32 values into packed bf16 heads (round to nearest) and packed
+// bf16 remainders: x = head + rem up to the remainder's own rounding.
+DD_DEV void split_bf16(float x0, float x1, uint32_t& head, uint32_t& rem) {
+  head = pack_bf16(x0, x1);
+  const float h0 = __uint_as_float(head << 16);
+  const float h1 = __uint_as_float(head & 0xffff0000u);
+  rem = pack_bf16(x0 - h0, x1 - h1);
+}
 
 }  // namespace dd

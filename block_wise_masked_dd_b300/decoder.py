@@ -36,9 +36,13 @@ def bits_to_tensor(bits: np.ndarray, device) -> torch.Tensor:
 
 
 def pack_weights(cfg, w_bits: dict, device) -> dict:
-    """Stack per-layer bf16 weights into the layout dd_weights expects."""
+    """Stack per-layer bf16 weights (np.uint16 bit patterns or bf16 tensors)
+    into the layout dd_weights expects."""
     L = cfg.n_layers
-    t = lambda name: bits_to_tensor(w_bits[name], "cpu")
+
+    def t(name):
+        v = w_bits[name]
+        return v if isinstance(v, torch.Tensor) else bits_to_tensor(v, "cpu")
     out = {
         "embed": t("embed"),
         "pos": t("pos"),

@@ -180,6 +180,24 @@ typedef struct dd_probe {
 dd_status dd_denoise_step_probe(dd_ctx* ctx, int32_t* tokens, uint32_t* mask, float gamma, int32_t mode,
                                 int32_t* n_committed, const dd_probe* probe, void* stream);
 
+/* Kernel launches one denoising step enqueues (embedding through commit). */
+dd_status dd_step_launch_count(dd_ctx* ctx, int32_t* n);
+
+/* Launch kinds reported by dd_profile_step. */
+enum {
+  DD_KIND_EMBED = 0, DD_KIND_GEMM_QKV, DD_KIND_REDUCE_QKV, DD_KIND_ATTENTION, DD_KIND_ATTN_COMBINE, DD_KIND_GEMM_O,
+  DD_KIND_NORM_O, DD_KIND_GEMM_GATE_UP, DD_KIND_SWIGLU, DD_KIND_GEMM_DOWN, DD_KIND_NORM_DOWN, DD_KIND_LM_SELECT,
+  DD_KIND_SELECT_COMBINE, DD_KIND_COMMIT
+};
+
+/* One denoising step, as dd_denoise_step, but launched eagerly with a CUDA
+ * event recorded after every kernel on `stream`; synchronises, then writes
+ * the duration of each launch (ms, event to event) to times_ms and its
+ * DD_KIND_* to kinds (capacity `cap`) and the number written to *n.
+ * tokens/mask: device or host, updated in place. */
+dd_status dd_profile_step(dd_ctx* ctx, int32_t* tokens, uint32_t* mask, float gamma, int32_t mode, float* times_ms,
+                          int32_t* kinds, int32_t cap, int32_t* n, void* stream);
+
 /* ------------------------------------------- single-kernel entry points */
 
 /* Block attention for one layer (TwoTower article, "技術/ビジネス面"): for

@@ -223,12 +223,45 @@ def make_qkv(cfg: Config, seed: int = 0) -> np.ndarray:
 # Device-side draws for the large workloads (torch generator, seeded)
 # ---------------------------------------------------------------------------
 
-def torch_normal_bf16(shape, std: float, gen, device):
-    """A bf16 tensor ~ N(0, std^2) drawn on `device` with torch's generator `gen`."""
+def torch_normal_bf16(shape, std: float, gen, device, chunk_elems: int = 1 << 28):
+    """A bf16 tensor ~ N(0, std^2) drawn on `device` with torch's generator `gen`.
+
+    Drawn in fp32 slices of at most `chunk_elems` elements along the first
+    dimension, so a large tensor never needs a full fp32 copy.
+    """
     import torch
-    x = torch.empty(shape, dtype=torch.float32, device=device)
-    x.normal_(0.0, std, generator=gen)
-    return x.to(torch.bfloat16)
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    flat = out.view(shape[0], -1) if len(shape) > 1 else out.view(-1, 1)
+    per_row = flat.shape[1]
+    rows = max(1, chunk_elems // max(per_row, 1))
+    for r0 in range(0, flat.shape[0], rows):
+        r1 = min(flat.shape[0], r0 + rows)
+        tmp = torch.empty((r1 - r0, per_row), dtype=torch.float32, device=device)
+        tmp.normal_(0.0, std, generator=gen)
+        flat[r0:r1].copy_(tmp)
+    return out
+
+
+def make_weights_torch(cfg: Config, seed: int, device) -> dict:
+    """All weights as bf16 torch tensors drawn on `device` (same names, shapes
+    and scales as `make_weights`, different random stream)."""
+    import torch
+    gen = torch_generator(seed, device)
+    w = {name: torch_normal_bf16(shape, weight_std(cfg, name), gen, device) for name, shape in weight_names(cfg)}
+    one = torch.ones(cfg.hidden, dtype=torch.bfloat16, device=device)
+    for l in range(cfg.n_layers):
+        w[f"g_attn{l}"] = one.clone()
+        w[f"g_mlp{l}"] = one.clone()
+    w["g_final"] = one.clone()
+    return w
+
+
+def make_context_kv_torch(cfg: Config, seed: int, device, t0: int = 0, n: int | None = None):
+    """Context K and V on `device`, bf16 [L][B][Hkv][n][D] ~ N(0,1)."""
+    n = cfg.ctx_len if n is None else n
+    gen = torch_generator(seed * 1000003 + t0 * 7 + n, device)
+    shape = (max(cfg.n_layers, 1), cfg.batch, cfg.n_kv_heads, n, cfg.head_dim)
+    return torch_normal_bf16(shape, 1.0, gen, device), torch_normal_bf16(shape, 1.0, gen, device)
 
 
 def torch_generator(seed: int, device):

@@ -48,7 +48,7 @@ def _attn_case(B, S, Hq, Hkv, D, T, stride, seed):
         kb = q32[b, :, Hq * D:(Hq + Hkv) * D].reshape(S, Hkv, D)
         vb = q32[b, :, (Hq + Hkv) * D:].reshape(S, Hkv, D)
         want = oracle.block_attention(q, kb, vb, kc32[b, :, :T], vc32[b, :, :T])
-        close(got[b], want, TOL_ATTN, f"attention b={b} T={T}")
+        close(got[b], want, TOL_ATTN, f"attention b={b} T={T}", rel_rms=3e-3)
 
 
 @pytest.mark.parametrize("B,S,Hq,Hkv,D,T,stride", [
@@ -85,7 +85,7 @@ def test_block_attention_microbench_size_sampled():
         want = oracle.block_attention(q, kb, vb, kc[b, kvh:kvh + 1].float().cpu().numpy(),
                                       vc[b, kvh:kvh + 1].float().cpu().numpy())
         got = bf16_to_f32(out[b * S:(b + 1) * S]).reshape(S, Hq, D)[:, kvh * G:(kvh + 1) * G]
-        close(got, want, TOL_ATTN, f"attention b={b} kvh={kvh}")
+        close(got, want, TOL_ATTN, f"attention b={b} kvh={kvh}", rel_rms=3e-3)
 
 
 # ------------------------------------------------------- LM head + select
