@@ -83,6 +83,8 @@ _SIGS = {
     "dd_commit": ([c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_float, c_int32, c_void_p, c_void_p,
                    c_void_p], c_int32),
     "dd_test_wait_timeout": ([c_int32, c_void_p, c_void_p], c_int32),
+    "dd_lmhead_select_noalloc": ([c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p],
+                                 c_int32),
     "dd_step_launch_count": ([c_void_p, ctypes.POINTER(c_int32)], c_int32),
     "dd_profile_step": ([c_void_p, c_void_p, c_void_p, c_float, c_int32, c_void_p, c_void_p, c_int32,
                          ctypes.POINTER(c_int32), c_void_p], c_int32),
@@ -189,6 +191,13 @@ def dd_lmhead_select_workspace_size(rows: int, hidden: int, vocab: int) -> int:
 def dd_lmhead_select(rows: int, hidden: int, vocab: int, x: int, w: int, conf: int, arg: int, workspace: int,
                      workspace_bytes: int, stream: int = 0):
     _check(load().dd_lmhead_select(rows, hidden, vocab, x, w, conf, arg, workspace, workspace_bytes, stream))
+
+
+def dd_lmhead_select_noalloc(rows: int, hidden: int, vocab: int, x: int, w: int, conf: int, arg: int,
+                             stream: int = 0):
+    """LM head + select for callers that cannot allocate: no workspace
+    argument; scratch comes from an array inside the library (see dd.h)."""
+    _check(load().dd_lmhead_select_noalloc(rows, hidden, vocab, x, w, conf, arg, stream))
 
 
 def dd_gemm_workspace_size(rows: int, n: int, k: int) -> int:

@@ -54,6 +54,8 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 
 namespace dd {
 
+void set_error_message(const char* msg) { g_last_error = msg; }
+
 bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;

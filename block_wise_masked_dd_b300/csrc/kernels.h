@@ -105,6 +105,9 @@ cudaError_t launch_init_block(int32_t* tokens, uint32_t* mask, int B, int S, int
 cudaError_t launch_copy_i32(int32_t* dst, const int32_t* src, int n, cudaStream_t st);
 cudaError_t launch_wait_forever_bounded(int* status, uint64_t timeout_ns, cudaStream_t st);
 
+// Set the thread-local message dd_last_error() returns.
+void set_error_message(const char* msg);
+
 // ------------------------------------------------------------ tensor maps
 
 // 2D bf16 map over a row-major [rows][cols] matrix, box {64 cols, box_rows}.

@@ -235,6 +235,24 @@ dd_status dd_lmhead_select_workspace_size(int32_t rows, int32_t hidden, int32_t 
 dd_status dd_lmhead_select(int32_t rows, int32_t hidden, int32_t vocab, const void* x, const void* w,
                            float* conf, int32_t* arg, void* workspace, size_t workspace_bytes, void* stream);
 
+/* The same LM head + confidence select as dd_lmhead_select, for callers that
+ * cannot allocate device memory: code running under a host framework's memory
+ * pool or a fixed device-memory budget it must not bypass, or latency-critical
+ * loops that cannot afford the device synchronisation an allocation may
+ * cause.  The web pages on the method have no counterpart of this call; it
+ * is a deployment convenience.  It takes no workspace: the per-tile scratch
+ * lives in an 8 MiB array inside the library, held on every device that loads
+ * the library until the process exits, which limits rows * (vocab/256) to
+ * about 699000 (larger requests fail with DD_ERR_INVALID_ARG before anything
+ * is launched).  It calls no allocating routine.  The first call on each
+ * device looks up that array's device address (with the device current); make
+ * that first call before any stream capture.  All calls share the array and
+ * it keeps the last call's contents, so calls that overlap on the GPU race.
+ * x: bf16 [rows][hidden], w: bf16 [vocab][hidden], conf: fp32 [rows],
+ * arg: int32 [rows], all device memory; asynchronous on `stream`. */
+dd_status dd_lmhead_select_noalloc(int32_t rows, int32_t hidden, int32_t vocab, const void* x, const void* w,
+                                   float* conf, int32_t* arg, void* stream);
+
 /* Plain tensor-core GEMM y = x w^T with fp32 output, through the same kernel
  * the linear layers use.  x: bf16 [rows][k], w: bf16 [n][k], y: fp32 [rows][n].
  * n a multiple of 128, k a multiple of 64, rows a multiple of 16.  workspace:
