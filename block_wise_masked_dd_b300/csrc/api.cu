@@ -154,12 +154,13 @@ Layout make_layout(const dd_config& c) {
   const int qkvw = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
   const int HqD = c.n_q_heads * c.head_dim;
   L.alloc_ctx = c.max_ctx < 64 ? 64 : c.max_ctx;
-  L.p_qkv = dd::plan_gemm(dd::kEpiPartial, R, qkvw, c.hidden);
-  L.p_o = dd::plan_gemm(dd::kEpiPartial, R, c.hidden, HqD);
-  L.p_gu = dd::plan_gemm(dd::kEpiPartial, R, 2 * c.mlp, c.hidden);
-  L.p_d = dd::plan_gemm(dd::kEpiPartial, R, c.hidden, c.mlp);
-  L.p_lm = dd::plan_gemm(dd::kEpiSelect, R, c.vocab, c.hidden);
-  L.p_store = dd::plan_gemm(dd::kEpiStore, R, c.vocab, c.hidden);
+  // Every activation operand of the step is split (bf16 head + remainder).
+  L.p_qkv = dd::plan_gemm(dd::kEpiPartial, R, qkvw, c.hidden, 1);
+  L.p_o = dd::plan_gemm(dd::kEpiPartial, R, c.hidden, HqD, 1);
+  L.p_gu = dd::plan_gemm(dd::kEpiPartial, R, 2 * c.mlp, c.hidden, 1);
+  L.p_d = dd::plan_gemm(dd::kEpiPartial, R, c.hidden, c.mlp, 1);
+  L.p_lm = dd::plan_gemm(dd::kEpiSelect, R, c.vocab, c.hidden, 1);
+  L.p_store = dd::plan_gemm(dd::kEpiStore, R, c.vocab, c.hidden, 1);
   L.p_attn = dd::plan_attention(c.batch, c.block, c.n_q_heads, c.n_kv_heads, c.head_dim, c.max_ctx);
   size_t pe = 0;
   auto upd = [&](const dd::GemmPlan& p, int N) {
@@ -181,10 +182,11 @@ Layout make_layout(const dd_config& c) {
   L.kc = take(kv);
   L.vc = take(kv);
   L.x = take((size_t)R * c.hidden * 4);
-  L.y = take((size_t)R * c.hidden * 2);
-  L.qkv = take((size_t)R * qkvw * 2);
-  L.attn = take((size_t)R * HqD * 2);
-  L.hmid = take((size_t)R * c.mlp * 2);
+  // bf16 activations: heads in rows [0, R), remainders in rows [R, 2R)
+  L.y = take((size_t)2 * R * c.hidden * 2);
+  L.qkv = take((size_t)2 * R * qkvw * 2);
+  L.attn = take((size_t)2 * R * HqD * 2);
+  L.hmid = take((size_t)2 * R * c.mlp * 2);
   L.part = take(pe * 4);
   L.attn_part = take(dd::attention_partial_bytes(L.p_attn, c.batch, c.n_kv_heads));
   const size_t sel = (size_t)L.p_lm.n_tiles * R * 4;
@@ -254,12 +256,13 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
     o.split_stride = (long long)R * c->qkvw;
     DD_CUDA(dd::launch_gemm(L.p_qkv, c->m_wqkv[l], c->m_y_b, o, status, c->timeout_ns, st));
     mk(kKGemmQkv);
-    DD_CUDA(dd::launch_reduce_bf16(part, L.p_qkv.splits, o.split_stride, R, c->qkvw, ws + L.qkv, st));
+    DD_CUDA(dd::launch_reduce_bf16(part, L.p_qkv.splits, o.split_stride, R, c->qkvw, ws + L.qkv, 1, st));
     mk(kKReduceQkv);
     // block attention
     dd::AttnArgs a{};
     a.qkv = ws + L.qkv;
     a.ld_qkv = c->qkvw;
+    a.split = 1;
     a.B = cf.batch;
     a.S = cf.block;
     a.Hq = cf.n_q_heads;
@@ -283,8 +286,8 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
       mk(kKAttnCombine);
     }
     if (probe && probe->attn_out)
-      DD_CUDA(cudaMemcpyAsync(static_cast<uint8_t*>(probe->attn_out) + (size_t)l * R * c->HqD * 2, ws + L.attn,
-                              (size_t)R * c->HqD * 2, cudaMemcpyDeviceToDevice, st));
+      DD_CUDA(cudaMemcpyAsync(static_cast<uint8_t*>(probe->attn_out) + (size_t)l * 2 * R * c->HqD * 2, ws + L.attn,
+                              (size_t)2 * R * c->HqD * 2, cudaMemcpyDeviceToDevice, st));
     // x += attn Wo^T ; y = norm(x) g_mlp
     o.ld = H;
     o.split_stride = (long long)R * H;
@@ -322,7 +325,7 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
   mk(kKSelectCombine);
   if (probe) {
     if (probe->hidden)
-      DD_CUDA(cudaMemcpyAsync(probe->hidden, y, (size_t)R * H * 2, cudaMemcpyDeviceToDevice, st));
+      DD_CUDA(cudaMemcpyAsync(probe->hidden, y, (size_t)2 * R * H * 2, cudaMemcpyDeviceToDevice, st));
     if (probe->conf) DD_CUDA(cudaMemcpyAsync(probe->conf, ws + L.conf, (size_t)R * 4, cudaMemcpyDeviceToDevice, st));
     if (probe->arg) DD_CUDA(cudaMemcpyAsync(probe->arg, ws + L.arg, (size_t)R * 4, cudaMemcpyDeviceToDevice, st));
     if (probe->logits) {
@@ -433,10 +436,10 @@ dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_byte
   const uint64_t planes = (uint64_t)cf.n_layers * cf.batch * cf.n_kv_heads;
   bool ok = dd::make_map_3d(&c->m_kc, c->ws + L.kc, planes, L.alloc_ctx, cf.head_dim, 64) &&
             dd::make_map_3d(&c->m_vc, c->ws + L.vc, planes, L.alloc_ctx, cf.head_dim, 64) &&
-            dd::make_map_2d(&c->m_y_b, c->ws + L.y, c->R, cf.hidden, L.p_qkv.BN) &&
-            dd::make_map_2d(&c->m_attn_b, c->ws + L.attn, c->R, c->HqD, L.p_o.BN) &&
-            dd::make_map_2d(&c->m_h_b, c->ws + L.hmid, c->R, cf.mlp, L.p_d.BN) &&
-            dd::make_map_2d(&c->m_y_a, c->ws + L.y, c->R, cf.hidden, 128);
+            dd::make_map_2d(&c->m_y_b, c->ws + L.y, 2 * c->R, cf.hidden, L.p_qkv.BN) &&
+            dd::make_map_2d(&c->m_attn_b, c->ws + L.attn, 2 * c->R, c->HqD, L.p_o.BN) &&
+            dd::make_map_2d(&c->m_h_b, c->ws + L.hmid, 2 * c->R, cf.mlp, L.p_d.BN) &&
+            dd::make_map_2d(&c->m_y_a, c->ws + L.y, 2 * c->R, cf.hidden, 128);
   if (!ok) {
     dd_destroy(c);
     return fail(DD_ERR_CUDA, "tensor map encoding failed for the workspace buffers");

@@ -14,6 +14,12 @@
 // are staged once, by split 0.  With several splits per (sequence, kv head)
 // each CTA writes an unnormalised partial (o, m, l) and a combine kernel
 // merges them.
+//
+// Precision: P is multiplied as a bf16 head plus a bf16 remainder.  With
+// SPLIT, the activations (q and the block k/v) also arrive as head +
+// remainder rows and the remainder products are added (q_lo K, q K_blk_lo,
+// P V_blk_lo), and the output is written as head + remainder rows, so the
+// result tracks an fp32 computation to ~1e-5 relative.
 #include <math.h>
 
 #include "kernels.h"
@@ -29,30 +35,23 @@ constexpr int kKTB = 32;     // block-key tile (S <= 32)
 // Byte offset of element (row, col) in a tile of `rows` rows x D columns
 // stored as D/64 boxes of [rows][128 B] with the TMA 128-byte swizzle
 // (16-byte chunk c of row r lives at chunk c ^ (r & 7)).
-template <int D>
 __device__ __forceinline__ uint32_t swz_off(int rows, int r, int col) {
   const int box = col >> 6;
   const int chunk = (col & 63) >> 3;
   return box * rows * 128 + r * 128 + ((chunk ^ (r & 7)) << 4) + (col & 7) * 2;
 }
 
-template <int D>
-struct Tile {
-  static constexpr int kBytes = kKT * D * 2;
-  static constexpr int kBlkBytes = kKTB * D * 2;
-};
-
 // Process one tile of NK keys (NK = 64 context keys, or 32 block keys).
-template <int D, int NK>
-__device__ __forceinline__ void attend_tile(uint32_t k_base, uint32_t v_base, int n_valid, const uint32_t (&qf)[D / 16][4],
-                                            float (&o)[D / 8][4], float& m0, float& m1, float& l0, float& l1,
-                                            float scale_log2, int lane) {
+// QLO: add q_lo K^T.  KVLO: the tile has remainder K/V (block keys) to add.
+template <int D, int NK, bool QLO, bool KVLO>
+__device__ __forceinline__ void attend_tile(uint32_t k_base, uint32_t v_base, uint32_t k_lo, uint32_t v_lo,
+                                            int n_valid, const uint32_t (&qh)[D / 16][4],
+                                            const uint32_t (&ql)[D / 16][4], float (&o)[D / 8][4], float& m0,
+                                            float& m1, float& l0, float& l1, float scale_log2, int lane) {
   // S = Q K^T : 16 rows x NK keys
   float s[NK / 8][4];
 #pragma unroll
-  for (int j = 0; j < NK / 8; ++j) {
-    s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
-  }
+  for (int j = 0; j < NK / 8; ++j) s[j][0] = s[j][1] = s[j][2] = s[j][3] = 0.f;
 #pragma unroll
   for (int j = 0; j < NK / 8; ++j) {
     const int key = j * 8 + (lane & 7);
@@ -60,9 +59,18 @@ __device__ __forceinline__ void attend_tile(uint32_t k_base, uint32_t v_base, in
     for (int kk = 0; kk < D / 16; kk += 2) {
       const int col = kk * 16 + (lane >> 3) * 8;
       uint32_t b0, b1, b2, b3;
-      ldmatrix_x4(k_base + swz_off<D>(NK, key, col), b0, b1, b2, b3);
-      mma_bf16_16816(s[j], qf[kk], b0, b1);
-      mma_bf16_16816(s[j], qf[kk + 1], b2, b3);
+      ldmatrix_x4(k_base + swz_off(NK, key, col), b0, b1, b2, b3);
+      mma_bf16_16816(s[j], qh[kk], b0, b1);
+      mma_bf16_16816(s[j], qh[kk + 1], b2, b3);
+      if (QLO) {
+        mma_bf16_16816(s[j], ql[kk], b0, b1);
+        mma_bf16_16816(s[j], ql[kk + 1], b2, b3);
+      }
+      if (KVLO) {
+        ldmatrix_x4(k_lo + swz_off(NK, key, col), b0, b1, b2, b3);
+        mma_bf16_16816(s[j], qh[kk], b0, b1);
+        mma_bf16_16816(s[j], qh[kk + 1], b2, b3);
+      }
     }
   }
   // scale to base-2 units and mask keys beyond n_valid
@@ -125,27 +133,43 @@ __device__ __forceinline__ void attend_tile(uint32_t k_base, uint32_t v_base, in
     for (int jj = 0; jj < D / 16; ++jj) {
       const int col = jj * 16 + (mi >> 1) * 8;
       uint32_t b0, b1, b2, b3;
-      ldmatrix_x4_trans(v_base + swz_off<D>(NK, key, col), b0, b1, b2, b3);
+      ldmatrix_x4_trans(v_base + swz_off(NK, key, col), b0, b1, b2, b3);
       mma_bf16_16816(o[2 * jj], ph, b0, b1);
       mma_bf16_16816(o[2 * jj + 1], ph, b2, b3);
       mma_bf16_16816(o[2 * jj], pl, b0, b1);
       mma_bf16_16816(o[2 * jj + 1], pl, b2, b3);
+      if (KVLO) {
+        ldmatrix_x4_trans(v_lo + swz_off(NK, key, col), b0, b1, b2, b3);
+        mma_bf16_16816(o[2 * jj], ph, b0, b1);
+        mma_bf16_16816(o[2 * jj + 1], ph, b2, b3);
+      }
     }
   }
 }
 
-template <int D, int STAGES>
-__global__ void __launch_bounds__(288) k_block_attn(const __grid_constant__ CUtensorMap map_k,
+template <int D>
+__host__ __device__ constexpr int attn_stages() {
+  return D == 128 ? 3 : 4;
+}
+
+template <int D, bool SPLIT>
+__host__ __device__ constexpr int attn_smem_bytes() {
+  return 1024 + attn_stages<D>() * 2 * kKT * D * 2 + (SPLIT ? 4 : 2) * kKTB * D * 2 + 2 * attn_stages<D>() * 8 + 16;
+}
+
+// MAXW: most compute warps a launch may use (register budget follows it).
+template <int D, bool SPLIT, int MAXW>
+__global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_block_attn(const __grid_constant__ CUtensorMap map_k,
                                                     const __grid_constant__ CUtensorMap map_v, const AttnArgs a,
                                                     int n_splits, int warps_c) {
+  constexpr int STAGES = attn_stages<D>();
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  constexpr int kTileB = Tile<D>::kBytes;
-  constexpr int kBlkB = Tile<D>::kBlkBytes;
-  uint8_t* kv_stages = smem;                                  // STAGES x (K tile, V tile)
-  uint8_t* blk_k = smem + STAGES * 2 * kTileB;                // block keys
-  uint8_t* blk_v = blk_k + kBlkB;
-  uint64_t* full = reinterpret_cast<uint64_t*>(blk_v + kBlkB);
+  constexpr int kTileB = kKT * D * 2;
+  constexpr int kBlkB = kKTB * D * 2;
+  uint8_t* kv_stages = smem;                      // STAGES x (K tile, V tile)
+  uint8_t* blk = smem + STAGES * 2 * kTileB;       // block K, V (then K_lo, V_lo with SPLIT)
+  uint64_t* full = reinterpret_cast<uint64_t*>(blk + (SPLIT ? 4 : 2) * kBlkB);
   uint64_t* empty = full + STAGES;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
 
@@ -157,6 +181,7 @@ __global__ void __launch_bounds__(288) k_block_attn(const __grid_constant__ CUte
   const int tile0 = split * per;
   const int tile1 = min(ntiles, tile0 + per);
   const int z = a.z0 + b * a.Hkv + kvh;
+  const int R = a.B * a.S;
   const __nv_bfloat16* qkv = reinterpret_cast<const __nv_bfloat16*>(a.qkv);
 
   if (threadIdx.x == 0) {
@@ -168,19 +193,21 @@ __global__ void __launch_bounds__(288) k_block_attn(const __grid_constant__ CUte
     fence_mbar_init();
   }
   if (split == 0) {
-    // Stage the block keys/values of this kv head (rows >= S zero-filled).
+    // Stage the block keys/values of this kv head (rows >= S zero-filled):
+    // tiles k, v, and with SPLIT k_lo, v_lo.
     const int chunks = kKTB * (D / 8);
-    for (int c = threadIdx.x; c < 2 * chunks; c += blockDim.x) {
-      const int which = c / chunks;  // 0 = k, 1 = v
+    const int ntile = SPLIT ? 4 : 2;
+    for (int c = threadIdx.x; c < ntile * chunks; c += blockDim.x) {
+      const int which = c / chunks;  // 0 = k, 1 = v, 2 = k_lo, 3 = v_lo
       const int cc = c % chunks;
       const int r = cc / (D / 8), col = (cc % (D / 8)) * 8;
       uint4 val = make_uint4(0, 0, 0, 0);
       if (r < a.S) {
-        const long long off = (long long)(b * a.S + r) * a.ld_qkv + (a.Hq + which * a.Hkv + kvh) * D + col;
+        const long long row = (long long)(which >= 2 ? R : 0) + b * a.S + r;
+        const long long off = row * a.ld_qkv + (a.Hq + (which & 1) * a.Hkv + kvh) * D + col;
         val = *reinterpret_cast<const uint4*>(qkv + off);
       }
-      uint8_t* dst = (which == 0 ? blk_k : blk_v) + swz_off<D>(kKTB, r, col);
-      *reinterpret_cast<uint4*>(dst) = val;
+      *reinterpret_cast<uint4*>(blk + which * kBlkB + swz_off(kKTB, r, col)) = val;
     }
   }
   __syncthreads();
@@ -215,10 +242,13 @@ __global__ void __launch_bounds__(288) k_block_attn(const __grid_constant__ CUte
   const int g0 = r0 / a.S, i0 = r0 % a.S;
   const int g1 = r1 / a.S, i1 = r1 % a.S;
   const int h0 = kvh * a.G + g0, h1 = kvh * a.G + g1;
-  uint32_t qf[D / 16][4];
-  {
-    const __nv_bfloat16* q0 = qkv + (long long)(b * a.S + i0) * a.ld_qkv + h0 * D + (lane & 3) * 2;
-    const __nv_bfloat16* q1 = qkv + (long long)(b * a.S + i1) * a.ld_qkv + h1 * D + (lane & 3) * 2;
+  uint32_t qh[D / 16][4], ql[D / 16][4];
+#pragma unroll
+  for (int half = 0; half < (SPLIT ? 2 : 1); ++half) {
+    const long long ro = half ? R : 0;
+    const __nv_bfloat16* q0 = qkv + (ro + b * a.S + i0) * a.ld_qkv + h0 * D + (lane & 3) * 2;
+    const __nv_bfloat16* q1 = qkv + (ro + b * a.S + i1) * a.ld_qkv + h1 * D + (lane & 3) * 2;
+    uint32_t(&qf)[D / 16][4] = half ? ql : qh;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
       qf[kk][0] = *reinterpret_cast<const uint32_t*>(q0 + kk * 16);
@@ -233,7 +263,9 @@ __global__ void __launch_bounds__(288) k_block_attn(const __grid_constant__ CUte
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
 
   if (split == 0) {
-    attend_tile<D, kKTB>(smem_u32(blk_k), smem_u32(blk_v), a.S, qf, o, m0, m1, l0, l1, a.scale_log2, lane);
+    const uint32_t bk = smem_u32(blk);
+    attend_tile<D, kKTB, SPLIT, SPLIT>(bk, bk + kBlkB, bk + 2 * kBlkB, bk + 3 * kBlkB, a.S, qh, ql, o, m0, m1, l0,
+                                       l1, a.scale_log2, lane);
   }
   {
     int s = 0;
@@ -244,7 +276,8 @@ __global__ void __launch_bounds__(288) k_block_attn(const __grid_constant__ CUte
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       const uint32_t kb = smem_u32(kv_stages + s * 2 * kTileB);
-      attend_tile<D, kKT>(kb, kb + kTileB, min(kKT, T - t * kKT), qf, o, m0, m1, l0, l1, a.scale_log2, lane);
+      attend_tile<D, kKT, SPLIT, false>(kb, kb + kTileB, 0, 0, min(kKT, T - t * kKT), qh, ql, o, m0, m1, l0, l1,
+                                        a.scale_log2, lane);
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[s]);
       if (++s == STAGES) { s = 0; phase ^= 1; }
@@ -258,12 +291,18 @@ __global__ void __launch_bounds__(288) k_block_attn(const __grid_constant__ CUte
   if (n_splits == 1) {
     __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
     const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+    const long long lo_off = (long long)R * a.ld_out;
     __nv_bfloat16* d0 = out + (long long)(b * a.S + i0) * a.ld_out + h0 * D + (lane & 3) * 2;
     __nv_bfloat16* d1 = out + (long long)(b * a.S + i1) * a.ld_out + h1 * D + (lane & 3) * 2;
 #pragma unroll
     for (int n = 0; n < D / 8; ++n) {
-      *reinterpret_cast<uint32_t*>(d0 + n * 8) = pack_bf16(o[n][0] * inv0, o[n][1] * inv0);
-      *reinterpret_cast<uint32_t*>(d1 + n * 8) = pack_bf16(o[n][2] * inv1, o[n][3] * inv1);
+      uint32_t hi, lo;
+      split_bf16(o[n][0] * inv0, o[n][1] * inv0, hi, lo);
+      *reinterpret_cast<uint32_t*>(d0 + n * 8) = hi;
+      if (SPLIT) *reinterpret_cast<uint32_t*>(d0 + lo_off + n * 8) = lo;
+      split_bf16(o[n][2] * inv1, o[n][3] * inv1, hi, lo);
+      *reinterpret_cast<uint32_t*>(d1 + n * 8) = hi;
+      if (SPLIT) *reinterpret_cast<uint32_t*>(d1 + lo_off + n * 8) = lo;
     }
   } else {
     const long long prow = ((long long)(b * a.Hkv + kvh) * n_splits + split) * (a.G * a.S);
@@ -308,16 +347,28 @@ __global__ void k_attn_combine(const AttnArgs a, int n_splits) {
     for (int k = 0; k < D / 32; ++k) acc[k] += w * po[lane + 32 * k];
   }
   const int g = r / a.S, i = r % a.S;
+  const long long R = (long long)a.B * a.S;
   __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + (long long)(b * a.S + i) * a.ld_out +
                        (kvh * a.G + g) * D;
   const float inv = 1.f / L;
 #pragma unroll
-  for (int k = 0; k < D / 32; ++k) out[lane + 32 * k] = __float2bfloat16_rn(acc[k] * inv);
+  for (int k = 0; k < D / 32; ++k) {
+    const float v = acc[k] * inv;
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    out[lane + 32 * k] = h;
+    if (a.split) out[R * a.ld_out + lane + 32 * k] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
 }
 
-template <int D>
-constexpr int attn_stages() {
-  return D == 128 ? 3 : 4;
+template <int D, bool SPLIT>
+void launch_attn_kernel(const AttnPlan& p, const AttnArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
+                        cudaStream_t st) {
+  dim3 grid(p.n_splits, a.Hkv, a.B);
+  const int threads = (p.warps_c + 1) * 32;
+  if (p.warps_c <= 4)
+    k_block_attn<D, SPLIT, 4><<<grid, threads, attn_smem_bytes<D, SPLIT>(), st>>>(mk, mv, a, p.n_splits, p.warps_c);
+  else
+    k_block_attn<D, SPLIT, 8><<<grid, threads, attn_smem_bytes<D, SPLIT>(), st>>>(mk, mv, a, p.n_splits, p.warps_c);
 }
 
 }  // namespace
@@ -328,8 +379,7 @@ AttnPlan plan_attention(int B, int S, int Hq, int Hkv, int D, int max_ctx) {
   p.rows = (Hq / Hkv) * S;
   p.warps_c = p.rows / 16;
   p.stages = D == 128 ? attn_stages<128>() : attn_stages<64>();
-  const int tile_b = kKT * D * 2, blk_b = kKTB * D * 2;
-  p.smem_bytes = 1024 + p.stages * 2 * tile_b + 2 * blk_b + 2 * p.stages * 8 + 16;
+  p.smem_bytes = D == 128 ? attn_smem_bytes<128, true>() : attn_smem_bytes<64, true>();
   const int pairs = B * Hkv;
   const int ntiles = (max_ctx + kKT - 1) / kKT;
   // Enough CTAs for ~4 resident waves (2 CTAs per SM), at least 4 tiles per split.
@@ -349,12 +399,13 @@ size_t attention_partial_bytes(const AttnPlan& p, int B, int Hkv) {
 
 cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a, const CUtensorMap& map_k, const CUtensorMap& map_v,
                              cudaStream_t st) {
-  dim3 grid(p.n_splits, a.Hkv, a.B);
-  const int threads = (p.warps_c + 1) * 32;
-  if (p.D == 128)
-    k_block_attn<128, attn_stages<128>()><<<grid, threads, p.smem_bytes, st>>>(map_k, map_v, a, p.n_splits, p.warps_c);
-  else
-    k_block_attn<64, attn_stages<64>()><<<grid, threads, p.smem_bytes, st>>>(map_k, map_v, a, p.n_splits, p.warps_c);
+  if (p.D == 128) {
+    if (a.split) launch_attn_kernel<128, true>(p, a, map_k, map_v, st);
+    else launch_attn_kernel<128, false>(p, a, map_k, map_v, st);
+  } else {
+    if (a.split) launch_attn_kernel<64, true>(p, a, map_k, map_v, st);
+    else launch_attn_kernel<64, false>(p, a, map_k, map_v, st);
+  }
   return cudaGetLastError();
 }
 
@@ -369,10 +420,14 @@ cudaError_t launch_attention_combine(const AttnPlan& p, const AttnArgs& a, cudaS
 
 cudaError_t prepare_attention_kernels() {
   const int lim = 227 * 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_block_attn<128, attn_stages<128>()>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_block_attn<64, attn_stages<64>()>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  const void* fns[] = {(const void*)k_block_attn<128, true, 4>,  (const void*)k_block_attn<128, false, 4>,
+                       (const void*)k_block_attn<64, true, 4>,   (const void*)k_block_attn<64, false, 4>,
+                       (const void*)k_block_attn<128, true, 8>,  (const void*)k_block_attn<128, false, 8>,
+                       (const void*)k_block_attn<64, true, 8>,   (const void*)k_block_attn<64, false, 8>};
+  cudaError_t e = cudaSuccess;
+  for (const void* f : fns) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  }
   return e;
 }
 

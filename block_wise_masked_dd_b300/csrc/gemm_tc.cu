@@ -8,12 +8,17 @@
 //     M side (128 output features per tile) and the B*S activation rows on
 //     the N side, so a 128-row decode batch still fills the 128-lane
 //     accumulator; K may be split across CTAs, each writing an fp32 partial
-//     that a reduce kernel sums and post-processes (bias-free epilogues:
-//     bf16 store, residual + RMSNorm, SwiGLU);
+//     that a reduce kernel sums and post-processes (bf16 store, residual +
+//     RMSNorm, SwiGLU);
 //   * the LM head: activation rows on the M side (one TMEM lane per row) and
 //     256 vocab entries per tile on the N side; the epilogue folds each
 //     row's 256 logits into a running (max, sum of exp, first argmax) so the
 //     logits never reach global memory.
+//
+// Split activations: an activation operand may be stored as a bf16 head
+// (rows [0, R)) and a bf16 remainder (rows [R, 2R)) of the same tensor map;
+// both tiles are loaded per K block and both products accumulate into the
+// same fp32 accumulator, so the GEMM sees the activation to ~2^-17.
 //
 // Roles (192 threads): warp 0 issues TMA loads, warp 1 owns TMEM and issues
 // MMAs, warps 2-5 run the epilogue (TMEM lane quarter = warp % 4).  Two
@@ -37,11 +42,20 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct KArgs {
   int m_tiles, n_tiles, splits, kb_total, kb_per_split, BN, stages, tiles_total;
+  int split_act;   // activation operand carries a remainder half
+  int split_rows;  // row offset of the remainder half in the activation map
   uint32_t tmem_half;
   GemmOut out;
   int* status;
   uint64_t timeout_ns;
 };
+
+// Bytes of one pipeline stage: A tile, B tile, and the activation remainder.
+__host__ __device__ inline int stage_bytes_of(int epi, int BN, int split) {
+  const int b = BN * kBK * 2;
+  const int act = (epi == kEpiPartial) ? b : kStageA;
+  return kStageA + b + (split ? act : 0);
+}
 
 template <int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -49,7 +63,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int stage_b = args.BN * kBK * 2;
-  const int stage_bytes = kStageA + stage_b;
+  const int stage_bytes = stage_bytes_of(EPI, args.BN, args.split_act);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + args.stages * stage_bytes);
   uint64_t* empty = full + args.stages;
   uint64_t* acc_full = empty + args.stages;
@@ -105,6 +119,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(&full[s], stage_bytes);
           tma_load_2d(sa, &map_a, &full[s], kb * kBK, mt * kBM);
           tma_load_2d(sa + kStageA, &map_b, &full[s], kb * kBK, nt * args.BN);
+          if (args.split_act) {
+            if (EPI == kEpiPartial)
+              tma_load_2d(sa + kStageA + stage_b, &map_b, &full[s], kb * kBK, args.split_rows + nt * args.BN);
+            else
+              tma_load_2d(sa + kStageA + stage_b, &map_a, &full[s], kb * kBK, args.split_rows + mt * kBM);
+          }
           if (++s == args.stages) { s = 0; phase ^= 1; }
         }
       }
@@ -132,10 +152,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + s * stage_bytes);
           const uint32_t b_addr = a_addr + kStageA;
+          const uint32_t lo_addr = b_addr + stage_b;
 #pragma unroll
           for (int k = 0; k < kBK / 16; ++k) {
             tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
                         (kb > kb0 || k > 0) ? 1u : 0u);
+            if (args.split_act) {
+              if (EPI == kEpiPartial)
+                tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(lo_addr + k * 32), idesc, 1u);
+              else
+                tc_mma_bf16(d_tmem, smem_desc_sw128(lo_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc, 1u);
+            }
           }
           tc_commit(&empty[s]);
           if (++s == args.stages) { s = 0; phase ^= 1; }
@@ -241,9 +268,11 @@ uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
 
 }  // namespace
 
-GemmPlan plan_gemm(int epi, int rows, int N, int K) {
+GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act) {
   GemmPlan p{};
   p.epi = epi;
+  p.split_act = split_act;
+  p.split_rows = rows;
   p.kb_total = K / kBK;
   if (epi == kEpiPartial) {
     // features on M, activation rows on N
@@ -256,7 +285,7 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K) {
     p.BN = 256;
     p.n_tiles = N / p.BN;
   }
-  const int stage_bytes = kStageA + p.BN * kBK * 2;
+  const int stage_bytes = stage_bytes_of(epi, p.BN, split_act);
   p.stages = (200 * 1024) / stage_bytes;
   if (p.stages > 8) p.stages = 8;
   if (p.stages < 2) p.stages = 2;
@@ -303,6 +332,8 @@ cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUten
   a.BN = p.BN;
   a.stages = p.stages;
   a.tiles_total = p.tiles_total;
+  a.split_act = p.split_act;
+  a.split_rows = p.split_rows;
   a.tmem_half = p.tmem_half;
   a.out = out;
   a.status = status;

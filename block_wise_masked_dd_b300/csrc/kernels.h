@@ -28,6 +28,8 @@ struct GemmPlan {
   int grid;
   int smem_bytes;
   uint32_t tmem_half;             // TMEM columns per accumulator buffer (power of two >= BN)
+  int split_act;                  // activation operand = bf16 head rows [0,R) + remainder rows [R,2R)
+  int split_rows;                 // R
 };
 
 struct GemmOut {
@@ -40,8 +42,9 @@ struct GemmOut {
   int* sel_a;
 };
 
-// Plan a GEMM over activations [rows][K] and weights [N][K].
-GemmPlan plan_gemm(int epi, int rows, int N, int K);
+// Plan a GEMM over activations [rows][K] and weights [N][K].  With
+// split_act the activation map covers [2*rows][K]: bf16 heads then remainders.
+GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act = 0);
 // Enqueue.  map_w / map_x: 2D bf16 tensor maps with 128-byte swizzle, box
 // {64, 128} for the operand on the MMA M side and {64, BN} for the other.
 cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmOut& out,
@@ -54,8 +57,9 @@ struct AttnPlan {
 };
 
 struct AttnArgs {
-  const void* qkv;     // bf16 [B*S][ld_qkv]
+  const void* qkv;     // bf16 [B*S][ld_qkv] (with split: [2*B*S][ld_qkv], heads then remainders)
   int ld_qkv;
+  int split;           // q and block k/v carry bf16 remainders; the output is written as head + remainder
   int B, S, Hq, Hkv, G;
   const int* ctx_len;  // device int (context length)
   int z0;              // tensor-map z offset of (b=0, kvh=0) for this layer
@@ -77,17 +81,19 @@ cudaError_t launch_attention_combine(const AttnPlan& p, const AttnArgs& a, cudaS
 
 // --------------------------------------------------- elementwise / small
 
+// Activation outputs named "split" below are written as bf16 heads in rows
+// [0, rows) and bf16 remainders (value - head, rounded) in rows [rows, 2*rows).
 cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const void* embed, const void* pos,
-                              const void* g, float* x, void* y, int B, int S, int H, int V, float eps,
+                              const void* g, float* x, void* y_split, int B, int S, int H, int V, float eps,
                               cudaStream_t st);
 cudaError_t launch_reduce_bf16(const float* part, int splits, long long split_stride, int rows, int N, void* out,
-                               cudaStream_t st);
+                               int split, cudaStream_t st);
 cudaError_t launch_reduce_f32(const float* part, int splits, long long split_stride, int rows, int N, float* out,
                               cudaStream_t st);
 cudaError_t launch_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
-                                        const void* g, void* y, int rows, int H, float eps, cudaStream_t st);
-cudaError_t launch_reduce_swiglu(const float* part, int splits, long long split_stride, void* h, int rows, int F,
-                                 cudaStream_t st);
+                                        const void* g, void* y_split, int rows, int H, float eps, cudaStream_t st);
+cudaError_t launch_reduce_swiglu(const float* part, int splits, long long split_stride, void* h_split, int rows,
+                                 int F, cudaStream_t st);
 cudaError_t launch_select_combine(const float* sel_m, const float* sel_s, const int* sel_a, int n_tiles, int rows,
                                   float* conf, int* arg, cudaStream_t st);
 // params: device float[2] {gamma, mode-as-float}, read at run time so one

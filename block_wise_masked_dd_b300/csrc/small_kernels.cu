@@ -27,11 +27,20 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 
 __device__ __forceinline__ float bf(const __nv_bfloat16* p, long long i) { return __bfloat162float(p[i]); }
 
+// Store v as a bf16 head at hi[0] and the bf16-rounded remainder at lo[0].
+__device__ __forceinline__ void store_split(__nv_bfloat16* hi, __nv_bfloat16* lo, float v) {
+  const __nv_bfloat16 h = __float2bfloat16_rn(v);
+  *hi = h;
+  *lo = __float2bfloat16_rn(v - __bfloat162float(h));
+}
+
 // x[r] = E[id] + Pos[i] with id = V ([MASK]) for masked positions;
-// y[r] = bf16(x / sqrt(mean(x^2) + eps) * g).  One CTA per row.
+// y[r] = x / sqrt(mean(x^2) + eps) * g, split into head (row r) and
+// remainder (row R + r).  One CTA per row.
 __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const __nv_bfloat16* embed,
                              const __nv_bfloat16* pos, const __nv_bfloat16* g, float* x, __nv_bfloat16* y, int S,
                              int H, int V, float eps) {
+  const long long lo_off = (long long)gridDim.x * H;
   __shared__ float red[32];
   extern __shared__ float xs[];
   const int r = blockIdx.x, b = r / S, i = r % S;
@@ -49,13 +58,15 @@ __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const 
   const float rs = rsqrtf(ss / H + eps);
   for (int c = threadIdx.x; c < H; c += blockDim.x) {
     x[(long long)r * H + c] = xs[c];
-    y[(long long)r * H + c] = __float2bfloat16_rn(xs[c] * rs * bf(g, c));
+    store_split(y + (long long)r * H + c, y + lo_off + (long long)r * H + c, xs[c] * rs * bf(g, c));
   }
 }
 
-// out[r][n] = sum over splits of part[s][r][n]
+// out[r][n] = sum over splits of part[s][r][n]; bf16 output optionally split
+// (remainder at out + total).
 template <typename OutT>
-__global__ void k_reduce(const float* part, int splits, long long split_stride, long long total, OutT* out) {
+__global__ void k_reduce(const float* part, int splits, long long split_stride, long long total, OutT* out,
+                         int split) {
   for (long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 4; e < total;
        e += (long long)gridDim.x * blockDim.x * 4) {
     float4 acc = *reinterpret_cast<const float4*>(part + e);
@@ -64,22 +75,26 @@ __global__ void k_reduce(const float* part, int splits, long long split_stride, 
       acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
     }
     if constexpr (sizeof(OutT) == 2) {
-      uint2 pk;
-      pk.x = pack_bf16(acc.x, acc.y);
-      pk.y = pack_bf16(acc.z, acc.w);
-      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + e) = pk;
+      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
+      uint2 hi, lo;
+      split_bf16(acc.x, acc.y, hi.x, lo.x);
+      split_bf16(acc.z, acc.w, hi.y, lo.y);
+      *reinterpret_cast<uint2*>(o + e) = hi;
+      if (split) *reinterpret_cast<uint2*>(o + total + e) = lo;
     } else {
       *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + e) = acc;
     }
   }
 }
 
-// x[r] += sum_s part[s][r]; y[r] = bf16(rmsnorm(x[r]) * g).  One CTA per row.
+// x[r] += sum_s part[s][r]; y[r] = rmsnorm(x[r]) * g, split into head (row r)
+// and remainder (row R + r).  One CTA per row.
 __global__ void k_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
                                        const __nv_bfloat16* g, __nv_bfloat16* y, int H, float eps) {
   __shared__ float red[32];
   extern __shared__ float xs[];
   const int r = blockIdx.x;
+  const long long lo_off = (long long)gridDim.x * H;
   float ss = 0.f;
   for (int c = threadIdx.x; c < H; c += blockDim.x) {
     float v = x[(long long)r * H + c];
@@ -91,12 +106,12 @@ __global__ void k_reduce_residual_norm(const float* part, int splits, long long 
   const float rs = rsqrtf(ss / H + eps);
   for (int c = threadIdx.x; c < H; c += blockDim.x) {
     x[(long long)r * H + c] = xs[c];
-    y[(long long)r * H + c] = __float2bfloat16_rn(xs[c] * rs * bf(g, c));
+    store_split(y + (long long)r * H + c, y + lo_off + (long long)r * H + c, xs[c] * rs * bf(g, c));
   }
 }
 
-// h[r][f] = bf16(silu(gate) * up), gate = column f, up = column F + f of the
-// summed partials [rows][2F].
+// h[r][f] = silu(gate) * up, gate = column f, up = column F + f of the
+// summed partials [rows][2F]; split into head and remainder (at h + rows*F).
 __global__ void k_reduce_swiglu(const float* part, int splits, long long split_stride, __nv_bfloat16* h, int rows,
                                 int F) {
   const long long total = (long long)rows * F;
@@ -111,7 +126,7 @@ __global__ void k_reduce_swiglu(const float* part, int splits, long long split_s
       up += part[s * split_stride + gi + F];
     }
     const float si = gt / (1.f + expf(-gt));
-    h[e] = __float2bfloat16_rn(si * up);
+    store_split(h + e, h + total + e, si * up);
   }
 }
 
@@ -262,17 +277,17 @@ cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const
 }
 
 cudaError_t launch_reduce_bf16(const float* part, int splits, long long split_stride, int rows, int N, void* out,
-                               cudaStream_t st) {
+                               int split, cudaStream_t st) {
   const long long total = (long long)rows * N;
   k_reduce<__nv_bfloat16><<<grid_for(total / 4, 256), 256, 0, st>>>(part, splits, split_stride, total,
-                                                                    (__nv_bfloat16*)out);
+                                                                    (__nv_bfloat16*)out, split);
   return cudaGetLastError();
 }
 
 cudaError_t launch_reduce_f32(const float* part, int splits, long long split_stride, int rows, int N, float* out,
                               cudaStream_t st) {
   const long long total = (long long)rows * N;
-  k_reduce<float><<<grid_for(total / 4, 256), 256, 0, st>>>(part, splits, split_stride, total, out);
+  k_reduce<float><<<grid_for(total / 4, 256), 256, 0, st>>>(part, splits, split_stride, total, out, 0);
   return cudaGetLastError();
 }
 

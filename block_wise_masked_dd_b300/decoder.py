@@ -112,9 +112,11 @@ class Decoder:
         cfg = self.cfg
         R = cfg.batch * cfg.block
         dev = self.device
+        # activations come back as bf16 heads (rows [0,R)) and remainders (rows [R,2R))
         out = {
-            "attn_out": torch.empty((cfg.n_layers, R, cfg.n_q_heads * cfg.head_dim), dtype=torch.bfloat16, device=dev),
-            "hidden": torch.empty((R, cfg.hidden), dtype=torch.bfloat16, device=dev),
+            "attn_out": torch.empty((cfg.n_layers, 2 * R, cfg.n_q_heads * cfg.head_dim), dtype=torch.bfloat16,
+                                    device=dev),
+            "hidden": torch.empty((2 * R, cfg.hidden), dtype=torch.bfloat16, device=dev),
             "logits": torch.empty((R, cfg.vocab), dtype=torch.float32, device=dev) if logits else None,
             "conf": torch.empty(R, dtype=torch.float32, device=dev),
             "arg": torch.empty(R, dtype=torch.int32, device=dev),
@@ -125,6 +127,13 @@ class Decoder:
         B.dd_denoise_step_probe(self.ctx, _ptr(tokens), _ptr(mask), gamma, mode, _ptr(out["n_committed"]), p,
                                 _stream(stream))
         return out
+
+
+def join_split(t: torch.Tensor) -> torch.Tensor:
+    """fp32 value of a head/remainder bf16 tensor whose second-to-last axis
+    holds heads in its first half and remainders in its second half."""
+    n = t.shape[-2] // 2
+    return t[..., :n, :].float() + t[..., n:, :].float()
 
     def device_status(self, stream=None):
         B.dd_device_status(self.ctx, _stream(stream))

@@ -163,8 +163,11 @@ const char* dd_last_error(void);
 /* ------------------------------------------------------ step probes (tests) */
 
 /* Optional device outputs of one step, for parity checks.  Any pointer may be
- * NULL.  attn_out: bf16 [L][B*S][Hq*D], the attention output of every layer
- * (before the O projection); hidden: bf16 [B*S][H], the final RMSNorm output;
+ * NULL.  Activations are kept as a bf16 head plus a bf16 remainder (their sum
+ * carries the fp32 value to ~2^-17), so the two bf16 outputs hold heads in
+ * rows [0, B*S) and remainders in rows [B*S, 2*B*S).
+ * attn_out: bf16 [L][2*B*S][Hq*D], the attention output of every layer
+ * (before the O projection); hidden: bf16 [2*B*S][H], the final RMSNorm output;
  * logits: fp32 [B*S][V], computed by the same tensor-core LM-head mainloop with
  * a plain store instead of the fused select; conf: fp32 [B*S]; arg: int32 [B*S]. */
 typedef struct dd_probe {

@@ -30,11 +30,12 @@ design notes):
   ties); mock-AR commits the leftmost masked position;
 * RMSNorm eps = 1e-5, gains from the weights (ones in the synthetic set),
   silu(x) = x / (1 + exp(-x));
-* activations are stored in bf16 where a bf16 model stores them -- the
-  normalised GEMM inputs, q/k/v, the attention output and the SwiGLU
-  product -- when `act_bf16` is true (the default); the residual stream,
-  scores, softmax and logits stay fp32.  `act_bf16=False` keeps every
-  activation in fp32.
+* weights and context K/V are bf16 values; every activation is fp32 (the
+  default).  `act_bf16=True` instead stores the normalised GEMM inputs,
+  q/k/v, the attention output and the SwiGLU product in bf16 the way a bf16
+  model would; it exists to measure how far bf16 storage alone moves the
+  result (several tenths of a logit after a few layers, because rounding
+  flips compound), which is why the fp32 reading is the reference.
 """
 from __future__ import annotations
 
@@ -218,7 +219,7 @@ class StepResult:
 
 
 def denoise_step(model: OracleModel, tokens, mask, gamma: float, mode: int = MODE_THRESHOLD,
-                 act_bf16: bool = True, keep_intermediates: bool = False) -> StepResult:
+                 act_bf16: bool = False, keep_intermediates: bool = False) -> StepResult:
     """One reverse-process application over the block, then the commit rule.
 
     Explainer step 2 ("逆過程ネットワークに入力する") with the TwoTower denoiser
@@ -274,7 +275,7 @@ def denoise_step(model: OracleModel, tokens, mask, gamma: float, mode: int = MOD
 
 
 def decode_block(model: OracleModel, gamma: float, mode: int = MODE_THRESHOLD,
-                 max_steps: int | None = None, act_bf16: bool = True):
+                 max_steps: int | None = None, act_bf16: bool = False):
     """Fill one block: start all-[MASK], step until no position is masked
     (explainer step 5).  Returns (tokens [B,S], steps, per-step commit counts)."""
     cfg = model.cfg

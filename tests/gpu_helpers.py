@@ -88,8 +88,11 @@ def compare_step(p: Problem, tok, mask, gamma, mode=0, logits=True):
     out = p.dec.probe_step(t, m, gamma, mode, logits=logits)
     torch.cuda.synchronize()
     r = oracle.denoise_step(p.model, tok, mask, gamma, mode, keep_intermediates=True)
+    from block_wise_masked_dd_b300.decoder import join_split
     for l in range(cfg.n_layers):
-        close(bf16_to_f32(out["attn_out"][l]), r.attn_out[l], TOL_ATTN, f"attention output, layer {l}", rel_rms=3e-3)
+        close(join_split(out["attn_out"][l]).cpu().numpy(), r.attn_out[l], TOL_ATTN, f"attention output, layer {l}",
+              rel_rms=1e-3)
+    close(join_split(out["hidden"]).cpu().numpy(), r.hidden_final, TOL_LOGIT, "final hidden", rel_rms=1e-3)
     if logits:
         close(out["logits"].cpu().numpy(), r.logits, TOL_LOGIT, "logits")
     close(out["conf"].cpu().numpy(), r.conf.reshape(-1), TOL_CONF, "confidence")
