@@ -104,7 +104,7 @@ struct dd_ctx {
   bool have_weights;
   dd_weights w;
   std::vector<CUtensorMap> m_wqkv, m_wo, m_wgu, m_wd;
-  CUtensorMap m_lm, m_y_b, m_attn_b, m_h_b, m_y_a, m_kc, m_vc;
+  CUtensorMap m_lm, m_y_b, m_attn_b, m_h_b, m_y_a, m_kc, m_vc, m_kc128, m_vc128;
   cudaStream_t cap_stream;
   cudaGraphExec_t exec;
   int32_t* hpin;  // pinned host: [0] remaining, [1] status
@@ -153,7 +153,7 @@ Layout make_layout(const dd_config& c) {
   const int R = c.batch * c.block;
   const int qkvw = (c.n_q_heads + 2 * c.n_kv_heads) * c.head_dim;
   const int HqD = c.n_q_heads * c.head_dim;
-  L.alloc_ctx = c.max_ctx < 64 ? 64 : c.max_ctx;
+  L.alloc_ctx = c.max_ctx < 128 ? 128 : c.max_ctx;  // at least one 128-position TMA box
   // Every activation operand of the step is split (bf16 head + remainder).
   L.p_qkv = dd::plan_gemm(dd::kEpiPartial, R, qkvw, c.hidden, 1);
   L.p_o = dd::plan_gemm(dd::kEpiPartial, R, c.hidden, HqD, 1);
@@ -279,7 +279,7 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)cf.head_dim);
     a.status = status;
     a.timeout_ns = c->timeout_ns;
-    DD_CUDA(dd::launch_attention(L.p_attn, a, c->m_kc, c->m_vc, st));
+    DD_CUDA(dd::launch_attention(L.p_attn, a, c->m_kc, c->m_vc, c->m_kc128, c->m_vc128, st));
     mk(kKAttention);
     if (L.p_attn.n_splits > 1) {
       DD_CUDA(dd::launch_attention_combine(L.p_attn, a, st));
@@ -436,6 +436,8 @@ dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_byte
   const uint64_t planes = (uint64_t)cf.n_layers * cf.batch * cf.n_kv_heads;
   bool ok = dd::make_map_3d(&c->m_kc, c->ws + L.kc, planes, L.alloc_ctx, cf.head_dim, 64) &&
             dd::make_map_3d(&c->m_vc, c->ws + L.vc, planes, L.alloc_ctx, cf.head_dim, 64) &&
+            dd::make_map_3d(&c->m_kc128, c->ws + L.kc, planes, L.alloc_ctx, cf.head_dim, 128) &&
+            dd::make_map_3d(&c->m_vc128, c->ws + L.vc, planes, L.alloc_ctx, cf.head_dim, 128) &&
             dd::make_map_2d(&c->m_y_b, c->ws + L.y, 2 * c->R, cf.hidden, L.p_qkv.BN) &&
             dd::make_map_2d(&c->m_attn_b, c->ws + L.attn, 2 * c->R, c->HqD, L.p_o.BN) &&
             dd::make_map_2d(&c->m_h_b, c->ws + L.hmid, 2 * c->R, cf.mlp, L.p_d.BN) &&
@@ -664,7 +666,9 @@ static dd_status attn_check(const dd_attn_problem* p) {
 }
 
 static size_t attn_ws_bytes(const dd_attn_problem* p, dd::AttnPlan* plan) {
-  *plan = dd::plan_attention(p->batch, p->block, p->n_q_heads, p->n_kv_heads, p->head_dim, p->ctx_len);
+  // the tcgen05 path streams 128-position boxes: it needs ctx_stride >= 128
+  *plan = dd::plan_attention(p->batch, p->block, p->n_q_heads, p->n_kv_heads, p->head_dim, p->ctx_len,
+                             p->ctx_stride >= 128);
   return 256 + dd::attention_partial_bytes(*plan, p->batch, p->n_kv_heads);
 }
 
@@ -689,10 +693,12 @@ dd_status dd_block_attention(const dd_attn_problem* p, void* stream) {
   DD_CUDA(dd::prepare_kernels());
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = static_cast<uint8_t*>(p->workspace);
-  CUtensorMap mk, mv;
+  CUtensorMap mk, mv, mk128, mv128;
   const uint64_t planes = (uint64_t)p->batch * p->n_kv_heads;
   if (!dd::make_map_3d(&mk, p->k_ctx, planes, p->ctx_stride, p->head_dim, 64) ||
-      !dd::make_map_3d(&mv, p->v_ctx, planes, p->ctx_stride, p->head_dim, 64))
+      !dd::make_map_3d(&mv, p->v_ctx, planes, p->ctx_stride, p->head_dim, 64) ||
+      !dd::make_map_3d(&mk128, p->k_ctx, planes, p->ctx_stride, p->head_dim, 128) ||
+      !dd::make_map_3d(&mv128, p->v_ctx, planes, p->ctx_stride, p->head_dim, 128))
     return fail(DD_ERR_CUDA, "tensor map encoding failed for k_ctx/v_ctx");
   int* small = reinterpret_cast<int*>(ws);  // [0] ctx_len, [1] status
   DD_CUDA(dd::launch_set_int(small, p->ctx_len, st));
@@ -714,7 +720,7 @@ dd_status dd_block_attention(const dd_attn_problem* p, void* stream) {
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)p->head_dim);
   a.status = small + 1;
   a.timeout_ns = dd::kDefaultTimeoutNs;
-  DD_CUDA(dd::launch_attention(plan, a, mk, mv, st));
+  DD_CUDA(dd::launch_attention(plan, a, mk, mv, mk128, mv128, st));
   DD_CUDA(dd::launch_attention_combine(plan, a, st));
   return DD_OK;
 }

@@ -175,7 +175,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_block_attn(const __grid_
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = warp_id(), lane = lane_id();
-  const int T = *a.ctx_len;
+  const int T = a.block_only ? 0 : *a.ctx_len;
   const int ntiles = (T + kKT - 1) / kKT;
   const int per = (ntiles + n_splits - 1) / n_splits;
   const int tile0 = split * per;
@@ -361,9 +361,9 @@ __global__ void k_attn_combine(const AttnArgs a, int n_splits) {
 }
 
 template <int D, bool SPLIT>
-void launch_attn_kernel(const AttnPlan& p, const AttnArgs& a, const CUtensorMap& mk, const CUtensorMap& mv,
-                        cudaStream_t st) {
-  dim3 grid(p.n_splits, a.Hkv, a.B);
+void launch_attn_kernel(const AttnPlan& p, const AttnArgs& a, int grid_x, const CUtensorMap& mk,
+                        const CUtensorMap& mv, cudaStream_t st) {
+  dim3 grid(grid_x, a.Hkv, a.B);
   const int threads = (p.warps_c + 1) * 32;
   if (p.warps_c <= 4)
     k_block_attn<D, SPLIT, 4><<<grid, threads, attn_smem_bytes<D, SPLIT>(), st>>>(mk, mv, a, p.n_splits, p.warps_c);
@@ -373,13 +373,19 @@ void launch_attn_kernel(const AttnPlan& p, const AttnArgs& a, const CUtensorMap&
 
 }  // namespace
 
-AttnPlan plan_attention(int B, int S, int Hq, int Hkv, int D, int max_ctx) {
+AttnPlan plan_attention(int B, int S, int Hq, int Hkv, int D, int max_ctx, int allow_tc) {
   AttnPlan p{};
   p.D = D;
   p.rows = (Hq / Hkv) * S;
   p.warps_c = p.rows / 16;
   p.stages = D == 128 ? attn_stages<128>() : attn_stages<64>();
   p.smem_bytes = D == 128 ? attn_smem_bytes<128, true>() : attn_smem_bytes<64, true>();
+  if (allow_tc && attention_tc_supported(D, p.rows) && max_ctx > 0) {
+    p.use_tc = 1;
+    p.n_ctx = attention_tc_splits(B, Hkv, max_ctx);
+    p.n_splits = p.n_ctx + 1;
+    return p;
+  }
   const int pairs = B * Hkv;
   const int ntiles = (max_ctx + kKT - 1) / kKT;
   // Enough CTAs for ~4 resident waves (2 CTAs per SM), at least 4 tiles per split.
@@ -397,16 +403,26 @@ size_t attention_partial_bytes(const AttnPlan& p, int B, int Hkv) {
   return n * p.D * sizeof(float) + n * sizeof(float2) + 256;
 }
 
-cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a, const CUtensorMap& map_k, const CUtensorMap& map_v,
-                             cudaStream_t st) {
-  if (p.D == 128) {
-    if (a.split) launch_attn_kernel<128, true>(p, a, map_k, map_v, st);
-    else launch_attn_kernel<128, false>(p, a, map_k, map_v, st);
-  } else {
-    if (a.split) launch_attn_kernel<64, true>(p, a, map_k, map_v, st);
-    else launch_attn_kernel<64, false>(p, a, map_k, map_v, st);
+cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a_in, const CUtensorMap& map_k, const CUtensorMap& map_v,
+                             const CUtensorMap& map_k128, const CUtensorMap& map_v128, cudaStream_t st) {
+  AttnArgs a = a_in;
+  int grid_x = p.n_splits;
+  if (p.use_tc) {
+    // block keys -> partial slot 0 (one CTA per (sequence, kv head))
+    a.block_only = 1;
+    grid_x = 1;
   }
-  return cudaGetLastError();
+  if (p.D == 128) {
+    if (a.split) launch_attn_kernel<128, true>(p, a, grid_x, map_k, map_v, st);
+    else launch_attn_kernel<128, false>(p, a, grid_x, map_k, map_v, st);
+  } else {
+    if (a.split) launch_attn_kernel<64, true>(p, a, grid_x, map_k, map_v, st);
+    else launch_attn_kernel<64, false>(p, a, grid_x, map_k, map_v, st);
+  }
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess || !p.use_tc) return e;
+  a.block_only = 0;
+  return launch_attention_tc(a, p.n_ctx, p.n_splits, map_k128, map_v128, st);
 }
 
 cudaError_t launch_attention_combine(const AttnPlan& p, const AttnArgs& a, cudaStream_t st) {

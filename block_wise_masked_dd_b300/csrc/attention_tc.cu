@@ -1,0 +1,438 @@
+// Context part of the block attention on the tcgen05 tensor cores (head dim
+// 128, 64 query rows per (sequence, kv head)).  The block keys are handled by
+// the mma.sync kernel as one more partial, and the combine kernel merges all
+// partials (TwoTower article, "技術/ビジネス面": one softmax over the context
+// and the block).
+//
+// Per 128-key tile:
+//   S[64 q][128 keys] = Q[64][128] . K_tile[128][128]^T     (M=64, K-major A and B)
+//   O[64 q][128 d]    = P[64][128 keys] . V_tile[128][128]    (M=64, K-major A, MN-major B)
+// With M = 64 the accumulator rows 16w..16w+15 live in TMEM lanes 32w..32w+15,
+// and the 16x256b load shape hands them to warp w in the m16n8 fragment
+// layout (row = 16w + lane/4 (+8), column = 8*rep + 2*(lane%4) (+1)).  So each
+// softmax warp owns 16 query rows: row maxima and sums are in-thread plus two
+// quad shuffles, and P (a bf16 head and a bf16 remainder) goes to shared
+// memory with stmatrix in the swizzled K-major layout the PV MMA reads.
+// Each tile's O lands in a fresh TMEM buffer and is folded into registers
+// with the running rescale.
+//
+// Roles (192 threads): warp 0 streams K and V tiles with TMA (two slots each;
+// K released after QK^T, V after PV), warp 1 owns TMEM and issues the MMAs,
+// warps 2-5 run the softmax and fold the outputs.  Every mbarrier wait is
+// bounded.
+#include <math.h>
+
+#include "kernels.h"
+#include "ptx.cuh"
+
+namespace dd {
+
+namespace {
+
+constexpr int kKT = 128;                 // keys per tile (MMA N of QK^T, K of PV)
+constexpr int kNQ = 64;                  // query rows (MMA M)
+constexpr int kD = 128;                  // head dim
+constexpr int kBox = kKT * 128;          // one [128 keys][64 d] TMA box: 16 KB
+constexpr int kKV = 2 * kBox;            // K or V tile: 32 KB
+constexpr int kRowBox = kNQ * 128;       // one [64 rows][64 cols] box: 8 KB
+constexpr int kQ = 2 * kRowBox;          // Q head or remainder: 16 KB
+constexpr int kP = 2 * kRowBox;          // P head or remainder [64][128 keys]: 16 KB
+constexpr int kThreads = 192;
+constexpr int kOffK = 0;                 // 2 K slots
+constexpr int kOffV = 2 * kKV;           // 2 V slots
+constexpr int kOffQh = 4 * kKV;
+constexpr int kOffQl = kOffQh + kQ;
+constexpr int kOffPh = kOffQl + kQ;
+constexpr int kOffPl = kOffPh + kP;
+constexpr int kOffBar = kOffPl + kP;
+constexpr int kNumBars = 19;
+constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 16;
+constexpr uint32_t kTmemCols = 512;      // S x2 (128 cols each), O x2 (128 cols each)
+
+__device__ __forceinline__ uint64_t desc_sw128(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Offset of element (row, col) of a [rows][...] tile stored as 64-column
+// boxes of `rows` x 128 bytes with the 128-byte swizzle.
+__device__ __forceinline__ uint32_t swz(int rows, int r, int col) {
+  return (col >> 6) * rows * 128 + r * 128 + ((((col & 63) >> 3) ^ (r & 7)) << 4) + (col & 7) * 2;
+}
+
+// 64 fp32 values of this warp's 16 accumulator rows (M = 64 layout), columns
+// [col, col + 128): register i holds row lane/4 + 8*((i%4)/2), column
+// 8*(i/4) + 2*(lane%4) + (i%2).
+__device__ __forceinline__ void tmem_ld_frag(uint32_t taddr, float (&v)[64]) {
+  uint32_t r[64];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,"
+      "%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63}, [%64];\n\t"
+      "tcgen05.wait::ld.sync.aligned;"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]), "=r"(r[8]),
+        "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]), "=r"(r[16]),
+        "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]),
+        "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31]), "=r"(r[32]),
+        "=r"(r[33]), "=r"(r[34]), "=r"(r[35]), "=r"(r[36]), "=r"(r[37]), "=r"(r[38]), "=r"(r[39]), "=r"(r[40]),
+        "=r"(r[41]), "=r"(r[42]), "=r"(r[43]), "=r"(r[44]), "=r"(r[45]), "=r"(r[46]), "=r"(r[47]), "=r"(r[48]),
+        "=r"(r[49]), "=r"(r[50]), "=r"(r[51]), "=r"(r[52]), "=r"(r[53]), "=r"(r[54]), "=r"(r[55]), "=r"(r[56]),
+        "=r"(r[57]), "=r"(r[58]), "=r"(r[59]), "=r"(r[60]), "=r"(r[61]), "=r"(r[62]), "=r"(r[63])
+      : "r"(taddr)
+      : "memory");
+#pragma unroll
+  for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void stmatrix_x4(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(r0), "r"(r1),
+               "r"(r2), "r"(r3)
+               : "memory");
+}
+
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool SPLITQ>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attn_ctx_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                  const AttnArgs a, int n_ctx_splits, int n_slots) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* kfull = bars + 0;
+  uint64_t* kempty = bars + 2;
+  uint64_t* vfull = bars + 4;
+  uint64_t* vempty = bars + 6;
+  uint64_t* sfull = bars + 8;
+  uint64_t* sfree = bars + 10;
+  uint64_t* pfull = bars + 12;
+  uint64_t* pfree = bars + 13;
+  uint64_t* ofull = bars + 14;
+  uint64_t* ofree = bars + 16;
+  uint64_t* drain = bars + 18;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int warp = warp_id(), lane = lane_id();
+  const int T = *a.ctx_len;
+  const int ntiles_all = (T + kKT - 1) / kKT;
+  const int per = (ntiles_all + n_ctx_splits - 1) / n_ctx_splits;
+  const int tile0 = split * per;
+  const int nt = max(0, min(ntiles_all, tile0 + per) - tile0);
+  // Each CTA walks its tiles starting at a rotated position: CTAs that run
+  // side by side otherwise stream addresses at the same offset inside
+  // equally aligned planes, in lockstep, which concentrates traffic on a few
+  // memory channels (measured: 2.3 TB/s instead of ~5.5 TB/s).  The softmax
+  // is independent of the order in which tiles are visited.
+  const int rot = nt > 0 ? (int)(((unsigned)(b * a.Hkv + kvh) * 2654435761u + split * 40503u) % (unsigned)nt) : 0;
+  const int z = a.z0 + b * a.Hkv + kvh;
+  const int R = a.B * a.S;
+  const __nv_bfloat16* qkv = reinterpret_cast<const __nv_bfloat16*>(a.qkv);
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&kempty[i], 1);
+      mbar_init(&vfull[i], 1);
+      mbar_init(&vempty[i], 1);
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sfree[i], 4);
+      mbar_init(&ofull[i], 1);
+      mbar_init(&ofree[i], 4);
+    }
+    mbar_init(pfull, 4);
+    mbar_init(pfree, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  // Stage Q (64 rows: row r = (g, i) -> query head kvh*G + g, position i) as
+  // a K-major swizzled operand; with SPLITQ also the remainder rows.
+  for (int c = threadIdx.x; c < (SPLITQ ? 2 : 1) * kNQ * (kD / 8); c += blockDim.x) {
+    const int half = c / (kNQ * (kD / 8));
+    const int cc = c % (kNQ * (kD / 8));
+    const int r = cc / (kD / 8), col = (cc % (kD / 8)) * 8;
+    const int g = r / a.S, i = r % a.S;
+    const long long row = (long long)(half ? R : 0) + b * a.S + i;
+    const uint4 v = *reinterpret_cast<const uint4*>(qkv + row * a.ld_qkv + (kvh * a.G + g) * kD + col);
+    *reinterpret_cast<uint4*>(smem + (half ? kOffQl : kOffQh) + swz(kNQ, r, col)) = v;
+  }
+  fence_proxy_async_smem();
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_s = tmem;             // S buffers at columns 0 and 128
+  const uint32_t t_o = tmem + 256;       // O buffers at columns 256 and 384
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      for (int t = 0; t < nt; ++t) {
+        const int s = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        const int key0 = (tile0 + (t + rot) % nt) * kKT;
+        if (!mbar_wait_bounded(&kempty[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) break;
+        mbar_arrive_expect_tx(&kfull[s], kKV);
+        tma_load_3d(smem + kOffK + s * kKV, &map_k, &kfull[s], 0, key0, z);
+        tma_load_3d(smem + kOffK + s * kKV + kBox, &map_k, &kfull[s], 64, key0, z);
+        if (!mbar_wait_bounded(&vempty[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) break;
+        mbar_arrive_expect_tx(&vfull[s], kKV);
+        tma_load_3d(smem + kOffV + s * kKV, &map_v, &vfull[s], 0, key0, z);
+        tma_load_3d(smem + kOffV + s * kKV + kBox, &map_v, &vfull[s], 64, key0, z);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_bf16_f32(kNQ, kKT);
+      const uint32_t idesc_pv = idesc_bf16_f32(kNQ, kD) | (1u << 16);  // B (V) MN-major
+      const uint32_t qh = smem_u32(smem + kOffQh), ql = smem_u32(smem + kOffQl);
+      const uint32_t p_h = smem_u32(smem + kOffPh), p_l = smem_u32(smem + kOffPl);
+      bool ok = true;
+      auto issue_pv = [&](int u) {
+        const int s = u & 1;
+        const uint32_t ph = (u >> 1) & 1;
+        if (!mbar_wait_bounded(&vfull[s], ph, a.timeout_ns, abort_flag, a.status)) return false;
+        if (!mbar_wait_bounded(pfull, u & 1, a.timeout_ns, abort_flag, a.status)) return false;
+        if (!mbar_wait_bounded(&ofree[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) return false;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(smem + kOffV + s * kKV);
+#pragma unroll
+        for (int j = 0; j < kKT / 16; ++j) {
+          const uint32_t aoff = (j >> 2) * kRowBox + (j & 3) * 32;
+          tc_mma_bf16(t_o + s * kD, desc_sw128(p_h + aoff, 0, 1024), desc_sw128(vb + j * 2048, kBox, 1024), idesc_pv,
+                      j > 0 ? 1u : 0u);
+        }
+#pragma unroll
+        for (int j = 0; j < kKT / 16; ++j) {
+          const uint32_t aoff = (j >> 2) * kRowBox + (j & 3) * 32;
+          tc_mma_bf16(t_o + s * kD, desc_sw128(p_l + aoff, 0, 1024), desc_sw128(vb + j * 2048, kBox, 1024), idesc_pv,
+                      1u);
+        }
+        tc_commit(&ofull[s]);
+        tc_commit(&vempty[s]);
+        tc_commit(pfree);
+        return true;
+      };
+      for (int t = 0; t < nt && ok; ++t) {
+        const int s = t & 1;
+        const uint32_t ph = (t >> 1) & 1;
+        if (!mbar_wait_bounded(&kfull[s], ph, a.timeout_ns, abort_flag, a.status)) { ok = false; break; }
+        if (!mbar_wait_bounded(&sfree[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t kb = smem_u32(smem + kOffK + s * kKV);
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk & 3) * 32;
+          tc_mma_bf16(t_s + s * kKT, desc_sw128(qh + (kk >> 2) * kRowBox + off, 0, 1024),
+                      desc_sw128(kb + (kk >> 2) * kBox + off, 0, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+        }
+        if (SPLITQ) {
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = (kk & 3) * 32;
+            tc_mma_bf16(t_s + s * kKT, desc_sw128(ql + (kk >> 2) * kRowBox + off, 0, 1024),
+                        desc_sw128(kb + (kk >> 2) * kBox + off, 0, 1024), idesc_qk, 1u);
+          }
+        }
+        tc_commit(&sfull[s]);
+        tc_commit(&kempty[s]);
+        if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
+      }
+      if (ok && nt >= 1) issue_pv(nt - 1);
+      tc_commit(drain);
+      volatile int no_abort = 0;
+      mbar_wait_bounded(drain, 0, a.timeout_ns, &no_abort, a.status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int q4 = warp & 3;                        // TMEM lane quarter -> rows 16*q4 .. 16*q4+15
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const int r0 = 16 * q4 + (lane >> 2);           // the two rows this thread holds
+    const int r1 = r0 + 8;
+    const int cq = 2 * (lane & 3);                  // column offset inside each 8-column block
+    const float c = a.scale_log2;
+    float o[64];                                    // O rows r0/r1 in fragment order
+#pragma unroll
+    for (int j = 0; j < 64; ++j) o[j] = 0.f;
+    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+    float al0 = 0.f, al1 = 0.f;                     // rescale of the previous tile
+    // stmatrix row address of this lane: matrix mi = lane/8 covers rows
+    // 16*q4 + 8*(mi&1) + lane%8 and columns +8*(mi>>1) of each 16-key group
+    const int st_row = 16 * q4 + 8 * ((lane >> 3) & 1) + (lane & 7);
+    const int st_colh = 8 * (lane >> 4);
+    bool ok = true;
+    auto consume_o = [&](int u, float a0, float a1) {
+      const int s = u & 1;
+      bool w = true;
+      if (lane == 0) w = mbar_wait_bounded(&ofull[s], (u >> 1) & 1, a.timeout_ns, abort_flag, a.status);
+      w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      if (!w) return false;
+      tc_fence_after();
+      float pv[64];
+      tmem_ld_frag(t_o + s * kD + lane_off, pv);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&ofree[s]);
+#pragma unroll
+      for (int j = 0; j < 64; ++j) o[j] = fmaf(o[j], (j & 2) ? a1 : a0, pv[j]);
+      return true;
+    };
+    for (int t = 0; t < nt; ++t) {
+      const int s = t & 1;
+      bool w = true;
+      if (lane == 0) w = mbar_wait_bounded(&sfull[s], (t >> 1) & 1, a.timeout_ns, abort_flag, a.status);
+      w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
+      if (!w) { ok = false; break; }
+      tc_fence_after();
+      float v[64];
+      tmem_ld_frag(t_s + s * kKT + lane_off, v);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sfree[s]);
+      const int kbase = (tile0 + (t + rot) % nt) * kKT;
+      if (kbase + kKT > T) {  // tail tile: keys >= T do not exist
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          const int key = kbase + 8 * (j >> 2) + cq + (j & 1);
+          if (key >= T) v[j] = -INFINITY;
+        }
+      }
+      float mx0 = -INFINITY, mx1 = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) {
+        mx0 = fmaxf(mx0, fmaxf(v[j], v[j + 1]));
+        mx1 = fmaxf(mx1, fmaxf(v[j + 2], v[j + 3]));
+      }
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+      // running max in base-2 units (scores times c)
+      const float mn0 = fmaxf(m0, mx0 * c), mn1 = fmaxf(m1, mx1 * c);
+      const float a0 = m0 == -INFINITY ? 0.f : ex2(m0 - mn0);
+      const float a1 = m1 == -INFINITY ? 0.f : ex2(m1 - mn1);
+      m0 = mn0;
+      m1 = mn1;
+      float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) {
+        v[j] = ex2(fmaf(v[j], c, -mn0));
+        v[j + 1] = ex2(fmaf(v[j + 1], c, -mn0));
+        v[j + 2] = ex2(fmaf(v[j + 2], c, -mn1));
+        v[j + 3] = ex2(fmaf(v[j + 3], c, -mn1));
+        s0 += v[j] + v[j + 1];
+        s1 += v[j + 2] + v[j + 3];
+      }
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+      s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+      s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+      l0 = l0 * a0 + s0;
+      l1 = l1 * a1 + s1;
+      // P (head, remainder) -> shared memory, once PV of the previous tile is done
+      if (t >= 1) {
+        bool pw = true;
+        if (lane == 0) pw = mbar_wait_bounded(pfree, (t - 1) & 1, a.timeout_ns, abort_flag, a.status);
+        pw = __shfl_sync(0xffffffffu, pw ? 1 : 0, 0) != 0;
+        if (!pw) { ok = false; break; }
+      }
+#pragma unroll
+      for (int g = 0; g < kKT / 16; ++g) {
+        // 16-key group g: fragment reps 2g (keys 16g..16g+7) and 2g+1 (16g+8..)
+        uint32_t h0, l0p, h1, l1p, h2, l2p, h3, l3p;
+        split_bf16(v[8 * g + 0], v[8 * g + 1], h0, l0p);   // rows 0-7,  keys 16g + cq
+        split_bf16(v[8 * g + 2], v[8 * g + 3], h1, l1p);   // rows 8-15, keys 16g + cq
+        split_bf16(v[8 * g + 4], v[8 * g + 5], h2, l2p);   // rows 0-7,  keys 16g + 8 + cq
+        split_bf16(v[8 * g + 6], v[8 * g + 7], h3, l3p);   // rows 8-15, keys 16g + 8 + cq
+        const uint32_t off = swz(kNQ, st_row, 16 * g + st_colh);
+        stmatrix_x4(smem_u32(smem + kOffPh) + off, h0, h1, h2, h3);
+        stmatrix_x4(smem_u32(smem + kOffPl) + off, l0p, l1p, l2p, l3p);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(pfull);
+      if (t >= 1 && !consume_o(t - 1, al0, al1)) { ok = false; break; }
+      al0 = a0;
+      al1 = a1;
+    }
+    if (ok && nt >= 1) ok = consume_o(nt - 1, al0, al1);
+    // partial slot 1 + split: o (unnormalised, [q][d]), (m, l) per q
+    const long long prow = ((long long)(b * a.Hkv + kvh) * n_slots + 1 + split) * kNQ;
+#pragma unroll
+    for (int rep = 0; rep < 16; ++rep) {
+      const int d = 8 * rep + cq;
+      *reinterpret_cast<float2*>(a.part_o + (prow + r0) * kD + d) = make_float2(o[4 * rep], o[4 * rep + 1]);
+      *reinterpret_cast<float2*>(a.part_o + (prow + r1) * kD + d) = make_float2(o[4 * rep + 2], o[4 * rep + 3]);
+    }
+    if ((lane & 3) == 0) {
+      a.part_ml[prow + r0] = make_float2(m0, l0);
+      a.part_ml[prow + r1] = make_float2(m1, l1);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace
+
+bool attention_tc_supported(int D, int rows) { return D == kD && rows == kNQ; }
+
+int attention_tc_splits(int B, int Hkv, int max_ctx) {
+  const int pairs = B * Hkv;
+  const int ntiles = (max_ctx + kKT - 1) / kKT;
+  if (ntiles <= 0) return 1;
+  // One CTA per SM; a CTA costs its tiles plus a fixed start-up/drain of
+  // about 5 tiles (Q staging, TMEM allocation, pipeline fill, partial
+  // write), measured from the time of 1..8 splits on the 64 x 8 x 8192 case.
+  constexpr int kFixedTiles = 5;
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= 32 && s <= ntiles; ++s) {
+    const long long waves = ((long long)pairs * s + kNumSMs - 1) / kNumSMs;
+    const long long cost = waves * ((ntiles + s - 1) / s + kFixedTiles) * 64 + s;
+    if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = s; }
+  }
+  return best;
+}
+
+int attention_tc_smem_bytes() { return kSmemBytes; }
+
+cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx_splits, int n_slots, const CUtensorMap& map_k128,
+                                const CUtensorMap& map_v128, cudaStream_t st) {
+  dim3 grid(n_ctx_splits, a.Hkv, a.B);
+  if (a.split)
+    k_attn_ctx_tc<true><<<grid, kThreads, kSmemBytes, st>>>(map_k128, map_v128, a, n_ctx_splits, n_slots);
+  else
+    k_attn_ctx_tc<false><<<grid, kThreads, kSmemBytes, st>>>(map_k128, map_v128, a, n_ctx_splits, n_slots);
+  return cudaGetLastError();
+}
+
+cudaError_t prepare_attention_tc_kernels() {
+  cudaError_t e = cudaFuncSetAttribute(k_attn_ctx_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(k_attn_ctx_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  return e;
+}
+
+}  // namespace dd

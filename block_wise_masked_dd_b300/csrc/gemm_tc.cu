@@ -361,6 +361,7 @@ cudaError_t prepare_kernels() {
   if (done == cudaSuccess) return done;
   cudaError_t e = prepare_gemm_kernels();
   if (e == cudaSuccess) e = prepare_attention_kernels();
+  if (e == cudaSuccess) e = prepare_attention_tc_kernels();
   done = e;
   return e;
 }

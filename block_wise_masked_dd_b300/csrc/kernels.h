@@ -54,12 +54,17 @@ cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUten
 
 struct AttnPlan {
   int D, rows, warps_c, n_splits, stages, smem_bytes;
+  // tcgen05 context path (D = 128, 64 query rows): partial slot 0 holds the
+  // block keys (mma.sync kernel), slots 1..n_ctx the context splits;
+  // n_splits = n_ctx + 1 partial slots in total.
+  int use_tc, n_ctx;
 };
 
 struct AttnArgs {
   const void* qkv;     // bf16 [B*S][ld_qkv] (with split: [2*B*S][ld_qkv], heads then remainders)
   int ld_qkv;
   int split;           // q and block k/v carry bf16 remainders; the output is written as head + remainder
+  int block_only;      // attend to the block keys only (context handled elsewhere), write partial slot 0
   int B, S, Hq, Hkv, G;
   const int* ctx_len;  // device int (context length)
   int z0;              // tensor-map z offset of (b=0, kvh=0) for this layer
@@ -72,10 +77,19 @@ struct AttnArgs {
   uint64_t timeout_ns;
 };
 
-AttnPlan plan_attention(int B, int S, int Hq, int Hkv, int D, int max_ctx);
+AttnPlan plan_attention(int B, int S, int Hq, int Hkv, int D, int max_ctx, int allow_tc = 1);
 size_t attention_partial_bytes(const AttnPlan& p, int B, int Hkv);
+// map_k/map_v: context cache maps with 64-row boxes; map_k128/map_v128: the
+// same caches with 128-row boxes (tcgen05 path).
 cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a, const CUtensorMap& map_k, const CUtensorMap& map_v,
-                             cudaStream_t st);
+                             const CUtensorMap& map_k128, const CUtensorMap& map_v128, cudaStream_t st);
+// tcgen05 context attention (attention_tc.cu)
+bool attention_tc_supported(int D, int rows);
+int attention_tc_splits(int B, int Hkv, int max_ctx);
+int attention_tc_smem_bytes();
+cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx_splits, int n_slots, const CUtensorMap& map_k128,
+                                const CUtensorMap& map_v128, cudaStream_t st);
+cudaError_t prepare_attention_tc_kernels();
 // Merge the split partials (no-op with one split).
 cudaError_t launch_attention_combine(const AttnPlan& p, const AttnArgs& a, cudaStream_t st);
 
