@@ -136,6 +136,8 @@ dd_status check_config(const dd_config* c) {
                 G * c->block);
   if (c->hidden < 128 || c->hidden % 128)
     return fail(DD_ERR_UNSUPPORTED, "hidden must be a multiple of 128 (got %d)", c->hidden);
+  if (c->hidden > 4096 || (c->hidden > 2048 && c->hidden % 2048))
+    return fail(DD_ERR_UNSUPPORTED, "hidden must be <= 2048, or 4096 (got %d)", c->hidden);
   if (c->mlp < 128 || c->mlp % 128) return fail(DD_ERR_UNSUPPORTED, "mlp must be a multiple of 128 (got %d)", c->mlp);
   if (((c->n_q_heads + 2 * c->n_kv_heads) * c->head_dim) % 128)
     return fail(DD_ERR_UNSUPPORTED, "(n_q_heads+2*n_kv_heads)*head_dim must be a multiple of 128");

@@ -175,6 +175,8 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_block_attn(const __grid_
 
   const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = warp_id(), lane = lane_id();
+  pdl_wait();  // q|k|v come from the preceding kernel
+  pdl_launch_dependents();
   const int T = a.block_only ? 0 : *a.ctx_len;
   const int ntiles = (T + kKT - 1) / kKT;
   const int per = (ntiles + n_splits - 1) / n_splits;
@@ -195,19 +197,37 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_block_attn(const __grid_
   if (split == 0) {
     // Stage the block keys/values of this kv head (rows >= S zero-filled):
     // tiles k, v, and with SPLIT k_lo, v_lo.
+    // Loads are issued in batches of 8 per thread before their stores, so
+    // their latencies overlap.
     const int chunks = kKTB * (D / 8);
     const int ntile = SPLIT ? 4 : 2;
-    for (int c = threadIdx.x; c < ntile * chunks; c += blockDim.x) {
-      const int which = c / chunks;  // 0 = k, 1 = v, 2 = k_lo, 3 = v_lo
-      const int cc = c % chunks;
-      const int r = cc / (D / 8), col = (cc % (D / 8)) * 8;
-      uint4 val = make_uint4(0, 0, 0, 0);
-      if (r < a.S) {
-        const long long row = (long long)(which >= 2 ? R : 0) + b * a.S + r;
-        const long long off = row * a.ld_qkv + (a.Hq + (which & 1) * a.Hkv + kvh) * D + col;
-        val = *reinterpret_cast<const uint4*>(qkv + off);
+    for (int c0 = 0; c0 < ntile * chunks; c0 += 8 * blockDim.x) {
+      uint4 val[8];
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int c = c0 + threadIdx.x + j * blockDim.x;
+        val[j] = make_uint4(0, 0, 0, 0);
+        if (c < ntile * chunks) {
+          const int which = c / chunks;  // 0 = k, 1 = v, 2 = k_lo, 3 = v_lo
+          const int cc = c % chunks;
+          const int r = cc / (D / 8), col = (cc % (D / 8)) * 8;
+          if (r < a.S) {
+            const long long row = (long long)(which >= 2 ? R : 0) + b * a.S + r;
+            const long long off = row * a.ld_qkv + (a.Hq + (which & 1) * a.Hkv + kvh) * D + col;
+            val[j] = *reinterpret_cast<const uint4*>(qkv + off);
+          }
+        }
       }
-      *reinterpret_cast<uint4*>(blk + which * kBlkB + swz_off(kKTB, r, col)) = val;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const int c = c0 + threadIdx.x + j * blockDim.x;
+        if (c < ntile * chunks) {
+          const int which = c / chunks;
+          const int cc = c % chunks;
+          const int r = cc / (D / 8), col = (cc % (D / 8)) * 8;
+          *reinterpret_cast<uint4*>(blk + which * kBlkB + swz_off(kKTB, r, col)) = val[j];
+        }
+      }
     }
   }
   __syncthreads();
@@ -324,6 +344,8 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_block_attn(const __grid_
 // One warp per (sequence, kv head, row).
 template <int D>
 __global__ void k_attn_combine(const AttnArgs a, int n_splits) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int rows = a.G * a.S;
   const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const long long total = (long long)a.B * a.Hkv * rows;
@@ -366,9 +388,11 @@ void launch_attn_kernel(const AttnPlan& p, const AttnArgs& a, int grid_x, const 
   dim3 grid(grid_x, a.Hkv, a.B);
   const int threads = (p.warps_c + 1) * 32;
   if (p.warps_c <= 4)
-    k_block_attn<D, SPLIT, 4><<<grid, threads, attn_smem_bytes<D, SPLIT>(), st>>>(mk, mv, a, p.n_splits, p.warps_c);
+    launch_k(k_block_attn<D, SPLIT, 4>, grid, threads, attn_smem_bytes<D, SPLIT>(), st, mk, mv, a, p.n_splits,
+             p.warps_c);
   else
-    k_block_attn<D, SPLIT, 8><<<grid, threads, attn_smem_bytes<D, SPLIT>(), st>>>(mk, mv, a, p.n_splits, p.warps_c);
+    launch_k(k_block_attn<D, SPLIT, 8>, grid, threads, attn_smem_bytes<D, SPLIT>(), st, mk, mv, a, p.n_splits,
+             p.warps_c);
 }
 
 }  // namespace
@@ -429,8 +453,8 @@ cudaError_t launch_attention_combine(const AttnPlan& p, const AttnArgs& a, cudaS
   if (p.n_splits == 1) return cudaSuccess;
   const long long warps = (long long)a.B * a.Hkv * p.rows;
   const int blocks = (int)((warps + 7) / 8);
-  if (p.D == 128) k_attn_combine<128><<<blocks, 256, 0, st>>>(a, p.n_splits);
-  else k_attn_combine<64><<<blocks, 256, 0, st>>>(a, p.n_splits);
+  if (p.D == 128) return launch_k(k_attn_combine<128>, blocks, 256, 0, st, a, p.n_splits);
+  else return launch_k(k_attn_combine<64>, blocks, 256, 0, st, a, p.n_splits);
   return cudaGetLastError();
 }
 

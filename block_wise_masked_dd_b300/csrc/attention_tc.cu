@@ -129,12 +129,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int per = (ntiles_all + n_ctx_splits - 1) / n_ctx_splits;
   const int tile0 = split * per;
   const int nt = max(0, min(ntiles_all, tile0 + per) - tile0);
-  // Each CTA walks its tiles starting at a rotated position: CTAs that run
-  // side by side otherwise stream addresses at the same offset inside
-  // equally aligned planes, in lockstep, which concentrates traffic on a few
-  // memory channels (measured: 2.3 TB/s instead of ~5.5 TB/s).  The softmax
-  // is independent of the order in which tiles are visited.
-  const int rot = nt > 0 ? (int)(((unsigned)(b * a.Hkv + kvh) * 2654435761u + split * 40503u) % (unsigned)nt) : 0;
   const int z = a.z0 + b * a.Hkv + kvh;
   const int R = a.B * a.S;
   const __nv_bfloat16* qkv = reinterpret_cast<const __nv_bfloat16*>(a.qkv);
@@ -155,17 +149,50 @@ __global__ void __launch_bounds__(kThreads, 1)
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
+    // The context K/V do not depend on the preceding kernel: the first two
+    // tiles go out before waiting for it (programmatic dependent launch).
+    for (int t = 0; t < min(nt, 2); ++t) {
+      const int key0 = (tile0 + t) * kKT;
+      mbar_arrive_expect_tx(&kfull[t], kKV);
+      tma_load_3d(smem + kOffK + t * kKV, &map_k, &kfull[t], 0, key0, z);
+      tma_load_3d(smem + kOffK + t * kKV + kBox, &map_k, &kfull[t], 64, key0, z);
+      mbar_arrive_expect_tx(&vfull[t], kKV);
+      tma_load_3d(smem + kOffV + t * kKV, &map_v, &vfull[t], 0, key0, z);
+      tma_load_3d(smem + kOffV + t * kKV + kBox, &map_v, &vfull[t], 64, key0, z);
+    }
   }
+  pdl_wait();  // q comes from the preceding kernel
+  pdl_launch_dependents();
   // Stage Q (64 rows: row r = (g, i) -> query head kvh*G + g, position i) as
   // a K-major swizzled operand; with SPLITQ also the remainder rows.
-  for (int c = threadIdx.x; c < (SPLITQ ? 2 : 1) * kNQ * (kD / 8); c += blockDim.x) {
-    const int half = c / (kNQ * (kD / 8));
-    const int cc = c % (kNQ * (kD / 8));
-    const int r = cc / (kD / 8), col = (cc % (kD / 8)) * 8;
-    const int g = r / a.S, i = r % a.S;
-    const long long row = (long long)(half ? R : 0) + b * a.S + i;
-    const uint4 v = *reinterpret_cast<const uint4*>(qkv + row * a.ld_qkv + (kvh * a.G + g) * kD + col);
-    *reinterpret_cast<uint4*>(smem + (half ? kOffQl : kOffQh) + swz(kNQ, r, col)) = v;
+  {
+    // All of this thread's 16-byte loads are issued before any is stored, so
+    // their latencies overlap.
+    constexpr int kChunks = (SPLITQ ? 2 : 1) * kNQ * (kD / 8);
+    constexpr int kPer = (kChunks + kThreads - 1) / kThreads;
+    uint4 v[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int c = threadIdx.x + j * kThreads;
+      if (c < kChunks) {
+        const int half = c / (kNQ * (kD / 8));
+        const int cc = c % (kNQ * (kD / 8));
+        const int r = cc / (kD / 8), col = (cc % (kD / 8)) * 8;
+        const int g = r / a.S, i = r % a.S;
+        const long long row = (long long)(half ? R : 0) + b * a.S + i;
+        v[j] = *reinterpret_cast<const uint4*>(qkv + row * a.ld_qkv + (kvh * a.G + g) * kD + col);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int c = threadIdx.x + j * kThreads;
+      if (c < kChunks) {
+        const int half = c / (kNQ * (kD / 8));
+        const int cc = c % (kNQ * (kD / 8));
+        const int r = cc / (kD / 8), col = (cc % (kD / 8)) * 8;
+        *reinterpret_cast<uint4*>(smem + (half ? kOffQl : kOffQh) + swz(kNQ, r, col)) = v[j];
+      }
+    }
   }
   fence_proxy_async_smem();
   if (warp == 1) {
@@ -181,10 +208,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      for (int t = 0; t < nt; ++t) {
+      for (int t = 2; t < nt; ++t) {  // tiles 0 and 1 were issued in the prologue
         const int s = t & 1;
         const uint32_t ph = (t >> 1) & 1;
-        const int key0 = (tile0 + (t + rot) % nt) * kKT;
+        const int key0 = (tile0 + t) * kKT;
         if (!mbar_wait_bounded(&kempty[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) break;
         mbar_arrive_expect_tx(&kfull[s], kKV);
         tma_load_3d(smem + kOffK + s * kKV, &map_k, &kfull[s], 0, key0, z);
@@ -306,7 +333,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&sfree[s]);
-      const int kbase = (tile0 + (t + rot) % nt) * kKT;
+      const int kbase = (tile0 + t) * kKT;
       if (kbase + kKT > T) {  // tail tile: keys >= T do not exist
 #pragma unroll
         for (int j = 0; j < 64; ++j) {
@@ -422,10 +449,10 @@ cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx_splits, int n_slots
                                 const CUtensorMap& map_v128, cudaStream_t st) {
   dim3 grid(n_ctx_splits, a.Hkv, a.B);
   if (a.split)
-    k_attn_ctx_tc<true><<<grid, kThreads, kSmemBytes, st>>>(map_k128, map_v128, a, n_ctx_splits, n_slots);
-  else
-    k_attn_ctx_tc<false><<<grid, kThreads, kSmemBytes, st>>>(map_k128, map_v128, a, n_ctx_splits, n_slots);
-  return cudaGetLastError();
+    return launch_k(k_attn_ctx_tc<true>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, a, n_ctx_splits,
+                    n_slots);
+  return launch_k(k_attn_ctx_tc<false>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, a, n_ctx_splits,
+                  n_slots);
 }
 
 cudaError_t prepare_attention_tc_kernels() {

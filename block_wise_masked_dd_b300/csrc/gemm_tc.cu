@@ -42,7 +42,6 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct KArgs {
   int m_tiles, n_tiles, splits, kb_total, kb_per_split, BN, stages, tiles_total;
-  int split_act;   // activation operand carries a remainder half
   int split_rows;  // row offset of the remainder half in the activation map
   uint32_t tmem_half;
   GemmOut out;
@@ -57,13 +56,15 @@ __host__ __device__ inline int stage_bytes_of(int epi, int BN, int split) {
   return kStageA + b + (split ? act : 0);
 }
 
-template <int EPI>
+// SPLIT is a template parameter: a run-time test inside the MMA issue loop
+// slowed the LM head by a sixth.
+template <int EPI, int SPLIT>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, const KArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const int stage_b = args.BN * kBK * 2;
-  const int stage_bytes = stage_bytes_of(EPI, args.BN, args.split_act);
+  const int stage_bytes = stage_bytes_of(EPI, args.BN, SPLIT);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + args.stages * stage_bytes);
   uint64_t* empty = full + args.stages;
   uint64_t* acc_full = empty + args.stages;
@@ -103,9 +104,28 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // Weight tiles do not depend on the preceding kernel: the first stages'
+      // weight loads go out before waiting for it (programmatic dependent
+      // launch), the activation loads of those stages right after the wait.
+      auto load_w = [&](uint8_t* sa, int s, int kb, int mt, int nt) {
+        if (EPI == kEpiPartial) tma_load_2d(sa, &map_a, &full[s], kb * kBK, mt * kBM);
+        else tma_load_2d(sa + kStageA, &map_b, &full[s], kb * kBK, nt * args.BN);
+      };
+      auto load_x = [&](uint8_t* sa, int s, int kb, int mt, int nt) {
+        if (EPI == kEpiPartial) {
+          tma_load_2d(sa + kStageA, &map_b, &full[s], kb * kBK, nt * args.BN);
+          if (SPLIT)
+            tma_load_2d(sa + kStageA + stage_b, &map_b, &full[s], kb * kBK, args.split_rows + nt * args.BN);
+        } else {
+          tma_load_2d(sa, &map_a, &full[s], kb * kBK, mt * kBM);
+          if (SPLIT)
+            tma_load_2d(sa + kStageA + stage_b, &map_a, &full[s], kb * kBK, args.split_rows + mt * kBM);
+        }
+      };
       int s = 0;
       uint32_t phase = 0;
-      bool ok = true;
+      bool ok = true, waited = false;
+      int pend_s[8], pend_kb[8], pend_n = 0;
       for (int t = blockIdx.x; t < args.tiles_total && ok; t += gridDim.x) {
         const int split = t / per_split, r = t % per_split;
         int mt, nt;
@@ -113,20 +133,32 @@ __global__ void __launch_bounds__(kThreads, 1)
         else { mt = r % args.m_tiles; nt = r / args.m_tiles; }
         const int kb0 = split * args.kb_per_split;
         const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
-        for (int kb = kb0; kb < kb1; ++kb) {
+        const int count = kb1 - kb0;
+        for (int i = 0; i < count; ++i) {
+          const int kb = kb0 + i;
           if (!mbar_wait_bounded(&empty[s], phase ^ 1, args.timeout_ns, abort_flag, args.status)) { ok = false; break; }
           uint8_t* sa = smem + s * stage_bytes;
           mbar_arrive_expect_tx(&full[s], stage_bytes);
-          tma_load_2d(sa, &map_a, &full[s], kb * kBK, mt * kBM);
-          tma_load_2d(sa + kStageA, &map_b, &full[s], kb * kBK, nt * args.BN);
-          if (args.split_act) {
-            if (EPI == kEpiPartial)
-              tma_load_2d(sa + kStageA + stage_b, &map_b, &full[s], kb * kBK, args.split_rows + nt * args.BN);
-            else
-              tma_load_2d(sa + kStageA + stage_b, &map_a, &full[s], kb * kBK, args.split_rows + mt * kBM);
+          load_w(sa, s, kb, mt, nt);
+          if (waited) {
+            load_x(sa, s, kb, mt, nt);
+          } else {
+            pend_s[pend_n] = s;
+            pend_kb[pend_n] = kb;
+            ++pend_n;
+            if (pend_n == args.stages || pend_n == 8 || i == count - 1) {
+              pdl_wait();
+              pdl_launch_dependents();
+              waited = true;
+              for (int i = 0; i < pend_n; ++i) load_x(smem + pend_s[i] * stage_bytes, pend_s[i], pend_kb[i], mt, nt);
+            }
           }
           if (++s == args.stages) { s = 0; phase ^= 1; }
         }
+      }
+      if (!waited) {
+        pdl_wait();
+        pdl_launch_dependents();
       }
     }
     __syncwarp();
@@ -147,7 +179,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_bounded(&acc_empty[ab], aphase ^ 1, args.timeout_ns, abort_flag, args.status)) { ok = false; break; }
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + ab * args.tmem_half;
-        for (int kb = kb0; kb < kb1; ++kb) {
+        for (int kb = kb0; kb < kb1; ++kb) {  // stage order; the producer picks which K block fills it
           if (!mbar_wait_bounded(&full[s], phase, args.timeout_ns, abort_flag, args.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + s * stage_bytes);
@@ -157,7 +189,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int k = 0; k < kBK / 16; ++k) {
             tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
                         (kb > kb0 || k > 0) ? 1u : 0u);
-            if (args.split_act) {
+            if (SPLIT) {
               if (EPI == kEpiPartial)
                 tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(lo_addr + k * 32), idesc, 1u);
               else
@@ -294,24 +326,27 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act) {
 
   const int base = p.m_tiles * p.n_tiles;
   if (epi == kEpiPartial) {
-    // Split K so that the tile count fills the SMs: pick the split count that
-    // minimises (waves x K-blocks per split), preferring fewer splits.
+    // Persistent CTAs (at most one per SM) walk the tiles; split K so that
+    // the busiest SM's K blocks are few, charging each split for the fp32
+    // partial it writes and the reduce kernel reads back (in units of one
+    // K block of weights per SM).
     int best_s = 1;
-    long long best_cost = -1;
+    double best_cost = -1.0;
     const int max_s = p.kb_total < 16 ? p.kb_total : 16;
+    const double partial_kb = 0.5 * (double)rows * N * 8.0 / ((double)kNumSMs * kStageA);
     for (int s = 1; s <= max_s; ++s) {
       const int kbps = (p.kb_total + s - 1) / s;
       const int real_s = (p.kb_total + kbps - 1) / kbps;
       if (real_s != s) continue;
-      const long long ctas = (long long)base * s;
-      const long long waves = (ctas + kNumSMs - 1) / kNumSMs;
-      const long long cost = waves * kbps * 100 + s;  // tie-break: fewer splits
+      const long long tiles = (long long)base * s;
+      const long long per_sm = (tiles + kNumSMs - 1) / kNumSMs;
+      const double cost = (double)(per_sm * kbps) + partial_kb * s + 0.01 * s;
       if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_s = s; }
     }
     p.kb_per_split = (p.kb_total + best_s - 1) / best_s;
     p.splits = best_s;
     p.tiles_total = base * p.splits;
-    p.grid = p.tiles_total;
+    p.grid = p.tiles_total < kNumSMs ? p.tiles_total : kNumSMs;
   } else {
     p.splits = 1;
     p.kb_per_split = p.kb_total;
@@ -332,27 +367,28 @@ cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUten
   a.BN = p.BN;
   a.stages = p.stages;
   a.tiles_total = p.tiles_total;
-  a.split_act = p.split_act;
   a.split_rows = p.split_rows;
   a.tmem_half = p.tmem_half;
   a.out = out;
   a.status = status;
   a.timeout_ns = timeout_ns;
+  void (*k)(const CUtensorMap, const CUtensorMap, const KArgs) = nullptr;
   switch (p.epi) {
-    case kEpiPartial: k_gemm_tc<kEpiPartial><<<p.grid, kThreads, p.smem_bytes, st>>>(map_a, map_b, a); break;
-    case kEpiSelect: k_gemm_tc<kEpiSelect><<<p.grid, kThreads, p.smem_bytes, st>>>(map_a, map_b, a); break;
-    default: k_gemm_tc<kEpiStore><<<p.grid, kThreads, p.smem_bytes, st>>>(map_a, map_b, a); break;
+    case kEpiPartial: k = p.split_act ? k_gemm_tc<kEpiPartial, 1> : k_gemm_tc<kEpiPartial, 0>; break;
+    case kEpiSelect: k = p.split_act ? k_gemm_tc<kEpiSelect, 1> : k_gemm_tc<kEpiSelect, 0>; break;
+    default: k = p.split_act ? k_gemm_tc<kEpiStore, 1> : k_gemm_tc<kEpiStore, 0>; break;
   }
-  return cudaGetLastError();
+  return launch_k(k, p.grid, kThreads, p.smem_bytes, st, map_a, map_b, a);
 }
 
 cudaError_t prepare_gemm_kernels() {
   const int lim = 227 * 1024;
-  cudaError_t e = cudaFuncSetAttribute(k_gemm_tc<kEpiPartial>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_gemm_tc<kEpiSelect>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_gemm_tc<kEpiStore>, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  const void* ks[6] = {(const void*)k_gemm_tc<kEpiPartial, 0>, (const void*)k_gemm_tc<kEpiPartial, 1>,
+                       (const void*)k_gemm_tc<kEpiSelect, 0>,  (const void*)k_gemm_tc<kEpiSelect, 1>,
+                       (const void*)k_gemm_tc<kEpiStore, 0>,   (const void*)k_gemm_tc<kEpiStore, 1>};
+  cudaError_t e = cudaSuccess;
+  for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+    e = cudaFuncSetAttribute(ks[i], cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
   return e;
 }
 

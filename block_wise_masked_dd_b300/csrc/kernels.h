@@ -7,6 +7,29 @@
 
 namespace dd {
 
+// Launch `kernel` on `st`, allowing programmatic dependent launch when
+// `pdl_enabled()`: the kernel may start while its predecessor drains and must
+// call pdl_wait() before touching the predecessor's outputs (every kernel of
+// this library does).
+bool pdl_enabled();
+void set_pdl_enabled(bool on);
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                     Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 constexpr int kNumSMs = 148;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per bounded wait
 

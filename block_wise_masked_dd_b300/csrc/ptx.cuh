@@ -23,6 +23,13 @@ DD_DEV uint64_t globaltimer_ns() {
   return t;
 }
 
+// Programmatic dependent launch: wait until the preceding kernel of the
+// stream has completed and its writes are visible (a no-op when the kernel
+// was launched without the programmatic-serialization attribute), and let
+// the following kernel start its own prologue early.
+DD_DEV void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+DD_DEV void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 DD_DEV int lane_id() { return threadIdx.x & 31; }
 DD_DEV int warp_id() { return __shfl_sync(0xffffffffu, threadIdx.x >> 5, 0); }
 
@@ -103,6 +110,21 @@ DD_DEV void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, i
       "[%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
+}
+
+// Prefetch a tensor tile into L2 (no shared memory, no completion tracking).
+DD_DEV void tma_prefetch_l2_2d(const CUtensorMap* map, int c0, int c1) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1)
+               : "memory");
+}
+
+DD_DEV void tma_prefetch_l2_3d(const CUtensorMap* map, int c0, int c1, int c2) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2)
+               : "memory");
 }
 
 // ------------------------------------------------------------------ tcgen05

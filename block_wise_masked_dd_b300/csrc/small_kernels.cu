@@ -1,7 +1,8 @@
 // Bandwidth-trivial kernels of the denoising step: embedding + RMSNorm, the
 // split-K reduce epilogues of the linear layers (bf16 store, residual +
 // RMSNorm, SwiGLU), the vocab-tile merge of the LM-head select, and the
-// commit rule.
+// commit rule.  Each kernel waits for its predecessor (programmatic dependent
+// launch) before reading its outputs, then lets its successor start.
 #include <math.h>
 
 #include "kernels.h"
@@ -11,7 +12,7 @@ namespace dd {
 
 namespace {
 
-constexpr int kNormThreads = 256;
+constexpr int kMaxRowPasses = 2;  // rows up to 2 * 256 * 8 = 4096 wide
 
 __device__ __forceinline__ float block_sum(float v, float* red) {
 #pragma unroll
@@ -27,39 +28,111 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
 
 __device__ __forceinline__ float bf(const __nv_bfloat16* p, long long i) { return __bfloat162float(p[i]); }
 
-// Store v as a bf16 head at hi[0] and the bf16-rounded remainder at lo[0].
-__device__ __forceinline__ void store_split(__nv_bfloat16* hi, __nv_bfloat16* lo, float v) {
-  const __nv_bfloat16 h = __float2bfloat16_rn(v);
-  *hi = h;
-  *lo = __float2bfloat16_rn(v - __bfloat162float(h));
+// 8 bf16 (one 16-byte load) -> fp32
+__device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float (&v)[8]) {
+  const uint4 u = *reinterpret_cast<const uint4*>(p);
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    v[2 * i] = __uint_as_float(w[i] << 16);
+    v[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+  }
+}
+
+__device__ __forceinline__ void load8_f32(const float* p, float (&v)[8]) {
+  const float4 a = *reinterpret_cast<const float4*>(p);
+  const float4 b = *reinterpret_cast<const float4*>(p + 4);
+  v[0] = a.x; v[1] = a.y; v[2] = a.z; v[3] = a.w;
+  v[4] = b.x; v[5] = b.y; v[6] = b.z; v[7] = b.w;
+}
+
+__device__ __forceinline__ void store8_f32(float* p, const float (&v)[8]) {
+  *reinterpret_cast<float4*>(p) = make_float4(v[0], v[1], v[2], v[3]);
+  *reinterpret_cast<float4*>(p + 4) = make_float4(v[4], v[5], v[6], v[7]);
+}
+
+// Store 8 values as bf16 heads at hi and bf16 remainders at lo (16 B each).
+__device__ __forceinline__ void store8_split(__nv_bfloat16* hi, __nv_bfloat16* lo, const float (&v)[8]) {
+  uint4 h, l;
+  split_bf16(v[0], v[1], h.x, l.x);
+  split_bf16(v[2], v[3], h.y, l.y);
+  split_bf16(v[4], v[5], h.z, l.z);
+  split_bf16(v[6], v[7], h.w, l.w);
+  *reinterpret_cast<uint4*>(hi) = h;
+  *reinterpret_cast<uint4*>(lo) = l;
+}
+
+// y[r] = x[r] * rsqrt(mean(x[r]^2) + eps) * g, written as head (row r) and
+// remainder (row R + r); x held in registers (passes of 8 per thread).
+__device__ __forceinline__ void norm_store(const float (&xv)[kMaxRowPasses][8], int passes, int r, int H, int R,
+                                           const __nv_bfloat16* g, __nv_bfloat16* y, float eps, float* red) {
+  float ss = 0.f;
+  for (int p = 0; p < passes; ++p) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) ss += xv[p][i] * xv[p][i];
+  }
+  ss = block_sum(ss, red);
+  const float rs = rsqrtf(ss / H + eps);
+  for (int p = 0; p < passes; ++p) {
+    const int c = (p * blockDim.x + threadIdx.x) * 8;
+    float gv[8], yv[8];
+    load8_bf16(g + c, gv);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) yv[i] = xv[p][i] * rs * gv[i];
+    store8_split(y + (long long)r * H + c, y + ((long long)R + r) * H + c, yv);
+  }
 }
 
 // x[r] = E[id] + Pos[i] with id = V ([MASK]) for masked positions;
-// y[r] = x / sqrt(mean(x^2) + eps) * g, split into head (row r) and
-// remainder (row R + r).  One CTA per row.
+// y[r] = RMSNorm(x[r]) * g as head + remainder.  One CTA per row.
 __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const __nv_bfloat16* embed,
                              const __nv_bfloat16* pos, const __nv_bfloat16* g, float* x, __nv_bfloat16* y, int S,
                              int H, int V, float eps) {
-  const long long lo_off = (long long)gridDim.x * H;
   __shared__ float red[32];
-  extern __shared__ float xs[];
-  const int r = blockIdx.x, b = r / S, i = r % S;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int r = blockIdx.x, b = r / S, i = r % S, R = gridDim.x;
   const bool masked = (mask[b] >> i) & 1u;
   // Ids outside [0, V] (never produced by the commit rule) read the [MASK] row.
   const int t = tokens[r];
   const int id = (masked || t < 0 || t > V) ? V : t;
-  float ss = 0.f;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    const float v = bf(embed, (long long)id * H + c) + bf(pos, (long long)i * H + c);
-    xs[c] = v;
-    ss += v * v;
+  const int passes = H / (8 * blockDim.x);
+  float xv[kMaxRowPasses][8];
+  for (int p = 0; p < passes; ++p) {
+    const int c = (p * blockDim.x + threadIdx.x) * 8;
+    float e[8], q[8];
+    load8_bf16(embed + (long long)id * H + c, e);
+    load8_bf16(pos + (long long)i * H + c, q);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) xv[p][k] = e[k] + q[k];
+    store8_f32(x + (long long)r * H + c, xv[p]);
   }
-  ss = block_sum(ss, red);
-  const float rs = rsqrtf(ss / H + eps);
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    x[(long long)r * H + c] = xs[c];
-    store_split(y + (long long)r * H + c, y + lo_off + (long long)r * H + c, xs[c] * rs * bf(g, c));
+  norm_store(xv, passes, r, H, R, g, y, eps, red);
+}
+
+// x[r] += sum_s part[s][r]; y[r] = RMSNorm(x[r]) * g as head + remainder.
+// One CTA per row; the split partial loads of each pass are independent.
+__global__ void k_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
+                                       const __nv_bfloat16* g, __nv_bfloat16* y, int H, float eps) {
+  __shared__ float red[32];
+  pdl_wait();
+  pdl_launch_dependents();
+  const int r = blockIdx.x, R = gridDim.x;
+  const int passes = H / (8 * blockDim.x);
+  float xv[kMaxRowPasses][8];
+  for (int p = 0; p < passes; ++p) {
+    const long long e = (long long)r * H + (p * blockDim.x + threadIdx.x) * 8;
+    load8_f32(x + e, xv[p]);
+#pragma unroll 4
+    for (int s = 0; s < splits; ++s) {
+      float v[8];
+      load8_f32(part + s * split_stride + e, v);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) xv[p][k] += v[k];
+    }
+    store8_f32(x + e, xv[p]);
   }
+  norm_store(xv, passes, r, H, R, g, y, eps, red);
 }
 
 // out[r][n] = sum over splits of part[s][r][n]; bf16 output optionally split
@@ -67,66 +140,67 @@ __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const 
 template <typename OutT>
 __global__ void k_reduce(const float* part, int splits, long long split_stride, long long total, OutT* out,
                          int split) {
-  for (long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 4; e < total;
-       e += (long long)gridDim.x * blockDim.x * 4) {
-    float4 acc = *reinterpret_cast<const float4*>(part + e);
+  pdl_wait();
+  pdl_launch_dependents();
+  for (long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8; e < total;
+       e += (long long)gridDim.x * blockDim.x * 8) {
+    float acc[8];
+    load8_f32(part + e, acc);
+#pragma unroll 4
     for (int s = 1; s < splits; ++s) {
-      const float4 v = *reinterpret_cast<const float4*>(part + s * split_stride + e);
-      acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+      float v[8];
+      load8_f32(part + s * split_stride + e, v);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) acc[k] += v[k];
     }
     if constexpr (sizeof(OutT) == 2) {
       __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
-      uint2 hi, lo;
-      split_bf16(acc.x, acc.y, hi.x, lo.x);
-      split_bf16(acc.z, acc.w, hi.y, lo.y);
-      *reinterpret_cast<uint2*>(o + e) = hi;
-      if (split) *reinterpret_cast<uint2*>(o + total + e) = lo;
+      if (split) {
+        store8_split(o + e, o + total + e, acc);
+      } else {
+        uint4 h, l;
+        split_bf16(acc[0], acc[1], h.x, l.x);
+        split_bf16(acc[2], acc[3], h.y, l.y);
+        split_bf16(acc[4], acc[5], h.z, l.z);
+        split_bf16(acc[6], acc[7], h.w, l.w);
+        *reinterpret_cast<uint4*>(o + e) = h;
+      }
     } else {
-      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + e) = acc;
+      store8_f32(reinterpret_cast<float*>(out) + e, acc);
     }
-  }
-}
-
-// x[r] += sum_s part[s][r]; y[r] = rmsnorm(x[r]) * g, split into head (row r)
-// and remainder (row R + r).  One CTA per row.
-__global__ void k_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
-                                       const __nv_bfloat16* g, __nv_bfloat16* y, int H, float eps) {
-  __shared__ float red[32];
-  extern __shared__ float xs[];
-  const int r = blockIdx.x;
-  const long long lo_off = (long long)gridDim.x * H;
-  float ss = 0.f;
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    float v = x[(long long)r * H + c];
-    for (int s = 0; s < splits; ++s) v += part[s * split_stride + (long long)r * H + c];
-    xs[c] = v;
-    ss += v * v;
-  }
-  ss = block_sum(ss, red);
-  const float rs = rsqrtf(ss / H + eps);
-  for (int c = threadIdx.x; c < H; c += blockDim.x) {
-    x[(long long)r * H + c] = xs[c];
-    store_split(y + (long long)r * H + c, y + lo_off + (long long)r * H + c, xs[c] * rs * bf(g, c));
   }
 }
 
 // h[r][f] = silu(gate) * up, gate = column f, up = column F + f of the
-// summed partials [rows][2F]; split into head and remainder (at h + rows*F).
+// summed partials [rows][2F]; head + remainder (remainder at h + rows*F).
 __global__ void k_reduce_swiglu(const float* part, int splits, long long split_stride, __nv_bfloat16* h, int rows,
                                 int F) {
+  pdl_wait();
+  pdl_launch_dependents();
   const long long total = (long long)rows * F;
-  for (long long e = (long long)blockIdx.x * blockDim.x + threadIdx.x; e < total;
-       e += (long long)gridDim.x * blockDim.x) {
+  for (long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8; e < total;
+       e += (long long)gridDim.x * blockDim.x * 8) {
     const long long r = e / F;
     const int f = (int)(e % F);
     const long long gi = r * 2 * F + f;
-    float gt = 0.f, up = 0.f;
-    for (int s = 0; s < splits; ++s) {
-      gt += part[s * split_stride + gi];
-      up += part[s * split_stride + gi + F];
+    float gt[8], up[8];
+    load8_f32(part + gi, gt);
+    load8_f32(part + gi + F, up);
+#pragma unroll 4
+    for (int s = 1; s < splits; ++s) {
+      float a[8], c[8];
+      load8_f32(part + s * split_stride + gi, a);
+      load8_f32(part + s * split_stride + gi + F, c);
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        gt[k] += a[k];
+        up[k] += c[k];
+      }
     }
-    const float si = gt / (1.f + expf(-gt));
-    store_split(h + e, h + total + e, si * up);
+    float hv[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) hv[k] = gt[k] / (1.f + expf(-gt[k])) * up[k];
+    store8_split(h + e, h + total + e, hv);
   }
 }
 
@@ -134,6 +208,8 @@ __global__ void k_reduce_swiglu(const float* part, int splits, long long split_s
 // and the lowest argmax.  One warp per row.
 __global__ void k_select_combine(const float* sel_m, const float* sel_s, const int* sel_a, int n_tiles, int rows,
                                  float* conf, int* arg) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
   if (r >= rows) return;
@@ -180,6 +256,8 @@ __global__ void k_select_combine(const float* sel_m, const float* sel_s, const i
 __global__ void k_commit(const float* conf, const int* arg, int32_t* tokens, uint32_t* mask, const float* params,
                          float gamma_arg, int mode_arg, int32_t* n_committed, int32_t* remaining, int B, int S) {
   __shared__ int left[32];
+  pdl_wait();
+  pdl_launch_dependents();
   const float gamma = params ? params[0] : gamma_arg;
   const int mode = params ? (int)params[1] : mode_arg;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -265,51 +343,50 @@ int grid_for(long long work, int threads) {
   return (int)b;
 }
 
+// threads per row for the row kernels: 8 elements per thread per pass
+int row_threads(int H) {
+  int t = H / 8;
+  if (t > 256) t = 256;
+  return t;
+}
+
 }  // namespace
 
 cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const void* embed, const void* pos,
                               const void* g, float* x, void* y, int B, int S, int H, int V, float eps,
                               cudaStream_t st) {
-  k_embed_norm<<<B * S, kNormThreads, H * sizeof(float), st>>>(
-      tokens, mask, (const __nv_bfloat16*)embed, (const __nv_bfloat16*)pos, (const __nv_bfloat16*)g, x,
-      (__nv_bfloat16*)y, S, H, V, eps);
-  return cudaGetLastError();
+  return launch_k(k_embed_norm, B * S, row_threads(H), 0, st, tokens, mask, (const __nv_bfloat16*)embed,
+                  (const __nv_bfloat16*)pos, (const __nv_bfloat16*)g, x, (__nv_bfloat16*)y, S, H, V, eps);
 }
 
 cudaError_t launch_reduce_bf16(const float* part, int splits, long long split_stride, int rows, int N, void* out,
                                int split, cudaStream_t st) {
   const long long total = (long long)rows * N;
-  k_reduce<__nv_bfloat16><<<grid_for(total / 4, 256), 256, 0, st>>>(part, splits, split_stride, total,
-                                                                    (__nv_bfloat16*)out, split);
-  return cudaGetLastError();
+  return launch_k(k_reduce<__nv_bfloat16>, grid_for(total / 8, 256), 256, 0, st, part, splits, split_stride, total,
+                  (__nv_bfloat16*)out, split);
 }
 
 cudaError_t launch_reduce_f32(const float* part, int splits, long long split_stride, int rows, int N, float* out,
                               cudaStream_t st) {
   const long long total = (long long)rows * N;
-  k_reduce<float><<<grid_for(total / 4, 256), 256, 0, st>>>(part, splits, split_stride, total, out, 0);
-  return cudaGetLastError();
+  return launch_k(k_reduce<float>, grid_for(total / 8, 256), 256, 0, st, part, splits, split_stride, total, out, 0);
 }
 
 cudaError_t launch_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
                                         const void* g, void* y, int rows, int H, float eps, cudaStream_t st) {
-  k_reduce_residual_norm<<<rows, kNormThreads, H * sizeof(float), st>>>(part, splits, split_stride, x,
-                                                                        (const __nv_bfloat16*)g,
-                                                                        (__nv_bfloat16*)y, H, eps);
-  return cudaGetLastError();
+  return launch_k(k_reduce_residual_norm, rows, row_threads(H), 0, st, part, splits, split_stride, x,
+                  (const __nv_bfloat16*)g, (__nv_bfloat16*)y, H, eps);
 }
 
 cudaError_t launch_reduce_swiglu(const float* part, int splits, long long split_stride, void* h, int rows, int F,
                                  cudaStream_t st) {
-  k_reduce_swiglu<<<grid_for((long long)rows * F, 256), 256, 0, st>>>(part, splits, split_stride,
-                                                                      (__nv_bfloat16*)h, rows, F);
-  return cudaGetLastError();
+  return launch_k(k_reduce_swiglu, grid_for((long long)rows * F / 8, 256), 256, 0, st, part, splits, split_stride,
+                  (__nv_bfloat16*)h, rows, F);
 }
 
 cudaError_t launch_select_combine(const float* sel_m, const float* sel_s, const int* sel_a, int n_tiles, int rows,
                                   float* conf, int* arg, cudaStream_t st) {
-  k_select_combine<<<(rows + 7) / 8, 256, 0, st>>>(sel_m, sel_s, sel_a, n_tiles, rows, conf, arg);
-  return cudaGetLastError();
+  return launch_k(k_select_combine, (rows + 7) / 8, 256, 0, st, sel_m, sel_s, sel_a, n_tiles, rows, conf, arg);
 }
 
 cudaError_t launch_commit(const float* conf, const int* arg, int32_t* tokens, uint32_t* mask, const float* params,
@@ -317,8 +394,8 @@ cudaError_t launch_commit(const float* conf, const int* arg, int32_t* tokens, ui
                           cudaStream_t st) {
   int warps = B < 32 ? B : 32;
   if (warps < 1) warps = 1;
-  k_commit<<<1, warps * 32, 0, st>>>(conf, arg, tokens, mask, params, gamma, mode, n_committed, remaining, B, S);
-  return cudaGetLastError();
+  return launch_k(k_commit, 1, warps * 32, 0, st, conf, arg, tokens, mask, params, gamma, mode, n_committed,
+                  remaining, B, S);
 }
 
 cudaError_t launch_set_params(float* params, float gamma, int mode, cudaStream_t st) {
@@ -346,5 +423,12 @@ cudaError_t launch_wait_forever_bounded(int* status, uint64_t timeout_ns, cudaSt
   k_wait_forever_bounded<<<1, 32, 0, st>>>(status, timeout_ns);
   return cudaGetLastError();
 }
+
+namespace {
+bool g_pdl = true;
+}
+
+bool pdl_enabled() { return g_pdl; }
+void set_pdl_enabled(bool on) { g_pdl = on; }
 
 }  // namespace dd
