@@ -107,6 +107,10 @@ class Decoder:
         steps = B.dd_decode_block(self.ctx, _ptr(tokens), gamma, mode, max_steps, _stream(stream))
         return tokens, steps
 
+    def device_status(self, stream=None):
+        """Raise DDError if a kernel of this context recorded an expired bounded wait."""
+        B.dd_device_status(self.ctx, _stream(stream))
+
     def probe_step(self, tokens, mask, gamma, mode=MODE_THRESHOLD, logits=True, stream=None):
         """One step with every probe output; returns a dict of tensors."""
         cfg = self.cfg
@@ -134,9 +138,6 @@ def join_split(t: torch.Tensor) -> torch.Tensor:
     holds heads in its first half and remainders in its second half."""
     n = t.shape[-2] // 2
     return t[..., :n, :].float() + t[..., n:, :].float()
-
-    def device_status(self, stream=None):
-        B.dd_device_status(self.ctx, _stream(stream))
 
 
 # ------------------------------------------------------------- single kernels

@@ -1,0 +1,127 @@
+"""The large decode workload on the GPU: batch 32, context 32768, block 16,
+hidden 4096, 32 q / 8 kv heads x 128, 8 layers, SwiGLU 14336, vocab 131072,
+run at full size in the launch configuration the decoder uses, and checked
+against the oracle on sampled sequences (the oracle decodes those sequences
+alone: sequences never interact, which the oracle's own batch-independence
+pin establishes)."""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import oracle
+import synth
+from tests.gpu_helpers import TOL_ATTN, TOL_CONF, TOL_LOGIT, close, require_gpu, torch
+
+pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+SAMPLE = [0, 13, 31]
+
+
+class LargeProblem:
+    def __init__(self, sample):
+        from block_wise_masked_dd_b300.decoder import Decoder, pack_weights
+        cfg = synth.LARGE
+        self.cfg = cfg
+        self.sample = list(sample)
+        w = synth.make_weights_torch(cfg, 0, "cuda")
+        k, v = synth.make_context_kv_torch(cfg, 1, "cuda")
+        self.dec = Decoder(cfg, pack_weights(cfg, w, "cuda"), "cuda")
+        self.dec.set_context_kv(k, v, 0)
+        idx = torch.tensor(self.sample, device="cuda")
+        k_s = k.index_select(1, idx).float().cpu().numpy()
+        v_s = v.index_select(1, idx).float().cpu().numpy()
+        del k, v
+        wf = {n: t.float().cpu().numpy() for n, t in w.items()}
+        del w
+        torch.cuda.synchronize()
+        sub = dataclasses.replace(cfg, batch=len(self.sample))
+        self.model = oracle.OracleModel(sub, wf, k_s, v_s, cfg.ctx_len)
+
+    def rows(self):
+        S = self.cfg.block
+        return np.concatenate([np.arange(b * S, (b + 1) * S) for b in self.sample])
+
+    def compare(self, tok, mask, gamma, mode=0, logits=True):
+        """One step of the whole batch on the GPU from (tok, mask); the sampled
+        sequences are checked against the oracle run from the same state."""
+        from block_wise_masked_dd_b300.decoder import join_split
+        cfg, sel, rows = self.cfg, self.sample, self.rows()
+        t = torch.from_numpy(tok.copy()).cuda()
+        m = torch.from_numpy(mask.view(np.int32).copy()).cuda()
+        out = self.dec.probe_step(t, m, gamma, mode, logits=logits)
+        torch.cuda.synchronize()
+        r = oracle.denoise_step(self.model, tok[sel], mask[sel], gamma, mode, keep_intermediates=True)
+        for l in range(cfg.n_layers):
+            got = join_split(out["attn_out"][l]).cpu().numpy()[rows]
+            close(got, r.attn_out[l], TOL_ATTN, f"attention output, layer {l}", rel_rms=1e-3)
+        close(join_split(out["hidden"]).cpu().numpy()[rows], r.hidden_final, TOL_LOGIT, "final hidden",
+              rel_rms=1e-3)
+        if logits:
+            close(out["logits"].cpu().numpy()[rows], r.logits, TOL_LOGIT, "logits")
+        close(out["conf"].cpu().numpy()[rows], r.conf.reshape(-1), TOL_CONF, "confidence")
+        tie = r.near_tie.reshape(-1)
+        arg = out["arg"].cpu().numpy()[rows]
+        mism = (arg != r.arg.reshape(-1)) & ~tie
+        assert not mism.any(), f"argmax differs at non-tie rows {rows[np.nonzero(mism)[0][:10]]}"
+        g_tok = t.cpu().numpy()
+        g_mask = m.cpu().numpy().view(np.uint32)
+        S = cfg.block
+        for j, b in enumerate(sel):
+            if tie[j * S:(j + 1) * S].any():
+                continue
+            assert g_mask[b] == r.mask[j], f"seq {b}: mask {g_mask[b]:#x} vs oracle {r.mask[j]:#x}"
+            assert (g_tok[b] == r.tokens[j]).all(), f"seq {b}: tokens differ"
+            assert out["n_committed"][b].item() == r.n_committed[j]
+        # every sequence (sampled or not) committed at least one masked position
+        newly = mask & ~g_mask
+        assert ((newly != 0) | (mask == 0)).all()
+        assert ((g_mask & ~mask) == 0).all()
+        return g_tok, g_mask, int(tie.sum())
+
+
+@pytest.fixture(scope="module")
+def large():
+    require_gpu()
+    free, _ = torch.cuda.mem_get_info()
+    if free < 100 * 2 ** 30:
+        pytest.skip("the large workload needs ~100 GB of free device memory")
+    return LargeProblem(SAMPLE)
+
+
+def start_state(cfg):
+    return (np.full((cfg.batch, cfg.block), cfg.vocab, np.int32),
+            np.full(cfg.batch, (1 << cfg.block) - 1, np.uint32))
+
+
+def test_large_state_synced_decode(large):
+    """gamma 0.8 through a whole block; every step compared on the sample."""
+    tok, mask = start_state(large.cfg)
+    steps = ties = 0
+    while mask.max():
+        tok, mask, t = large.compare(tok, mask, 0.8, logits=(steps == 0))
+        ties += t
+        steps += 1
+        assert steps <= large.cfg.block
+    assert (tok < large.cfg.vocab).all()
+    print(f"large, gamma 0.8: {steps} steps, {ties} near-tie positions in the sample")
+
+
+@pytest.mark.parametrize("gamma,mode", [(0.5, 0), (0.95, 0), (0.8, 1)])
+def test_large_first_step(large, gamma, mode):
+    tok, mask = start_state(large.cfg)
+    large.compare(tok, mask, gamma, mode, logits=False)
+
+
+@pytest.mark.parametrize("gamma,mode", [(0.5, 0), (0.8, 0), (0.95, 0), (0.8, 1)])
+def test_large_decode_block_invariants(large, gamma, mode):
+    cfg = large.cfg
+    tokens, steps = large.dec.decode_block(gamma, mode)
+    torch.cuda.synchronize()
+    tok = tokens.cpu().numpy()
+    assert ((tok >= 0) & (tok < cfg.vocab)).all()
+    if mode == 1:
+        assert steps == cfg.block
+    else:
+        assert 1 <= steps <= cfg.block
+    large.dec.device_status()
