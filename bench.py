@@ -222,7 +222,7 @@ def algorithmic_bytes(cfg, kind, ctx_len):
         return 2 * (H * F + R * F + R * H)
     if kind == "lm_head_select":
         return 2 * (V * H + R * H) + 12 * R
-    if kind == "block_attention":
+    if kind == "attention_context":
         return 2 * 2 * cfg.batch * cfg.n_kv_heads * ctx_len * cfg.head_dim + 2 * R * (qkvw + HqD)
     return None
 

@@ -90,7 +90,7 @@ _SIGS = {
                          ctypes.POINTER(c_int32), c_void_p], c_int32),
 }
 
-KIND_NAMES = ["embed_norm", "gemm_qkv", "reduce_qkv", "block_attention", "attn_combine", "gemm_o", "norm_o",
+KIND_NAMES = ["embed_norm", "gemm_qkv", "reduce_qkv", "attention_context", "attention_merge", "gemm_o", "norm_o",
               "gemm_gate_up", "swiglu", "gemm_down", "norm_down", "lm_head_select", "select_combine", "commit"]
 
 _lib = None

@@ -283,7 +283,7 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
     a.timeout_ns = c->timeout_ns;
     DD_CUDA(dd::launch_attention(L.p_attn, a, c->m_kc, c->m_vc, c->m_kc128, c->m_vc128, st));
     mk(kKAttention);
-    if (L.p_attn.n_splits > 1) {
+    if (L.p_attn.use_tc || L.p_attn.n_splits > 1) {
       DD_CUDA(dd::launch_attention_combine(L.p_attn, a, st));
       mk(kKAttnCombine);
     }

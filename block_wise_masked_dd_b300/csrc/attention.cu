@@ -177,7 +177,7 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_block_attn(const __grid_
   const int warp = warp_id(), lane = lane_id();
   pdl_wait();  // q|k|v come from the preceding kernel
   pdl_launch_dependents();
-  const int T = a.block_only ? 0 : *a.ctx_len;
+  const int T = *a.ctx_len;
   const int ntiles = (T + kKT - 1) / kKT;
   const int per = (ntiles + n_splits - 1) / n_splits;
   const int tile0 = split * per;
@@ -382,6 +382,185 @@ __global__ void k_attn_combine(const AttnArgs a, int n_splits) {
   }
 }
 
+// tcgen05 path, after the context kernel: attention over the S in-block keys
+// for one query row, in fp32 with q, k and v rebuilt from bf16 head +
+// remainder, then the log-sum-exp merge with the n_ctx context partials:
+// o = (2^(m_b - M) o_b + sum_s 2^(m_s - M) o_s) / (2^(m_b - M) l_b + sum_s 2^(m_s - M) l_s).
+// One warp per row (sequence b, kv head, r = g * S + i), 8 rows per CTA;
+// the CTA stages q, and the block K and V of its (b, kv head), in shared
+// memory.  Scores: lane = (key j = lane / 2, half of the head dim), so each
+// dot product is split over two lanes; the output: lane owns dims
+// lane + 32 k.  The context partials are loaded before the block keys'
+// arithmetic so that their latency overlaps it.
+template <int D>
+__global__ void __launch_bounds__(256) k_attn_merge_block(const AttnArgs a, int n_ctx) {
+  constexpr int P = D / 32;      // output dims per lane
+  constexpr int H2 = D / 2;      // dims per half dot product
+  constexpr int KS = D + 8;      // padded row stride of the staged K (floats)
+  constexpr int kBatch = 8;      // context partials loaded per round trip
+  __shared__ __align__(16) float ks[kKTB * KS];
+  __shared__ __align__(16) float vs[kKTB * D];
+  __shared__ __align__(16) float qs[8][D];
+  pdl_wait();  // q|k|v and the context partials come from the preceding kernels
+  pdl_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = a.S, rows = a.G * S;
+  const int ctas_per_bk = (rows + 7) / 8;
+  const int bk = blockIdx.x / ctas_per_bk;  // b * Hkv + kvh
+  const int r0 = (blockIdx.x % ctas_per_bk) * 8;
+  const int kvh = bk % a.Hkv, b = bk / a.Hkv;
+  const long long R = (long long)a.B * S;
+  const long long lo = a.split ? R * a.ld_qkv : 0;
+  const __nv_bfloat16* qkv = reinterpret_cast<const __nv_bfloat16*>(a.qkv);
+
+  // context partials of this warp's row: issued first (consumed last)
+  const int nq = min(8, rows - r0);
+  const int r = r0 + warp;
+  const bool active = warp < nq;
+  const long long base = (long long)bk * n_ctx * rows + r;
+  float2 ml[kBatch];
+  float po[kBatch][P];
+#pragma unroll
+  for (int t = 0; t < kBatch; ++t) {
+    if (active && t < n_ctx) {
+      const long long pr = base + (long long)t * rows;
+      ml[t] = a.part_ml[pr];
+#pragma unroll
+      for (int k = 0; k < P; ++k) po[t][k] = a.part_o[pr * D + lane + 32 * k];
+    }
+  }
+
+  // q rows of this CTA, block K and block V -> shared memory (fp32, head +
+  // remainder); every load of this thread is issued before the first store
+  constexpr int CPR = D / 8;                                // 16-byte chunks per row
+  constexpr int kPer = ((8 + 2 * kKTB) * CPR + 255) / 256;  // chunks per thread, at most
+  const int total = (nq + 2 * S) * CPR;
+  uint4 hv[kPer], lv[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int c = threadIdx.x + u * 256;
+    if (c < total) {
+      const int row = c / CPR, col = (c % CPR) * 8;
+      long long off;
+      if (row < nq) {
+        const int rr = r0 + row;
+        off = (long long)(b * S + rr % S) * a.ld_qkv + (kvh * a.G + rr / S) * D + col;
+      } else {
+        const int kv = row - nq, which = kv >= S ? 1 : 0, j = kv - which * S;
+        off = (long long)(b * S + j) * a.ld_qkv + (a.Hq + which * a.Hkv + kvh) * D + col;
+      }
+      hv[u] = *reinterpret_cast<const uint4*>(qkv + off);
+      lv[u] = a.split ? *reinterpret_cast<const uint4*>(qkv + lo + off) : make_uint4(0, 0, 0, 0);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int c = threadIdx.x + u * 256;
+    if (c < total) {
+      const int row = c / CPR, col = (c % CPR) * 8;
+      float* dst;
+      if (row < nq) {
+        dst = &qs[row][col];
+      } else {
+        const int kv = row - nq, which = kv >= S ? 1 : 0, j = kv - which * S;
+        dst = which ? &vs[j * D + col] : &ks[j * KS + col];
+      }
+      const uint32_t hw[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w}, lw[4] = {lv[u].x, lv[u].y, lv[u].z, lv[u].w};
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[2 * e] = __uint_as_float(hw[e] << 16) + __uint_as_float(lw[e] << 16);
+        v[2 * e + 1] = __uint_as_float(hw[e] & 0xffff0000u) + __uint_as_float(lw[e] & 0xffff0000u);
+      }
+      reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+  }
+  __syncthreads();
+  if (!active) return;
+
+  // scores of keys j = lane / 2 + 16 u (u = 0, 1; S <= 32), each dot product
+  // split over the two halves of the dims (half = lane & 1), in base-2 units
+  const int half = lane & 1;
+  float sj[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int j = (lane >> 1) + 16 * u;
+    float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+    if (j < S) {
+      const float4* kr = reinterpret_cast<const float4*>(&ks[j * KS]);
+      const float4* qr = reinterpret_cast<const float4*>(&qs[warp][0]);
+#pragma unroll
+      for (int m = 0; m < H2 / 4; ++m) {
+        // interleaved 16-byte chunks: this half takes chunk 2m + half
+        const float4 kv = kr[2 * m + half], qv = qr[2 * m + half];
+        t0 = fmaf(qv.x, kv.x, t0);
+        t1 = fmaf(qv.y, kv.y, t1);
+        t2 = fmaf(qv.z, kv.z, t2);
+        t3 = fmaf(qv.w, kv.w, t3);
+      }
+    }
+    float t = (t0 + t1) + (t2 + t3);
+    t += __shfl_xor_sync(0xffffffffu, t, 1);
+    sj[u] = j < S ? t * a.scale_log2 : -INFINITY;
+  }
+  float mb = fmaxf(sj[0], sj[1]);
+#pragma unroll
+  for (int o = 2; o < 32; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+  float pj[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) pj[u] = sj[u] == -INFINITY ? 0.f : exp2f(sj[u] - mb);
+  float lb = half ? 0.f : pj[0] + pj[1];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) lb += __shfl_xor_sync(0xffffffffu, lb, o);
+  float acc[P];
+#pragma unroll
+  for (int k = 0; k < P; ++k) acc[k] = 0.f;
+  for (int jj = 0; jj < S; ++jj) {
+    const float p = __shfl_sync(0xffffffffu, jj < 16 ? pj[0] : pj[1], 2 * (jj & 15));
+#pragma unroll
+    for (int k = 0; k < P; ++k) acc[k] = fmaf(p, vs[jj * D + lane + 32 * k], acc[k]);
+  }
+
+  // merge with the context partials
+  float M = mb, L = lb;
+  for (int s0 = 0; s0 < n_ctx; s0 += kBatch) {
+    if (s0 > 0) {
+#pragma unroll
+      for (int t = 0; t < kBatch; ++t) {
+        if (s0 + t < n_ctx) {
+          const long long pr = base + (long long)(s0 + t) * rows;
+          ml[t] = a.part_ml[pr];
+#pragma unroll
+          for (int k = 0; k < P; ++k) po[t][k] = a.part_o[pr * D + lane + 32 * k];
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kBatch; ++t) {
+      if (s0 + t < n_ctx && ml[t].x != -INFINITY) {
+        const float Mn = fmaxf(M, ml[t].x);
+        const float wa = exp2f(M - Mn), wb = exp2f(ml[t].x - Mn);
+        L = L * wa + ml[t].y * wb;
+#pragma unroll
+        for (int k = 0; k < P; ++k) acc[k] = acc[k] * wa + po[t][k] * wb;
+        M = Mn;
+      }
+    }
+  }
+  const int g = r / S, i = r % S;
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + (long long)(b * S + i) * a.ld_out +
+                       (kvh * a.G + g) * D + lane;
+  const float inv = 1.f / L;
+#pragma unroll
+  for (int k = 0; k < P; ++k) {
+    const float v = acc[k] * inv;
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    out[32 * k] = h;
+    if (a.split) out[R * a.ld_out + 32 * k] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
+}
+
 template <int D, bool SPLIT>
 void launch_attn_kernel(const AttnPlan& p, const AttnArgs& a, int grid_x, const CUtensorMap& mk,
                         const CUtensorMap& mv, cudaStream_t st) {
@@ -407,7 +586,7 @@ AttnPlan plan_attention(int B, int S, int Hq, int Hkv, int D, int max_ctx, int a
   if (allow_tc && attention_tc_supported(D, p.rows) && max_ctx > 0) {
     p.use_tc = 1;
     p.n_ctx = attention_tc_splits(B, Hkv, max_ctx);
-    p.n_splits = p.n_ctx + 1;
+    p.n_splits = p.n_ctx;  // partial slots: the context splits (block keys are merged in-line)
     return p;
   }
   const int pairs = B * Hkv;
@@ -422,7 +601,7 @@ AttnPlan plan_attention(int B, int S, int Hq, int Hkv, int D, int max_ctx, int a
 }
 
 size_t attention_partial_bytes(const AttnPlan& p, int B, int Hkv) {
-  if (p.n_splits <= 1) return 0;
+  if (p.n_splits <= 1 && !p.use_tc) return 0;
   const size_t n = (size_t)B * Hkv * p.n_splits * p.rows;
   return n * p.D * sizeof(float) + n * sizeof(float2) + 256;
 }
@@ -430,26 +609,24 @@ size_t attention_partial_bytes(const AttnPlan& p, int B, int Hkv) {
 cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a_in, const CUtensorMap& map_k, const CUtensorMap& map_v,
                              const CUtensorMap& map_k128, const CUtensorMap& map_v128, cudaStream_t st) {
   AttnArgs a = a_in;
-  int grid_x = p.n_splits;
-  if (p.use_tc) {
-    // block keys -> partial slot 0 (one CTA per (sequence, kv head))
-    a.block_only = 1;
-    grid_x = 1;
-  }
+  // tcgen05 path: context splits only; the block keys join in the merge
+  if (p.use_tc) return launch_attention_tc(a, p.n_ctx, p.n_splits, map_k128, map_v128, st);
   if (p.D == 128) {
-    if (a.split) launch_attn_kernel<128, true>(p, a, grid_x, map_k, map_v, st);
-    else launch_attn_kernel<128, false>(p, a, grid_x, map_k, map_v, st);
+    if (a.split) launch_attn_kernel<128, true>(p, a, p.n_splits, map_k, map_v, st);
+    else launch_attn_kernel<128, false>(p, a, p.n_splits, map_k, map_v, st);
   } else {
-    if (a.split) launch_attn_kernel<64, true>(p, a, grid_x, map_k, map_v, st);
-    else launch_attn_kernel<64, false>(p, a, grid_x, map_k, map_v, st);
+    if (a.split) launch_attn_kernel<64, true>(p, a, p.n_splits, map_k, map_v, st);
+    else launch_attn_kernel<64, false>(p, a, p.n_splits, map_k, map_v, st);
   }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess || !p.use_tc) return e;
-  a.block_only = 0;
-  return launch_attention_tc(a, p.n_ctx, p.n_splits, map_k128, map_v128, st);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_attention_combine(const AttnPlan& p, const AttnArgs& a, cudaStream_t st) {
+  if (p.use_tc) {
+    const int blocks = a.B * a.Hkv * ((p.rows + 7) / 8);
+    if (p.D == 128) return launch_k(k_attn_merge_block<128>, blocks, 256, 0, st, a, p.n_ctx);
+    return launch_k(k_attn_merge_block<64>, blocks, 256, 0, st, a, p.n_ctx);
+  }
   if (p.n_splits == 1) return cudaSuccess;
   const long long warps = (long long)a.B * a.Hkv * p.rows;
   const int blocks = (int)((warps + 7) / 8);
@@ -467,6 +644,12 @@ cudaError_t prepare_attention_kernels() {
   cudaError_t e = cudaSuccess;
   for (const void* f : fns) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  }
+  const void* comb[] = {(const void*)k_attn_combine<128>, (const void*)k_attn_combine<64>,
+                        (const void*)k_attn_merge_block<128>, (const void*)k_attn_merge_block<64>};
+  for (const void* f : comb) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   }
   return e;
 }

@@ -1,8 +1,8 @@
 // Context part of the block attention on the tcgen05 tensor cores (head dim
-// 128, 64 query rows per (sequence, kv head)).  The block keys are handled by
-// the mma.sync kernel as one more partial, and the combine kernel merges all
-// partials (TwoTower article, "技術/ビジネス面": one softmax over the context
-// and the block).
+// 128, 64 query rows per (sequence, kv head)).  Each split writes a partial
+// (o, m, l); the merge kernel adds the block keys and combines them all
+// (TwoTower article, "技術/ビジネス面": one softmax over the context and the
+// block).
 //
 // Per 128-key tile:
 //   S[64 q][128 keys] = Q[64][128] . K_tile[128][128]^T     (M=64, K-major A and B)
@@ -400,8 +400,8 @@ __global__ void __launch_bounds__(kThreads, 1)
       al1 = a1;
     }
     if (ok && nt >= 1) ok = consume_o(nt - 1, al0, al1);
-    // partial slot 1 + split: o (unnormalised, [q][d]), (m, l) per q
-    const long long prow = ((long long)(b * a.Hkv + kvh) * n_slots + 1 + split) * kNQ;
+    // partial slot `split`: o (unnormalised, [q][d]), (m, l) per q
+    const long long prow = ((long long)(b * a.Hkv + kvh) * n_slots + split) * kNQ;
 #pragma unroll
     for (int rep = 0; rep < 16; ++rep) {
       const int d = 8 * rep + cq;

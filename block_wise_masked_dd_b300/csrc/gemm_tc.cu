@@ -227,9 +227,20 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int lrow = mt * kBM + q * 32 + lane;  // accumulator row owned by this thread
 
       if (EPI == kEpiPartial) {
-        // lrow = output feature, columns = activation rows.
+        // lrow = output feature, columns = activation rows.  TMEM is read 64
+        // columns per wait (16 for a ragged tail).
         float* dst = args.out.partial + (long long)split * args.out.split_stride + lrow;
-        for (int c = 0; c < args.BN; c += 16) {
+        int c = 0;
+        for (; c + 64 <= args.BN; c += 64) {
+          float v[64];
+          tmem_ld64(tbase + c, v);
+          const int row0 = nt * args.BN + c;
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            if (row0 + j < args.out.rows_valid) dst[(long long)(row0 + j) * args.out.ld] = v[j];
+          }
+        }
+        for (; c < args.BN; c += 16) {
           float v[16];
           tmem_ld16(tbase + c, v);
           const int row0 = nt * args.BN + c;
@@ -242,13 +253,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // lrow = activation row, columns = vocab ids nt*BN + c.
         float m = -INFINITY, ssum = 0.f;
         int arg = 0;
-        for (int c = 0; c < args.BN; c += 16) {
-          float v[16];
-          tmem_ld16(tbase + c, v);
+        for (int c = 0; c < args.BN; c += 64) {  // BN is 256
+          float v[64];
+          tmem_ld64(tbase + c, v);
           float cm = v[0];
           int ci = 0;
 #pragma unroll
-          for (int j = 1; j < 16; ++j) {
+          for (int j = 1; j < 64; ++j) {
             if (v[j] > cm) { cm = v[j]; ci = j; }
           }
           if (cm > m) {
@@ -258,7 +269,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           const float mb = m * kLog2e;
 #pragma unroll
-          for (int j = 0; j < 16; ++j) ssum += exp2f(fmaf(v[j], kLog2e, -mb));
+          for (int j = 0; j < 64; ++j) ssum += exp2f(fmaf(v[j], kLog2e, -mb));
         }
         if (lrow < args.out.rows_valid) {
           const long long o = (long long)nt * args.out.rows_valid + lrow;
@@ -332,7 +343,7 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act) {
     // K block of weights per SM).
     int best_s = 1;
     double best_cost = -1.0;
-    const int max_s = p.kb_total < 16 ? p.kb_total : 16;
+    const int max_s = p.kb_total < kMaxSplits ? p.kb_total : kMaxSplits;
     const double partial_kb = 0.5 * (double)rows * N * 8.0 / ((double)kNumSMs * kStageA);
     for (int s = 1; s <= max_s; ++s) {
       const int kbps = (p.kb_total + s - 1) / s;
@@ -389,6 +400,8 @@ cudaError_t prepare_gemm_kernels() {
   cudaError_t e = cudaSuccess;
   for (int i = 0; i < 6 && e == cudaSuccess; ++i)
     e = cudaFuncSetAttribute(ks[i], cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
+  for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+    e = cudaFuncSetAttribute(ks[i], cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   return e;
 }
 
@@ -398,6 +411,7 @@ cudaError_t prepare_kernels() {
   cudaError_t e = prepare_gemm_kernels();
   if (e == cudaSuccess) e = prepare_attention_kernels();
   if (e == cudaSuccess) e = prepare_attention_tc_kernels();
+  if (e == cudaSuccess) e = prepare_small_kernels();
   done = e;
   return e;
 }

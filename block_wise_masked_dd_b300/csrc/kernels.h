@@ -31,6 +31,7 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
 }
 
 constexpr int kNumSMs = 148;
+constexpr int kMaxSplits = 16;  // split-K partials of one linear layer, at most
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per bounded wait
 
 // ------------------------------------------------------------ tcgen05 GEMM
@@ -77,9 +78,9 @@ cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUten
 
 struct AttnPlan {
   int D, rows, warps_c, n_splits, stages, smem_bytes;
-  // tcgen05 context path (D = 128, 64 query rows): partial slot 0 holds the
-  // block keys (mma.sync kernel), slots 1..n_ctx the context splits;
-  // n_splits = n_ctx + 1 partial slots in total.
+  // tcgen05 context path (D = 128, 64 query rows): the context splits write
+  // partial slots 0..n_ctx-1 (n_splits = n_ctx); the merge kernel adds the
+  // block keys and combines.
   int use_tc, n_ctx;
 };
 
@@ -87,7 +88,6 @@ struct AttnArgs {
   const void* qkv;     // bf16 [B*S][ld_qkv] (with split: [2*B*S][ld_qkv], heads then remainders)
   int ld_qkv;
   int split;           // q and block k/v carry bf16 remainders; the output is written as head + remainder
-  int block_only;      // attend to the block keys only (context handled elsewhere), write partial slot 0
   int B, S, Hq, Hkv, G;
   const int* ctx_len;  // device int (context length)
   int z0;              // tensor-map z offset of (b=0, kvh=0) for this layer
@@ -113,7 +113,8 @@ int attention_tc_smem_bytes();
 cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx_splits, int n_slots, const CUtensorMap& map_k128,
                                 const CUtensorMap& map_v128, cudaStream_t st);
 cudaError_t prepare_attention_tc_kernels();
-// Merge the split partials (no-op with one split).
+// Merge the split partials (no-op for the mma.sync path with one split); on
+// the tcgen05 path this also attends to the block keys.
 cudaError_t launch_attention_combine(const AttnPlan& p, const AttnArgs& a, cudaStream_t st);
 
 // --------------------------------------------------- elementwise / small
@@ -142,6 +143,7 @@ cudaError_t launch_commit(const float* conf, const int* arg, int32_t* tokens, ui
 cudaError_t prepare_kernels();
 cudaError_t prepare_gemm_kernels();
 cudaError_t prepare_attention_kernels();
+cudaError_t prepare_small_kernels();
 cudaError_t launch_set_params(float* params, float gamma, int mode, cudaStream_t st);
 cudaError_t launch_set_int(int* dst, int value, cudaStream_t st);
 cudaError_t launch_init_block(int32_t* tokens, uint32_t* mask, int B, int S, int V, cudaStream_t st);

@@ -62,25 +62,57 @@ __device__ __forceinline__ void store8_split(__nv_bfloat16* hi, __nv_bfloat16* l
   *reinterpret_cast<uint4*>(lo) = l;
 }
 
+// acc += p[s * stride .. + 8] for s = s0, s0 + 1, ..., s1 - 1 in that order.
+// The loads of up to MAXS partials are issued together before the first add,
+// so a reduce costs about one L2 round trip per MAXS splits.
+template <int MAXS>
+__device__ __forceinline__ void add_partials(const float* p, int s0, int s1, long long stride, float (&acc)[8]) {
+  for (int b = s0; b < s1; b += MAXS) {
+    float v[MAXS][8];
+#pragma unroll
+    for (int j = 0; j < MAXS; ++j)
+      if (b + j < s1) load8_f32(p + (long long)(b + j) * stride, v[j]);
+#pragma unroll
+    for (int j = 0; j < MAXS; ++j) {
+      if (b + j < s1) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) acc[k] += v[j][k];
+      }
+    }
+  }
+}
+
 // y[r] = x[r] * rsqrt(mean(x[r]^2) + eps) * g, written as head (row r) and
 // remainder (row R + r); x held in registers (passes of 8 per thread).
 __device__ __forceinline__ void norm_store(const float (&xv)[kMaxRowPasses][8], int passes, int r, int H, int R,
-                                           const __nv_bfloat16* g, __nv_bfloat16* y, float eps, float* red) {
+                                           const float (&gv)[kMaxRowPasses][8], __nv_bfloat16* y, float eps,
+                                           float* red) {
   float ss = 0.f;
-  for (int p = 0; p < passes; ++p) {
+#pragma unroll
+  for (int p = 0; p < kMaxRowPasses; ++p) {
+    if (p >= passes) break;
 #pragma unroll
     for (int i = 0; i < 8; ++i) ss += xv[p][i] * xv[p][i];
   }
   ss = block_sum(ss, red);
   const float rs = rsqrtf(ss / H + eps);
-  for (int p = 0; p < passes; ++p) {
-    const int c = (p * blockDim.x + threadIdx.x) * 8;
-    float gv[8], yv[8];
-    load8_bf16(g + c, gv);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) yv[i] = xv[p][i] * rs * gv[i];
+  for (int p = 0; p < kMaxRowPasses; ++p) {
+    if (p >= passes) break;
+    const int c = (p * blockDim.x + threadIdx.x) * 8;
+    float yv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) yv[i] = xv[p][i] * rs * gv[p][i];
     store8_split(y + (long long)r * H + c, y + ((long long)R + r) * H + c, yv);
   }
+}
+
+// The gains of this thread's columns (weights: read before the wait on the
+// preceding kernel).
+__device__ __forceinline__ void load_gains(const __nv_bfloat16* g, int passes, float (&gv)[kMaxRowPasses][8]) {
+#pragma unroll
+  for (int p = 0; p < kMaxRowPasses; ++p)
+    if (p < passes) load8_bf16(g + (p * blockDim.x + threadIdx.x) * 8, gv[p]);
 }
 
 // x[r] = E[id] + Pos[i] with id = V ([MASK]) for masked positions;
@@ -89,25 +121,31 @@ __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const 
                              const __nv_bfloat16* pos, const __nv_bfloat16* g, float* x, __nv_bfloat16* y, int S,
                              int H, int V, float eps) {
   __shared__ float red[32];
+  const int r = blockIdx.x, b = r / S, i = r % S, R = gridDim.x;
+  const int passes = H / (8 * blockDim.x);
+  float gv[kMaxRowPasses][8], pv[kMaxRowPasses][8];
+  load_gains(g, passes, gv);
+#pragma unroll
+  for (int p = 0; p < kMaxRowPasses; ++p)
+    if (p < passes) load8_bf16(pos + (long long)i * H + (p * blockDim.x + threadIdx.x) * 8, pv[p]);
   pdl_wait();
   pdl_launch_dependents();
-  const int r = blockIdx.x, b = r / S, i = r % S, R = gridDim.x;
   const bool masked = (mask[b] >> i) & 1u;
   // Ids outside [0, V] (never produced by the commit rule) read the [MASK] row.
   const int t = tokens[r];
   const int id = (masked || t < 0 || t > V) ? V : t;
-  const int passes = H / (8 * blockDim.x);
   float xv[kMaxRowPasses][8];
-  for (int p = 0; p < passes; ++p) {
-    const int c = (p * blockDim.x + threadIdx.x) * 8;
-    float e[8], q[8];
-    load8_bf16(embed + (long long)id * H + c, e);
-    load8_bf16(pos + (long long)i * H + c, q);
 #pragma unroll
-    for (int k = 0; k < 8; ++k) xv[p][k] = e[k] + q[k];
+  for (int p = 0; p < kMaxRowPasses; ++p) {
+    if (p >= passes) break;
+    const int c = (p * blockDim.x + threadIdx.x) * 8;
+    float e[8];
+    load8_bf16(embed + (long long)id * H + c, e);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) xv[p][k] = e[k] + pv[p][k];
     store8_f32(x + (long long)r * H + c, xv[p]);
   }
-  norm_store(xv, passes, r, H, R, g, y, eps, red);
+  norm_store(xv, passes, r, H, R, gv, y, eps, red);
 }
 
 // x[r] += sum_s part[s][r]; y[r] = RMSNorm(x[r]) * g as head + remainder.
@@ -115,24 +153,22 @@ __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const 
 __global__ void k_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
                                        const __nv_bfloat16* g, __nv_bfloat16* y, int H, float eps) {
   __shared__ float red[32];
-  pdl_wait();
-  pdl_launch_dependents();
   const int r = blockIdx.x, R = gridDim.x;
   const int passes = H / (8 * blockDim.x);
+  float gv[kMaxRowPasses][8];
+  load_gains(g, passes, gv);
+  pdl_wait();
+  pdl_launch_dependents();
   float xv[kMaxRowPasses][8];
-  for (int p = 0; p < passes; ++p) {
+#pragma unroll
+  for (int p = 0; p < kMaxRowPasses; ++p) {
+    if (p >= passes) break;
     const long long e = (long long)r * H + (p * blockDim.x + threadIdx.x) * 8;
     load8_f32(x + e, xv[p]);
-#pragma unroll 4
-    for (int s = 0; s < splits; ++s) {
-      float v[8];
-      load8_f32(part + s * split_stride + e, v);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) xv[p][k] += v[k];
-    }
+    add_partials<8>(part + e, 0, splits, split_stride, xv[p]);
     store8_f32(x + e, xv[p]);
   }
-  norm_store(xv, passes, r, H, R, g, y, eps, red);
+  norm_store(xv, passes, r, H, R, gv, y, eps, red);
 }
 
 // out[r][n] = sum over splits of part[s][r][n]; bf16 output optionally split
@@ -146,13 +182,7 @@ __global__ void k_reduce(const float* part, int splits, long long split_stride, 
        e += (long long)gridDim.x * blockDim.x * 8) {
     float acc[8];
     load8_f32(part + e, acc);
-#pragma unroll 4
-    for (int s = 1; s < splits; ++s) {
-      float v[8];
-      load8_f32(part + s * split_stride + e, v);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) acc[k] += v[k];
-    }
+    add_partials<8>(part + e, 1, splits, split_stride, acc);
     if constexpr (sizeof(OutT) == 2) {
       __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
       if (split) {
@@ -186,17 +216,8 @@ __global__ void k_reduce_swiglu(const float* part, int splits, long long split_s
     float gt[8], up[8];
     load8_f32(part + gi, gt);
     load8_f32(part + gi + F, up);
-#pragma unroll 4
-    for (int s = 1; s < splits; ++s) {
-      float a[8], c[8];
-      load8_f32(part + s * split_stride + gi, a);
-      load8_f32(part + s * split_stride + gi + F, c);
-#pragma unroll
-      for (int k = 0; k < 8; ++k) {
-        gt[k] += a[k];
-        up[k] += c[k];
-      }
-    }
+    add_partials<4>(part + gi, 1, splits, split_stride, gt);
+    add_partials<4>(part + gi + F, 1, splits, split_stride, up);
     float hv[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) hv[k] = gt[k] / (1.f + expf(-gt[k])) * up[k];
@@ -351,6 +372,21 @@ int row_threads(int H) {
 }
 
 }  // namespace
+
+// Every kernel of the step runs with the largest shared-memory carveout, the
+// one the tensor-core kernels need: an SM then never has to drain to change
+// its L1 / shared split before the next kernel's CTAs can join it.
+cudaError_t prepare_small_kernels() {
+  const void* fns[] = {(const void*)k_embed_norm,           (const void*)k_reduce_residual_norm,
+                       (const void*)k_reduce<__nv_bfloat16>, (const void*)k_reduce<float>,
+                       (const void*)k_reduce_swiglu,         (const void*)k_select_combine,
+                       (const void*)k_commit};
+  cudaError_t e = cudaSuccess;
+  for (const void* f : fns) {
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  }
+  return e;
+}
 
 cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const void* embed, const void* pos,
                               const void* g, float* x, void* y, int B, int S, int H, int V, float eps,

@@ -186,7 +186,9 @@ dd_status dd_denoise_step_probe(dd_ctx* ctx, int32_t* tokens, uint32_t* mask, fl
 /* Kernel launches one denoising step enqueues (embedding through commit). */
 dd_status dd_step_launch_count(dd_ctx* ctx, int32_t* n);
 
-/* Launch kinds reported by dd_profile_step. */
+/* Launch kinds reported by dd_profile_step.  DD_KIND_ATTENTION is the context
+ * attention (all of it on the mma.sync path); DD_KIND_ATTN_COMBINE merges the
+ * split partials and, on the tcgen05 path, attends to the in-block keys. */
 enum {
   DD_KIND_EMBED = 0, DD_KIND_GEMM_QKV, DD_KIND_REDUCE_QKV, DD_KIND_ATTENTION, DD_KIND_ATTN_COMBINE, DD_KIND_GEMM_O,
   DD_KIND_NORM_O, DD_KIND_GEMM_GATE_UP, DD_KIND_SWIGLU, DD_KIND_GEMM_DOWN, DD_KIND_NORM_DOWN, DD_KIND_LM_SELECT,
