@@ -36,7 +36,7 @@ METRIC = "committed tokens/sec on 1 B300 (block 16, γ=0.8); block-attn HBM GB/s
 UNIT = "tokens/s"
 
 
-def parse():
+def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=20)
@@ -47,7 +47,7 @@ def parse():
     ap.add_argument("--mode", default="threshold", choices=["threshold", "mock_ar"])
     ap.add_argument("--no-micro", action="store_true", help="skip the attention / LM-head microbenchmarks")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
-    return ap.parse_args()
+    return ap.parse_args(argv)
 
 
 def workload_desc(cfg, gamma, mode):

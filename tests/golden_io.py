@@ -1,0 +1,39 @@
+"""Readers for the text fixtures under tests/golden/."""
+import os
+
+import numpy as np
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def _kv(tokens):
+    return dict(t.split("=", 1) for t in tokens)
+
+
+def commit_cases():
+    """Yield dicts: name, gamma, mode (0 threshold / 1 mock-AR), mask, conf [16],
+    committed (list of positions), mask_after."""
+    lines = [l.strip() for l in open(os.path.join(GOLDEN, "commit_rule.txt")) if l.strip() and not l.startswith("#")]
+    for i in range(0, len(lines), 3):
+        head, conf, expect = lines[i].split(), lines[i + 1].split(), lines[i + 2].split()
+        assert head[0] == "case" and conf[0] == "conf" and expect[0] == "expect"
+        h, e = _kv(head[2:]), _kv(expect[1:])
+        yield {"name": head[1], "gamma": float(h["gamma"]), "mode": 1 if h["mode"] == "mock_ar" else 0,
+               "mask": int(h["mask"], 16), "conf": np.array([float(v) for v in conf[1:]], np.float32),
+               "committed": [] if e["committed"] == "-" else [int(v) for v in e["committed"].split(",")],
+               "mask_after": int(e["mask"], 16)}
+
+
+def tiny_decode_cases():
+    """Yield dicts: gamma, mode, steps, trajectory_tie, tokens, commits,
+    first_conf, first_arg, first_tie."""
+    lines = [l.split() for l in open(os.path.join(GOLDEN, "tiny_decode.txt")) if l.strip() and not l.startswith("#")]
+    for i in range(0, len(lines), 6):
+        h = _kv(lines[i][1:])
+        rec = {"gamma": float(h["gamma"]), "mode": 1 if h["mode"] == "mock_ar" else 0, "steps": int(h["steps"]),
+               "trajectory_tie": bool(int(h["trajectory_tie"]))}
+        for row in lines[i + 1:i + 6]:
+            key, vals = row[0], row[1:]
+            rec[key] = np.array([float(v) for v in vals], np.float32) if key == "first_conf" else \
+                np.array([int(v) for v in vals], np.int64)
+        yield rec

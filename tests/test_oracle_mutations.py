@@ -1,0 +1,107 @@
+"""The oracle's pins must catch plausible mistakes.
+
+Each mutant below edits the source of one oracle function (a dropped term, a
+wrong index or sign, a transposed operand, an off-by-one in the commit rule),
+runs on the CPU only, and must make at least one pin of
+tests/test_oracle_pins.py fail.  Nothing here touches the CUDA path.
+"""
+import inspect
+import textwrap
+
+import numpy as np
+import pytest
+
+import oracle
+import oracle.decode as od
+import synth
+from tests import test_oracle_pins as pins
+
+# (function, [(old source text, new source text), ...])
+MUTANTS = {
+    "attention_without_scale": ("block_attention", [(") * scale", ")")]),
+    "attention_gqa_modulo": ("block_attention", [("kvh = h // G", "kvh = h % Hkv")]),
+    "attention_drops_context": ("block_attention", [
+        ("np.concatenate([k_ctx[kvh], k_blk[:, kvh, :]], axis=0)", "k_blk[:, kvh, :]"),
+        ("np.concatenate([v_ctx[kvh], v_blk[:, kvh, :]], axis=0)", "v_blk[:, kvh, :]")]),
+    "attention_drops_block": ("block_attention", [
+        ("np.concatenate([k_ctx[kvh], k_blk[:, kvh, :]], axis=0)", "np.concatenate([k_ctx[kvh], k_blk[:1, kvh, :]], axis=0)"),
+        ("np.concatenate([v_ctx[kvh], v_blk[:, kvh, :]], axis=0)", "np.concatenate([v_ctx[kvh], v_blk[:1, kvh, :]], axis=0)")]),
+    "attention_normalises_wrong_axis": ("block_attention", [("p.sum(axis=1,", "p.sum(axis=0,")]),
+    "rmsnorm_mean_abs": ("rmsnorm", [("np.mean(x * x,", "np.mean(np.abs(x),")]),
+    "rmsnorm_without_gain": ("rmsnorm", [(") * g.astype(F32)", ")")]),
+    "rmsnorm_without_eps": ("rmsnorm", [("ms + F32(eps)", "ms")]),
+    "silu_is_sigmoid": ("silu", [("return x / (F32(1.0)", "return F32(1.0) / (F32(1.0)")]),
+    "argmax_last_on_ties": ("select_from_logits", [
+        ("np.argmax(logits, axis=1)", "(logits.shape[1] - 1 - np.argmax(logits[:, ::-1], axis=1))")]),
+    "confidence_at_temperature_2": ("select_from_logits", [("np.exp(logits - m)", "np.exp((logits - m) / F32(2.0))")]),
+    "round_bf16_ties_away": ("round_bf16", [("np.uint64(0x7FFF) + lsb", "np.uint64(0x8000)")]),
+    "commit_strict_threshold": ("commit", [(">= g]", "> g]")]),
+    "fallback_last_on_ties": ("commit", [("if F32(conf[b, i]) > F32(conf[b, best]):",
+                                          "if F32(conf[b, i]) >= F32(conf[b, best]):")]),
+    "mock_ar_rightmost": ("commit", [("chosen = [masked[0]]", "chosen = [masked[-1]]")]),
+    "step_drops_attention_residual": ("denoise_step", [("x = x + o @", "x = o @")]),
+    "step_swaps_gate_and_up": ("denoise_step", [('silu(y @ w[f"wg{l}"].T) * (y @ w[f"wu{l}"].T)',
+                                                 'silu(y @ w[f"wu{l}"].T) * (y @ w[f"wg{l}"].T)')]),
+    "step_mask_reads_token_zero": ("denoise_step", [("[[V if (int(mask[b]) >> i) & 1", "[[0 if (int(mask[b]) >> i) & 1")]),
+    "step_without_positions": ("denoise_step", [(' + w["pos"][None, :, :]', "")]),
+    "step_transposed_wq": ("denoise_step", [('y @ w[f"wq{l}"].T', 'y @ w[f"wq{l}"]')]),
+    "step_mlp_norm_gain_from_attention": ("denoise_step", [('w[f"g_mlp{l}"]', 'w[f"g_attn{l}"]')]),
+}
+
+
+def _mutant(fn_name, edits):
+    src = textwrap.dedent(inspect.getsource(getattr(od, fn_name)))
+    for old, new in edits:
+        assert old in src, f"{fn_name}: {old!r} not found"
+        src = src.replace(old, new)
+    ns = dict(od.__dict__)
+    exec(compile(src, f"<mutant of {fn_name}>", "exec"), ns)
+    return ns[fn_name]
+
+
+@pytest.fixture(scope="module")
+def tiny_model():
+    cfg = synth.TINY.replace(batch=2, ctx_len=64, max_ctx=64)
+    return oracle.OracleModel.from_bits(cfg, synth.make_weights(cfg, 0), *synth.make_context_kv(cfg, 0),
+                                        synth.bf16_bits_to_f32)
+
+
+def _pins(tiny):
+    """The pins, cheapest first."""
+    return [
+        pins.test_silu_values,
+        pins.test_rmsnorm_closed_forms,
+        pins.test_round_bf16_matches_bruteforce,
+        pins.test_select_equal_logits,
+        lambda: pins.test_select_single_lead_closed_form(3.0),
+        pins.test_select_vs_bruteforce_and_first_max,
+        lambda: pins.test_attention_vs_bruteforce(17, 4, 1),
+        lambda: pins.test_attention_vs_bruteforce(1, 4, 2),
+        pins.test_attention_constant_values,
+        pins.test_attention_zero_query_is_uniform_mean,
+        pins.test_attention_gqa_equals_repeated_mha,
+        pins.test_attention_is_bidirectional_and_sees_context,
+        pins.test_commit_exhaustive_masks,
+        pins.test_commit_gamma_zero_and_above_one,
+        pins.test_commit_monotone_in_gamma,
+        lambda: pins.test_full_step_vs_bruteforce(False),
+        pins.test_full_step_vs_bruteforce_random_gains,
+        lambda: pins.test_decode_mock_ar_is_left_to_right(tiny),
+        lambda: pins.test_decode_committed_never_change_and_progress(tiny),
+    ]
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, monkeypatch, tiny_model):
+    fn_name, edits = MUTANTS[name]
+    bad = _mutant(fn_name, edits)
+    monkeypatch.setattr(od, fn_name, bad)
+    if hasattr(oracle, fn_name):
+        monkeypatch.setattr(oracle, fn_name, bad)
+    for pin in _pins(tiny_model):
+        try:
+            with np.errstate(all="ignore"):
+                pin()
+        except Exception:  # an assertion, or the mutant breaking outright
+            return
+    pytest.fail(f"no pin caught the mutant {name}")

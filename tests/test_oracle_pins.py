@@ -184,6 +184,23 @@ def test_full_step_vs_bruteforce(round_act):
     assert (r.arg.reshape(-1) == np.array(arg)).all()
 
 
+def test_full_step_vs_bruteforce_random_gains():
+    """Non-unit RMSNorm gains, so a gain applied at the wrong norm shows."""
+    cfg = MICRO
+    m = _micro_model(cfg)
+    rng = np.random.default_rng(11)
+    for name in list(m.w):
+        if name.startswith("g_"):
+            m.w[name] = oracle.round_bf16((1.0 + 0.4 * rng.standard_normal(m.w[name].shape)).astype(F32))
+    tok, mask = synth.make_tokens(cfg, seed=4, masked_frac=0.5)
+    r = oracle.denoise_step(m, tok, mask, 0.8, keep_intermediates=True)
+    w = {k: _nested(v) for k, v in m.w.items()}
+    logits, conf, arg = bf.denoise_step(cfg, w, _nested(m.k_ctx), _nested(m.v_ctx),
+                                        tok.tolist(), [int(v) for v in mask], False)
+    np.testing.assert_allclose(r.logits, np.array(logits), rtol=2e-4, atol=2e-5)
+    assert (r.arg.reshape(-1) == np.array(arg)).all()
+
+
 def test_bf16_storage_alone_moves_logits():
     """Storing activations in bf16 (a bf16 model's dataflow) moves the tiny
     workload's logits by far more than the 2e-2 parity bar: the reason the
