@@ -68,11 +68,14 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-bool make_map_3d(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+// planes x rows x cols bf16 with planes `stride_rows` rows apart; rows at or
+// beyond `rows` read as zero (TMA out-of-bounds fill).
+bool make_map_3d(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t stride_rows, uint64_t cols,
+                 uint32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[3] = {cols, rows, planes};
-  cuuint64_t strides[2] = {cols * 2, rows * cols * 2};
+  cuuint64_t strides[2] = {cols * 2, stride_rows * cols * 2};
   cuuint32_t box[3] = {64, box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, es,
@@ -436,10 +439,10 @@ dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_byte
   }
   const dd_config& cf = *cfg;
   const uint64_t planes = (uint64_t)cf.n_layers * cf.batch * cf.n_kv_heads;
-  bool ok = dd::make_map_3d(&c->m_kc, c->ws + L.kc, planes, L.alloc_ctx, cf.head_dim, 64) &&
-            dd::make_map_3d(&c->m_vc, c->ws + L.vc, planes, L.alloc_ctx, cf.head_dim, 64) &&
-            dd::make_map_3d(&c->m_kc128, c->ws + L.kc, planes, L.alloc_ctx, cf.head_dim, 128) &&
-            dd::make_map_3d(&c->m_vc128, c->ws + L.vc, planes, L.alloc_ctx, cf.head_dim, 128) &&
+  bool ok = dd::make_map_3d(&c->m_kc, c->ws + L.kc, planes, L.alloc_ctx, L.alloc_ctx, cf.head_dim, 64) &&
+            dd::make_map_3d(&c->m_vc, c->ws + L.vc, planes, L.alloc_ctx, L.alloc_ctx, cf.head_dim, 64) &&
+            dd::make_map_3d(&c->m_kc128, c->ws + L.kc, planes, L.alloc_ctx, L.alloc_ctx, cf.head_dim, 128) &&
+            dd::make_map_3d(&c->m_vc128, c->ws + L.vc, planes, L.alloc_ctx, L.alloc_ctx, cf.head_dim, 128) &&
             dd::make_map_2d(&c->m_y_b, c->ws + L.y, 2 * c->R, cf.hidden, L.p_qkv.BN) &&
             dd::make_map_2d(&c->m_attn_b, c->ws + L.attn, 2 * c->R, c->HqD, L.p_o.BN) &&
             dd::make_map_2d(&c->m_h_b, c->ws + L.hmid, 2 * c->R, cf.mlp, L.p_d.BN) &&
@@ -697,10 +700,12 @@ dd_status dd_block_attention(const dd_attn_problem* p, void* stream) {
   uint8_t* ws = static_cast<uint8_t*>(p->workspace);
   CUtensorMap mk, mv, mk128, mv128;
   const uint64_t planes = (uint64_t)p->batch * p->n_kv_heads;
-  if (!dd::make_map_3d(&mk, p->k_ctx, planes, p->ctx_stride, p->head_dim, 64) ||
-      !dd::make_map_3d(&mv, p->v_ctx, planes, p->ctx_stride, p->head_dim, 64) ||
-      !dd::make_map_3d(&mk128, p->k_ctx, planes, p->ctx_stride, p->head_dim, 128) ||
-      !dd::make_map_3d(&mv128, p->v_ctx, planes, p->ctx_stride, p->head_dim, 128))
+  // rows beyond ctx_len read as zero, whatever the caller's buffer holds there
+  const uint64_t ext = p->ctx_len > 0 ? (uint64_t)p->ctx_len : 1;
+  if (!dd::make_map_3d(&mk, p->k_ctx, planes, ext, p->ctx_stride, p->head_dim, 64) ||
+      !dd::make_map_3d(&mv, p->v_ctx, planes, ext, p->ctx_stride, p->head_dim, 64) ||
+      !dd::make_map_3d(&mk128, p->k_ctx, planes, ext, p->ctx_stride, p->head_dim, 128) ||
+      !dd::make_map_3d(&mv128, p->v_ctx, planes, ext, p->ctx_stride, p->head_dim, 128))
     return fail(DD_ERR_CUDA, "tensor map encoding failed for k_ctx/v_ctx");
   int* small = reinterpret_cast<int*>(ws);  // [0] ctx_len, [1] status
   DD_CUDA(dd::launch_set_int(small, p->ctx_len, st));

@@ -157,7 +157,9 @@ void set_error_message(const char* msg);
 
 // 2D bf16 map over a row-major [rows][cols] matrix, box {64 cols, box_rows}.
 bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
-// 3D bf16 map over [planes][rows][cols] (cols = head dim), box {64, box_rows, 1}.
-bool make_map_3d(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// 3D bf16 map over [planes][rows][cols] (cols = head dim), box {64, box_rows, 1};
+// planes lie stride_rows rows apart and rows >= `rows` read as zero.
+bool make_map_3d(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t stride_rows, uint64_t cols,
+                 uint32_t box_rows);
 
 }  // namespace dd

@@ -1,0 +1,50 @@
+"""Committed tokens/s for every decode workload, gamma and commit mode.
+
+    python -m block_wise_masked_dd_b300.sweep [--configs tiny small large] [--steps K] [--warmup W]
+
+Runs `bench.py` once per (workload, gamma, mode) in a fresh process (so each
+measurement sees a fresh context and its own clock record), and prints one
+JSON line per run followed by a markdown table.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import subprocess
+import sys
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GAMMAS = (0.5, 0.8, 0.95)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--configs", nargs="+", default=["tiny", "small", "large"])
+    ap.add_argument("--steps", type=int, default=3)
+    ap.add_argument("--warmup", type=int, default=3)
+    args = ap.parse_args()
+    rows = []
+    for cfg in args.configs:
+        for gamma, mode in [(g, "threshold") for g in GAMMAS] + [(0.8, "mock_ar")]:
+            cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--config", cfg, "--gamma", str(gamma), "--mode",
+                   mode, "--steps", str(args.steps), "--warmup", str(args.warmup), "--no-micro", "--no-cpu"]
+            out = subprocess.run(cmd, capture_output=True, text=True, cwd=ROOT)
+            if out.returncode != 0:
+                print(json.dumps({"config": cfg, "gamma": gamma, "mode": mode, "error": out.stderr[-2000:]}))
+                continue
+            line = json.loads(out.stdout.strip().splitlines()[-1])
+            print(json.dumps(line), flush=True)
+            rows.append((cfg, gamma, mode, line))
+    print("\n| workload | gamma | mode | steps/block | committed tokens/s | e2e tokens/s | ms per bench step | "
+          "SM MHz | throttle |")
+    print("|---|---|---|---|---|---|---|---|---|")
+    for cfg, gamma, mode, l in rows:
+        c = l.get("clocks") or {}
+        print(f"| {cfg} | {gamma} | {mode} | {l['config']['denoise_steps_per_block']:.2f} | {l['value']:.0f} | "
+              f"{l['e2e']['value']:.0f} | {l['ms_per_step']:.2f} | {c.get('sm_mhz', 'n/a')} | "
+              f"{','.join(c.get('reasons', [])) or 'none'} |")
+
+
+if __name__ == "__main__":
+    main()

@@ -31,13 +31,16 @@ def test_gemm_vs_oracle_linear(rows, n, k):
 
 # -------------------------------------------------------------- attention
 
-def _attn_case(B, S, Hq, Hkv, D, T, stride, seed):
+def _attn_case(B, S, Hq, Hkv, D, T, stride, seed, nan_tail=False):
     from block_wise_masked_dd_b300.decoder import block_attention
     qkvw = (Hq + 2 * Hkv) * D
     qkv = synth.make_activations(B * S, qkvw, seed=seed)
     rng = np.random.default_rng(seed + 1)
     kc = synth.to_bf16_bits(rng.standard_normal((B, Hkv, stride, D), dtype=np.float32))
     vc = synth.to_bf16_bits(rng.standard_normal((B, Hkv, stride, D), dtype=np.float32))
+    if nan_tail:  # rows beyond the context length must never reach the output
+        kc[:, :, T:, :] = 0x7FC0
+        vc[:, :, T:, :] = 0x7FC0
     out = block_attention(to_dev(qkv), to_dev(kc), to_dev(vc), T, B, S, Hq, Hkv, D)
     torch.cuda.synchronize()
     q32 = synth.bf16_bits_to_f32(qkv).reshape(B, S, -1)
@@ -49,6 +52,14 @@ def _attn_case(B, S, Hq, Hkv, D, T, stride, seed):
         vb = q32[b, :, (Hq + Hkv) * D:].reshape(S, Hkv, D)
         want = oracle.block_attention(q, kb, vb, kc32[b, :, :T], vc32[b, :, :T])
         close(got[b], want, TOL_ATTN, f"attention b={b} T={T}", rel_rms=3e-3)
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,D,T,stride", [
+    (2, 16, 8, 2, 128, 200, 256),     # tcgen05 path, NaN rows in the last tile and beyond
+    (3, 16, 4, 1, 64, 200, 256),      # mma.sync path
+])
+def test_block_attention_ignores_rows_beyond_context(B, S, Hq, Hkv, D, T, stride):
+    _attn_case(B, S, Hq, Hkv, D, T, stride, seed=5, nan_tail=True)
 
 
 @pytest.mark.parametrize("B,S,Hq,Hkv,D,T,stride", [
