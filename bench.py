@@ -227,6 +227,20 @@ def algorithmic_bytes(cfg, kind, ctx_len):
     return None
 
 
+def step_roofline(cfg, T0, hbm_peak, ms_per_step, denoise_per_step, peak_src):
+    """The whole denoising step against HBM: every weight read once, the context
+    K/V of every layer read once (mean context over the step's blocks)."""
+    H, F, V, L = cfg.hidden, cfg.mlp, cfg.vocab, cfg.n_layers
+    HqD = cfg.n_q_heads * cfg.head_dim
+    weights = 2 * (L * (cfg.qkv_width * H + H * HqD + 2 * F * H + H * F) + V * H)
+    t_mean = T0 + cfg.block * (BLOCKS_PER_STEP - 1) / 2
+    kv = 2 * 2 * L * cfg.batch * cfg.n_kv_heads * t_mean * cfg.head_dim
+    ideal_us = (weights + kv) / (hbm_peak * 1e9) * 1e6
+    measured_us = 1e3 * ms_per_step / max(denoise_per_step, 1e-9)
+    return {"bytes_per_denoising_step": weights + kv, "ideal_us": ideal_us, "measured_us": measured_us,
+            "frac": ideal_us / measured_us, "peak_GBps": hbm_peak, "peak_source": peak_src}
+
+
 def gpu_arm(args, world, rank, local):
     import torch
 
@@ -277,7 +291,7 @@ def gpu_arm(args, world, rank, local):
             out = tokens_host[blk] if host else tokens[blk]
             _, steps = dec.decode_block(args.gamma, mode, tokens=out)
             counters["denoise_steps"] += steps
-            counters["launches"] += 2 + steps * per_step_launches
+            counters["launches"] += 3 + steps * per_step_launches  # block init, params, loop init
             k, v = app_host[blk] if host else app[blk]
             dec.set_context_kv(k, v, T0 + blk * cfg.block)
             counters["launches"] += 1
@@ -325,13 +339,21 @@ def gpu_arm(args, world, rank, local):
               torch.full((cfg.batch,), (1 << cfg.block) - 1, dtype=torch.int32, device=dev))
     dec.set_context_len(T0)
     nprof = 0
-    while int(m_.max().item()) != 0 and nprof < 4 * cfg.block:
+    commits = []  # positions committed per denoising step of the first block (all sequences)
+
+    def masked_count():
+        return int(sum(bin(int(v) & 0xFFFFFFFF).count("1") for v in m_.cpu().tolist()))
+    left = masked_count()
+    while left and nprof < 4 * cfg.block:
         for kind, msk in B.dd_profile_step(dec.ctx, t_.data_ptr(), m_.data_ptr(), args.gamma, mode,
                                            stream=stream.cuda_stream):
             p = prof.setdefault(kind, [0.0, 0])
             p[0] += msk
             p[1] += 1
         nprof += 1
+        now = masked_count()
+        commits.append(left - now)
+        left = now
     total_prof = sum(v[0] for v in prof.values())
     kernels = {k: {"launches": v[1], "ms_total": v[0], "share": v[0] / total_prof,
                    "us_per_launch": 1e3 * v[0] / v[1]} for k, v in prof.items()}
@@ -354,7 +376,10 @@ def gpu_arm(args, world, rank, local):
                        "l2": "inputs larger than L2 (weights + context K/V per denoising step exceed 126 MB)"},
             "gpu_launches": timed_launches, "clocks": clk,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "roofline": roofline, "kernels": kernels}
+            "roofline": roofline, "kernels": kernels,
+            "commits_per_step": {"first_block": commits, "mean": float(np.mean(commits)) if commits else None},
+            "step_roofline": step_roofline(cfg, T0, hbm_peak, ms_max / args.steps,
+                                           timed_denoise / max(args.steps, 1), peak_src)}
 
     # -------------------------------- microbenchmarks named by the metric
     if not args.no_micro and rank == 0:

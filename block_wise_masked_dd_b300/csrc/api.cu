@@ -109,8 +109,10 @@ struct dd_ctx {
   std::vector<CUtensorMap> m_wqkv, m_wo, m_wgu, m_wd;
   CUtensorMap m_lm, m_y_b, m_attn_b, m_h_b, m_y_a, m_kc, m_vc, m_kc128, m_vc128;
   cudaStream_t cap_stream;
-  cudaGraphExec_t exec;
-  int32_t* hpin;  // pinned host: [0] remaining, [1] status
+  cudaGraphExec_t exec;       // one denoising step
+  cudaGraphExec_t loop_exec;  // while (masked left): step  -- the device-side decode loop
+  bool loop_tried;
+  int32_t* hpin;  // pinned host: [0] remaining, [1] status, [2] ctx_len, [3] steps, [4] step limit
   uint64_t timeout_ns;
   int device;
   int step_launches;  // kernels one denoising step launches
@@ -203,7 +205,7 @@ Layout make_layout(const dd_config& c) {
   L.tok = take((size_t)R * 4);
   L.mask = take((size_t)c.batch * 4);
   L.ncommit = take((size_t)c.batch * 4);
-  L.small = take(16);   // [0] remaining, [1] status, [2] ctx_len
+  L.small = take(32);   // [0] remaining, [1] status, [2] ctx_len, [3] steps, [4] step limit
   L.params = take(8);   // gamma, mode
   L.total = off;
   return L;
@@ -371,6 +373,47 @@ dd_status ensure_graph(dd_ctx* c) {
   return DD_OK;
 }
 
+// The decode loop as one graph: a conditional while node whose body is the
+// step followed by k_loop_control, which sets the condition on the device.
+// Returns false (and leaves loop_exec unset) where the driver refuses the
+// graph; dd_decode_block then loops on the host.
+bool ensure_loop_graph(dd_ctx* c) {
+  if (c->loop_exec) return true;
+  if (c->loop_tried) return false;
+  c->loop_tried = true;
+  cudaGraph_t g = nullptr;
+  if (cudaGraphCreate(&g, 0) != cudaSuccess) return false;
+  cudaGraphConditionalHandle h = 0;
+  cudaGraphNodeParams np = {};
+  cudaGraphNode_t node = nullptr;
+  bool ok = cudaGraphConditionalHandleCreate(&h, g, 1, cudaGraphCondAssignDefault) == cudaSuccess;
+  if (ok) {
+    np.type = cudaGraphNodeTypeConditional;
+    np.conditional.handle = h;
+    np.conditional.type = cudaGraphCondTypeWhile;
+    np.conditional.size = 1;
+    ok = cudaGraphAddNode(&node, g, nullptr, nullptr, 0, &np) == cudaSuccess;
+  }
+  if (ok) {
+    cudaGraph_t body = np.conditional.phGraph_out[0];
+    ok = cudaStreamBeginCaptureToGraph(c->cap_stream, body, nullptr, nullptr, 0, cudaStreamCaptureModeThreadLocal) ==
+         cudaSuccess;
+    if (ok) {
+      dd_status s = enqueue_step(c, c->cap_stream, nullptr, nullptr);
+      const bool launched = s == DD_OK && dd::launch_loop_control(small_ptr(c), h, c->cap_stream) == cudaSuccess;
+      cudaGraph_t captured = nullptr;
+      ok = cudaStreamEndCapture(c->cap_stream, &captured) == cudaSuccess && launched;
+    }
+  }
+  if (ok) ok = cudaGraphInstantiate(&c->loop_exec, g, 0) == cudaSuccess;
+  if (!ok) {
+    c->loop_exec = nullptr;
+    cudaGetLastError();  // clear a refused capture or instantiation
+  }
+  cudaGraphDestroy(g);
+  return ok;
+}
+
 dd_status check_ctx(dd_ctx* c) {
   if (!c) return fail(DD_ERR_INVALID_ARG, "ctx is NULL");
   if (!c->have_weights) return fail(DD_ERR_NOT_READY, "weights not set (call dd_init_weights)");
@@ -431,7 +474,7 @@ dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_byte
   if (e == cudaSuccess) e = dd::prepare_kernels();
   if (e == cudaSuccess) e = cudaMemset(workspace, 0, L.total);
   if (e == cudaSuccess) e = cudaStreamCreateWithFlags(&c->cap_stream, cudaStreamNonBlocking);
-  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&c->hpin), 16, cudaHostAllocDefault);
+  if (e == cudaSuccess) e = cudaHostAlloc(reinterpret_cast<void**>(&c->hpin), 32, cudaHostAllocDefault);
   if (e == cudaSuccess) e = cudaDeviceSynchronize();
   if (e != cudaSuccess) {
     dd_destroy(c);
@@ -458,6 +501,7 @@ dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_byte
 void dd_destroy(dd_ctx* c) {
   if (!c) return;
   if (c->exec) cudaGraphExecDestroy(c->exec);
+  if (c->loop_exec) cudaGraphExecDestroy(c->loop_exec);
   if (c->cap_stream) cudaStreamDestroy(c->cap_stream);
   if (c->hpin) cudaFreeHost(c->hpin);
   delete c;
@@ -575,8 +619,21 @@ dd_status dd_decode_block(dd_ctx* c, int32_t* tokens, float gamma, int32_t mode,
   uint8_t* ws = c->ws;
   DD_CUDA(dd::launch_init_block(at<int32_t>(ws, c->L.tok), at<uint32_t>(ws, c->L.mask), cf.batch, cf.block, cf.vocab, st));
   DD_CUDA(dd::launch_set_params(at<float>(ws, c->L.params), gamma, mode, st));
+  DD_CUDA(dd::launch_loop_init(small_ptr(c), max_steps, st));
   int steps = 0;
   bool done = false;
+  if (ensure_loop_graph(c)) {
+    // device-side loop: one graph launch and one read-back per block
+    DD_CUDA(cudaGraphLaunch(c->loop_exec, st));
+    DD_CUDA(cudaMemcpyAsync(c->hpin, small_ptr(c), 20, cudaMemcpyDeviceToHost, st));
+    DD_CUDA(cudaMemcpyAsync(tokens, ws + c->L.tok, (size_t)c->R * 4, cudaMemcpyDefault, st));
+    DD_CUDA(cudaStreamSynchronize(st));
+    steps = c->hpin[3];
+    if (steps_out) *steps_out = steps;
+    if (c->hpin[1] != 0) return fail(DD_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired during step %d", steps);
+    if (c->hpin[0] != 0) return fail(DD_ERR_STEP_LIMIT, "%d steps without filling the block", max_steps);
+    return DD_OK;
+  }
   while (steps < max_steps) {
     DD_CUDA(cudaGraphLaunch(c->exec, st));
     ++steps;
@@ -616,7 +673,7 @@ dd_status dd_step_launch_count(dd_ctx* c, int32_t* n) {
   if (!n) return fail(DD_ERR_INVALID_ARG, "n is NULL");
   s = ensure_graph(c);
   if (s != DD_OK) return s;
-  *n = c->step_launches;
+  *n = c->step_launches + (ensure_loop_graph(c) ? 1 : 0);
   return DD_OK;
 }
 

@@ -146,6 +146,10 @@ cudaError_t prepare_attention_kernels();
 cudaError_t prepare_small_kernels();
 cudaError_t launch_set_params(float* params, float gamma, int mode, cudaStream_t st);
 cudaError_t launch_set_int(int* dst, int value, cudaStream_t st);
+// Device-side decode loop: reset the step counter and set the limit; count
+// a step and set the while-loop condition (see small_kernels.cu).
+cudaError_t launch_loop_init(int32_t* small, int max_steps, cudaStream_t st);
+cudaError_t launch_loop_control(int32_t* small, cudaGraphConditionalHandle handle, cudaStream_t st);
 cudaError_t launch_init_block(int32_t* tokens, uint32_t* mask, int B, int S, int V, cudaStream_t st);
 cudaError_t launch_copy_i32(int32_t* dst, const int32_t* src, int n, cudaStream_t st);
 cudaError_t launch_wait_forever_bounded(int* status, uint64_t timeout_ns, cudaStream_t st);

@@ -332,6 +332,24 @@ __global__ void k_set_params(float* params, float gamma, int mode) {
 
 __global__ void k_set_int(int* dst, int v) { *dst = v; }
 
+// Device-side decode loop.  small: [0] masked positions left, [1] status,
+// [3] steps taken in this block, [4] step limit.
+__global__ void k_loop_init(int32_t* small, int max_steps) {
+  small[3] = 0;
+  small[4] = max_steps;
+}
+
+// Last kernel of each step in the while-loop graph: count the step and keep
+// looping while a position is masked, no kernel timed out and the limit is
+// not reached.
+__global__ void k_loop_control(int32_t* small, cudaGraphConditionalHandle handle) {
+  pdl_wait();  // the commit's remaining count
+  const int steps = small[3] + 1;
+  small[3] = steps;
+  const bool more = small[0] > 0 && small[1] == 0 && steps < small[4];
+  cudaGraphSetConditional(handle, more ? 1u : 0u);
+}
+
 __global__ void k_init_block(int32_t* tokens, uint32_t* mask, int B, int S, int V) {
   const int e = blockIdx.x * blockDim.x + threadIdx.x;
   if (e < B * S) tokens[e] = V;
@@ -442,6 +460,15 @@ cudaError_t launch_set_params(float* params, float gamma, int mode, cudaStream_t
 cudaError_t launch_set_int(int* dst, int value, cudaStream_t st) {
   k_set_int<<<1, 1, 0, st>>>(dst, value);
   return cudaGetLastError();
+}
+
+cudaError_t launch_loop_init(int32_t* small, int max_steps, cudaStream_t st) {
+  k_loop_init<<<1, 1, 0, st>>>(small, max_steps);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_loop_control(int32_t* small, cudaGraphConditionalHandle handle, cudaStream_t st) {
+  return launch_k(k_loop_control, 1, 1, 0, st, small, handle);
 }
 
 cudaError_t launch_init_block(int32_t* tokens, uint32_t* mask, int B, int S, int V, cudaStream_t st) {

@@ -145,8 +145,12 @@ dd_status dd_denoise_step(dd_ctx* ctx, int32_t* tokens, uint32_t* mask, float ga
 /* Decode one block (explainer step 5): set every position to [MASK] and run
  * denoising steps until no position is masked.  tokens: int32 [B][S], device
  * or host memory, receives the committed ids.  max_steps <= 0 means 4*S.
- * Synchronises `stream` once per step to read the number of masked positions
- * left.  steps_out (host, may be NULL) receives the step count.  Returns
+ * The steps run as one CUDA graph whose conditional while node repeats the
+ * step on the device until no position is masked (or a kernel timed out, or
+ * max_steps is reached), so the call synchronises `stream` once, at the end;
+ * where the driver refuses that graph the loop runs on the host, one
+ * synchronisation per step.  steps_out (host, may be NULL) receives the step
+ * count.  Returns
  * DD_ERR_STEP_LIMIT if positions are still masked after max_steps and
  * DD_ERR_DEVICE_TIMEOUT if a kernel's bounded wait expired. */
 dd_status dd_decode_block(dd_ctx* ctx, int32_t* tokens, float gamma, int32_t mode, int32_t max_steps,
@@ -183,7 +187,9 @@ typedef struct dd_probe {
 dd_status dd_denoise_step_probe(dd_ctx* ctx, int32_t* tokens, uint32_t* mask, float gamma, int32_t mode,
                                 int32_t* n_committed, const dd_probe* probe, void* stream);
 
-/* Kernel launches one denoising step enqueues (embedding through commit). */
+/* Kernel launches one denoising step enqueues (embedding through commit,
+ * plus the loop-control kernel when dd_decode_block runs the device-side
+ * loop). */
 dd_status dd_step_launch_count(dd_ctx* ctx, int32_t* n);
 
 /* Launch kinds reported by dd_profile_step.  DD_KIND_ATTENTION is the context

@@ -127,3 +127,25 @@ def test_host_buffers_through_the_abi(tiny):
     _, steps = tiny.dec.decode_block(0.8, tokens=h_tok)
     torch.cuda.synchronize()
     assert (h_tok.numpy() == d_tok.cpu().numpy()).all()
+
+
+def test_decode_block_runs_the_device_side_loop(small):
+    """dd_decode_block repeats the step inside one graph (conditional while
+    node) and gives the same block as stepping the single-step graph."""
+    from block_wise_masked_dd_b300 import binding as B
+    dec = small.dec
+    tok, mask = small.start_state()
+    t, m = small.gpu_state(tok, mask)
+    kinds = B.dd_profile_step(dec.ctx, t.data_ptr(), m.data_ptr(), 0.8, 0,
+                              stream=torch.cuda.current_stream().cuda_stream)
+    assert B.dd_step_launch_count(dec.ctx) == len(kinds) + 1   # + the loop-control kernel
+    tokens, steps = dec.decode_block(0.8)
+    torch.cuda.synchronize()
+    t, m = small.gpu_state(tok, mask)
+    n = 0
+    while int(m.max().item()) != 0:
+        dec.denoise_step(t, m, 0.8)
+        n += 1
+    torch.cuda.synchronize()
+    assert n == steps
+    assert (t.cpu().numpy() == tokens.cpu().numpy()).all()
