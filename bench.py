@@ -36,6 +36,25 @@ METRIC = "committed tokens/sec on 1 B300 (block 16, γ=0.8); block-attn HBM GB/s
 UNIT = "tokens/s"
 
 
+def mode_arg(s: str) -> str:
+    if s in ("threshold", "mock_ar"):
+        return s
+    name, _, val = s.partition(":")
+    if name in ("topk", "steps") and val.isdigit() and 1 <= int(val) <= 65535:
+        return s
+    raise argparse.ArgumentTypeError(f"bad mode {s!r}")
+
+
+def mode_code(s: str) -> int:
+    """The library's mode value for a --mode string."""
+    if s == "threshold":
+        return 0
+    if s == "mock_ar":
+        return 1
+    name, _, val = s.partition(":")
+    return (2 if name == "topk" else 3) | (int(val) << 8)
+
+
 def parse(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -44,7 +63,8 @@ def parse(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--config", default="small", choices=["tiny", "small", "large"])
     ap.add_argument("--gamma", type=float, default=0.8)
-    ap.add_argument("--mode", default="threshold", choices=["threshold", "mock_ar"])
+    ap.add_argument("--mode", default="threshold", type=mode_arg,
+                    help="threshold | mock_ar | topk:K (the K most confident) | steps:N (fixed N steps per block)")
     ap.add_argument("--no-micro", action="store_true", help="skip the attention / LM-head microbenchmarks")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     return ap.parse_args(argv)
@@ -169,7 +189,7 @@ def oracle_block_sample(cfg, gamma, mode, seed=0, batch=None):
     kb, vb = synth.make_context_kv(c, seed)
     m = oracle.OracleModel.from_bits(c, wb, kb, vb, synth.bf16_bits_to_f32)
     t0 = time.perf_counter()
-    tok, steps, _ = oracle.decode_block(m, gamma, 0 if mode == "threshold" else 1)
+    tok, steps, _ = oracle.decode_block(m, gamma, mode_code(mode))
     dt = time.perf_counter() - t0
     return c.batch * c.block, dt, os.cpu_count()
 
@@ -184,7 +204,7 @@ def run_reference(args, world, rank):
     wb = synth.make_weights(c, 0)
     kb, vb = synth.make_context_kv(c, 0)
     m = oracle.OracleModel.from_bits(c, wb, kb, vb, synth.bf16_bits_to_f32)
-    mode = 0 if args.mode == "threshold" else 1
+    mode = mode_code(args.mode)
     for _ in range(args.warmup):
         oracle.decode_block(m, args.gamma, mode)
     t0 = time.perf_counter()
@@ -254,7 +274,7 @@ def gpu_arm(args, world, rank, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     cfg = bench_cfg(args.config)
-    mode = 0 if args.mode == "threshold" else 1
+    mode = mode_code(args.mode)
     hbm_peak, tc_peak, tc_sust, peak_src = load_peaks()
 
     # weights: the same replica on every rank; context differs per rank

@@ -22,6 +22,13 @@ DD_ERR_UNSUPPORTED = 6
 
 DD_MODE_THRESHOLD = 0
 DD_MODE_MOCK_AR = 1
+DD_MODE_TOPK = 2
+DD_MODE_STEPS = 3
+
+
+def DD_MODE_PARAM(mode: int, param: int) -> int:
+    """A commit mode with its parameter (k for top-k, N for fixed steps)."""
+    return mode | (param << 8)
 
 c_int32 = ctypes.c_int32
 c_void_p = ctypes.c_void_p

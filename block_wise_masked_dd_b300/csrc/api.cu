@@ -125,6 +125,15 @@ T* at(uint8_t* ws, size_t off) {
   return reinterpret_cast<T*>(ws + off);
 }
 
+// Commit mode: threshold or mock-AR with no parameter; top-k or fixed steps
+// with a parameter (k or N) in [1, 65535] in bits 8 and up.
+bool valid_mode(int32_t mode) {
+  const int base = mode & 0xFF, param = (int)((uint32_t)mode >> 8);
+  if (base == DD_MODE_THRESHOLD || base == DD_MODE_MOCK_AR) return param == 0;
+  if (base == DD_MODE_TOPK || base == DD_MODE_STEPS) return param >= 1 && param <= 65535;
+  return false;
+}
+
 dd_status check_config(const dd_config* c) {
   if (!c) return fail(DD_ERR_INVALID_ARG, "config is NULL");
   if (c->batch < 1 || c->block < 1 || c->block > 32)
@@ -565,7 +574,7 @@ dd_status dd_denoise_step(dd_ctx* c, int32_t* tokens, uint32_t* mask, float gamm
   dd_status s = check_ctx(c);
   if (s != DD_OK) return s;
   if (!tokens || !mask) return fail(DD_ERR_INVALID_ARG, "tokens/mask is NULL");
-  if (mode != DD_MODE_THRESHOLD && mode != DD_MODE_MOCK_AR) return fail(DD_ERR_INVALID_ARG, "bad mode %d", mode);
+  if (!valid_mode(mode)) return fail(DD_ERR_INVALID_ARG, "bad mode %d", mode);
   if (!(gamma == gamma)) return fail(DD_ERR_INVALID_ARG, "gamma is NaN");
   s = ensure_graph(c);
   if (s != DD_OK) return s;
@@ -588,7 +597,7 @@ dd_status dd_denoise_step_probe(dd_ctx* c, int32_t* tokens, uint32_t* mask, floa
   dd_status s = check_ctx(c);
   if (s != DD_OK) return s;
   if (!tokens || !mask) return fail(DD_ERR_INVALID_ARG, "tokens/mask is NULL");
-  if (mode != DD_MODE_THRESHOLD && mode != DD_MODE_MOCK_AR) return fail(DD_ERR_INVALID_ARG, "bad mode %d", mode);
+  if (!valid_mode(mode)) return fail(DD_ERR_INVALID_ARG, "bad mode %d", mode);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const dd_config& cf = c->cfg;
   uint8_t* ws = c->ws;
@@ -609,7 +618,7 @@ dd_status dd_decode_block(dd_ctx* c, int32_t* tokens, float gamma, int32_t mode,
   dd_status s = check_ctx(c);
   if (s != DD_OK) return s;
   if (!tokens) return fail(DD_ERR_INVALID_ARG, "tokens is NULL");
-  if (mode != DD_MODE_THRESHOLD && mode != DD_MODE_MOCK_AR) return fail(DD_ERR_INVALID_ARG, "bad mode %d", mode);
+  if (!valid_mode(mode)) return fail(DD_ERR_INVALID_ARG, "bad mode %d", mode);
   if (!(gamma == gamma)) return fail(DD_ERR_INVALID_ARG, "gamma is NaN");
   s = ensure_graph(c);
   if (s != DD_OK) return s;
@@ -682,7 +691,7 @@ dd_status dd_profile_step(dd_ctx* c, int32_t* tokens, uint32_t* mask, float gamm
   dd_status s = check_ctx(c);
   if (s != DD_OK) return s;
   if (!tokens || !mask || !times_ms || !kinds || !n || cap < 1) return fail(DD_ERR_INVALID_ARG, "bad profile arguments");
-  if (mode != DD_MODE_THRESHOLD && mode != DD_MODE_MOCK_AR) return fail(DD_ERR_INVALID_ARG, "bad mode %d", mode);
+  if (!valid_mode(mode)) return fail(DD_ERR_INVALID_ARG, "bad mode %d", mode);
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const dd_config& cf = c->cfg;
   uint8_t* ws = c->ws;
@@ -863,7 +872,7 @@ dd_status dd_commit(int32_t batch, int32_t block, const float* conf, const int32
                     void* stream) {
   if (batch < 1 || block < 1 || block > 32) return fail(DD_ERR_INVALID_ARG, "bad batch/block");
   if (!conf || !arg || !tokens || !mask || !remaining) return fail(DD_ERR_INVALID_ARG, "null pointer");
-  if (mode != DD_MODE_THRESHOLD && mode != DD_MODE_MOCK_AR) return fail(DD_ERR_INVALID_ARG, "bad mode %d", mode);
+  if (!valid_mode(mode)) return fail(DD_ERR_INVALID_ARG, "bad mode %d", mode);
   DD_CUDA(dd::launch_commit(conf, arg, tokens, mask, nullptr, gamma, mode, n_committed, remaining, batch, block,
                             static_cast<cudaStream_t>(stream)));
   return DD_OK;

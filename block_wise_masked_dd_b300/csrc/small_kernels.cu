@@ -269,10 +269,25 @@ __global__ void k_select_combine(const float* sel_m, const float* sel_s, const i
   }
 }
 
+// Positions the fixed-steps schedule commits when `left` of a block of S are
+// masked: the schedule commits ceil(left_t / (N - t)) at its step t, so the
+// block fills in N steps; t is the first step whose count is at most `left`.
+__device__ int steps_schedule_k(int S, int N, int left) {
+  int rem = S, t = 0;
+  while (rem > left && t < N) {
+    rem -= (rem + (N - t) - 1) / (N - t);
+    ++t;
+  }
+  const int steps_left = N - t;
+  return steps_left <= 0 ? left : (left + steps_left - 1) / steps_left;
+}
+
 // Commit rule, one warp per sequence, lane i = block position i (S <= 32).
-// Threshold mode: every masked position with conf >= gamma; if none, the
-// masked position of highest confidence (lowest position on ties).
-// Mock-AR mode: the lowest masked position.  Writes the remaining masked
+// The mode's low byte selects the rule and its upper bits carry k or N.
+// Threshold: every masked position with conf >= gamma; if none, the masked
+// position of highest confidence (lowest position on ties).  Mock-AR: the
+// lowest masked position.  Top-k: the k most confident masked positions.
+// Fixed steps: top-k with k from steps_schedule_k.  Writes the remaining masked
 // count over all sequences to remaining[0].
 __global__ void k_commit(const float* conf, const int* arg, int32_t* tokens, uint32_t* mask, const float* params,
                          float gamma_arg, int mode_arg, int32_t* n_committed, int32_t* remaining, int B, int S) {
@@ -289,8 +304,18 @@ __global__ void k_commit(const float* conf, const int* arg, int32_t* tokens, uin
     const bool masked = lane < S && ((mk >> lane) & 1u);
     const float c = lane < S ? conf[b * S + lane] : 0.f;
     uint32_t chosen = 0;
+    const int base = mode & 0xFF, param = mode >> 8;
     if (mk != 0) {
-      if (mode == 1) {
+      if (base == 2 || base == 3) {
+        // top-k: the k most confident masked positions (ties: lower position)
+        const int k = base == 2 ? param : steps_schedule_k(S, param, __popc(mk));
+        int rank = 0;
+        for (int j = 0; j < S; ++j) {
+          const float cj = __shfl_sync(0xffffffffu, c, j);
+          rank += (((mk >> j) & 1u) && (cj > c || (cj == c && j < lane))) ? 1 : 0;
+        }
+        chosen = __ballot_sync(0xffffffffu, masked && rank < k);
+      } else if (base == 1) {
         chosen = mk & (~mk + 1u);  // lowest set bit
       } else {
         chosen = __ballot_sync(0xffffffffu, masked && c >= gamma);

@@ -11,6 +11,9 @@ from . import binding as B
 
 MODE_THRESHOLD = B.DD_MODE_THRESHOLD
 MODE_MOCK_AR = B.DD_MODE_MOCK_AR
+MODE_TOPK = B.DD_MODE_TOPK
+MODE_STEPS = B.DD_MODE_STEPS
+mode_param = B.DD_MODE_PARAM
 
 
 def _stream(stream=None) -> int:

@@ -1,6 +1,7 @@
 """Committed tokens/s for every decode workload, gamma and commit mode.
 
     python -m block_wise_masked_dd_b300.sweep [--configs tiny small large] [--steps K] [--warmup W]
+                                              [--modes mock_ar topk:2 steps:8]
 
 Runs `bench.py` once per (workload, gamma, mode) in a fresh process (so each
 measurement sees a fresh context and its own clock record), and prints one
@@ -23,10 +24,12 @@ def main():
     ap.add_argument("--configs", nargs="+", default=["tiny", "small", "large"])
     ap.add_argument("--steps", type=int, default=3)
     ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--modes", nargs="+", default=["mock_ar", "topk:2", "steps:8"],
+                    help="commit modes run besides the threshold rule at each gamma")
     args = ap.parse_args()
     rows = []
     for cfg in args.configs:
-        for gamma, mode in [(g, "threshold") for g in GAMMAS] + [(0.8, "mock_ar")]:
+        for gamma, mode in [(g, "threshold") for g in GAMMAS] + [(0.8, m) for m in args.modes]:
             cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--config", cfg, "--gamma", str(gamma), "--mode",
                    mode, "--steps", str(args.steps), "--warmup", str(args.warmup), "--no-micro", "--no-cpu"]
             out = subprocess.run(cmd, capture_output=True, text=True, cwd=ROOT)

@@ -57,10 +57,20 @@ typedef enum dd_status {
   DD_ERR_UNSUPPORTED = 6     /* shape outside what the kernels implement */
 } dd_status;
 
+/* Commit modes (the `mode` argument of the step and decode calls).  Top-k and
+ * fixed steps carry a parameter in bits 8 and up: DD_MODE_PARAM(DD_MODE_TOPK, k)
+ * or DD_MODE_PARAM(DD_MODE_STEPS, N), 1 <= k, N <= 65535; gamma is ignored by
+ * mock-AR, top-k and fixed steps. */
 enum {
   DD_MODE_THRESHOLD = 0, /* commit masked positions with confidence >= gamma (fallback: the most confident one) */
-  DD_MODE_MOCK_AR = 1    /* commit the leftmost masked position each step (one token per step) */
+  DD_MODE_MOCK_AR = 1,   /* commit the leftmost masked position each step (one token per step) */
+  DD_MODE_TOPK = 2,      /* commit the k most confident masked positions (the explainer's "adopt the top few"
+                          * alternative, prednext.com "拡散言語モデルで推論するには" step 3); ties: lower position */
+  DD_MODE_STEPS = 3      /* fixed-steps schedule: with r positions masked after t steps, commit the
+                          * ceil(r / (N - t)) most confident, so a block fills in N steps (N <= block);
+                          * t is recovered from r by replaying the schedule from the full block */
 };
+#define DD_MODE_PARAM(mode, param) ((int32_t)((mode) | ((param) << 8)))
 
 /* Model and batch shape.  Supported: 1 <= block <= 32 with batch*block a
  * multiple of 16; head_dim 64 or 128; (n_q_heads/n_kv_heads)*block a multiple

@@ -20,7 +20,9 @@ Parity status of each function:
 """
 from .decode import (  # noqa: F401
     MODE_MOCK_AR,
+    MODE_STEPS,
     MODE_THRESHOLD,
+    MODE_TOPK,
     OracleModel,
     StepResult,
     block_attention,
@@ -33,5 +35,7 @@ from .decode import (  # noqa: F401
     rmsnorm,
     round_bf16,
     select_from_logits,
+    steps_schedule_k,
+    with_param,
     silu,
 )

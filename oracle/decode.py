@@ -45,6 +45,29 @@ import numpy as np
 
 MODE_THRESHOLD = 0
 MODE_MOCK_AR = 1
+MODE_TOPK = 2     # with k: commit the k most confident masked positions
+MODE_STEPS = 3    # with N: the fixed-steps schedule (N denoising steps per block)
+
+
+def with_param(mode: int, param: int) -> int:
+    """A commit mode with its parameter (k or N) in bits 8 and up."""
+    return mode | (param << 8)
+
+
+def steps_schedule_k(block: int, n_steps: int, left: int) -> int:
+    """Positions the fixed-steps schedule commits when `left` are masked.
+
+    The schedule starts from `block` masked positions and at its step t
+    commits ceil(left_t / (N - t)), so the block fills in exactly N steps
+    (N <= block).  The step index is not carried: t is the first step of the
+    schedule whose count is at most `left`.
+    """
+    rem, t = block, 0
+    while rem > left and t < n_steps:
+        rem -= -(-rem // (n_steps - t))
+        t += 1
+    steps_left = n_steps - t
+    return left if steps_left <= 0 else -(-left // steps_left)
 
 F32 = np.float32
 
@@ -148,6 +171,12 @@ def commit(conf, arg, tokens, mask, gamma: float, mode: int, block: int):
     """Commit rule for one step, per sequence (explainer steps 3-4; mock-AR from
     the TwoTower news page).
 
+    Threshold: every masked position with conf >= gamma, else the most
+    confident one.  Mock-AR: the leftmost masked position.  Top-k (the
+    explainer's alternative of forcibly adopting the top few): the k most
+    confident masked positions.  Fixed steps: top-k with k from
+    `steps_schedule_k`.  Confidence ties go to the lower position.
+
     conf, arg  [B, S]       tokens [B, S] int32 (updated copy returned)
     mask       [B] uint32, bit i set = position i still [MASK]
     Returns (tokens, mask, n_committed [B] int32, fallback [B] bool) where
@@ -163,7 +192,12 @@ def commit(conf, arg, tokens, mask, gamma: float, mode: int, block: int):
         masked = [i for i in range(block) if (int(mask[b]) >> i) & 1]
         if not masked:
             continue
-        if mode == MODE_MOCK_AR:
+        base, param = mode & 0xFF, mode >> 8
+        if base in (MODE_TOPK, MODE_STEPS):
+            k = param if base == MODE_TOPK else steps_schedule_k(block, param, len(masked))
+            ranked = sorted(masked, key=lambda i: (-float(F32(conf[b, i])), i))
+            chosen = sorted(ranked[:k])
+        elif mode == MODE_MOCK_AR:
             chosen = [masked[0]]
         else:
             chosen = [i for i in masked if F32(conf[b, i]) >= g]
@@ -270,6 +304,18 @@ def denoise_step(model: OracleModel, tokens, mask, gamma: float, mode: int = MOD
             for i in masked:
                 if c[0] - float(conf[b, i]) < TIE_CONF_GAP:
                     tie[b, i] = True
+    # Top-k and fixed-steps: the cut between the k-th and (k+1)-th most
+    # confident masked positions is fragile when their confidences nearly tie.
+    base = mode & 0xFF
+    if base in (MODE_TOPK, MODE_STEPS):
+        for b in range(B):
+            masked = [i for i in range(S) if (int(mask[b]) >> i) & 1]
+            k = (mode >> 8) if base == MODE_TOPK else steps_schedule_k(S, mode >> 8, len(masked))
+            c = sorted((float(conf[b, i]) for i in masked), reverse=True)
+            if 0 < k < len(c) and c[k - 1] - c[k] < TIE_CONF_GAP:
+                for i in masked:
+                    if min(abs(float(conf[b, i]) - c[k - 1]), abs(float(conf[b, i]) - c[k])) < TIE_CONF_GAP:
+                        tie[b, i] = True
     return StepResult(new_tok, new_mask, n, conf, arg, logits if keep_intermediates else None,
                       tie, fallback, attn_outs, hf if keep_intermediates else None)
 

@@ -10,6 +10,14 @@ def _kv(tokens):
     return dict(t.split("=", 1) for t in tokens)
 
 
+def mode_code(name: str) -> int:
+    """threshold | mock_ar | topk:k | steps:N -> the library's mode value."""
+    if name in ("threshold", "mock_ar"):
+        return 0 if name == "threshold" else 1
+    kind, _, val = name.partition(":")
+    return {"topk": 2, "steps": 3}[kind] | (int(val) << 8)
+
+
 def commit_cases():
     """Yield dicts: name, gamma, mode (0 threshold / 1 mock-AR), mask, conf [16],
     committed (list of positions), mask_after."""
@@ -18,7 +26,7 @@ def commit_cases():
         head, conf, expect = lines[i].split(), lines[i + 1].split(), lines[i + 2].split()
         assert head[0] == "case" and conf[0] == "conf" and expect[0] == "expect"
         h, e = _kv(head[2:]), _kv(expect[1:])
-        yield {"name": head[1], "gamma": float(h["gamma"]), "mode": 1 if h["mode"] == "mock_ar" else 0,
+        yield {"name": head[1], "gamma": float(h["gamma"]), "mode": mode_code(h["mode"]),
                "mask": int(h["mask"], 16), "conf": np.array([float(v) for v in conf[1:]], np.float32),
                "committed": [] if e["committed"] == "-" else [int(v) for v in e["committed"].split(",")],
                "mask_after": int(e["mask"], 16)}

@@ -143,8 +143,11 @@ def test_lmhead_select_equal_logits():
 # ------------------------------------------------------------------ commit
 
 @pytest.mark.parametrize("gamma", [0.0, 0.5, 0.8, 0.95, 1.5])
-@pytest.mark.parametrize("mode", [0, 1])
+@pytest.mark.parametrize("mode", [0, 1, 2 | (1 << 8), 2 | (3 << 8), 2 | (16 << 8), 3 | (1 << 8), 3 | (5 << 8),
+                                  3 | (16 << 8)])
 def test_commit_bit_exact(gamma, mode):
+    """Every commit mode (threshold, mock-AR, top-k with k = 1, 3, 16, fixed
+    steps with N = 1, 5, 16) against the oracle's rule, bit-exact."""
     from block_wise_masked_dd_b300.decoder import commit
     rng = np.random.default_rng(int(gamma * 100) + mode)
     B, S = 64, 16

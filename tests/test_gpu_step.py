@@ -149,3 +149,20 @@ def test_decode_block_runs_the_device_side_loop(small):
     torch.cuda.synchronize()
     assert n == steps
     assert (t.cpu().numpy() == tokens.cpu().numpy()).all()
+
+
+@pytest.mark.parametrize("mode", [oracle.with_param(oracle.MODE_TOPK, 3), oracle.with_param(oracle.MODE_STEPS, 5)])
+def test_tiny_state_synced_topk_and_fixed_steps(tiny, mode):
+    tok, mask = tiny.start_state()
+    steps = 0
+    while mask.max():
+        tok, mask, _, _ = compare_step(tiny, tok, mask, 0.8, mode)
+        steps += 1
+        assert steps <= 16
+    assert steps == (6 if (mode & 0xFF) == oracle.MODE_TOPK else 5)
+
+
+@pytest.mark.parametrize("N", [1, 4, 16])
+def test_decode_block_fixed_steps(small, N):
+    _, steps = small.dec.decode_block(0.8, oracle.with_param(oracle.MODE_STEPS, N))
+    assert steps == N

@@ -14,7 +14,9 @@ import pytest
 import oracle
 import oracle.decode as od
 import synth
+from tests import test_golden
 from tests import test_oracle_pins as pins
+from tests.golden_io import commit_cases
 
 # (function, [(old source text, new source text), ...])
 MUTANTS = {
@@ -46,6 +48,10 @@ MUTANTS = {
     "step_without_positions": ("denoise_step", [(' + w["pos"][None, :, :]', "")]),
     "step_transposed_wq": ("denoise_step", [('y @ w[f"wq{l}"].T', 'y @ w[f"wq{l}"]')]),
     "step_mlp_norm_gain_from_attention": ("denoise_step", [('w[f"g_mlp{l}"]', 'w[f"g_attn{l}"]')]),
+    "topk_ties_to_higher_position": ("commit", [("key=lambda i: (-float(F32(conf[b, i])), i)",
+                                                 "key=lambda i: (-float(F32(conf[b, i])), -i)")]),
+    "topk_takes_one_more": ("commit", [("chosen = sorted(ranked[:k])", "chosen = sorted(ranked[:k + 1])")]),
+    "steps_schedule_off_by_one": ("steps_schedule_k", [("steps_left = n_steps - t\n", "steps_left = n_steps - t + 1\n")]),
 }
 
 
@@ -84,11 +90,20 @@ def _pins(tiny):
         pins.test_commit_exhaustive_masks,
         pins.test_commit_gamma_zero_and_above_one,
         pins.test_commit_monotone_in_gamma,
+        _golden_commit_cases,
+        lambda: pins.test_steps_schedule_fills_block_in_n_steps(16),
+        pins.test_commit_topk_exhaustive_masks,
         lambda: pins.test_full_step_vs_bruteforce(False),
         pins.test_full_step_vs_bruteforce_random_gains,
         lambda: pins.test_decode_mock_ar_is_left_to_right(tiny),
         lambda: pins.test_decode_committed_never_change_and_progress(tiny),
+        lambda: pins.test_decode_topk_and_fixed_steps(tiny),
     ]
+
+
+def _golden_commit_cases():
+    for case in commit_cases():
+        test_golden.test_commit_rule_cases(case)
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))

@@ -345,3 +345,55 @@ def test_batch_independence(tiny_model):
                                  tiny_model.ctx_len)
         tok_one, _, _ = oracle.decode_block(one, 0.8)
         assert (tok_one[0] == tok_all[b]).all()
+
+
+# ------------------------------------------------- top-k and fixed steps
+
+def test_commit_topk_exhaustive_masks():
+    """Top-k over every mask of a 16-position block: the committed set is the
+    k masked positions that precede every other masked position in the order
+    (higher confidence first, lower position on equal confidence)."""
+    S = 16
+    conf = np.array([[0.5, 0.9, 0.1, 0.9, 0.3, 0.7, 0.7, 0.2, 0.05, 0.6, 0.9, 0.4, 0.35, 0.8, 0.15, 0.7]], F32)
+    arg = np.arange(S, dtype=np.int32).reshape(1, S) + 1000
+    for k in (1, 3, 16):
+        mode = oracle.with_param(oracle.MODE_TOPK, k)
+        for mk in range(1 << S):
+            tok0 = np.zeros((1, S), np.int32)
+            tok, m, n, _ = oracle.commit(conf, arg, tok0, np.array([mk], np.uint32), 0.8, mode, S)
+            masked = [i for i in range(S) if (mk >> i) & 1]
+            chosen = [i for i in masked if not (int(m[0]) >> i) & 1]
+            assert len(chosen) == min(k, len(masked)) and int(n[0]) == len(chosen)
+            rest = [j for j in masked if j not in chosen]
+            for i in chosen:
+                assert tok[0, i] == 1000 + i
+                for j in rest:
+                    assert conf[0, i] > conf[0, j] or (conf[0, i] == conf[0, j] and i < j)
+
+
+@pytest.mark.parametrize("S", [1, 5, 16, 32])
+def test_steps_schedule_fills_block_in_n_steps(S):
+    for N in range(1, S + 4):
+        left, steps = S, 0
+        while left:
+            k = oracle.steps_schedule_k(S, N, left)
+            assert 1 <= k <= left
+            left -= k
+            steps += 1
+        assert steps == min(N, S)
+
+
+def test_decode_topk_and_fixed_steps(tiny_model):
+    _, steps, hist = oracle.decode_block(tiny_model, 0.8, oracle.with_param(oracle.MODE_TOPK, 3))
+    assert steps == 6 and all((h == 3).all() for h in hist[:5]) and (hist[5] == 1).all()
+    for N in (1, 5, 16):
+        _, steps, _ = oracle.decode_block(tiny_model, 0.8, oracle.with_param(oracle.MODE_STEPS, N))
+        assert steps == N
+
+
+def test_decode_top1_equals_gamma_above_one(tiny_model):
+    """Top-1 commits the single most confident masked position every step,
+    which is what the threshold rule does when no confidence can reach gamma."""
+    a, sa, _ = oracle.decode_block(tiny_model, 0.8, oracle.with_param(oracle.MODE_TOPK, 1))
+    b, sb, _ = oracle.decode_block(tiny_model, 1.01)
+    assert sa == sb == 16 and (a == b).all()
