@@ -83,6 +83,18 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t planes, uint64_t row
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_map_q(CUtensorMap* m, const void* qkv, uint64_t rows, uint64_t ld, int Hq, int D, int G, int S) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hq, rows};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, ld * 2};
+  cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)S};
+  cuuint32_t es[3] = {1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(qkv), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace dd
 
 // ---------------------------------------------------------------------------
@@ -107,7 +119,7 @@ struct dd_ctx {
   bool have_weights;
   dd_weights w;
   std::vector<CUtensorMap> m_wqkv, m_wo, m_wgu, m_wd;
-  CUtensorMap m_lm, m_y_b, m_attn_b, m_h_b, m_y_a, m_kc, m_vc, m_kc128, m_vc128;
+  CUtensorMap m_lm, m_y_b, m_attn_b, m_h_b, m_y_a, m_kc, m_vc, m_kc128, m_vc128, m_q;
   cudaStream_t cap_stream;
   cudaGraphExec_t exec;       // one denoising step
   cudaGraphExec_t loop_exec;  // while (masked left): step  -- the device-side decode loop
@@ -295,7 +307,7 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)cf.head_dim);
     a.status = status;
     a.timeout_ns = c->timeout_ns;
-    DD_CUDA(dd::launch_attention(L.p_attn, a, c->m_kc, c->m_vc, c->m_kc128, c->m_vc128, st));
+    DD_CUDA(dd::launch_attention(L.p_attn, a, c->m_kc, c->m_vc, c->m_kc128, c->m_vc128, c->m_q, st));
     mk(kKAttention);
     if (L.p_attn.use_tc || L.p_attn.n_splits > 1) {
       DD_CUDA(dd::launch_attention_combine(L.p_attn, a, st));
@@ -498,7 +510,8 @@ dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_byte
             dd::make_map_2d(&c->m_y_b, c->ws + L.y, 2 * c->R, cf.hidden, L.p_qkv.BN) &&
             dd::make_map_2d(&c->m_attn_b, c->ws + L.attn, 2 * c->R, c->HqD, L.p_o.BN) &&
             dd::make_map_2d(&c->m_h_b, c->ws + L.hmid, 2 * c->R, cf.mlp, L.p_d.BN) &&
-            dd::make_map_2d(&c->m_y_a, c->ws + L.y, 2 * c->R, cf.hidden, 128);
+            dd::make_map_2d(&c->m_y_a, c->ws + L.y, 2 * c->R, cf.hidden, 128) &&
+            dd::make_map_q(&c->m_q, c->ws + L.qkv, 2 * c->R, c->qkvw, cf.n_q_heads, cf.head_dim, c->G, cf.block);
   if (!ok) {
     dd_destroy(c);
     return fail(DD_ERR_CUDA, "tensor map encoding failed for the workspace buffers");
@@ -793,7 +806,10 @@ dd_status dd_block_attention(const dd_attn_problem* p, void* stream) {
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)p->head_dim);
   a.status = small + 1;
   a.timeout_ns = dd::kDefaultTimeoutNs;
-  DD_CUDA(dd::launch_attention(plan, a, mk, mv, mk128, mv128, st));
+  CUtensorMap mq;
+  if (!dd::make_map_q(&mq, p->qkv, (uint64_t)p->batch * p->block, a.ld_qkv, p->n_q_heads, p->head_dim, a.G, p->block))
+    return fail(DD_ERR_CUDA, "tensor map encoding failed for qkv");
+  DD_CUDA(dd::launch_attention(plan, a, mk, mv, mk128, mv128, mq, st));
   DD_CUDA(dd::launch_attention_combine(plan, a, st));
   return DD_OK;
 }

@@ -736,10 +736,11 @@ size_t attention_partial_bytes(const AttnPlan& p, int B, int Hkv) {
 }
 
 cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a_in, const CUtensorMap& map_k, const CUtensorMap& map_v,
-                             const CUtensorMap& map_k128, const CUtensorMap& map_v128, cudaStream_t st) {
+                             const CUtensorMap& map_k128, const CUtensorMap& map_v128, const CUtensorMap& map_q,
+                             cudaStream_t st) {
   AttnArgs a = a_in;
   // tcgen05 path: context splits only; the block keys join in the merge
-  if (p.use_tc) return launch_attention_tc(a, p.n_ctx, p.n_splits, map_k128, map_v128, st);
+  if (p.use_tc) return launch_attention_tc(a, p.n_ctx, map_k128, map_v128, map_q, st);
   if (p.D == 128) {
     if (a.split) launch_attn_kernel<128, true>(p, a, p.n_splits, map_k, map_v, st);
     else launch_attn_kernel<128, false>(p, a, p.n_splits, map_k, map_v, st);

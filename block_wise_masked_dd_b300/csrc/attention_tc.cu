@@ -16,9 +16,10 @@
 // Each tile's O lands in a fresh TMEM buffer and is folded into registers
 // with the running rescale.
 //
-// Roles (192 threads): warp 0 streams K and V tiles with TMA (two slots each;
-// K released after QK^T, V after PV), warp 1 owns TMEM and issues the MMAs,
-// warps 2-5 run the softmax and fold the outputs.  Every mbarrier wait is
+// Roles (192 threads): warp 0 streams Q (double-buffered, one per work item)
+// and the K and V tiles with TMA (two slots each; K released after QK^T, V
+// after PV), warp 1 owns TMEM and issues the MMAs, warps 2-5 run the softmax,
+// fold the outputs and write each item's partial.  Every mbarrier wait is
 // bounded.
 #include <math.h>
 
@@ -40,12 +41,11 @@ constexpr int kP = 2 * kRowBox;          // P head or remainder [64][128 keys]: 
 constexpr int kThreads = 192;
 constexpr int kOffK = 0;                 // 2 K slots
 constexpr int kOffV = 2 * kKV;           // 2 V slots
-constexpr int kOffQh = 4 * kKV;
-constexpr int kOffQl = kOffQh + kQ;
-constexpr int kOffPh = kOffQl + kQ;
+constexpr int kOffQ = 4 * kKV;           // 2 Q buffers, each a head then a remainder
+constexpr int kOffPh = kOffQ + 4 * kQ;
 constexpr int kOffPl = kOffPh + kP;
 constexpr int kOffBar = kOffPl + kP;
-constexpr int kNumBars = 19;
+constexpr int kNumBars = 23;
 constexpr int kSmemBytes = 1024 + kOffBar + kNumBars * 8 + 16;
 constexpr uint32_t kTmemCols = 512;      // S x2 (128 cols each), O x2 (128 cols each)
 
@@ -101,10 +101,17 @@ __device__ __forceinline__ float ex2(float x) {
   return y;
 }
 
+// Persistent: CTA c takes the work items c, c + gridDim.x, ... where item w
+// is context split w % n_ctx of the (sequence, kv head) pair w / n_ctx.  The
+// producer streams the next item's Q and K/V tiles while the softmax warps
+// still fold and write the previous item, so an SM pays the pipeline fill
+// once rather than once per item.  Q arrives by TMA from the q|k|v rows with
+// the box {64 dims, G heads, S positions}, i.e. in row order i * G + g; the
+// partials are written in the order g * S + i that the merge kernels read.
 template <bool SPLITQ>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_ctx_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                  const AttnArgs a, int n_ctx_splits, int n_slots) {
+                  const __grid_constant__ CUtensorMap map_q, const AttnArgs a, int n_ctx, int n_items) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -119,19 +126,25 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* ofull = bars + 14;
   uint64_t* ofree = bars + 16;
   uint64_t* drain = bars + 18;
+  uint64_t* qfull = bars + 19;
+  uint64_t* qempty = bars + 21;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
   const int warp = warp_id(), lane = lane_id();
   const int T = *a.ctx_len;
   const int ntiles_all = (T + kKT - 1) / kKT;
-  const int per = (ntiles_all + n_ctx_splits - 1) / n_ctx_splits;
-  const int tile0 = split * per;
-  const int nt = max(0, min(ntiles_all, tile0 + per) - tile0);
-  const int z = a.z0 + b * a.Hkv + kvh;
+  const int per = (ntiles_all + n_ctx - 1) / n_ctx;
   const int R = a.B * a.S;
-  const __nv_bfloat16* qkv = reinterpret_cast<const __nv_bfloat16*>(a.qkv);
+  // item w -> (split, kv head, sequence, first tile, tile count)
+  auto item = [&](int w, int& split, int& kvh, int& b, int& tile0, int& nt) {
+    split = w % n_ctx;
+    const int pair = w / n_ctx;
+    kvh = pair % a.Hkv;
+    b = pair / a.Hkv;
+    tile0 = split * per;
+    nt = max(0, min(ntiles_all, tile0 + per) - tile0);
+  };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -143,58 +156,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&sfree[i], 4);
       mbar_init(&ofull[i], 1);
       mbar_init(&ofree[i], 4);
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], 1);
     }
     mbar_init(pfull, 4);
     mbar_init(pfree, 1);
     mbar_init(drain, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    // The context K/V do not depend on the preceding kernel: the first two
-    // tiles go out before waiting for it (programmatic dependent launch).
-    for (int t = 0; t < min(nt, 2); ++t) {
-      const int key0 = (tile0 + t) * kKT;
-      mbar_arrive_expect_tx(&kfull[t], kKV);
-      tma_load_3d(smem + kOffK + t * kKV, &map_k, &kfull[t], 0, key0, z);
-      tma_load_3d(smem + kOffK + t * kKV + kBox, &map_k, &kfull[t], 64, key0, z);
-      mbar_arrive_expect_tx(&vfull[t], kKV);
-      tma_load_3d(smem + kOffV + t * kKV, &map_v, &vfull[t], 0, key0, z);
-      tma_load_3d(smem + kOffV + t * kKV + kBox, &map_v, &vfull[t], 64, key0, z);
-    }
+    tma_prefetch_desc(&map_k);
+    tma_prefetch_desc(&map_v);
+    tma_prefetch_desc(&map_q);
   }
-  pdl_wait();  // q comes from the preceding kernel
-  pdl_launch_dependents();
-  // Stage Q (64 rows: row r = (g, i) -> query head kvh*G + g, position i) as
-  // a K-major swizzled operand; with SPLITQ also the remainder rows.
-  {
-    // All of this thread's 16-byte loads are issued before any is stored, so
-    // their latencies overlap.
-    constexpr int kChunks = (SPLITQ ? 2 : 1) * kNQ * (kD / 8);
-    constexpr int kPer = (kChunks + kThreads - 1) / kThreads;
-    uint4 v[kPer];
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int c = threadIdx.x + j * kThreads;
-      if (c < kChunks) {
-        const int half = c / (kNQ * (kD / 8));
-        const int cc = c % (kNQ * (kD / 8));
-        const int r = cc / (kD / 8), col = (cc % (kD / 8)) * 8;
-        const int g = r / a.S, i = r % a.S;
-        const long long row = (long long)(half ? R : 0) + b * a.S + i;
-        v[j] = *reinterpret_cast<const uint4*>(qkv + row * a.ld_qkv + (kvh * a.G + g) * kD + col);
-      }
-    }
-#pragma unroll
-    for (int j = 0; j < kPer; ++j) {
-      const int c = threadIdx.x + j * kThreads;
-      if (c < kChunks) {
-        const int half = c / (kNQ * (kD / 8));
-        const int cc = c % (kNQ * (kD / 8));
-        const int r = cc / (kD / 8), col = (cc % (kD / 8)) * 8;
-        *reinterpret_cast<uint4*>(smem + (half ? kOffQl : kOffQh) + swz(kNQ, r, col)) = v[j];
-      }
-    }
-  }
-  fence_proxy_async_smem();
   if (warp == 1) {
     tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
@@ -208,18 +181,46 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
-      for (int t = 2; t < nt; ++t) {  // tiles 0 and 1 were issued in the prologue
-        const int s = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        const int key0 = (tile0 + t) * kKT;
-        if (!mbar_wait_bounded(&kempty[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) break;
+      auto load_kv = [&](int g, int key0, int z) {
+        const int s = g & 1;
+        const uint32_t ph = (g >> 1) & 1;
+        if (!mbar_wait_bounded(&kempty[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) return false;
         mbar_arrive_expect_tx(&kfull[s], kKV);
         tma_load_3d(smem + kOffK + s * kKV, &map_k, &kfull[s], 0, key0, z);
         tma_load_3d(smem + kOffK + s * kKV + kBox, &map_k, &kfull[s], 64, key0, z);
-        if (!mbar_wait_bounded(&vempty[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) break;
+        if (!mbar_wait_bounded(&vempty[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) return false;
         mbar_arrive_expect_tx(&vfull[s], kKV);
         tma_load_3d(smem + kOffV + s * kKV, &map_v, &vfull[s], 0, key0, z);
         tma_load_3d(smem + kOffV + s * kKV + kBox, &map_v, &vfull[s], 64, key0, z);
+        return true;
+      };
+      // The context K/V do not depend on the preceding kernel: the first
+      // item's first two tiles go out before waiting for it (programmatic
+      // dependent launch); q does, so its load waits.
+      int split, kvh, b, tile0, nt;
+      int pre = 0;
+      bool ok = true;
+      if ((int)blockIdx.x < n_items) {
+        item(blockIdx.x, split, kvh, b, tile0, nt);
+        for (; pre < min(nt, 2) && ok; ++pre) ok = load_kv(pre, (tile0 + pre) * kKT, a.z0 + b * a.Hkv + kvh);
+      }
+      pdl_wait();
+      pdl_launch_dependents();
+      int g = 0;
+      for (int w = blockIdx.x, it = 0; w < n_items && ok; w += gridDim.x, ++it) {
+        item(w, split, kvh, b, tile0, nt);
+        const int qb = it & 1;
+        if (!mbar_wait_bounded(&qempty[qb], ((it >> 1) & 1) ^ 1, a.timeout_ns, abort_flag, a.status)) break;
+        uint8_t* q = smem + kOffQ + qb * 2 * kQ;
+        mbar_arrive_expect_tx(&qfull[qb], (SPLITQ ? 2 : 1) * kQ);
+        tma_load_3d(q, &map_q, &qfull[qb], 0, kvh * a.G, b * a.S);
+        tma_load_3d(q + kRowBox, &map_q, &qfull[qb], 64, kvh * a.G, b * a.S);
+        if (SPLITQ) {
+          tma_load_3d(q + kQ, &map_q, &qfull[qb], 0, kvh * a.G, R + b * a.S);
+          tma_load_3d(q + kQ + kRowBox, &map_q, &qfull[qb], 64, kvh * a.G, R + b * a.S);
+        }
+        for (int t = 0; t < nt && ok; ++t, ++g)
+          if (g >= pre) ok = load_kv(g, (tile0 + t) * kKT, a.z0 + b * a.Hkv + kvh);
       }
     }
     __syncwarp();
@@ -228,7 +229,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) {
       const uint32_t idesc_qk = idesc_bf16_f32(kNQ, kKT);
       const uint32_t idesc_pv = idesc_bf16_f32(kNQ, kD) | (1u << 16);  // B (V) MN-major
-      const uint32_t qh = smem_u32(smem + kOffQh), ql = smem_u32(smem + kOffQl);
       const uint32_t p_h = smem_u32(smem + kOffPh), p_l = smem_u32(smem + kOffPl);
       bool ok = true;
       auto issue_pv = [&](int u) {
@@ -256,32 +256,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_commit(pfree);
         return true;
       };
-      for (int t = 0; t < nt && ok; ++t) {
-        const int s = t & 1;
-        const uint32_t ph = (t >> 1) & 1;
-        if (!mbar_wait_bounded(&kfull[s], ph, a.timeout_ns, abort_flag, a.status)) { ok = false; break; }
-        if (!mbar_wait_bounded(&sfree[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) { ok = false; break; }
-        tc_fence_after();
-        const uint32_t kb = smem_u32(smem + kOffK + s * kKV);
-#pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
-          const uint32_t off = (kk & 3) * 32;
-          tc_mma_bf16(t_s + s * kKT, desc_sw128(qh + (kk >> 2) * kRowBox + off, 0, 1024),
-                      desc_sw128(kb + (kk >> 2) * kBox + off, 0, 1024), idesc_qk, kk > 0 ? 1u : 0u);
-        }
-        if (SPLITQ) {
+      int g = 0;
+      for (int w = blockIdx.x, it = 0; w < n_items && ok; w += gridDim.x, ++it) {
+        int split, kvh, b, tile0, nt;
+        item(w, split, kvh, b, tile0, nt);
+        const int qb = it & 1;
+        if (!mbar_wait_bounded(&qfull[qb], (it >> 1) & 1, a.timeout_ns, abort_flag, a.status)) { ok = false; break; }
+        const uint32_t qh = smem_u32(smem + kOffQ + qb * 2 * kQ), ql = qh + kQ;
+        for (int t = 0; t < nt; ++t, ++g) {
+          const int s = g & 1;
+          const uint32_t ph = (g >> 1) & 1;
+          if (!mbar_wait_bounded(&kfull[s], ph, a.timeout_ns, abort_flag, a.status)) { ok = false; break; }
+          if (!mbar_wait_bounded(&sfree[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kb = smem_u32(smem + kOffK + s * kKV);
 #pragma unroll
           for (int kk = 0; kk < kD / 16; ++kk) {
             const uint32_t off = (kk & 3) * 32;
-            tc_mma_bf16(t_s + s * kKT, desc_sw128(ql + (kk >> 2) * kRowBox + off, 0, 1024),
-                        desc_sw128(kb + (kk >> 2) * kBox + off, 0, 1024), idesc_qk, 1u);
+            tc_mma_bf16(t_s + s * kKT, desc_sw128(qh + (kk >> 2) * kRowBox + off, 0, 1024),
+                        desc_sw128(kb + (kk >> 2) * kBox + off, 0, 1024), idesc_qk, kk > 0 ? 1u : 0u);
           }
+          if (SPLITQ) {
+#pragma unroll
+            for (int kk = 0; kk < kD / 16; ++kk) {
+              const uint32_t off = (kk & 3) * 32;
+              tc_mma_bf16(t_s + s * kKT, desc_sw128(ql + (kk >> 2) * kRowBox + off, 0, 1024),
+                          desc_sw128(kb + (kk >> 2) * kBox + off, 0, 1024), idesc_qk, 1u);
+            }
+          }
+          tc_commit(&sfull[s]);
+          tc_commit(&kempty[s]);
+          if (g >= 1 && !issue_pv(g - 1)) { ok = false; break; }
         }
-        tc_commit(&sfull[s]);
-        tc_commit(&kempty[s]);
-        if (t >= 1 && !issue_pv(t - 1)) { ok = false; break; }
+        tc_commit(&qempty[qb]);  // this item's QK^T products are all issued
       }
-      if (ok && nt >= 1) issue_pv(nt - 1);
+      if (ok && g >= 1) issue_pv(g - 1);
       tc_commit(drain);
       volatile int no_abort = 0;
       mbar_wait_bounded(drain, 0, a.timeout_ns, &no_abort, a.status);
@@ -291,126 +300,134 @@ __global__ void __launch_bounds__(kThreads, 1)
     // ------------------------------------------------------------- softmax
     const int q4 = warp & 3;                        // TMEM lane quarter -> rows 16*q4 .. 16*q4+15
     const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const int r0 = 16 * q4 + (lane >> 2);           // the two rows this thread holds
+    const int r0 = 16 * q4 + (lane >> 2);           // the two rows this thread holds (order i * G + g)
     const int r1 = r0 + 8;
     const int cq = 2 * (lane & 3);                  // column offset inside each 8-column block
     const float c = a.scale_log2;
-    float o[64];                                    // O rows r0/r1 in fragment order
-#pragma unroll
-    for (int j = 0; j < 64; ++j) o[j] = 0.f;
-    float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-    float al0 = 0.f, al1 = 0.f;                     // rescale of the previous tile
     // stmatrix row address of this lane: matrix mi = lane/8 covers rows
     // 16*q4 + 8*(mi&1) + lane%8 and columns +8*(mi>>1) of each 16-key group
     const int st_row = 16 * q4 + 8 * ((lane >> 3) & 1) + (lane & 7);
     const int st_colh = 8 * (lane >> 4);
+    // partial rows in the order g * S + i
+    const int pr0 = (r0 % a.G) * a.S + r0 / a.G;
+    const int pr1 = (r1 % a.G) * a.S + r1 / a.G;
     bool ok = true;
-    auto consume_o = [&](int u, float a0, float a1) {
-      const int s = u & 1;
-      bool w = true;
-      if (lane == 0) w = mbar_wait_bounded(&ofull[s], (u >> 1) & 1, a.timeout_ns, abort_flag, a.status);
-      w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-      if (!w) return false;
-      tc_fence_after();
-      float pv[64];
-      tmem_ld_frag(t_o + s * kD + lane_off, pv);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&ofree[s]);
+    int g = 0;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      int split, kvh, b, tile0, nt;
+      item(w, split, kvh, b, tile0, nt);
+      float o[64];                                  // O rows r0/r1 in fragment order
 #pragma unroll
-      for (int j = 0; j < 64; ++j) o[j] = fmaf(o[j], (j & 2) ? a1 : a0, pv[j]);
-      return true;
-    };
-    for (int t = 0; t < nt; ++t) {
-      const int s = t & 1;
-      bool w = true;
-      if (lane == 0) w = mbar_wait_bounded(&sfull[s], (t >> 1) & 1, a.timeout_ns, abort_flag, a.status);
-      w = __shfl_sync(0xffffffffu, w ? 1 : 0, 0) != 0;
-      if (!w) { ok = false; break; }
-      tc_fence_after();
-      float v[64];
-      tmem_ld_frag(t_s + s * kKT + lane_off, v);
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&sfree[s]);
-      const int kbase = (tile0 + t) * kKT;
-      if (kbase + kKT > T) {  // tail tile: keys >= T do not exist
+      for (int j = 0; j < 64; ++j) o[j] = 0.f;
+      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+      float al0 = 0.f, al1 = 0.f;                   // rescale of the previous tile
+      auto consume_o = [&](int u, float a0, float a1) {
+        const int s = u & 1;
+        bool wt = true;
+        if (lane == 0) wt = mbar_wait_bounded(&ofull[s], (u >> 1) & 1, a.timeout_ns, abort_flag, a.status);
+        wt = __shfl_sync(0xffffffffu, wt ? 1 : 0, 0) != 0;
+        if (!wt) return false;
+        tc_fence_after();
+        float pv[64];
+        tmem_ld_frag(t_o + s * kD + lane_off, pv);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ofree[s]);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          const int key = kbase + 8 * (j >> 2) + cq + (j & 1);
-          if (key >= T) v[j] = -INFINITY;
+        for (int j = 0; j < 64; ++j) o[j] = fmaf(o[j], (j & 2) ? a1 : a0, pv[j]);
+        return true;
+      };
+      for (int t = 0; t < nt; ++t, ++g) {
+        const int s = g & 1;
+        bool wt = true;
+        if (lane == 0) wt = mbar_wait_bounded(&sfull[s], (g >> 1) & 1, a.timeout_ns, abort_flag, a.status);
+        wt = __shfl_sync(0xffffffffu, wt ? 1 : 0, 0) != 0;
+        if (!wt) { ok = false; break; }
+        tc_fence_after();
+        float v[64];
+        tmem_ld_frag(t_s + s * kKT + lane_off, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfree[s]);
+        const int kbase = (tile0 + t) * kKT;
+        if (kbase + kKT > T) {  // tail tile: keys >= T do not exist
+#pragma unroll
+          for (int j = 0; j < 64; ++j) {
+            const int key = kbase + 8 * (j >> 2) + cq + (j & 1);
+            if (key >= T) v[j] = -INFINITY;
+          }
         }
-      }
-      float mx0 = -INFINITY, mx1 = -INFINITY;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-      for (int j = 0; j < 64; j += 4) {
-        mx0 = fmaxf(mx0, fmaxf(v[j], v[j + 1]));
-        mx1 = fmaxf(mx1, fmaxf(v[j + 2], v[j + 3]));
-      }
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
-      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
-      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-      // running max in base-2 units (scores times c)
-      const float mn0 = fmaxf(m0, mx0 * c), mn1 = fmaxf(m1, mx1 * c);
-      const float a0 = m0 == -INFINITY ? 0.f : ex2(m0 - mn0);
-      const float a1 = m1 == -INFINITY ? 0.f : ex2(m1 - mn1);
-      m0 = mn0;
-      m1 = mn1;
-      float s0 = 0.f, s1 = 0.f;
+        for (int j = 0; j < 64; j += 4) {
+          mx0 = fmaxf(mx0, fmaxf(v[j], v[j + 1]));
+          mx1 = fmaxf(mx1, fmaxf(v[j + 2], v[j + 3]));
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
+        // running max in base-2 units (scores times c)
+        const float mn0 = fmaxf(m0, mx0 * c), mn1 = fmaxf(m1, mx1 * c);
+        const float a0 = m0 == -INFINITY ? 0.f : ex2(m0 - mn0);
+        const float a1 = m1 == -INFINITY ? 0.f : ex2(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-      for (int j = 0; j < 64; j += 4) {
-        v[j] = ex2(fmaf(v[j], c, -mn0));
-        v[j + 1] = ex2(fmaf(v[j + 1], c, -mn0));
-        v[j + 2] = ex2(fmaf(v[j + 2], c, -mn1));
-        v[j + 3] = ex2(fmaf(v[j + 3], c, -mn1));
-        s0 += v[j] + v[j + 1];
-        s1 += v[j + 2] + v[j + 3];
-      }
-      s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-      s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
-      s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-      s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
-      l0 = l0 * a0 + s0;
-      l1 = l1 * a1 + s1;
-      // P (head, remainder) -> shared memory, once PV of the previous tile is done
-      if (t >= 1) {
-        bool pw = true;
-        if (lane == 0) pw = mbar_wait_bounded(pfree, (t - 1) & 1, a.timeout_ns, abort_flag, a.status);
-        pw = __shfl_sync(0xffffffffu, pw ? 1 : 0, 0) != 0;
-        if (!pw) { ok = false; break; }
-      }
+        for (int j = 0; j < 64; j += 4) {
+          v[j] = ex2(fmaf(v[j], c, -mn0));
+          v[j + 1] = ex2(fmaf(v[j + 1], c, -mn0));
+          v[j + 2] = ex2(fmaf(v[j + 2], c, -mn1));
+          v[j + 3] = ex2(fmaf(v[j + 3], c, -mn1));
+          s0 += v[j] + v[j + 1];
+          s1 += v[j + 2] + v[j + 3];
+        }
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+        l0 = l0 * a0 + s0;
+        l1 = l1 * a1 + s1;
+        // P (head, remainder) -> shared memory, once the previous PV is done
+        if (g >= 1) {
+          bool pw = true;
+          if (lane == 0) pw = mbar_wait_bounded(pfree, (g - 1) & 1, a.timeout_ns, abort_flag, a.status);
+          pw = __shfl_sync(0xffffffffu, pw ? 1 : 0, 0) != 0;
+          if (!pw) { ok = false; break; }
+        }
 #pragma unroll
-      for (int g = 0; g < kKT / 16; ++g) {
-        // 16-key group g: fragment reps 2g (keys 16g..16g+7) and 2g+1 (16g+8..)
-        uint32_t h0, l0p, h1, l1p, h2, l2p, h3, l3p;
-        split_bf16(v[8 * g + 0], v[8 * g + 1], h0, l0p);   // rows 0-7,  keys 16g + cq
-        split_bf16(v[8 * g + 2], v[8 * g + 3], h1, l1p);   // rows 8-15, keys 16g + cq
-        split_bf16(v[8 * g + 4], v[8 * g + 5], h2, l2p);   // rows 0-7,  keys 16g + 8 + cq
-        split_bf16(v[8 * g + 6], v[8 * g + 7], h3, l3p);   // rows 8-15, keys 16g + 8 + cq
-        const uint32_t off = swz(kNQ, st_row, 16 * g + st_colh);
-        stmatrix_x4(smem_u32(smem + kOffPh) + off, h0, h1, h2, h3);
-        stmatrix_x4(smem_u32(smem + kOffPl) + off, l0p, l1p, l2p, l3p);
+        for (int gg = 0; gg < kKT / 16; ++gg) {
+          // 16-key group gg: fragment reps 2gg (keys 16gg..16gg+7) and 2gg+1 (16gg+8..)
+          uint32_t h0, l0p, h1, l1p, h2, l2p, h3, l3p;
+          split_bf16(v[8 * gg + 0], v[8 * gg + 1], h0, l0p);   // rows 0-7,  keys 16gg + cq
+          split_bf16(v[8 * gg + 2], v[8 * gg + 3], h1, l1p);   // rows 8-15, keys 16gg + cq
+          split_bf16(v[8 * gg + 4], v[8 * gg + 5], h2, l2p);   // rows 0-7,  keys 16gg + 8 + cq
+          split_bf16(v[8 * gg + 6], v[8 * gg + 7], h3, l3p);   // rows 8-15, keys 16gg + 8 + cq
+          const uint32_t off = swz(kNQ, st_row, 16 * gg + st_colh);
+          stmatrix_x4(smem_u32(smem + kOffPh) + off, h0, h1, h2, h3);
+          stmatrix_x4(smem_u32(smem + kOffPl) + off, l0p, l1p, l2p, l3p);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pfull);
+        if (t >= 1 && !consume_o(g - 1, al0, al1)) { ok = false; break; }
+        al0 = a0;
+        al1 = a1;
       }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(pfull);
-      if (t >= 1 && !consume_o(t - 1, al0, al1)) { ok = false; break; }
-      al0 = a0;
-      al1 = a1;
-    }
-    if (ok && nt >= 1) ok = consume_o(nt - 1, al0, al1);
-    // partial slot `split`: o (unnormalised, [q][d]), (m, l) per q
-    const long long prow = ((long long)(b * a.Hkv + kvh) * n_slots + split) * kNQ;
+      if (ok && nt >= 1) ok = consume_o(g - 1, al0, al1);
+      // partial slot `split`: o (unnormalised, [q][d]), (m, l) per q
+      const long long prow = ((long long)(b * a.Hkv + kvh) * n_ctx + split) * kNQ;
 #pragma unroll
-    for (int rep = 0; rep < 16; ++rep) {
-      const int d = 8 * rep + cq;
-      *reinterpret_cast<float2*>(a.part_o + (prow + r0) * kD + d) = make_float2(o[4 * rep], o[4 * rep + 1]);
-      *reinterpret_cast<float2*>(a.part_o + (prow + r1) * kD + d) = make_float2(o[4 * rep + 2], o[4 * rep + 3]);
-    }
-    if ((lane & 3) == 0) {
-      a.part_ml[prow + r0] = make_float2(m0, l0);
-      a.part_ml[prow + r1] = make_float2(m1, l1);
+      for (int rep = 0; rep < 16; ++rep) {
+        const int d = 8 * rep + cq;
+        *reinterpret_cast<float2*>(a.part_o + (prow + pr0) * kD + d) = make_float2(o[4 * rep], o[4 * rep + 1]);
+        *reinterpret_cast<float2*>(a.part_o + (prow + pr1) * kD + d) = make_float2(o[4 * rep + 2], o[4 * rep + 3]);
+      }
+      if ((lane & 3) == 0) {
+        a.part_ml[prow + pr0] = make_float2(m0, l0);
+        a.part_ml[prow + pr1] = make_float2(m1, l1);
+      }
     }
   }
 
@@ -429,15 +446,14 @@ int attention_tc_splits(int B, int Hkv, int max_ctx) {
   const int pairs = B * Hkv;
   const int ntiles = (max_ctx + kKT - 1) / kKT;
   if (ntiles <= 0) return 1;
-  // One CTA per SM; a CTA costs its tiles plus a fixed start-up/drain of
-  // about 5 tiles (Q staging, TMEM allocation, pipeline fill, partial
-  // write), measured from the time of 1..8 splits on the 64 x 8 x 8192 case.
-  constexpr int kFixedTiles = 5;
+  // Persistent CTAs (one per SM) walk pairs x splits items; the busiest CTA
+  // takes ceil(items / SMs) items of ceil(tiles / splits) tiles each, plus
+  // about one tile's worth per item for its partial write.
   int best = 1;
   long long best_cost = -1;
   for (int s = 1; s <= 32 && s <= ntiles; ++s) {
-    const long long waves = ((long long)pairs * s + kNumSMs - 1) / kNumSMs;
-    const long long cost = waves * ((ntiles + s - 1) / s + kFixedTiles) * 64 + s;
+    const long long per_cta = ((long long)pairs * s + kNumSMs - 1) / kNumSMs;
+    const long long cost = per_cta * ((ntiles + s - 1) / s + 1) * 64 + s;
     if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = s; }
   }
   return best;
@@ -445,14 +461,13 @@ int attention_tc_splits(int B, int Hkv, int max_ctx) {
 
 int attention_tc_smem_bytes() { return kSmemBytes; }
 
-cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx_splits, int n_slots, const CUtensorMap& map_k128,
-                                const CUtensorMap& map_v128, cudaStream_t st) {
-  dim3 grid(n_ctx_splits, a.Hkv, a.B);
+cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx, const CUtensorMap& map_k128,
+                                const CUtensorMap& map_v128, const CUtensorMap& map_q, cudaStream_t st) {
+  const int items = a.B * a.Hkv * n_ctx;
+  const int grid = items < kNumSMs ? items : kNumSMs;
   if (a.split)
-    return launch_k(k_attn_ctx_tc<true>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, a, n_ctx_splits,
-                    n_slots);
-  return launch_k(k_attn_ctx_tc<false>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, a, n_ctx_splits,
-                  n_slots);
+    return launch_k(k_attn_ctx_tc<true>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, map_q, a, n_ctx, items);
+  return launch_k(k_attn_ctx_tc<false>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, map_q, a, n_ctx, items);
 }
 
 cudaError_t prepare_attention_tc_kernels() {

@@ -103,15 +103,17 @@ struct AttnArgs {
 AttnPlan plan_attention(int B, int S, int Hq, int Hkv, int D, int max_ctx, int allow_tc = 1);
 size_t attention_partial_bytes(const AttnPlan& p, int B, int Hkv);
 // map_k/map_v: context cache maps with 64-row boxes; map_k128/map_v128: the
-// same caches with 128-row boxes (tcgen05 path).
+// same caches with 128-row boxes, and map_q the query rows (make_map_q), for
+// the tcgen05 path.
 cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a, const CUtensorMap& map_k, const CUtensorMap& map_v,
-                             const CUtensorMap& map_k128, const CUtensorMap& map_v128, cudaStream_t st);
+                             const CUtensorMap& map_k128, const CUtensorMap& map_v128, const CUtensorMap& map_q,
+                             cudaStream_t st);
 // tcgen05 context attention (attention_tc.cu)
 bool attention_tc_supported(int D, int rows);
 int attention_tc_splits(int B, int Hkv, int max_ctx);
 int attention_tc_smem_bytes();
-cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx_splits, int n_slots, const CUtensorMap& map_k128,
-                                const CUtensorMap& map_v128, cudaStream_t st);
+cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx, const CUtensorMap& map_k128,
+                                const CUtensorMap& map_v128, const CUtensorMap& map_q, cudaStream_t st);
 cudaError_t prepare_attention_tc_kernels();
 // Merge the split partials (no-op for the mma.sync path with one split); on
 // the tcgen05 path this also attends to the block keys.
@@ -165,5 +167,9 @@ bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols,
 // planes lie stride_rows rows apart and rows >= `rows` read as zero.
 bool make_map_3d(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t stride_rows, uint64_t cols,
                  uint32_t box_rows);
+// The query heads of a q|k|v buffer [rows][ld] (query head h at columns
+// h*D..h*D+D-1) as a 3D bf16 map {D, Hq, rows}, box {64, G, S}: one box is the
+// G query heads of a kv head at S consecutive rows, in row order i * G + g.
+bool make_map_q(CUtensorMap* m, const void* qkv, uint64_t rows, uint64_t ld, int Hq, int D, int G, int S);
 
 }  // namespace dd
