@@ -227,6 +227,12 @@ def run_reference(args, world, rank):
 
 # ---------------------------------------------------------------- GPU arm
 
+# DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch, from
+# one ncu capture of the same kernel at the same workload; kinds and workloads
+# not captured report null.
+TRAFFIC = {("small", "gemm_gate_up"): 47.23e6 + 0.40e6}
+
+
 def algorithmic_bytes(cfg, kind, ctx_len):
     """Minimum HBM bytes of one launch of `kind` (weights/KV read once,
     activations in and out at their stored precision)."""
@@ -384,7 +390,7 @@ def gpu_arm(args, world, rank, local):
     if dom_bytes is not None:
         ach = dom_bytes / (dom_us * 1e-6) / 1e9
         roofline = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                    "frac": ach / hbm_peak, "traffic": None, "peak_source": peak_src,
+                    "frac": ach / hbm_peak, "traffic": TRAFFIC.get((cfg.name, dom)), "peak_source": peak_src,
                     "algorithmic_bytes_per_launch": dom_bytes, "us_per_launch": dom_us}
 
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
