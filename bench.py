@@ -65,6 +65,8 @@ def parse(argv=None):
     ap.add_argument("--gamma", type=float, default=0.8)
     ap.add_argument("--mode", default="threshold", type=mode_arg,
                     help="threshold | mock_ar | topk:K (the K most confident) | steps:N (fixed N steps per block)")
+    ap.add_argument("--rope-theta", type=float, default=0.0,
+                    help="rotary positions on the block's queries and keys (0: learned in-block positions only)")
     ap.add_argument("--no-micro", action="store_true", help="skip the attention / LM-head microbenchmarks")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     return ap.parse_args(argv)
@@ -74,12 +76,13 @@ def workload_desc(cfg, gamma, mode):
     return (f"{cfg.name} decode: batch {cfg.batch}, context {cfg.ctx_len} (+16 per block, "
             f"{BLOCKS_PER_STEP} consecutive blocks), block {cfg.block}, hidden {cfg.hidden}, "
             f"{cfg.n_q_heads} q / {cfg.n_kv_heads} kv heads x d{cfg.head_dim}, {cfg.n_layers} layers, "
-            f"SwiGLU {cfg.mlp}, vocab {cfg.vocab}, gamma {gamma}, {mode}")
+            f"SwiGLU {cfg.mlp}, vocab {cfg.vocab}, gamma {gamma}, {mode}"
+            + (f", RoPE theta {cfg.rope_theta:g}" if cfg.rope_theta > 0 else ""))
 
 
-def bench_cfg(name):
+def bench_cfg(name, rope_theta=0.0):
     cfg = synth.CONFIGS[name]
-    return cfg.replace(max_ctx=cfg.ctx_len + BLOCKS_PER_STEP * cfg.block)
+    return cfg.replace(max_ctx=cfg.ctx_len + BLOCKS_PER_STEP * cfg.block, rope_theta=rope_theta)
 
 
 def load_peaks():
@@ -195,7 +198,7 @@ def oracle_block_sample(cfg, gamma, mode, seed=0, batch=None):
 
 
 def run_reference(args, world, rank):
-    cfg = bench_cfg(args.config)
+    cfg = bench_cfg(args.config, args.rope_theta)
     if rank != 0:
         return
     import oracle
@@ -279,7 +282,7 @@ def gpu_arm(args, world, rank, local):
     libbuild.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    cfg = bench_cfg(args.config)
+    cfg = bench_cfg(args.config, args.rope_theta)
     mode = mode_code(args.mode)
     hbm_peak, tc_peak, tc_sust, peak_src = load_peaks()
 

@@ -39,7 +39,8 @@ c_float = ctypes.c_float
 class dd_config(ctypes.Structure):
     _fields_ = [("batch", c_int32), ("block", c_int32), ("hidden", c_int32), ("n_q_heads", c_int32),
                 ("n_kv_heads", c_int32), ("head_dim", c_int32), ("n_layers", c_int32), ("mlp", c_int32),
-                ("vocab", c_int32), ("max_ctx", c_int32), ("rms_eps", c_float)]
+                ("vocab", c_int32), ("max_ctx", c_int32), ("rms_eps", c_float),
+                ("rope_theta", c_float)]
 
 
 class dd_weights(ctypes.Structure):

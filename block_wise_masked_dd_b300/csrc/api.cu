@@ -173,6 +173,7 @@ dd_status check_config(const dd_config* c) {
   if (c->n_layers < 1) return fail(DD_ERR_INVALID_ARG, "n_layers must be >= 1");
   if (c->max_ctx < 0) return fail(DD_ERR_INVALID_ARG, "max_ctx must be >= 0");
   if (!(c->rms_eps >= 0.f)) return fail(DD_ERR_INVALID_ARG, "rms_eps must be >= 0");
+  if (!(c->rope_theta >= 0.f) || c->rope_theta > 1e30f) return fail(DD_ERR_INVALID_ARG, "rope_theta must be >= 0 and finite");
   return DD_OK;
 }
 
@@ -284,7 +285,9 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
     o.split_stride = (long long)R * c->qkvw;
     DD_CUDA(dd::launch_gemm(L.p_qkv, c->m_wqkv[l], c->m_y_b, o, status, c->timeout_ns, st));
     mk(kKGemmQkv);
-    DD_CUDA(dd::launch_reduce_bf16(part, L.p_qkv.splits, o.split_stride, R, c->qkvw, ws + L.qkv, 1, st));
+    DD_CUDA(dd::launch_reduce_qkv(part, L.p_qkv.splits, o.split_stride, R, c->qkvw, ws + L.qkv, cf.block,
+                                  cf.head_dim, (cf.n_q_heads + cf.n_kv_heads) * cf.head_dim, small_ptr(c) + 2,
+                                  cf.rope_theta, st));
     mk(kKReduceQkv);
     // block attention
     dd::AttnArgs a{};

@@ -126,8 +126,11 @@ cudaError_t launch_attention_combine(const AttnPlan& p, const AttnArgs& a, cudaS
 cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const void* embed, const void* pos,
                               const void* g, float* x, void* y_split, int B, int S, int H, int V, float eps,
                               cudaStream_t st);
-cudaError_t launch_reduce_bf16(const float* part, int splits, long long split_stride, int rows, int N, void* out,
-                               int split, cudaStream_t st);
+// q|k|v of the step: the split-K sum written as bf16 head + remainder; with
+// theta > 0 the query and key heads (columns < qk_cols) of row r are rotated
+// to position *ctx_len + r % S (see dd_config.rope_theta).
+cudaError_t launch_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N, void* out, int S,
+                              int D, int qk_cols, const int* ctx_len, float theta, cudaStream_t st);
 cudaError_t launch_reduce_f32(const float* part, int splits, long long split_stride, int rows, int N, float* out,
                               cudaStream_t st);
 cudaError_t launch_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,

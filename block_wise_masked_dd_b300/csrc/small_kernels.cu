@@ -171,11 +171,8 @@ __global__ void k_reduce_residual_norm(const float* part, int splits, long long 
   norm_store(xv, passes, r, H, R, gv, y, eps, red);
 }
 
-// out[r][n] = sum over splits of part[s][r][n]; bf16 output optionally split
-// (remainder at out + total).
-template <typename OutT>
-__global__ void k_reduce(const float* part, int splits, long long split_stride, long long total, OutT* out,
-                         int split) {
+// out[r][n] = sum over splits of part[s][r][n] (fp32; the standalone GEMM).
+__global__ void k_reduce(const float* part, int splits, long long split_stride, long long total, float* out) {
   pdl_wait();
   pdl_launch_dependents();
   for (long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8; e < total;
@@ -183,21 +180,43 @@ __global__ void k_reduce(const float* part, int splits, long long split_stride, 
     float acc[8];
     load8_f32(part + e, acc);
     add_partials<8>(part + e, 1, splits, split_stride, acc);
-    if constexpr (sizeof(OutT) == 2) {
-      __nv_bfloat16* o = reinterpret_cast<__nv_bfloat16*>(out);
-      if (split) {
-        store8_split(o + e, o + total + e, acc);
-      } else {
-        uint4 h, l;
-        split_bf16(acc[0], acc[1], h.x, l.x);
-        split_bf16(acc[2], acc[3], h.y, l.y);
-        split_bf16(acc[4], acc[5], h.z, l.z);
-        split_bf16(acc[6], acc[7], h.w, l.w);
-        *reinterpret_cast<uint4*>(o + e) = h;
+    store8_f32(out + e, acc);
+  }
+}
+
+// q|k|v = the sum of the split-K partials, written as bf16 head (rows
+// [0, rows)) + remainder (rows [rows, 2 rows)).  With theta > 0 the pairs
+// (2j, 2j+1) of every query and key head (columns < qk_cols) of row r turn by
+// (T + r % S) * theta^(-2j/D) radians, T = *ctx_len: angle, cosine and sine in
+// double, the rotation in fp32.
+__global__ void k_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N,
+                             __nv_bfloat16* out, int S, int D, int qk_cols, const int* ctx_len, float theta) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const long long total = (long long)rows * N;
+  const int T = theta > 0.f ? *ctx_len : 0;
+  for (long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8; e < total;
+       e += (long long)gridDim.x * blockDim.x * 8) {
+    float acc[8];
+    load8_f32(part + e, acc);
+    add_partials<8>(part + e, 1, splits, split_stride, acc);
+    const int n = (int)(e % N);
+    if (theta > 0.f && n < qk_cols) {
+      const int d0 = n % D;
+      const double pos = (double)(T + (int)(e / N) % S);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        const int j = (d0 >> 1) + p;
+        const double ang = pos * pow((double)theta, -2.0 * j / D);
+        double sd, cd;
+        sincos(ang, &sd, &cd);
+        const float c = (float)cd, sn = (float)sd;
+        const float x0 = acc[2 * p], x1 = acc[2 * p + 1];
+        acc[2 * p] = x0 * c - x1 * sn;
+        acc[2 * p + 1] = x0 * sn + x1 * c;
       }
-    } else {
-      store8_f32(reinterpret_cast<float*>(out) + e, acc);
     }
+    store8_split(out + e, out + total + e, acc);
   }
 }
 
@@ -421,8 +440,9 @@ int row_threads(int H) {
 // its L1 / shared split before the next kernel's CTAs can join it.
 cudaError_t prepare_small_kernels() {
   const void* fns[] = {(const void*)k_embed_norm,           (const void*)k_reduce_residual_norm,
-                       (const void*)k_reduce<__nv_bfloat16>, (const void*)k_reduce<float>,
+                       (const void*)k_reduce,
                        (const void*)k_reduce_swiglu,         (const void*)k_select_combine,
+                       (const void*)k_reduce_qkv,
                        (const void*)k_commit};
   cudaError_t e = cudaSuccess;
   for (const void* f : fns) {
@@ -438,17 +458,16 @@ cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const
                   (const __nv_bfloat16*)pos, (const __nv_bfloat16*)g, x, (__nv_bfloat16*)y, S, H, V, eps);
 }
 
-cudaError_t launch_reduce_bf16(const float* part, int splits, long long split_stride, int rows, int N, void* out,
-                               int split, cudaStream_t st) {
-  const long long total = (long long)rows * N;
-  return launch_k(k_reduce<__nv_bfloat16>, grid_for(total / 8, 256), 256, 0, st, part, splits, split_stride, total,
-                  (__nv_bfloat16*)out, split);
+cudaError_t launch_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N, void* out, int S,
+                              int D, int qk_cols, const int* ctx_len, float theta, cudaStream_t st) {
+  return launch_k(k_reduce_qkv, grid_for((long long)rows * N / 8, 256), 256, 0, st, part, splits, split_stride, rows,
+                  N, (__nv_bfloat16*)out, S, D, qk_cols, ctx_len, theta);
 }
 
 cudaError_t launch_reduce_f32(const float* part, int splits, long long split_stride, int rows, int N, float* out,
                               cudaStream_t st) {
   const long long total = (long long)rows * N;
-  return launch_k(k_reduce<float>, grid_for(total / 8, 256), 256, 0, st, part, splits, split_stride, total, out, 0);
+  return launch_k(k_reduce, grid_for(total / 8, 256), 256, 0, st, part, splits, split_stride, total, out);
 }
 
 cudaError_t launch_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,

@@ -29,7 +29,8 @@ def _ptr(t) -> int:
 def config_struct(cfg) -> B.dd_config:
     """dd_config from any object with the synthetic Config field names."""
     return B.dd_config(cfg.batch, cfg.block, cfg.hidden, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim,
-                       cfg.n_layers, cfg.mlp, cfg.vocab, cfg.max_ctx, float(cfg.rms_eps))
+                       cfg.n_layers, cfg.mlp, cfg.vocab, cfg.max_ctx, float(cfg.rms_eps),
+                       float(getattr(cfg, "rope_theta", 0.0)))
 
 
 def bits_to_tensor(bits: np.ndarray, device) -> torch.Tensor:

@@ -89,6 +89,12 @@ typedef struct dd_config {
   int32_t vocab;      /* V */
   int32_t max_ctx;    /* capacity of the context KV cache, in positions */
   float rms_eps;      /* RMSNorm epsilon (1e-5 in the synthetic workloads) */
+  float rope_theta;   /* 0: in-block positions from the learned table only.  > 0: also rotary
+                       * positions on the block's queries and keys: block position i sits at
+                       * T + i (T = context length) and the pair (2j, 2j+1) of every query and
+                       * key head turns by (T + i) * rope_theta^(-2j/D) radians; the context
+                       * keys are taken as already positioned (the pages are silent on
+                       * positions; this is the survey's NEXT-4 option) */
 } dd_config;
 
 /* Borrowed device pointers to bf16 weights (stacked over layers). */

@@ -33,6 +33,7 @@ from .decode import (  # noqa: F401
     lm_head_select,
     near_tie_flags,
     rmsnorm,
+    rope,
     round_bf16,
     select_from_logits,
     steps_schedule_k,

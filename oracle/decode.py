@@ -100,6 +100,24 @@ def silu(x: np.ndarray) -> np.ndarray:
     return x / (F32(1.0) + np.exp(-x))
 
 
+def rope(x: np.ndarray, positions: np.ndarray, theta: float) -> np.ndarray:
+    """Rotary positions for the block's queries or keys (reading: interleaved
+    pairs; the pages are silent).  x [S, heads, D] fp32; the pair (2j, 2j+1) of
+    every head at position p turns by p * theta^(-2j/D) radians (angle, cosine
+    and sine in double, the rotation in fp32).
+    """
+    D = x.shape[-1]
+    freq = float(theta) ** (-2.0 * np.arange(D // 2, dtype=np.float64) / D)
+    ang = np.asarray(positions, np.float64)[:, None] * freq[None, :]
+    c = np.cos(ang).astype(F32)[:, None, :]
+    s = np.sin(ang).astype(F32)[:, None, :]
+    x = x.astype(F32, copy=False)
+    out = np.empty_like(x)
+    out[..., 0::2] = x[..., 0::2] * c - x[..., 1::2] * s
+    out[..., 1::2] = x[..., 0::2] * s + x[..., 1::2] * c
+    return out
+
+
 def block_attention(q, k_blk, v_blk, k_ctx, v_ctx):
     """Block attention for one sequence.
 
@@ -275,8 +293,14 @@ def denoise_step(model: OracleModel, tokens, mask, gamma: float, mode: int = MOD
     attn_outs = []
     for l in range(cfg.n_layers):
         y = st(rmsnorm(x, w[f"g_attn{l}"], cfg.rms_eps))
-        q = st(y @ w[f"wq{l}"].T).reshape(B, S, Hq, D)
-        k = st(y @ w[f"wk{l}"].T).reshape(B, S, Hkv, D)
+        q = (y @ w[f"wq{l}"].T).reshape(B, S, Hq, D)
+        k = (y @ w[f"wk{l}"].T).reshape(B, S, Hkv, D)
+        if getattr(cfg, "rope_theta", 0.0) > 0:
+            # block position i sits at T + i, after the context (NEXT-4 reading)
+            pos = T + np.arange(S)
+            q = np.stack([rope(q[b], pos, cfg.rope_theta) for b in range(B)])
+            k = np.stack([rope(k[b], pos, cfg.rope_theta) for b in range(B)])
+        q, k = st(q), st(k)
         v = st(y @ w[f"wv{l}"].T).reshape(B, S, Hkv, D)
         o = np.empty((B, S, Hq, D), F32)
         for b in range(B):

@@ -47,6 +47,9 @@ class Config:
     vocab      LM-head outputs (V); the embedding has V+1 rows, row V = [MASK]
     ctx_len    context positions present in the KV cache (T)
     max_ctx    capacity of the KV cache (>= ctx_len)
+    rms_eps    RMSNorm epsilon
+    rope_theta rotary base for the block's queries and keys (0: learned
+               in-block positions only)
     """
 
     name: str
@@ -62,6 +65,7 @@ class Config:
     ctx_len: int
     max_ctx: int
     rms_eps: float = 1e-5
+    rope_theta: float = 0.0
 
     @property
     def rows(self) -> int:

@@ -108,8 +108,15 @@ def denoise_step(cfg, w, k_ctx, v_ctx, tokens, mask, round_act=False):
             xs.append([w["embed"][tid][c] + w["pos"][i][c] for c in range(H)])
     for l in range(cfg.n_layers):
         ys = [[st(v) for v in rmsnorm(x, w[f"g_attn{l}"], cfg.rms_eps)] for x in xs]
-        qs = [[st(v) for v in matvec(w[f"wq{l}"], y)] for y in ys]
-        ks = [[st(v) for v in matvec(w[f"wk{l}"], y)] for y in ys]
+        qs = [matvec(w[f"wq{l}"], y) for y in ys]
+        ks = [matvec(w[f"wk{l}"], y) for y in ys]
+        theta = getattr(cfg, "rope_theta", 0.0)
+        if theta > 0:
+            T = len(k_ctx[l][0][0]) if k_ctx[l] and k_ctx[l][0] else 0
+            qs = [rope_row(qs[r], T + r % S, Hq, D, theta) for r in range(len(qs))]
+            ks = [rope_row(ks[r], T + r % S, Hkv, D, theta) for r in range(len(ks))]
+        qs = [[st(v) for v in q] for q in qs]
+        ks = [[st(v) for v in k] for k in ks]
         vs = [[st(v) for v in matvec(w[f"wv{l}"], y)] for y in ys]
         new_xs = []
         for b in range(B):
@@ -140,6 +147,19 @@ def denoise_step(cfg, w, k_ctx, v_ctx, tokens, mask, round_act=False):
         conf.append(c)
         arg.append(a)
     return logits, conf, arg
+
+
+def rope_row(x, pos, heads, D, theta):
+    """Rotate the pairs (2j, 2j+1) of every head of one row by pos * theta^(-2j/D)."""
+    out = list(x)
+    for h in range(heads):
+        for j in range(D // 2):
+            a = pos * theta ** (-2.0 * j / D)
+            c, s = math.cos(a), math.sin(a)
+            e, o = x[h * D + 2 * j], x[h * D + 2 * j + 1]
+            out[h * D + 2 * j] = e * c - o * s
+            out[h * D + 2 * j + 1] = e * s + o * c
+    return out
 
 
 def commit_sets(conf_row, masked, gamma, mock_ar):

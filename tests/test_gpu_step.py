@@ -166,3 +166,30 @@ def test_tiny_state_synced_topk_and_fixed_steps(tiny, mode):
 def test_decode_block_fixed_steps(small, N):
     _, steps = small.dec.decode_block(0.8, oracle.with_param(oracle.MODE_STEPS, N))
     assert steps == N
+
+
+# ------------------------------------------------------------------- RoPE
+
+@pytest.fixture(scope="module")
+def tiny_rope():
+    require_gpu()
+    return Problem(synth.TINY.replace(rope_theta=10000.0))
+
+
+@pytest.mark.parametrize("gamma,mode", [(0.8, 0), (0.8, 1)])
+def test_tiny_rope_state_synced_decode(tiny_rope, gamma, mode):
+    tok, mask = tiny_rope.start_state()
+    steps = 0
+    while mask.max():
+        tok, mask, _, _ = compare_step(tiny_rope, tok, mask, gamma, mode)
+        steps += 1
+        assert steps <= 16
+
+
+def test_small_rope_first_step():
+    require_gpu()
+    p = Problem(synth.SMALL.replace(rope_theta=10000.0))
+    tok, mask = p.start_state()
+    compare_step(p, tok, mask, 0.8)
+    tok, mask = synth.make_tokens(p.cfg, seed=9, masked_frac=0.4)
+    compare_step(p, tok, mask, 0.8)

@@ -51,6 +51,9 @@ MUTANTS = {
     "topk_ties_to_higher_position": ("commit", [("key=lambda i: (-float(F32(conf[b, i])), i)",
                                                  "key=lambda i: (-float(F32(conf[b, i])), -i)")]),
     "topk_takes_one_more": ("commit", [("chosen = sorted(ranked[:k])", "chosen = sorted(ranked[:k + 1])")]),
+    "rope_wrong_sign": ("rope", [("x[..., 0::2] * s + x[..., 1::2] * c", "x[..., 1::2] * c - x[..., 0::2] * s")]),
+    "rope_wrong_frequency": ("rope", [("-2.0 * np.arange(D // 2, dtype=np.float64) / D", "-1.0 * np.arange(D // 2, dtype=np.float64) / D")]),
+    "step_rope_keys_unrotated": ("denoise_step", [("k = np.stack([rope(k[b], pos, cfg.rope_theta) for b in range(B)])", "pass")]),
     "steps_schedule_off_by_one": ("steps_schedule_k", [("steps_left = n_steps - t\n", "steps_left = n_steps - t + 1\n")]),
 }
 
@@ -98,6 +101,9 @@ def _pins(tiny):
         lambda: pins.test_decode_mock_ar_is_left_to_right(tiny),
         lambda: pins.test_decode_committed_never_change_and_progress(tiny),
         lambda: pins.test_decode_topk_and_fixed_steps(tiny),
+        pins.test_rope_closed_forms,
+        pins.test_rope_scores_depend_on_relative_position,
+        pins.test_full_step_with_rope_vs_bruteforce,
     ]
 
 

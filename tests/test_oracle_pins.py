@@ -397,3 +397,43 @@ def test_decode_top1_equals_gamma_above_one(tiny_model):
     a, sa, _ = oracle.decode_block(tiny_model, 0.8, oracle.with_param(oracle.MODE_TOPK, 1))
     b, sb, _ = oracle.decode_block(tiny_model, 1.01)
     assert sa == sb == 16 and (a == b).all()
+
+
+# ------------------------------------------------------------------- RoPE
+
+def test_rope_closed_forms():
+    x = np.zeros((3, 1, 2), F32)
+    x[:, 0, 0] = 1.0
+    got = oracle.rope(x, np.array([0, 1, 2]), 10000.0)       # D = 2: frequency theta^0 = 1
+    np.testing.assert_allclose(got[:, 0, 0], np.cos([0.0, 1.0, 2.0]), atol=1e-7)
+    np.testing.assert_allclose(got[:, 0, 1], np.sin([0.0, 1.0, 2.0]), atol=1e-7)
+    rng = np.random.default_rng(12)
+    y = rng.standard_normal((5, 3, 16)).astype(F32)
+    r = oracle.rope(y, np.arange(5) * 37 + 3, 500.0)
+    np.testing.assert_allclose(np.linalg.norm(r, axis=-1), np.linalg.norm(y, axis=-1), rtol=1e-5)
+    np.testing.assert_array_equal(oracle.rope(y, np.zeros(5, int), 500.0), y)
+
+
+def test_rope_scores_depend_on_relative_position():
+    rng = np.random.default_rng(13)
+    q = rng.standard_normal((4, 2, 8)).astype(F32)
+    k = rng.standard_normal((4, 2, 8)).astype(F32)
+    pos = np.array([0, 3, 7, 20])
+    for shift in (1, 50, 1000):
+        a = np.einsum("ihd,jhd->hij", oracle.rope(q, pos, 100.0), oracle.rope(k, pos, 100.0))
+        b = np.einsum("ihd,jhd->hij", oracle.rope(q, pos + shift, 100.0), oracle.rope(k, pos + shift, 100.0))
+        np.testing.assert_allclose(a, b, rtol=1e-4, atol=1e-4)
+
+
+def test_full_step_with_rope_vs_bruteforce():
+    cfg = MICRO.replace(rope_theta=100.0)
+    m = _micro_model(cfg)
+    tok, mask = synth.make_tokens(cfg, seed=5, masked_frac=0.5)
+    r = oracle.denoise_step(m, tok, mask, 0.8, keep_intermediates=True)
+    w = {k: _nested(v) for k, v in m.w.items()}
+    logits, conf, arg = bf.denoise_step(cfg, w, _nested(m.k_ctx), _nested(m.v_ctx),
+                                        tok.tolist(), [int(v) for v in mask], False)
+    np.testing.assert_allclose(r.logits, np.array(logits), rtol=2e-4, atol=2e-5)
+    assert (r.arg.reshape(-1) == np.array(arg)).all()
+    plain = oracle.denoise_step(_micro_model(MICRO), tok, mask, 0.8, keep_intermediates=True)
+    assert np.abs(plain.logits - r.logits).max() > 1e-3   # the rotation reaches the logits
