@@ -67,17 +67,21 @@ def parse(argv=None):
                     help="threshold | mock_ar | topk:K (the K most confident) | steps:N (fixed N steps per block)")
     ap.add_argument("--rope-theta", type=float, default=0.0,
                     help="rotary positions on the block's queries and keys (0: learned in-block positions only)")
+    ap.add_argument("--context-tower", action="store_true",
+                    help="append each decoded block to the context with the synthetic context tower on the device "
+                         "(default: fresh seeded K/V from the host)")
     ap.add_argument("--no-micro", action="store_true", help="skip the attention / LM-head microbenchmarks")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     return ap.parse_args(argv)
 
 
-def workload_desc(cfg, gamma, mode):
+def workload_desc(cfg, gamma, mode, tower=False):
     return (f"{cfg.name} decode: batch {cfg.batch}, context {cfg.ctx_len} (+16 per block, "
             f"{BLOCKS_PER_STEP} consecutive blocks), block {cfg.block}, hidden {cfg.hidden}, "
             f"{cfg.n_q_heads} q / {cfg.n_kv_heads} kv heads x d{cfg.head_dim}, {cfg.n_layers} layers, "
             f"SwiGLU {cfg.mlp}, vocab {cfg.vocab}, gamma {gamma}, {mode}"
-            + (f", RoPE theta {cfg.rope_theta:g}" if cfg.rope_theta > 0 else ""))
+            + (f", RoPE theta {cfg.rope_theta:g}" if cfg.rope_theta > 0 else "")
+            + (", context grown on the device by the context tower" if tower else ""))
 
 
 def bench_cfg(name, rope_theta=0.0):
@@ -313,17 +317,30 @@ def gpu_arm(args, world, rank, local):
     per_step_launches = B.dd_step_launch_count(dec.ctx)
     counters = {"denoise_steps": 0, "launches": 0}
 
+    if args.context_tower:
+        tw = (synth.make_tower_weights_torch(cfg, 0, dev) if cfg.name == "large" else synth.make_tower_weights(cfg, 0))
+        dec.set_context_tower(tw)
+        del tw
+
     def one_step(host: bool):
         dec.set_context_len(T0)
         counters["launches"] += 1
         for blk in range(BLOCKS_PER_STEP):
-            out = tokens_host[blk] if host else tokens[blk]
-            _, steps = dec.decode_block(args.gamma, mode, tokens=out)
+            if args.context_tower:
+                # the committed block goes to the context on the device; the
+                # host only reads the committed ids
+                _, steps = dec.decode_block(args.gamma, mode, tokens=tokens[blk])
+                dec.append_block(tokens[blk])
+                if host:
+                    tokens_host[blk].copy_(tokens[blk], non_blocking=True)
+                counters["launches"] += 3 + steps * per_step_launches + 3  # + embed, GEMM, reduce-append
+            else:
+                out = tokens_host[blk] if host else tokens[blk]
+                _, steps = dec.decode_block(args.gamma, mode, tokens=out)
+                k, v = app_host[blk] if host else app[blk]
+                dec.set_context_kv(k, v, T0 + blk * cfg.block)
+                counters["launches"] += 3 + steps * per_step_launches + 1  # block init, params, loop init; length
             counters["denoise_steps"] += steps
-            counters["launches"] += 3 + steps * per_step_launches  # block init, params, loop init
-            k, v = app_host[blk] if host else app[blk]
-            dec.set_context_kv(k, v, T0 + blk * cfg.block)
-            counters["launches"] += 1
 
     # ---------------------------------------------------- timed region
     for _ in range(args.warmup):
@@ -359,7 +376,7 @@ def gpu_arm(args, world, rank, local):
     torch.cuda.synchronize(dev)
     e2e_s = max_over_ranks(time.perf_counter() - t0, world)
     e2e_value = total_tokens / e2e_s
-    h2d = BLOCKS_PER_STEP * 2 * app_host[0][0].numel() * 2
+    h2d = 0 if args.context_tower else BLOCKS_PER_STEP * 2 * app_host[0][0].numel() * 2
     d2h = tokens_per_step * 4
 
     # ------------------------------------- per-kernel profile of the step
@@ -399,7 +416,7 @@ def gpu_arm(args, world, rank, local):
     line = {"metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_max / args.steps, "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": workload_desc(cfg, args.gamma, args.mode),
+            "config": {"workload": workload_desc(cfg, args.gamma, args.mode, args.context_tower),
                        "tokens_per_step": tokens_per_step, "parallelism": f"dp{world} (independent batches)",
                        "denoise_steps_per_block": timed_denoise / (args.steps * BLOCKS_PER_STEP),
                        "l2": "inputs larger than L2 (weights + context K/V per denoising step exceed 126 MB)"},

@@ -48,6 +48,10 @@ class dd_weights(ctypes.Structure):
                                         "g_final", "lm_head")]
 
 
+class dd_context_tower(ctypes.Structure):
+    _fields_ = [("embed", c_void_p), ("g", c_void_p), ("wkv", c_void_p)]
+
+
 class dd_probe(ctypes.Structure):
     _fields_ = [("attn_out", c_void_p), ("hidden", c_void_p), ("logits", c_void_p), ("conf", c_void_p),
                 ("arg", c_void_p)]
@@ -77,6 +81,8 @@ _SIGS = {
     "dd_decode_block": ([c_void_p, c_void_p, c_float, c_int32, c_int32, ctypes.POINTER(c_int32), c_void_p],
                         c_int32),
     "dd_device_status": ([c_void_p, c_void_p], c_int32),
+    "dd_set_context_tower": ([c_void_p, ctypes.POINTER(dd_context_tower)], c_int32),
+    "dd_append_block": ([c_void_p, c_void_p, c_void_p], c_int32),
     "dd_status_string": ([c_int32], ctypes.c_char_p),
     "dd_last_error": ([], ctypes.c_char_p),
     "dd_denoise_step_probe": ([c_void_p, c_void_p, c_void_p, c_float, c_int32, c_void_p,
@@ -157,6 +163,15 @@ def dd_init_weights(ctx: int, w: dd_weights):
 
 def dd_set_context_kv(ctx: int, k: int, v: int, t0: int, n: int, stream: int = 0):
     _check(load().dd_set_context_kv(ctx, k, v, t0, n, stream))
+
+
+def dd_set_context_tower(ctx: int, embed: int, g: int, wkv: int):
+    t = dd_context_tower(embed, g, wkv)
+    _check(load().dd_set_context_tower(ctx, ctypes.byref(t)))
+
+
+def dd_append_block(ctx: int, tokens: int, stream: int = 0):
+    _check(load().dd_append_block(ctx, tokens, stream))
 
 
 def dd_denoise_step(ctx: int, tokens: int, mask: int, gamma: float, mode: int, n_committed: int | None,

@@ -106,7 +106,7 @@ struct Layout {
       params, total;
   size_t part_elems;
   int alloc_ctx;
-  dd::GemmPlan p_qkv, p_o, p_gu, p_d, p_lm, p_store;
+  dd::GemmPlan p_qkv, p_o, p_gu, p_d, p_lm, p_store, p_tower;
   dd::AttnPlan p_attn;
 };
 
@@ -119,6 +119,8 @@ struct dd_ctx {
   bool have_weights;
   dd_weights w;
   std::vector<CUtensorMap> m_wqkv, m_wo, m_wgu, m_wd;
+  dd_context_tower tower;  // borrowed; tower.wkv == nullptr until dd_set_context_tower
+  CUtensorMap m_tower;
   CUtensorMap m_lm, m_y_b, m_attn_b, m_h_b, m_y_a, m_kc, m_vc, m_kc128, m_vc128, m_q;
   cudaStream_t cap_stream;
   cudaGraphExec_t exec;       // one denoising step
@@ -191,6 +193,7 @@ Layout make_layout(const dd_config& c) {
   L.p_lm = dd::plan_gemm(dd::kEpiSelect, R, c.vocab, c.hidden, 1);
   L.p_store = dd::plan_gemm(dd::kEpiStore, R, c.vocab, c.hidden, 1);
   L.p_attn = dd::plan_attention(c.batch, c.block, c.n_q_heads, c.n_kv_heads, c.head_dim, c.max_ctx);
+  L.p_tower = dd::plan_gemm(dd::kEpiPartial, R, c.n_layers * 2 * c.n_kv_heads * c.head_dim, c.hidden, 1);
   size_t pe = 0;
   auto upd = [&](const dd::GemmPlan& p, int N) {
     size_t e = (size_t)p.splits * R * N;
@@ -200,6 +203,7 @@ Layout make_layout(const dd_config& c) {
   upd(L.p_o, c.hidden);
   upd(L.p_gu, 2 * c.mlp);
   upd(L.p_d, c.hidden);
+  upd(L.p_tower, c.n_layers * 2 * c.n_kv_heads * c.head_dim);
   L.part_elems = pe;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -227,7 +231,7 @@ Layout make_layout(const dd_config& c) {
   L.tok = take((size_t)R * 4);
   L.mask = take((size_t)c.batch * 4);
   L.ncommit = take((size_t)c.batch * 4);
-  L.small = take(32);   // [0] remaining, [1] status, [2] ctx_len, [3] steps, [4] step limit
+  L.small = take(32);   // [0] remaining, [1] status, [2] ctx_len, [3] steps, [4] step limit, [5] append counter
   L.params = take(8);   // gamma, mode
   L.total = off;
   return L;
@@ -582,6 +586,50 @@ dd_status dd_set_context_kv(dd_ctx* c, const void* k, const void* v, int32_t t0,
   }
   DD_CUDA(dd::launch_set_int(small_ptr(c) + 2, t0 + n, st));
   c->ctx_len = t0 + n;
+  return DD_OK;
+}
+
+dd_status dd_set_context_tower(dd_ctx* c, const dd_context_tower* t) {
+  if (!c) return fail(DD_ERR_INVALID_ARG, "ctx is NULL");
+  if (!t || !t->embed || !t->g || !t->wkv) return fail(DD_ERR_INVALID_ARG, "context tower weights are NULL");
+  const dd_config& cf = c->cfg;
+  for (const void* ptr : {t->embed, t->g, t->wkv})
+    if (reinterpret_cast<uintptr_t>(ptr) % 16) return fail(DD_ERR_INVALID_ARG, "context tower weights must be 16-byte aligned");
+  if (!encode_fn()) return fail(DD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
+  const uint64_t n = (uint64_t)cf.n_layers * 2 * cf.n_kv_heads * cf.head_dim;
+  if (n % 128) return fail(DD_ERR_UNSUPPORTED, "n_layers*2*n_kv_heads*head_dim must be a multiple of 128");
+  if (!dd::make_map_2d(&c->m_tower, t->wkv, n, cf.hidden, 128))
+    return fail(DD_ERR_CUDA, "tensor map encoding failed for the context tower");
+  c->tower = *t;
+  return DD_OK;
+}
+
+dd_status dd_append_block(dd_ctx* c, const int32_t* tokens, void* stream) {
+  dd_status s = check_ctx(c);
+  if (s != DD_OK) return s;
+  if (!c->tower.wkv) return fail(DD_ERR_NOT_READY, "no context tower (call dd_set_context_tower)");
+  if (!tokens) return fail(DD_ERR_INVALID_ARG, "tokens is NULL");
+  const dd_config& cf = c->cfg;
+  if (c->ctx_len + cf.block > cf.max_ctx)
+    return fail(DD_ERR_INVALID_ARG, "context %d + block %d exceeds max_ctx %d", c->ctx_len, cf.block, cf.max_ctx);
+  DD_CUDA(dd::prepare_kernels());
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = c->ws;
+  const Layout& L = c->L;
+  const int R = c->R, N = cf.n_layers * 2 * cf.n_kv_heads * cf.head_dim;
+  int* small = small_ptr(c);
+  DD_CUDA(dd::launch_tower_embed_norm(tokens, c->tower.embed, c->tower.g, ws + L.y, R, cf.hidden, cf.vocab,
+                                      cf.rms_eps, st));
+  dd::GemmOut o{};
+  o.partial = at<float>(ws, L.part);
+  o.split_stride = (long long)R * N;
+  o.ld = N;
+  o.rows_valid = R;
+  DD_CUDA(dd::launch_gemm(L.p_tower, c->m_tower, c->m_y_b, o, small + 1, c->timeout_ns, st));
+  DD_CUDA(dd::launch_reduce_kv_append(o.partial, L.p_tower.splits, o.split_stride, R, N, cf.block, cf.batch,
+                                      cf.n_kv_heads, cf.head_dim, L.alloc_ctx, small + 2,
+                                      reinterpret_cast<unsigned int*>(small + 5), ws + L.kc, ws + L.vc, st));
+  c->ctx_len += cf.block;
   return DD_OK;
 }
 

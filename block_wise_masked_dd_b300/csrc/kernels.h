@@ -131,6 +131,16 @@ cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const
 // to position *ctx_len + r % S (see dd_config.rope_theta).
 cudaError_t launch_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N, void* out, int S,
                               int D, int qk_cols, const int* ctx_len, float theta, cudaStream_t st);
+// Context tower (dd_append_block): y = RMSNorm(embed[token]) * g as bf16
+// head + remainder; then the split-K sum of y W_kv^T scattered as bf16 into the
+// K/V cache [L][B][Hkv][alloc_ctx][D] at positions *ctx_len + i, after which
+// *ctx_len grows by S.
+cudaError_t launch_tower_embed_norm(const int32_t* tokens, const void* embed, const void* g, void* y_split, int rows,
+                                    int H, int V, float eps, cudaStream_t st);
+// `done` is a zeroed counter the kernel leaves zeroed again.
+cudaError_t launch_reduce_kv_append(const float* part, int splits, long long split_stride, int rows, int N, int S,
+                                    int B, int Hkv, int D, int alloc_ctx, int* ctx_len, unsigned int* done, void* kc,
+                                    void* vc, cudaStream_t st);
 cudaError_t launch_reduce_f32(const float* part, int splits, long long split_stride, int rows, int N, float* out,
                               cudaStream_t st);
 cudaError_t launch_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,

@@ -220,6 +220,68 @@ __global__ void k_reduce_qkv(const float* part, int splits, long long split_stri
   }
 }
 
+// Context tower, first half: y[r] = RMSNorm(embed[tokens[r]]) * g as head +
+// remainder (ids outside [0, V) read row 0).  One CTA per row.
+__global__ void k_tower_embed_norm(const int32_t* tokens, const __nv_bfloat16* embed, const __nv_bfloat16* g,
+                                   __nv_bfloat16* y, int H, int V, float eps) {
+  __shared__ float red[32];
+  const int r = blockIdx.x, R = gridDim.x;
+  const int passes = H / (8 * blockDim.x);
+  float gv[kMaxRowPasses][8];
+  load_gains(g, passes, gv);
+  pdl_wait();
+  pdl_launch_dependents();
+  const int t = tokens[r];
+  const int id = (t < 0 || t >= V) ? 0 : t;
+  float xv[kMaxRowPasses][8];
+#pragma unroll
+  for (int p = 0; p < kMaxRowPasses; ++p) {
+    if (p >= passes) break;
+    load8_bf16(embed + (long long)id * H + (p * blockDim.x + threadIdx.x) * 8, xv[p]);
+  }
+  norm_store(xv, passes, r, H, R, gv, y, eps, red);
+}
+
+// Context tower, second half: the split-K sum of y W_kv^T (column n of row
+// r = b*S + i is layer n / (2 Hkv D), K or V, kv head, dim) rounded to bf16
+// and stored at cache position T + i, T = *ctx_len; the last CTA to finish
+// then advances *ctx_len by S.
+__global__ void k_reduce_kv_append(const float* part, int splits, long long split_stride, int rows, int N, int S,
+                                   int B, int Hkv, int D, int alloc_ctx, int* ctx_len, __nv_bfloat16* kc,
+                                   __nv_bfloat16* vc, unsigned int* done) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int T = *ctx_len;
+  const long long total = (long long)rows * N;
+  const int kvw = Hkv * D;
+  for (long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8; e < total;
+       e += (long long)gridDim.x * blockDim.x * 8) {
+    float acc[8];
+    load8_f32(part + e, acc);
+    add_partials<8>(part + e, 1, splits, split_stride, acc);
+    const int r = (int)(e / N), n = (int)(e % N);
+    const int l = n / (2 * kvw), rem = n % (2 * kvw);
+    const int h = (rem % kvw) / D, d = rem % D;
+    const int b = r / S, i = r % S;
+    __nv_bfloat16* dst = (rem < kvw ? kc : vc) + ((((long long)l * B + b) * Hkv + h) * alloc_ctx + T + i) * D + d;
+    uint4 o, unused;
+    split_bf16(acc[0], acc[1], o.x, unused.x);
+    split_bf16(acc[2], acc[3], o.y, unused.y);
+    split_bf16(acc[4], acc[5], o.z, unused.z);
+    split_bf16(acc[6], acc[7], o.w, unused.w);
+    *reinterpret_cast<uint4*>(dst) = o;
+  }
+  // every CTA has read *ctx_len; the last one to get here moves it on
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(done, 1u) == gridDim.x - 1) {
+      *ctx_len = T + S;
+      *done = 0;
+    }
+  }
+}
+
 // h[r][f] = silu(gate) * up, gate = column f, up = column F + f of the
 // summed partials [rows][2F]; head + remainder (remainder at h + rows*F).
 __global__ void k_reduce_swiglu(const float* part, int splits, long long split_stride, __nv_bfloat16* h, int rows,
@@ -443,6 +505,7 @@ cudaError_t prepare_small_kernels() {
                        (const void*)k_reduce,
                        (const void*)k_reduce_swiglu,         (const void*)k_select_combine,
                        (const void*)k_reduce_qkv,
+                       (const void*)k_tower_embed_norm,      (const void*)k_reduce_kv_append,
                        (const void*)k_commit};
   cudaError_t e = cudaSuccess;
   for (const void* f : fns) {
@@ -462,6 +525,19 @@ cudaError_t launch_reduce_qkv(const float* part, int splits, long long split_str
                               int D, int qk_cols, const int* ctx_len, float theta, cudaStream_t st) {
   return launch_k(k_reduce_qkv, grid_for((long long)rows * N / 8, 256), 256, 0, st, part, splits, split_stride, rows,
                   N, (__nv_bfloat16*)out, S, D, qk_cols, ctx_len, theta);
+}
+
+cudaError_t launch_tower_embed_norm(const int32_t* tokens, const void* embed, const void* g, void* y, int rows, int H,
+                                    int V, float eps, cudaStream_t st) {
+  return launch_k(k_tower_embed_norm, rows, row_threads(H), 0, st, tokens, (const __nv_bfloat16*)embed,
+                  (const __nv_bfloat16*)g, (__nv_bfloat16*)y, H, V, eps);
+}
+
+cudaError_t launch_reduce_kv_append(const float* part, int splits, long long split_stride, int rows, int N, int S,
+                                    int B, int Hkv, int D, int alloc_ctx, int* ctx_len, unsigned int* done, void* kc,
+                                    void* vc, cudaStream_t st) {
+  return launch_k(k_reduce_kv_append, grid_for((long long)rows * N / 8, 256), 256, 0, st, part, splits, split_stride,
+                  rows, N, S, B, Hkv, D, alloc_ctx, ctx_len, (__nv_bfloat16*)kc, (__nv_bfloat16*)vc, done);
 }
 
 cudaError_t launch_reduce_f32(const float* part, int splits, long long split_stride, int rows, int N, float* out,

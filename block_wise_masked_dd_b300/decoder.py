@@ -111,6 +111,22 @@ class Decoder:
         steps = B.dd_decode_block(self.ctx, _ptr(tokens), gamma, mode, max_steps, _stream(stream))
         return tokens, steps
 
+    def set_context_tower(self, tower: dict):
+        """Register the synthetic context tower: "ctx_embed" [V][H], "ctx_g" [H],
+        "ctx_wkv" [L][2*Hkv*D][H] (np.uint16 bf16 bits or bf16 tensors; kept
+        alive here)."""
+        def t(name):
+            v = tower[name]
+            return (v if isinstance(v, torch.Tensor) else bits_to_tensor(v, "cpu")).contiguous().to(self.device)
+        self.tower = {n: t(n) for n in ("ctx_embed", "ctx_g", "ctx_wkv")}
+        B.dd_set_context_tower(self.ctx, _ptr(self.tower["ctx_embed"]), _ptr(self.tower["ctx_g"]),
+                               _ptr(self.tower["ctx_wkv"]))
+
+    def append_block(self, tokens: torch.Tensor, stream=None):
+        """Encode the committed block `tokens` [B][S] (device int32) with the
+        context tower and append its K/V to the context."""
+        B.dd_append_block(self.ctx, _ptr(tokens), _stream(stream))
+
     def device_status(self, stream=None):
         """Raise DDError if a kernel of this context recorded an expired bounded wait."""
         B.dd_device_status(self.ctx, _stream(stream))

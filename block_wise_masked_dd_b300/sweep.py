@@ -26,19 +26,24 @@ def main():
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--modes", nargs="+", default=["mock_ar", "topk:2", "steps:8"],
                     help="commit modes run besides the threshold rule at each gamma")
+    ap.add_argument("--extras", action="store_true",
+                    help="also gamma 0.8 with the context grown by the context tower, and with RoPE positions")
     args = ap.parse_args()
     rows = []
     for cfg in args.configs:
-        for gamma, mode in [(g, "threshold") for g in GAMMAS] + [(0.8, m) for m in args.modes]:
+        runs = [(g, "threshold", []) for g in GAMMAS] + [(0.8, m, []) for m in args.modes]
+        if args.extras:
+            runs += [(0.8, "threshold", ["--context-tower"]), (0.8, "threshold", ["--rope-theta", "10000"])]
+        for gamma, mode, extra in runs:
             cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--config", cfg, "--gamma", str(gamma), "--mode",
-                   mode, "--steps", str(args.steps), "--warmup", str(args.warmup), "--no-micro", "--no-cpu"]
+                   mode, "--steps", str(args.steps), "--warmup", str(args.warmup), "--no-micro", "--no-cpu", *extra]
             out = subprocess.run(cmd, capture_output=True, text=True, cwd=ROOT)
             if out.returncode != 0:
                 print(json.dumps({"config": cfg, "gamma": gamma, "mode": mode, "error": out.stderr[-2000:]}))
                 continue
             line = json.loads(out.stdout.strip().splitlines()[-1])
             print(json.dumps(line), flush=True)
-            rows.append((cfg, gamma, mode, line))
+            rows.append((cfg, gamma, mode + (" " + " ".join(extra) if extra else ""), line))
     print("\n| workload | gamma | mode | steps/block | committed tokens/s | e2e tokens/s | ms per bench step | "
           "SM MHz | throttle |")
     print("|---|---|---|---|---|---|---|---|---|")

@@ -143,6 +143,28 @@ dd_status dd_init_weights(dd_ctx* ctx, const dd_weights* w);
 dd_status dd_set_context_kv(dd_ctx* ctx, const void* k, const void* v, int32_t t0, int32_t n,
                             void* stream);
 
+/* Weights of a synthetic context tower (the survey's NEXT-2 row; the pages'
+ * frozen autoregressive tower is out of scope): one position-wise dense layer,
+ * y = RMSNorm(embed[token]) * g, and per denoiser layer l the K rows then the V
+ * rows y W_kv[l]^T.  Borrowed bf16 device pointers, 16-byte aligned:
+ * embed [V][H], g [H], wkv [L][2*Hkv*D][H]. */
+typedef struct dd_context_tower {
+  const void* embed;
+  const void* g;
+  const void* wkv;
+} dd_context_tower;
+
+/* Register (or replace) the context tower.  Synchronous on the host; enqueues
+ * nothing. */
+dd_status dd_set_context_tower(dd_ctx* ctx, const dd_context_tower* tower);
+
+/* Encode a committed block with the context tower and append it to the
+ * context on the device: the K/V of every layer at positions [T, T+S) (T =
+ * the current context length, then T += S), with no host round trip.
+ * tokens: int32 [B][S] device memory (ids in [0, V); others read id 0).
+ * Requires T + S <= max_ctx.  Asynchronous on `stream`. */
+dd_status dd_append_block(dd_ctx* ctx, const int32_t* tokens, void* stream);
+
 /* ------------------------------------------------------------------ decode */
 
 /* One denoising step (explainer steps 2-4).  tokens: int32 [B][S], mask:

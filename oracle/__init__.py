@@ -24,6 +24,7 @@ from .decode import (  # noqa: F401
     MODE_THRESHOLD,
     MODE_TOPK,
     OracleModel,
+    append_block,
     StepResult,
     block_attention,
     commit,

@@ -344,6 +344,34 @@ def denoise_step(model: OracleModel, tokens, mask, gamma: float, mode: int = MOD
                       tie, fallback, attn_outs, hf if keep_intermediates else None)
 
 
+def append_block(model: OracleModel, tower: dict, tokens) -> OracleModel:
+    """The context tower's encoding of a committed block, appended to the
+    context (the TwoTower article's frozen causal tower; the survey's NEXT-2
+    reading: one position-wise dense layer, hence causal): per committed token
+    y = RMSNorm(E_ctx[token]) * g_ctx, then for every denoiser layer l the K and
+    V rows y W_kv[l]^T, stored in bf16 like the rest of the context at
+    positions [T, T + S).  Returns the model with the longer context.
+
+    tower: "ctx_embed" [V, H], "ctx_g" [H], "ctx_wkv" [L, 2*Hkv*D, H] (fp32
+    holding bf16 values).
+    """
+    cfg = model.cfg
+    B, S, L = cfg.batch, cfg.block, cfg.n_layers
+    Hkv, D = cfg.n_kv_heads, cfg.head_dim
+    T = model.ctx_len
+    ids = np.asarray(tokens, np.int64).reshape(B * S)
+    y = rmsnorm(tower["ctx_embed"][ids].astype(F32), tower["ctx_g"], cfg.rms_eps)
+    k_new = np.empty((L, B, Hkv, S, D), F32)
+    v_new = np.empty((L, B, Hkv, S, D), F32)
+    for l in range(L):
+        kv = round_bf16(y @ tower["ctx_wkv"][l].astype(F32).T)         # [B*S, 2*Hkv*D]
+        k_new[l] = kv[:, :Hkv * D].reshape(B, S, Hkv, D).transpose(0, 2, 1, 3)
+        v_new[l] = kv[:, Hkv * D:].reshape(B, S, Hkv, D).transpose(0, 2, 1, 3)
+    k = np.concatenate([model.k_ctx[:, :, :, :T], k_new], axis=3)
+    v = np.concatenate([model.v_ctx[:, :, :, :T], v_new], axis=3)
+    return OracleModel(cfg, model.w, k, v, T + S)
+
+
 def decode_block(model: OracleModel, gamma: float, mode: int = MODE_THRESHOLD,
                  max_steps: int | None = None, act_bf16: bool = False):
     """Fill one block: start all-[MASK], step until no position is masked

@@ -173,6 +173,27 @@ def make_weights(cfg: Config, seed: int = 0) -> dict:
     return w
 
 
+def tower_names(cfg: Config):
+    """The synthetic context tower's tensors: its token embedding [V][H] and, per
+    denoiser layer, the K rows then the V rows it produces ([L][2*Hkv*D][H])."""
+    return [("ctx_embed", (cfg.vocab, cfg.hidden)),
+            ("ctx_wkv", (cfg.n_layers, 2 * cfg.n_kv_heads * cfg.head_dim, cfg.hidden))]
+
+
+def make_tower_weights(cfg: Config, seed: int = 0) -> dict:
+    """Context-tower weights as bf16 bits: embedding N(0, 0.02), projections
+    N(0, 1/H) so the produced K/V are ~N(0,1) like the synthetic context;
+    gain "ctx_g" ones."""
+    names = tower_names(cfg)
+    streams = np.random.SeedSequence([seed, 0x544F57]).spawn(len(names))
+    w = {}
+    for (name, shape), ss in zip(names, streams):
+        std = WEIGHT_STD if name == "ctx_embed" else 1.0 / np.sqrt(cfg.hidden)
+        w[name] = _normal_bf16(np.random.default_rng(ss), shape, std)
+    w["ctx_g"] = to_bf16_bits(np.ones(cfg.hidden, np.float32))
+    return w
+
+
 def make_context_kv(cfg: Config, seed: int = 0, t0: int = 0, n: int | None = None):
     """Context K and V for positions [t0, t0+n) as bf16 bits, layout [L][B][Hkv][n][D].
 
@@ -257,6 +278,18 @@ def make_weights_torch(cfg: Config, seed: int, device) -> dict:
         w[f"g_attn{l}"] = one.clone()
         w[f"g_mlp{l}"] = one.clone()
     w["g_final"] = one.clone()
+    return w
+
+
+def make_tower_weights_torch(cfg: Config, seed: int, device) -> dict:
+    """Context-tower weights as bf16 torch tensors drawn on `device` (same
+    names, shapes and scales as `make_tower_weights`, different stream)."""
+    import torch
+    gen = torch_generator(seed * 7919 + 0x544F57, device)
+    w = {name: torch_normal_bf16(shape, WEIGHT_STD if name == "ctx_embed" else 1.0 / np.sqrt(cfg.hidden), gen,
+                                 device)
+         for name, shape in tower_names(cfg)}
+    w["ctx_g"] = torch.ones(cfg.hidden, dtype=torch.bfloat16, device=device)
     return w
 
 

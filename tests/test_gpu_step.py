@@ -193,3 +193,27 @@ def test_small_rope_first_step():
     compare_step(p, tok, mask, 0.8)
     tok, mask = synth.make_tokens(p.cfg, seed=9, masked_frac=0.4)
     compare_step(p, tok, mask, 0.8)
+
+
+# ------------------------------------------------------ context tower on device
+
+@pytest.mark.parametrize("cfg", [synth.TINY.replace(max_ctx=256 + 32), synth.SMALL],
+                         ids=["tiny", "small"])
+def test_append_block_then_next_block_matches_oracle(cfg):
+    """Decode a block, encode it with the context tower on the device, then step
+    the next block state-synced against the oracle's own append (twice)."""
+    require_gpu()
+    p = Problem(cfg)
+    tw_bits = synth.make_tower_weights(cfg, 0)
+    tw = {k: synth.bf16_bits_to_f32(v) for k, v in tw_bits.items()}
+    p.dec.set_context_tower(tw_bits)
+    for blk in range(2):
+        tokens, _ = p.dec.decode_block(0.8)
+        p.dec.append_block(tokens)
+        torch.cuda.synchronize()
+        p.model = oracle.append_block(p.model, tw, tokens.cpu().numpy())
+        tok, mask = p.start_state()
+        steps = 0
+        while mask.max() and steps < (16 if cfg.name == "tiny" else 3):
+            tok, mask, _, _ = compare_step(p, tok, mask, 0.8, logits=(steps == 0))
+            steps += 1

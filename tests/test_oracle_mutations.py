@@ -54,6 +54,9 @@ MUTANTS = {
     "rope_wrong_sign": ("rope", [("x[..., 0::2] * s + x[..., 1::2] * c", "x[..., 1::2] * c - x[..., 0::2] * s")]),
     "rope_wrong_frequency": ("rope", [("-2.0 * np.arange(D // 2, dtype=np.float64) / D", "-1.0 * np.arange(D // 2, dtype=np.float64) / D")]),
     "step_rope_keys_unrotated": ("denoise_step", [("k = np.stack([rope(k[b], pos, cfg.rope_theta) for b in range(B)])", "pass")]),
+    "append_swaps_k_and_v": ("append_block", [("k_new[l] = kv[:, :Hkv * D]", "k_new[l] = kv[:, Hkv * D:]")]),
+    "append_without_norm": ("append_block", [('y = rmsnorm(tower["ctx_embed"][ids].astype(F32), tower["ctx_g"], cfg.rms_eps)',
+                                              'y = tower["ctx_embed"][ids].astype(F32)')]),
     "steps_schedule_off_by_one": ("steps_schedule_k", [("steps_left = n_steps - t\n", "steps_left = n_steps - t + 1\n")]),
 }
 
@@ -104,6 +107,8 @@ def _pins(tiny):
         pins.test_rope_closed_forms,
         pins.test_rope_scores_depend_on_relative_position,
         pins.test_full_step_with_rope_vs_bruteforce,
+        pins.test_append_block_vs_bruteforce,
+        lambda: pins.test_decode_after_append_sees_the_new_context(tiny),
     ]
 
 

@@ -437,3 +437,47 @@ def test_full_step_with_rope_vs_bruteforce():
     assert (r.arg.reshape(-1) == np.array(arg)).all()
     plain = oracle.denoise_step(_micro_model(MICRO), tok, mask, 0.8, keep_intermediates=True)
     assert np.abs(plain.logits - r.logits).max() > 1e-3   # the rotation reaches the logits
+
+
+# ------------------------------------------------- context tower (append)
+
+def _tower(cfg, seed=0):
+    return {k: synth.bf16_bits_to_f32(v) for k, v in synth.make_tower_weights(cfg, seed).items()}
+
+
+def test_append_block_vs_bruteforce():
+    cfg = MICRO
+    m = _micro_model(cfg)
+    tw = _tower(cfg)
+    rng = np.random.default_rng(14)
+    tok = rng.integers(0, cfg.vocab, (cfg.batch, cfg.block)).astype(np.int32)
+    tok[0, 1] = tok[0, 3]                                         # a repeated token
+    m2 = oracle.append_block(m, tw, tok)
+    T, S, Hkv, D = m.ctx_len, cfg.block, cfg.n_kv_heads, cfg.head_dim
+    assert m2.ctx_len == T + S
+    np.testing.assert_array_equal(m2.k_ctx[:, :, :, :T], m.k_ctx[:, :, :, :T])
+    np.testing.assert_array_equal(m2.v_ctx[:, :, :, :T], m.v_ctx[:, :, :, :T])
+    g = tw["ctx_g"].tolist()
+    for b in range(cfg.batch):
+        for i in range(S):
+            y = bf.rmsnorm(tw["ctx_embed"][tok[b, i]].tolist(), g, cfg.rms_eps)
+            for l in range(cfg.n_layers):
+                kv = [bf.bf16(v) for v in bf.matvec(tw["ctx_wkv"][l].tolist(), y)]
+                for h in range(Hkv):
+                    want_k = np.array(kv[h * D:(h + 1) * D], F32)
+                    want_v = np.array(kv[Hkv * D + h * D:Hkv * D + (h + 1) * D], F32)
+                    ulp = np.abs(want_k) * 2.0 ** -7 + 1e-30
+                    assert (np.abs(m2.k_ctx[l, b, h, T + i] - want_k) <= ulp).all()
+                    assert (np.abs(m2.v_ctx[l, b, h, T + i] - want_v) <= np.abs(want_v) * 2.0 ** -7 + 1e-30).all()
+    np.testing.assert_array_equal(m2.k_ctx[:, 0, :, T + 1], m2.k_ctx[:, 0, :, T + 3])   # position-wise layer
+
+
+def test_decode_after_append_sees_the_new_context(tiny_model):
+    cfg = tiny_model.cfg
+    tw = _tower(cfg)
+    tok, _, _ = oracle.decode_block(tiny_model, 0.8)
+    m2 = oracle.append_block(tiny_model, tw, tok)
+    start = np.full((cfg.batch, cfg.block), cfg.vocab, np.int32), np.full(cfg.batch, 0xFFFF, np.uint32)
+    a = oracle.denoise_step(tiny_model, *start, 0.8, keep_intermediates=True)
+    b = oracle.denoise_step(m2, *start, 0.8, keep_intermediates=True)
+    assert np.abs(a.logits - b.logits).max() > 1e-4
