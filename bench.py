@@ -225,7 +225,10 @@ def run_reference(args, world, rank):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-            "data": "synthetic", "config": {"workload": workload_desc(cfg, args.gamma, args.mode)},
+            "data": "synthetic",
+            "config": {"workload": workload_desc(cfg, args.gamma, args.mode), "tokens_per_step": c.batch * c.block,
+                       "parallelism": f"host cores ({os.cpu_count()} threads), rank 0 only",
+                       "sample": f"{c.batch} sequence(s) of the workload, one block per step"},
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
