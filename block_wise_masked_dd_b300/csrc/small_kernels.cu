@@ -187,10 +187,14 @@ __global__ void k_reduce(const float* part, int splits, long long split_stride, 
 // q|k|v = the sum of the split-K partials, written as bf16 head (rows
 // [0, rows)) + remainder (rows [rows, 2 rows)).  With theta > 0 the pairs
 // (2j, 2j+1) of every query and key head (columns < qk_cols) of row r turn by
-// (T + r % S) * theta^(-2j/D) radians, T = *ctx_len: angle, cosine and sine in
-// double, the rotation in fp32.
+// (T + r % S) * theta^(-2j/D) radians, T = *ctx_len: the frequencies and the
+// angle in double, the angle reduced modulo 2 pi in double before an fp32
+// sine and cosine, the rotation in fp32.
 __global__ void k_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N,
                              __nv_bfloat16* out, int S, int D, int qk_cols, const int* ctx_len, float theta) {
+  __shared__ double freq[64];  // theta^(-2j/D), j < D/2 (D <= 128)
+  if (theta > 0.f && threadIdx.x < D / 2) freq[threadIdx.x] = pow((double)theta, -2.0 * threadIdx.x / D);
+  __syncthreads();
   pdl_wait();
   pdl_launch_dependents();
   const long long total = (long long)rows * N;
@@ -206,11 +210,11 @@ __global__ void k_reduce_qkv(const float* part, int splits, long long split_stri
       const double pos = (double)(T + (int)(e / N) % S);
 #pragma unroll
       for (int p = 0; p < 4; ++p) {
-        const int j = (d0 >> 1) + p;
-        const double ang = pos * pow((double)theta, -2.0 * j / D);
-        double sd, cd;
-        sincos(ang, &sd, &cd);
-        const float c = (float)cd, sn = (float)sd;
+        const double ang = pos * freq[(d0 >> 1) + p];
+        const double two_pi = 6.283185307179586;
+        const float red = (float)(ang - rint(ang / two_pi) * two_pi);
+        float sn, c;
+        sincosf(red, &sn, &c);
         const float x0 = acc[2 * p], x1 = acc[2 * p + 1];
         acc[2 * p] = x0 * c - x1 * sn;
         acc[2 * p + 1] = x0 * sn + x1 * c;
