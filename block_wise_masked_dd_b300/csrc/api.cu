@@ -102,8 +102,8 @@ bool make_map_q(CUtensorMap* m, const void* qkv, uint64_t rows, uint64_t ld, int
 // ---------------------------------------------------------------------------
 
 struct Layout {
-  size_t kc, vc, x, y, qkv, attn, hmid, part, attn_part, sel_m, sel_s, sel_a, conf, arg, tok, mask, ncommit, small,
-      params, total;
+  size_t kc, vc, x, y, yc, row_index, qkv, attn, hmid, part, attn_part, sel_m, sel_s, sel_a, conf, arg, tok, mask,
+      ncommit, small, params, total;
   size_t part_elems;
   int alloc_ctx;
   dd::GemmPlan p_qkv, p_o, p_gu, p_d, p_lm, p_store, p_tower;
@@ -121,7 +121,7 @@ struct dd_ctx {
   std::vector<CUtensorMap> m_wqkv, m_wo, m_wgu, m_wd;
   dd_context_tower tower;  // borrowed; tower.wkv == nullptr until dd_set_context_tower
   CUtensorMap m_tower;
-  CUtensorMap m_lm, m_y_b, m_attn_b, m_h_b, m_y_a, m_kc, m_vc, m_kc128, m_vc128, m_q;
+  CUtensorMap m_lm, m_y_b, m_attn_b, m_h_b, m_y_a, m_yc_a, m_kc, m_vc, m_kc128, m_vc128, m_q;
   cudaStream_t cap_stream;
   cudaGraphExec_t exec;       // one denoising step
   cudaGraphExec_t loop_exec;  // while (masked left): step  -- the device-side decode loop
@@ -217,6 +217,9 @@ Layout make_layout(const dd_config& c) {
   L.x = take((size_t)R * c.hidden * 4);
   // bf16 activations: heads in rows [0, R), remainders in rows [R, 2R)
   L.y = take((size_t)2 * R * c.hidden * 2);
+  // the final norm's rows still masked, compacted (LM-head input), and their rows
+  L.yc = take((size_t)2 * R * c.hidden * 2);
+  L.row_index = take((size_t)R * 4);
   L.qkv = take((size_t)2 * R * qkvw * 2);
   L.attn = take((size_t)2 * R * HqD * 2);
   L.hmid = take((size_t)2 * R * c.mlp * 2);
@@ -231,7 +234,8 @@ Layout make_layout(const dd_config& c) {
   L.tok = take((size_t)R * 4);
   L.mask = take((size_t)c.batch * 4);
   L.ncommit = take((size_t)c.batch * 4);
-  L.small = take(32);   // [0] remaining, [1] status, [2] ctx_len, [3] steps, [4] step limit, [5] append counter
+  L.small = take(32);   // [0] remaining, [1] status, [2] ctx_len, [3] steps, [4] step limit, [5] append counter,
+                        // [6] rows still masked (the LM head's compacted rows)
   L.params = take(8);   // gamma, mode
   L.total = off;
   return L;
@@ -276,6 +280,7 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
   int* status = small_ptr(c) + 1;
   const uint8_t* g_attn = static_cast<const uint8_t*>(c->w.g_attn);
   const uint8_t* g_mlp = static_cast<const uint8_t*>(c->w.g_mlp);
+  const bool lm_compact = !probe && L.p_lm.m_tiles > 1;
 
   DD_CUDA(dd::launch_embed_norm(at<int32_t>(ws, L.tok), at<uint32_t>(ws, L.mask), c->w.embed, c->w.pos, g_attn,
                                 x, y, cf.batch, cf.block, H, cf.vocab, cf.rms_eps, st));
@@ -344,19 +349,27 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
     DD_CUDA(dd::launch_gemm(L.p_d, c->m_wd[l], c->m_h_b, o, status, c->timeout_ns, st));
     mk(kKGemmDown);
     const void* gn = (l + 1 < cf.n_layers) ? (const void*)(g_attn + (size_t)(l + 1) * H * 2) : c->w.g_final;
-    DD_CUDA(dd::launch_reduce_residual_norm(part, L.p_d.splits, o.split_stride, x, gn, y, R, H, cf.rms_eps, st));
+    // The final norm also compacts the rows still masked for the LM head
+    // (except on the probe path, which reports every row, and when the LM
+    // head has one row tile, which no compaction can skip).
+    const bool compact = lm_compact && l + 1 == cf.n_layers;
+    DD_CUDA(dd::launch_reduce_residual_norm(part, L.p_d.splits, o.split_stride, x, gn, y, R, H, cf.rms_eps, st,
+                                            compact ? at<uint32_t>(ws, L.mask) : nullptr, cf.block, ws + L.yc,
+                                            at<int>(ws, L.row_index), small_ptr(c) + 6));
     mk(kKNormDown);
   }
-  // LM head + fused select
+  // LM head + fused select, over the compacted masked rows (all rows when not compacting)
   dd::GemmOut so{};
   so.rows_valid = R;
   so.sel_m = at<float>(ws, L.sel_m);
   so.sel_s = at<float>(ws, L.sel_s);
   so.sel_a = at<int>(ws, L.sel_a);
-  DD_CUDA(dd::launch_gemm(L.p_lm, c->m_y_a, c->m_lm, so, status, c->timeout_ns, st));
+  so.rows_dev = lm_compact ? small_ptr(c) + 6 : nullptr;
+  DD_CUDA(dd::launch_gemm(L.p_lm, lm_compact ? c->m_yc_a : c->m_y_a, c->m_lm, so, status, c->timeout_ns, st));
   mk(kKLmSelect);
   DD_CUDA(dd::launch_select_combine(so.sel_m, so.sel_s, so.sel_a, L.p_lm.n_tiles, R, at<float>(ws, L.conf),
-                                    at<int>(ws, L.arg), st));
+                                    at<int>(ws, L.arg), st, so.rows_dev,
+                                    lm_compact ? at<int>(ws, L.row_index) : nullptr));
   mk(kKSelectCombine);
   if (probe) {
     if (probe->hidden)
@@ -518,6 +531,7 @@ dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_byte
             dd::make_map_2d(&c->m_attn_b, c->ws + L.attn, 2 * c->R, c->HqD, L.p_o.BN) &&
             dd::make_map_2d(&c->m_h_b, c->ws + L.hmid, 2 * c->R, cf.mlp, L.p_d.BN) &&
             dd::make_map_2d(&c->m_y_a, c->ws + L.y, 2 * c->R, cf.hidden, 128) &&
+            dd::make_map_2d(&c->m_yc_a, c->ws + L.yc, 2 * c->R, cf.hidden, 128) &&
             dd::make_map_q(&c->m_q, c->ws + L.qkv, 2 * c->R, c->qkvw, cf.n_q_heads, cf.head_dim, c->G, cf.block);
   if (!ok) {
     dd_destroy(c);

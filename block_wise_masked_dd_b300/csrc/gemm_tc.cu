@@ -70,8 +70,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint64_t* acc_full = empty + args.stages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(drain + 1);
+  uint64_t* ready = drain + 1;  // the producer has read the activation row count
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+  volatile int* rows_smem = abort_flag + 1;
+  // LM head with compacted rows: the valid row count is known on the device
+  // only.  A CTA never skips its first tile (its weights were requested
+  // before the count existed); a later tile is skipped when it starts at or
+  // beyond the count.  (A shorter MMA for a partly filled tile does not pay:
+  // tcgen05 M = 64 takes as long as M = 128.)
+  const bool dyn = EPI == kEpiSelect && args.out.rows_dev != nullptr;
 
   const int warp = warp_id();
   const int lane = lane_id();
@@ -86,6 +94,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_empty[a], 4);
     }
     mbar_init(drain, 1);
+    mbar_init(ready, 1);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&map_a);
@@ -122,6 +131,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             tma_load_2d(sa + kStageA + stage_b, &map_a, &full[s], kb * kBK, args.split_rows + mt * kBM);
         }
       };
+      auto publish_rows = [&]() {
+        *rows_smem = dyn ? *args.out.rows_dev : args.out.rows_valid;
+        mbar_arrive(ready);
+      };
       int s = 0;
       uint32_t phase = 0;
       bool ok = true, waited = false;
@@ -131,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int mt, nt;
         if (EPI == kEpiPartial) { nt = r % args.n_tiles; mt = r / args.n_tiles; }
         else { mt = r % args.m_tiles; nt = r / args.m_tiles; }
+        if (dyn && t != (int)blockIdx.x && mt * kBM >= *rows_smem) continue;
         const int kb0 = split * args.kb_per_split;
         const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
         const int count = kb1 - kb0;
@@ -150,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               pdl_wait();
               pdl_launch_dependents();
               waited = true;
+              publish_rows();
               for (int i = 0; i < pend_n; ++i) load_x(smem + pend_s[i] * stage_bytes, pend_s[i], pend_kb[i], mt, nt);
             }
           }
@@ -159,19 +174,29 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (!waited) {
         pdl_wait();
         pdl_launch_dependents();
+        publish_rows();
       }
     }
     __syncwarp();
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16_f32(kBM, args.BN);
+      bool ok = true;
+      int rows = -1;  // read when the first skippable tile comes up
       int s = 0;
       uint32_t phase = 0;
       int it = 0;
-      bool ok = true;
-      for (int t = blockIdx.x; t < args.tiles_total && ok; t += gridDim.x, ++it) {
+      for (int t = blockIdx.x; t < args.tiles_total && ok; t += gridDim.x) {
         const int split = t / per_split;
+        const int mt = EPI == kEpiPartial ? (t % per_split) / args.n_tiles : (t % per_split) % args.m_tiles;
+        if (dyn && t != (int)blockIdx.x) {
+          if (rows < 0) {
+            if (!mbar_wait_bounded(ready, 0, args.timeout_ns, abort_flag, args.status)) break;
+            rows = *rows_smem;
+          }
+          if (mt * kBM >= rows) continue;
+        }
+        const uint32_t idesc = idesc_bf16_f32(kBM, args.BN);
         const int kb0 = split * args.kb_per_split;
         const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
         const int ab = it & 1;
@@ -200,6 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (++s == args.stages) { s = 0; phase ^= 1; }
         }
         if (ok) tc_commit(&acc_full[ab]);
+        ++it;
       }
       // Drain: wait until every MMA issued by this thread has completed, so
       // TMEM can be released safely on every exit path.
@@ -210,14 +236,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else {
     // ---------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    bool rows_ok = true;
+    if (dyn) {
+      if (lane == 0) rows_ok = mbar_wait_bounded(ready, 0, args.timeout_ns, abort_flag, args.status);
+      rows_ok = __shfl_sync(0xffffffffu, rows_ok ? 1 : 0, 0) != 0;
+    }
+    const int rows = dyn ? *rows_smem : args.out.rows_valid;
     int it = 0;
-    for (int t = blockIdx.x; t < args.tiles_total; t += gridDim.x, ++it) {
+    for (int t = blockIdx.x; t < args.tiles_total && rows_ok; t += gridDim.x) {
       const int split = t / per_split, r = t % per_split;
       int mt, nt;
       if (EPI == kEpiPartial) { nt = r % args.n_tiles; mt = r / args.n_tiles; }
       else { mt = r % args.m_tiles; nt = r / args.m_tiles; }
+      if (dyn && t != (int)blockIdx.x && mt * kBM >= rows) continue;
       const int ab = it & 1;
       const uint32_t aphase = (it >> 1) & 1;
+      ++it;
       bool ok = true;
       if (lane == 0) ok = mbar_wait_bounded(&acc_full[ab], aphase, args.timeout_ns, abort_flag, args.status);
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -271,7 +305,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int j = 0; j < 64; ++j) ssum += exp2f(fmaf(v[j], kLog2e, -mb));
         }
-        if (lrow < args.out.rows_valid) {
+        if (lrow < (dyn ? rows : args.out.rows_valid)) {
           const long long o = (long long)nt * args.out.rows_valid + lrow;
           args.out.sel_m[o] = m;
           args.out.sel_s[o] = ssum;

@@ -64,6 +64,7 @@ struct GemmOut {
   float* sel_m;            // kEpiSelect: [n_tiles][rows_valid]
   float* sel_s;
   int* sel_a;
+  const int* rows_dev;     // kEpiSelect: device count of valid activation rows (compacted), or nullptr
 };
 
 // Plan a GEMM over activations [rows][K] and weights [N][K].  With
@@ -143,12 +144,19 @@ cudaError_t launch_reduce_kv_append(const float* part, int splits, long long spl
                                     void* vc, cudaStream_t st);
 cudaError_t launch_reduce_f32(const float* part, int splits, long long split_stride, int rows, int N, float* out,
                               cudaStream_t st);
+// With mask != nullptr the rows still masked are also written, compacted, to
+// y_c (head rows [0, count), remainders [rows, rows + count)), with
+// row_index[k] = the row of compacted row k and *count their number.
 cudaError_t launch_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
-                                        const void* g, void* y_split, int rows, int H, float eps, cudaStream_t st);
+                                        const void* g, void* y_split, int rows, int H, float eps, cudaStream_t st,
+                                        const uint32_t* mask = nullptr, int S = 1, void* y_c = nullptr,
+                                        int* row_index = nullptr, int* count = nullptr);
 cudaError_t launch_reduce_swiglu(const float* part, int splits, long long split_stride, void* h_split, int rows,
                                  int F, cudaStream_t st);
+// With count/row_index (compacted rows): rows r < *count, written to row_index[r].
 cudaError_t launch_select_combine(const float* sel_m, const float* sel_s, const int* sel_a, int n_tiles, int rows,
-                                  float* conf, int* arg, cudaStream_t st);
+                                  float* conf, int* arg, cudaStream_t st, const int* count = nullptr,
+                                  const int* row_index = nullptr);
 // params: device float[2] {gamma, mode-as-float}, read at run time so one
 // captured graph serves every gamma; when NULL, `gamma` and `mode` are used.
 cudaError_t launch_commit(const float* conf, const int* arg, int32_t* tokens, uint32_t* mask, const float* params,

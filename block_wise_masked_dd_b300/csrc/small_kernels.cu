@@ -86,7 +86,7 @@ __device__ __forceinline__ void add_partials(const float* p, int s0, int s1, lon
 // remainder (row R + r); x held in registers (passes of 8 per thread).
 __device__ __forceinline__ void norm_store(const float (&xv)[kMaxRowPasses][8], int passes, int r, int H, int R,
                                            const float (&gv)[kMaxRowPasses][8], __nv_bfloat16* y, float eps,
-                                           float* red) {
+                                           float* red, __nv_bfloat16* y2 = nullptr, int r2 = -1) {
   float ss = 0.f;
 #pragma unroll
   for (int p = 0; p < kMaxRowPasses; ++p) {
@@ -104,6 +104,7 @@ __device__ __forceinline__ void norm_store(const float (&xv)[kMaxRowPasses][8], 
 #pragma unroll
     for (int i = 0; i < 8; ++i) yv[i] = xv[p][i] * rs * gv[p][i];
     store8_split(y + (long long)r * H + c, y + ((long long)R + r) * H + c, yv);
+    if (r2 >= 0) store8_split(y2 + (long long)r2 * H + c, y2 + ((long long)R + r2) * H + c, yv);
   }
 }
 
@@ -151,8 +152,10 @@ __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const 
 // x[r] += sum_s part[s][r]; y[r] = RMSNorm(x[r]) * g as head + remainder.
 // One CTA per row; the split partial loads of each pass are independent.
 __global__ void k_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
-                                       const __nv_bfloat16* g, __nv_bfloat16* y, int H, float eps) {
+                                       const __nv_bfloat16* g, __nv_bfloat16* y, int H, float eps,
+                                       const uint32_t* mask, int S, __nv_bfloat16* y_c, int* row_index, int* count) {
   __shared__ float red[32];
+  __shared__ int cpos;
   const int r = blockIdx.x, R = gridDim.x;
   const int passes = H / (8 * blockDim.x);
   float gv[kMaxRowPasses][8];
@@ -168,7 +171,33 @@ __global__ void k_reduce_residual_norm(const float* part, int splits, long long 
     add_partials<8>(part + e, 0, splits, split_stride, xv[p]);
     store8_f32(x + e, xv[p]);
   }
-  norm_store(xv, passes, r, H, R, gv, y, eps, red);
+  // With `mask`: the rows still masked are also written, in order, to y_c
+  // (rows [0, count) and their remainders at [R, R + count)) for the LM head.
+  int r2 = -1;
+  if (mask) {
+    // masked rows before this one: the sequences before b (their mask words
+    // read in parallel, one block sum) plus the positions before i in b
+    const int b = r / S, i = r % S;
+    int before = 0, all = 0;
+    for (int bb = threadIdx.x; bb < R / S; bb += blockDim.x) {
+      const int n = __popc(mask[bb]);
+      before += bb < b ? n : 0;
+      all += n;
+    }
+    before = (int)block_sum((float)before, red);
+    if (r == 0) all = (int)block_sum((float)all, red);
+    if (threadIdx.x == 0) {
+      const uint32_t mb = mask[b];
+      const bool masked = (mb >> i) & 1u;
+      const int pos = before + __popc(mb & ((1u << i) - 1u));
+      cpos = masked ? pos : -1;
+      if (masked) row_index[pos] = r;
+      if (r == 0) *count = all;
+    }
+    __syncthreads();
+    r2 = cpos;
+  }
+  norm_store(xv, passes, r, H, R, gv, y, eps, red, y_c, r2);
 }
 
 // out[r][n] = sum over splits of part[s][r][n] (fp32; the standalone GEMM).
@@ -313,12 +342,12 @@ __global__ void k_reduce_swiglu(const float* part, int splits, long long split_s
 // Merge per-vocab-tile (max, sumexp, argmax) into conf = 1/sum exp(l - max)
 // and the lowest argmax.  One warp per row.
 __global__ void k_select_combine(const float* sel_m, const float* sel_s, const int* sel_a, int n_tiles, int rows,
-                                 float* conf, int* arg) {
+                                 float* conf, int* arg, const int* count, const int* row_index) {
   pdl_wait();
   pdl_launch_dependents();
   const int r = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
   const int lane = threadIdx.x & 31;
-  if (r >= rows) return;
+  if (r >= rows || (count && r >= *count)) return;
   float m = -INFINITY, s = 0.f;
   int t_best = 0x7fffffff;
   for (int t = lane; t < n_tiles; t += 32) {
@@ -349,8 +378,9 @@ __global__ void k_select_combine(const float* sel_m, const float* sel_s, const i
     t_best = tn;
   }
   if (lane == 0) {
-    conf[r] = 1.f / s;
-    arg[r] = sel_a[(long long)t_best * rows + r];
+    const int dst = row_index ? row_index[r] : r;  // compacted rows go back to their positions
+    conf[dst] = 1.f / s;
+    arg[dst] = sel_a[(long long)t_best * rows + r];
   }
 }
 
@@ -551,9 +581,10 @@ cudaError_t launch_reduce_f32(const float* part, int splits, long long split_str
 }
 
 cudaError_t launch_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
-                                        const void* g, void* y, int rows, int H, float eps, cudaStream_t st) {
+                                        const void* g, void* y, int rows, int H, float eps, cudaStream_t st,
+                                        const uint32_t* mask, int S, void* y_c, int* row_index, int* count) {
   return launch_k(k_reduce_residual_norm, rows, row_threads(H), 0, st, part, splits, split_stride, x,
-                  (const __nv_bfloat16*)g, (__nv_bfloat16*)y, H, eps);
+                  (const __nv_bfloat16*)g, (__nv_bfloat16*)y, H, eps, mask, S, (__nv_bfloat16*)y_c, row_index, count);
 }
 
 cudaError_t launch_reduce_swiglu(const float* part, int splits, long long split_stride, void* h, int rows, int F,
@@ -563,8 +594,9 @@ cudaError_t launch_reduce_swiglu(const float* part, int splits, long long split_
 }
 
 cudaError_t launch_select_combine(const float* sel_m, const float* sel_s, const int* sel_a, int n_tiles, int rows,
-                                  float* conf, int* arg, cudaStream_t st) {
-  return launch_k(k_select_combine, (rows + 7) / 8, 256, 0, st, sel_m, sel_s, sel_a, n_tiles, rows, conf, arg);
+                                  float* conf, int* arg, cudaStream_t st, const int* count, const int* row_index) {
+  return launch_k(k_select_combine, (rows + 7) / 8, 256, 0, st, sel_m, sel_s, sel_a, n_tiles, rows, conf, arg, count,
+                  row_index);
 }
 
 cudaError_t launch_commit(const float* conf, const int* arg, int32_t* tokens, uint32_t* mask, const float* params,

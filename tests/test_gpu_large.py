@@ -125,3 +125,22 @@ def test_large_decode_block_invariants(large, gamma, mode):
     else:
         assert 1 <= steps <= cfg.block
     large.dec.device_status()
+
+
+@pytest.mark.parametrize("masked_frac", [0.3, 0.05])
+def test_large_graph_step_compacted_lm_head(large, masked_frac):
+    """The step graph (LM head over the compacted masked rows: four M tiles,
+    the empty ones skipped) against the oracle on the sampled sequences."""
+    cfg = large.cfg
+    tok, mask = synth.make_tokens(cfg, seed=int(masked_frac * 100) + 7, masked_frac=masked_frac)
+    t = torch.from_numpy(tok.copy()).cuda()
+    m = torch.from_numpy(mask.view(np.int32).copy()).cuda()
+    large.dec.denoise_step(t, m, 0.8, 0)
+    torch.cuda.synchronize()
+    sel = large.sample
+    r = oracle.denoise_step(large.model, tok[sel], mask[sel], 0.8, 0)
+    g_tok, g_mask = t.cpu().numpy(), m.cpu().numpy().view(np.uint32)
+    for j, b in enumerate(sel):
+        if r.near_tie[j].any():
+            continue
+        assert g_mask[b] == r.mask[j] and (g_tok[b] == r.tokens[j]).all(), b

@@ -217,3 +217,44 @@ def test_append_block_then_next_block_matches_oracle(cfg):
         while mask.max() and steps < (16 if cfg.name == "tiny" else 3):
             tok, mask, _, _ = compare_step(p, tok, mask, 0.8, logits=(steps == 0))
             steps += 1
+
+
+# ------------------------------------------- LM head over the compacted rows
+
+def _graph_step_vs_oracle(p, tok, mask, gamma=0.8):
+    """One step through the step graph (LM head over the compacted masked rows)
+    against the oracle; sequences with a flagged near-tie are skipped."""
+    cfg = p.cfg
+    t, m = p.gpu_state(tok, mask)
+    n = torch.empty(cfg.batch, dtype=torch.int32, device="cuda")
+    p.dec.denoise_step(t, m, gamma, 0, n_committed=n)
+    torch.cuda.synchronize()
+    r = oracle.denoise_step(p.model, tok, mask, gamma, 0)
+    g_tok, g_mask = t.cpu().numpy(), m.cpu().numpy().view(np.uint32)
+    S = cfg.block
+    for b in range(cfg.batch):
+        if r.near_tie[b].any():
+            continue
+        assert g_mask[b] == r.mask[b] and (g_tok[b] == r.tokens[b]).all() and int(n[b]) == r.n_committed[b], b
+
+
+@pytest.mark.parametrize("masked_frac", [1.0, 0.6, 0.3, 0.05])
+def test_compacted_lm_head_two_row_tiles(masked_frac):
+    """256 rows (two M tiles of the LM head): masked-row counts above 128,
+    between 64 and 128 and at most 64 (a CTA whose only tile has no row left
+    still runs it, with its outputs dropped)."""
+    require_gpu()
+    p = Problem(synth.TINY.replace(batch=16))
+    if masked_frac == 1.0:
+        tok, mask = p.start_state()
+    else:
+        tok, mask = synth.make_tokens(p.cfg, seed=int(masked_frac * 100), masked_frac=masked_frac)
+    _graph_step_vs_oracle(p, tok, mask)
+
+
+@pytest.mark.parametrize("masked_frac", [0.6, 0.3, 0.05])
+def test_compacted_lm_head_small(small, masked_frac):
+    """128 rows, one M tile: the step graph with partly filled blocks (no
+    compaction, since the single tile always runs)."""
+    tok, mask = synth.make_tokens(small.cfg, seed=int(masked_frac * 100) + 1, masked_frac=masked_frac)
+    _graph_step_vs_oracle(small, tok, mask)
