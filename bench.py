@@ -70,6 +70,9 @@ def parse(argv=None):
     ap.add_argument("--context-tower", action="store_true",
                     help="append each decoded block to the context with the synthetic context tower on the device "
                          "(default: fresh seeded K/V from the host)")
+    ap.add_argument("--fused-reduce", action="store_true",
+                    help="linear layers reduce their split-K partials inside the GEMM (thread-block clusters) "
+                         "instead of in separate kernels (the default)")
     ap.add_argument("--no-micro", action="store_true", help="skip the attention / LM-head microbenchmarks")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     return ap.parse_args(argv)
@@ -240,7 +243,7 @@ def run_reference(args, world, rank):
 # DRAM bytes (dram__bytes_read.sum + dram__bytes_write.sum) of one launch, from
 # one ncu capture of the same kernel at the same workload; kinds and workloads
 # not captured report null.
-TRAFFIC = {("small", "gemm_gate_up"): 47.23e6 + 0.40e6}
+TRAFFIC = {("small", "gemm_gate_up"): 47.23e6 + 0.33e6}
 
 
 def algorithmic_bytes(cfg, kind, ctx_len):
@@ -305,6 +308,13 @@ def gpu_arm(args, world, rank, local):
     weights = pack_weights(cfg, w, dev)
     del w
     dec = Decoder(cfg, weights, dev)
+    if args.fused_reduce:
+        dec.fused_reduce = True
+    if dec.fused_reduce:
+        linear = "split-K reduced in the GEMM by clusters of " + ", ".join(
+            f"{k} {cs}" for k, (cs, _) in dec.fused_plan().items())
+    else:
+        linear = "split-K partials reduced by separate kernels"
     T0 = cfg.ctx_len
     dec.set_context_kv(k0, v0, 0)
     del k0, v0
@@ -422,6 +432,7 @@ def gpu_arm(args, world, rank, local):
             "config": {"workload": workload_desc(cfg, args.gamma, args.mode, args.context_tower),
                        "tokens_per_step": tokens_per_step, "parallelism": f"dp{world} (independent batches)",
                        "denoise_steps_per_block": timed_denoise / (args.steps * BLOCKS_PER_STEP),
+                       "linear_layers": linear,
                        "l2": "inputs larger than L2 (weights + context K/V per denoising step exceed 126 MB)"},
             "gpu_launches": timed_launches, "clocks": clk,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

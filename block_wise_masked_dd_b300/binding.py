@@ -100,9 +100,16 @@ _SIGS = {
     "dd_lmhead_select_noalloc": ([c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_void_p],
                                  c_int32),
     "dd_step_launch_count": ([c_void_p, ctypes.POINTER(c_int32)], c_int32),
+    "dd_set_option": ([c_void_p, c_int32, c_int32], c_int32),
+    "dd_get_option": ([c_void_p, c_int32, ctypes.POINTER(c_int32)], c_int32),
     "dd_profile_step": ([c_void_p, c_void_p, c_void_p, c_float, c_int32, c_void_p, c_void_p, c_int32,
                          ctypes.POINTER(c_int32), c_void_p], c_int32),
 }
+
+# dd_set_option / dd_get_option
+DD_OPT_FUSED_REDUCE = 1
+DD_OPT_FUSED_CLUSTER = {"qkv": 2, "o": 3, "gate_up": 4, "down": 5}
+DD_OPT_FUSED_GRID = {"qkv": 6, "o": 7, "gate_up": 8, "down": 9}
 
 KIND_NAMES = ["embed_norm", "gemm_qkv", "reduce_qkv", "attention_context", "attention_merge", "gemm_o", "norm_o",
               "gemm_gate_up", "swiglu", "gemm_down", "norm_down", "lm_head_select", "select_combine", "commit"]
@@ -248,6 +255,16 @@ def dd_step_launch_count(ctx: int) -> int:
     n = c_int32(0)
     _check(load().dd_step_launch_count(ctx, ctypes.byref(n)))
     return n.value
+
+
+def dd_set_option(ctx: int, option: int, value: int):
+    _check(load().dd_set_option(ctx, option, value))
+
+
+def dd_get_option(ctx: int, option: int) -> int:
+    v = c_int32(0)
+    _check(load().dd_get_option(ctx, option, ctypes.byref(v)))
+    return v.value
 
 
 def dd_profile_step(ctx: int, tokens: int, mask: int, gamma: float, mode: int, cap: int = 512, stream: int = 0):

@@ -12,7 +12,7 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libdd.so")
-SOURCES = ["api.cu", "gemm_tc.cu", "attention.cu", "attention_tc.cu", "small_kernels.cu", "noalloc.cu"]
+SOURCES = ["api.cu", "gemm_tc.cu", "gemm_fused.cu", "attention.cu", "attention_tc.cu", "small_kernels.cu", "noalloc.cu"]
 HEADERS = ["kernels.h", "ptx.cuh"]
 NVCC = os.environ.get("NVCC", "/usr/local/cuda/bin/nvcc")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

@@ -103,7 +103,7 @@ bool make_map_q(CUtensorMap* m, const void* qkv, uint64_t rows, uint64_t ld, int
 
 struct Layout {
   size_t kc, vc, x, y, yc, row_index, qkv, attn, hmid, part, attn_part, sel_m, sel_s, sel_a, conf, arg, tok, mask,
-      ncommit, small, params, total;
+      ncommit, small, params, sq_a, sq_b, total;
   size_t part_elems;
   int alloc_ctx;
   dd::GemmPlan p_qkv, p_o, p_gu, p_d, p_lm, p_store, p_tower;
@@ -119,6 +119,11 @@ struct dd_ctx {
   bool have_weights;
   dd_weights w;
   std::vector<CUtensorMap> m_wqkv, m_wo, m_wgu, m_wd;
+  std::vector<CUtensorMap> m_wgu64;  // gate|up weights with 64-row boxes (the fused SwiGLU tiles)
+  // Linear layers with the split-K reduction and epilogue inside the GEMM
+  // (thread-block clusters); fused_ok: planned for this shape and device.
+  dd::GemmPlan f_qkv, f_o, f_gu, f_d;
+  bool fused_ok, fused_on;
   dd_context_tower tower;  // borrowed; tower.wkv == nullptr until dd_set_context_tower
   CUtensorMap m_tower;
   CUtensorMap m_lm, m_y_b, m_attn_b, m_h_b, m_y_a, m_yc_a, m_kc, m_vc, m_kc128, m_vc128, m_q;
@@ -237,6 +242,10 @@ Layout make_layout(const dd_config& c) {
   L.small = take(32);   // [0] remaining, [1] status, [2] ctx_len, [3] steps, [4] step limit, [5] append counter,
                         // [6] rows still masked (the LM head's compacted rows)
   L.params = take(8);   // gamma, mode
+  // per-128-feature-tile row sums of squares of the deferred RMSNorms (fused
+  // linear layers): before attention and before the MLP
+  L.sq_a = take((size_t)(c.hidden / 128) * R * 4);
+  L.sq_b = take((size_t)(c.hidden / 128) * R * 4);
   L.total = off;
   return L;
 }
@@ -281,23 +290,46 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
   const uint8_t* g_attn = static_cast<const uint8_t*>(c->w.g_attn);
   const uint8_t* g_mlp = static_cast<const uint8_t*>(c->w.g_mlp);
   const bool lm_compact = !probe && L.p_lm.m_tiles > 1;
+  // Fused linear layers: the norms before attention and before the MLP are
+  // deferred (y = x * g, sums of squares in sq_a / sq_b) and applied by the
+  // consuming GEMM; the last layer's down projection keeps the separate
+  // residual + RMSNorm kernel (final norm, LM-head row compaction).
+  const bool fz = c->fused_on;
+  float* sq_a = at<float>(ws, L.sq_a);
+  float* sq_b = at<float>(ws, L.sq_b);
+  dd::FusedOut fo{};
+  fo.hidden = H;
+  fo.eps = cf.rms_eps;
+  fo.S = cf.block;
+  fo.D = cf.head_dim;
+  fo.qk_cols = (cf.n_q_heads + cf.n_kv_heads) * cf.head_dim;
+  fo.ctx_len = small_ptr(c) + 2;
+  fo.theta = cf.rope_theta;
 
   DD_CUDA(dd::launch_embed_norm(at<int32_t>(ws, L.tok), at<uint32_t>(ws, L.mask), c->w.embed, c->w.pos, g_attn,
-                                x, y, cf.batch, cf.block, H, cf.vocab, cf.rms_eps, st));
+                                x, y, cf.batch, cf.block, H, cf.vocab, cf.rms_eps, st, fz ? sq_a : nullptr));
   mk(kKEmbed);
   for (int l = 0; l < cf.n_layers; ++l) {
     dd::GemmOut o{};
     o.partial = part;
     o.rows_valid = R;
     // q|k|v = y Wqkv^T
-    o.ld = c->qkvw;
-    o.split_stride = (long long)R * c->qkvw;
-    DD_CUDA(dd::launch_gemm(L.p_qkv, c->m_wqkv[l], c->m_y_b, o, status, c->timeout_ns, st));
-    mk(kKGemmQkv);
-    DD_CUDA(dd::launch_reduce_qkv(part, L.p_qkv.splits, o.split_stride, R, c->qkvw, ws + L.qkv, cf.block,
-                                  cf.head_dim, (cf.n_q_heads + cf.n_kv_heads) * cf.head_dim, small_ptr(c) + 2,
-                                  cf.rope_theta, st));
-    mk(kKReduceQkv);
+    if (fz) {
+      fo.out = ws + L.qkv;
+      fo.ld = c->qkvw;
+      fo.sq_in = sq_a;
+      fo.n_sq = l == 0 ? 1 : H / 128;  // the embedding's norm sums a whole row in one slot
+      DD_CUDA(dd::launch_gemm_fused(c->f_qkv, c->m_wqkv[l], c->m_y_b, fo, status, c->timeout_ns, st));
+      mk(kKGemmQkv);
+    } else {
+      o.ld = c->qkvw;
+      o.split_stride = (long long)R * c->qkvw;
+      DD_CUDA(dd::launch_gemm(L.p_qkv, c->m_wqkv[l], c->m_y_b, o, status, c->timeout_ns, st));
+      mk(kKGemmQkv);
+      DD_CUDA(dd::launch_reduce_qkv(part, L.p_qkv.splits, o.split_stride, R, c->qkvw, ws + L.qkv, cf.block,
+                                    cf.head_dim, fo.qk_cols, small_ptr(c) + 2, cf.rope_theta, st));
+      mk(kKReduceQkv);
+    }
     // block attention
     dd::AttnArgs a{};
     a.qkv = ws + L.qkv;
@@ -328,27 +360,55 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
     if (probe && probe->attn_out)
       DD_CUDA(cudaMemcpyAsync(static_cast<uint8_t*>(probe->attn_out) + (size_t)l * 2 * R * c->HqD * 2, ws + L.attn,
                               (size_t)2 * R * c->HqD * 2, cudaMemcpyDeviceToDevice, st));
-    // x += attn Wo^T ; y = norm(x) g_mlp
-    o.ld = H;
-    o.split_stride = (long long)R * H;
-    DD_CUDA(dd::launch_gemm(L.p_o, c->m_wo[l], c->m_attn_b, o, status, c->timeout_ns, st));
-    mk(kKGemmO);
-    DD_CUDA(dd::launch_reduce_residual_norm(part, L.p_o.splits, o.split_stride, x, g_mlp + (size_t)l * H * 2, y, R, H,
-                                            cf.rms_eps, st));
-    mk(kKNormO);
-    // h = silu(y Wg^T) * (y Wu^T)
-    o.ld = 2 * F;
-    o.split_stride = (long long)R * 2 * F;
-    DD_CUDA(dd::launch_gemm(L.p_gu, c->m_wgu[l], c->m_y_b, o, status, c->timeout_ns, st));
-    mk(kKGemmGu);
-    DD_CUDA(dd::launch_reduce_swiglu(part, L.p_gu.splits, o.split_stride, ws + L.hmid, R, F, st));
-    mk(kKSwiglu);
+    if (fz) {
+      // x += attn Wo^T ; y = x g_mlp (deferred norm) ; then h = silu(y Wg^T) * (y Wu^T)
+      fo.out = y;
+      fo.ld = H;
+      fo.x = x;
+      fo.g = g_mlp + (size_t)l * H * 2;
+      fo.sq_out = sq_b;
+      DD_CUDA(dd::launch_gemm_fused(c->f_o, c->m_wo[l], c->m_attn_b, fo, status, c->timeout_ns, st));
+      mk(kKGemmO);
+      fo.out = ws + L.hmid;
+      fo.ld = F;
+      fo.sq_in = sq_b;
+      fo.n_sq = H / 128;
+      DD_CUDA(dd::launch_gemm_fused(c->f_gu, c->m_wgu64[l], c->m_y_b, fo, status, c->timeout_ns, st));
+      mk(kKGemmGu);
+    } else {
+      // x += attn Wo^T ; y = norm(x) g_mlp
+      o.ld = H;
+      o.split_stride = (long long)R * H;
+      DD_CUDA(dd::launch_gemm(L.p_o, c->m_wo[l], c->m_attn_b, o, status, c->timeout_ns, st));
+      mk(kKGemmO);
+      DD_CUDA(dd::launch_reduce_residual_norm(part, L.p_o.splits, o.split_stride, x, g_mlp + (size_t)l * H * 2, y, R,
+                                              H, cf.rms_eps, st));
+      mk(kKNormO);
+      // h = silu(y Wg^T) * (y Wu^T)
+      o.ld = 2 * F;
+      o.split_stride = (long long)R * 2 * F;
+      DD_CUDA(dd::launch_gemm(L.p_gu, c->m_wgu[l], c->m_y_b, o, status, c->timeout_ns, st));
+      mk(kKGemmGu);
+      DD_CUDA(dd::launch_reduce_swiglu(part, L.p_gu.splits, o.split_stride, ws + L.hmid, R, F, st));
+      mk(kKSwiglu);
+    }
+    const void* gn = (l + 1 < cf.n_layers) ? (const void*)(g_attn + (size_t)(l + 1) * H * 2) : c->w.g_final;
+    if (fz && l + 1 < cf.n_layers) {
+      // x += h Wd^T ; y = x g_attn[l + 1] (deferred norm)
+      fo.out = y;
+      fo.ld = H;
+      fo.x = x;
+      fo.g = gn;
+      fo.sq_out = sq_a;
+      DD_CUDA(dd::launch_gemm_fused(c->f_d, c->m_wd[l], c->m_h_b, fo, status, c->timeout_ns, st));
+      mk(kKGemmDown);
+      continue;
+    }
     // x += h Wd^T ; y = norm(x) g (next layer's attention norm, or the final norm)
     o.ld = H;
     o.split_stride = (long long)R * H;
     DD_CUDA(dd::launch_gemm(L.p_d, c->m_wd[l], c->m_h_b, o, status, c->timeout_ns, st));
     mk(kKGemmDown);
-    const void* gn = (l + 1 < cf.n_layers) ? (const void*)(g_attn + (size_t)(l + 1) * H * 2) : c->w.g_final;
     // The final norm also compacts the rows still masked for the LM head
     // (except on the probe path, which reports every row, and when the LM
     // head has one row tile, which no compaction can skip).
@@ -537,6 +597,19 @@ dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_byte
     dd_destroy(c);
     return fail(DD_ERR_CUDA, "tensor map encoding failed for the workspace buffers");
   }
+  // Fused linear layers (at most 128 activation rows, which the activation
+  // maps above then hold in one box).
+  if (c->R <= 128) {
+    c->f_qkv = dd::plan_gemm_fused(dd::kOpQkv, c->R, c->qkvw, cf.hidden);
+    c->f_o = dd::plan_gemm_fused(dd::kOpResidual, c->R, cf.hidden, c->HqD);
+    c->f_gu = dd::plan_gemm_fused(dd::kOpSwiglu, c->R, 2 * cf.mlp, cf.hidden);
+    c->f_d = dd::plan_gemm_fused(dd::kOpResidual, c->R, cf.hidden, cf.mlp);
+    c->fused_ok = c->f_qkv.fused_op >= 0 && c->f_o.fused_op >= 0 && c->f_gu.fused_op >= 0 &&
+                  c->f_d.fused_op >= 0 && L.p_qkv.BN == c->R && L.p_o.BN == c->R && L.p_d.BN == c->R;
+  }
+  // Measured on the small decode workload the fused layers lose to the
+  // separate reduce kernels inside the step graph, so they are opt-in.
+  c->fused_on = false;
   *out = c;
   return DD_OK;
 }
@@ -565,11 +638,13 @@ dd_status dd_init_weights(dd_ctx* c, const dd_weights* w) {
   c->m_wo.assign(cf.n_layers, CUtensorMap{});
   c->m_wgu.assign(cf.n_layers, CUtensorMap{});
   c->m_wd.assign(cf.n_layers, CUtensorMap{});
+  c->m_wgu64.assign(cf.n_layers, CUtensorMap{});
   bool ok = true;
   for (int l = 0; l < cf.n_layers && ok; ++l) {
     ok = dd::make_map_2d(&c->m_wqkv[l], (const uint8_t*)w->wqkv + (size_t)l * c->qkvw * H * 2, c->qkvw, H, 128) &&
          dd::make_map_2d(&c->m_wo[l], (const uint8_t*)w->wo + (size_t)l * H * c->HqD * 2, H, c->HqD, 128) &&
          dd::make_map_2d(&c->m_wgu[l], (const uint8_t*)w->wgu + (size_t)l * 2 * F * H * 2, 2 * F, H, 128) &&
+         dd::make_map_2d(&c->m_wgu64[l], (const uint8_t*)w->wgu + (size_t)l * 2 * F * H * 2, 2 * F, H, 64) &&
          dd::make_map_2d(&c->m_wd[l], (const uint8_t*)w->wd + (size_t)l * H * F * 2, H, F, 128);
   }
   ok = ok && dd::make_map_2d(&c->m_lm, w->lm_head, cf.vocab, H, c->L.p_lm.BN);
@@ -762,6 +837,51 @@ dd_status dd_step_launch_count(dd_ctx* c, int32_t* n) {
   if (s != DD_OK) return s;
   *n = c->step_launches + (ensure_loop_graph(c) ? 1 : 0);
   return DD_OK;
+}
+
+dd_status dd_set_option(dd_ctx* c, int32_t option, int32_t value) {
+  if (!c) return fail(DD_ERR_INVALID_ARG, "ctx is NULL");
+  if (option != DD_OPT_FUSED_REDUCE) return fail(DD_ERR_INVALID_ARG, "option %d cannot be set", option);
+  if (value != 0 && value != 1) return fail(DD_ERR_INVALID_ARG, "DD_OPT_FUSED_REDUCE takes 0 or 1 (got %d)", value);
+  if (value && !c->fused_ok)
+    return fail(DD_ERR_UNSUPPORTED, "the fused linear layers are not available for this shape or device");
+  if ((value != 0) != c->fused_on) {
+    // the captured graphs hold the other path
+    DD_CUDA(cudaDeviceSynchronize());
+    if (c->exec) cudaGraphExecDestroy(c->exec);
+    if (c->loop_exec) cudaGraphExecDestroy(c->loop_exec);
+    c->exec = nullptr;
+    c->loop_exec = nullptr;
+    c->loop_tried = false;
+    c->fused_on = value != 0;
+  }
+  return DD_OK;
+}
+
+dd_status dd_get_option(dd_ctx* c, int32_t option, int32_t* value) {
+  if (!c) return fail(DD_ERR_INVALID_ARG, "ctx is NULL");
+  if (!value) return fail(DD_ERR_INVALID_ARG, "value is NULL");
+  const dd::GemmPlan* fp[] = {&c->f_qkv, &c->f_o, &c->f_gu, &c->f_d};
+  switch (option) {
+    case DD_OPT_FUSED_REDUCE: *value = c->fused_on ? 1 : 0; return DD_OK;
+    case DD_OPT_FUSED_CLUSTER_QKV:
+    case DD_OPT_FUSED_CLUSTER_O:
+    case DD_OPT_FUSED_CLUSTER_GATE_UP:
+    case DD_OPT_FUSED_CLUSTER_DOWN: {
+      const dd::GemmPlan& p = *fp[option - DD_OPT_FUSED_CLUSTER_QKV];
+      *value = c->fused_ok ? p.splits : 0;
+      return DD_OK;
+    }
+    case DD_OPT_FUSED_GRID_QKV:
+    case DD_OPT_FUSED_GRID_O:
+    case DD_OPT_FUSED_GRID_GATE_UP:
+    case DD_OPT_FUSED_GRID_DOWN: {
+      const dd::GemmPlan& p = *fp[option - DD_OPT_FUSED_GRID_QKV];
+      *value = c->fused_ok ? p.grid : 0;
+      return DD_OK;
+    }
+  }
+  return fail(DD_ERR_INVALID_ARG, "unknown option %d", option);
 }
 
 dd_status dd_profile_step(dd_ctx* c, int32_t* tokens, uint32_t* mask, float gamma, int32_t mode, float* times_ms,

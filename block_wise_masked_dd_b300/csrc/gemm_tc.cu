@@ -443,6 +443,7 @@ cudaError_t prepare_kernels() {
   static cudaError_t done = cudaErrorNotReady;
   if (done == cudaSuccess) return done;
   cudaError_t e = prepare_gemm_kernels();
+  if (e == cudaSuccess) e = prepare_gemm_fused_kernels();
   if (e == cudaSuccess) e = prepare_attention_kernels();
   if (e == cudaSuccess) e = prepare_attention_tc_kernels();
   if (e == cudaSuccess) e = prepare_small_kernels();

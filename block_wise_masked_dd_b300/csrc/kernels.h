@@ -54,6 +54,7 @@ struct GemmPlan {
   uint32_t tmem_half;             // TMEM columns per accumulator buffer (power of two >= BN)
   int split_act;                  // activation operand = bf16 head rows [0,R) + remainder rows [R,2R)
   int split_rows;                 // R
+  int fused_op;                   // fused plans (plan_gemm_fused): the epilogue op; splits = cluster size
 };
 
 struct GemmOut {
@@ -74,6 +75,52 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act = 0);
 // {64, 128} for the operand on the MMA M side and {64, BN} for the other.
 cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmOut& out,
                         int* status, uint64_t timeout_ns, cudaStream_t st);
+
+// ------------------------------------------- fused split-K linear layers
+//
+// A linear layer of the step whose K splits run as one thread-block cluster:
+// the CTAs of a cluster each take a K range of the same 128-feature tile,
+// stage their fp32 partial tile in shared memory, and each sums a share of
+// the tile's rows over the cluster (distributed shared memory) and applies
+// the layer's epilogue, so no partial reaches global memory and no reduce
+// kernel runs.  Activations are split (bf16 head + remainder rows) and at
+// most 128 rows long.
+//
+// Deferred RMSNorm: a residual epilogue writes y' = x * g (not normalised)
+// and, per 128-feature tile, the sum of x^2 of each row; the consuming GEMM
+// scales row r of its result by rsqrt(sum over tiles / hidden + eps), which
+// equals normalising first since the layer is linear in its input.
+
+enum FusedOp : int {
+  kOpQkv = 0,       // q|k|v = rs * sum, rotary on q and k heads, bf16 head + remainder
+  kOpSwiglu = 1,    // tile = 64 gate + 64 up features: h = silu(rs g) * (rs u), head + remainder
+  kOpResidual = 2,  // x += sum; y' = x * g as head + remainder; per-tile row sums of x^2
+};
+
+struct FusedOut {
+  void* out;            // bf16 [2*rows][ld]: heads, then remainders
+  int ld;               // features of `out` (qkv width, F, or hidden)
+  float* x;             // kOpResidual: fp32 [rows][ld], updated in place
+  const void* g;        // kOpResidual: bf16 gain [ld]
+  float* sq_out;        // kOpResidual: [ld/128][rows] sums of x^2 per feature tile
+  const float* sq_in;   // kOpQkv, kOpSwiglu: [n_sq][rows] sums of squares of the input rows
+  int n_sq;
+  int hidden;
+  float eps;
+  int S, D, qk_cols;    // kOpQkv rotary: block length, head dim, columns of the q and k heads
+  const int* ctx_len;
+  float theta;          // 0: no rotary
+};
+
+// rows <= 128 and a multiple of 16; N = features (2F for kOpSwiglu).  Queries
+// the device for how many clusters of each size fit; returns a plan with
+// fused_op = -1 when none does.
+GemmPlan plan_gemm_fused(int op, int rows, int N, int K);
+// map_w: the weights, box {64, 128} (kOpSwiglu: box {64, 64}; the up rows
+// start at row F = N / 2); map_x: the split activations, box {64, rows}.
+cudaError_t launch_gemm_fused(const GemmPlan& p, const CUtensorMap& map_w, const CUtensorMap& map_x,
+                              const FusedOut& out, int* status, uint64_t timeout_ns, cudaStream_t st);
+cudaError_t prepare_gemm_fused_kernels();
 
 // ------------------------------------------------------------- attention
 
@@ -124,9 +171,11 @@ cudaError_t launch_attention_combine(const AttnPlan& p, const AttnArgs& a, cudaS
 
 // Activation outputs named "split" below are written as bf16 heads in rows
 // [0, rows) and bf16 remainders (value - head, rounded) in rows [rows, 2*rows).
+// With sq != nullptr the norm is deferred: y = x * g (not normalised) and
+// sq[r] = sum of x[r]^2 (the consumer scales by rsqrt(sq / H + eps)).
 cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const void* embed, const void* pos,
                               const void* g, float* x, void* y_split, int B, int S, int H, int V, float eps,
-                              cudaStream_t st);
+                              cudaStream_t st, float* sq = nullptr);
 // q|k|v of the step: the split-K sum written as bf16 head + remainder; with
 // theta > 0 the query and key heads (columns < qk_cols) of row r are rotated
 // to position *ctx_len + r % S (see dd_config.rope_theta).

@@ -84,9 +84,11 @@ __device__ __forceinline__ void add_partials(const float* p, int s0, int s1, lon
 
 // y[r] = x[r] * rsqrt(mean(x[r]^2) + eps) * g, written as head (row r) and
 // remainder (row R + r); x held in registers (passes of 8 per thread).
+// With sq != nullptr the norm is deferred: rs = 1 and sq[r] = sum of x^2.
 __device__ __forceinline__ void norm_store(const float (&xv)[kMaxRowPasses][8], int passes, int r, int H, int R,
                                            const float (&gv)[kMaxRowPasses][8], __nv_bfloat16* y, float eps,
-                                           float* red, __nv_bfloat16* y2 = nullptr, int r2 = -1) {
+                                           float* red, __nv_bfloat16* y2 = nullptr, int r2 = -1,
+                                           float* sq = nullptr) {
   float ss = 0.f;
 #pragma unroll
   for (int p = 0; p < kMaxRowPasses; ++p) {
@@ -95,7 +97,8 @@ __device__ __forceinline__ void norm_store(const float (&xv)[kMaxRowPasses][8], 
     for (int i = 0; i < 8; ++i) ss += xv[p][i] * xv[p][i];
   }
   ss = block_sum(ss, red);
-  const float rs = rsqrtf(ss / H + eps);
+  if (sq && threadIdx.x == 0) sq[r] = ss;
+  const float rs = sq ? 1.f : rsqrtf(ss / H + eps);
 #pragma unroll
   for (int p = 0; p < kMaxRowPasses; ++p) {
     if (p >= passes) break;
@@ -120,7 +123,7 @@ __device__ __forceinline__ void load_gains(const __nv_bfloat16* g, int passes, f
 // y[r] = RMSNorm(x[r]) * g as head + remainder.  One CTA per row.
 __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const __nv_bfloat16* embed,
                              const __nv_bfloat16* pos, const __nv_bfloat16* g, float* x, __nv_bfloat16* y, int S,
-                             int H, int V, float eps) {
+                             int H, int V, float eps, float* sq) {
   __shared__ float red[32];
   const int r = blockIdx.x, b = r / S, i = r % S, R = gridDim.x;
   const int passes = H / (8 * blockDim.x);
@@ -146,7 +149,7 @@ __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const 
     for (int k = 0; k < 8; ++k) xv[p][k] = e[k] + pv[p][k];
     store8_f32(x + (long long)r * H + c, xv[p]);
   }
-  norm_store(xv, passes, r, H, R, gv, y, eps, red);
+  norm_store(xv, passes, r, H, R, gv, y, eps, red, nullptr, -1, sq);
 }
 
 // x[r] += sum_s part[s][r]; y[r] = RMSNorm(x[r]) * g as head + remainder.
@@ -238,16 +241,7 @@ __global__ void k_reduce_qkv(const float* part, int splits, long long split_stri
       const int d0 = n % D;
       const double pos = (double)(T + (int)(e / N) % S);
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
-        const double ang = pos * freq[(d0 >> 1) + p];
-        const double two_pi = 6.283185307179586;
-        const float red = (float)(ang - rint(ang / two_pi) * two_pi);
-        float sn, c;
-        sincosf(red, &sn, &c);
-        const float x0 = acc[2 * p], x1 = acc[2 * p + 1];
-        acc[2 * p] = x0 * c - x1 * sn;
-        acc[2 * p + 1] = x0 * sn + x1 * c;
-      }
+      for (int p = 0; p < 4; ++p) rope_pair(acc[2 * p], acc[2 * p + 1], pos, freq[(d0 >> 1) + p]);
     }
     store8_split(out + e, out + total + e, acc);
   }
@@ -550,9 +544,9 @@ cudaError_t prepare_small_kernels() {
 
 cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const void* embed, const void* pos,
                               const void* g, float* x, void* y, int B, int S, int H, int V, float eps,
-                              cudaStream_t st) {
+                              cudaStream_t st, float* sq) {
   return launch_k(k_embed_norm, B * S, row_threads(H), 0, st, tokens, mask, (const __nv_bfloat16*)embed,
-                  (const __nv_bfloat16*)pos, (const __nv_bfloat16*)g, x, (__nv_bfloat16*)y, S, H, V, eps);
+                  (const __nv_bfloat16*)pos, (const __nv_bfloat16*)g, x, (__nv_bfloat16*)y, S, H, V, eps, sq);
 }
 
 cudaError_t launch_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N, void* out, int S,
