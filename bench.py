@@ -71,7 +71,7 @@ def parse(argv=None):
                     help="append each decoded block to the context with the synthetic context tower on the device "
                          "(default: fresh seeded K/V from the host)")
     ap.add_argument("--fused-reduce", action="store_true",
-                    help="linear layers reduce their split-K partials inside the GEMM (thread-block clusters) "
+                    help="linear layers reduce their split-K partials inside the GEMM (groups of CTAs) "
                          "instead of in separate kernels (the default)")
     ap.add_argument("--no-micro", action="store_true", help="skip the attention / LM-head microbenchmarks")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
@@ -311,7 +311,7 @@ def gpu_arm(args, world, rank, local):
     if args.fused_reduce:
         dec.fused_reduce = True
     if dec.fused_reduce:
-        linear = "split-K reduced in the GEMM by clusters of " + ", ".join(
+        linear = "split-K reduced in the GEMM by groups of " + ", ".join(
             f"{k} {cs}" for k, (cs, _) in dec.fused_plan().items())
     else:
         linear = "split-K partials reduced by separate kernels"

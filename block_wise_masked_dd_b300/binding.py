@@ -108,7 +108,7 @@ _SIGS = {
 
 # dd_set_option / dd_get_option
 DD_OPT_FUSED_REDUCE = 1
-DD_OPT_FUSED_CLUSTER = {"qkv": 2, "o": 3, "gate_up": 4, "down": 5}
+DD_OPT_FUSED_SPLITS = {"qkv": 2, "o": 3, "gate_up": 4, "down": 5}
 DD_OPT_FUSED_GRID = {"qkv": 6, "o": 7, "gate_up": 8, "down": 9}
 
 KIND_NAMES = ["embed_norm", "gemm_qkv", "reduce_qkv", "attention_context", "attention_merge", "gemm_o", "norm_o",

@@ -103,7 +103,7 @@ bool make_map_q(CUtensorMap* m, const void* qkv, uint64_t rows, uint64_t ld, int
 
 struct Layout {
   size_t kc, vc, x, y, yc, row_index, qkv, attn, hmid, part, attn_part, sel_m, sel_s, sel_a, conf, arg, tok, mask,
-      ncommit, small, params, sq_a, sq_b, total;
+      ncommit, small, params, sq_a, sq_b, xpart, fcnt, total;
   size_t part_elems;
   int alloc_ctx;
   dd::GemmPlan p_qkv, p_o, p_gu, p_d, p_lm, p_store, p_tower;
@@ -121,7 +121,7 @@ struct dd_ctx {
   std::vector<CUtensorMap> m_wqkv, m_wo, m_wgu, m_wd;
   std::vector<CUtensorMap> m_wgu64;  // gate|up weights with 64-row boxes (the fused SwiGLU tiles)
   // Linear layers with the split-K reduction and epilogue inside the GEMM
-  // (thread-block clusters); fused_ok: planned for this shape and device.
+  // (groups of CTAs); fused_ok: planned for this shape.
   dd::GemmPlan f_qkv, f_o, f_gu, f_d;
   bool fused_ok, fused_on;
   dd_context_tower tower;  // borrowed; tower.wkv == nullptr until dd_set_context_tower
@@ -246,6 +246,11 @@ Layout make_layout(const dd_config& c) {
   // linear layers): before attention and before the MLP
   L.sq_a = take((size_t)(c.hidden / 128) * R * 4);
   L.sq_b = take((size_t)(c.hidden / 128) * R * 4);
+  // fused linear layers: partial-tile scratch and group counters (zeroed here,
+  // left zero by every launch)
+  const bool fusable = R <= 128;
+  L.xpart = take(fusable ? dd::fused_scratch_bytes(R) : 0);
+  L.fcnt = take(fusable ? dd::fused_counter_bytes() : 0);
   L.total = off;
   return L;
 }
@@ -305,6 +310,8 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
   fo.qk_cols = (cf.n_q_heads + cf.n_kv_heads) * cf.head_dim;
   fo.ctx_len = small_ptr(c) + 2;
   fo.theta = cf.rope_theta;
+  fo.xpart = at<float>(ws, L.xpart);
+  fo.cnt = at<unsigned>(ws, L.fcnt);
 
   DD_CUDA(dd::launch_embed_norm(at<int32_t>(ws, L.tok), at<uint32_t>(ws, L.mask), c->w.embed, c->w.pos, g_attn,
                                 x, y, cf.batch, cf.block, H, cf.vocab, cf.rms_eps, st, fz ? sq_a : nullptr));
@@ -864,11 +871,11 @@ dd_status dd_get_option(dd_ctx* c, int32_t option, int32_t* value) {
   const dd::GemmPlan* fp[] = {&c->f_qkv, &c->f_o, &c->f_gu, &c->f_d};
   switch (option) {
     case DD_OPT_FUSED_REDUCE: *value = c->fused_on ? 1 : 0; return DD_OK;
-    case DD_OPT_FUSED_CLUSTER_QKV:
-    case DD_OPT_FUSED_CLUSTER_O:
-    case DD_OPT_FUSED_CLUSTER_GATE_UP:
-    case DD_OPT_FUSED_CLUSTER_DOWN: {
-      const dd::GemmPlan& p = *fp[option - DD_OPT_FUSED_CLUSTER_QKV];
+    case DD_OPT_FUSED_SPLITS_QKV:
+    case DD_OPT_FUSED_SPLITS_O:
+    case DD_OPT_FUSED_SPLITS_GATE_UP:
+    case DD_OPT_FUSED_SPLITS_DOWN: {
+      const dd::GemmPlan& p = *fp[option - DD_OPT_FUSED_SPLITS_QKV];
       *value = c->fused_ok ? p.splits : 0;
       return DD_OK;
     }

@@ -1,18 +1,21 @@
 // Linear layers of the denoising step with their split-K reduction and
-// elementwise epilogue inside the GEMM (tcgen05 + TMA + thread-block
-// clusters), so a layer is one launch instead of a GEMM plus a reduce kernel.
+// elementwise epilogue inside the GEMM (tcgen05 + TMA), so a layer is one
+// launch instead of a GEMM plus a reduce kernel.
 //
-// Work split: a cluster of cs CTAs owns one 128-feature weight tile at a time
-// (persistent clusters walk the tiles).  CTA rank r of the cluster multiplies
-// K blocks [r*kbps, (r+1)*kbps) of the tile against every activation row, so
-// the cs CTAs stream disjoint weight bytes.  Each CTA then copies its fp32
-// accumulator tile from TMEM into its own shared memory as [row][feature].
-// When all cs tiles are staged (an mbarrier in every CTA on which each CTA of
-// the cluster arrives), CTA r sums rows r, r+cs, r+2cs, ... over the cs
-// staged tiles (distributed shared memory loads, always in rank order) and
-// applies the layer's epilogue to them; a second mbarrier tells each CTA when
-// all have read its staged tile.  The accumulator is double-buffered in TMEM,
-// so the MMAs of a cluster's next tile run during this epilogue.
+// Work split: the grid is G groups of gs CTAs, at most one CTA per SM and at
+// most one CTA per SM's worth of grid, so every CTA is resident at once.  A
+// group owns one 128-feature weight tile at a time (groups walk the tiles);
+// CTA rank r of the group multiplies K blocks [r*kbps, (r+1)*kbps) of the tile
+// against every activation row, so the gs CTAs stream disjoint weight bytes.
+// Each CTA writes its fp32 accumulator tile ([row][feature], from TMEM) to a
+// double-buffered scratch slot in global memory (it stays in L2), then
+// raises the group's arrival counter; once the counter shows all gs partials
+// of the tile, CTA r sums rows r, r+gs, r+2gs, ... over them (always in rank
+// order) and applies the layer's epilogue.  A group waits only on its own
+// members, all resident, so the waits always end; they are bounded all the
+// same.  The last member to finish resets the group's counters for the next
+// launch.  The accumulator is double-buffered in TMEM, so the MMAs of a
+// group's next tile run during this epilogue.
 //
 // Epilogues (see FusedOp): q|k|v with rotary positions, SwiGLU over a tile
 // made of 64 gate and the matching 64 up rows of the weight, and the residual
@@ -23,15 +26,16 @@
 // rounding order.
 //
 // Inside the step graph of the small decode workload (128 rows) this path
-// measured slower than plain GEMMs followed by reduce kernels (19.9k against
-// 24.7k committed tokens/s): the clusters fit on fewer SMs (96-135 of 148)
-// and a cluster launch overlaps its predecessor less.  The step therefore
-// runs it only when DD_OPT_FUSED_REDUCE asks for it.
+// measured slower than plain GEMMs followed by reduce kernels (20.2k against
+// 24.8k committed tokens/s): under programmatic dependent launch a reduce
+// kernel overlaps the next GEMM's first weight loads, while a reduction at
+// the end of the GEMM is on the critical path.  The step runs it only when
+// DD_OPT_FUSED_REDUCE asks for it.
 //
 // Roles (192 threads) as in the plain GEMM: warp 0 issues TMA loads, warp 1
-// owns TMEM and issues the MMAs, warps 2-5 run the epilogue.  Every mbarrier
-// wait is bounded; a decision that ends the epilogue loop is taken jointly by
-// its four warps (bar.red), so no named barrier is ever left short.
+// owns TMEM and issues the MMAs, warps 2-5 run the epilogue.  Every wait is
+// bounded; a decision that ends the epilogue loop is taken jointly by its four
+// warps (bar.red), so no named barrier is ever left short.
 #include <math.h>
 
 #include "kernels.h"
@@ -47,11 +51,12 @@ constexpr int kThreads = 192;
 constexpr int kEpiThreads = 128;
 constexpr int kEpiBar = 1;              // named barrier of the epilogue warps (0 is __syncthreads)
 constexpr int kStageA = kBM * kBK * 2;  // 16 KB weight tile per K block
-constexpr int kMaxCluster = 8;   // portable cluster sizes only
+constexpr int kMaxGroup = 8;     // CTAs that split one tile's K, at most
 constexpr int kRB = 4;           // rows an epilogue warp reduces per batch (their loads issued together)
 
 struct FArgs {
   int m_tiles, kb_total, kb_per_split, BN, stages, rows, F;
+  int gs;  // group size (K splits of a tile)
   uint32_t tmem_half;
   FusedOut o;
   int* status;
@@ -60,14 +65,34 @@ struct FArgs {
 
 // One pipeline stage: the weight tile, then the activation heads and remainders.
 __host__ __device__ inline int fused_stage_bytes(int BN) { return kStageA + 2 * BN * kBK * 2; }
-// The staged fp32 accumulator tile [BN rows][128 features].
-__host__ __device__ inline int fused_staging_bytes(int BN) { return BN * kBM * 4; }
-// Alignment slack, stages, staging, mbarriers, the rotary frequency table
-// (64 doubles), the per-row norm scales (128 floats), the TMEM address and
-// the abort flag.
+// One fp32 partial tile [BN rows][128 features] in the global scratch.
+__host__ __device__ inline int fused_partial_elems(int BN) { return BN * kBM; }
+// Alignment slack, stages, mbarriers, the rotary frequency table (64
+// doubles), the per-row norm scales (128 floats), the TMEM address and the
+// abort flag.
 __host__ inline int fused_smem_bytes(int BN, int stages) {
-  return 1024 + stages * fused_stage_bytes(BN) + fused_staging_bytes(BN) + (2 * stages + 7) * 8 + 64 * 8 + 128 * 4 +
-         16;
+  return 1024 + stages * fused_stage_bytes(BN) + (2 * stages + 5) * 8 + 64 * 8 + 128 * 4 + 16;
+}
+
+// Spin until *p >= target (acquire, GPU scope), bounded like the mbarrier waits.
+__device__ __forceinline__ bool wait_count_bounded(const unsigned* p, unsigned target, uint64_t limit_ns,
+                                                   volatile int* abort, int* status) {
+  auto load = [&]() {
+    unsigned v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+  };
+  if (load() >= target) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (load() >= target) return true;
+    if (*abort) return false;
+    if (globaltimer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      if (status) atomicExch(status, kStatusTimeout);
+      return false;
+    }
+  }
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -86,7 +111,7 @@ __device__ __forceinline__ void store4_split(__nv_bfloat16* hi, __nv_bfloat16* l
 }
 
 // The epilogue of activation row j for this lane's four features of tile t:
-// v = the cluster's sum over K of those four outputs; rs = the row's deferred
+// v = the group's sum over K of those four outputs; rs = the row's deferred
 // norm scale (kOpQkv, kOpSwiglu); xv = x at those features and gv the gains
 // (kOpResidual).
 template <int OP>
@@ -145,26 +170,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int BN = args.BN;
   const int stage_b = BN * kBK * 2;
   const int stage_bytes = fused_stage_bytes(BN);
-  float* staging = reinterpret_cast<float*>(smem + args.stages * stage_bytes);
-  uint64_t* full = reinterpret_cast<uint64_t*>(smem + args.stages * stage_bytes + fused_staging_bytes(BN));
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + args.stages * stage_bytes);
   uint64_t* empty = full + args.stages;
   uint64_t* acc_full = empty + args.stages;
   uint64_t* acc_empty = acc_full + 2;
   uint64_t* drain = acc_empty + 2;
-  uint64_t* staged = drain + 1;    // all cs partial tiles of the current tile are staged
-  uint64_t* consumed = staged + 1;  // all cs CTAs have read this CTA's staged tile
-  double* freq = reinterpret_cast<double*>(consumed + 1);
+  double* freq = reinterpret_cast<double*>(drain + 1);
   float* rs_s = reinterpret_cast<float*>(freq + 64);  // deferred norm scale of each activation row
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(rs_s + 128);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  const uint32_t cs = cluster_nctarank();
-  const uint32_t rank = cluster_ctarank();
-  const int cid = (int)cluster_id_x();
-  const int ncl = (int)ncluster_x();
+  const int cs = args.gs;
+  const int rank = (int)blockIdx.x % cs;
+  const int cid = (int)blockIdx.x / cs;  // group
+  const int ncl = (int)gridDim.x / cs;   // groups
   const int warp = warp_id();
   const int lane = lane_id();
-  const int kb0 = (int)rank * args.kb_per_split;
+  const int kb0 = rank * args.kb_per_split;
   const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
 
   if (threadIdx.x == 0) {
@@ -177,8 +199,6 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(&acc_empty[a], 1);
     }
     mbar_init(drain, 1);
-    mbar_init(staged, cs);
-    mbar_init(consumed, cs);
     *abort_flag = 0;
     fence_mbar_init();
     tma_prefetch_desc(&map_w);
@@ -193,7 +213,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_before();
   }
   __syncthreads();
-  cluster_sync_all();  // every CTA's mbarriers exist before any CTA arrives on them
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
@@ -304,7 +323,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int et = threadIdx.x - 64;
     pdl_wait();  // x, the squares and the context length come from preceding kernels
     const int T = (OP == kOpQkv && args.o.theta > 0.f) ? *args.o.ctx_len : 0;
-    const uint32_t stg = smem_u32(staging);
     if (OP != kOpResidual && et < BN) {
       // the row scales do not depend on the tile: once, during the first mainloop
       const float* sq = args.o.sq_in + et;
@@ -321,44 +339,50 @@ __global__ void __launch_bounds__(kThreads, 1)
       rs_s[et] = rsqrtf(ss / args.o.hidden + args.o.eps);
     }
     // this CTA's rows: rank, rank + cs, ... (owned of them)
-    const int owned = BN > (int)rank ? (BN - (int)rank + (int)cs - 1) / (int)cs : 0;
+    const int owned = BN > rank ? (BN - rank + cs - 1) / cs : 0;
+    unsigned* arrivals = args.o.cnt + 2 * cid;  // [0] partials written, [1] members finished
+    auto slot = [&](int member, int buf) {
+      return args.o.xpart + ((long long)(cid * cs + member) * 2 + buf) * fused_partial_elems(BN);
+    };
     int it = 0;
     for (int t = cid; t < args.m_tiles; t += ncl, ++it) {
       const int ab = it & 1;
       const uint32_t aphase = (it >> 1) & 1;
+      const int buf = it & 1;
       bool w = true;
-      if (et == 0) {
-        w = mbar_wait_bounded(&acc_full[ab], aphase, args.timeout_ns, abort_flag, args.status);
-        if (w && it > 0)
-          w = mbar_wait_cluster_bounded(consumed, (it - 1) & 1, args.timeout_ns, abort_flag, args.status);
-      }
+      if (et == 0) w = mbar_wait_bounded(&acc_full[ab], aphase, args.timeout_ns, abort_flag, args.status);
       if (!bar_and(kEpiBar, kEpiThreads, w)) break;
       tc_fence_after();
-      // accumulator (TMEM lane = feature, column = activation row) -> staging[row][feature]
+      // accumulator (TMEM lane = feature, column = activation row) -> this
+      // member's scratch slot [row][feature].  The slot of two tiles back is
+      // free: every member passed the previous tile's count, which it raised
+      // only after reading that tile's partials.
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + ab * args.tmem_half;
       const int lf = q * 32 + lane;
+      float* mine = slot(rank, buf);
       int c = 0;
       for (; c + 64 <= BN; c += 64) {
         float v[64];
         tmem_ld64(tbase + c, v);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) staging[(c + j) * kBM + lf] = v[j];
+        for (int j = 0; j < 64; ++j) mine[(c + j) * kBM + lf] = v[j];
       }
       for (; c < BN; c += 16) {
         float v[16];
         tmem_ld16(tbase + c, v);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) staging[(c + j) * kBM + lf] = v[j];
+        for (int j = 0; j < 16; ++j) mine[(c + j) * kBM + lf] = v[j];
       }
       tc_fence_before();
-      bar_and(kEpiBar, kEpiThreads, true);  // the whole tile is staged and the TMEM buffer read
+      __threadfence();
+      bar_and(kEpiBar, kEpiThreads, true);  // the whole partial is written and the TMEM buffer read
+      w = true;
       if (et == 0) {
         mbar_arrive(&acc_empty[ab]);
-        fence_acq_rel_cluster();
-        for (uint32_t p = 0; p < cs; ++p) mbar_arrive_cluster(cluster_map(smem_u32(staged), p));
+        atomicAdd(&arrivals[0], 1u);
+        w = wait_count_bounded(&arrivals[0], (unsigned)(cs * (it + 1)), args.timeout_ns, abort_flag, args.status);
+        __threadfence();
       }
-      w = true;
-      if (et == 0) w = mbar_wait_cluster_bounded(staged, it & 1, args.timeout_ns, abort_flag, args.status);
       if (!bar_and(kEpiBar, kEpiThreads, w)) break;
       // Owned rows in batches of kRB consecutive ones, batch b to the warp of
       // quarter b % 4; a batch's loads (staged partials of every rank, and x)
@@ -372,30 +396,31 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       for (int k0 = q * kRB; k0 < owned; k0 += 4 * kRB) {
         float4 xv[kRB];
-        float4 v[kRB][kMaxCluster];
+        float4 v[kRB][kMaxGroup];
 #pragma unroll
         for (int b = 0; b < kRB; ++b) {
-          const int j = (int)rank + (int)cs * (k0 + b);
+          const int j = rank + cs * (k0 + b);
           xv[b] = make_float4(0.f, 0.f, 0.f, 0.f);
           if (OP == kOpResidual && k0 + b < owned)
             xv[b] = *reinterpret_cast<const float4*>(args.o.x + (long long)j * args.o.ld + t * kBM + 4 * lane);
         }
 #pragma unroll
         for (int b = 0; b < kRB; ++b) {
-          const int j = (int)rank + (int)cs * (k0 + b);
-          const uint32_t off = stg + (uint32_t)((j * kBM + 4 * lane) * 4);
+          // member p's slot lies p * 2 partial tiles after member 0's
+          const float* pb = slot(0, buf) + (rank + cs * (k0 + b)) * kBM + 4 * lane;
 #pragma unroll
-          for (int p = 0; p < kMaxCluster; ++p)
-            if (k0 + b < owned && p < (int)cs) v[b][p] = ld_cluster_f4(cluster_map(off, (uint32_t)p));
+          for (int p = 0; p < kMaxGroup; ++p)
+            if (k0 + b < owned && p < cs)
+              v[b][p] = __ldcg(reinterpret_cast<const float4*>(pb + (long long)p * 2 * fused_partial_elems(BN)));
         }
 #pragma unroll
         for (int b = 0; b < kRB; ++b) {
           if (k0 + b >= owned) break;
-          const int j = (int)rank + (int)cs * (k0 + b);
+          const int j = rank + cs * (k0 + b);
           float4 acc = v[b][0];
 #pragma unroll
-          for (int p = 1; p < kMaxCluster; ++p) {
-            if (p < (int)cs) {
+          for (int p = 1; p < kMaxGroup; ++p) {
+            if (p < cs) {
               acc.x += v[b][p].x;
               acc.y += v[b][p].y;
               acc.z += v[b][p].z;
@@ -405,15 +430,20 @@ __global__ void __launch_bounds__(kThreads, 1)
           epilogue_row<OP>(args, t, j, lane, acc, OP == kOpResidual ? 1.f : rs_s[j], xv[b], gv, freq, T);
         }
       }
-      bar_and(kEpiBar, kEpiThreads, true);  // every read of the cluster's staged tiles is done
-      if (et == 0) {
-        for (uint32_t p = 0; p < cs; ++p) mbar_arrive_cluster(cluster_map(smem_u32(consumed), p));
+    }
+    // The last member to finish resets the group's counters: every member
+    // has passed its last wait on them.
+    bar_and(kEpiBar, kEpiThreads, true);
+    if (et == 0) {
+      __threadfence();
+      if (atomicAdd(&arrivals[1], 1u) == (unsigned)(cs - 1)) {
+        atomicExch(&arrivals[0], 0u);
+        atomicExch(&arrivals[1], 0u);
       }
     }
   }
 
   __syncthreads();
-  cluster_sync_all();  // no CTA leaves while another may still read its shared memory
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 2 * args.tmem_half);
@@ -436,27 +466,6 @@ uint32_t pow2_cols(uint32_t v) {
   return p;
 }
 
-// Clusters of `cs` CTAs of this kernel that can be resident at once.
-int max_active_clusters(int op, int cs, int smem) {
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(cs * kNumSMs);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = smem;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = cs;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  int n = 0;
-  if (cudaOccupancyMaxActiveClusters(&n, (const void*)fused_kernel(op), &cfg) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  return n;
-}
-
 }  // namespace
 
 GemmPlan plan_gemm_fused(int op, int rows, int N, int K) {
@@ -476,25 +485,25 @@ GemmPlan plan_gemm_fused(int op, int rows, int N, int K) {
   p.stages = stages;
   p.smem_bytes = fused_smem_bytes(rows, stages);
   p.tmem_half = pow2_cols(rows);
-  // Cost in microseconds: the busiest CTA's weight bytes at about the fair
-  // share of HBM per SM (48 GB/s) against the whole weight at 6.4 TB/s, plus
-  // a small charge per cluster rank (staging and cluster synchronisation).
+  // One CTA per SM (shared memory), at most kNumSMs CTAs: all resident at
+  // once.  Cost in microseconds: the busiest CTA's weight bytes at about the
+  // fair share of HBM per SM (48 GB/s) against the whole weight at 6.4 TB/s,
+  // plus an exchange per tile round and a small charge per group member.
   const double weight_us = (double)N * K * 2 / 6.4e6;
   double best = -1.0;
-  for (int cs = 1; cs <= kMaxCluster && cs <= p.kb_total; ++cs) {
-    const int kbps = (p.kb_total + cs - 1) / cs;
-    if ((p.kb_total + kbps - 1) / kbps != cs) continue;  // every rank gets at least one K block
-    const int mc = max_active_clusters(op, cs, p.smem_bytes);
-    if (mc < 1) continue;
-    const int ncl = mc < p.m_tiles ? mc : p.m_tiles;
-    const int rounds = (p.m_tiles + ncl - 1) / ncl;
+  for (int gs = 1; gs <= kMaxGroup && gs <= p.kb_total; ++gs) {
+    const int kbps = (p.kb_total + gs - 1) / gs;
+    if ((p.kb_total + kbps - 1) / kbps != gs) continue;  // every member gets at least one K block
+    const int groups = kNumSMs / gs < p.m_tiles ? kNumSMs / gs : p.m_tiles;
+    if (groups < 1) continue;
+    const int rounds = (p.m_tiles + groups - 1) / groups;
     const double sm_us = (double)rounds * kbps * kStageA / 48e3;
-    const double cost = (sm_us > weight_us ? sm_us : weight_us) + 0.05 * cs;
+    const double cost = (sm_us > weight_us ? sm_us : weight_us) + 0.3 * rounds + 0.05 * gs;
     if (best < 0 || cost < best) {
       best = cost;
-      p.splits = cs;
+      p.splits = gs;
       p.kb_per_split = kbps;
-      p.grid = ncl * cs;
+      p.grid = groups * gs;
     }
   }
   if (best < 0) return p;
@@ -503,9 +512,13 @@ GemmPlan plan_gemm_fused(int op, int rows, int N, int K) {
   return p;
 }
 
+size_t fused_scratch_bytes(int rows) { return (size_t)kNumSMs * 2 * fused_partial_elems(rows) * 4; }
+size_t fused_counter_bytes() { return (size_t)kNumSMs * 2 * 4; }
+
 cudaError_t launch_gemm_fused(const GemmPlan& p, const CUtensorMap& map_w, const CUtensorMap& map_x,
                               const FusedOut& out, int* status, uint64_t timeout_ns, cudaStream_t st) {
-  if (p.fused_op < 0 || p.splits < 1 || p.grid % p.splits) return cudaErrorInvalidValue;
+  if (p.fused_op < 0 || p.splits < 1 || p.grid % p.splits || p.grid > kNumSMs || !out.xpart || !out.cnt)
+    return cudaErrorInvalidValue;
   FArgs a;
   a.m_tiles = p.m_tiles;
   a.kb_total = p.kb_total;
@@ -514,25 +527,12 @@ cudaError_t launch_gemm_fused(const GemmPlan& p, const CUtensorMap& map_w, const
   a.stages = p.stages;
   a.rows = p.split_rows;
   a.F = p.fused_op == kOpSwiglu ? p.m_tiles * 64 : 0;  // the up rows follow the F gate rows
+  a.gs = p.splits;
   a.tmem_half = p.tmem_half;
   a.o = out;
   a.status = status;
   a.timeout_ns = timeout_ns;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.grid);
-  cfg.blockDim = dim3(kThreads);
-  cfg.dynamicSmemBytes = p.smem_bytes;
-  cfg.stream = st;
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = p.splits;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
-  cfg.attrs = attr;
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, fused_kernel(p.fused_op), map_w, map_x, a);
+  return launch_k(fused_kernel(p.fused_op), p.grid, kThreads, p.smem_bytes, st, map_w, map_x, a);
 }
 
 cudaError_t prepare_gemm_fused_kernels() {
@@ -540,7 +540,6 @@ cudaError_t prepare_gemm_fused_kernels() {
   for (int op = 0; op < 3 && e == cudaSuccess; ++op) {
     const void* k = (const void*)fused_kernel(op);
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, 227 * 1024);
-    if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   }
   return e;

@@ -78,11 +78,11 @@ cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUten
 
 // ------------------------------------------- fused split-K linear layers
 //
-// A linear layer of the step whose K splits run as one thread-block cluster:
-// the CTAs of a cluster each take a K range of the same 128-feature tile,
-// stage their fp32 partial tile in shared memory, and each sums a share of
-// the tile's rows over the cluster (distributed shared memory) and applies
-// the layer's epilogue, so no partial reaches global memory and no reduce
+// A linear layer of the step whose K splits run as one group of CTAs (all
+// CTAs of the grid resident at once): the members each take a K range of the
+// same 128-feature tile, write their fp32 partial tile to a scratch slot that
+// stays in L2, and once the group's counter shows all of them, each sums a
+// share of the tile's rows and applies the layer's epilogue, so no reduce
 // kernel runs.  Activations are split (bf16 head + remainder rows) and at
 // most 128 rows long.
 //
@@ -110,12 +110,15 @@ struct FusedOut {
   int S, D, qk_cols;    // kOpQkv rotary: block length, head dim, columns of the q and k heads
   const int* ctx_len;
   float theta;          // 0: no rotary
+  float* xpart;         // scratch of fused_scratch_bytes(rows)
+  unsigned* cnt;        // fused_counter_bytes() of zeros; left zero by every launch
 };
 
-// rows <= 128 and a multiple of 16; N = features (2F for kOpSwiglu).  Queries
-// the device for how many clusters of each size fit; returns a plan with
-// fused_op = -1 when none does.
+// rows <= 128 and a multiple of 16; N = features (2F for kOpSwiglu).  Returns
+// a plan with fused_op = -1 for shapes it does not take; splits = group size.
 GemmPlan plan_gemm_fused(int op, int rows, int N, int K);
+size_t fused_scratch_bytes(int rows);
+size_t fused_counter_bytes();
 // map_w: the weights, box {64, 128} (kOpSwiglu: box {64, 64}; the up rows
 // start at row F = N / 2); map_x: the split activations, box {64, rows}.
 cudaError_t launch_gemm_fused(const GemmPlan& p, const CUtensorMap& map_w, const CUtensorMap& map_x,

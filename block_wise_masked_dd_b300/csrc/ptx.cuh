@@ -90,86 +90,7 @@ DD_DEV bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns,
   }
 }
 
-// ----------------------------------------------------------------- clusters
-
-DD_DEV uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-DD_DEV uint32_t cluster_nctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
-  return r;
-}
-DD_DEV uint32_t cluster_id_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
-  return r;
-}
-DD_DEV uint32_t ncluster_x() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
-  return r;
-}
-
-// Every thread of every CTA of the cluster: arrive (release) and wait (acquire).
-DD_DEV void cluster_sync_all() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
-DD_DEV void fence_acq_rel_cluster() { asm volatile("fence.acq_rel.cluster;" ::: "memory"); }
-
-// Address of the same shared-memory variable in CTA `rank` of the cluster.
-DD_DEV uint32_t cluster_map(uint32_t saddr, uint32_t rank) {
-  uint32_t r;
-  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
-  return r;
-}
-
-// Arrive (release, cluster scope) on an mbarrier of any CTA of the cluster.
-DD_DEV void mbar_arrive_cluster(uint32_t cluster_addr) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr) : "memory");
-}
-
-DD_DEV bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n\t.reg .pred p;\n\t"
-      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-      "selp.u32 %0, 1, 0, p;\n\t}"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-
-// mbar_wait_bounded with acquire semantics at cluster scope (the phase is
-// completed by arrivals of other CTAs of the cluster).
-DD_DEV bool mbar_wait_cluster_bounded(uint64_t* bar, uint32_t parity, uint64_t limit_ns, volatile int* abort,
-                                      int* status) {
-  if (mbar_try_wait_cluster(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  while (true) {
-    if (mbar_try_wait_cluster(bar, parity)) return true;
-    if (*abort) return false;
-    if (globaltimer_ns() - t0 > limit_ns) {
-      *abort = 1;
-      if (status) atomicExch(status, kStatusTimeout);
-      return false;
-    }
-  }
-}
-
-// 16 bytes of another CTA's shared memory (address from cluster_map).
-DD_DEV float4 ld_cluster_f4(uint32_t cluster_addr) {
-  float4 v;
-  asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
-               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-               : "r"(cluster_addr)
-               : "memory");
-  return v;
-}
+// ------------------------------------------------------------ named barriers
 
 // Named barrier `id` over `n` threads whose result is the AND of `v` over them.
 DD_DEV bool bar_and(int id, int n, bool v) {

@@ -133,8 +133,8 @@ class Decoder:
 
     @property
     def fused_reduce(self) -> bool:
-        """Linear layers reduce their K splits inside the GEMM (thread-block
-        clusters); False: separate reduce kernels."""
+        """Linear layers reduce their K splits inside the GEMM (groups of
+        CTAs exchanging partials through L2); False: separate reduce kernels."""
         return bool(B.dd_get_option(self.ctx, B.DD_OPT_FUSED_REDUCE))
 
     @fused_reduce.setter
@@ -142,9 +142,9 @@ class Decoder:
         B.dd_set_option(self.ctx, B.DD_OPT_FUSED_REDUCE, 1 if on else 0)
 
     def fused_plan(self) -> dict:
-        """{layer: (cluster size, grid)} of the fused linear layers (zeros when unavailable)."""
-        return {k: (B.dd_get_option(self.ctx, B.DD_OPT_FUSED_CLUSTER[k]), B.dd_get_option(self.ctx, B.DD_OPT_FUSED_GRID[k]))
-                for k in B.DD_OPT_FUSED_CLUSTER}
+        """{layer: (K splits, grid)} of the fused linear layers (zeros when unavailable)."""
+        return {k: (B.dd_get_option(self.ctx, B.DD_OPT_FUSED_SPLITS[k]), B.dd_get_option(self.ctx, B.DD_OPT_FUSED_GRID[k]))
+                for k in B.DD_OPT_FUSED_SPLITS}
 
     def probe_step(self, tokens, mask, gamma, mode=MODE_THRESHOLD, logits=True, stream=None):
         """One step with every probe output; returns a dict of tensors."""

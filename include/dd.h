@@ -233,24 +233,22 @@ dd_status dd_step_launch_count(dd_ctx* ctx, int32_t* n);
 /* Context options.
  *   DD_OPT_FUSED_REDUCE (set/get, 0 or 1): with 1 the linear layers of the
  *     step (QKV, O, gate|up and every down projection but the last) sum
- *     their split-K partials inside the GEMM, the K splits of a 128-feature
- *     tile running as one thread-block cluster that reduces through
- *     distributed shared memory, and apply their epilogue there (rotary
+ *     their split-K partials inside the GEMM: the CTAs that split one
+ *     128-feature tile's K form a group (the whole grid resident at once),
+ *     exchange fp32 partial tiles through an L2-resident scratch and a
+ *     per-group counter, and apply the layer's epilogue there (rotary
  *     positions, SwiGLU, residual add); the RMSNorms before attention and
- *     before the MLP are then deferred into the consuming GEMM (the layer
- *     is linear in its input, so only the rounding order changes).  With 0
+ *     before the MLP are then deferred into the consuming GEMM (the layer is
+ *     linear in its input, so only the rounding order changes).  With 0
  *     every linear layer writes fp32 partials and a separate kernel reduces
- *     them.  The default is 0 (on the small decode workload the separate
- *     kernels overlap better inside the step graph); 1 is available where
- *     batch * block <= 128 and the clusters fit on the device, elsewhere
- *     setting it returns DD_ERR_UNSUPPORTED.  Switching drops the captured
- *     graphs.
- *   DD_OPT_FUSED_CLUSTER_* / DD_OPT_FUSED_GRID_* (get only): the cluster
- *     size (= K splits) and grid of each fused layer (0 when unavailable).
+ *     them.  1 is available where batch * block <= 128; elsewhere setting it
+ *     returns DD_ERR_UNSUPPORTED.  Switching drops the captured graphs.
+ *   DD_OPT_FUSED_SPLITS_* / DD_OPT_FUSED_GRID_* (get only): the K splits
+ *     (group size) and grid of each fused layer (0 when unavailable).
  */
 enum {
   DD_OPT_FUSED_REDUCE = 1,
-  DD_OPT_FUSED_CLUSTER_QKV = 2, DD_OPT_FUSED_CLUSTER_O, DD_OPT_FUSED_CLUSTER_GATE_UP, DD_OPT_FUSED_CLUSTER_DOWN,
+  DD_OPT_FUSED_SPLITS_QKV = 2, DD_OPT_FUSED_SPLITS_O, DD_OPT_FUSED_SPLITS_GATE_UP, DD_OPT_FUSED_SPLITS_DOWN,
   DD_OPT_FUSED_GRID_QKV = 6, DD_OPT_FUSED_GRID_O, DD_OPT_FUSED_GRID_GATE_UP, DD_OPT_FUSED_GRID_DOWN
 };
 dd_status dd_set_option(dd_ctx* ctx, int32_t option, int32_t value);

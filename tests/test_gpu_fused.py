@@ -1,7 +1,7 @@
-"""The linear layers with the split-K reduction inside the GEMM (thread-block
-clusters reducing through distributed shared memory, deferred RMSNorm) and
+"""The linear layers with the split-K reduction inside the GEMM (groups of CTAs
+exchanging partial tiles through L2, deferred RMSNorm) and
 the path with separate reduce kernels: both against the oracle, and against
-each other, on several row counts (one and several TMEM column blocks, cluster
+each other, on several row counts (one and several TMEM column blocks, group
 sizes from the planner), with and without rotary positions."""
 import numpy as np
 import pytest
@@ -92,7 +92,7 @@ def test_option_errors():
     with pytest.raises(B.DDError):
         B.dd_get_option(p.dec.ctx, 77)
     with pytest.raises(B.DDError):
-        B.dd_set_option(p.dec.ctx, B.DD_OPT_FUSED_CLUSTER["qkv"], 4)
+        B.dd_set_option(p.dec.ctx, B.DD_OPT_FUSED_SPLITS["qkv"], 4)
     p.dec.close()
 
 
