@@ -28,9 +28,9 @@
 // Inside the step graph of the small decode workload (128 rows) this path
 // measured slower than plain GEMMs followed by reduce kernels (20.2k against
 // 24.8k committed tokens/s): under programmatic dependent launch a reduce
-// kernel overlaps the next GEMM's first weight loads, while a reduction at
-// the end of the GEMM is on the critical path.  The step runs it only when
-// DD_OPT_FUSED_REDUCE asks for it.
+// kernel overlaps the GEMM's drain and the next GEMM's first weight loads,
+// while a reduction at the end of the GEMM is wholly on the critical path.
+// The step runs it only when DD_OPT_FUSED_REDUCE asks for it.
 //
 // Roles (192 threads) as in the plain GEMM: warp 0 issues TMA loads, warp 1
 // owns TMEM and issues the MMAs, warps 2-5 run the epilogue.  Every wait is

@@ -87,6 +87,24 @@ def test_null_pointers_rejected_before_cuda(lib):
         B.dd_commit(0, 16, 0, 0, 0, 0, 0.8, 0, 0, 0)
     with pytest.raises(B.DDError):
         B.dd_test_wait_timeout(0, 0)
+    with pytest.raises(B.DDError) as e:
+        B.dd_set_option(0, B.DD_OPT_FUSED_REDUCE, 1)
+    assert e.value.status == B.DD_ERR_INVALID_ARG
+    with pytest.raises(B.DDError) as e:
+        B.dd_get_option(0, B.DD_OPT_FUSED_REDUCE)
+    assert e.value.status == B.DD_ERR_INVALID_ARG
+
+
+def test_workspace_holds_the_fused_layer_scratch(lib):
+    """Configurations of at most 128 activation rows reserve the fused linear
+    layers' partial-tile scratch (one CTA per SM, two slots of [rows][128]
+    fp32 each) and counters; larger ones do not."""
+    small = B.dd_workspace_size(config_struct(synth.SMALL))
+    big = B.dd_workspace_size(config_struct(synth.SMALL.replace(batch=16)))
+    scratch = 148 * 2 * 128 * 128 * 4
+    assert small > scratch
+    # doubling the batch doubles the activations but drops the scratch
+    assert big < 2 * small
 
 
 def test_kernel_workspace_sizes(lib):
