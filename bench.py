@@ -266,6 +266,28 @@ def algorithmic_bytes(cfg, kind, ctx_len):
     return None
 
 
+def mlp_gemm_rates(cfg, kernels, hbm_peak, tc_sust, peak_src):
+    """The MLP GEMMs (gate|up, down) of the step from the per-kind profile: HBM
+    rate of their algorithmic bytes, and tensor rate of their algorithmic
+    FLOPs (2*R*K*N) and of the FLOPs the tensor cores execute (twice that: the
+    activation operand is a bf16 head plus a bf16 remainder), against the
+    sustained bf16 peak (kernels timed inside a long step)."""
+    R, H, F = cfg.rows, cfg.hidden, cfg.mlp
+    out = {}
+    for kind, n, k in (("gemm_gate_up", 2 * F, H), ("gemm_down", H, F)):
+        if kind not in kernels:
+            continue
+        us = kernels[kind]["us_per_launch"]
+        flops = 2.0 * R * k * n
+        tf = flops / (us * 1e-6) / 1e12
+        gbs = algorithmic_bytes(cfg, kind, 0) / (us * 1e-6) / 1e9
+        out[kind] = {"us_per_launch": us, "hbm_GBps": gbs, "hbm_frac": gbs / hbm_peak,
+                     "tflops_algorithmic": tf, "tflops_executed": 2 * tf, "tensor_peak_tflops": tc_sust,
+                     "tensor_frac_algorithmic": tf / tc_sust, "tensor_frac_executed": 2 * tf / tc_sust,
+                     "peak_source": peak_src + " (sustained bf16)"}
+    return out
+
+
 def step_roofline(cfg, T0, hbm_peak, ms_per_step, denoise_per_step, peak_src):
     """The whole denoising step against HBM: every weight read once, the context
     K/V of every layer read once (mean context over the step's blocks)."""
@@ -439,7 +461,8 @@ def gpu_arm(args, world, rank, local):
             "roofline": roofline, "kernels": kernels,
             "commits_per_step": {"first_block": commits, "mean": float(np.mean(commits)) if commits else None},
             "step_roofline": step_roofline(cfg, T0, hbm_peak, ms_max / args.steps,
-                                           timed_denoise / max(args.steps, 1), peak_src)}
+                                           timed_denoise / max(args.steps, 1), peak_src),
+            "mlp_gemms": mlp_gemm_rates(cfg, kernels, hbm_peak, tc_sust, peak_src)}
 
     # -------------------------------- microbenchmarks named by the metric
     if not args.no_micro and rank == 0:
