@@ -126,7 +126,7 @@ struct dd_ctx {
   bool fused_ok, fused_on;
   dd_context_tower tower;  // borrowed; tower.wkv == nullptr until dd_set_context_tower
   CUtensorMap m_tower;
-  CUtensorMap m_lm, m_y_b, m_attn_b, m_h_b, m_y_a, m_yc_a, m_kc, m_vc, m_kc128, m_vc128, m_q, m_blk;
+  CUtensorMap m_lm, m_y_b, m_attn_b, m_h_b, m_y_a, m_yc_a, m_kc, m_vc, m_kc128, m_vc128, m_q;
   cudaStream_t cap_stream;
   cudaGraphExec_t exec;       // one denoising step
   cudaGraphExec_t loop_exec;  // while (masked left): step  -- the device-side decode loop
@@ -358,7 +358,7 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)cf.head_dim);
     a.status = status;
     a.timeout_ns = c->timeout_ns;
-    DD_CUDA(dd::launch_attention(L.p_attn, a, c->m_kc, c->m_vc, c->m_kc128, c->m_vc128, c->m_q, c->m_blk, st));
+    DD_CUDA(dd::launch_attention(L.p_attn, a, c->m_kc, c->m_vc, c->m_kc128, c->m_vc128, c->m_q, st));
     mk(kKAttention);
     if (L.p_attn.use_tc || L.p_attn.n_splits > 1) {
       DD_CUDA(dd::launch_attention_combine(L.p_attn, a, st));
@@ -599,8 +599,7 @@ dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_byte
             dd::make_map_2d(&c->m_h_b, c->ws + L.hmid, 2 * c->R, cf.mlp, L.p_d.BN) &&
             dd::make_map_2d(&c->m_y_a, c->ws + L.y, 2 * c->R, cf.hidden, 128) &&
             dd::make_map_2d(&c->m_yc_a, c->ws + L.yc, 2 * c->R, cf.hidden, 128) &&
-            dd::make_map_q(&c->m_q, c->ws + L.qkv, 2 * c->R, c->qkvw, cf.n_q_heads, cf.head_dim, c->G, cf.block) &&
-            dd::make_map_2d(&c->m_blk, c->ws + L.qkv, 2 * c->R, c->qkvw, cf.block);
+            dd::make_map_q(&c->m_q, c->ws + L.qkv, 2 * c->R, c->qkvw, cf.n_q_heads, cf.head_dim, c->G, cf.block);
   if (!ok) {
     dd_destroy(c);
     return fail(DD_ERR_CUDA, "tensor map encoding failed for the workspace buffers");
@@ -999,11 +998,10 @@ dd_status dd_block_attention(const dd_attn_problem* p, void* stream) {
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)p->head_dim);
   a.status = small + 1;
   a.timeout_ns = dd::kDefaultTimeoutNs;
-  CUtensorMap mq, mblk;
-  if (!dd::make_map_q(&mq, p->qkv, (uint64_t)p->batch * p->block, a.ld_qkv, p->n_q_heads, p->head_dim, a.G, p->block) ||
-      !dd::make_map_2d(&mblk, p->qkv, (uint64_t)p->batch * p->block, a.ld_qkv, p->block))
+  CUtensorMap mq;
+  if (!dd::make_map_q(&mq, p->qkv, (uint64_t)p->batch * p->block, a.ld_qkv, p->n_q_heads, p->head_dim, a.G, p->block))
     return fail(DD_ERR_CUDA, "tensor map encoding failed for qkv");
-  DD_CUDA(dd::launch_attention(plan, a, mk, mv, mk128, mv128, mq, mblk, st));
+  DD_CUDA(dd::launch_attention(plan, a, mk, mv, mk128, mv128, mq, st));
   DD_CUDA(dd::launch_attention_combine(plan, a, st));
   return DD_OK;
 }

@@ -382,6 +382,314 @@ __global__ void k_attn_combine(const AttnArgs a, int n_splits) {
   }
 }
 
+// tcgen05 path, after the context kernel: the S in-block keys of one
+// (sequence, kv head) on the mma.sync tensor cores (q, k, v and p as bf16
+// head + remainder, as in the context kernels), then the log-sum-exp merge
+// with the n_ctx context partials:
+// o = (2^(m_b - M) o_b + sum_s 2^(m_s - M) o_s) / (2^(m_b - M) l_b + sum_s 2^(m_s - M) l_s).
+// One CTA per (sequence, kv head); warp w takes query rows 16w .. 16w + 15
+// (row r = g * S + i) and keeps them in the m16n8 fragment layout throughout.
+template <int D, bool SPLIT>
+__global__ void __launch_bounds__(128) k_attn_merge_block(const AttnArgs a, int n_ctx) {
+  constexpr int kBlkB = kKTB * D * 2;
+  __shared__ __align__(128) uint8_t blk[(SPLIT ? 4 : 2) * kBlkB];  // k, v (, k_lo, v_lo)
+  pdl_wait();  // q|k|v and the context partials come from the preceding kernels
+  pdl_launch_dependents();
+  const int kvh = blockIdx.x % a.Hkv, b = blockIdx.x / a.Hkv;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int rows = a.G * a.S;
+  const int R = a.B * a.S;
+  const __nv_bfloat16* qkv = reinterpret_cast<const __nv_bfloat16*>(a.qkv);
+
+  // block K and V (rows >= S zero) -> swizzled tiles; all of a thread's
+  // loads are issued before its stores
+  {
+    constexpr int kChunks = kKTB * (D / 8);
+    constexpr int kTiles = SPLIT ? 4 : 2;
+    constexpr int kPer = (kTiles * kChunks + 127) / 128;
+    uint4 val[kPer];
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int c = threadIdx.x + j * 128;
+      const int which = c / kChunks;  // 0 = k, 1 = v, 2 = k_lo, 3 = v_lo
+      const int cc = c % kChunks;
+      const int r = cc / (D / 8), col = (cc % (D / 8)) * 8;
+      val[j] = make_uint4(0, 0, 0, 0);
+      if (c < kTiles * kChunks && r < a.S) {
+        const long long row = (long long)(which >= 2 ? R : 0) + b * a.S + r;
+        val[j] = *reinterpret_cast<const uint4*>(qkv + row * a.ld_qkv + (a.Hq + (which & 1) * a.Hkv + kvh) * D + col);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kPer; ++j) {
+      const int c = threadIdx.x + j * 128;
+      if (c < kTiles * kChunks) {
+        const int which = c / kChunks;
+        const int cc = c % kChunks;
+        const int r = cc / (D / 8), col = (cc % (D / 8)) * 8;
+        *reinterpret_cast<uint4*>(blk + which * kBlkB + swz_off(kKTB, r, col)) = val[j];
+      }
+    }
+  }
+  // q fragments of this warp's rows (r0 = 16w + lane/4, r1 = r0 + 8)
+  const int r0 = warp * 16 + (lane >> 2);
+  const int r1 = r0 + 8;
+  const int g0 = r0 / a.S, i0 = r0 % a.S;
+  const int g1 = r1 / a.S, i1 = r1 % a.S;
+  const int h0 = kvh * a.G + g0, h1 = kvh * a.G + g1;
+  uint32_t qh[D / 16][4], ql[D / 16][4];
+#pragma unroll
+  for (int half = 0; half < (SPLIT ? 2 : 1); ++half) {
+    const long long ro = half ? R : 0;
+    const __nv_bfloat16* q0 = qkv + (ro + b * a.S + i0) * a.ld_qkv + h0 * D + (lane & 3) * 2;
+    const __nv_bfloat16* q1 = qkv + (ro + b * a.S + i1) * a.ld_qkv + h1 * D + (lane & 3) * 2;
+    uint32_t(&qf)[D / 16][4] = half ? ql : qh;
+#pragma unroll
+    for (int kk = 0; kk < D / 16; ++kk) {
+      qf[kk][0] = *reinterpret_cast<const uint32_t*>(q0 + kk * 16);
+      qf[kk][1] = *reinterpret_cast<const uint32_t*>(q1 + kk * 16);
+      qf[kk][2] = *reinterpret_cast<const uint32_t*>(q0 + kk * 16 + 8);
+      qf[kk][3] = *reinterpret_cast<const uint32_t*>(q1 + kk * 16 + 8);
+    }
+  }
+  __syncthreads();
+  if (warp * 16 >= rows) return;
+
+  float o[D / 8][4];
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const uint32_t bk = smem_u32(blk);
+  attend_tile<D, kKTB, SPLIT, SPLIT>(bk, bk + kBlkB, bk + 2 * kBlkB, bk + 3 * kBlkB, a.S, qh, ql, o, m0, m1, l0, l1,
+                                     a.scale_log2, lane);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+
+  // fold in the context partials, one slot per round trip
+  const long long pbase = (long long)(b * a.Hkv + kvh) * n_ctx * rows;
+  for (int sl = 0; sl < n_ctx; ++sl) {
+    const long long pr = pbase + (long long)sl * rows;
+    const float2 ml0 = a.part_ml[pr + r0], ml1 = a.part_ml[pr + r1];
+    const float* p0 = a.part_o + (pr + r0) * D + (lane & 3) * 2;
+    const float* p1 = a.part_o + (pr + r1) * D + (lane & 3) * 2;
+    float2 v0[D / 8], v1[D / 8];
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      v0[n] = *reinterpret_cast<const float2*>(p0 + n * 8);
+      v1[n] = *reinterpret_cast<const float2*>(p1 + n * 8);
+    }
+    const float mn0 = fmaxf(m0, ml0.x), mn1 = fmaxf(m1, ml1.x);
+    const float wa0 = exp2f(m0 - mn0), wb0 = ml0.x == -INFINITY ? 0.f : exp2f(ml0.x - mn0);
+    const float wa1 = exp2f(m1 - mn1), wb1 = ml1.x == -INFINITY ? 0.f : exp2f(ml1.x - mn1);
+    l0 = l0 * wa0 + ml0.y * wb0;
+    l1 = l1 * wa1 + ml1.y * wb1;
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) {
+      o[n][0] = o[n][0] * wa0 + v0[n].x * wb0;
+      o[n][1] = o[n][1] * wa0 + v0[n].y * wb0;
+      o[n][2] = o[n][2] * wa1 + v1[n].x * wb1;
+      o[n][3] = o[n][3] * wa1 + v1[n].y * wb1;
+    }
+    m0 = mn0;
+    m1 = mn1;
+  }
+
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out);
+  const float inv0 = 1.f / l0, inv1 = 1.f / l1;
+  const long long lo_off = (long long)R * a.ld_out;
+  __nv_bfloat16* d0 = out + (long long)(b * a.S + i0) * a.ld_out + h0 * D + (lane & 3) * 2;
+  __nv_bfloat16* d1 = out + (long long)(b * a.S + i1) * a.ld_out + h1 * D + (lane & 3) * 2;
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n) {
+    uint32_t hi, lo;
+    split_bf16(o[n][0] * inv0, o[n][1] * inv0, hi, lo);
+    *reinterpret_cast<uint32_t*>(d0 + n * 8) = hi;
+    if (SPLIT) *reinterpret_cast<uint32_t*>(d0 + lo_off + n * 8) = lo;
+    split_bf16(o[n][2] * inv1, o[n][3] * inv1, hi, lo);
+    *reinterpret_cast<uint32_t*>(d1 + n * 8) = hi;
+    if (SPLIT) *reinterpret_cast<uint32_t*>(d1 + lo_off + n * 8) = lo;
+  }
+}
+
+// The same merge for shapes with few (sequence, kv head) pairs, where one
+// CTA per pair would leave most SMs idle: one warp per query row, 8 rows per
+// CTA, the block keys in fp32 on the CUDA cores (q, k, v rebuilt from head +
+// remainder).  Scores: lane = (key j = lane / 2, half of the head dim), so
+// each dot product is split over two lanes; the output: lane owns dims
+// lane + 32 k.  The row's context partials are loaded first, so their
+// latency overlaps the staging and the block keys' arithmetic.
+constexpr int kMergeBatch = 4;  // context partials per row held in registers
+
+template <int D>
+__global__ void __launch_bounds__(256) k_attn_merge_rows(const AttnArgs a, int n_ctx) {
+  constexpr int P = D / 32;      // output dims per lane
+  constexpr int H2 = D / 2;      // dims per half dot product
+  constexpr int KS = D + 8;      // padded row stride of the staged K (floats)
+  __shared__ __align__(16) float ks[kKTB * KS];
+  __shared__ __align__(16) float vs[kKTB * D];
+  __shared__ __align__(16) float qs[8 * D];
+  pdl_wait();  // q|k|v and the context partials come from the preceding kernels
+  pdl_launch_dependents();
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int S = a.S, rows = a.G * S;
+  const int ctas_per_bk = (rows + 7) / 8;
+  const int bk = blockIdx.x / ctas_per_bk;  // b * Hkv + kvh
+  const int r0 = (blockIdx.x % ctas_per_bk) * 8;
+  const int nq = min(8, rows - r0);
+  const int kvh = bk % a.Hkv, b = bk / a.Hkv;
+  const long long R = (long long)a.B * S;
+  const long long lo = a.split ? R * a.ld_qkv : 0;
+  const __nv_bfloat16* qkv = reinterpret_cast<const __nv_bfloat16*>(a.qkv);
+
+  // context partials of this warp's row
+  const int r = r0 + warp;
+  const bool active = warp < nq;
+  const long long pbase = (long long)bk * n_ctx * rows + r;
+  float2 ml[kMergeBatch];
+  float po[kMergeBatch][P];
+#pragma unroll
+  for (int t = 0; t < kMergeBatch; ++t) {
+    if (active && t < n_ctx) {
+      const long long pr = pbase + (long long)t * rows;
+      ml[t] = a.part_ml[pr];
+#pragma unroll
+      for (int k = 0; k < P; ++k) po[t][k] = a.part_o[pr * D + lane + 32 * k];
+    }
+  }
+
+  // q rows of this CTA, block K and block V -> shared memory (fp32, head +
+  // remainder); every load of this thread is issued before its first store
+  constexpr int CPR = D / 8;                                // 16-byte chunks per row
+  constexpr int kPer = ((8 + 2 * kKTB) * CPR + 255) / 256;  // chunks per thread, at most
+  const int total = (nq + 2 * S) * CPR;
+  uint4 hv[kPer], lv[kPer];
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int c = threadIdx.x + u * 256;
+    if (c < total) {
+      const int row = c / CPR, col = (c % CPR) * 8;
+      long long off;
+      if (row < nq) {
+        const int rr = r0 + row;
+        off = (long long)(b * S + rr % S) * a.ld_qkv + (kvh * a.G + rr / S) * D + col;
+      } else {
+        const int kv = row - nq, which = kv >= S ? 1 : 0, j = kv - which * S;
+        off = (long long)(b * S + j) * a.ld_qkv + (a.Hq + which * a.Hkv + kvh) * D + col;
+      }
+      hv[u] = *reinterpret_cast<const uint4*>(qkv + off);
+      lv[u] = a.split ? *reinterpret_cast<const uint4*>(qkv + lo + off) : make_uint4(0, 0, 0, 0);
+    }
+  }
+#pragma unroll
+  for (int u = 0; u < kPer; ++u) {
+    const int c = threadIdx.x + u * 256;
+    if (c < total) {
+      const int row = c / CPR, col = (c % CPR) * 8;
+      float* dst;
+      if (row < nq) {
+        dst = qs + row * D + col;
+      } else {
+        const int kv = row - nq, which = kv >= S ? 1 : 0, j = kv - which * S;
+        dst = which ? vs + j * D + col : ks + j * KS + col;
+      }
+      const uint32_t hw[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
+      const uint32_t lw[4] = {lv[u].x, lv[u].y, lv[u].z, lv[u].w};
+      float v[8];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        v[2 * e] = __uint_as_float(hw[e] << 16) + __uint_as_float(lw[e] << 16);
+        v[2 * e + 1] = __uint_as_float(hw[e] & 0xffff0000u) + __uint_as_float(lw[e] & 0xffff0000u);
+      }
+      reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
+      reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+    }
+  }
+  __syncthreads();
+  if (!active) return;
+
+  // scores of keys j = lane / 2 + 16 u (u = 0, 1; S <= 32), in base-2 units
+  const int half = lane & 1;
+  float sj[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) {
+    const int j = (lane >> 1) + 16 * u;
+    float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+    if (j < S) {
+      const float4* kr = reinterpret_cast<const float4*>(ks + j * KS);
+      const float4* qr = reinterpret_cast<const float4*>(qs + warp * D);
+#pragma unroll
+      for (int m = 0; m < H2 / 4; ++m) {
+        // interleaved 16-byte chunks: this half takes chunk 2m + half
+        const float4 kv = kr[2 * m + half], qv = qr[2 * m + half];
+        t0 = fmaf(qv.x, kv.x, t0);
+        t1 = fmaf(qv.y, kv.y, t1);
+        t2 = fmaf(qv.z, kv.z, t2);
+        t3 = fmaf(qv.w, kv.w, t3);
+      }
+    }
+    float t = (t0 + t1) + (t2 + t3);
+    t += __shfl_xor_sync(0xffffffffu, t, 1);
+    sj[u] = j < S ? t * a.scale_log2 : -INFINITY;
+  }
+  float mb = fmaxf(sj[0], sj[1]);
+#pragma unroll
+  for (int o = 2; o < 32; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+  float pj[2];
+#pragma unroll
+  for (int u = 0; u < 2; ++u) pj[u] = sj[u] == -INFINITY ? 0.f : exp2f(sj[u] - mb);
+  float lb = half ? 0.f : pj[0] + pj[1];
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) lb += __shfl_xor_sync(0xffffffffu, lb, o);
+  float acc[P];
+#pragma unroll
+  for (int k = 0; k < P; ++k) acc[k] = 0.f;
+  for (int jj = 0; jj < S; ++jj) {
+    const float p = __shfl_sync(0xffffffffu, jj < 16 ? pj[0] : pj[1], 2 * (jj & 15));
+#pragma unroll
+    for (int k = 0; k < P; ++k) acc[k] = fmaf(p, vs[jj * D + lane + 32 * k], acc[k]);
+  }
+
+  // merge with the context partials (beyond the first kMergeBatch: loaded here)
+  float M = mb, L = lb;
+  for (int s0 = 0; s0 < n_ctx; s0 += kMergeBatch) {
+    if (s0 > 0) {
+#pragma unroll
+      for (int t = 0; t < kMergeBatch; ++t) {
+        if (s0 + t < n_ctx) {
+          const long long pr = pbase + (long long)(s0 + t) * rows;
+          ml[t] = a.part_ml[pr];
+#pragma unroll
+          for (int k = 0; k < P; ++k) po[t][k] = a.part_o[pr * D + lane + 32 * k];
+        }
+      }
+    }
+#pragma unroll
+    for (int t = 0; t < kMergeBatch; ++t) {
+      if (s0 + t < n_ctx && ml[t].x != -INFINITY) {
+        const float Mn = fmaxf(M, ml[t].x);
+        const float wa = exp2f(M - Mn), wb = exp2f(ml[t].x - Mn);
+        L = L * wa + ml[t].y * wb;
+#pragma unroll
+        for (int k = 0; k < P; ++k) acc[k] = acc[k] * wa + po[t][k] * wb;
+        M = Mn;
+      }
+    }
+  }
+  const int g = r / S, i = r % S;
+  __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(a.out) + (long long)(b * S + i) * a.ld_out +
+                       (kvh * a.G + g) * D + lane;
+  const float inv = 1.f / L;
+#pragma unroll
+  for (int k = 0; k < P; ++k) {
+    const float v = acc[k] * inv;
+    const __nv_bfloat16 h = __float2bfloat16_rn(v);
+    out[32 * k] = h;
+    if (a.split) out[R * a.ld_out + 32 * k] = __float2bfloat16_rn(v - __bfloat162float(h));
+  }
+}
+
 template <int D, bool SPLIT>
 void launch_attn_kernel(const AttnPlan& p, const AttnArgs& a, int grid_x, const CUtensorMap& mk,
                         const CUtensorMap& mv, cudaStream_t st) {
@@ -404,10 +712,10 @@ AttnPlan plan_attention(int B, int S, int Hq, int Hkv, int D, int max_ctx, int a
   p.warps_c = p.rows / 16;
   p.stages = D == 128 ? attn_stages<128>() : attn_stages<64>();
   p.smem_bytes = D == 128 ? attn_smem_bytes<128, true>() : attn_smem_bytes<64, true>();
-  if (allow_tc && attention_tc_supported(D, p.rows, S) && max_ctx > 0) {
+  if (allow_tc && attention_tc_supported(D, p.rows) && max_ctx > 0) {
     p.use_tc = 1;
     p.n_ctx = attention_tc_splits(B, Hkv, max_ctx);
-    p.n_splits = p.n_ctx;  // partial slots: the context splits, the last with the block keys
+    p.n_splits = p.n_ctx;  // partial slots: the context splits (block keys are merged in-line)
     return p;
   }
   const int pairs = B * Hkv;
@@ -429,10 +737,10 @@ size_t attention_partial_bytes(const AttnPlan& p, int B, int Hkv) {
 
 cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a_in, const CUtensorMap& map_k, const CUtensorMap& map_v,
                              const CUtensorMap& map_k128, const CUtensorMap& map_v128, const CUtensorMap& map_q,
-                             const CUtensorMap& map_blk, cudaStream_t st) {
+                             cudaStream_t st) {
   AttnArgs a = a_in;
-  // tcgen05 path: context splits, the block keys in the last one
-  if (p.use_tc) return launch_attention_tc(a, p.n_ctx, map_k128, map_v128, map_q, map_blk, st);
+  // tcgen05 path: context splits only; the block keys join in the merge
+  if (p.use_tc) return launch_attention_tc(a, p.n_ctx, map_k128, map_v128, map_q, st);
   if (p.D == 128) {
     if (a.split) launch_attn_kernel<128, true>(p, a, p.n_splits, map_k, map_v, st);
     else launch_attn_kernel<128, false>(p, a, p.n_splits, map_k, map_v, st);
@@ -445,11 +753,21 @@ cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a_in, const CUte
 
 cudaError_t launch_attention_combine(const AttnPlan& p, const AttnArgs& a, cudaStream_t st) {
   if (p.use_tc) {
-    // every key (context and block) is in the n_ctx partials
-    const long long warps = (long long)a.B * a.Hkv * p.rows;
-    const int blocks = (int)((warps + 7) / 8);
-    if (p.D == 128) return launch_k(k_attn_combine<128>, blocks, 256, 0, st, a, p.n_ctx);
-    return launch_k(k_attn_combine<64>, blocks, 256, 0, st, a, p.n_ctx);
+    const int bk = a.B * a.Hkv;
+    if (bk < kNumSMs) {
+      // few pairs: one warp per row, 8 rows per CTA
+      const int blocks = bk * ((p.rows + 7) / 8);
+      if (p.D == 128) return launch_k(k_attn_merge_rows<128>, blocks, 256, 0, st, a, p.n_ctx);
+      return launch_k(k_attn_merge_rows<64>, blocks, 256, 0, st, a, p.n_ctx);
+    }
+    // one CTA per (sequence, kv head), one warp per 16 query rows
+    const int blocks = bk, threads = ((p.rows + 15) / 16) * 32;
+    if (p.D == 128) {
+      if (a.split) return launch_k(k_attn_merge_block<128, true>, blocks, threads, 0, st, a, p.n_ctx);
+      return launch_k(k_attn_merge_block<128, false>, blocks, threads, 0, st, a, p.n_ctx);
+    }
+    if (a.split) return launch_k(k_attn_merge_block<64, true>, blocks, threads, 0, st, a, p.n_ctx);
+    return launch_k(k_attn_merge_block<64, false>, blocks, threads, 0, st, a, p.n_ctx);
   }
   if (p.n_splits == 1) return cudaSuccess;
   const long long warps = (long long)a.B * a.Hkv * p.rows;
@@ -470,7 +788,10 @@ cudaError_t prepare_attention_kernels() {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
     if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   }
-  const void* comb[] = {(const void*)k_attn_combine<128>, (const void*)k_attn_combine<64>};
+  const void* comb[] = {(const void*)k_attn_combine<128>,          (const void*)k_attn_combine<64>,
+                        (const void*)k_attn_merge_block<128, true>, (const void*)k_attn_merge_block<128, false>,
+                        (const void*)k_attn_merge_block<64, true>,  (const void*)k_attn_merge_block<64, false>,
+                        (const void*)k_attn_merge_rows<128>,        (const void*)k_attn_merge_rows<64>};
   for (const void* f : comb) {
     if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   }

@@ -1,16 +1,8 @@
-// Block attention on the tcgen05 tensor cores (head dim 128, 64 query rows
-// per (sequence, kv head)): the context keys, split over work items, and the
-// S in-block keys as one more tile of the pair's last split.  Each split
-// writes a partial (o, m, l) and a combine kernel merges them (TwoTower
-// article, "技術/ビジネス面": one softmax over the context and the block).
-//
-// The block tile holds the S block keys' bf16 heads in key rows 0..S-1 and,
-// with split activations, their bf16 remainders in rows S..2S-1 (both read by
-// TMA from the q|k|v rows).  Score column j + S then carries q . k_rem(j), so
-// the softmax adds it to column j and masks every column from S on; it writes
-// P(j) to both column j and column j + S, so the PV product adds p v_head +
-// p v_rem.  Key rows from 2S on keep whatever an earlier tile left there (the
-// V slots are zeroed at the start, so that is always finite) and meet P = 0.
+// Context part of the block attention on the tcgen05 tensor cores (head dim
+// 128, 64 query rows per (sequence, kv head)).  Each split writes a partial
+// (o, m, l); the merge kernel adds the block keys and combines them all
+// (TwoTower article, "技術/ビジネス面": one softmax over the context and the
+// block).
 //
 // Per 128-key tile:
 //   S[64 q][128 keys] = Q[64][128] . K_tile[128][128]^T     (M=64, K-major A and B)
@@ -103,28 +95,6 @@ __device__ __forceinline__ void stmatrix_x4(uint32_t saddr, uint32_t r0, uint32_
                : "memory");
 }
 
-// Scores of a block tile in the fragment layout (value i: fragment rep i/4,
-// columns 8*(i/4) + 2*(lane%4) + i%2): block key j < S sits in reps < SH = S/8;
-// with split activations rep r + SH holds the same keys' remainder products,
-// added here; every column from S on is then masked.
-template <int SH>
-__device__ __forceinline__ void blk_scores(float (&v)[64], bool split) {
-  if (split) {
-#pragma unroll
-    for (int i = 0; i < 4 * SH; ++i) v[i] += v[i + 4 * SH];
-  }
-#pragma unroll
-  for (int i = 4 * SH; i < 64; ++i) v[i] = -INFINITY;
-}
-
-// P of the block keys also into the remainder rows' columns (PV then adds
-// p v_head + p v_rem).
-template <int SH>
-__device__ __forceinline__ void blk_dup(float (&v)[64]) {
-#pragma unroll
-  for (int i = 0; i < 4 * SH; ++i) v[i + 4 * SH] = v[i];
-}
-
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -141,8 +111,7 @@ __device__ __forceinline__ float ex2(float x) {
 template <bool SPLITQ>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_ctx_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                  const __grid_constant__ CUtensorMap map_q, const __grid_constant__ CUtensorMap map_blk,
-                  const AttnArgs a, int n_ctx, int n_items) {
+                  const __grid_constant__ CUtensorMap map_q, const AttnArgs a, int n_ctx, int n_items) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -167,8 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int ntiles_all = (T + kKT - 1) / kKT;
   const int per = (ntiles_all + n_ctx - 1) / n_ctx;
   const int R = a.B * a.S;
-  // item w -> (split, kv head, sequence, first tile, context tile count);
-  // the last split of a pair also takes the block tile (tile index nt)
+  // item w -> (split, kv head, sequence, first tile, tile count)
   auto item = [&](int w, int& split, int& kvh, int& b, int& tile0, int& nt) {
     split = w % n_ctx;
     const int pair = w / n_ctx;
@@ -177,7 +145,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tile0 = split * per;
     nt = max(0, min(ntiles_all, tile0 + per) - tile0);
   };
-  auto tiles_of = [&](int split, int nt) { return nt + (split == n_ctx - 1 ? 1 : 0); };
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -205,10 +172,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tmem_alloc(tmem_slot, kTmemCols);
     tc_fence_before();
   }
-  // V rows a tile leaves unwritten meet P = 0 in PV: they must be finite
-  for (int i = threadIdx.x; i < 2 * kKV / 16; i += blockDim.x)
-    *reinterpret_cast<uint4*>(smem + kOffV + 16 * i) = make_uint4(0u, 0u, 0u, 0u);
-  fence_proxy_async_smem();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
@@ -229,29 +192,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_arrive_expect_tx(&vfull[s], kKV);
         tma_load_3d(smem + kOffV + s * kKV, &map_v, &vfull[s], 0, key0, z);
         tma_load_3d(smem + kOffV + s * kKV + kBox, &map_v, &vfull[s], 64, key0, z);
-        return true;
-      };
-      // the block tile of (sequence b, kv head kvh): heads in key rows 0..S-1,
-      // remainders in rows S..2S-1
-      auto load_blk = [&](int g, int b, int kvh) {
-        const int s = g & 1;
-        const uint32_t ph = (g >> 1) & 1;
-        const uint32_t bytes = (SPLITQ ? 2 : 1) * 2 * a.S * 128;
-        const int xk = a.Hq * kD + kvh * kD, xv = (a.Hq + a.Hkv) * kD + kvh * kD;
-        if (!mbar_wait_bounded(&kempty[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) return false;
-        mbar_arrive_expect_tx(&kfull[s], bytes);
-        for (int h = 0; h < 2; ++h) {
-          uint8_t* d = smem + kOffK + s * kKV + h * kBox;
-          tma_load_2d(d, &map_blk, &kfull[s], xk + 64 * h, b * a.S);
-          if (SPLITQ) tma_load_2d(d + a.S * 128, &map_blk, &kfull[s], xk + 64 * h, R + b * a.S);
-        }
-        if (!mbar_wait_bounded(&vempty[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) return false;
-        mbar_arrive_expect_tx(&vfull[s], bytes);
-        for (int h = 0; h < 2; ++h) {
-          uint8_t* d = smem + kOffV + s * kKV + h * kBox;
-          tma_load_2d(d, &map_blk, &vfull[s], xv + 64 * h, b * a.S);
-          if (SPLITQ) tma_load_2d(d + a.S * 128, &map_blk, &vfull[s], xv + 64 * h, R + b * a.S);
-        }
         return true;
       };
       // The context K/V do not depend on the preceding kernel: the first
@@ -279,9 +219,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(q + kQ, &map_q, &qfull[qb], 0, kvh * a.G, R + b * a.S);
           tma_load_3d(q + kQ + kRowBox, &map_q, &qfull[qb], 64, kvh * a.G, R + b * a.S);
         }
-        const int nte = tiles_of(split, nt);
-        for (int t = 0; t < nte && ok; ++t, ++g)
-          if (g >= pre) ok = t < nt ? load_kv(g, (tile0 + t) * kKT, a.z0 + b * a.Hkv + kvh) : load_blk(g, b, kvh);
+        for (int t = 0; t < nt && ok; ++t, ++g)
+          if (g >= pre) ok = load_kv(g, (tile0 + t) * kKT, a.z0 + b * a.Hkv + kvh);
       }
     }
     __syncwarp();
@@ -324,8 +263,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int qb = it & 1;
         if (!mbar_wait_bounded(&qfull[qb], (it >> 1) & 1, a.timeout_ns, abort_flag, a.status)) { ok = false; break; }
         const uint32_t qh = smem_u32(smem + kOffQ + qb * 2 * kQ), ql = qh + kQ;
-        const int nte = tiles_of(split, nt);
-        for (int t = 0; t < nte; ++t, ++g) {
+        for (int t = 0; t < nt; ++t, ++g) {
           const int s = g & 1;
           const uint32_t ph = (g >> 1) & 1;
           if (!mbar_wait_bounded(&kfull[s], ph, a.timeout_ns, abort_flag, a.status)) { ok = false; break; }
@@ -399,8 +337,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 64; ++j) o[j] = fmaf(o[j], (j & 2) ? a1 : a0, pv[j]);
         return true;
       };
-      const int nte = tiles_of(split, nt);
-      for (int t = 0; t < nte; ++t, ++g) {
+      for (int t = 0; t < nt; ++t, ++g) {
         const int s = g & 1;
         bool wt = true;
         if (lane == 0) wt = mbar_wait_bounded(&sfull[s], (g >> 1) & 1, a.timeout_ns, abort_flag, a.status);
@@ -412,15 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sfree[s]);
-        const bool blk = t == nt;
         const int kbase = (tile0 + t) * kKT;
-        if (blk) {
-          switch (a.S) {
-            case 8: blk_scores<1>(v, SPLITQ); break;
-            case 16: blk_scores<2>(v, SPLITQ); break;
-            default: blk_scores<4>(v, SPLITQ); break;  // 32
-          }
-        } else if (kbase + kKT > T) {  // tail tile: keys >= T do not exist
+        if (kbase + kKT > T) {  // tail tile: keys >= T do not exist
 #pragma unroll
           for (int j = 0; j < 64; ++j) {
             const int key = kbase + 8 * (j >> 2) + cq + (j & 1);
@@ -459,13 +389,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
         l0 = l0 * a0 + s0;
         l1 = l1 * a1 + s1;
-        if (SPLITQ && blk) {
-          switch (a.S) {
-            case 8: blk_dup<1>(v); break;
-            case 16: blk_dup<2>(v); break;
-            default: blk_dup<4>(v); break;
-          }
-        }
         // P (head, remainder) -> shared memory, once the previous PV is done
         if (g >= 1) {
           bool pw = true;
@@ -492,7 +415,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         al0 = a0;
         al1 = a1;
       }
-      if (ok && nte >= 1) ok = consume_o(g - 1, al0, al1);
+      if (ok && nt >= 1) ok = consume_o(g - 1, al0, al1);
       // partial slot `split`: o (unnormalised, [q][d]), (m, l) per q
       const long long prow = ((long long)(b * a.Hkv + kvh) * n_ctx + split) * kNQ;
 #pragma unroll
@@ -517,7 +440,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 }  // namespace
 
-bool attention_tc_supported(int D, int rows, int S) { return D == kD && rows == kNQ && S % 8 == 0 && S <= 32; }
+bool attention_tc_supported(int D, int rows) { return D == kD && rows == kNQ; }
 
 int attention_tc_splits(int B, int Hkv, int max_ctx) {
   const int pairs = B * Hkv;
@@ -539,16 +462,12 @@ int attention_tc_splits(int B, int Hkv, int max_ctx) {
 int attention_tc_smem_bytes() { return kSmemBytes; }
 
 cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx, const CUtensorMap& map_k128,
-                                const CUtensorMap& map_v128, const CUtensorMap& map_q, const CUtensorMap& map_blk,
-                                cudaStream_t st) {
-  if (a.S % 8 || a.S > 32 || (a.G * a.S) != kNQ) return cudaErrorInvalidValue;
+                                const CUtensorMap& map_v128, const CUtensorMap& map_q, cudaStream_t st) {
   const int items = a.B * a.Hkv * n_ctx;
   const int grid = items < kNumSMs ? items : kNumSMs;
   if (a.split)
-    return launch_k(k_attn_ctx_tc<true>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, map_q, map_blk, a, n_ctx,
-                    items);
-  return launch_k(k_attn_ctx_tc<false>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, map_q, map_blk, a, n_ctx,
-                  items);
+    return launch_k(k_attn_ctx_tc<true>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, map_q, a, n_ctx, items);
+  return launch_k(k_attn_ctx_tc<false>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, map_q, a, n_ctx, items);
 }
 
 cudaError_t prepare_attention_tc_kernels() {

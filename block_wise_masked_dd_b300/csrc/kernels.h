@@ -129,9 +129,9 @@ cudaError_t prepare_gemm_fused_kernels();
 
 struct AttnPlan {
   int D, rows, warps_c, n_splits, stages, smem_bytes;
-  // tcgen05 path (D = 128, 64 query rows, S a multiple of 8 up to 32): the
-  // context splits write partial slots 0..n_ctx-1 (n_splits = n_ctx), the
-  // last one including the S block keys; a combine kernel merges them.
+  // tcgen05 context path (D = 128, 64 query rows): the context splits write
+  // partial slots 0..n_ctx-1 (n_splits = n_ctx); the merge kernel adds the
+  // block keys and combines.
   int use_tc, n_ctx;
 };
 
@@ -154,20 +154,20 @@ struct AttnArgs {
 AttnPlan plan_attention(int B, int S, int Hq, int Hkv, int D, int max_ctx, int allow_tc = 1);
 size_t attention_partial_bytes(const AttnPlan& p, int B, int Hkv);
 // map_k/map_v: context cache maps with 64-row boxes; map_k128/map_v128: the
-// same caches with 128-row boxes, map_q the query rows (make_map_q) and
-// map_blk the q|k|v rows with S-row boxes (make_map_2d), for the tcgen05 path.
+// same caches with 128-row boxes, and map_q the query rows (make_map_q), for
+// the tcgen05 path.
 cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a, const CUtensorMap& map_k, const CUtensorMap& map_v,
                              const CUtensorMap& map_k128, const CUtensorMap& map_v128, const CUtensorMap& map_q,
-                             const CUtensorMap& map_blk, cudaStream_t st);
-// tcgen05 block attention (attention_tc.cu)
-bool attention_tc_supported(int D, int rows, int S);
+                             cudaStream_t st);
+// tcgen05 context attention (attention_tc.cu)
+bool attention_tc_supported(int D, int rows);
 int attention_tc_splits(int B, int Hkv, int max_ctx);
 int attention_tc_smem_bytes();
 cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx, const CUtensorMap& map_k128,
-                                const CUtensorMap& map_v128, const CUtensorMap& map_q, const CUtensorMap& map_blk,
-                                cudaStream_t st);
+                                const CUtensorMap& map_v128, const CUtensorMap& map_q, cudaStream_t st);
 cudaError_t prepare_attention_tc_kernels();
-// Merge the split partials (no-op for the mma.sync path with one split).
+// Merge the split partials (no-op for the mma.sync path with one split); on
+// the tcgen05 path this also attends to the block keys.
 cudaError_t launch_attention_combine(const AttnPlan& p, const AttnArgs& a, cudaStream_t st);
 
 // --------------------------------------------------- elementwise / small
