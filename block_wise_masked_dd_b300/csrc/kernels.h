@@ -54,7 +54,7 @@ struct GemmPlan {
   uint32_t tmem_half;             // TMEM columns per accumulator buffer (power of two >= BN)
   int split_act;                  // activation operand = bf16 head rows [0,R) + remainder rows [R,2R)
   int split_rows;                 // R
-  int fused_op;                   // fused plans (plan_gemm_fused): the epilogue op; splits = cluster size
+  int fused_op;                   // fused plans (plan_gemm_fused): the epilogue op; splits = group size
 };
 
 struct GemmOut {
