@@ -1,5 +1,7 @@
 """Denoising-step and decode-loop parity through the C-ABI against the oracle,
 plus the decode invariants, on the tiny and small decode workloads."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -217,6 +219,27 @@ def test_append_block_then_next_block_matches_oracle(cfg):
         while mask.max() and steps < (16 if cfg.name == "tiny" else 3):
             tok, mask, _, _ = compare_step(p, tok, mask, 0.8, logits=(steps == 0))
             steps += 1
+
+
+# --------------------------------------------------------- empty context
+
+@pytest.mark.parametrize("which", ["tiny", "small"])
+def test_step_with_empty_context(which, request):
+    """Context length 0: each query attends to the block keys alone (every
+    context split of the tcgen05 path, and the mma.sync path's context loop,
+    is empty)."""
+    import copy
+    p = request.getfixturevalue(which)
+    q = copy.copy(p)
+    q.model = dataclasses.replace(p.model, ctx_len=0)
+    p.dec.set_context_len(0)
+    try:
+        tok, mask = q.start_state()
+        compare_step(q, tok, mask, 0.8)
+        tok, mask = synth.make_tokens(q.cfg, seed=21, masked_frac=0.5)
+        compare_step(q, tok, mask, 0.8, logits=False)
+    finally:
+        p.dec.set_context_len(p.cfg.ctx_len)
 
 
 # ------------------------------------------- LM head over the compacted rows
