@@ -94,7 +94,8 @@ typedef struct dd_config {
                        * T + i (T = context length) and the pair (2j, 2j+1) of every query and
                        * key head turns by (T + i) * rope_theta^(-2j/D) radians; the context
                        * keys are taken as already positioned (the pages are silent on
-                       * positions; this is the survey's NEXT-4 option) */
+                       * positions; rotary positions are an optional alternative to the
+                       * learned in-block table alone) */
 } dd_config;
 
 /* Borrowed device pointers to bf16 weights (stacked over layers). */

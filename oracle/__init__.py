@@ -14,6 +14,10 @@ Parity status of each function:
 * attention, confidence/argmax, commit, RMSNorm, SwiGLU, full step:
   pinned by the tests under tests/ (double-precision brute force on tiny
   shapes, closed forms, invariants, exhaustive commit enumeration).
+* near-tie flags (which positions the parity tests may waive): pinned by
+  hand-derived cases in tests/golden/near_tie_cases.txt and by a soundness
+  property (perturbing logits and confidences within half the thresholds
+  changes the commit only at flagged positions).
 * The denoiser's weights are synthetic: end-to-end token ids have no
   published value to match, so beyond the pins above they are checked
   only for agreement between this oracle and the CUDA path.
@@ -33,6 +37,8 @@ from .decode import (  # noqa: F401
     linear,
     lm_head_select,
     near_tie_flags,
+    near_tie_positions,
+    top2_gap,
     rmsnorm,
     rope,
     round_bf16,

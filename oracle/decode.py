@@ -14,8 +14,7 @@ the passage it follows.  Sources:
   16, threshold gamma = 0.8 (higher gamma = more quality), the mock-AR mode
   that commits one token per step through the diffusion tower.
 
-Where the pages are silent the readings are fixed here (and listed in the
-design notes):
+Where the pages are silent the readings are fixed here:
 
 * denoiser = pre-norm dense transformer: RMSNorm -> GQA attention -> residual
   -> RMSNorm -> SwiGLU -> residual, L layers, final RMSNorm, untied LM head;
@@ -174,15 +173,74 @@ def lm_head_select(h: np.ndarray, w_lm: np.ndarray):
     return conf, arg, logits
 
 
+def top2_gap(logits: np.ndarray) -> np.ndarray:
+    """Per row: largest logit minus the second largest (0 on an exact tie)."""
+    top2 = -np.partition(-logits, 1, axis=1)[:, :2]
+    return (top2[:, 0] - top2[:, 1]).astype(np.float64)
+
+
 def near_tie_flags(logits: np.ndarray, conf: np.ndarray, gamma: float):
-    """Rows whose committed id or commit decision is fragile under rounding.
+    """Rows whose argmax or threshold decision is fragile under rounding.
 
     A row is flagged when its top-2 logit gap is below TIE_LOGIT_GAP or its
-    confidence lies within TIE_GAMMA_GAP of gamma.
+    confidence lies within TIE_GAMMA_GAP of gamma.  This is a per-row
+    statement over every row (masked or not); `near_tie_positions` gives the
+    per-position flags that decide which commits may differ.
     """
-    top2 = -np.partition(-logits, 1, axis=1)[:, :2]
-    gap = top2[:, 0] - top2[:, 1]
-    return (gap < TIE_LOGIT_GAP) | (np.abs(conf.astype(np.float64) - gamma) < TIE_GAMMA_GAP)
+    return (top2_gap(logits) < TIE_LOGIT_GAP) | (np.abs(conf.astype(np.float64) - gamma) < TIE_GAMMA_GAP)
+
+
+def near_tie_positions(logits, conf, mask, gamma: float, mode: int, block: int) -> np.ndarray:
+    """Masked positions whose commit outcome is fragile under rounding (the
+    parity bar's near-ties).  Returns bool [B, S]; committed positions are
+    never flagged (the commit rule cannot change them).
+
+    A masked position i of sequence b is flagged when
+      * its top-2 logit gap is below TIE_LOGIT_GAP (its argmax id may differ), in
+        every mode;
+      * threshold mode: its confidence is within TIE_GAMMA_GAP of gamma (the
+        ">= gamma" decision may differ);
+      * threshold mode, fallback (no masked confidence reaches gamma): the two
+        largest masked confidences are closer than TIE_CONF_GAP, and conf_i is
+        within TIE_CONF_GAP of the largest (the choice of the single most
+        confident position may differ);
+      * top-k and fixed-steps modes, with k positions to commit out of r > k
+        masked: the k-th and (k+1)-th largest masked confidences are closer than
+        TIE_CONF_GAP, and conf_i is within TIE_CONF_GAP of either (the cut may
+        differ).
+    Mock-AR commits the leftmost masked position whatever the confidences, so
+    only the logit-gap flag applies there.
+    """
+    conf = np.asarray(conf, np.float64).reshape(-1, block)
+    mask = np.asarray(mask, np.uint32)
+    B, S = conf.shape
+    gap = top2_gap(np.asarray(logits)).reshape(B, S)
+    base, param = mode & 0xFF, mode >> 8
+    flags = np.zeros((B, S), bool)
+    for b in range(B):
+        masked = [i for i in range(S) if (int(mask[b]) >> i) & 1]
+        for i in masked:
+            if gap[b, i] < TIE_LOGIT_GAP:
+                flags[b, i] = True
+        if not masked:
+            continue
+        c = sorted((conf[b, i] for i in masked), reverse=True)
+        if base == MODE_THRESHOLD:
+            for i in masked:
+                if abs(conf[b, i] - gamma) < TIE_GAMMA_GAP:
+                    flags[b, i] = True
+            fallback = not any(F32(conf[b, i]) >= F32(gamma) for i in masked)
+            if fallback and len(c) > 1 and c[0] - c[1] < TIE_CONF_GAP:
+                for i in masked:
+                    if c[0] - conf[b, i] < TIE_CONF_GAP:
+                        flags[b, i] = True
+        elif base in (MODE_TOPK, MODE_STEPS):
+            k = param if base == MODE_TOPK else steps_schedule_k(S, param, len(masked))
+            if 0 < k < len(c) and c[k - 1] - c[k] < TIE_CONF_GAP:
+                for i in masked:
+                    if min(abs(conf[b, i] - c[k - 1]), abs(conf[b, i] - c[k])) < TIE_CONF_GAP:
+                        flags[b, i] = True
+    return flags
 
 
 def commit(conf, arg, tokens, mask, gamma: float, mode: int, block: int):
@@ -264,7 +322,8 @@ class StepResult:
     conf: np.ndarray             # [B,S]
     arg: np.ndarray              # [B,S]
     logits: np.ndarray           # [B*S, V]
-    near_tie: np.ndarray         # [B,S] bool (position flags)
+    near_tie: np.ndarray         # [B,S] bool: masked positions whose commit may differ (near_tie_positions)
+    logit_tie: np.ndarray        # [B,S] bool: every row whose top-2 logit gap is below TIE_LOGIT_GAP
     fallback: np.ndarray         # [B] bool
     attn_out: list = field(default_factory=list)   # per layer [B*S, Hq*D]
     hidden_final: np.ndarray | None = None          # [B*S, H] final-norm output
@@ -296,7 +355,7 @@ def denoise_step(model: OracleModel, tokens, mask, gamma: float, mode: int = MOD
         q = (y @ w[f"wq{l}"].T).reshape(B, S, Hq, D)
         k = (y @ w[f"wk{l}"].T).reshape(B, S, Hkv, D)
         if getattr(cfg, "rope_theta", 0.0) > 0:
-            # block position i sits at T + i, after the context (NEXT-4 reading)
+            # block position i sits at T + i, right after the T context positions
             pos = T + np.arange(S)
             q = np.stack([rope(q[b], pos, cfg.rope_theta) for b in range(B)])
             k = np.stack([rope(k[b], pos, cfg.rope_theta) for b in range(B)])
@@ -318,30 +377,10 @@ def denoise_step(model: OracleModel, tokens, mask, gamma: float, mode: int = MOD
     conf = conf.reshape(B, S)
     arg = arg.reshape(B, S)
     new_tok, new_mask, n, fallback = commit(conf, arg, tokens, mask, gamma, mode, S)
-    tie = near_tie_flags(logits, conf.reshape(-1), gamma).reshape(B, S)
-    # In a fallback step the choice between two masked positions whose
-    # confidences nearly tie is fragile too: flag both.
-    for b in np.nonzero(fallback)[0]:
-        masked = [i for i in range(S) if (int(mask[b]) >> i) & 1]
-        c = sorted((float(conf[b, i]) for i in masked), reverse=True)
-        if len(c) > 1 and c[0] - c[1] < TIE_CONF_GAP:
-            for i in masked:
-                if c[0] - float(conf[b, i]) < TIE_CONF_GAP:
-                    tie[b, i] = True
-    # Top-k and fixed-steps: the cut between the k-th and (k+1)-th most
-    # confident masked positions is fragile when their confidences nearly tie.
-    base = mode & 0xFF
-    if base in (MODE_TOPK, MODE_STEPS):
-        for b in range(B):
-            masked = [i for i in range(S) if (int(mask[b]) >> i) & 1]
-            k = (mode >> 8) if base == MODE_TOPK else steps_schedule_k(S, mode >> 8, len(masked))
-            c = sorted((float(conf[b, i]) for i in masked), reverse=True)
-            if 0 < k < len(c) and c[k - 1] - c[k] < TIE_CONF_GAP:
-                for i in masked:
-                    if min(abs(float(conf[b, i]) - c[k - 1]), abs(float(conf[b, i]) - c[k])) < TIE_CONF_GAP:
-                        tie[b, i] = True
+    tie = near_tie_positions(logits, conf, mask, gamma, mode, S)
+    logit_tie = (top2_gap(logits) < TIE_LOGIT_GAP).reshape(B, S)
     return StepResult(new_tok, new_mask, n, conf, arg, logits if keep_intermediates else None,
-                      tie, fallback, attn_outs, hf if keep_intermediates else None)
+                      tie, logit_tie, fallback, attn_outs, hf if keep_intermediates else None)
 
 
 def append_block(model: OracleModel, tower: dict, tokens) -> OracleModel:

@@ -179,3 +179,40 @@ def commit_sets(conf_row, masked, gamma, mock_ar):
         return hit
     top = max(conf_row[i] for i in masked)
     return {min(i for i in masked if conf_row[i] == top)}
+
+
+def top2_gap(row):
+    """Largest value of a list minus the second largest (0 on an exact tie)."""
+    a = sorted(row, reverse=True)
+    return a[0] - a[1]
+
+
+def near_tie_positions(rows, conf, masked, gamma, kind, k=0):
+    """The near-tie positions of one sequence, stated as sets.
+
+    rows[i]: logit row of position i; conf[i]: its confidence; masked: the
+    masked positions; kind: "threshold", "mock_ar" or "cut" (top-k and
+    fixed steps, k = positions to commit).  A masked position is a near-tie
+    when its top-2 logit gap is below 1e-2; in threshold mode also when its
+    confidence is within 1e-3 of gamma, or, when no masked confidence reaches
+    gamma, when two masked confidences lie within 1e-3 of the largest one
+    and it is one of them; in the cut modes when the k-th and (k+1)-th
+    largest masked confidences are within 1e-3 and its confidence is within
+    1e-3 of either.
+    """
+    masked = sorted(set(masked))
+    out = {i for i in masked if top2_gap(rows[i]) < 1e-2}
+    if not masked:
+        return out
+    ranked = sorted((conf[i] for i in masked), reverse=True)
+    if kind == "threshold":
+        out |= {i for i in masked if abs(conf[i] - gamma) < 1e-3}
+        if all(conf[i] < gamma for i in masked):
+            near_top = {i for i in masked if ranked[0] - conf[i] < 1e-3}
+            if len(near_top) > 1:
+                out |= near_top
+    elif kind == "cut" and 0 < k < len(masked):
+        a, b = ranked[k - 1], ranked[k]
+        if a - b < 1e-3:
+            out |= {i for i in masked if abs(conf[i] - a) < 1e-3 or abs(conf[i] - b) < 1e-3}
+    return out

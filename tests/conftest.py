@@ -9,3 +9,9 @@ if ROOT not in sys.path:
 def pytest_configure(config):
     config.addinivalue_line("markers", "gpu: needs a B300 (sm_103a) and the built CUDA library")
     config.addinivalue_line("markers", "slow: CPU test that takes more than a few seconds")
+
+
+def pytest_terminal_summary(terminalreporter):
+    from tests import near_tie_log
+    for line in near_tie_log.summary_lines():
+        terminalreporter.write_line(line)

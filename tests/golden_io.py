@@ -45,3 +45,26 @@ def tiny_decode_cases():
             rec[key] = np.array([float(v) for v in vals], np.float32) if key == "first_conf" else \
                 np.array([int(v) for v in vals], np.int64)
         yield rec
+
+
+def near_tie_cases():
+    """Yield dicts: name, gamma, mode, mask, conf [16] fp32, gap [16], flagged
+    (list of positions); the logit row of position i is [0, -gap_i, -20, -20]."""
+    lines = [l.strip() for l in open(os.path.join(GOLDEN, "near_tie_cases.txt")) if l.strip() and not l.startswith("#")]
+    for i in range(0, len(lines), 4):
+        head, conf, gap, expect = (lines[i + j].split() for j in range(4))
+        assert head[0] == "case" and conf[0] == "conf" and gap[0] == "gap" and expect[0] == "expect"
+        h, e = _kv(head[2:]), _kv(expect[1:])
+        yield {"name": head[1], "gamma": float(h["gamma"]), "mode": mode_code(h["mode"]),
+               "mask": int(h["mask"], 16), "conf": np.array([float(v) for v in conf[1:]], np.float32),
+               "gap": np.array([float(v) for v in gap[1:]], np.float32),
+               "flagged": [] if e["flagged"] == "-" else [int(v) for v in e["flagged"].split(",")]}
+
+
+def near_tie_logits(gap):
+    """Logit rows [0, -gap_i, -20, -20] (fp32) whose top-2 gap is gap_i."""
+    g = np.asarray(gap, np.float32)
+    rows = np.full((g.size, 4), -20.0, np.float32)
+    rows[:, 0] = 0.0
+    rows[:, 1] = -g
+    return rows

@@ -2,11 +2,14 @@
 through the C-ABI, the expected values from `oracle`."""
 from __future__ import annotations
 
+import os
+
 import numpy as np
 import pytest
 
 import oracle
 import synth
+from tests import near_tie_log
 
 torch = pytest.importorskip("torch")
 
@@ -80,6 +83,44 @@ class Problem:
         return t, m
 
 
+def _masked_bits(mask, S):
+    return ((np.asarray(mask, np.uint32)[:, None] >> np.arange(S)) & 1).astype(bool)
+
+
+def check_commit(tok, mask, gamma, mode, S, r_tokens, r_mask, r_tie, g_tok, g_mask, g_n=None, r_n=None,
+                 g_conf=None, g_arg=None, what="step"):
+    """Token parity of one step taken by both sides from the same state
+    (tok [B,S], mask [B]):
+
+    * with the CUDA path's own confidences and ids (g_conf, g_arg, when
+      given), its new ids, mask and counts are exactly the commit rule
+      (`oracle.commit`) applied to them, in every sequence;
+    * every position where the CUDA path and the oracle differ (committed
+      id or mask bit) is a masked position the oracle flags as a near-tie;
+      the counts agree in every sequence with no flagged position.
+
+    Records and returns (flagged masked positions, masked positions)."""
+    g_tok = np.asarray(g_tok)
+    g_mask = np.asarray(g_mask, np.uint32)
+    if g_conf is not None:
+        e_tok, e_mask, e_n, _ = oracle.commit(np.asarray(g_conf, np.float32).reshape(-1, S),
+                                              np.asarray(g_arg, np.int32).reshape(-1, S), tok, mask, gamma, mode, S)
+        assert (g_mask == e_mask).all(), f"{what}: mask is not the commit rule on the CUDA path's own confidences"
+        assert (g_tok == e_tok).all(), f"{what}: ids are not the commit rule on the CUDA path's own confidences"
+        if g_n is not None:
+            assert (np.asarray(g_n) == e_n).all(), f"{what}: counts are not the commit rule's"
+    diff = (g_tok != r_tokens) | (_masked_bits(g_mask, S) != _masked_bits(r_mask, S))
+    bad = diff & ~r_tie
+    assert not bad.any(), f"{what}: CUDA path and oracle differ at non-tie positions {np.argwhere(bad)[:8].tolist()}"
+    if g_n is not None and r_n is not None:
+        clean = ~r_tie.any(axis=1)
+        assert (np.asarray(g_n)[clean] == np.asarray(r_n)[clean]).all(), f"{what}: commit counts differ"
+    masked = _masked_bits(mask, S)
+    flagged, compared = int((r_tie & masked).sum()), int(masked.sum())
+    near_tie_log.record(os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], flagged, compared)
+    return flagged, compared
+
+
 def compare_step(p: Problem, tok, mask, gamma, mode=0, logits=True):
     """Run one step on both sides from the same state; check every probe.
     Returns (gpu new tokens, gpu new mask, oracle result, near-tie count)."""
@@ -95,19 +136,13 @@ def compare_step(p: Problem, tok, mask, gamma, mode=0, logits=True):
     close(join_split(out["hidden"]).cpu().numpy(), r.hidden_final, TOL_LOGIT, "final hidden", rel_rms=1e-3)
     if logits:
         close(out["logits"].cpu().numpy(), r.logits, TOL_LOGIT, "logits")
-    close(out["conf"].cpu().numpy(), r.conf.reshape(-1), TOL_CONF, "confidence")
-    tie = r.near_tie.reshape(-1)
+    g_conf = out["conf"].cpu().numpy()
+    close(g_conf, r.conf.reshape(-1), TOL_CONF, "confidence")
     arg = out["arg"].cpu().numpy()
-    want = r.arg.reshape(-1)
-    mism = (arg != want) & ~tie
-    assert not mism.any(), f"argmax differs at non-tie rows {np.nonzero(mism)[0][:10]}"
+    mism = (arg != r.arg.reshape(-1)) & ~r.logit_tie.reshape(-1)
+    assert not mism.any(), f"argmax differs at rows {np.nonzero(mism)[0][:10]} whose top-2 logit gap is not a near-tie"
     g_tok = t.cpu().numpy()
     g_mask = m.cpu().numpy().view(np.uint32)
-    # committed sets and ids agree, except in sequences with a flagged position
-    for b in range(cfg.batch):
-        if tie[b * cfg.block:(b + 1) * cfg.block].any():
-            continue
-        assert g_mask[b] == r.mask[b], f"seq {b}: mask {g_mask[b]:#x} vs oracle {r.mask[b]:#x}"
-        assert (g_tok[b] == r.tokens[b]).all(), f"seq {b}: tokens differ"
-        assert out["n_committed"][b].item() == r.n_committed[b]
-    return g_tok, g_mask, r, int(tie.sum())
+    flagged, _ = check_commit(tok, mask, gamma, mode, cfg.block, r.tokens, r.mask, r.near_tie, g_tok, g_mask,
+                              out["n_committed"].cpu().numpy(), r.n_committed, g_conf, arg)
+    return g_tok, g_mask, r, flagged

@@ -6,7 +6,7 @@ import numpy as np
 import pytest
 
 import oracle
-from tests.golden_io import commit_cases, tiny_decode_cases
+from tests.golden_io import commit_cases, near_tie_cases, near_tie_logits, tiny_decode_cases
 from tests.golden.make_golden import decode, tiny_model
 
 
@@ -22,6 +22,15 @@ def test_commit_rule_cases(case):
     assert int(n[0]) == len(case["committed"])
     for i in range(S):
         assert tok[0, i] == (100 + i if i in case["committed"] else 7)
+
+
+@pytest.mark.parametrize("case", list(near_tie_cases()), ids=lambda c: c["name"])
+def test_near_tie_cases(case):
+    """The oracle's near-tie flags equal the hand-derived ones."""
+    S = 16
+    flags = oracle.near_tie_positions(near_tie_logits(case["gap"]), case["conf"].reshape(1, S),
+                                      np.array([case["mask"]], np.uint32), case["gamma"], case["mode"], S)
+    assert sorted(np.nonzero(flags[0])[0].tolist()) == case["flagged"]
 
 
 @pytest.fixture(scope="module")

@@ -48,7 +48,11 @@ def test_tiny_decode_against_fixture(tiny, case):
     tokens, steps = tiny.dec.decode_block(case["gamma"], case["mode"])
     torch.cuda.synchronize()
     got = tokens[0].cpu().numpy()
+    assert ((got >= 0) & (got < cfg.vocab)).all()
     if not (got == case["tokens"]).all():
+        # a free-running decode may leave the oracle's path only where that
+        # path crosses a near-tie; the step where it does is checked position
+        # by position in test_gpu_step.test_tiny_decode_block_matches_oracle
         assert case["trajectory_tie"], "decoded block differs from the oracle's with no near-tie on its path"
-        pytest.skip("the free-running decode left the oracle's path at a near-tie recorded in the fixture")
+        return
     assert steps == case["steps"]

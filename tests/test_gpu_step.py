@@ -7,7 +7,7 @@ import pytest
 
 import oracle
 import synth
-from tests.gpu_helpers import Problem, compare_step, require_gpu, torch
+from tests.gpu_helpers import Problem, check_commit, compare_step, require_gpu, torch
 
 pytestmark = pytest.mark.gpu
 
@@ -47,13 +47,40 @@ def test_tiny_state_synced_decode(tiny, gamma, mode):
 
 
 def test_tiny_decode_block_matches_oracle(tiny):
+    """The free-running decode (the device-side loop graph) against the
+    oracle's free-running decode.  Where the two trajectories part, the step
+    graph replays the CUDA trajectory one step at a time from the same start
+    (it must reproduce the loop's result) and the first step at which the two
+    states differ must differ only at positions the oracle flags there."""
+    cfg = tiny.cfg
     tokens, steps = tiny.dec.decode_block(0.8)
     torch.cuda.synchronize()
     want, w_steps, _ = oracle.decode_block(tiny.model, 0.8)
-    # free-running trajectories agree unless a near-tie sent them apart
-    if not (tokens.cpu().numpy() == want).all():
-        pytest.skip("free-running trajectories diverged at a near-tie (state-synced test covers parity)")
-    assert steps == w_steps
+    got = tokens.cpu().numpy()
+    if (got == want).all():
+        assert steps == w_steps
+        return
+    tok, mask = tiny.start_state()
+    for step in range(4 * cfg.block):
+        t, m = tiny.gpu_state(tok, mask)
+        tiny.dec.denoise_step(t, m, 0.8, 0)
+        torch.cuda.synchronize()
+        g_tok, g_mask = t.cpu().numpy(), m.cpu().numpy().view(np.uint32)
+        r = oracle.denoise_step(tiny.model, tok, mask, 0.8, 0)
+        if not ((g_tok == r.tokens).all() and (g_mask == r.mask).all()):
+            check_commit(tok, mask, 0.8, 0, cfg.block, r.tokens, r.mask, r.near_tie, g_tok, g_mask,
+                         what=f"first divergent step {step}")
+            assert r.near_tie.any()
+            break
+        tok, mask = g_tok, g_mask
+        assert mask.max(), "the trajectories agreed to the end but the final ids differ"
+    # the step-by-step CUDA trajectory reproduces the loop graph's result
+    while mask.max():
+        t, m = tiny.gpu_state(tok, mask)
+        tiny.dec.denoise_step(t, m, 0.8, 0)
+        torch.cuda.synchronize()
+        tok, mask = t.cpu().numpy(), m.cpu().numpy().view(np.uint32)
+    assert (tok == got).all()
 
 
 def test_small_first_step(small):
@@ -246,7 +273,7 @@ def test_step_with_empty_context(which, request):
 
 def _graph_step_vs_oracle(p, tok, mask, gamma=0.8):
     """One step through the step graph (LM head over the compacted masked rows)
-    against the oracle; sequences with a flagged near-tie are skipped."""
+    against the oracle: they may differ only at the oracle's near-ties."""
     cfg = p.cfg
     t, m = p.gpu_state(tok, mask)
     n = torch.empty(cfg.batch, dtype=torch.int32, device="cuda")
@@ -254,11 +281,8 @@ def _graph_step_vs_oracle(p, tok, mask, gamma=0.8):
     torch.cuda.synchronize()
     r = oracle.denoise_step(p.model, tok, mask, gamma, 0)
     g_tok, g_mask = t.cpu().numpy(), m.cpu().numpy().view(np.uint32)
-    S = cfg.block
-    for b in range(cfg.batch):
-        if r.near_tie[b].any():
-            continue
-        assert g_mask[b] == r.mask[b] and (g_tok[b] == r.tokens[b]).all() and int(n[b]) == r.n_committed[b], b
+    check_commit(tok, mask, gamma, 0, cfg.block, r.tokens, r.mask, r.near_tie, g_tok, g_mask, n.cpu().numpy(),
+                 r.n_committed, what="graph step")
 
 
 @pytest.mark.parametrize("masked_frac", [1.0, 0.6, 0.3, 0.05])

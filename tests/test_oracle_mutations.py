@@ -16,7 +16,7 @@ import oracle.decode as od
 import synth
 from tests import test_golden
 from tests import test_oracle_pins as pins
-from tests.golden_io import commit_cases
+from tests.golden_io import commit_cases, near_tie_cases
 
 # (function, [(old source text, new source text), ...])
 MUTANTS = {
@@ -58,6 +58,27 @@ MUTANTS = {
     "append_without_norm": ("append_block", [('y = rmsnorm(tower["ctx_embed"][ids].astype(F32), tower["ctx_g"], cfg.rms_eps)',
                                               'y = tower["ctx_embed"][ids].astype(F32)')]),
     "steps_schedule_off_by_one": ("steps_schedule_k", [("steps_left = n_steps - t\n", "steps_left = n_steps - t + 1\n")]),
+    # near-tie flags: thresholds, the pairs compared, the modes and positions they cover
+    "tie_logit_gap_doubled": ("near_tie_positions", [("if gap[b, i] < TIE_LOGIT_GAP:", "if gap[b, i] < 2 * TIE_LOGIT_GAP:")]),
+    "tie_gap_top1_minus_top3": ("top2_gap", [("-np.partition(-logits, 1, axis=1)[:, :2]",
+                                               "-np.partition(-logits, 2, axis=1)[:, [0, 2]]")]),
+    "tie_flags_every_masked": ("near_tie_positions", [("if gap[b, i] < TIE_LOGIT_GAP:", "if True:")]),
+    "tie_gamma_ignored": ("near_tie_positions", [("if abs(conf[b, i] - gamma) < TIE_GAMMA_GAP:", "if False:")]),
+    "tie_gamma_gap_tenfold": ("near_tie_positions", [("if abs(conf[b, i] - gamma) < TIE_GAMMA_GAP:",
+                                                      "if abs(conf[b, i] - gamma) < 10 * TIE_GAMMA_GAP:")]),
+    "tie_gamma_in_every_mode": ("near_tie_positions", [("if base == MODE_THRESHOLD:",
+                                                        "if base in (MODE_THRESHOLD, MODE_MOCK_AR, MODE_TOPK, MODE_STEPS):")]),
+    "tie_fallback_wrong_pair": ("near_tie_positions", [("c[0] - c[1] < TIE_CONF_GAP", "c[0] - c[min(2, len(c) - 1)] < TIE_CONF_GAP")]),
+    "tie_fallback_missing": ("near_tie_positions", [("if fallback and len(c) > 1", "if False and len(c) > 1")]),
+    "tie_fallback_without_fallback": ("near_tie_positions", [("if fallback and len(c) > 1", "if len(c) > 1")]),
+    "tie_ranks_committed_positions": ("near_tie_positions", [("c = sorted((conf[b, i] for i in masked), reverse=True)",
+                                                              "c = sorted((conf[b, i] for i in range(S)), reverse=True)")]),
+    "tie_cut_off_by_one": ("near_tie_positions", [("if 0 < k < len(c) and c[k - 1] - c[k] < TIE_CONF_GAP:",
+                                                   "if 0 < k < len(c) - 1 and c[k] - c[k + 1] < TIE_CONF_GAP:")]),
+    "tie_cut_missing": ("near_tie_positions", [("if 0 < k < len(c) and c[k - 1] - c[k] < TIE_CONF_GAP:", "if False:")]),
+    "tie_steps_wrong_k": ("near_tie_positions", [("else steps_schedule_k(S, param, len(masked))", "else param")]),
+    "tie_flags_committed_positions": ("near_tie_positions", [("masked = [i for i in range(S) if (int(mask[b]) >> i) & 1]",
+                                                              "masked = list(range(S))")]),
 }
 
 
@@ -97,6 +118,8 @@ def _pins(tiny):
         pins.test_commit_gamma_zero_and_above_one,
         pins.test_commit_monotone_in_gamma,
         _golden_commit_cases,
+        _golden_near_tie_cases,
+        *[lambda g=g, m=m: pins.test_near_tie_flags_are_sound(g, m) for g, m in pins.NEAR_TIE_MODES],
         lambda: pins.test_steps_schedule_fills_block_in_n_steps(16),
         pins.test_commit_topk_exhaustive_masks,
         lambda: pins.test_full_step_vs_bruteforce(False),
@@ -110,6 +133,11 @@ def _pins(tiny):
         pins.test_append_block_vs_bruteforce,
         lambda: pins.test_decode_after_append_sees_the_new_context(tiny),
     ]
+
+
+def _golden_near_tie_cases():
+    for case in near_tie_cases():
+        test_golden.test_near_tie_cases(case)
 
 
 def _golden_commit_cases():

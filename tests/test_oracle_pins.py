@@ -288,6 +288,79 @@ def test_commit_monotone_in_gamma():
         prev = done
 
 
+# ------------------------------------------------------------- near-ties
+
+NEAR_TIE_MODES = ([(0.8, oracle.MODE_THRESHOLD), (0.5, oracle.MODE_THRESHOLD), (0.8, oracle.MODE_MOCK_AR)]
+                  + [(0.8, oracle.with_param(oracle.MODE_TOPK, k)) for k in (1, 2, 3, 5)]
+                  + [(0.8, oracle.with_param(oracle.MODE_STEPS, n)) for n in (2, 4, 7)])
+
+
+def _near_tie_dense(seed, B=48, S=16, V=6, gamma=0.8):
+    """Logits, confidences and masks crowded with near-ties: a third of the
+    logit rows have a top-2 gap under 2e-2, and confidences cluster within
+    2e-3 of a few anchors (gamma among them)."""
+    rng = np.random.default_rng(seed)
+    logits = rng.normal(0, 1, (B * S, V)).astype(F32)
+    close_rows = rng.random(B * S) < 0.35
+    top = logits.argmax(axis=1)
+    second = (top + 1 + rng.integers(0, V - 1, B * S)) % V
+    gap = rng.uniform(0, 0.02, B * S).astype(F32)
+    logits[np.arange(B * S), second] = np.where(close_rows, logits[np.arange(B * S), top] - gap,
+                                                logits[np.arange(B * S), second])
+    anchors = np.array([gamma, 0.5, 0.62, 0.3, 0.95, 0.7], F32)
+    conf = (anchors[rng.integers(0, anchors.size, (B, S))] + rng.uniform(-2e-3, 2e-3, (B, S))).astype(F32)
+    mask = rng.integers(1, 1 << S, B).astype(np.uint32)
+    return logits, conf, mask
+
+
+@pytest.mark.parametrize("gamma,mode", NEAR_TIE_MODES)
+def test_near_tie_positions_vs_bruteforce(gamma, mode):
+    """The oracle's near-tie flags equal the set statement in tests/bruteforce.py."""
+    S = 16
+    logits, conf, mask = _near_tie_dense(11, gamma=gamma)
+    flags = oracle.near_tie_positions(logits, conf, mask, gamma, mode, S)
+    base, param = mode & 0xFF, mode >> 8
+    for b in range(mask.size):
+        masked = [i for i in range(S) if (int(mask[b]) >> i) & 1]
+        rows = [logits[b * S + i].astype(np.float64).tolist() for i in range(S)]
+        c = [float(v) for v in conf[b]]
+        if base == oracle.MODE_THRESHOLD:
+            want = bf.near_tie_positions(rows, c, masked, float(F32(gamma)), "threshold")
+        elif base == oracle.MODE_MOCK_AR:
+            want = bf.near_tie_positions(rows, c, masked, gamma, "mock_ar")
+        else:
+            k = param if base == oracle.MODE_TOPK else oracle.steps_schedule_k(S, param, len(masked))
+            want = bf.near_tie_positions(rows, c, masked, gamma, "cut", k)
+        assert set(np.nonzero(flags[b])[0].tolist()) == want, (b, hex(int(mask[b])))
+
+
+@pytest.mark.parametrize("gamma,mode", NEAR_TIE_MODES)
+def test_near_tie_flags_are_sound(gamma, mode):
+    """What the flags promise: perturbing every logit by less than half the
+    logit-gap bound and every confidence by less than half the confidence
+    bounds changes the committed ids and mask only at flagged positions."""
+    S = 16
+    logits, conf, mask = _near_tie_dense(12, gamma=gamma)
+    B = mask.size
+    flags = oracle.near_tie_positions(logits, conf, mask, gamma, mode, S)
+    tok0 = np.full((B, S), 1 << 20, np.int32)
+    arg = logits.argmax(axis=1).astype(np.int32).reshape(B, S)
+    t_ref, m_ref, _, _ = oracle.commit(conf, arg, tok0, mask, gamma, mode, S)
+    bits = (m_ref[:, None] >> np.arange(S)) & 1
+    rng = np.random.default_rng(13)
+    changed = 0
+    for _ in range(150):
+        lp = logits + rng.uniform(-4.9e-3, 4.9e-3, logits.shape).astype(F32)
+        cp = (conf + rng.uniform(-4.9e-4, 4.9e-4, conf.shape)).astype(F32)
+        ap = lp.argmax(axis=1).astype(np.int32).reshape(B, S)
+        t, m, _, _ = oracle.commit(cp, ap, tok0, mask, gamma, mode, S)
+        diff = (t != t_ref) | ((((m[:, None] >> np.arange(S)) & 1) != bits))
+        assert not (diff & ~flags).any(), np.argwhere(diff & ~flags)[:5]
+        changed += int(diff.any())
+    if mode & 0xFF != oracle.MODE_MOCK_AR:
+        assert changed > 0   # the data does sit on near-ties
+
+
 # ------------------------------------------------------- decode invariants
 
 @pytest.fixture(scope="module")
