@@ -12,10 +12,19 @@
 //
 // The array's name is only a host-side stand-in in host code, so the first
 // call on each device looks up its device address with
-// cudaGetSymbolAddress (with that device current) and caches it; that first
-// call should come before any stream capture.  Every call shares the array
+// cudaGetSymbolAddress (with that device current) and caches it.  With lazy
+// module loading (CUDA's default) that lookup is also what loads the module
+// and creates the array, so the first call may allocate and synchronise: it
+// is a warm-up, to be made before any stream capture and outside any region
+// that must not allocate.  The cached address is not refreshed, so a device
+// reset after the first call is not supported.  Every call shares the array
 // and it keeps the previous call's contents; calls that overlap on the GPU
 // (on different streams, or from different threads) race on it.
+//
+// A bounded wait inside the GEMM that expires sets the status word at the
+// start of the array; a last kernel reads it and, when it is set, overwrites
+// every output with conf = NaN and arg = -1, so an expired wait never leaves
+// plausible-looking results behind.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -60,6 +69,16 @@ dd_status scratch_address(void** out) {
   return DD_OK;
 }
 
+// Runs after the select: if the GEMM recorded an expired wait, no output of
+// this call is valid.
+__global__ void k_noalloc_status_outputs(const int* status, float* conf, int* arg, int rows) {
+  if (*status == 0) return;
+  for (int r = blockIdx.x * blockDim.x + threadIdx.x; r < rows; r += gridDim.x * blockDim.x) {
+    conf[r] = __int_as_float(0x7fc00000);
+    arg[r] = -1;
+  }
+}
+
 }  // namespace
 
 extern "C" dd_status dd_lmhead_select_noalloc(int32_t rows, int32_t hidden, int32_t vocab, const void* x,
@@ -72,7 +91,7 @@ extern "C" dd_status dd_lmhead_select_noalloc(int32_t rows, int32_t hidden, int3
   if (kStatusBytes + 3 * part > kScratchBytes)
     return error(DD_ERR_INVALID_ARG,
                  "dd_lmhead_select_noalloc: rows * (vocab / 256) exceeds the built-in scratch "
-                 "(8 MiB: at most about 699000 row-tiles)");
+                 "(8 MiB: rows * (vocab / 256) must be at most 698944)");
   void* scratch = nullptr;
   dd_status s = scratch_address(&scratch);
   if (s != DD_OK) return s;
@@ -84,7 +103,7 @@ extern "C" dd_status dd_lmhead_select_noalloc(int32_t rows, int32_t hidden, int3
   if (!dd::make_map_2d(&mx, x, rows, hidden, 128) || !dd::make_map_2d(&mw, w, vocab, hidden, p.BN))
     return error(DD_ERR_CUDA, "dd_lmhead_select_noalloc: tensor map encoding failed");
   unsigned char* base = static_cast<unsigned char*>(scratch);
-  // The status word is the only state read as "starts at zero"; the partials
+  // The status word is the only state that must start at zero; the partials
   // are fully overwritten by every call.
   if (cudaMemsetAsync(base, 0, kStatusBytes, st) != cudaSuccess)
     return error(DD_ERR_CUDA, "dd_lmhead_select_noalloc: clearing the status word failed");
@@ -93,8 +112,13 @@ extern "C" dd_status dd_lmhead_select_noalloc(int32_t rows, int32_t hidden, int3
   o.sel_m = reinterpret_cast<float*>(base + kStatusBytes);
   o.sel_s = reinterpret_cast<float*>(base + kStatusBytes + part);
   o.sel_a = reinterpret_cast<int*>(base + kStatusBytes + 2 * part);
+  const int* status = reinterpret_cast<const int*>(base);
   if (dd::launch_gemm(p, mx, mw, o, reinterpret_cast<int*>(base), dd::kDefaultTimeoutNs, st) != cudaSuccess ||
       dd::launch_select_combine(o.sel_m, o.sel_s, o.sel_a, p.n_tiles, rows, conf, arg, st) != cudaSuccess)
     return error(DD_ERR_CUDA, "dd_lmhead_select_noalloc: kernel launch failed");
+  const int threads = 256, blocks = (rows + threads - 1) / threads < 148 ? (rows + threads - 1) / threads : 148;
+  k_noalloc_status_outputs<<<blocks, threads, 0, st>>>(status, conf, arg, rows);
+  if (cudaGetLastError() != cudaSuccess)
+    return error(DD_ERR_CUDA, "dd_lmhead_select_noalloc: status kernel launch failed");
   return DD_OK;
 }
