@@ -23,6 +23,9 @@ Parity status of each function:
   only for agreement between this oracle and the CUDA path.
 """
 from .decode import (  # noqa: F401
+    TIE_CONF_GAP,
+    TIE_GAMMA_GAP,
+    TIE_LOGIT_GAP,
     MODE_MOCK_AR,
     MODE_STEPS,
     MODE_THRESHOLD,
@@ -39,6 +42,7 @@ from .decode import (  # noqa: F401
     near_tie_flags,
     near_tie_positions,
     top2_gap,
+    tower_causal_attention,
     rmsnorm,
     rope,
     round_bf16,

@@ -383,27 +383,61 @@ def denoise_step(model: OracleModel, tokens, mask, gamma: float, mode: int = MOD
                       tie, logit_tie, fallback, attn_outs, hf if keep_intermediates else None)
 
 
+def tower_causal_attention(q, k, v):
+    """Causal self-attention inside one committed block: position i attends to
+    positions j <= i, one softmax per (query position, head), scale 1/sqrt(D).
+
+    q, k, v [S, heads, D] fp32 -> [S, heads, D] fp32.
+    """
+    S, Hc, D = q.shape
+    scale = F32(1.0 / np.sqrt(D))
+    out = np.empty((S, Hc, D), F32)
+    for h in range(Hc):
+        s = (q[:, h, :] @ k[:, h, :].T) * scale                 # [S, S]
+        s = np.where(np.tril(np.ones((S, S), bool)), s, F32(-np.inf))
+        s = s - s.max(axis=1, keepdims=True)
+        p = np.exp(s)
+        p = p / p.sum(axis=1, keepdims=True, dtype=F32)
+        out[:, h, :] = p @ v[:, h, :]
+    return out
+
+
 def append_block(model: OracleModel, tower: dict, tokens) -> OracleModel:
     """The context tower's encoding of a committed block, appended to the
-    context (the TwoTower article's frozen causal tower; the survey's NEXT-2
-    reading: one position-wise dense layer, hence causal): per committed token
-    y = RMSNorm(E_ctx[token]) * g_ctx, then for every denoiser layer l the K and
-    V rows y W_kv[l]^T, stored in bf16 like the rest of the context at
-    positions [T, T + S).  Returns the model with the longer context.
+    context (TwoTower article, "技術/ビジネス面": a frozen causal tower encodes
+    the committed tokens and the denoiser cross-attends to its state).  The
+    trained tower is out of scope; its stand-in is one causal self-attention
+    layer over the committed block followed by the K/V projections:
 
-    tower: "ctx_embed" [V, H], "ctx_g" [H], "ctx_wkv" [L, 2*Hkv*D, H] (fp32
-    holding bf16 values).
+      e_i = E_ctx[t_i]                      y_i = RMSNorm(e_i) * g
+      q_i, k_i, v_i = y_i Wq^T, y_i Wk^T, y_i Wv^T      (Hkv heads of D)
+      a_i = causal attention of position i over positions j <= i of the block
+      h_i = e_i + a_i Wo^T                  z_i = RMSNorm(h_i) * g2
+      for every denoiser layer l: the K rows then the V rows z_i W_kv[l]^T,
+      stored in bf16 like the rest of the context at positions [T, T + S).
+
+    Position i of the appended block therefore depends on the committed
+    tokens at positions <= i only.  Returns the model with the longer context.
+
+    tower: "ctx_embed" [V, H], "ctx_g" [H], "ctx_wqkv" [3*Hkv*D, H] (q rows,
+    then k, then v), "ctx_wo" [H, Hkv*D], "ctx_g2" [H], "ctx_wkv" [L, 2*Hkv*D, H]
+    (fp32 holding bf16 values).
     """
     cfg = model.cfg
     B, S, L = cfg.batch, cfg.block, cfg.n_layers
     Hkv, D = cfg.n_kv_heads, cfg.head_dim
     T = model.ctx_len
     ids = np.asarray(tokens, np.int64).reshape(B * S)
-    y = rmsnorm(tower["ctx_embed"][ids].astype(F32), tower["ctx_g"], cfg.rms_eps)
+    e = tower["ctx_embed"][ids].astype(F32)                                 # [B*S, H]
+    y = rmsnorm(e, tower["ctx_g"], cfg.rms_eps)
+    qkv = linear(y, tower["ctx_wqkv"]).reshape(B, S, 3, Hkv, D)
+    a = np.stack([tower_causal_attention(qkv[b, :, 0], qkv[b, :, 1], qkv[b, :, 2]) for b in range(B)])
+    h = e + linear(a.reshape(B * S, Hkv * D), tower["ctx_wo"])
+    z = rmsnorm(h, tower["ctx_g2"], cfg.rms_eps)
     k_new = np.empty((L, B, Hkv, S, D), F32)
     v_new = np.empty((L, B, Hkv, S, D), F32)
     for l in range(L):
-        kv = round_bf16(y @ tower["ctx_wkv"][l].astype(F32).T)         # [B*S, 2*Hkv*D]
+        kv = round_bf16(z @ tower["ctx_wkv"][l].astype(F32).T)         # [B*S, 2*Hkv*D]
         k_new[l] = kv[:, :Hkv * D].reshape(B, S, Hkv, D).transpose(0, 2, 1, 3)
         v_new[l] = kv[:, Hkv * D:].reshape(B, S, Hkv, D).transpose(0, 2, 1, 3)
     k = np.concatenate([model.k_ctx[:, :, :, :T], k_new], axis=3)

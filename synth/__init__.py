@@ -174,23 +174,40 @@ def make_weights(cfg: Config, seed: int = 0) -> dict:
 
 
 def tower_names(cfg: Config):
-    """The synthetic context tower's tensors: its token embedding [V][H] and, per
-    denoiser layer, the K rows then the V rows it produces ([L][2*Hkv*D][H])."""
+    """The synthetic context tower's tensors: its token embedding [V][H], per
+    denoiser layer the K rows then the V rows it produces ([L][2*Hkv*D][H]),
+    and its causal self-attention layer: q|k|v projection [3*Hkv*D][H] and
+    output projection [H][Hkv*D] (drawn after the first two, so their draws
+    do not move)."""
+    kvd = cfg.n_kv_heads * cfg.head_dim
     return [("ctx_embed", (cfg.vocab, cfg.hidden)),
-            ("ctx_wkv", (cfg.n_layers, 2 * cfg.n_kv_heads * cfg.head_dim, cfg.hidden))]
+            ("ctx_wkv", (cfg.n_layers, 2 * kvd, cfg.hidden)),
+            ("ctx_wqkv", (3 * kvd, cfg.hidden)),
+            ("ctx_wo", (cfg.hidden, kvd))]
+
+
+def tower_std(cfg: Config, name: str) -> float:
+    """Embedding N(0, 0.02); q|k|v and K/V projections N(0, 1/H) so their
+    outputs are ~N(0, 1) (like the synthetic context); the attention output
+    projection N(0, 0.02^2 / (Hkv*D)), so its contribution is on the scale of
+    the embedding it is added to."""
+    if name == "ctx_embed":
+        return WEIGHT_STD
+    if name == "ctx_wo":
+        return WEIGHT_STD / np.sqrt(cfg.n_kv_heads * cfg.head_dim)
+    return 1.0 / np.sqrt(cfg.hidden)
 
 
 def make_tower_weights(cfg: Config, seed: int = 0) -> dict:
-    """Context-tower weights as bf16 bits: embedding N(0, 0.02), projections
-    N(0, 1/H) so the produced K/V are ~N(0,1) like the synthetic context;
-    gain "ctx_g" ones."""
+    """Context-tower weights as bf16 bits (scales in `tower_std`); gains
+    "ctx_g" and "ctx_g2" ones."""
     names = tower_names(cfg)
     streams = np.random.SeedSequence([seed, 0x544F57]).spawn(len(names))
     w = {}
     for (name, shape), ss in zip(names, streams):
-        std = WEIGHT_STD if name == "ctx_embed" else 1.0 / np.sqrt(cfg.hidden)
-        w[name] = _normal_bf16(np.random.default_rng(ss), shape, std)
+        w[name] = _normal_bf16(np.random.default_rng(ss), shape, tower_std(cfg, name))
     w["ctx_g"] = to_bf16_bits(np.ones(cfg.hidden, np.float32))
+    w["ctx_g2"] = to_bf16_bits(np.ones(cfg.hidden, np.float32))
     return w
 
 
@@ -286,10 +303,9 @@ def make_tower_weights_torch(cfg: Config, seed: int, device) -> dict:
     names, shapes and scales as `make_tower_weights`, different stream)."""
     import torch
     gen = torch_generator(seed * 7919 + 0x544F57, device)
-    w = {name: torch_normal_bf16(shape, WEIGHT_STD if name == "ctx_embed" else 1.0 / np.sqrt(cfg.hidden), gen,
-                                 device)
-         for name, shape in tower_names(cfg)}
+    w = {name: torch_normal_bf16(shape, tower_std(cfg, name), gen, device) for name, shape in tower_names(cfg)}
     w["ctx_g"] = torch.ones(cfg.hidden, dtype=torch.bfloat16, device=device)
+    w["ctx_g2"] = torch.ones(cfg.hidden, dtype=torch.bfloat16, device=device)
     return w
 
 

@@ -216,3 +216,29 @@ def near_tie_positions(rows, conf, masked, gamma, kind, k=0):
         if a - b < 1e-3:
             out |= {i for i in masked if abs(conf[i] - a) < 1e-3 or abs(conf[i] - b) < 1e-3}
     return out
+
+
+def tower_kv(tw, tokens, eps, n_layers, Hkv, D):
+    """The context tower's K/V for one committed block, pure Python:
+    returns kv[l][i] = the 2*Hkv*D bf16-rounded values (K rows, then V rows)
+    of position i for denoiser layer l.  One causal self-attention layer
+    (position i sees positions j <= i), residual, RMSNorm, then the per-layer
+    projections.  tw: nested lists with the names of the synthetic tower."""
+    S = len(tokens)
+    H = len(tw["ctx_g"])
+    es = [list(tw["ctx_embed"][t]) for t in tokens]
+    ys = [rmsnorm(e, tw["ctx_g"], eps) for e in es]
+    qkv = [matvec(tw["ctx_wqkv"], y) for y in ys]
+    W = Hkv * D
+    zs = []
+    for i in range(S):
+        a = []
+        for h in range(Hkv):
+            q = qkv[i][h * D:(h + 1) * D]
+            keys = [qkv[j][W + h * D:W + (h + 1) * D] for j in range(i + 1)]
+            vals = [qkv[j][2 * W + h * D:2 * W + (h + 1) * D] for j in range(i + 1)]
+            a += attention_one_query(q, keys, vals)
+        o = matvec(tw["ctx_wo"], a)
+        hrow = [es[i][c] + o[c] for c in range(H)]
+        zs.append(rmsnorm(hrow, tw["ctx_g2"], eps))
+    return [[[bf16(v) for v in matvec(tw["ctx_wkv"][l], zs[i])] for i in range(S)] for l in range(n_layers)]

@@ -55,8 +55,15 @@ MUTANTS = {
     "rope_wrong_frequency": ("rope", [("-2.0 * np.arange(D // 2, dtype=np.float64) / D", "-1.0 * np.arange(D // 2, dtype=np.float64) / D")]),
     "step_rope_keys_unrotated": ("denoise_step", [("k = np.stack([rope(k[b], pos, cfg.rope_theta) for b in range(B)])", "pass")]),
     "append_swaps_k_and_v": ("append_block", [("k_new[l] = kv[:, :Hkv * D]", "k_new[l] = kv[:, Hkv * D:]")]),
-    "append_without_norm": ("append_block", [('y = rmsnorm(tower["ctx_embed"][ids].astype(F32), tower["ctx_g"], cfg.rms_eps)',
-                                              'y = tower["ctx_embed"][ids].astype(F32)')]),
+    "append_without_norm": ("append_block", [('y = rmsnorm(e, tower["ctx_g"], cfg.rms_eps)', 'y = e')]),
+    "append_without_residual": ("append_block", [("h = e + linear(", "h = linear(")]),
+    "append_second_norm_uses_first_gain": ("append_block", [('tower["ctx_g2"]', 'tower["ctx_g"]')]),
+    "append_attends_without_positions_order": ("append_block", [
+        ("a = np.stack([tower_causal_attention(qkv[b, :, 0], qkv[b, :, 1], qkv[b, :, 2]) for b in range(B)])",
+         "a = np.stack([tower_causal_attention(qkv[b, :, 0], qkv[b, :, 2], qkv[b, :, 1]) for b in range(B)])")]),
+    "tower_attention_not_causal": ("tower_causal_attention", [("s = np.where(np.tril(np.ones((S, S), bool)), s, F32(-np.inf))", "pass")]),
+    "tower_attention_without_scale": ("tower_causal_attention", [(") * scale", ")")]),
+    "tower_attention_anticausal": ("tower_causal_attention", [("np.tril(np.ones((S, S), bool))", "np.triu(np.ones((S, S), bool))")]),
     "steps_schedule_off_by_one": ("steps_schedule_k", [("steps_left = n_steps - t\n", "steps_left = n_steps - t + 1\n")]),
     # near-tie flags: thresholds, the pairs compared, the modes and positions they cover
     "tie_logit_gap_doubled": ("near_tie_positions", [("if gap[b, i] < TIE_LOGIT_GAP:", "if gap[b, i] < 2 * TIE_LOGIT_GAP:")]),
@@ -131,6 +138,8 @@ def _pins(tiny):
         pins.test_rope_scores_depend_on_relative_position,
         pins.test_full_step_with_rope_vs_bruteforce,
         pins.test_append_block_vs_bruteforce,
+        pins.test_append_block_is_causal,
+        pins.test_tower_attention_closed_forms,
         lambda: pins.test_decode_after_append_sees_the_new_context(tiny),
     ]
 

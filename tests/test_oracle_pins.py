@@ -523,6 +523,8 @@ def test_append_block_vs_bruteforce():
     m = _micro_model(cfg)
     tw = _tower(cfg)
     rng = np.random.default_rng(14)
+    for g in ("ctx_g", "ctx_g2"):        # non-unit gains, so each norm's gain is checked
+        tw[g] = oracle.round_bf16(rng.normal(1.0, 0.3, cfg.hidden).astype(F32))
     tok = rng.integers(0, cfg.vocab, (cfg.batch, cfg.block)).astype(np.int32)
     tok[0, 1] = tok[0, 3]                                         # a repeated token
     m2 = oracle.append_block(m, tw, tok)
@@ -530,19 +532,54 @@ def test_append_block_vs_bruteforce():
     assert m2.ctx_len == T + S
     np.testing.assert_array_equal(m2.k_ctx[:, :, :, :T], m.k_ctx[:, :, :, :T])
     np.testing.assert_array_equal(m2.v_ctx[:, :, :, :T], m.v_ctx[:, :, :, :T])
-    g = tw["ctx_g"].tolist()
+    twl = {k: v.tolist() for k, v in tw.items()}
     for b in range(cfg.batch):
-        for i in range(S):
-            y = bf.rmsnorm(tw["ctx_embed"][tok[b, i]].tolist(), g, cfg.rms_eps)
-            for l in range(cfg.n_layers):
-                kv = [bf.bf16(v) for v in bf.matvec(tw["ctx_wkv"][l].tolist(), y)]
+        kv = bf.tower_kv(twl, tok[b].tolist(), cfg.rms_eps, cfg.n_layers, Hkv, D)
+        for l in range(cfg.n_layers):
+            for i in range(S):
                 for h in range(Hkv):
-                    want_k = np.array(kv[h * D:(h + 1) * D], F32)
-                    want_v = np.array(kv[Hkv * D + h * D:Hkv * D + (h + 1) * D], F32)
-                    ulp = np.abs(want_k) * 2.0 ** -7 + 1e-30
-                    assert (np.abs(m2.k_ctx[l, b, h, T + i] - want_k) <= ulp).all()
+                    want_k = np.array(kv[l][i][h * D:(h + 1) * D], F32)
+                    want_v = np.array(kv[l][i][Hkv * D + h * D:Hkv * D + (h + 1) * D], F32)
+                    # one bf16 rounding apart at most (fp32 vs double before the rounding)
+                    assert (np.abs(m2.k_ctx[l, b, h, T + i] - want_k) <= np.abs(want_k) * 2.0 ** -7 + 1e-30).all()
                     assert (np.abs(m2.v_ctx[l, b, h, T + i] - want_v) <= np.abs(want_v) * 2.0 ** -7 + 1e-30).all()
-    np.testing.assert_array_equal(m2.k_ctx[:, 0, :, T + 1], m2.k_ctx[:, 0, :, T + 3])   # position-wise layer
+    # the repeated token sits at positions 1 and 3 but sees different prefixes
+    assert not np.array_equal(m2.k_ctx[:, 0, :, T + 1], m2.k_ctx[:, 0, :, T + 3])
+
+
+def test_append_block_is_causal():
+    """Changing the committed token at position j changes the appended K/V of
+    positions j and after, and of no position before j."""
+    cfg = MICRO.replace(block=6, batch=1)
+    m = _micro_model(cfg)
+    tw = _tower(cfg)
+    rng = np.random.default_rng(15)
+    tok = rng.integers(0, cfg.vocab, (1, cfg.block)).astype(np.int32)
+    base = oracle.append_block(m, tw, tok)
+    T = m.ctx_len
+    for j in range(cfg.block):
+        t2 = tok.copy()
+        t2[0, j] = (t2[0, j] + 1 + j) % cfg.vocab
+        m2 = oracle.append_block(m, tw, t2)
+        for i in range(cfg.block):
+            same = (np.array_equal(m2.k_ctx[:, 0, :, T + i], base.k_ctx[:, 0, :, T + i]) and
+                    np.array_equal(m2.v_ctx[:, 0, :, T + i], base.v_ctx[:, 0, :, T + i]))
+            assert same == (i < j), (i, j)
+
+
+def test_tower_attention_closed_forms():
+    """Position 0 sees only itself (output = v_0); equal keys give the running
+    mean of the values."""
+    rng = np.random.default_rng(16)
+    q = rng.standard_normal((5, 2, 4)).astype(F32)
+    k = rng.standard_normal((5, 2, 4)).astype(F32)
+    v = rng.standard_normal((5, 2, 4)).astype(F32)
+    out = oracle.tower_causal_attention(q, k, v)
+    np.testing.assert_allclose(out[0], v[0], rtol=1e-6)
+    ke = np.broadcast_to(k[:1], k.shape).copy()
+    out = oracle.tower_causal_attention(q, ke, v)
+    for i in range(5):
+        np.testing.assert_allclose(out[i], v[:i + 1].mean(axis=0), rtol=1e-5, atol=1e-6)
 
 
 def test_decode_after_append_sees_the_new_context(tiny_model):
