@@ -49,7 +49,7 @@ class dd_weights(ctypes.Structure):
 
 
 class dd_context_tower(ctypes.Structure):
-    _fields_ = [("embed", c_void_p), ("g", c_void_p), ("wkv", c_void_p)]
+    _fields_ = [(n, c_void_p) for n in ("embed", "g", "wqkv", "wo", "g2", "wkv")]
 
 
 class dd_probe(ctypes.Structure):
@@ -108,6 +108,7 @@ _SIGS = {
 
 # dd_set_option / dd_get_option
 DD_OPT_FUSED_REDUCE = 1
+DD_OPT_COMPACT_SEQUENCES = 10
 DD_OPT_FUSED_SPLITS = {"qkv": 2, "o": 3, "gate_up": 4, "down": 5}
 DD_OPT_FUSED_GRID = {"qkv": 6, "o": 7, "gate_up": 8, "down": 9}
 
@@ -172,8 +173,8 @@ def dd_set_context_kv(ctx: int, k: int, v: int, t0: int, n: int, stream: int = 0
     _check(load().dd_set_context_kv(ctx, k, v, t0, n, stream))
 
 
-def dd_set_context_tower(ctx: int, embed: int, g: int, wkv: int):
-    t = dd_context_tower(embed, g, wkv)
+def dd_set_context_tower(ctx: int, embed: int, g: int, wqkv: int, wo: int, g2: int, wkv: int):
+    t = dd_context_tower(embed, g, wqkv, wo, g2, wkv)
     _check(load().dd_set_context_tower(ctx, ctypes.byref(t)))
 
 

@@ -95,6 +95,18 @@ bool make_map_q(CUtensorMap* m, const void* qkv, uint64_t rows, uint64_t ld, int
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool make_map_q_stacked(CUtensorMap* m, const void* qkv, uint64_t rows, uint64_t ld, int Hq, int D, int G, int S) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hq, 2, rows};
+  cuuint64_t strides[3] = {(cuuint64_t)D * 2, rows * ld * 2, ld * 2};
+  cuuint32_t box[4] = {64, (cuuint32_t)G, 2, (cuuint32_t)S};
+  cuuint32_t es[4] = {1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(qkv), dims, strides, box, es,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace dd
 
 // ---------------------------------------------------------------------------
@@ -103,10 +115,10 @@ bool make_map_q(CUtensorMap* m, const void* qkv, uint64_t rows, uint64_t ld, int
 
 struct Layout {
   size_t kc, vc, x, y, yc, row_index, qkv, attn, hmid, part, attn_part, sel_m, sel_s, sel_a, conf, arg, tok, mask,
-      ncommit, small, params, sq_a, sq_b, xpart, fcnt, total;
+      ncommit, small, params, sq_a, sq_b, xpart, fcnt, cmp, total;
   size_t part_elems;
   int alloc_ctx;
-  dd::GemmPlan p_qkv, p_o, p_gu, p_d, p_lm, p_store, p_tower;
+  dd::GemmPlan p_qkv, p_o, p_gu, p_d, p_lm, p_store, p_tower, p_tqkv, p_to;
   dd::AttnPlan p_attn;
 };
 
@@ -124,9 +136,14 @@ struct dd_ctx {
   // (groups of CTAs); fused_ok: planned for this shape.
   dd::GemmPlan f_qkv, f_o, f_gu, f_d;
   bool fused_ok, fused_on;
+  // Active-sequence compaction: each step runs only the rows of sequences
+  // that still have a masked position (not with the fused linear layers).
+  bool compact_on;
   dd_context_tower tower;  // borrowed; tower.wkv == nullptr until dd_set_context_tower
-  CUtensorMap m_tower;
+  CUtensorMap m_tower, m_tower_qkv, m_tower_o, m_tower_a;
   CUtensorMap m_lm, m_y_b, m_attn_b, m_h_b, m_y_a, m_yc_a, m_kc, m_vc, m_kc128, m_vc128, m_q;
+  CUtensorMap m_q2;  // stacked query map (head and remainder rows), when the stacked context kernel applies
+  bool have_q2;
   cudaStream_t cap_stream;
   cudaGraphExec_t exec;       // one denoising step
   cudaGraphExec_t loop_exec;  // while (masked left): step  -- the device-side decode loop
@@ -199,6 +216,9 @@ Layout make_layout(const dd_config& c) {
   L.p_store = dd::plan_gemm(dd::kEpiStore, R, c.vocab, c.hidden, 1);
   L.p_attn = dd::plan_attention(c.batch, c.block, c.n_q_heads, c.n_kv_heads, c.head_dim, c.max_ctx);
   L.p_tower = dd::plan_gemm(dd::kEpiPartial, R, c.n_layers * 2 * c.n_kv_heads * c.head_dim, c.hidden, 1);
+  // context tower's attention layer: q|k|v projection and output projection
+  L.p_tqkv = dd::plan_gemm(dd::kEpiPartial, R, 3 * c.n_kv_heads * c.head_dim, c.hidden, 1);
+  L.p_to = dd::plan_gemm(dd::kEpiPartial, R, c.hidden, c.n_kv_heads * c.head_dim, 1);
   size_t pe = 0;
   auto upd = [&](const dd::GemmPlan& p, int N) {
     size_t e = (size_t)p.splits * R * N;
@@ -209,6 +229,8 @@ Layout make_layout(const dd_config& c) {
   upd(L.p_gu, 2 * c.mlp);
   upd(L.p_d, c.hidden);
   upd(L.p_tower, c.n_layers * 2 * c.n_kv_heads * c.head_dim);
+  upd(L.p_tqkv, 3 * c.n_kv_heads * c.head_dim);
+  upd(L.p_to, c.hidden);
   L.part_elems = pe;
   size_t off = 0;
   auto take = [&](size_t bytes) {
@@ -251,11 +273,17 @@ Layout make_layout(const dd_config& c) {
   const bool fusable = R <= 128;
   L.xpart = take(fusable ? dd::fused_scratch_bytes(R) : 0);
   L.fcnt = take(fusable ? dd::fused_counter_bytes() : 0);
+  // active-sequence compaction record (written by the embedding kernel each step)
+  L.cmp = take((size_t)dd::cmp_words(c.batch, c.block) * 4);
   L.total = off;
   return L;
 }
 
 int32_t* small_ptr(dd_ctx* c) { return at<int32_t>(c->ws, c->L.small); }
+
+// The stacked form of the tcgen05 context-attention kernel (head and
+// remainder rows of one M = 128 operand) for split activations.
+constexpr bool kStackedContextKernel = false;
 
 // Kinds of launches in one step (for the per-kernel profile).
 enum LaunchKind : int {
@@ -295,6 +323,8 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
   const uint8_t* g_attn = static_cast<const uint8_t*>(c->w.g_attn);
   const uint8_t* g_mlp = static_cast<const uint8_t*>(c->w.g_mlp);
   const bool lm_compact = !probe && L.p_lm.m_tiles > 1;
+  // Active-sequence compaction record (nullptr: every sequence's rows run).
+  int* cmp = (c->compact_on && !c->fused_on) ? at<int>(ws, L.cmp) : nullptr;
   // Fused linear layers: the norms before attention and before the MLP are
   // deferred (y = x * g, sums of squares in sq_a / sq_b) and applied by the
   // consuming GEMM; the last layer's down projection keeps the separate
@@ -314,12 +344,13 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
   fo.cnt = at<unsigned>(ws, L.fcnt);
 
   DD_CUDA(dd::launch_embed_norm(at<int32_t>(ws, L.tok), at<uint32_t>(ws, L.mask), c->w.embed, c->w.pos, g_attn,
-                                x, y, cf.batch, cf.block, H, cf.vocab, cf.rms_eps, st, fz ? sq_a : nullptr));
+                                x, y, cf.batch, cf.block, H, cf.vocab, cf.rms_eps, st, fz ? sq_a : nullptr, cmp));
   mk(kKEmbed);
   for (int l = 0; l < cf.n_layers; ++l) {
     dd::GemmOut o{};
     o.partial = part;
     o.rows_valid = R;
+    o.rows_dev = cmp;  // active rows (cmp[0]); N tiles past them are skipped
     // q|k|v = y Wqkv^T
     if (fz) {
       fo.out = ws + L.qkv;
@@ -334,7 +365,7 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
       DD_CUDA(dd::launch_gemm(L.p_qkv, c->m_wqkv[l], c->m_y_b, o, status, c->timeout_ns, st));
       mk(kKGemmQkv);
       DD_CUDA(dd::launch_reduce_qkv(part, L.p_qkv.splits, o.split_stride, R, c->qkvw, ws + L.qkv, cf.block,
-                                    cf.head_dim, fo.qk_cols, small_ptr(c) + 2, cf.rope_theta, st));
+                                    cf.head_dim, fo.qk_cols, small_ptr(c) + 2, cf.rope_theta, st, cmp));
       mk(kKReduceQkv);
     }
     // block attention
@@ -358,7 +389,9 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
     a.scale_log2 = 1.4426950408889634f / sqrtf((float)cf.head_dim);
     a.status = status;
     a.timeout_ns = c->timeout_ns;
-    DD_CUDA(dd::launch_attention(L.p_attn, a, c->m_kc, c->m_vc, c->m_kc128, c->m_vc128, c->m_q, st));
+    a.cmp = cmp;
+    DD_CUDA(dd::launch_attention(L.p_attn, a, c->m_kc, c->m_vc, c->m_kc128, c->m_vc128, c->m_q, st,
+                                 c->have_q2 ? &c->m_q2 : nullptr));
     mk(kKAttention);
     if (L.p_attn.use_tc || L.p_attn.n_splits > 1) {
       DD_CUDA(dd::launch_attention_combine(L.p_attn, a, st));
@@ -389,14 +422,14 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
       DD_CUDA(dd::launch_gemm(L.p_o, c->m_wo[l], c->m_attn_b, o, status, c->timeout_ns, st));
       mk(kKGemmO);
       DD_CUDA(dd::launch_reduce_residual_norm(part, L.p_o.splits, o.split_stride, x, g_mlp + (size_t)l * H * 2, y, R,
-                                              H, cf.rms_eps, st));
+                                              H, cf.rms_eps, st, nullptr, cf.block, nullptr, nullptr, nullptr, cmp));
       mk(kKNormO);
       // h = silu(y Wg^T) * (y Wu^T)
       o.ld = 2 * F;
       o.split_stride = (long long)R * 2 * F;
       DD_CUDA(dd::launch_gemm(L.p_gu, c->m_wgu[l], c->m_y_b, o, status, c->timeout_ns, st));
       mk(kKGemmGu);
-      DD_CUDA(dd::launch_reduce_swiglu(part, L.p_gu.splits, o.split_stride, ws + L.hmid, R, F, st));
+      DD_CUDA(dd::launch_reduce_swiglu(part, L.p_gu.splits, o.split_stride, ws + L.hmid, R, F, st, cmp));
       mk(kKSwiglu);
     }
     const void* gn = (l + 1 < cf.n_layers) ? (const void*)(g_attn + (size_t)(l + 1) * H * 2) : c->w.g_final;
@@ -422,21 +455,23 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
     const bool compact = lm_compact && l + 1 == cf.n_layers;
     DD_CUDA(dd::launch_reduce_residual_norm(part, L.p_d.splits, o.split_stride, x, gn, y, R, H, cf.rms_eps, st,
                                             compact ? at<uint32_t>(ws, L.mask) : nullptr, cf.block, ws + L.yc,
-                                            at<int>(ws, L.row_index), small_ptr(c) + 6));
+                                            at<int>(ws, L.row_index), small_ptr(c) + 6, cmp));
     mk(kKNormDown);
   }
-  // LM head + fused select, over the compacted masked rows (all rows when not compacting)
+  // LM head + fused select, over the compacted masked rows (all rows when not
+  // compacting them; with active-sequence compaction those rows are in
+  // compacted order, and the select scatters them back to their own rows)
   dd::GemmOut so{};
   so.rows_valid = R;
   so.sel_m = at<float>(ws, L.sel_m);
   so.sel_s = at<float>(ws, L.sel_s);
   so.sel_a = at<int>(ws, L.sel_a);
-  so.rows_dev = lm_compact ? small_ptr(c) + 6 : nullptr;
+  so.rows_dev = lm_compact ? small_ptr(c) + 6 : cmp;
   DD_CUDA(dd::launch_gemm(L.p_lm, lm_compact ? c->m_yc_a : c->m_y_a, c->m_lm, so, status, c->timeout_ns, st));
   mk(kKLmSelect);
+  const int* sel_index = lm_compact ? at<int>(ws, L.row_index) : (cmp ? cmp + 2 + cf.batch : nullptr);
   DD_CUDA(dd::launch_select_combine(so.sel_m, so.sel_s, so.sel_a, L.p_lm.n_tiles, R, at<float>(ws, L.conf),
-                                    at<int>(ws, L.arg), st, so.rows_dev,
-                                    lm_compact ? at<int>(ws, L.row_index) : nullptr));
+                                    at<int>(ws, L.arg), st, so.rows_dev, sel_index));
   mk(kKSelectCombine);
   if (probe) {
     if (probe->hidden)
@@ -604,6 +639,15 @@ dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_byte
     dd_destroy(c);
     return fail(DD_ERR_CUDA, "tensor map encoding failed for the workspace buffers");
   }
+  // stacked query rows for the tcgen05 context kernel (head and remainder as
+  // two rows of one M = 128 operand)
+  if (kStackedContextKernel && L.p_attn.use_tc && dd::attention_tc_stacked_supported(c->G, cf.block)) {
+    if (!dd::make_map_q_stacked(&c->m_q2, c->ws + L.qkv, c->R, c->qkvw, cf.n_q_heads, cf.head_dim, c->G, cf.block)) {
+      dd_destroy(c);
+      return fail(DD_ERR_CUDA, "tensor map encoding failed for the stacked query rows");
+    }
+    c->have_q2 = true;
+  }
   // Fused linear layers (at most 128 activation rows, which the activation
   // maps above then hold in one box).
   if (c->R <= 128) {
@@ -617,6 +661,7 @@ dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_byte
   // Measured on the small decode workload the fused layers lose to the
   // separate reduce kernels inside the step graph, so they are opt-in.
   c->fused_on = false;
+  c->compact_on = true;
   *out = c;
   return DD_OK;
 }
@@ -687,14 +732,20 @@ dd_status dd_set_context_kv(dd_ctx* c, const void* k, const void* v, int32_t t0,
 
 dd_status dd_set_context_tower(dd_ctx* c, const dd_context_tower* t) {
   if (!c) return fail(DD_ERR_INVALID_ARG, "ctx is NULL");
-  if (!t || !t->embed || !t->g || !t->wkv) return fail(DD_ERR_INVALID_ARG, "context tower weights are NULL");
+  if (!t || !t->embed || !t->g || !t->wqkv || !t->wo || !t->g2 || !t->wkv)
+    return fail(DD_ERR_INVALID_ARG, "context tower weights are NULL");
   const dd_config& cf = c->cfg;
-  for (const void* ptr : {t->embed, t->g, t->wkv})
+  for (const void* ptr : {t->embed, t->g, t->wqkv, t->wo, t->g2, t->wkv})
     if (reinterpret_cast<uintptr_t>(ptr) % 16) return fail(DD_ERR_INVALID_ARG, "context tower weights must be 16-byte aligned");
   if (!encode_fn()) return fail(DD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
-  const uint64_t n = (uint64_t)cf.n_layers * 2 * cf.n_kv_heads * cf.head_dim;
-  if (n % 128) return fail(DD_ERR_UNSUPPORTED, "n_layers*2*n_kv_heads*head_dim must be a multiple of 128");
-  if (!dd::make_map_2d(&c->m_tower, t->wkv, n, cf.hidden, 128))
+  const uint64_t W = (uint64_t)cf.n_kv_heads * cf.head_dim;
+  const uint64_t n = (uint64_t)cf.n_layers * 2 * W;
+  if (n % 128 || (3 * W) % 128)
+    return fail(DD_ERR_UNSUPPORTED, "n_layers*2*n_kv_heads*head_dim and 3*n_kv_heads*head_dim must be multiples of 128");
+  if (!dd::make_map_2d(&c->m_tower, t->wkv, n, cf.hidden, 128) ||
+      !dd::make_map_2d(&c->m_tower_qkv, t->wqkv, 3 * W, cf.hidden, 128) ||
+      !dd::make_map_2d(&c->m_tower_o, t->wo, cf.hidden, W, 128) ||
+      !dd::make_map_2d(&c->m_tower_a, c->ws + c->L.attn, 2 * c->R, W, c->L.p_to.BN))
     return fail(DD_ERR_CUDA, "tensor map encoding failed for the context tower");
   c->tower = *t;
   return DD_OK;
@@ -712,15 +763,33 @@ dd_status dd_append_block(dd_ctx* c, const int32_t* tokens, void* stream) {
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   uint8_t* ws = c->ws;
   const Layout& L = c->L;
-  const int R = c->R, N = cf.n_layers * 2 * cf.n_kv_heads * cf.head_dim;
+  const int R = c->R, H = cf.hidden, W = cf.n_kv_heads * cf.head_dim, N = cf.n_layers * 2 * W;
   int* small = small_ptr(c);
-  DD_CUDA(dd::launch_tower_embed_norm(tokens, c->tower.embed, c->tower.g, ws + L.y, R, cf.hidden, cf.vocab,
-                                      cf.rms_eps, st));
+  float* x = at<float>(ws, L.x);
+  float* part = at<float>(ws, L.part);
+  // e = E_ctx[token] (x), y = RMSNorm(e) g
+  DD_CUDA(dd::launch_tower_embed_norm(tokens, c->tower.embed, c->tower.g, x, ws + L.y, R, H, cf.vocab, cf.rms_eps,
+                                      st));
+  // q|k|v = y Wqkv^T (fp32, in the q|k|v activation buffer, which is large enough)
   dd::GemmOut o{};
-  o.partial = at<float>(ws, L.part);
-  o.split_stride = (long long)R * N;
-  o.ld = N;
+  o.partial = part;
   o.rows_valid = R;
+  o.ld = 3 * W;
+  o.split_stride = (long long)R * 3 * W;
+  float* tqkv = at<float>(ws, L.qkv);
+  DD_CUDA(dd::launch_gemm(L.p_tqkv, c->m_tower_qkv, c->m_y_b, o, small + 1, c->timeout_ns, st));
+  DD_CUDA(dd::launch_reduce_f32(part, L.p_tqkv.splits, o.split_stride, R, 3 * W, tqkv, st));
+  // causal self-attention over each committed block -> a (head + remainder)
+  DD_CUDA(dd::launch_tower_attention(tqkv, ws + L.attn, R, cf.block, cf.n_kv_heads, cf.head_dim, st));
+  // x = e + a Wo^T ; y = RMSNorm(x) g2
+  o.ld = H;
+  o.split_stride = (long long)R * H;
+  DD_CUDA(dd::launch_gemm(L.p_to, c->m_tower_o, c->m_tower_a, o, small + 1, c->timeout_ns, st));
+  DD_CUDA(dd::launch_reduce_residual_norm(part, L.p_to.splits, o.split_stride, x, c->tower.g2, ws + L.y, R, H,
+                                          cf.rms_eps, st));
+  // K/V of every denoiser layer = y W_kv^T, appended at positions [T, T + S)
+  o.ld = N;
+  o.split_stride = (long long)R * N;
   DD_CUDA(dd::launch_gemm(L.p_tower, c->m_tower, c->m_y_b, o, small + 1, c->timeout_ns, st));
   DD_CUDA(dd::launch_reduce_kv_append(o.partial, L.p_tower.splits, o.split_stride, R, N, cf.block, cf.batch,
                                       cf.n_kv_heads, cf.head_dim, L.alloc_ctx, small + 2,
@@ -848,11 +917,13 @@ dd_status dd_step_launch_count(dd_ctx* c, int32_t* n) {
 
 dd_status dd_set_option(dd_ctx* c, int32_t option, int32_t value) {
   if (!c) return fail(DD_ERR_INVALID_ARG, "ctx is NULL");
-  if (option != DD_OPT_FUSED_REDUCE) return fail(DD_ERR_INVALID_ARG, "option %d cannot be set", option);
-  if (value != 0 && value != 1) return fail(DD_ERR_INVALID_ARG, "DD_OPT_FUSED_REDUCE takes 0 or 1 (got %d)", value);
-  if (value && !c->fused_ok)
+  if (option != DD_OPT_FUSED_REDUCE && option != DD_OPT_COMPACT_SEQUENCES)
+    return fail(DD_ERR_INVALID_ARG, "option %d cannot be set", option);
+  if (value != 0 && value != 1) return fail(DD_ERR_INVALID_ARG, "option %d takes 0 or 1 (got %d)", option, value);
+  if (option == DD_OPT_FUSED_REDUCE && value && !c->fused_ok)
     return fail(DD_ERR_UNSUPPORTED, "the fused linear layers are not available for this shape or device");
-  if ((value != 0) != c->fused_on) {
+  bool& flag = option == DD_OPT_FUSED_REDUCE ? c->fused_on : c->compact_on;
+  if ((value != 0) != flag) {
     // the captured graphs hold the other path
     DD_CUDA(cudaDeviceSynchronize());
     if (c->exec) cudaGraphExecDestroy(c->exec);
@@ -860,7 +931,7 @@ dd_status dd_set_option(dd_ctx* c, int32_t option, int32_t value) {
     c->exec = nullptr;
     c->loop_exec = nullptr;
     c->loop_tried = false;
-    c->fused_on = value != 0;
+    flag = value != 0;
   }
   return DD_OK;
 }
@@ -871,6 +942,7 @@ dd_status dd_get_option(dd_ctx* c, int32_t option, int32_t* value) {
   const dd::GemmPlan* fp[] = {&c->f_qkv, &c->f_o, &c->f_gu, &c->f_d};
   switch (option) {
     case DD_OPT_FUSED_REDUCE: *value = c->fused_on ? 1 : 0; return DD_OK;
+    case DD_OPT_COMPACT_SEQUENCES: *value = c->compact_on ? 1 : 0; return DD_OK;
     case DD_OPT_FUSED_SPLITS_QKV:
     case DD_OPT_FUSED_SPLITS_O:
     case DD_OPT_FUSED_SPLITS_GATE_UP:

@@ -173,16 +173,17 @@ __global__ void __launch_bounds__((MAXW + 1) * 32, 1) k_block_attn(const __grid_
   uint64_t* empty = full + STAGES;
   volatile int* abort_flag = reinterpret_cast<volatile int*>(empty + STAGES);
 
-  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;
+  const int split = blockIdx.x, kvh = blockIdx.y, b = blockIdx.z;  // b: compacted sequence
   const int warp = warp_id(), lane = lane_id();
   pdl_wait();  // q|k|v come from the preceding kernel
   pdl_launch_dependents();
+  if (a.cmp && b >= a.cmp[1]) return;  // not an active sequence
   const int T = *a.ctx_len;
   const int ntiles = (T + kKT - 1) / kKT;
   const int per = (ntiles + n_splits - 1) / n_splits;
   const int tile0 = split * per;
   const int tile1 = min(ntiles, tile0 + per);
-  const int z = a.z0 + b * a.Hkv + kvh;
+  const int z = a.z0 + (a.cmp ? a.cmp[2 + b] : b) * a.Hkv + kvh;
   const int R = a.B * a.S;
   const __nv_bfloat16* qkv = reinterpret_cast<const __nv_bfloat16*>(a.qkv);
 
@@ -354,6 +355,7 @@ __global__ void k_attn_combine(const AttnArgs a, int n_splits) {
   const int r = (int)(gw % rows);
   const long long bk = gw / rows;  // b * Hkv + kvh
   const int kvh = (int)(bk % a.Hkv), b = (int)(bk / a.Hkv);
+  if (a.cmp && b >= a.cmp[1]) return;  // not an active sequence
   float M = -INFINITY;
   for (int s = 0; s < n_splits; ++s) M = fmaxf(M, a.part_ml[(bk * n_splits + s) * rows + r].x);
   float L = 0.f;
@@ -396,6 +398,7 @@ __global__ void __launch_bounds__(128) k_attn_merge_block(const AttnArgs a, int 
   pdl_wait();  // q|k|v and the context partials come from the preceding kernels
   pdl_launch_dependents();
   const int kvh = blockIdx.x % a.Hkv, b = blockIdx.x / a.Hkv;
+  if (a.cmp && b >= a.cmp[1]) return;  // not an active sequence
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows = a.G * a.S;
   const int R = a.B * a.S;
@@ -539,6 +542,7 @@ __global__ void __launch_bounds__(256) k_attn_merge_rows(const AttnArgs a, int n
   const int r0 = (blockIdx.x % ctas_per_bk) * 8;
   const int nq = min(8, rows - r0);
   const int kvh = bk % a.Hkv, b = bk / a.Hkv;
+  if (a.cmp && b >= a.cmp[1]) return;  // not an active sequence
   const long long R = (long long)a.B * S;
   const long long lo = a.split ? R * a.ld_qkv : 0;
   const __nv_bfloat16* qkv = reinterpret_cast<const __nv_bfloat16*>(a.qkv);
@@ -737,10 +741,10 @@ size_t attention_partial_bytes(const AttnPlan& p, int B, int Hkv) {
 
 cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a_in, const CUtensorMap& map_k, const CUtensorMap& map_v,
                              const CUtensorMap& map_k128, const CUtensorMap& map_v128, const CUtensorMap& map_q,
-                             cudaStream_t st) {
+                             cudaStream_t st, const CUtensorMap* map_q2) {
   AttnArgs a = a_in;
   // tcgen05 path: context splits only; the block keys join in the merge
-  if (p.use_tc) return launch_attention_tc(a, p.n_ctx, map_k128, map_v128, map_q, st);
+  if (p.use_tc) return launch_attention_tc(a, p.n_ctx, map_k128, map_v128, map_q, st, map_q2);
   if (p.D == 128) {
     if (a.split) launch_attn_kernel<128, true>(p, a, p.n_splits, map_k, map_v, st);
     else launch_attn_kernel<128, false>(p, a, p.n_splits, map_k, map_v, st);

@@ -111,7 +111,7 @@ __device__ __forceinline__ float ex2(float x) {
 template <bool SPLITQ>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_ctx_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                  const __grid_constant__ CUtensorMap map_q, const AttnArgs a, int n_ctx, int n_items) {
+                  const __grid_constant__ CUtensorMap map_q, const AttnArgs a, int n_ctx, int n_items_max) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -133,10 +133,14 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   const int warp = warp_id(), lane = lane_id();
   const int T = *a.ctx_len;
+  // With active-sequence compaction the pairs are those of the active
+  // sequences; the record was written by the step's first kernel, at least
+  // three launches upstream, so it is complete before this kernel starts.
+  const int n_items = a.cmp ? a.cmp[1] * a.Hkv * n_ctx : n_items_max;
   const int ntiles_all = (T + kKT - 1) / kKT;
   const int per = (ntiles_all + n_ctx - 1) / n_ctx;
   const int R = a.B * a.S;
-  // item w -> (split, kv head, sequence, first tile, tile count)
+  // item w -> (split, kv head, sequence (compacted), first tile, tile count)
   auto item = [&](int w, int& split, int& kvh, int& b, int& tile0, int& nt) {
     split = w % n_ctx;
     const int pair = w / n_ctx;
@@ -197,12 +201,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       // The context K/V do not depend on the preceding kernel: the first
       // item's first two tiles go out before waiting for it (programmatic
       // dependent launch); q does, so its load waits.
+      // the context cache plane of (compacted sequence b, kv head)
+      auto plane = [&](int b, int kvh) { return a.z0 + (a.cmp ? a.cmp[2 + b] : b) * a.Hkv + kvh; };
       int split, kvh, b, tile0, nt;
       int pre = 0;
       bool ok = true;
       if ((int)blockIdx.x < n_items) {
         item(blockIdx.x, split, kvh, b, tile0, nt);
-        for (; pre < min(nt, 2) && ok; ++pre) ok = load_kv(pre, (tile0 + pre) * kKT, a.z0 + b * a.Hkv + kvh);
+        const int z = plane(b, kvh);
+        for (; pre < min(nt, 2) && ok; ++pre) ok = load_kv(pre, (tile0 + pre) * kKT, z);
       }
       pdl_wait();
       pdl_launch_dependents();
@@ -219,8 +226,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           tma_load_3d(q + kQ, &map_q, &qfull[qb], 0, kvh * a.G, R + b * a.S);
           tma_load_3d(q + kQ + kRowBox, &map_q, &qfull[qb], 64, kvh * a.G, R + b * a.S);
         }
+        const int z = plane(b, kvh);
         for (int t = 0; t < nt && ok; ++t, ++g)
-          if (g >= pre) ok = load_kv(g, (tile0 + t) * kKT, a.z0 + b * a.Hkv + kvh);
+          if (g >= pre) ok = load_kv(g, (tile0 + t) * kKT, z);
       }
     }
     __syncwarp();
@@ -438,6 +446,326 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
+// Stacked form, for split activations (q as a bf16 head plus a bf16
+// remainder).  An M = 64 MMA occupies the tensor core as long as an M = 128
+// one, so instead of two M = 64 products per step (head and remainder) the
+// head and the remainder of every query row are two rows of one M = 128
+// operand, and their two product rows are added afterwards:
+//   S'[128][128 keys] = Q'[128][128] . K_tile^T   rows rho = i*2G + part*G + g
+//   O'[128][128 d]    = P'[128][128 keys] . V_tile rows as in S'
+// where part 0 holds the head and part 1 the remainder of query (i, g), and
+// P' row (i, 0, g) is the bf16 head and row (i, 1, g) the bf16 remainder of
+// that query's probabilities.  Q' comes from the q|k|v rows by one 4D TMA
+// box {64 dims, G heads, 2 parts, S positions} (the part dimension strides
+// from the head rows to the remainder rows).  With the 32x32b TMEM load,
+// thread rho holds row rho; the rows of one query sit G lanes apart in the
+// same warp, so one shuffle per value adds them: the part-0 thread keeps
+// the sum for keys (or dims) 0..63 and the part-1 thread for 64..127, and
+// the two carry the same running max and sum.  Per 128-key tile this is 16
+// MMAs instead of 32.
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+    k_attn_ctx_stk(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
+                   const __grid_constant__ CUtensorMap map_q2, const AttnArgs a, int n_ctx, int n_items_max) {
+  static_assert(G >= 1 && G <= 16 && (G & (G - 1)) == 0, "G must be a power of two <= 16");
+  constexpr int kAtom = 128 * 128;  // [128 rows][64 cols] bf16, 128-byte swizzle: 16 KB
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
+  uint64_t* kfull = bars + 0;
+  uint64_t* kempty = bars + 2;
+  uint64_t* vfull = bars + 4;
+  uint64_t* vempty = bars + 6;
+  uint64_t* sfull = bars + 8;
+  uint64_t* sfree = bars + 10;
+  uint64_t* pfull = bars + 12;
+  uint64_t* pfree = bars + 13;
+  uint64_t* ofull = bars + 14;
+  uint64_t* ofree = bars + 16;
+  uint64_t* drain = bars + 18;
+  uint64_t* qfull = bars + 19;
+  uint64_t* qempty = bars + 21;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + kNumBars);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = warp_id(), lane = lane_id();
+  const int S = a.S;  // S * G == 64
+  const int T = *a.ctx_len;
+  // the active sequences' record is written by the step's first kernel, at
+  // least three launches upstream, so it is complete before this kernel starts
+  const int n_items = a.cmp ? a.cmp[1] * a.Hkv * n_ctx : n_items_max;
+  const int ntiles_all = (T + kKT - 1) / kKT;
+  const int per = (ntiles_all + n_ctx - 1) / n_ctx;
+  auto item = [&](int w, int& split, int& kvh, int& b, int& tile0, int& nt) {
+    split = w % n_ctx;
+    const int pair = w / n_ctx;
+    kvh = pair % a.Hkv;
+    b = pair / a.Hkv;
+    tile0 = split * per;
+    nt = max(0, min(ntiles_all, tile0 + per) - tile0);
+  };
+
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kfull[i], 1);
+      mbar_init(&kempty[i], 1);
+      mbar_init(&vfull[i], 1);
+      mbar_init(&vempty[i], 1);
+      mbar_init(&sfull[i], 1);
+      mbar_init(&sfree[i], 4);
+      mbar_init(&ofull[i], 1);
+      mbar_init(&ofree[i], 4);
+      mbar_init(&qfull[i], 1);
+      mbar_init(&qempty[i], 1);
+    }
+    mbar_init(pfull, 4);
+    mbar_init(pfree, 1);
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    tma_prefetch_desc(&map_k);
+    tma_prefetch_desc(&map_v);
+    tma_prefetch_desc(&map_q2);
+  }
+  if (warp == 1) {
+    tmem_alloc(tmem_slot, kTmemCols);
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t t_s = tmem;        // S' buffers at columns 0 and 128
+  const uint32_t t_o = tmem + 256;  // O' buffers at columns 256 and 384
+
+  if (warp == 0) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      auto load_kv = [&](int g, int key0, int z) {
+        const int s = g & 1;
+        const uint32_t ph = (g >> 1) & 1;
+        if (!mbar_wait_bounded(&kempty[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) return false;
+        mbar_arrive_expect_tx(&kfull[s], kKV);
+        tma_load_3d(smem + kOffK + s * kKV, &map_k, &kfull[s], 0, key0, z);
+        tma_load_3d(smem + kOffK + s * kKV + kBox, &map_k, &kfull[s], 64, key0, z);
+        if (!mbar_wait_bounded(&vempty[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) return false;
+        mbar_arrive_expect_tx(&vfull[s], kKV);
+        tma_load_3d(smem + kOffV + s * kKV, &map_v, &vfull[s], 0, key0, z);
+        tma_load_3d(smem + kOffV + s * kKV + kBox, &map_v, &vfull[s], 64, key0, z);
+        return true;
+      };
+      auto plane = [&](int b, int kvh) { return a.z0 + (a.cmp ? a.cmp[2 + b] : b) * a.Hkv + kvh; };
+      int split, kvh, b, tile0, nt;
+      int pre = 0;
+      bool ok = true;
+      // context K/V do not depend on the preceding kernel: the first item's
+      // first two tiles go out before waiting for it; q does, so it waits
+      if ((int)blockIdx.x < n_items) {
+        item(blockIdx.x, split, kvh, b, tile0, nt);
+        const int z = plane(b, kvh);
+        for (; pre < min(nt, 2) && ok; ++pre) ok = load_kv(pre, (tile0 + pre) * kKT, z);
+      }
+      pdl_wait();
+      pdl_launch_dependents();
+      int g = 0;
+      for (int w = blockIdx.x, it = 0; w < n_items && ok; w += gridDim.x, ++it) {
+        item(w, split, kvh, b, tile0, nt);
+        const int qb = it & 1;
+        if (!mbar_wait_bounded(&qempty[qb], ((it >> 1) & 1) ^ 1, a.timeout_ns, abort_flag, a.status)) break;
+        uint8_t* q = smem + kOffQ + qb * 2 * kAtom;
+        mbar_arrive_expect_tx(&qfull[qb], 2 * kAtom);
+        tma_load_4d(q, &map_q2, &qfull[qb], 0, kvh * G, 0, b * S);
+        tma_load_4d(q + kAtom, &map_q2, &qfull[qb], 64, kvh * G, 0, b * S);
+        const int z = plane(b, kvh);
+        for (int t = 0; t < nt && ok; ++t, ++g)
+          if (g >= pre) ok = load_kv(g, (tile0 + t) * kKT, z);
+      }
+    }
+    __syncwarp();
+  } else if (warp == 1) {
+    // ----------------------------------------------------------------- MMA
+    if (lane == 0) {
+      const uint32_t idesc_qk = idesc_bf16_f32(128, kKT);
+      const uint32_t idesc_pv = idesc_bf16_f32(128, kD) | (1u << 16);  // B (V) MN-major
+      const uint32_t p_base = smem_u32(smem + kOffPh);                  // P' [128 rows][128 keys]
+      bool ok = true;
+      auto issue_pv = [&](int u) {
+        const int s = u & 1;
+        const uint32_t ph = (u >> 1) & 1;
+        if (!mbar_wait_bounded(&vfull[s], ph, a.timeout_ns, abort_flag, a.status)) return false;
+        if (!mbar_wait_bounded(pfull, u & 1, a.timeout_ns, abort_flag, a.status)) return false;
+        if (!mbar_wait_bounded(&ofree[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) return false;
+        tc_fence_after();
+        const uint32_t vb = smem_u32(smem + kOffV + s * kKV);
+#pragma unroll
+        for (int j = 0; j < kKT / 16; ++j) {
+          const uint32_t aoff = (j >> 2) * kAtom + (j & 3) * 32;
+          tc_mma_bf16(t_o + s * kD, desc_sw128(p_base + aoff, 0, 1024), desc_sw128(vb + j * 2048, kBox, 1024),
+                      idesc_pv, j > 0 ? 1u : 0u);
+        }
+        tc_commit(&ofull[s]);
+        tc_commit(&vempty[s]);
+        tc_commit(pfree);
+        return true;
+      };
+      int g = 0;
+      for (int w = blockIdx.x, it = 0; w < n_items && ok; w += gridDim.x, ++it) {
+        int split, kvh, b, tile0, nt;
+        item(w, split, kvh, b, tile0, nt);
+        const int qb = it & 1;
+        if (!mbar_wait_bounded(&qfull[qb], (it >> 1) & 1, a.timeout_ns, abort_flag, a.status)) { ok = false; break; }
+        const uint32_t qa = smem_u32(smem + kOffQ + qb * 2 * kAtom);
+        for (int t = 0; t < nt; ++t, ++g) {
+          const int s = g & 1;
+          const uint32_t ph = (g >> 1) & 1;
+          if (!mbar_wait_bounded(&kfull[s], ph, a.timeout_ns, abort_flag, a.status)) { ok = false; break; }
+          if (!mbar_wait_bounded(&sfree[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t kb = smem_u32(smem + kOffK + s * kKV);
+#pragma unroll
+          for (int kk = 0; kk < kD / 16; ++kk) {
+            const uint32_t off = (kk & 3) * 32;
+            tc_mma_bf16(t_s + s * kKT, desc_sw128(qa + (kk >> 2) * kAtom + off, 0, 1024),
+                        desc_sw128(kb + (kk >> 2) * kBox + off, 0, 1024), idesc_qk, kk > 0 ? 1u : 0u);
+          }
+          tc_commit(&sfull[s]);
+          tc_commit(&kempty[s]);
+          if (g >= 1 && !issue_pv(g - 1)) { ok = false; break; }
+        }
+        tc_commit(&qempty[qb]);  // this item's QK^T products are all issued
+      }
+      if (ok && g >= 1) issue_pv(g - 1);
+      tc_commit(drain);
+      volatile int no_abort = 0;
+      mbar_wait_bounded(drain, 0, a.timeout_ns, &no_abort, a.status);
+    }
+    __syncwarp();
+  } else {
+    // ------------------------------------------------------------- softmax
+    const int q4 = warp & 3;                        // TMEM lane quarter
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const int rho = 32 * q4 + lane;                 // stacked row = TMEM lane
+    const int part = (rho / G) & 1;                 // 0: head row, 1: remainder row
+    const int qi = rho / (2 * G), qg = rho % G;     // query: block position, head in the group
+    const int pr = qg * S + qi;                     // partial row (order g * S + i)
+    const int col0 = 64 * part;                     // the keys (and dims) this thread sums
+    const int rho_h = rho & ~G, rho_r = rho | G;    // P' rows of this query
+    const float c = a.scale_log2;
+    // sum of this row and its partner's (G lanes apart) over this thread's
+    // 64 columns of a 128-column TMEM row block
+    auto load_pair_sum = [&](uint32_t taddr, float (&out)[64]) {
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        float lo[32], hi[32];
+        tmem_ld32(taddr + 32 * h, lo);        // columns 32h ..
+        tmem_ld32(taddr + 64 + 32 * h, hi);   // columns 64 + 32h ..
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+          const float mine = part ? hi[j] : lo[j];
+          const float send = part ? lo[j] : hi[j];
+          out[32 * h + j] = mine + __shfl_xor_sync(0xffffffffu, send, G);
+        }
+      }
+    };
+    bool ok = true;
+    int g = 0;
+    for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
+      int split, kvh, b, tile0, nt;
+      item(w, split, kvh, b, tile0, nt);
+      float o[64];                                  // O of this query, dims col0 .. col0 + 63
+#pragma unroll
+      for (int j = 0; j < 64; ++j) o[j] = 0.f;
+      float m = -INFINITY, l = 0.f, al = 0.f;      // al: rescale of the previous tile
+      auto consume_o = [&](int u, float alpha) {
+        const int s = u & 1;
+        bool wt = true;
+        if (lane == 0) wt = mbar_wait_bounded(&ofull[s], (u >> 1) & 1, a.timeout_ns, abort_flag, a.status);
+        wt = __shfl_sync(0xffffffffu, wt ? 1 : 0, 0) != 0;
+        if (!wt) return false;
+        tc_fence_after();
+        float pv[64];
+        load_pair_sum(t_o + s * kD + lane_off, pv);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&ofree[s]);
+#pragma unroll
+        for (int j = 0; j < 64; ++j) o[j] = fmaf(o[j], alpha, pv[j]);
+        return true;
+      };
+      for (int t = 0; t < nt; ++t, ++g) {
+        const int s = g & 1;
+        bool wt = true;
+        if (lane == 0) wt = mbar_wait_bounded(&sfull[s], (g >> 1) & 1, a.timeout_ns, abort_flag, a.status);
+        wt = __shfl_sync(0xffffffffu, wt ? 1 : 0, 0) != 0;
+        if (!wt) { ok = false; break; }
+        tc_fence_after();
+        float v[64];
+        load_pair_sum(t_s + s * kKT + lane_off, v);
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&sfree[s]);
+        const int kbase = (tile0 + t) * kKT + col0;
+        if ((tile0 + t) * kKT + kKT > T) {  // tail tile: keys >= T do not exist
+#pragma unroll
+          for (int j = 0; j < 64; ++j)
+            if (kbase + j >= T) v[j] = -INFINITY;
+        }
+        float mx = -INFINITY;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, v[j]);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, G));
+        // running max in base-2 units (scores times c)
+        const float mn = fmaxf(m, mx * c);
+        const float alpha = m == -INFINITY ? 0.f : ex2(m - mn);
+        m = mn;
+        float ssum = 0.f;
+#pragma unroll
+        for (int j = 0; j < 64; ++j) {
+          v[j] = ex2(fmaf(v[j], c, -mn));
+          ssum += v[j];
+        }
+        ssum += __shfl_xor_sync(0xffffffffu, ssum, G);
+        l = l * alpha + ssum;
+        // P' rows (head, remainder) of this query, this thread's 64 keys
+        if (g >= 1) {
+          bool pw = true;
+          if (lane == 0) pw = mbar_wait_bounded(pfree, (g - 1) & 1, a.timeout_ns, abort_flag, a.status);
+          pw = __shfl_sync(0xffffffffu, pw ? 1 : 0, 0) != 0;
+          if (!pw) { ok = false; break; }
+        }
+        uint8_t* pb = smem + kOffPh;
+#pragma unroll
+        for (int cc = 0; cc < 8; ++cc) {
+          uint4 h, r;
+          split_bf16(v[8 * cc + 0], v[8 * cc + 1], h.x, r.x);
+          split_bf16(v[8 * cc + 2], v[8 * cc + 3], h.y, r.y);
+          split_bf16(v[8 * cc + 4], v[8 * cc + 5], h.z, r.z);
+          split_bf16(v[8 * cc + 6], v[8 * cc + 7], h.w, r.w);
+          *reinterpret_cast<uint4*>(pb + swz(128, rho_h, col0 + 8 * cc)) = h;
+          *reinterpret_cast<uint4*>(pb + swz(128, rho_r, col0 + 8 * cc)) = r;
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(pfull);
+        if (t >= 1 && !consume_o(g - 1, al)) { ok = false; break; }
+        al = alpha;
+      }
+      if (ok && nt >= 1) ok = consume_o(g - 1, al);
+      // partial slot `split`: o (unnormalised, [q][d]), (m, l) per q
+      const long long prow = ((long long)(b * a.Hkv + kvh) * n_ctx + split) * kNQ;
+      float* dst = a.part_o + (prow + pr) * kD + col0;
+#pragma unroll
+      for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
+      if (part == 0) a.part_ml[prow + pr] = make_float2(m, l);
+    }
+  }
+
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
 }  // namespace
 
 bool attention_tc_supported(int D, int rows) { return D == kD && rows == kNQ; }
@@ -461,19 +789,37 @@ int attention_tc_splits(int B, int Hkv, int max_ctx) {
 
 int attention_tc_smem_bytes() { return kSmemBytes; }
 
+bool attention_tc_stacked_supported(int G, int S) {
+  return (G == 1 || G == 2 || G == 4 || G == 8 || G == 16) && G * S == kNQ;
+}
+
 cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx, const CUtensorMap& map_k128,
-                                const CUtensorMap& map_v128, const CUtensorMap& map_q, cudaStream_t st) {
+                                const CUtensorMap& map_v128, const CUtensorMap& map_q, cudaStream_t st,
+                                const CUtensorMap* map_q2) {
   const int items = a.B * a.Hkv * n_ctx;
   const int grid = items < kNumSMs ? items : kNumSMs;
+  if (a.split && map_q2 && attention_tc_stacked_supported(a.G, a.S)) {
+    switch (a.G) {
+      case 1: return launch_k(k_attn_ctx_stk<1>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, *map_q2, a, n_ctx, items);
+      case 2: return launch_k(k_attn_ctx_stk<2>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, *map_q2, a, n_ctx, items);
+      case 4: return launch_k(k_attn_ctx_stk<4>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, *map_q2, a, n_ctx, items);
+      case 8: return launch_k(k_attn_ctx_stk<8>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, *map_q2, a, n_ctx, items);
+      default: return launch_k(k_attn_ctx_stk<16>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, *map_q2, a, n_ctx, items);
+    }
+  }
   if (a.split)
     return launch_k(k_attn_ctx_tc<true>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, map_q, a, n_ctx, items);
   return launch_k(k_attn_ctx_tc<false>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, map_q, a, n_ctx, items);
 }
 
 cudaError_t prepare_attention_tc_kernels() {
-  cudaError_t e = cudaFuncSetAttribute(k_attn_ctx_tc<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(k_attn_ctx_tc<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  const void* fns[] = {(const void*)k_attn_ctx_tc<true>, (const void*)k_attn_ctx_tc<false>,
+                       (const void*)k_attn_ctx_stk<1>,   (const void*)k_attn_ctx_stk<2>,
+                       (const void*)k_attn_ctx_stk<4>,   (const void*)k_attn_ctx_stk<8>,
+                       (const void*)k_attn_ctx_stk<16>};
+  cudaError_t e = cudaSuccess;
+  for (const void* f : fns)
+    if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   return e;
 }
 

@@ -74,12 +74,14 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* rows_smem = abort_flag + 1;
-  // LM head with compacted rows: the valid row count is known on the device
-  // only.  A CTA never skips its first tile (its weights were requested
-  // before the count existed); a later tile is skipped when it starts at or
-  // beyond the count.  (A shorter MMA for a partly filled tile does not pay:
-  // tcgen05 M = 64 takes as long as M = 128.)
-  const bool dyn = EPI == kEpiSelect && args.out.rows_dev != nullptr;
+  // Compacted activation rows (the LM head's masked rows, or the active
+  // sequences' rows of a linear layer): the valid row count is known on the
+  // device only.  A CTA never skips its first tile (its weights were
+  // requested before the count existed); a later tile is skipped when its
+  // first activation row is at or beyond the count.  (A shorter MMA for a
+  // partly filled tile does not pay: tcgen05 M = 64 takes as long as M = 128.)
+  const bool dyn = EPI != kEpiStore && args.out.rows_dev != nullptr;
+  auto first_row = [&](int mt, int nt) { return EPI == kEpiPartial ? nt * args.BN : mt * kBM; };
 
   const int warp = warp_id();
   const int lane = lane_id();
@@ -144,7 +146,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         int mt, nt;
         if (EPI == kEpiPartial) { nt = r % args.n_tiles; mt = r / args.n_tiles; }
         else { mt = r % args.m_tiles; nt = r / args.m_tiles; }
-        if (dyn && t != (int)blockIdx.x && mt * kBM >= *rows_smem) continue;
+        if (dyn && t != (int)blockIdx.x && first_row(mt, nt) >= *rows_smem) continue;
         const int kb0 = split * args.kb_per_split;
         const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
         const int count = kb1 - kb0;
@@ -187,14 +189,16 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       int it = 0;
       for (int t = blockIdx.x; t < args.tiles_total && ok; t += gridDim.x) {
-        const int split = t / per_split;
-        const int mt = EPI == kEpiPartial ? (t % per_split) / args.n_tiles : (t % per_split) % args.m_tiles;
+        const int split = t / per_split, r = t % per_split;
+        int mt, nt;
+        if (EPI == kEpiPartial) { nt = r % args.n_tiles; mt = r / args.n_tiles; }
+        else { mt = r % args.m_tiles; nt = r / args.m_tiles; }
         if (dyn && t != (int)blockIdx.x) {
           if (rows < 0) {
             if (!mbar_wait_bounded(ready, 0, args.timeout_ns, abort_flag, args.status)) break;
             rows = *rows_smem;
           }
-          if (mt * kBM >= rows) continue;
+          if (first_row(mt, nt) >= rows) continue;
         }
         const uint32_t idesc = idesc_bf16_f32(kBM, args.BN);
         const int kb0 = split * args.kb_per_split;
@@ -248,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       int mt, nt;
       if (EPI == kEpiPartial) { nt = r % args.n_tiles; mt = r / args.n_tiles; }
       else { mt = r % args.m_tiles; nt = r / args.m_tiles; }
-      if (dyn && t != (int)blockIdx.x && mt * kBM >= rows) continue;
+      if (dyn && t != (int)blockIdx.x && first_row(mt, nt) >= rows) continue;
       const int ab = it & 1;
       const uint32_t aphase = (it >> 1) & 1;
       ++it;

@@ -65,7 +65,8 @@ struct GemmOut {
   float* sel_m;            // kEpiSelect: [n_tiles][rows_valid]
   float* sel_s;
   int* sel_a;
-  const int* rows_dev;     // kEpiSelect: device count of valid activation rows (compacted), or nullptr
+  const int* rows_dev;     // device count of valid activation rows (compacted), or nullptr: tiles whose
+                           // first activation row is at or past it are skipped (except a CTA's first)
 };
 
 // Plan a GEMM over activations [rows][K] and weights [N][K].  With
@@ -149,6 +150,12 @@ struct AttnArgs {
   float scale_log2;
   int* status;
   uint64_t timeout_ns;
+  // Active-sequence compaction record (see launch_embed_norm) or nullptr: the
+  // rows of qkv/out and the partials are those of the cmp[1] active
+  // sequences, compacted; the context cache of compacted sequence k is that
+  // of sequence cmp[2 + k]; (sequence, kv head) pairs past the active ones do
+  // nothing.
+  const int* cmp;
 };
 
 AttnPlan plan_attention(int B, int S, int Hq, int Hkv, int D, int max_ctx, int allow_tc = 1);
@@ -156,15 +163,19 @@ size_t attention_partial_bytes(const AttnPlan& p, int B, int Hkv);
 // map_k/map_v: context cache maps with 64-row boxes; map_k128/map_v128: the
 // same caches with 128-row boxes, and map_q the query rows (make_map_q), for
 // the tcgen05 path.
+// map_q2 (optional): the stacked query map (make_map_q_stacked) for split
+// activations; with it the context kernel runs its stacked form.
 cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a, const CUtensorMap& map_k, const CUtensorMap& map_v,
                              const CUtensorMap& map_k128, const CUtensorMap& map_v128, const CUtensorMap& map_q,
-                             cudaStream_t st);
+                             cudaStream_t st, const CUtensorMap* map_q2 = nullptr);
 // tcgen05 context attention (attention_tc.cu)
 bool attention_tc_supported(int D, int rows);
 int attention_tc_splits(int B, int Hkv, int max_ctx);
 int attention_tc_smem_bytes();
+bool attention_tc_stacked_supported(int G, int S);
 cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx, const CUtensorMap& map_k128,
-                                const CUtensorMap& map_v128, const CUtensorMap& map_q, cudaStream_t st);
+                                const CUtensorMap& map_v128, const CUtensorMap& map_q, cudaStream_t st,
+                                const CUtensorMap* map_q2 = nullptr);
 cudaError_t prepare_attention_tc_kernels();
 // Merge the split partials (no-op for the mma.sync path with one split); on
 // the tcgen05 path this also attends to the block keys.
@@ -176,20 +187,37 @@ cudaError_t launch_attention_combine(const AttnPlan& p, const AttnArgs& a, cudaS
 // [0, rows) and bf16 remainders (value - head, rounded) in rows [rows, 2*rows).
 // With sq != nullptr the norm is deferred: y = x * g (not normalised) and
 // sq[r] = sum of x[r]^2 (the consumer scales by rsqrt(sq / H + eps)).
+//
+// Active-sequence compaction: with cmp != nullptr the step runs on the rows
+// of the sequences that still have a masked position only, compacted to the
+// front (row k*S + i = position i of the k-th active sequence).  The embedding
+// kernel writes the compaction record, int32 [2 + B + B*S]:
+//   cmp[0] active rows, cmp[1] active sequences, cmp[2 + k] the k-th active
+//   sequence, cmp[2 + B + r] the original row b*S + i of compacted row r;
+// every later kernel of the step reads it (&cmp[0] is the dynamic row count
+// of the linear layers and their reduces).
+constexpr int cmp_words(int B, int S) { return 2 + B + B * S; }
 cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const void* embed, const void* pos,
                               const void* g, float* x, void* y_split, int B, int S, int H, int V, float eps,
-                              cudaStream_t st, float* sq = nullptr);
+                              cudaStream_t st, float* sq = nullptr, int* cmp = nullptr);
 // q|k|v of the step: the split-K sum written as bf16 head + remainder; with
 // theta > 0 the query and key heads (columns < qk_cols) of row r are rotated
 // to position *ctx_len + r % S (see dd_config.rope_theta).
+// With rows_dev only the first *rows_dev rows (the active ones) are written.
 cudaError_t launch_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N, void* out, int S,
-                              int D, int qk_cols, const int* ctx_len, float theta, cudaStream_t st);
-// Context tower (dd_append_block): y = RMSNorm(embed[token]) * g as bf16
-// head + remainder; then the split-K sum of y W_kv^T scattered as bf16 into the
-// K/V cache [L][B][Hkv][alloc_ctx][D] at positions *ctx_len + i, after which
-// *ctx_len grows by S.
-cudaError_t launch_tower_embed_norm(const int32_t* tokens, const void* embed, const void* g, void* y_split, int rows,
-                                    int H, int V, float eps, cudaStream_t st);
+                              int D, int qk_cols, const int* ctx_len, float theta, cudaStream_t st,
+                              const int* rows_dev = nullptr);
+// Context tower (dd_append_block): e = embed[token] (fp32, to x) and
+// y = RMSNorm(e) * g as bf16 head + remainder; its causal self-attention over
+// each committed block (fp32 q|k|v [rows][3 * heads * D] -> head + remainder
+// [2 * rows][heads * D]); then, after the residual and second RMSNorm, the
+// split-K sum of y W_kv^T scattered as bf16 into the K/V cache
+// [L][B][Hkv][alloc_ctx][D] at positions *ctx_len + i, after which *ctx_len
+// grows by S.
+cudaError_t launch_tower_embed_norm(const int32_t* tokens, const void* embed, const void* g, float* x, void* y_split,
+                                    int rows, int H, int V, float eps, cudaStream_t st);
+cudaError_t launch_tower_attention(const float* qkv, void* out_split, int rows, int S, int heads, int D,
+                                   cudaStream_t st);
 // `done` is a zeroed counter the kernel leaves zeroed again.
 cudaError_t launch_reduce_kv_append(const float* part, int splits, long long split_stride, int rows, int N, int S,
                                     int B, int Hkv, int D, int alloc_ctx, int* ctx_len, unsigned int* done, void* kc,
@@ -198,13 +226,15 @@ cudaError_t launch_reduce_f32(const float* part, int splits, long long split_str
                               cudaStream_t st);
 // With mask != nullptr the rows still masked are also written, compacted, to
 // y_c (head rows [0, count), remainders [rows, rows + count)), with
-// row_index[k] = the row of compacted row k and *count their number.
+// row_index[k] = the original row (b*S + i) of compacted row k and *count
+// their number.  With cmp (active-sequence compaction) rows at or past cmp[0]
+// do nothing and row r belongs to sequence cmp[2 + r/S].
 cudaError_t launch_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
                                         const void* g, void* y_split, int rows, int H, float eps, cudaStream_t st,
                                         const uint32_t* mask = nullptr, int S = 1, void* y_c = nullptr,
-                                        int* row_index = nullptr, int* count = nullptr);
+                                        int* row_index = nullptr, int* count = nullptr, const int* cmp = nullptr);
 cudaError_t launch_reduce_swiglu(const float* part, int splits, long long split_stride, void* h_split, int rows,
-                                 int F, cudaStream_t st);
+                                 int F, cudaStream_t st, const int* rows_dev = nullptr);
 // With count/row_index (compacted rows): rows r < *count, written to row_index[r].
 cudaError_t launch_select_combine(const float* sel_m, const float* sel_s, const int* sel_a, int n_tiles, int rows,
                                   float* conf, int* arg, cudaStream_t st, const int* count = nullptr,
@@ -244,5 +274,11 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t planes, uint64_t row
 // h*D..h*D+D-1) as a 3D bf16 map {D, Hq, rows}, box {64, G, S}: one box is the
 // G query heads of a kv head at S consecutive rows, in row order i * G + g.
 bool make_map_q(CUtensorMap* m, const void* qkv, uint64_t rows, uint64_t ld, int Hq, int D, int G, int S);
+// The query heads of a split q|k|v buffer (bf16 heads in rows [0, rows),
+// remainders in rows [rows, 2 rows)) as a 4D map {D, Hq, 2 parts, rows}, box
+// {64, G, 2, S}: one box holds, for S consecutive rows, the G query heads of
+// a kv head as the head then the remainder of each row (row order
+// (i * 2 + part) * G + g).
+bool make_map_q_stacked(CUtensorMap* m, const void* qkv, uint64_t rows, uint64_t ld, int Hq, int D, int G, int S);
 
 }  // namespace dd

@@ -119,13 +119,42 @@ __device__ __forceinline__ void load_gains(const __nv_bfloat16* g, int passes, f
     if (p < passes) load8_bf16(g + (p * blockDim.x + threadIdx.x) * 8, gv[p]);
 }
 
+// The k-th sequence (in order) whose mask word is non-zero, and the number
+// of such sequences, for the calling lanes of warp 0 (lanes < min(32,
+// blockDim.x); every one gets both; seq = -1 if there is no k-th).
+__device__ __forceinline__ void kth_active(const uint32_t* mask, int B, int k, int& seq, int& n_act) {
+  const int lane = threadIdx.x & 31;
+  const int nl = blockDim.x < 32 ? (int)blockDim.x : 32;
+  const unsigned lanes = nl == 32 ? 0xffffffffu : ((1u << nl) - 1u);
+  seq = -1;
+  n_act = 0;
+  for (int base = 0; base < B; base += nl) {
+    const unsigned bal = __ballot_sync(lanes, base + lane < B && mask[base + lane] != 0u);
+    const int cnt = __popc(bal);
+    if (seq < 0 && k >= n_act && k < n_act + cnt) {
+      unsigned m = bal;
+      for (int j = 0; j < k - n_act; ++j) m &= m - 1u;
+      seq = base + __ffs(m) - 1;
+    }
+    n_act += cnt;
+  }
+}
+
 // x[r] = E[id] + Pos[i] with id = V ([MASK]) for masked positions;
 // y[r] = RMSNorm(x[r]) * g as head + remainder.  One CTA per row.
+//
+// With cmp != nullptr the rows are those of the active sequences (any
+// position still masked), compacted: row r = k*S + i is position i of the
+// k-th active sequence, and rows past the active ones do nothing.  The
+// kernel also writes the compaction record the rest of the step reads:
+// cmp[0] = active rows, cmp[1] = active sequences, cmp[2 + k] = the k-th
+// active sequence, cmp[2 + B + r] = the original row (b*S + i) of row r.
 __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const __nv_bfloat16* embed,
                              const __nv_bfloat16* pos, const __nv_bfloat16* g, float* x, __nv_bfloat16* y, int S,
-                             int H, int V, float eps, float* sq) {
+                             int H, int V, float eps, float* sq, int* cmp) {
   __shared__ float red[32];
-  const int r = blockIdx.x, b = r / S, i = r % S, R = gridDim.x;
+  __shared__ int s_seq, s_nact;
+  const int r = blockIdx.x, i = r % S, R = gridDim.x, B = R / S;
   const int passes = H / (8 * blockDim.x);
   float gv[kMaxRowPasses][8], pv[kMaxRowPasses][8];
   load_gains(g, passes, gv);
@@ -134,9 +163,31 @@ __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const 
     if (p < passes) load8_bf16(pos + (long long)i * H + (p * blockDim.x + threadIdx.x) * 8, pv[p]);
   pdl_wait();
   pdl_launch_dependents();
+  int b = r / S;
+  if (cmp) {
+    if (threadIdx.x < 32) {  // warp 0 (the whole CTA when it is narrower)
+      int seq, n_act;
+      kth_active(mask, B, r / S, seq, n_act);
+      if (threadIdx.x == 0) {
+        s_seq = seq;
+        s_nact = n_act;
+        if (r == 0) {
+          cmp[0] = n_act * S;
+          cmp[1] = n_act;
+        }
+        if (seq >= 0) {
+          cmp[2 + B + r] = seq * S + i;
+          if (i == 0) cmp[2 + r / S] = seq;
+        }
+      }
+    }
+    __syncthreads();
+    if (s_seq < 0) return;
+    b = s_seq;
+  }
   const bool masked = (mask[b] >> i) & 1u;
   // Ids outside [0, V] (never produced by the commit rule) read the [MASK] row.
-  const int t = tokens[r];
+  const int t = tokens[b * S + i];
   const int id = (masked || t < 0 || t > V) ? V : t;
   float xv[kMaxRowPasses][8];
 #pragma unroll
@@ -154,17 +205,25 @@ __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const 
 
 // x[r] += sum_s part[s][r]; y[r] = RMSNorm(x[r]) * g as head + remainder.
 // One CTA per row; the split partial loads of each pass are independent.
+// With cmp (the compaction record of k_embed_norm) rows past the active ones
+// do nothing, and row r belongs to sequence cmp[2 + r / S].
 __global__ void k_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
                                        const __nv_bfloat16* g, __nv_bfloat16* y, int H, float eps,
-                                       const uint32_t* mask, int S, __nv_bfloat16* y_c, int* row_index, int* count) {
+                                       const uint32_t* mask, int S, __nv_bfloat16* y_c, int* row_index, int* count,
+                                       const int* cmp) {
   __shared__ float red[32];
   __shared__ int cpos;
-  const int r = blockIdx.x, R = gridDim.x;
+  const int r = blockIdx.x, R = gridDim.x, B = R / S;
   const int passes = H / (8 * blockDim.x);
   float gv[kMaxRowPasses][8];
   load_gains(g, passes, gv);
   pdl_wait();
   pdl_launch_dependents();
+  const int n_act = cmp ? cmp[1] : B;
+  if (cmp && r >= cmp[0]) {
+    if (r == 0 && mask && threadIdx.x == 0) *count = 0;  // no sequence active
+    return;
+  }
   float xv[kMaxRowPasses][8];
 #pragma unroll
   for (int p = 0; p < kMaxRowPasses; ++p) {
@@ -175,26 +234,28 @@ __global__ void k_reduce_residual_norm(const float* part, int splits, long long 
     store8_f32(x + e, xv[p]);
   }
   // With `mask`: the rows still masked are also written, in order, to y_c
-  // (rows [0, count) and their remainders at [R, R + count)) for the LM head.
+  // (rows [0, count) and their remainders at [R, R + count)) for the LM head,
+  // with row_index[k] = the original row (b*S + i) of compacted row k.
   int r2 = -1;
   if (mask) {
-    // masked rows before this one: the sequences before b (their mask words
-    // read in parallel, one block sum) plus the positions before i in b
-    const int b = r / S, i = r % S;
+    // masked rows before this one: the sequences before this row's (their
+    // mask words read in parallel, one block sum) plus the positions before i
+    const int k = r / S, i = r % S;
     int before = 0, all = 0;
-    for (int bb = threadIdx.x; bb < R / S; bb += blockDim.x) {
-      const int n = __popc(mask[bb]);
-      before += bb < b ? n : 0;
+    for (int kk = threadIdx.x; kk < n_act; kk += blockDim.x) {
+      const int n = __popc(mask[cmp ? cmp[2 + kk] : kk]);
+      before += kk < k ? n : 0;
       all += n;
     }
     before = (int)block_sum((float)before, red);
     if (r == 0) all = (int)block_sum((float)all, red);
     if (threadIdx.x == 0) {
+      const int b = cmp ? cmp[2 + k] : k;
       const uint32_t mb = mask[b];
       const bool masked = (mb >> i) & 1u;
       const int pos = before + __popc(mb & ((1u << i) - 1u));
       cpos = masked ? pos : -1;
-      if (masked) row_index[pos] = r;
+      if (masked) row_index[pos] = b * S + i;
       if (r == 0) *count = all;
     }
     __syncthreads();
@@ -217,21 +278,24 @@ __global__ void k_reduce(const float* part, int splits, long long split_stride, 
 }
 
 // q|k|v = the sum of the split-K partials, written as bf16 head (rows
-// [0, rows)) + remainder (rows [rows, 2 rows)).  With theta > 0 the pairs
+// [0, rows)) + remainder (rows [rows, 2 rows)); with rows_dev only the first
+// *rows_dev rows (the active ones).  With theta > 0 the pairs
 // (2j, 2j+1) of every query and key head (columns < qk_cols) of row r turn by
 // (T + r % S) * theta^(-2j/D) radians, T = *ctx_len: the frequencies and the
 // angle in double, the angle reduced modulo 2 pi in double before an fp32
 // sine and cosine, the rotation in fp32.
 __global__ void k_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N,
-                             __nv_bfloat16* out, int S, int D, int qk_cols, const int* ctx_len, float theta) {
+                             __nv_bfloat16* out, int S, int D, int qk_cols, const int* ctx_len, float theta,
+                             const int* rows_dev) {
   __shared__ double freq[64];  // theta^(-2j/D), j < D/2 (D <= 128)
   if (theta > 0.f && threadIdx.x < D / 2) freq[threadIdx.x] = pow((double)theta, -2.0 * threadIdx.x / D);
   __syncthreads();
   pdl_wait();
   pdl_launch_dependents();
-  const long long total = (long long)rows * N;
+  const long long total = (long long)rows * N;  // remainders start here
+  const long long used = rows_dev ? (long long)*rows_dev * N : total;
   const int T = theta > 0.f ? *ctx_len : 0;
-  for (long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8; e < total;
+  for (long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8; e < used;
        e += (long long)gridDim.x * blockDim.x * 8) {
     float acc[8];
     load8_f32(part + e, acc);
@@ -247,10 +311,11 @@ __global__ void k_reduce_qkv(const float* part, int splits, long long split_stri
   }
 }
 
-// Context tower, first half: y[r] = RMSNorm(embed[tokens[r]]) * g as head +
+// Context tower, first step: e[r] = embed[tokens[r]] (fp32, the residual
+// stream of its attention layer) and y[r] = RMSNorm(e[r]) * g as head +
 // remainder (ids outside [0, V) read row 0).  One CTA per row.
 __global__ void k_tower_embed_norm(const int32_t* tokens, const __nv_bfloat16* embed, const __nv_bfloat16* g,
-                                   __nv_bfloat16* y, int H, int V, float eps) {
+                                   float* x, __nv_bfloat16* y, int H, int V, float eps) {
   __shared__ float red[32];
   const int r = blockIdx.x, R = gridDim.x;
   const int passes = H / (8 * blockDim.x);
@@ -264,9 +329,63 @@ __global__ void k_tower_embed_norm(const int32_t* tokens, const __nv_bfloat16* e
 #pragma unroll
   for (int p = 0; p < kMaxRowPasses; ++p) {
     if (p >= passes) break;
-    load8_bf16(embed + (long long)id * H + (p * blockDim.x + threadIdx.x) * 8, xv[p]);
+    const int c = (p * blockDim.x + threadIdx.x) * 8;
+    load8_bf16(embed + (long long)id * H + c, xv[p]);
+    store8_f32(x + (long long)r * H + c, xv[p]);
   }
   norm_store(xv, passes, r, H, R, gv, y, eps, red);
+}
+
+// Context tower, causal self-attention inside each committed block: query
+// position i of sequence b, head h attends to positions j <= i of the same
+// block, softmax(q.k / sqrt(D)) in fp32.  qkv: fp32 [rows][3 * heads * D]
+// (q heads, then k, then v); out: bf16 head + remainder [2 * rows][heads * D].
+// One CTA per (sequence, head), one warp per query position; lane l holds
+// dims l, l + 32, ...
+template <int D>
+__global__ void k_tower_attention(const float* qkv, __nv_bfloat16* out, int rows, int S, int heads, float scale) {
+  constexpr int P = D / 32;
+  pdl_wait();
+  pdl_launch_dependents();
+  const int b = blockIdx.x / heads, h = blockIdx.x % heads;
+  const int i = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (i >= S) return;
+  const int W = heads * D;
+  const float* qrow = qkv + (long long)(b * S + i) * 3 * W + h * D;
+  float q[P], acc[P];
+#pragma unroll
+  for (int k = 0; k < P; ++k) {
+    q[k] = qrow[lane + 32 * k];
+    acc[k] = 0.f;
+  }
+  // running max and sum over the keys j <= i (online softmax, one key at a time)
+  float m = -INFINITY, l = 0.f;
+  for (int j = 0; j <= i; ++j) {
+    const float* krow = qkv + (long long)(b * S + j) * 3 * W + W + h * D;
+    float d = 0.f;
+#pragma unroll
+    for (int k = 0; k < P; ++k) d = fmaf(q[k], krow[lane + 32 * k], d);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) d += __shfl_xor_sync(0xffffffffu, d, o);
+    const float s = d * scale;
+    const float mn = fmaxf(m, s);
+    const float a = expf(m - mn), e = expf(s - mn);
+    l = l * a + e;
+    const float* vrow = krow + W;
+#pragma unroll
+    for (int k = 0; k < P; ++k) acc[k] = fmaf(acc[k], a, e * vrow[lane + 32 * k]);
+    m = mn;
+  }
+  const float inv = 1.f / l;
+  __nv_bfloat16* o_hi = out + (long long)(b * S + i) * W + h * D;
+  __nv_bfloat16* o_lo = o_hi + (long long)rows * W;
+#pragma unroll
+  for (int k = 0; k < P; ++k) {
+    const float v = acc[k] * inv;
+    const __nv_bfloat16 hv = __float2bfloat16_rn(v);
+    o_hi[lane + 32 * k] = hv;
+    o_lo[lane + 32 * k] = __float2bfloat16_rn(v - __bfloat162float(hv));
+  }
 }
 
 // Context tower, second half: the split-K sum of y W_kv^T (column n of row
@@ -310,13 +429,15 @@ __global__ void k_reduce_kv_append(const float* part, int splits, long long spli
 }
 
 // h[r][f] = silu(gate) * up, gate = column f, up = column F + f of the
-// summed partials [rows][2F]; head + remainder (remainder at h + rows*F).
+// summed partials [rows][2F]; head + remainder (remainder at h + rows*F);
+// with rows_dev only the first *rows_dev rows.
 __global__ void k_reduce_swiglu(const float* part, int splits, long long split_stride, __nv_bfloat16* h, int rows,
-                                int F) {
+                                int F, const int* rows_dev) {
   pdl_wait();
   pdl_launch_dependents();
-  const long long total = (long long)rows * F;
-  for (long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8; e < total;
+  const long long total = (long long)rows * F;  // remainders start here
+  const long long used = rows_dev ? (long long)*rows_dev * F : total;
+  for (long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8; e < used;
        e += (long long)gridDim.x * blockDim.x * 8) {
     const long long r = e / F;
     const int f = (int)(e % F);
@@ -534,6 +655,7 @@ cudaError_t prepare_small_kernels() {
                        (const void*)k_reduce_swiglu,         (const void*)k_select_combine,
                        (const void*)k_reduce_qkv,
                        (const void*)k_tower_embed_norm,      (const void*)k_reduce_kv_append,
+                       (const void*)k_tower_attention<64>,   (const void*)k_tower_attention<128>,
                        (const void*)k_commit};
   cudaError_t e = cudaSuccess;
   for (const void* f : fns) {
@@ -544,21 +666,30 @@ cudaError_t prepare_small_kernels() {
 
 cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const void* embed, const void* pos,
                               const void* g, float* x, void* y, int B, int S, int H, int V, float eps,
-                              cudaStream_t st, float* sq) {
+                              cudaStream_t st, float* sq, int* cmp) {
   return launch_k(k_embed_norm, B * S, row_threads(H), 0, st, tokens, mask, (const __nv_bfloat16*)embed,
-                  (const __nv_bfloat16*)pos, (const __nv_bfloat16*)g, x, (__nv_bfloat16*)y, S, H, V, eps, sq);
+                  (const __nv_bfloat16*)pos, (const __nv_bfloat16*)g, x, (__nv_bfloat16*)y, S, H, V, eps, sq, cmp);
 }
 
 cudaError_t launch_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N, void* out, int S,
-                              int D, int qk_cols, const int* ctx_len, float theta, cudaStream_t st) {
+                              int D, int qk_cols, const int* ctx_len, float theta, cudaStream_t st,
+                              const int* rows_dev) {
   return launch_k(k_reduce_qkv, grid_for((long long)rows * N / 8, 256), 256, 0, st, part, splits, split_stride, rows,
-                  N, (__nv_bfloat16*)out, S, D, qk_cols, ctx_len, theta);
+                  N, (__nv_bfloat16*)out, S, D, qk_cols, ctx_len, theta, rows_dev);
 }
 
-cudaError_t launch_tower_embed_norm(const int32_t* tokens, const void* embed, const void* g, void* y, int rows, int H,
-                                    int V, float eps, cudaStream_t st) {
+cudaError_t launch_tower_embed_norm(const int32_t* tokens, const void* embed, const void* g, float* x, void* y,
+                                    int rows, int H, int V, float eps, cudaStream_t st) {
   return launch_k(k_tower_embed_norm, rows, row_threads(H), 0, st, tokens, (const __nv_bfloat16*)embed,
-                  (const __nv_bfloat16*)g, (__nv_bfloat16*)y, H, V, eps);
+                  (const __nv_bfloat16*)g, x, (__nv_bfloat16*)y, H, V, eps);
+}
+
+cudaError_t launch_tower_attention(const float* qkv, void* out, int rows, int S, int heads, int D, cudaStream_t st) {
+  const float scale = 1.f / sqrtf((float)D);
+  const int blocks = (rows / S) * heads;
+  if (D == 128)
+    return launch_k(k_tower_attention<128>, blocks, S * 32, 0, st, qkv, (__nv_bfloat16*)out, rows, S, heads, scale);
+  return launch_k(k_tower_attention<64>, blocks, S * 32, 0, st, qkv, (__nv_bfloat16*)out, rows, S, heads, scale);
 }
 
 cudaError_t launch_reduce_kv_append(const float* part, int splits, long long split_stride, int rows, int N, int S,
@@ -576,15 +707,17 @@ cudaError_t launch_reduce_f32(const float* part, int splits, long long split_str
 
 cudaError_t launch_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
                                         const void* g, void* y, int rows, int H, float eps, cudaStream_t st,
-                                        const uint32_t* mask, int S, void* y_c, int* row_index, int* count) {
+                                        const uint32_t* mask, int S, void* y_c, int* row_index, int* count,
+                                        const int* cmp) {
   return launch_k(k_reduce_residual_norm, rows, row_threads(H), 0, st, part, splits, split_stride, x,
-                  (const __nv_bfloat16*)g, (__nv_bfloat16*)y, H, eps, mask, S, (__nv_bfloat16*)y_c, row_index, count);
+                  (const __nv_bfloat16*)g, (__nv_bfloat16*)y, H, eps, mask, S, (__nv_bfloat16*)y_c, row_index, count,
+                  cmp);
 }
 
 cudaError_t launch_reduce_swiglu(const float* part, int splits, long long split_stride, void* h, int rows, int F,
-                                 cudaStream_t st) {
+                                 cudaStream_t st, const int* rows_dev) {
   return launch_k(k_reduce_swiglu, grid_for((long long)rows * F / 8, 256), 256, 0, st, part, splits, split_stride,
-                  (__nv_bfloat16*)h, rows, F);
+                  (__nv_bfloat16*)h, rows, F, rows_dev);
 }
 
 cudaError_t launch_select_combine(const float* sel_m, const float* sel_s, const int* sel_a, int n_tiles, int rows,

@@ -113,14 +113,16 @@ class Decoder:
 
     def set_context_tower(self, tower: dict):
         """Register the synthetic context tower: "ctx_embed" [V][H], "ctx_g" [H],
+        "ctx_wqkv" [3*Hkv*D][H], "ctx_wo" [H][Hkv*D], "ctx_g2" [H],
         "ctx_wkv" [L][2*Hkv*D][H] (np.uint16 bf16 bits or bf16 tensors; kept
         alive here)."""
+        names = ("ctx_embed", "ctx_g", "ctx_wqkv", "ctx_wo", "ctx_g2", "ctx_wkv")
+
         def t(name):
             v = tower[name]
             return (v if isinstance(v, torch.Tensor) else bits_to_tensor(v, "cpu")).contiguous().to(self.device)
-        self.tower = {n: t(n) for n in ("ctx_embed", "ctx_g", "ctx_wkv")}
-        B.dd_set_context_tower(self.ctx, _ptr(self.tower["ctx_embed"]), _ptr(self.tower["ctx_g"]),
-                               _ptr(self.tower["ctx_wkv"]))
+        self.tower = {n: t(n) for n in names}
+        B.dd_set_context_tower(self.ctx, *[_ptr(self.tower[n]) for n in names])
 
     def append_block(self, tokens: torch.Tensor, stream=None):
         """Encode the committed block `tokens` [B][S] (device int32) with the
@@ -130,6 +132,17 @@ class Decoder:
     def device_status(self, stream=None):
         """Raise DDError if a kernel of this context recorded an expired bounded wait."""
         B.dd_device_status(self.ctx, _stream(stream))
+
+    @property
+    def compact_sequences(self) -> bool:
+        """Each step runs only the rows of sequences that still have a masked
+        position (default True); probe activations are then in compacted row
+        order (see `active_rows`)."""
+        return bool(B.dd_get_option(self.ctx, B.DD_OPT_COMPACT_SEQUENCES))
+
+    @compact_sequences.setter
+    def compact_sequences(self, on: bool):
+        B.dd_set_option(self.ctx, B.DD_OPT_COMPACT_SEQUENCES, 1 if on else 0)
 
     @property
     def fused_reduce(self) -> bool:
@@ -166,6 +179,15 @@ class Decoder:
         B.dd_denoise_step_probe(self.ctx, _ptr(tokens), _ptr(mask), gamma, mode, _ptr(out["n_committed"]), p,
                                 _stream(stream))
         return out
+
+
+def active_rows(mask, block: int, compacted: bool):
+    """Original rows (b*S + i) in the order a probe reports them: with
+    active-sequence compaction, the rows of the sequences whose mask word is
+    non-zero, in sequence order; otherwise every row."""
+    m = np.asarray(mask).astype(np.uint32).reshape(-1)
+    seqs = np.nonzero(m)[0] if compacted else np.arange(m.size)
+    return (seqs[:, None] * block + np.arange(block)[None, :]).reshape(-1)
 
 
 def join_split(t: torch.Tensor) -> torch.Tensor:

@@ -1,7 +1,8 @@
 """Small, self-contained workloads for profiler captures (ncu).
 
-    python -m block_wise_masked_dd_b300.profile_cases step   [--config small] [--iters N]
-    python -m block_wise_masked_dd_b300.profile_cases attn   [--iters N]   # B=64, T=8192, 32/8 x 128
+    python -m block_wise_masked_dd_b300.profile_cases step   [--config small] [--iters N] [--batch B --layers L]
+    python -m block_wise_masked_dd_b300.profile_cases attn   [--iters N] [--batch B --ctx T]
+                                                    # default B=64, T=8192, 32/8 x 128
     python -m block_wise_masked_dd_b300.profile_cases lmhead [--iters N]   # 1024 x 4096 x 131072
     python -m block_wise_masked_dd_b300.profile_cases gemm   [--rows 128 --n 11264 --k 2048]
 
@@ -40,6 +41,10 @@ def case_step(args):
     import synth
     from block_wise_masked_dd_b300.decoder import Decoder, bits_to_tensor, pack_weights
     cfg = synth.CONFIGS[args.config]
+    if args.batch:
+        cfg = cfg.replace(batch=args.batch)
+    if args.layers:
+        cfg = cfg.replace(n_layers=args.layers)
     if cfg.name == "large":
         w = synth.make_weights_torch(cfg, 0, "cuda")
         k, v = synth.make_context_kv_torch(cfg, 1, "cuda")
@@ -66,7 +71,8 @@ def case_attn(args):
 
     import synth
     from block_wise_masked_dd_b300.decoder import BlockAttention
-    c = synth.ATTN_MICRO
+    c = synth.ATTN_MICRO.replace(batch=args.batch or synth.ATTN_MICRO.batch, ctx_len=args.ctx or synth.ATTN_MICRO.ctx_len)
+    c = c.replace(max_ctx=c.ctx_len)
     g = synth.torch_generator(7, "cuda")
     qkv = synth.torch_normal_bf16((c.rows, c.qkv_width), 1.0, g, "cuda")
     kc = synth.torch_normal_bf16((c.batch, c.n_kv_heads, c.ctx_len, c.head_dim), 1.0, g, "cuda")
@@ -75,7 +81,7 @@ def case_attn(args):
     op = BlockAttention(c.batch, c.block, c.n_q_heads, c.n_kv_heads, c.head_dim, c.ctx_len, c.ctx_len, "cuda")
     ms = _time(lambda: op(qkv, kc, vc, out), args.iters)
     nbytes = 4 * c.batch * c.n_kv_heads * c.ctx_len * c.head_dim
-    print(f"attn: {ms * 1e3:.1f} us per launch, {nbytes / ms / 1e6:.0f} GB/s of context K/V")
+    print(f"attn B{c.batch} T{c.ctx_len}: {ms * 1e3:.1f} us per launch, {nbytes / ms / 1e6:.0f} GB/s of context K/V")
 
 
 def case_lmhead(args):
@@ -113,6 +119,10 @@ def main():
     ap.add_argument("--iters", type=int, default=3)
     ap.add_argument("--config", default="small")
     ap.add_argument("--gamma", type=float, default=0.8)
+    ap.add_argument("--batch", type=int, default=0,
+                    help="attn: sequences (0: the microbenchmark's 64); step: sequences (0: the workload's)")
+    ap.add_argument("--layers", type=int, default=0, help="step: denoiser layers (0: the workload's)")
+    ap.add_argument("--ctx", type=int, default=0, help="attn: context length (0: the microbenchmark's 8192)")
     ap.add_argument("--rows", type=int, default=128)
     ap.add_argument("--n", type=int, default=11264)
     ap.add_argument("--k", type=int, default=2048)

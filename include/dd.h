@@ -144,14 +144,25 @@ dd_status dd_init_weights(dd_ctx* ctx, const dd_weights* w);
 dd_status dd_set_context_kv(dd_ctx* ctx, const void* k, const void* v, int32_t t0, int32_t n,
                             void* stream);
 
-/* Weights of a synthetic context tower (the survey's NEXT-2 row; the pages'
- * frozen autoregressive tower is out of scope): one position-wise dense layer,
- * y = RMSNorm(embed[token]) * g, and per denoiser layer l the K rows then the V
- * rows y W_kv[l]^T.  Borrowed bf16 device pointers, 16-byte aligned:
- * embed [V][H], g [H], wkv [L][2*Hkv*D][H]. */
+/* Weights of a synthetic context tower.  The pages' tower is a frozen, trained
+ * causal model that encodes the committed tokens (TwoTower article,
+ * "技術/ビジネス面"); it is out of scope, and this stand-in is one causal
+ * self-attention layer over each committed block followed by the K/V
+ * projections of every denoiser layer:
+ *   e_i = embed[t_i], y_i = RMSNorm(e_i) * g, q|k|v_i = y_i wqkv^T (n_kv_heads
+ *   heads of head_dim each), a_i = softmax over j <= i of q_i.k_j / sqrt(D)
+ *   applied to v_j, h_i = e_i + a_i wo^T, z_i = RMSNorm(h_i) * g2, and per
+ *   denoiser layer l the K rows then the V rows z_i wkv[l]^T.
+ * Position i of an appended block depends on the committed tokens at
+ * positions <= i only.  Borrowed bf16 device pointers, 16-byte aligned:
+ * embed [V][H], g [H], wqkv [3*Hkv*D][H] (q rows, then k, then v),
+ * wo [H][Hkv*D], g2 [H], wkv [L][2*Hkv*D][H]. */
 typedef struct dd_context_tower {
   const void* embed;
   const void* g;
+  const void* wqkv;
+  const void* wo;
+  const void* g2;
   const void* wkv;
 } dd_context_tower;
 
@@ -162,6 +173,8 @@ dd_status dd_set_context_tower(dd_ctx* ctx, const dd_context_tower* tower);
 /* Encode a committed block with the context tower and append it to the
  * context on the device: the K/V of every layer at positions [T, T+S) (T =
  * the current context length, then T += S), with no host round trip.
+ * Requires n_layers*2*n_kv_heads*head_dim and 3*n_kv_heads*head_dim to be
+ * multiples of 128 (checked by dd_set_context_tower).
  * tokens: int32 [B][S] device memory (ids in [0, V); others read id 0).
  * Requires T + S <= max_ctx.  Asynchronous on `stream`. */
 dd_status dd_append_block(dd_ctx* ctx, const int32_t* tokens, void* stream);
@@ -212,7 +225,10 @@ const char* dd_last_error(void);
  * attn_out: bf16 [L][2*B*S][Hq*D], the attention output of every layer
  * (before the O projection); hidden: bf16 [2*B*S][H], the final RMSNorm output;
  * logits: fp32 [B*S][V], computed by the same tensor-core LM-head mainloop with
- * a plain store instead of the fused select; conf: fp32 [B*S]; arg: int32 [B*S]. */
+ * a plain store instead of the fused select; conf: fp32 [B*S]; arg: int32 [B*S].
+ * With DD_OPT_COMPACT_SEQUENCES (the default) attn_out, hidden and logits hold
+ * the active sequences' rows first, compacted (see that option), and conf/arg
+ * are valid for the active sequences' rows only. */
 typedef struct dd_probe {
   void* attn_out;
   void* hidden;
@@ -232,6 +248,21 @@ dd_status dd_denoise_step_probe(dd_ctx* ctx, int32_t* tokens, uint32_t* mask, fl
 dd_status dd_step_launch_count(dd_ctx* ctx, int32_t* n);
 
 /* Context options.
+ *   DD_OPT_COMPACT_SEQUENCES (set/get, 0 or 1, default 1): with 1 each
+ *     denoising step runs only the rows of the sequences that still have a
+ *     masked position (explainer step 5: a block stops once no [MASK] is
+ *     left, and sequences are independent, so a finished sequence needs no
+ *     further computation): the first kernel of the step lists the active
+ *     sequences and every later kernel works on their rows, compacted to the
+ *     front, and skips the rest (linear-layer tiles past the active rows,
+ *     attention work items of finished sequences).  Results are those of the
+ *     uncompacted step; with 0 every step runs all B*S rows.  Not combined
+ *     with DD_OPT_FUSED_REDUCE (which runs all rows).  Activations reported by
+ *     dd_denoise_step_probe (attention outputs, final hidden state, logits)
+ *     are then in compacted row order: rows k*S .. k*S+S-1 belong to the k-th
+ *     sequence (in order) that had a masked position before the step; conf
+ *     and arg stay in the original order, valid for those sequences' rows.
+ *     Switching drops the captured graphs.
  *   DD_OPT_FUSED_REDUCE (set/get, 0 or 1): with 1 the linear layers of the
  *     step (QKV, O, gate|up and every down projection but the last) sum
  *     their split-K partials inside the GEMM: the CTAs that split one
@@ -249,6 +280,7 @@ dd_status dd_step_launch_count(dd_ctx* ctx, int32_t* n);
  */
 enum {
   DD_OPT_FUSED_REDUCE = 1,
+  DD_OPT_COMPACT_SEQUENCES = 10,
   DD_OPT_FUSED_SPLITS_QKV = 2, DD_OPT_FUSED_SPLITS_O, DD_OPT_FUSED_SPLITS_GATE_UP, DD_OPT_FUSED_SPLITS_DOWN,
   DD_OPT_FUSED_GRID_QKV = 6, DD_OPT_FUSED_GRID_O, DD_OPT_FUSED_GRID_GATE_UP, DD_OPT_FUSED_GRID_DOWN
 };
@@ -317,11 +349,18 @@ dd_status dd_lmhead_select(int32_t rows, int32_t hidden, int32_t vocab, const vo
  * is a deployment convenience.  It takes no workspace: the per-tile scratch
  * lives in an 8 MiB array inside the library, held on every device that loads
  * the library until the process exits, which limits rows * (vocab/256) to
- * about 699000 (larger requests fail with DD_ERR_INVALID_ARG before anything
- * is launched).  It calls no allocating routine.  The first call on each
- * device looks up that array's device address (with the device current); make
- * that first call before any stream capture.  All calls share the array and
- * it keeps the last call's contents, so calls that overlap on the GPU race.
+ * at most 698944 (larger requests fail with DD_ERR_INVALID_ARG before
+ * anything is launched).  It calls no allocating routine.  The first call on
+ * each device is a warm-up: it looks up that array's device address (with the
+ * device current), and under lazy module loading (CUDA's default) that
+ * lookup loads the module and creates the array, so it may allocate and
+ * synchronise; make it before any stream capture and outside any region that
+ * must not allocate.  The address is cached, so a device reset after the
+ * first call is not supported.  All calls share the array and it keeps the
+ * last call's contents, so calls that overlap on the GPU race.  If a bounded
+ * wait inside the kernel expires, every output of the call is overwritten
+ * with conf = NaN and arg = -1 (the call itself has already returned DD_OK,
+ * being asynchronous).
  * x: bf16 [rows][hidden], w: bf16 [vocab][hidden], conf: fp32 [rows],
  * arg: int32 [rows], all device memory; asynchronous on `stream`. */
 dd_status dd_lmhead_select_noalloc(int32_t rows, int32_t hidden, int32_t vocab, const void* x, const void* w,

@@ -121,6 +121,25 @@ def check_commit(tok, mask, gamma, mode, S, r_tokens, r_mask, r_tie, g_tok, g_ma
     return flagged, compared
 
 
+def probe_rows(dec, mask, S):
+    """Original rows (b*S + i) in the order the probe reports activations:
+    with active-sequence compaction (the default), the rows of the sequences
+    that had a masked position before the step, in sequence order."""
+    from block_wise_masked_dd_b300.decoder import active_rows
+    return active_rows(mask, S, dec.compact_sequences and not dec.fused_reduce)
+
+
+def with_finished(cfg, tok, mask, finished, seed=0):
+    """The state (tok, mask) with the sequences in `finished` fully committed
+    (mask word 0, every position holding a seeded id in [0, V))."""
+    tok, mask = tok.copy(), mask.copy()
+    rng = np.random.default_rng(seed)
+    for b in finished:
+        tok[b] = rng.integers(0, cfg.vocab, cfg.block, dtype=np.int32)
+        mask[b] = 0
+    return tok, mask
+
+
 def compare_step(p: Problem, tok, mask, gamma, mode=0, logits=True):
     """Run one step on both sides from the same state; check every probe.
     Returns (gpu new tokens, gpu new mask, oracle result, near-tie count)."""
@@ -130,17 +149,19 @@ def compare_step(p: Problem, tok, mask, gamma, mode=0, logits=True):
     torch.cuda.synchronize()
     r = oracle.denoise_step(p.model, tok, mask, gamma, mode, keep_intermediates=True)
     from block_wise_masked_dd_b300.decoder import join_split
+    rows = probe_rows(p.dec, mask, cfg.block)
+    n = rows.size
     for l in range(cfg.n_layers):
-        close(join_split(out["attn_out"][l]).cpu().numpy(), r.attn_out[l], TOL_ATTN, f"attention output, layer {l}",
-              rel_rms=1e-3)
-    close(join_split(out["hidden"]).cpu().numpy(), r.hidden_final, TOL_LOGIT, "final hidden", rel_rms=1e-3)
+        close(join_split(out["attn_out"][l]).cpu().numpy()[:n], r.attn_out[l][rows], TOL_ATTN,
+              f"attention output, layer {l}", rel_rms=1e-3)
+    close(join_split(out["hidden"]).cpu().numpy()[:n], r.hidden_final[rows], TOL_LOGIT, "final hidden", rel_rms=1e-3)
     if logits:
-        close(out["logits"].cpu().numpy(), r.logits, TOL_LOGIT, "logits")
+        close(out["logits"].cpu().numpy()[:n], r.logits[rows], TOL_LOGIT, "logits")
     g_conf = out["conf"].cpu().numpy()
-    close(g_conf, r.conf.reshape(-1), TOL_CONF, "confidence")
+    close(g_conf[rows], r.conf.reshape(-1)[rows], TOL_CONF, "confidence")
     arg = out["arg"].cpu().numpy()
-    mism = (arg != r.arg.reshape(-1)) & ~r.logit_tie.reshape(-1)
-    assert not mism.any(), f"argmax differs at rows {np.nonzero(mism)[0][:10]} whose top-2 logit gap is not a near-tie"
+    mism = (arg[rows] != r.arg.reshape(-1)[rows]) & ~r.logit_tie.reshape(-1)[rows]
+    assert not mism.any(), f"argmax differs at rows {rows[np.nonzero(mism)[0][:10]]} whose top-2 logit gap is not a near-tie"
     g_tok = t.cpu().numpy()
     g_mask = m.cpu().numpy().view(np.uint32)
     flagged, _ = check_commit(tok, mask, gamma, mode, cfg.block, r.tokens, r.mask, r.near_tie, g_tok, g_mask,

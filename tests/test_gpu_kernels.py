@@ -76,8 +76,12 @@ def test_block_attention_vs_oracle(B, S, Hq, Hkv, D, T, stride):
 
 
 def test_block_attention_microbench_size_sampled():
-    """The full microbenchmark shape (B=64, T=8192, 32/8 heads x 128), checked
-    on sampled (sequence, kv head) pairs that the oracle computes one by one."""
+    """The full microbenchmark shape (B=64, T=8192, 32/8 heads x 128).  Every
+    (sequence, kv head) pair is checked against an fp32 torch statement of the
+    same attention on the device (TF32 off), and pairs spread over the
+    persistent schedule -- the first and last pairs, both neighbours of the
+    middle, and those at the ends of the CTAs' item lists -- against the
+    oracle, computed one pair at a time on the host."""
     from block_wise_masked_dd_b300.decoder import block_attention
     cfg = synth.ATTN_MICRO
     B, S, Hq, Hkv, D, T = cfg.batch, cfg.block, cfg.n_q_heads, cfg.n_kv_heads, cfg.head_dim, cfg.ctx_len
@@ -88,7 +92,30 @@ def test_block_attention_microbench_size_sampled():
     out = block_attention(qkv, kc, vc, T, B, S, Hq, Hkv, D)
     torch.cuda.synchronize()
     G = Hq // Hkv
-    for b, kvh in [(0, 0), (17, 5), (63, 7), (40, 2)]:
+    got_all = out.float().reshape(B, S, Hkv, G, D)
+    # every pair, fp32 on the device: one softmax over [context | block] keys
+    prev = torch.backends.cuda.matmul.allow_tf32
+    torch.backends.cuda.matmul.allow_tf32 = False
+    try:
+        x = qkv.float().reshape(B, S, Hq + 2 * Hkv, D)
+        worst = 0.0
+        for b0 in range(0, B, 8):
+            q = x[b0:b0 + 8, :, :Hq].reshape(-1, S, Hkv, G, D).permute(0, 2, 3, 1, 4)      # [b, kvh, g, i, d]
+            kb = x[b0:b0 + 8, :, Hq:Hq + Hkv].permute(0, 2, 1, 3)                           # [b, kvh, S, d]
+            vb = x[b0:b0 + 8, :, Hq + Hkv:].permute(0, 2, 1, 3)
+            keys = torch.cat([kc[b0:b0 + 8].float(), kb], dim=2)                           # [b, kvh, T+S, d]
+            vals = torch.cat([vc[b0:b0 + 8].float(), vb], dim=2)
+            sc = torch.einsum("bhgid,bhjd->bhgij", q, keys) / np.sqrt(D)
+            ref = torch.einsum("bhgij,bhjd->bhgid", torch.softmax(sc, dim=-1), vals)        # [b, kvh, g, i, d]
+            got = got_all[b0:b0 + 8].permute(0, 2, 3, 1, 4)
+            err = (got - ref).abs() - (TOL_ATTN + TOL_ATTN * ref.abs())
+            worst = max(worst, float(err.max()))
+        assert worst <= 0, f"attention outside tolerance by {worst} against the fp32 device statement"
+    finally:
+        torch.backends.cuda.matmul.allow_tf32 = prev
+    pairs = [0, 1, 255, 256, 443, 444, B * Hkv - 2, B * Hkv - 1]
+    for pair in pairs:
+        b, kvh = divmod(pair, Hkv)
         rows = qkv[b * S:(b + 1) * S].float().cpu().numpy()
         q = rows[:, :Hq * D].reshape(S, Hq, D)[:, kvh * G:(kvh + 1) * G]
         kb = rows[:, (Hq + kvh) * D:(Hq + kvh + 1) * D].reshape(S, 1, D)

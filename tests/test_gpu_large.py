@@ -11,7 +11,7 @@ import pytest
 
 import oracle
 import synth
-from tests.gpu_helpers import TOL_ATTN, TOL_CONF, TOL_LOGIT, check_commit, close, require_gpu, torch
+from tests.gpu_helpers import TOL_ATTN, TOL_CONF, TOL_LOGIT, check_commit, close, probe_rows, require_gpu, torch
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -52,17 +52,23 @@ class LargeProblem:
         out = self.dec.probe_step(t, m, gamma, mode, logits=logits)
         torch.cuda.synchronize()
         r = oracle.denoise_step(self.model, tok[sel], mask[sel], gamma, mode, keep_intermediates=True)
+        # probe activations come in the compacted order of the active sequences
+        order = {int(row): k for k, row in enumerate(probe_rows(self.dec, mask, cfg.block))}
+        act = np.array([row in order for row in rows])
+        prow = np.array([order[row] for row in rows[act]], np.int64)
         for l in range(cfg.n_layers):
-            got = join_split(out["attn_out"][l]).cpu().numpy()[rows]
-            close(got, r.attn_out[l], TOL_ATTN, f"attention output, layer {l}", rel_rms=1e-3)
-        close(join_split(out["hidden"]).cpu().numpy()[rows], r.hidden_final, TOL_LOGIT, "final hidden",
+            got = join_split(out["attn_out"][l]).cpu().numpy()[prow]
+            close(got, r.attn_out[l][act], TOL_ATTN, f"attention output, layer {l}", rel_rms=1e-3)
+        close(join_split(out["hidden"]).cpu().numpy()[prow], r.hidden_final[act], TOL_LOGIT, "final hidden",
               rel_rms=1e-3)
         if logits:
-            close(out["logits"].cpu().numpy()[rows], r.logits, TOL_LOGIT, "logits")
+            close(out["logits"].cpu().numpy()[prow], r.logits[act], TOL_LOGIT, "logits")
+        rows = rows[act]
+        r_conf, r_arg, r_tie = (r.conf.reshape(-1)[act], r.arg.reshape(-1)[act], r.logit_tie.reshape(-1)[act])
         g_conf = out["conf"].cpu().numpy()
-        close(g_conf[rows], r.conf.reshape(-1), TOL_CONF, "confidence")
+        close(g_conf[rows], r_conf, TOL_CONF, "confidence")
         arg = out["arg"].cpu().numpy()
-        mism = (arg[rows] != r.arg.reshape(-1)) & ~r.logit_tie.reshape(-1)
+        mism = (arg[rows] != r_arg) & ~r_tie
         assert not mism.any(), f"argmax differs at non-tie rows {rows[np.nonzero(mism)[0][:10]]}"
         g_tok = t.cpu().numpy()
         g_mask = m.cpu().numpy().view(np.uint32)
@@ -143,3 +149,37 @@ def test_large_graph_step_compacted_lm_head(large, masked_frac):
     g_tok, g_mask = t.cpu().numpy(), m.cpu().numpy().view(np.uint32)
     check_commit(tok[sel], mask[sel], 0.8, 0, cfg.block, r.tokens, r.mask, r.near_tie, g_tok[sel], g_mask[sel],
                  what="large graph step")
+
+
+def test_large_graph_step_with_finished_sequences(large):
+    """20 of the 32 sequences finished (among them one sampled): 12 active
+    sequences = 192 rows, so the linear layers skip their second 256-row
+    tile and the attention runs 12 sequences' work items."""
+    from tests.gpu_helpers import with_finished
+    cfg = large.cfg
+    finished = [b for b in range(cfg.batch) if b % 8 not in (0, 3, 7)]
+    assert 13 in finished and 0 not in finished and 31 not in finished
+    tok, mask = synth.make_tokens(cfg, seed=31, masked_frac=0.5)
+    tok, mask = with_finished(cfg, tok, mask, finished)
+    t = torch.from_numpy(tok.copy()).cuda()
+    m = torch.from_numpy(mask.view(np.int32).copy()).cuda()
+    large.dec.denoise_step(t, m, 0.8, 0)
+    torch.cuda.synchronize()
+    sel = large.sample
+    r = oracle.denoise_step(large.model, tok[sel], mask[sel], 0.8, 0)
+    g_tok, g_mask = t.cpu().numpy(), m.cpu().numpy().view(np.uint32)
+    check_commit(tok[sel], mask[sel], 0.8, 0, cfg.block, r.tokens, r.mask, r.near_tie, g_tok[sel], g_mask[sel],
+                 what="large compacted graph step")
+    assert (g_tok[finished] == tok[finished]).all() and (g_mask[finished] == 0).all()
+
+
+def test_large_compacted_and_uncompacted_decode_agree(large):
+    results = []
+    for compact in (True, False):
+        large.dec.compact_sequences = compact
+        tokens, steps = large.dec.decode_block(0.8)
+        torch.cuda.synchronize()
+        results.append((tokens.cpu().numpy(), steps))
+    large.dec.compact_sequences = True
+    (a, sa), (b, sb) = results
+    assert sa == sb and (a == b).all()
