@@ -97,12 +97,13 @@ bool make_map_q(CUtensorMap* m, const void* qkv, uint64_t rows, uint64_t ld, int
 
 bool make_map_q_stacked(CUtensorMap* m, const void* qkv, uint64_t rows, uint64_t ld, int Hq, int D, int G, int S) {
   auto fn = encode_fn();
-  if (!fn) return false;
-  cuuint64_t dims[4] = {(cuuint64_t)D, (cuuint64_t)Hq, 2, rows};
-  cuuint64_t strides[3] = {(cuuint64_t)D * 2, rows * ld * 2, ld * 2};
-  cuuint32_t box[4] = {64, (cuuint32_t)G, 2, (cuuint32_t)S};
-  cuuint32_t es[4] = {1, 1, 1, 1};
-  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(qkv), dims, strides, box, es,
+  if (!fn || G < 1 || 8 % G || rows % (8 / G) || S % (8 / G)) return false;
+  const uint64_t q8 = 8 / G;  // block positions per 8-query group
+  cuuint64_t dims[5] = {(cuuint64_t)D, (cuuint64_t)Hq, q8, 2, rows / q8};
+  cuuint64_t strides[4] = {(cuuint64_t)D * 2, ld * 2, rows * ld * 2, q8 * ld * 2};
+  cuuint32_t box[5] = {64, (cuuint32_t)G, (cuuint32_t)q8, 2, (cuuint32_t)(S / q8)};
+  cuuint32_t es[5] = {1, 1, 1, 1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 5, const_cast<void*>(qkv), dims, strides, box, es,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -283,7 +284,7 @@ int32_t* small_ptr(dd_ctx* c) { return at<int32_t>(c->ws, c->L.small); }
 
 // The stacked form of the tcgen05 context-attention kernel (head and
 // remainder rows of one M = 128 operand) for split activations.
-constexpr bool kStackedContextKernel = false;
+constexpr bool kStackedContextKernel = true;
 
 // Kinds of launches in one step (for the per-kernel profile).
 enum LaunchKind : int {

@@ -448,26 +448,27 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // Stacked form, for split activations (q as a bf16 head plus a bf16
 // remainder).  An M = 64 MMA occupies the tensor core as long as an M = 128
-// one, so instead of two M = 64 products per step (head and remainder) the
-// head and the remainder of every query row are two rows of one M = 128
-// operand, and their two product rows are added afterwards:
-//   S'[128][128 keys] = Q'[128][128] . K_tile^T   rows rho = i*2G + part*G + g
-//   O'[128][128 d]    = P'[128][128 keys] . V_tile rows as in S'
-// where part 0 holds the head and part 1 the remainder of query (i, g), and
-// P' row (i, 0, g) is the bf16 head and row (i, 1, g) the bf16 remainder of
-// that query's probabilities.  Q' comes from the q|k|v rows by one 4D TMA
-// box {64 dims, G heads, 2 parts, S positions} (the part dimension strides
-// from the head rows to the remainder rows).  With the 32x32b TMEM load,
-// thread rho holds row rho; the rows of one query sit G lanes apart in the
-// same warp, so one shuffle per value adds them: the part-0 thread keeps
-// the sum for keys (or dims) 0..63 and the part-1 thread for 64..127, and
-// the two carry the same running max and sum.  Per 128-key tile this is 16
-// MMAs instead of 32.
+// one, so instead of two M = 64 products per K step (head and remainder) the
+// head and the remainder rows of the 64 queries form one M = 128 operand and
+// their product rows are added afterwards:
+//   S'[128][128 keys] = Q'[128][128] . K_tile^T      O'[128][128 d] = P'[128][128 keys] . V_tile
+// Row order: 16-row groups, each holding 8 consecutive queries (query order
+// i * G + g) as 8 head rows then the same queries' 8 remainder rows, so row
+// 16k + j is the head and 16k + 8 + j the remainder of query 8k + j.  Q'
+// comes from the q|k|v rows as one 5D TMA box {64 dims, G heads, 8/G
+// positions, 2 parts, S*G/8 position pairs} (the part dimension strides from
+// the head rows to the remainder rows); P' is written in the same order.
+// The 16x256b TMEM load hands a thread the rows r and r + 8 of its lane
+// group, i.e. the head and the remainder of one query, so the sum is one
+// in-thread add, and after it every register holds what the M = 64 form's
+// load would: rows q and q + 8 of the query order, 32 columns each.  Per
+// 128-key tile this is 16 MMAs instead of 32.
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_ctx_stk(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
                    const __grid_constant__ CUtensorMap map_q2, const AttnArgs a, int n_ctx, int n_items_max) {
-  static_assert(G >= 1 && G <= 16 && (G & (G - 1)) == 0, "G must be a power of two <= 16");
+  static_assert(G == 2 || G == 4 || G == 8, "G must be 2, 4 or 8");
+  constexpr int Q8 = 8 / G;         // block positions per 8-query group
   constexpr int kAtom = 128 * 128;  // [128 rows][64 cols] bf16, 128-byte swizzle: 16 KB
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -573,8 +574,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!mbar_wait_bounded(&qempty[qb], ((it >> 1) & 1) ^ 1, a.timeout_ns, abort_flag, a.status)) break;
         uint8_t* q = smem + kOffQ + qb * 2 * kAtom;
         mbar_arrive_expect_tx(&qfull[qb], 2 * kAtom);
-        tma_load_4d(q, &map_q2, &qfull[qb], 0, kvh * G, 0, b * S);
-        tma_load_4d(q + kAtom, &map_q2, &qfull[qb], 64, kvh * G, 0, b * S);
+        tma_load_5d(q, &map_q2, &qfull[qb], 0, kvh * G, 0, 0, b * S / Q8);
+        tma_load_5d(q + kAtom, &map_q2, &qfull[qb], 64, kvh * G, 0, 0, b * S / Q8);
         const int z = plane(b, kvh);
         for (int t = 0; t < nt && ok; ++t, ++g)
           if (g >= pre) ok = load_kv(g, (tile0 + t) * kKT, z);
@@ -641,29 +642,37 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ------------------------------------------------------------- softmax
-    const int q4 = warp & 3;                        // TMEM lane quarter
-    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
-    const int rho = 32 * q4 + lane;                 // stacked row = TMEM lane
-    const int part = (rho / G) & 1;                 // 0: head row, 1: remainder row
-    const int qi = rho / (2 * G), qg = rho % G;     // query: block position, head in the group
-    const int pr = qg * S + qi;                     // partial row (order g * S + i)
-    const int col0 = 64 * part;                     // the keys (and dims) this thread sums
-    const int rho_h = rho & ~G, rho_r = rho | G;    // P' rows of this query
+    const int q4 = warp & 3;                         // TMEM lane quarter: rows 32*q4 .. 32*q4 + 31
+    const uint32_t lane_a = (uint32_t)(q4 * 32) << 16;        // 16-row group 2*q4
+    const uint32_t lane_b = (uint32_t)(q4 * 32 + 16) << 16;   // 16-row group 2*q4 + 1
+    // the two queries (order i * G + g) whose rows this thread holds, as in
+    // the M = 64 form: r0 from group 2*q4, r1 = r0 + 8 from group 2*q4 + 1
+    const int r0 = 16 * q4 + (lane >> 2);
+    const int r1 = r0 + 8;
+    const int cq = 2 * (lane & 3);                   // column offset inside each 8-column block
     const float c = a.scale_log2;
-    // sum of this row and its partner's (G lanes apart) over this thread's
-    // 64 columns of a 128-column TMEM row block
-    auto load_pair_sum = [&](uint32_t taddr, float (&out)[64]) {
+    // stmatrix row addresses of P': matrix mi = lane/8 holds rows 32*q4 + 16*(mi&1) + lane%8 (heads;
+    // the remainders 8 rows further) and columns +8*(mi>>1) of each 16-key group
+    const int st_row = 32 * q4 + 16 * ((lane >> 3) & 1) + (lane & 7);
+    const int st_colh = 8 * (lane >> 4);
+    const int pr0 = (r0 % G) * S + r0 / G;           // partial rows in the order g * S + i
+    const int pr1 = (r1 % G) * S + r1 / G;
+    // the head + remainder sums of a 128-column TMEM block in the M = 64
+    // fragment order: register 4k + e holds row r0 (e < 2) or r1 (e >= 2),
+    // column 8k + cq + (e & 1)
+    auto load_sum = [&](uint32_t taddr, float (&v)[64]) {
+      float h[64];
+      tmem_ld_frag(taddr + lane_a, h);  // rows: group 2q4 head (e < 2) and remainder (e >= 2)
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        float lo[32], hi[32];
-        tmem_ld32(taddr + 32 * h, lo);        // columns 32h ..
-        tmem_ld32(taddr + 64 + 32 * h, hi);   // columns 64 + 32h ..
+      for (int k = 0; k < 16; ++k) {
+        v[4 * k] = h[4 * k] + h[4 * k + 2];
+        v[4 * k + 1] = h[4 * k + 1] + h[4 * k + 3];
+      }
+      tmem_ld_frag(taddr + lane_b, h);  // group 2q4 + 1
 #pragma unroll
-        for (int j = 0; j < 32; ++j) {
-          const float mine = part ? hi[j] : lo[j];
-          const float send = part ? lo[j] : hi[j];
-          out[32 * h + j] = mine + __shfl_xor_sync(0xffffffffu, send, G);
-        }
+      for (int k = 0; k < 16; ++k) {
+        v[4 * k + 2] = h[4 * k] + h[4 * k + 2];
+        v[4 * k + 3] = h[4 * k + 1] + h[4 * k + 3];
       }
     };
     bool ok = true;
@@ -671,11 +680,12 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       int split, kvh, b, tile0, nt;
       item(w, split, kvh, b, tile0, nt);
-      float o[64];                                  // O of this query, dims col0 .. col0 + 63
+      float o[64];                                  // O rows r0/r1 in fragment order
 #pragma unroll
       for (int j = 0; j < 64; ++j) o[j] = 0.f;
-      float m = -INFINITY, l = 0.f, al = 0.f;      // al: rescale of the previous tile
-      auto consume_o = [&](int u, float alpha) {
+      float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+      float al0 = 0.f, al1 = 0.f;                   // rescale of the previous tile
+      auto consume_o = [&](int u, float a0, float a1) {
         const int s = u & 1;
         bool wt = true;
         if (lane == 0) wt = mbar_wait_bounded(&ofull[s], (u >> 1) & 1, a.timeout_ns, abort_flag, a.status);
@@ -683,12 +693,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wt) return false;
         tc_fence_after();
         float pv[64];
-        load_pair_sum(t_o + s * kD + lane_off, pv);
+        load_sum(t_o + s * kD, pv);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&ofree[s]);
 #pragma unroll
-        for (int j = 0; j < 64; ++j) o[j] = fmaf(o[j], alpha, pv[j]);
+        for (int j = 0; j < 64; ++j) o[j] = fmaf(o[j], (j & 2) ? a1 : a0, pv[j]);
         return true;
       };
       for (int t = 0; t < nt; ++t, ++g) {
@@ -699,63 +709,89 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (!wt) { ok = false; break; }
         tc_fence_after();
         float v[64];
-        load_pair_sum(t_s + s * kKT + lane_off, v);
+        load_sum(t_s + s * kKT, v);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&sfree[s]);
-        const int kbase = (tile0 + t) * kKT + col0;
-        if ((tile0 + t) * kKT + kKT > T) {  // tail tile: keys >= T do not exist
+        const int kbase = (tile0 + t) * kKT;
+        if (kbase + kKT > T) {  // tail tile: keys >= T do not exist
 #pragma unroll
-          for (int j = 0; j < 64; ++j)
-            if (kbase + j >= T) v[j] = -INFINITY;
+          for (int j = 0; j < 64; ++j) {
+            const int key = kbase + 8 * (j >> 2) + cq + (j & 1);
+            if (key >= T) v[j] = -INFINITY;
+          }
         }
-        float mx = -INFINITY;
+        float mx0 = -INFINITY, mx1 = -INFINITY;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) mx = fmaxf(mx, v[j]);
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, G));
+        for (int j = 0; j < 64; j += 4) {
+          mx0 = fmaxf(mx0, fmaxf(v[j], v[j + 1]));
+          mx1 = fmaxf(mx1, fmaxf(v[j + 2], v[j + 3]));
+        }
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 1));
+        mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
+        mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
         // running max in base-2 units (scores times c)
-        const float mn = fmaxf(m, mx * c);
-        const float alpha = m == -INFINITY ? 0.f : ex2(m - mn);
-        m = mn;
-        float ssum = 0.f;
+        const float mn0 = fmaxf(m0, mx0 * c), mn1 = fmaxf(m1, mx1 * c);
+        const float a0 = m0 == -INFINITY ? 0.f : ex2(m0 - mn0);
+        const float a1 = m1 == -INFINITY ? 0.f : ex2(m1 - mn1);
+        m0 = mn0;
+        m1 = mn1;
+        float s0 = 0.f, s1 = 0.f;
 #pragma unroll
-        for (int j = 0; j < 64; ++j) {
-          v[j] = ex2(fmaf(v[j], c, -mn));
-          ssum += v[j];
+        for (int j = 0; j < 64; j += 4) {
+          v[j] = ex2(fmaf(v[j], c, -mn0));
+          v[j + 1] = ex2(fmaf(v[j + 1], c, -mn0));
+          v[j + 2] = ex2(fmaf(v[j + 2], c, -mn1));
+          v[j + 3] = ex2(fmaf(v[j + 3], c, -mn1));
+          s0 += v[j] + v[j + 1];
+          s1 += v[j + 2] + v[j + 3];
         }
-        ssum += __shfl_xor_sync(0xffffffffu, ssum, G);
-        l = l * alpha + ssum;
-        // P' rows (head, remainder) of this query, this thread's 64 keys
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+        s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+        l0 = l0 * a0 + s0;
+        l1 = l1 * a1 + s1;
+        // P' (heads, and remainders 8 rows further) once the previous PV is done
         if (g >= 1) {
           bool pw = true;
           if (lane == 0) pw = mbar_wait_bounded(pfree, (g - 1) & 1, a.timeout_ns, abort_flag, a.status);
           pw = __shfl_sync(0xffffffffu, pw ? 1 : 0, 0) != 0;
           if (!pw) { ok = false; break; }
         }
-        uint8_t* pb = smem + kOffPh;
+        const uint32_t pbase = smem_u32(smem + kOffPh);
 #pragma unroll
-        for (int cc = 0; cc < 8; ++cc) {
-          uint4 h, r;
-          split_bf16(v[8 * cc + 0], v[8 * cc + 1], h.x, r.x);
-          split_bf16(v[8 * cc + 2], v[8 * cc + 3], h.y, r.y);
-          split_bf16(v[8 * cc + 4], v[8 * cc + 5], h.z, r.z);
-          split_bf16(v[8 * cc + 6], v[8 * cc + 7], h.w, r.w);
-          *reinterpret_cast<uint4*>(pb + swz(128, rho_h, col0 + 8 * cc)) = h;
-          *reinterpret_cast<uint4*>(pb + swz(128, rho_r, col0 + 8 * cc)) = r;
+        for (int gg = 0; gg < kKT / 16; ++gg) {
+          // 16-key group gg: fragment reps 2gg (keys 16gg..16gg+7) and 2gg+1 (16gg+8..)
+          uint32_t h0, l0p, h1, l1p, h2, l2p, h3, l3p;
+          split_bf16(v[8 * gg + 0], v[8 * gg + 1], h0, l0p);   // query r0, keys 16gg + cq
+          split_bf16(v[8 * gg + 2], v[8 * gg + 3], h1, l1p);   // query r1, keys 16gg + cq
+          split_bf16(v[8 * gg + 4], v[8 * gg + 5], h2, l2p);   // query r0, keys 16gg + 8 + cq
+          split_bf16(v[8 * gg + 6], v[8 * gg + 7], h3, l3p);   // query r1, keys 16gg + 8 + cq
+          stmatrix_x4(pbase + swz(128, st_row, 16 * gg + st_colh), h0, h1, h2, h3);
+          stmatrix_x4(pbase + swz(128, st_row + 8, 16 * gg + st_colh), l0p, l1p, l2p, l3p);
         }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(pfull);
-        if (t >= 1 && !consume_o(g - 1, al)) { ok = false; break; }
-        al = alpha;
+        if (t >= 1 && !consume_o(g - 1, al0, al1)) { ok = false; break; }
+        al0 = a0;
+        al1 = a1;
       }
-      if (ok && nt >= 1) ok = consume_o(g - 1, al);
+      if (ok && nt >= 1) ok = consume_o(g - 1, al0, al1);
       // partial slot `split`: o (unnormalised, [q][d]), (m, l) per q
       const long long prow = ((long long)(b * a.Hkv + kvh) * n_ctx + split) * kNQ;
-      float* dst = a.part_o + (prow + pr) * kD + col0;
 #pragma unroll
-      for (int j = 0; j < 64; j += 4) *reinterpret_cast<float4*>(dst + j) = make_float4(o[j], o[j + 1], o[j + 2], o[j + 3]);
-      if (part == 0) a.part_ml[prow + pr] = make_float2(m, l);
+      for (int rep = 0; rep < 16; ++rep) {
+        const int d = 8 * rep + cq;
+        *reinterpret_cast<float2*>(a.part_o + (prow + pr0) * kD + d) = make_float2(o[4 * rep], o[4 * rep + 1]);
+        *reinterpret_cast<float2*>(a.part_o + (prow + pr1) * kD + d) = make_float2(o[4 * rep + 2], o[4 * rep + 3]);
+      }
+      if ((lane & 3) == 0) {
+        a.part_ml[prow + pr0] = make_float2(m0, l0);
+        a.part_ml[prow + pr1] = make_float2(m1, l1);
+      }
     }
   }
 
@@ -789,9 +825,7 @@ int attention_tc_splits(int B, int Hkv, int max_ctx) {
 
 int attention_tc_smem_bytes() { return kSmemBytes; }
 
-bool attention_tc_stacked_supported(int G, int S) {
-  return (G == 1 || G == 2 || G == 4 || G == 8 || G == 16) && G * S == kNQ;
-}
+bool attention_tc_stacked_supported(int G, int S) { return (G == 2 || G == 4 || G == 8) && G * S == kNQ; }
 
 cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx, const CUtensorMap& map_k128,
                                 const CUtensorMap& map_v128, const CUtensorMap& map_q, cudaStream_t st,
@@ -800,11 +834,9 @@ cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx, const CUtensorMap&
   const int grid = items < kNumSMs ? items : kNumSMs;
   if (a.split && map_q2 && attention_tc_stacked_supported(a.G, a.S)) {
     switch (a.G) {
-      case 1: return launch_k(k_attn_ctx_stk<1>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, *map_q2, a, n_ctx, items);
       case 2: return launch_k(k_attn_ctx_stk<2>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, *map_q2, a, n_ctx, items);
       case 4: return launch_k(k_attn_ctx_stk<4>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, *map_q2, a, n_ctx, items);
-      case 8: return launch_k(k_attn_ctx_stk<8>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, *map_q2, a, n_ctx, items);
-      default: return launch_k(k_attn_ctx_stk<16>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, *map_q2, a, n_ctx, items);
+      default: return launch_k(k_attn_ctx_stk<8>, grid, kThreads, kSmemBytes, st, map_k128, map_v128, *map_q2, a, n_ctx, items);
     }
   }
   if (a.split)
@@ -814,9 +846,8 @@ cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx, const CUtensorMap&
 
 cudaError_t prepare_attention_tc_kernels() {
   const void* fns[] = {(const void*)k_attn_ctx_tc<true>, (const void*)k_attn_ctx_tc<false>,
-                       (const void*)k_attn_ctx_stk<1>,   (const void*)k_attn_ctx_stk<2>,
-                       (const void*)k_attn_ctx_stk<4>,   (const void*)k_attn_ctx_stk<8>,
-                       (const void*)k_attn_ctx_stk<16>};
+                       (const void*)k_attn_ctx_stk<2>,   (const void*)k_attn_ctx_stk<4>,
+                       (const void*)k_attn_ctx_stk<8>};
   cudaError_t e = cudaSuccess;
   for (const void* f : fns)
     if (e == cudaSuccess) e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);

@@ -275,10 +275,11 @@ bool make_map_3d(CUtensorMap* m, const void* base, uint64_t planes, uint64_t row
 // G query heads of a kv head at S consecutive rows, in row order i * G + g.
 bool make_map_q(CUtensorMap* m, const void* qkv, uint64_t rows, uint64_t ld, int Hq, int D, int G, int S);
 // The query heads of a split q|k|v buffer (bf16 heads in rows [0, rows),
-// remainders in rows [rows, 2 rows)) as a 4D map {D, Hq, 2 parts, rows}, box
-// {64, G, 2, S}: one box holds, for S consecutive rows, the G query heads of
-// a kv head as the head then the remainder of each row (row order
-// (i * 2 + part) * G + g).
+// remainders in rows [rows, 2 rows)) as a 5D map {D, Hq, 8/G positions,
+// 2 parts, rows/(8/G)}, box {64, G, 8/G, 2, S*G/8}: one box holds, for S
+// consecutive rows, the G query heads of a kv head as 16-row groups of 8
+// queries (order i * G + g) -- their 8 head rows, then their 8 remainder rows.
+// G must divide 8.
 bool make_map_q_stacked(CUtensorMap* m, const void* qkv, uint64_t rows, uint64_t ld, int Hq, int D, int G, int S);
 
 }  // namespace dd
