@@ -46,29 +46,29 @@ def test_tiny_state_synced_decode(tiny, gamma, mode):
     assert (tok < tiny.cfg.vocab).all()
 
 
-def test_tiny_decode_block_matches_oracle(tiny):
+def _free_running_vs_oracle(p, gamma=0.8, mode=0):
     """The free-running decode (the device-side loop graph) against the
     oracle's free-running decode.  Where the two trajectories part, the step
     graph replays the CUDA trajectory one step at a time from the same start
-    (it must reproduce the loop's result) and the first step at which the two
-    states differ must differ only at positions the oracle flags there."""
-    cfg = tiny.cfg
-    tokens, steps = tiny.dec.decode_block(0.8)
+    (it must reproduce the loop's result), and the first step at which the
+    two states differ must differ only at positions the oracle flags there."""
+    cfg = p.cfg
+    tokens, steps = p.dec.decode_block(gamma, mode)
     torch.cuda.synchronize()
-    want, w_steps, _ = oracle.decode_block(tiny.model, 0.8)
+    want, w_steps, _ = oracle.decode_block(p.model, gamma, mode)
     got = tokens.cpu().numpy()
     if (got == want).all():
         assert steps == w_steps
         return
-    tok, mask = tiny.start_state()
+    tok, mask = p.start_state()
     for step in range(4 * cfg.block):
-        t, m = tiny.gpu_state(tok, mask)
-        tiny.dec.denoise_step(t, m, 0.8, 0)
+        t, m = p.gpu_state(tok, mask)
+        p.dec.denoise_step(t, m, gamma, mode)
         torch.cuda.synchronize()
         g_tok, g_mask = t.cpu().numpy(), m.cpu().numpy().view(np.uint32)
-        r = oracle.denoise_step(tiny.model, tok, mask, 0.8, 0)
+        r = oracle.denoise_step(p.model, tok, mask, gamma, mode)
         if not ((g_tok == r.tokens).all() and (g_mask == r.mask).all()):
-            check_commit(tok, mask, 0.8, 0, cfg.block, r.tokens, r.mask, r.near_tie, g_tok, g_mask,
+            check_commit(tok, mask, gamma, mode, cfg.block, r.tokens, r.mask, r.near_tie, g_tok, g_mask,
                          what=f"first divergent step {step}")
             assert r.near_tie.any()
             break
@@ -76,11 +76,22 @@ def test_tiny_decode_block_matches_oracle(tiny):
         assert mask.max(), "the trajectories agreed to the end but the final ids differ"
     # the step-by-step CUDA trajectory reproduces the loop graph's result
     while mask.max():
-        t, m = tiny.gpu_state(tok, mask)
-        tiny.dec.denoise_step(t, m, 0.8, 0)
+        t, m = p.gpu_state(tok, mask)
+        p.dec.denoise_step(t, m, gamma, mode)
         torch.cuda.synchronize()
         tok, mask = t.cpu().numpy(), m.cpu().numpy().view(np.uint32)
     assert (tok == got).all()
+
+
+def test_tiny_decode_block_matches_oracle(tiny):
+    _free_running_vs_oracle(tiny)
+
+
+@pytest.mark.parametrize("gamma", [0.5, 0.8])
+def test_small_decode_block_matches_oracle(small, gamma):
+    """The product path (the loop graph, with active-sequence compaction)
+    free-running on the small workload, 8 sequences."""
+    _free_running_vs_oracle(small, gamma)
 
 
 def test_small_first_step(small):
