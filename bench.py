@@ -362,25 +362,38 @@ def algorithmic_bytes(cfg, kind, ctx_len, n_act=None):
     return None
 
 
-def mlp_gemm_rates(cfg, kernels, hbm_peak, tc_sust, peak_src):
+def algorithmic_flops(cfg, kind, n_act=None):
+    """2*R*K*N of one launch of a linear layer or the LM head over the rows of
+    `n_act` active sequences (all of the batch by default); None for other
+    kinds."""
+    n_act = cfg.batch if n_act is None else n_act
+    R, H, F, V = n_act * cfg.block, cfg.hidden, cfg.mlp, cfg.vocab
+    HqD = cfg.n_q_heads * cfg.head_dim
+    kn = {"gemm_qkv": (H, cfg.qkv_width), "gemm_o": (HqD, H), "gemm_gate_up": (H, 2 * F), "gemm_down": (F, H),
+          "lm_head_select": (H, V)}.get(kind)
+    return None if kn is None else 2.0 * R * kn[0] * kn[1]
+
+
+def mlp_gemm_rates(cfg, prof, hbm_peak, tc_sust, peak_src):
     """The MLP GEMMs (gate|up, down) of the step from the per-kind profile: HBM
     rate of their algorithmic bytes, and tensor rate of their algorithmic
-    FLOPs (2*R*K*N) and of the FLOPs the tensor cores execute (twice that: the
-    activation operand is a bf16 head plus a bf16 remainder), against the
-    sustained bf16 peak (kernels timed inside a long step)."""
-    R, H, F = cfg.rows, cfg.hidden, cfg.mlp
+    FLOPs (2*R*K*N over the active rows of each launch) and of the FLOPs the
+    tensor cores execute (twice that: the activation operand is a bf16 head
+    plus a bf16 remainder), against the sustained bf16 peak (kernels timed
+    inside a long step)."""
     out = {}
-    for kind, n, k in (("gemm_gate_up", 2 * F, H), ("gemm_down", H, F)):
-        if kind not in kernels:
+    for kind in ("gemm_gate_up", "gemm_down"):
+        if kind not in prof:
             continue
-        us = kernels[kind]["us_per_launch"]
-        flops = 2.0 * R * k * n
-        tf = flops / (us * 1e-6) / 1e12
-        gbs = algorithmic_bytes(cfg, kind, 0) / (us * 1e-6) / 1e9
-        out[kind] = {"us_per_launch": us, "hbm_GBps": gbs, "hbm_frac": gbs / hbm_peak,
+        ms, n, nbytes, flops = prof[kind][:4]
+        sec = ms * 1e-3
+        tf = flops / sec / 1e12
+        gbs = nbytes / sec / 1e9
+        out[kind] = {"us_per_launch": 1e3 * ms / n, "hbm_GBps": gbs, "hbm_frac": gbs / hbm_peak,
                      "tflops_algorithmic": tf, "tflops_executed": 2 * tf, "tensor_peak_tflops": tc_sust,
                      "tensor_frac_algorithmic": tf / tc_sust, "tensor_frac_executed": 2 * tf / tc_sust,
-                     "peak_source": peak_src + " (sustained bf16)"}
+                     "peak_source": peak_src + " (sustained bf16)",
+                     "rows_note": "FLOPs and bytes count the active sequences' rows of each launch"}
     return out
 
 
@@ -574,11 +587,13 @@ def measure_workload(args, cfg, dev, world, rank, local, peaks, steps, warmup, f
         actives.append(n_act)
         for kind, msk in B.dd_profile_step(dec.ctx, t_.data_ptr(), m_.data_ptr(), args.gamma, mode,
                                            stream=stream.cuda_stream):
-            p = prof.setdefault(kind, [0.0, 0, 0.0])
+            p = prof.setdefault(kind, [0.0, 0, 0.0, 0.0])
             p[0] += msk
             p[1] += 1
             nb = algorithmic_bytes(cfg, kind, T0, n_act)
             p[2] += nb if nb is not None else float("nan")
+            nf = algorithmic_flops(cfg, kind, n_act)
+            p[3] += nf if nf is not None else float("nan")
         nprof += 1
         words = mask_words()
         now = sum(bin(w_).count("1") for w_ in words)
@@ -607,7 +622,7 @@ def measure_workload(args, cfg, dev, world, rank, local, peaks, steps, warmup, f
                  "step_roofline": step_roofline(cfg, T0, hbm_peak, ms_max / steps, timed_denoise / max(steps, 1),
                                                 peak_src, active_frac)})
     if full:
-        line["mlp_gemms"] = mlp_gemm_rates(cfg, kernels, hbm_peak, tc_sust, peak_src)
+        line["mlp_gemms"] = mlp_gemm_rates(cfg, prof, hbm_peak, tc_sust, peak_src)
 
     # --------------------- CPU oracle: baseline rate and near-tie sample
     if model is not None:

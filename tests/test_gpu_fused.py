@@ -93,6 +93,11 @@ def test_option_errors():
         B.dd_get_option(p.dec.ctx, 77)
     with pytest.raises(B.DDError):
         B.dd_set_option(p.dec.ctx, B.DD_OPT_FUSED_SPLITS["qkv"], 4)
+    assert B.dd_get_option(p.dec.ctx, B.DD_OPT_COMPACT_SEQUENCES) == 1     # on by default
+    with pytest.raises(B.DDError):
+        B.dd_set_option(p.dec.ctx, B.DD_OPT_COMPACT_SEQUENCES, 2)
+    B.dd_set_option(p.dec.ctx, B.DD_OPT_COMPACT_SEQUENCES, 0)
+    assert B.dd_get_option(p.dec.ctx, B.DD_OPT_COMPACT_SEQUENCES) == 0
     p.dec.close()
 
 
