@@ -391,6 +391,7 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
     a.status = status;
     a.timeout_ns = c->timeout_ns;
     a.cmp = cmp;
+    a.max_pair_splits = cf.batch * cf.n_kv_heads * L.p_attn.n_splits;
     DD_CUDA(dd::launch_attention(L.p_attn, a, c->m_kc, c->m_vc, c->m_kc128, c->m_vc128, c->m_q, st,
                                  c->have_q2 ? &c->m_q2 : nullptr));
     mk(kKAttention);
@@ -1071,6 +1072,7 @@ dd_status dd_block_attention(const dd_attn_problem* p, void* stream) {
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)p->head_dim);
   a.status = small + 1;
   a.timeout_ns = dd::kDefaultTimeoutNs;
+  a.max_pair_splits = p->batch * p->n_kv_heads * plan.n_splits;
   CUtensorMap mq;
   if (!dd::make_map_q(&mq, p->qkv, (uint64_t)p->batch * p->block, a.ld_qkv, p->n_q_heads, p->head_dim, a.G, p->block))
     return fail(DD_ERR_CUDA, "tensor map encoding failed for qkv");

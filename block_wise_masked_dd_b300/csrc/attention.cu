@@ -392,13 +392,14 @@ __global__ void k_attn_combine(const AttnArgs a, int n_splits) {
 // One CTA per (sequence, kv head); warp w takes query rows 16w .. 16w + 15
 // (row r = g * S + i) and keeps them in the m16n8 fragment layout throughout.
 template <int D, bool SPLIT>
-__global__ void __launch_bounds__(128) k_attn_merge_block(const AttnArgs a, int n_ctx) {
+__global__ void __launch_bounds__(128) k_attn_merge_block(const AttnArgs a, int n_ctx_plan) {
   constexpr int kBlkB = kKTB * D * 2;
   __shared__ __align__(128) uint8_t blk[(SPLIT ? 4 : 2) * kBlkB];  // k, v (, k_lo, v_lo)
   pdl_wait();  // q|k|v and the context partials come from the preceding kernels
   pdl_launch_dependents();
   const int kvh = blockIdx.x % a.Hkv, b = blockIdx.x / a.Hkv;
   if (a.cmp && b >= a.cmp[1]) return;  // not an active sequence
+  const int n_ctx = attn_launch_splits(a, n_ctx_plan, *a.ctx_len);  // as the context kernel chose
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows = a.G * a.S;
   const int R = a.B * a.S;
@@ -526,7 +527,7 @@ __global__ void __launch_bounds__(128) k_attn_merge_block(const AttnArgs a, int 
 constexpr int kMergeBatch = 4;  // context partials per row held in registers
 
 template <int D>
-__global__ void __launch_bounds__(256) k_attn_merge_rows(const AttnArgs a, int n_ctx) {
+__global__ void __launch_bounds__(256) k_attn_merge_rows(const AttnArgs a, int n_ctx_plan) {
   constexpr int P = D / 32;      // output dims per lane
   constexpr int H2 = D / 2;      // dims per half dot product
   constexpr int KS = D + 8;      // padded row stride of the staged K (floats)
@@ -543,6 +544,7 @@ __global__ void __launch_bounds__(256) k_attn_merge_rows(const AttnArgs a, int n
   const int nq = min(8, rows - r0);
   const int kvh = bk % a.Hkv, b = bk / a.Hkv;
   if (a.cmp && b >= a.cmp[1]) return;  // not an active sequence
+  const int n_ctx = attn_launch_splits(a, n_ctx_plan, *a.ctx_len);  // as the context kernel chose
   const long long R = (long long)a.B * S;
   const long long lo = a.split ? R * a.ld_qkv : 0;
   const __nv_bfloat16* qkv = reinterpret_cast<const __nv_bfloat16*>(a.qkv);

@@ -111,7 +111,7 @@ __device__ __forceinline__ float ex2(float x) {
 template <bool SPLITQ>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_ctx_tc(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                  const __grid_constant__ CUtensorMap map_q, const AttnArgs a, int n_ctx, int n_items_max) {
+                  const __grid_constant__ CUtensorMap map_q, const AttnArgs a, int n_ctx_plan, int n_items_max) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kOffBar);
@@ -136,6 +136,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   // With active-sequence compaction the pairs are those of the active
   // sequences; the record was written by the step's first kernel, at least
   // three launches upstream, so it is complete before this kernel starts.
+  const int n_ctx = attn_launch_splits(a, n_ctx_plan, T);
   const int n_items = a.cmp ? a.cmp[1] * a.Hkv * n_ctx : n_items_max;
   const int ntiles_all = (T + kKT - 1) / kKT;
   const int per = (ntiles_all + n_ctx - 1) / n_ctx;
@@ -466,7 +467,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
     k_attn_ctx_stk(const __grid_constant__ CUtensorMap map_k, const __grid_constant__ CUtensorMap map_v,
-                   const __grid_constant__ CUtensorMap map_q2, const AttnArgs a, int n_ctx, int n_items_max) {
+                   const __grid_constant__ CUtensorMap map_q2, const AttnArgs a, int n_ctx_plan, int n_items_max) {
   static_assert(G == 2 || G == 4 || G == 8, "G must be 2, 4 or 8");
   constexpr int Q8 = 8 / G;         // block positions per 8-query group
   constexpr int kAtom = 128 * 128;  // [128 rows][64 cols] bf16, 128-byte swizzle: 16 KB
@@ -494,6 +495,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = *a.ctx_len;
   // the active sequences' record is written by the step's first kernel, at
   // least three launches upstream, so it is complete before this kernel starts
+  const int n_ctx = attn_launch_splits(a, n_ctx_plan, T);
   const int n_items = a.cmp ? a.cmp[1] * a.Hkv * n_ctx : n_items_max;
   const int ntiles_all = (T + kKT - 1) / kKT;
   const int per = (ntiles_all + n_ctx - 1) / n_ctx;
@@ -807,20 +809,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 bool attention_tc_supported(int D, int rows) { return D == kD && rows == kNQ; }
 
 int attention_tc_splits(int B, int Hkv, int max_ctx) {
-  const int pairs = B * Hkv;
-  const int ntiles = (max_ctx + kKT - 1) / kKT;
-  if (ntiles <= 0) return 1;
-  // Persistent CTAs (one per SM) walk pairs x splits items; the busiest CTA
-  // takes ceil(items / SMs) items of ceil(tiles / splits) tiles each, plus
-  // about one tile's worth per item for its partial write.
-  int best = 1;
-  long long best_cost = -1;
-  for (int s = 1; s <= 32 && s <= ntiles; ++s) {
-    const long long per_cta = ((long long)pairs * s + kNumSMs - 1) / kNumSMs;
-    const long long cost = per_cta * ((ntiles + s - 1) / s + 1) * 64 + s;
-    if (best_cost < 0 || cost < best_cost) { best_cost = cost; best = s; }
-  }
-  return best;
+  return attn_ctx_splits(B * Hkv, (max_ctx + kKT - 1) / kKT, 32);
 }
 
 int attention_tc_smem_bytes() { return kSmemBytes; }

@@ -154,9 +154,42 @@ struct AttnArgs {
   // rows of qkv/out and the partials are those of the cmp[1] active
   // sequences, compacted; the context cache of compacted sequence k is that
   // of sequence cmp[2 + k]; (sequence, kv head) pairs past the active ones do
-  // nothing.
+  // nothing.  With it the tcgen05 path also chooses its context splits on the
+  // device, per launch, for the active pairs (attn_ctx_splits), within the
+  // partial slots the workspace holds (max_pair_splits = pairs x splits).
   const int* cmp;
+  int max_pair_splits;
 };
+
+// Context splits for `pairs` (sequence, kv head) pairs over `ntiles` 128-key
+// tiles: persistent CTAs (one per SM) walk pairs x splits items; the busiest
+// takes ceil(items / SMs) items of ceil(tiles / splits) tiles each, plus about
+// one tile's worth per item for its partial write.  At most max_splits (and
+// 32, and one tile per split).
+__host__ __device__ inline int attn_ctx_splits(int pairs, int ntiles, int max_splits) {
+  if (ntiles <= 0 || pairs <= 0) return 1;
+  int lim = ntiles < 32 ? ntiles : 32;
+  if (max_splits < lim) lim = max_splits < 1 ? 1 : max_splits;
+  int best = 1;
+  long long best_cost = -1;
+  for (int s = 1; s <= lim; ++s) {
+    const long long per_cta = ((long long)pairs * s + kNumSMs - 1) / kNumSMs;
+    const long long cost = per_cta * ((ntiles + s - 1) / s + 1) * 64 + s;
+    if (best_cost < 0 || cost < best_cost) {
+      best_cost = cost;
+      best = s;
+    }
+  }
+  return best;
+}
+
+// The context splits a tcgen05-path launch uses: the plan's, or with the
+// compaction record the device-side choice for the active pairs.
+__host__ __device__ inline int attn_launch_splits(const AttnArgs& a, int n_ctx_plan, int T) {
+  if (!a.cmp) return n_ctx_plan;
+  const int pairs = a.cmp[1] * a.Hkv;
+  return attn_ctx_splits(pairs, (T + 127) / 128, pairs > 0 ? a.max_pair_splits / pairs : 1);
+}
 
 AttnPlan plan_attention(int B, int S, int Hq, int Hkv, int D, int max_ctx, int allow_tc = 1);
 size_t attention_partial_bytes(const AttnPlan& p, int B, int Hkv);

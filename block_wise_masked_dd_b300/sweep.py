@@ -36,7 +36,7 @@ def main():
             runs += [(0.8, "threshold", ["--context-tower"]), (0.8, "threshold", ["--rope-theta", "10000"])]
         for gamma, mode, extra in runs:
             cmd = [sys.executable, os.path.join(ROOT, "bench.py"), "--config", cfg, "--gamma", str(gamma), "--mode",
-                   mode, "--steps", str(args.steps), "--warmup", str(args.warmup), "--no-micro", "--no-cpu", *extra]
+                   mode, "--steps", str(args.steps), "--warmup", str(args.warmup), "--no-micro", "--no-cpu", "--no-small", *extra]
             out = subprocess.run(cmd, capture_output=True, text=True, cwd=ROOT)
             if out.returncode != 0:
                 print(json.dumps({"config": cfg, "gamma": gamma, "mode": mode, "error": out.stderr[-2000:]}))
