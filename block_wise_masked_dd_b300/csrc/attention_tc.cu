@@ -135,9 +135,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = *a.ctx_len;
   // With active-sequence compaction the pairs are those of the active
   // sequences; the record was written by the step's first kernel, at least
-  // three launches upstream, so it is complete before this kernel starts.
+  // three launches upstream, so it is complete before this kernel starts
+  // (read through L2, since this happens before the launch's wait).
   const int n_ctx = attn_launch_splits(a, n_ctx_plan, T);
-  const int n_items = a.cmp ? a.cmp[1] * a.Hkv * n_ctx : n_items_max;
+  const int n_items = a.cmp ? __ldcg(a.cmp + 1) * a.Hkv * n_ctx : n_items_max;
   const int ntiles_all = (T + kKT - 1) / kKT;
   const int per = (ntiles_all + n_ctx - 1) / n_ctx;
   const int R = a.B * a.S;
@@ -203,7 +204,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // item's first two tiles go out before waiting for it (programmatic
       // dependent launch); q does, so its load waits.
       // the context cache plane of (compacted sequence b, kv head)
-      auto plane = [&](int b, int kvh) { return a.z0 + (a.cmp ? a.cmp[2 + b] : b) * a.Hkv + kvh; };
+      auto plane = [&](int b, int kvh) { return a.z0 + (a.cmp ? __ldcg(a.cmp + 2 + b) : b) * a.Hkv + kvh; };
       int split, kvh, b, tile0, nt;
       int pre = 0;
       bool ok = true;
@@ -495,8 +496,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   const int T = *a.ctx_len;
   // the active sequences' record is written by the step's first kernel, at
   // least three launches upstream, so it is complete before this kernel starts
+  // (read through L2, since this happens before the launch's wait)
   const int n_ctx = attn_launch_splits(a, n_ctx_plan, T);
-  const int n_items = a.cmp ? a.cmp[1] * a.Hkv * n_ctx : n_items_max;
+  const int n_items = a.cmp ? __ldcg(a.cmp + 1) * a.Hkv * n_ctx : n_items_max;
   const int ntiles_all = (T + kKT - 1) / kKT;
   const int per = (ntiles_all + n_ctx - 1) / n_ctx;
   auto item = [&](int w, int& split, int& kvh, int& b, int& tile0, int& nt) {
@@ -556,7 +558,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tma_load_3d(smem + kOffV + s * kKV + kBox, &map_v, &vfull[s], 64, key0, z);
         return true;
       };
-      auto plane = [&](int b, int kvh) { return a.z0 + (a.cmp ? a.cmp[2 + b] : b) * a.Hkv + kvh; };
+      auto plane = [&](int b, int kvh) { return a.z0 + (a.cmp ? __ldcg(a.cmp + 2 + b) : b) * a.Hkv + kvh; };
       int split, kvh, b, tile0, nt;
       int pre = 0;
       bool ok = true;

@@ -187,7 +187,11 @@ __host__ __device__ inline int attn_ctx_splits(int pairs, int ntiles, int max_sp
 // compaction record the device-side choice for the active pairs.
 __host__ __device__ inline int attn_launch_splits(const AttnArgs& a, int n_ctx_plan, int T) {
   if (!a.cmp) return n_ctx_plan;
+#ifdef __CUDA_ARCH__
+  const int pairs = __ldcg(a.cmp + 1) * a.Hkv;  // L2: the record may be read before the launch's wait
+#else
   const int pairs = a.cmp[1] * a.Hkv;
+#endif
   return attn_ctx_splits(pairs, (T + 127) / 128, pairs > 0 ? a.max_pair_splits / pairs : 1);
 }
 
