@@ -116,7 +116,7 @@ bool make_map_q_stacked(CUtensorMap* m, const void* qkv, uint64_t rows, uint64_t
 
 struct Layout {
   size_t kc, vc, x, y, yc, row_index, qkv, attn, hmid, part, attn_part, sel_m, sel_s, sel_a, conf, arg, tok, mask,
-      ncommit, small, params, sq_a, sq_b, xpart, fcnt, cmp, total;
+      ncommit, small, params, sq_a, sq_b, xpart, fcnt, cmp, rope_cs, total;
   size_t part_elems;
   int alloc_ctx;
   dd::GemmPlan p_qkv, p_o, p_gu, p_d, p_lm, p_store, p_tower, p_tqkv, p_to;
@@ -276,6 +276,8 @@ Layout make_layout(const dd_config& c) {
   L.fcnt = take(fusable ? dd::fused_counter_bytes() : 0);
   // active-sequence compaction record (written by the embedding kernel each step)
   L.cmp = take((size_t)dd::cmp_words(c.batch, c.block) * 4);
+  // rotary (cos, sin) table of the step's block positions (written by the embedding kernel)
+  L.rope_cs = take((size_t)c.block * (c.head_dim / 2) * 8);
   L.total = off;
   return L;
 }
@@ -344,8 +346,10 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
   fo.xpart = at<float>(ws, L.xpart);
   fo.cnt = at<unsigned>(ws, L.fcnt);
 
+  float2* rope_cs = cf.rope_theta > 0.f ? at<float2>(ws, L.rope_cs) : nullptr;
   DD_CUDA(dd::launch_embed_norm(at<int32_t>(ws, L.tok), at<uint32_t>(ws, L.mask), c->w.embed, c->w.pos, g_attn,
-                                x, y, cf.batch, cf.block, H, cf.vocab, cf.rms_eps, st, fz ? sq_a : nullptr, cmp));
+                                x, y, cf.batch, cf.block, H, cf.vocab, cf.rms_eps, st, fz ? sq_a : nullptr, cmp,
+                                rope_cs, cf.rope_theta, cf.head_dim, small_ptr(c) + 2));
   mk(kKEmbed);
   for (int l = 0; l < cf.n_layers; ++l) {
     dd::GemmOut o{};
@@ -366,7 +370,7 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
       DD_CUDA(dd::launch_gemm(L.p_qkv, c->m_wqkv[l], c->m_y_b, o, status, c->timeout_ns, st));
       mk(kKGemmQkv);
       DD_CUDA(dd::launch_reduce_qkv(part, L.p_qkv.splits, o.split_stride, R, c->qkvw, ws + L.qkv, cf.block,
-                                    cf.head_dim, fo.qk_cols, small_ptr(c) + 2, cf.rope_theta, st, cmp));
+                                    cf.head_dim, fo.qk_cols, small_ptr(c) + 2, cf.rope_theta, st, cmp, rope_cs));
       mk(kKReduceQkv);
     }
     // block attention

@@ -234,16 +234,21 @@ cudaError_t launch_attention_combine(const AttnPlan& p, const AttnArgs& a, cudaS
 // every later kernel of the step reads it (&cmp[0] is the dynamic row count
 // of the linear layers and their reduces).
 constexpr int cmp_words(int B, int S) { return 2 + B + B * S; }
+// With rope_cs (theta > 0) the embedding kernel also writes the step's rotary
+// table: rope_cs[i * D/2 + j] = (cos, sin) of (*ctx_len + i) * theta^(-2j/D),
+// the angle in double reduced modulo 2 pi, for block positions i < S.
 cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const void* embed, const void* pos,
                               const void* g, float* x, void* y_split, int B, int S, int H, int V, float eps,
-                              cudaStream_t st, float* sq = nullptr, int* cmp = nullptr);
+                              cudaStream_t st, float* sq = nullptr, int* cmp = nullptr, float2* rope_cs = nullptr,
+                              float theta = 0.f, int D = 0, const int* ctx_len = nullptr);
 // q|k|v of the step: the split-K sum written as bf16 head + remainder; with
 // theta > 0 the query and key heads (columns < qk_cols) of row r are rotated
 // to position *ctx_len + r % S (see dd_config.rope_theta).
-// With rows_dev only the first *rows_dev rows (the active ones) are written.
+// With rows_dev only the first *rows_dev rows (the active ones) are written;
+// with rope_cs the rotation reads the step's table instead of recomputing it.
 cudaError_t launch_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N, void* out, int S,
                               int D, int qk_cols, const int* ctx_len, float theta, cudaStream_t st,
-                              const int* rows_dev = nullptr);
+                              const int* rows_dev = nullptr, const float2* rope_cs = nullptr);
 // Context tower (dd_append_block): e = embed[token] (fp32, to x) and
 // y = RMSNorm(e) * g as bf16 head + remainder; its causal self-attention over
 // each committed block (fp32 q|k|v [rows][3 * heads * D] -> head + remainder

@@ -267,16 +267,22 @@ DD_DEV uint32_t pack_bf16(float lo, float hi) {
 // Rotary position of one (even, odd) pair: the angle pos * freq in double,
 // reduced modulo 2 pi in double, then an fp32 sine and cosine and an fp32
 // rotation (the same arithmetic wherever a pair is turned).
-DD_DEV void rope_pair(float& x0, float& x1, double pos, double freq) {
+DD_DEV float2 rope_cos_sin(double pos, double freq) {
   const double ang = pos * freq;
   const double two_pi = 6.283185307179586;
   const float red = (float)(ang - rint(ang / two_pi) * two_pi);
   float sn, c;
   sincosf(red, &sn, &c);
-  const float a = x0, b = x1;
-  x0 = a * c - b * sn;
-  x1 = a * sn + b * c;
+  return make_float2(c, sn);
 }
+
+DD_DEV void rope_rotate(float& x0, float& x1, float2 cs) {
+  const float a = x0, b = x1;
+  x0 = a * cs.x - b * cs.y;
+  x1 = a * cs.y + b * cs.x;
+}
+
+DD_DEV void rope_pair(float& x0, float& x1, double pos, double freq) { rope_rotate(x0, x1, rope_cos_sin(pos, freq)); }
 
 // Split two fp32 values into packed bf16 heads (round to nearest) and packed
 // bf16 remainders: x = head + rem up to the remainder's own rounding.

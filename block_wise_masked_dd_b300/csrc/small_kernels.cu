@@ -151,7 +151,8 @@ __device__ __forceinline__ void kth_active(const uint32_t* mask, int B, int k, i
 // active sequence, cmp[2 + B + r] = the original row (b*S + i) of row r.
 __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const __nv_bfloat16* embed,
                              const __nv_bfloat16* pos, const __nv_bfloat16* g, float* x, __nv_bfloat16* y, int S,
-                             int H, int V, float eps, float* sq, int* cmp) {
+                             int H, int V, float eps, float* sq, int* cmp, float2* rope_cs, float theta, int D,
+                             const int* ctx_len) {
   __shared__ float red[32];
   __shared__ int s_seq, s_nact;
   const int r = blockIdx.x, i = r % S, R = gridDim.x, B = R / S;
@@ -163,6 +164,12 @@ __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const 
     if (p < passes) load8_bf16(pos + (long long)i * H + (p * blockDim.x + threadIdx.x) * 8, pv[p]);
   pdl_wait();
   pdl_launch_dependents();
+  // rotary table of the step: CTA i < S writes block position i's row
+  if (rope_cs && r < S) {
+    const double p = (double)(*ctx_len + r);
+    for (int j = threadIdx.x; j < D / 2; j += blockDim.x)
+      rope_cs[r * (D / 2) + j] = rope_cos_sin(p, pow((double)theta, -2.0 * j / D));
+  }
   int b = r / S;
   if (cmp) {
     if (threadIdx.x < 32) {  // warp 0 (the whole CTA when it is narrower)
@@ -283,12 +290,14 @@ __global__ void k_reduce(const float* part, int splits, long long split_stride, 
 // (2j, 2j+1) of every query and key head (columns < qk_cols) of row r turn by
 // (T + r % S) * theta^(-2j/D) radians, T = *ctx_len: the frequencies and the
 // angle in double, the angle reduced modulo 2 pi in double before an fp32
-// sine and cosine, the rotation in fp32.
+// sine and cosine, the rotation in fp32.  With rope_cs (the step's table of
+// those cosines and sines, [S][D/2], written by the embedding kernel) the
+// rotation reads them instead of recomputing them per element.
 __global__ void k_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N,
                              __nv_bfloat16* out, int S, int D, int qk_cols, const int* ctx_len, float theta,
-                             const int* rows_dev) {
+                             const int* rows_dev, const float2* rope_cs) {
   __shared__ double freq[64];  // theta^(-2j/D), j < D/2 (D <= 128)
-  if (theta > 0.f && threadIdx.x < D / 2) freq[threadIdx.x] = pow((double)theta, -2.0 * threadIdx.x / D);
+  if (theta > 0.f && !rope_cs && threadIdx.x < D / 2) freq[threadIdx.x] = pow((double)theta, -2.0 * threadIdx.x / D);
   __syncthreads();
   pdl_wait();
   pdl_launch_dependents();
@@ -303,9 +312,15 @@ __global__ void k_reduce_qkv(const float* part, int splits, long long split_stri
     const int n = (int)(e % N);
     if (theta > 0.f && n < qk_cols) {
       const int d0 = n % D;
-      const double pos = (double)(T + (int)(e / N) % S);
+      const int i = (int)(e / N) % S;
+      if (rope_cs) {
 #pragma unroll
-      for (int p = 0; p < 4; ++p) rope_pair(acc[2 * p], acc[2 * p + 1], pos, freq[(d0 >> 1) + p]);
+        for (int p = 0; p < 4; ++p) rope_rotate(acc[2 * p], acc[2 * p + 1], rope_cs[i * (D / 2) + (d0 >> 1) + p]);
+      } else {
+        const double pos = (double)(T + i);
+#pragma unroll
+        for (int p = 0; p < 4; ++p) rope_pair(acc[2 * p], acc[2 * p + 1], pos, freq[(d0 >> 1) + p]);
+      }
     }
     store8_split(out + e, out + total + e, acc);
   }
@@ -666,16 +681,18 @@ cudaError_t prepare_small_kernels() {
 
 cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const void* embed, const void* pos,
                               const void* g, float* x, void* y, int B, int S, int H, int V, float eps,
-                              cudaStream_t st, float* sq, int* cmp) {
+                              cudaStream_t st, float* sq, int* cmp, float2* rope_cs, float theta, int D,
+                              const int* ctx_len) {
   return launch_k(k_embed_norm, B * S, row_threads(H), 0, st, tokens, mask, (const __nv_bfloat16*)embed,
-                  (const __nv_bfloat16*)pos, (const __nv_bfloat16*)g, x, (__nv_bfloat16*)y, S, H, V, eps, sq, cmp);
+                  (const __nv_bfloat16*)pos, (const __nv_bfloat16*)g, x, (__nv_bfloat16*)y, S, H, V, eps, sq, cmp,
+                  rope_cs, theta, D, ctx_len);
 }
 
 cudaError_t launch_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N, void* out, int S,
                               int D, int qk_cols, const int* ctx_len, float theta, cudaStream_t st,
-                              const int* rows_dev) {
+                              const int* rows_dev, const float2* rope_cs) {
   return launch_k(k_reduce_qkv, grid_for((long long)rows * N / 8, 256), 256, 0, st, part, splits, split_stride, rows,
-                  N, (__nv_bfloat16*)out, S, D, qk_cols, ctx_len, theta, rows_dev);
+                  N, (__nv_bfloat16*)out, S, D, qk_cols, ctx_len, theta, rows_dev, rope_cs);
 }
 
 cudaError_t launch_tower_embed_norm(const int32_t* tokens, const void* embed, const void* g, float* x, void* y,
