@@ -1,5 +1,6 @@
 """Why every activation operand of the CUDA path is a bf16 head plus a bf16
-remainder: each cheaper option, applied alone at one point of the step and
+remainder: each cheaper option, applied alone at one point of the step (or
+one fp16 pass at every GEMM input) and
 measured with the oracle on the small decode workload (two sequences, four
 layers, a partly committed block), moves some logit past the parity bar
 (|d| <= 2e-2 + 2e-2 |logit|).  The variants are the oracle with one operand
@@ -30,7 +31,25 @@ VARIANTS = {
     "attention query": [("block_attention", 's = (q[:, h, :].astype(F32) @ keys.T) * scale',
                          's = (round_bf16(q[:, h, :].astype(F32)) @ keys.T) * scale')],
     "attention probabilities": [("block_attention", "out[:, h, :] = p @ vals", "out[:, h, :] = round_bf16(p) @ vals")],
+    # every GEMM input (the four projections and the LM head) rounded once to
+    # fp16 (11-bit significand): the weights convert to fp16 exactly in the
+    # normal range, so this is a single fp16 tensor-core pass per GEMM
+    "every GEMM input in fp16": [("denoise_step", a, b) for a, b in [
+        ('q = (y @ w[f"wq{l}"].T)', 'q = (round_fp16(y) @ w[f"wq{l}"].T)'),
+        ('k = (y @ w[f"wk{l}"].T)', 'k = (round_fp16(y) @ w[f"wk{l}"].T)'),
+        ('v = st(y @ w[f"wv{l}"].T)', 'v = st(round_fp16(y) @ w[f"wv{l}"].T)'),
+        ('x = x + o @ w[f"wo{l}"].T', 'x = x + round_fp16(o) @ w[f"wo{l}"].T'),
+        ('hmid = st(silu(y @ w[f"wg{l}"].T) * (y @ w[f"wu{l}"].T))',
+         'hmid = st(silu(round_fp16(y) @ w[f"wg{l}"].T) * (round_fp16(y) @ w[f"wu{l}"].T))'),
+        ('x = x + hmid @ w[f"wd{l}"].T', 'x = x + round_fp16(hmid) @ w[f"wd{l}"].T'),
+        ('conf, arg, logits = lm_head_select(hf, w["lm_head"])',
+         'conf, arg, logits = lm_head_select(round_fp16(hf), w["lm_head"])')]],
 }
+
+
+def round_fp16(a):
+    """fp32 -> nearest fp16 -> fp32 (NumPy's conversion: round to nearest even)."""
+    return np.asarray(a, np.float32).astype(np.float16).astype(np.float32)
 
 
 @pytest.fixture(scope="module")
@@ -46,6 +65,7 @@ def problem():
 def _variant(edits):
     """A namespace holding the edited functions and a denoise_step that calls them."""
     ns = dict(od.__dict__)
+    ns["round_fp16"] = round_fp16
     edited = {fn for fn, _, _ in edits}
     for fn in sorted(edited | {"denoise_step"}):
         src = textwrap.dedent(inspect.getsource(getattr(od, fn)))
