@@ -42,6 +42,8 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct KArgs {
   int m_tiles, n_tiles, splits, kb_total, kb_per_split, BN, stages, tiles_total;
+  int sk_units;    // > 0: stream-K, each CTA takes this many consecutive (tile, K block) units
+  int sk_total;    // units of the whole GEMM (tiles x K blocks)
   int split_rows;  // row offset of the remainder half in the activation map
   uint32_t tmem_half;
   GemmOut out;
@@ -54,6 +56,50 @@ __host__ __device__ inline int stage_bytes_of(int epi, int BN, int split) {
   const int b = BN * kBK * 2;
   const int act = (epi == kEpiPartial) ? b : kStageA;
   return kStageA + b + (split ? act : 0);
+}
+
+// One piece of work of a CTA: K blocks [kb0, kb1) of tile (mt, nt), whose
+// fp32 result goes to partial slot `slot`.  Uniform split-K: the CTA takes
+// items blockIdx.x, blockIdx.x + gridDim.x, ... of tiles x splits.  Stream-K
+// (linear layers, sk_units > 0): the CTA takes units [c*L, (c+1)*L) of the
+// (tile, K block) sequence, tile by tile, so every CTA does the same number of
+// K blocks; a tile cut between CTAs gets one slot per piece (slot = the CTA's
+// place among the tile's CTAs), and the CTA finishing a tile zero-fills the
+// slots past its pieces so the reduce can sum `splits` slots everywhere.
+struct Seg {
+  int mt, nt, kb0, kb1, slot, zero_from;  // zero_from: first slot to clear after this piece (splits: none)
+  bool first;                             // the CTA's first piece (never skipped)
+};
+
+__device__ __forceinline__ bool seg_of(const KArgs& a, int epi, int i, Seg& g) {
+  const int per_split = a.m_tiles * a.n_tiles;
+  int tile;
+  if (a.sk_units > 0) {
+    const int u0 = blockIdx.x * a.sk_units;
+    const int u1 = min(u0 + a.sk_units, a.sk_total);
+    const int start = i == 0 ? u0 : (u0 / a.kb_total + i) * a.kb_total;
+    if (start >= u1) return false;
+    tile = start / a.kb_total;
+    g.kb0 = start - tile * a.kb_total;
+    g.kb1 = min(a.kb_total, u1 - tile * a.kb_total);
+    const int first_cta = tile * a.kb_total / a.sk_units;
+    const int last_cta = ((tile + 1) * a.kb_total - 1) / a.sk_units;
+    g.slot = blockIdx.x - first_cta;
+    g.zero_from = g.kb1 == a.kb_total ? last_cta - first_cta + 1 : a.splits;
+  } else {
+    const int t = blockIdx.x + i * gridDim.x;
+    if (t >= a.tiles_total) return false;
+    const int split = t / per_split;
+    tile = t % per_split;
+    g.kb0 = split * a.kb_per_split;
+    g.kb1 = min(a.kb_total, g.kb0 + a.kb_per_split);
+    g.slot = split;
+    g.zero_from = a.splits;
+  }
+  if (epi == kEpiPartial) { g.nt = tile % a.n_tiles; g.mt = tile / a.n_tiles; }
+  else { g.mt = tile % a.m_tiles; g.nt = tile / a.m_tiles; }
+  g.first = i == 0;
+  return true;
 }
 
 // SPLIT is a template parameter: a run-time test inside the MMA issue loop
@@ -110,7 +156,6 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
 
-  const int per_split = args.m_tiles * args.n_tiles;
 
   if (warp == 0) {
     // ------------------------------------------------------------ producer
@@ -141,14 +186,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t phase = 0;
       bool ok = true, waited = false;
       int pend_s[8], pend_kb[8], pend_n = 0;
-      for (int t = blockIdx.x; t < args.tiles_total && ok; t += gridDim.x) {
-        const int split = t / per_split, r = t % per_split;
-        int mt, nt;
-        if (EPI == kEpiPartial) { nt = r % args.n_tiles; mt = r / args.n_tiles; }
-        else { mt = r % args.m_tiles; nt = r / args.m_tiles; }
-        if (dyn && t != (int)blockIdx.x && first_row(mt, nt) >= *rows_smem) continue;
-        const int kb0 = split * args.kb_per_split;
-        const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
+      Seg sg;
+      for (int si = 0; ok && seg_of(args, EPI, si, sg); ++si) {
+        const int mt = sg.mt, nt = sg.nt;
+        if (dyn && !sg.first && first_row(mt, nt) >= *rows_smem) continue;
+        const int kb0 = sg.kb0, kb1 = sg.kb1;
         const int count = kb1 - kb0;
         for (int i = 0; i < count; ++i) {
           const int kb = kb0 + i;
@@ -188,12 +230,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       int s = 0;
       uint32_t phase = 0;
       int it = 0;
-      for (int t = blockIdx.x; t < args.tiles_total && ok; t += gridDim.x) {
-        const int split = t / per_split, r = t % per_split;
-        int mt, nt;
-        if (EPI == kEpiPartial) { nt = r % args.n_tiles; mt = r / args.n_tiles; }
-        else { mt = r % args.m_tiles; nt = r / args.m_tiles; }
-        if (dyn && t != (int)blockIdx.x) {
+      Seg sg;
+      for (int si = 0; ok && seg_of(args, EPI, si, sg); ++si) {
+        const int mt = sg.mt, nt = sg.nt;
+        if (dyn && !sg.first) {
           if (rows < 0) {
             if (!mbar_wait_bounded(ready, 0, args.timeout_ns, abort_flag, args.status)) break;
             rows = *rows_smem;
@@ -201,8 +241,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (first_row(mt, nt) >= rows) continue;
         }
         const uint32_t idesc = idesc_bf16_f32(kBM, args.BN);
-        const int kb0 = split * args.kb_per_split;
-        const int kb1 = min(args.kb_total, kb0 + args.kb_per_split);
+        const int kb0 = sg.kb0, kb1 = sg.kb1;
         const int ab = it & 1;
         const uint32_t aphase = (it >> 1) & 1;
         if (!mbar_wait_bounded(&acc_empty[ab], aphase ^ 1, args.timeout_ns, abort_flag, args.status)) { ok = false; break; }
@@ -247,12 +286,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     const int rows = dyn ? *rows_smem : args.out.rows_valid;
     int it = 0;
-    for (int t = blockIdx.x; t < args.tiles_total && rows_ok; t += gridDim.x) {
-      const int split = t / per_split, r = t % per_split;
-      int mt, nt;
-      if (EPI == kEpiPartial) { nt = r % args.n_tiles; mt = r / args.n_tiles; }
-      else { mt = r % args.m_tiles; nt = r / args.m_tiles; }
-      if (dyn && t != (int)blockIdx.x && first_row(mt, nt) >= rows) continue;
+    Seg sg;
+    for (int si = 0; rows_ok && seg_of(args, EPI, si, sg); ++si) {
+      const int mt = sg.mt, nt = sg.nt;
+      if (dyn && !sg.first && first_row(mt, nt) >= rows) continue;
       const int ab = it & 1;
       const uint32_t aphase = (it >> 1) & 1;
       ++it;
@@ -267,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (EPI == kEpiPartial) {
         // lrow = output feature, columns = activation rows.  TMEM is read 64
         // columns per wait (16 for a ragged tail).
-        float* dst = args.out.partial + (long long)split * args.out.split_stride + lrow;
+        float* dst = args.out.partial + (long long)sg.slot * args.out.split_stride + lrow;
         int c = 0;
         for (; c + 64 <= args.BN; c += 64) {
           float v[64];
@@ -286,6 +323,12 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) {
             if (row0 + j < args.out.rows_valid) dst[(long long)(row0 + j) * args.out.ld] = v[j];
           }
+        }
+        // stream-K: the tile's slots past its pieces hold zeros
+        for (int z = sg.zero_from; z < args.splits; ++z) {
+          float* zd = args.out.partial + (long long)z * args.out.split_stride + lrow;
+          for (int row = nt * args.BN; row < min((nt + 1) * args.BN, args.out.rows_valid); ++row)
+            zd[(long long)row * args.out.ld] = 0.f;
         }
       } else if (EPI == kEpiSelect) {
         // lrow = activation row, columns = vocab ids nt*BN + c.
@@ -396,6 +439,28 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act) {
     p.splits = best_s;
     p.tiles_total = base * p.splits;
     p.grid = p.tiles_total < kNumSMs ? p.tiles_total : kNumSMs;
+    // Stream-K for the wide activation shapes (more than 128 rows): every CTA
+    // an equal run of (tile, K block) units, a tile cut between CTAs reduced
+    // through one slot per piece.  Taken when its estimate (the run, the
+    // slots' partial traffic, one more epilogue) beats the uniform split by
+    // 5 %.  (At 128 rows the extra epilogue of a cut tile sits on the
+    // critical path of a latency-bound kernel, and it measured slower.)
+    if (rows > 128) {
+      const long long total = (long long)base * p.kb_total;
+      const int L = (int)((total + kNumSMs - 1) / kNumSMs);
+      int max_seg = 1;
+      for (int t = 0; t < base; ++t) {
+        const long long first = (long long)t * p.kb_total / L, last = ((long long)(t + 1) * p.kb_total - 1) / L;
+        if (last - first + 1 > max_seg) max_seg = (int)(last - first + 1);
+      }
+      const double cost_sk = L + partial_kb * max_seg + 2.0;
+      if (max_seg <= kMaxSplits && cost_sk < 0.95 * best_cost) {
+        p.sk_units = L;
+        p.sk_total = (int)total;
+        p.splits = max_seg;
+        p.grid = (int)((total + L - 1) / L);
+      }
+    }
   } else {
     p.splits = 1;
     p.kb_per_split = p.kb_total;
@@ -416,6 +481,8 @@ cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUten
   a.BN = p.BN;
   a.stages = p.stages;
   a.tiles_total = p.tiles_total;
+  a.sk_units = p.sk_units;
+  a.sk_total = p.sk_total;
   a.split_rows = p.split_rows;
   a.tmem_half = p.tmem_half;
   a.out = out;

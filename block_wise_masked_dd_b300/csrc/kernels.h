@@ -55,6 +55,7 @@ struct GemmPlan {
   int split_act;                  // activation operand = bf16 head rows [0,R) + remainder rows [R,2R)
   int split_rows;                 // R
   int fused_op;                   // fused plans (plan_gemm_fused): the epilogue op; splits = group size
+  int sk_units, sk_total;         // stream-K (> 0): (tile, K block) units per CTA and in all; splits = slots
 };
 
 struct GemmOut {
