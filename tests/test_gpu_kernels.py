@@ -19,8 +19,9 @@ def _gpu():
 
 @pytest.mark.parametrize("rows,n,k", [(16, 768, 256), (48, 384, 192), (128, 3072, 2048), (128, 2048, 5632),
                                       (512, 1024, 1024), (272, 256, 640),
+                                      (272, 5632, 4096),
                                       # stream-K schedules (tiles cut between CTAs, zero-filled slots):
-                                      (272, 5632, 4096), (384, 7168, 4096)])
+                                      (384, 7168, 4096), (512, 4096, 14336)])
 def test_gemm_vs_oracle_linear(rows, n, k):
     from block_wise_masked_dd_b300.decoder import gemm
     x = synth.make_activations(rows, k, seed=rows + n)
