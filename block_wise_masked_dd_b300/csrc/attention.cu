@@ -391,15 +391,20 @@ __global__ void k_attn_combine(const AttnArgs a, int n_splits) {
 // o = (2^(m_b - M) o_b + sum_s 2^(m_s - M) o_s) / (2^(m_b - M) l_b + sum_s 2^(m_s - M) l_s).
 // One CTA per (sequence, kv head); warp w takes query rows 16w .. 16w + 15
 // (row r = g * S + i) and keeps them in the m16n8 fragment layout throughout.
+// The block's q|k|v were written by the kernel before the context kernel,
+// which lets this kernel launch only after its own wait on that kernel: the
+// block keys are staged (through L2) and attended before waiting for the
+// context partials.
 template <int D, bool SPLIT>
 __global__ void __launch_bounds__(128) k_attn_merge_block(const AttnArgs a, int n_ctx_plan) {
   constexpr int kBlkB = kKTB * D * 2;
   __shared__ __align__(128) uint8_t blk[(SPLIT ? 4 : 2) * kBlkB];  // k, v (, k_lo, v_lo)
-  pdl_wait();  // q|k|v and the context partials come from the preceding kernels
-  pdl_launch_dependents();
   const int kvh = blockIdx.x % a.Hkv, b = blockIdx.x / a.Hkv;
-  if (a.cmp && b >= a.cmp[1]) return;  // not an active sequence
-  const int n_ctx = attn_launch_splits(a, n_ctx_plan, *a.ctx_len);  // as the context kernel chose
+  if (a.cmp && b >= __ldcg(a.cmp + 1)) {  // not an active sequence
+    pdl_wait();
+    pdl_launch_dependents();
+    return;
+  }
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int rows = a.G * a.S;
   const int R = a.B * a.S;
@@ -421,7 +426,8 @@ __global__ void __launch_bounds__(128) k_attn_merge_block(const AttnArgs a, int 
       val[j] = make_uint4(0, 0, 0, 0);
       if (c < kTiles * kChunks && r < a.S) {
         const long long row = (long long)(which >= 2 ? R : 0) + b * a.S + r;
-        val[j] = *reinterpret_cast<const uint4*>(qkv + row * a.ld_qkv + (a.Hq + (which & 1) * a.Hkv + kvh) * D + col);
+        val[j] = __ldcg(reinterpret_cast<const uint4*>(qkv + row * a.ld_qkv + (a.Hq + (which & 1) * a.Hkv + kvh) * D +
+                                                       col));
       }
     }
 #pragma unroll
@@ -450,26 +456,31 @@ __global__ void __launch_bounds__(128) k_attn_merge_block(const AttnArgs a, int 
     uint32_t(&qf)[D / 16][4] = half ? ql : qh;
 #pragma unroll
     for (int kk = 0; kk < D / 16; ++kk) {
-      qf[kk][0] = *reinterpret_cast<const uint32_t*>(q0 + kk * 16);
-      qf[kk][1] = *reinterpret_cast<const uint32_t*>(q1 + kk * 16);
-      qf[kk][2] = *reinterpret_cast<const uint32_t*>(q0 + kk * 16 + 8);
-      qf[kk][3] = *reinterpret_cast<const uint32_t*>(q1 + kk * 16 + 8);
+      qf[kk][0] = __ldcg(reinterpret_cast<const unsigned int*>(q0 + kk * 16));
+      qf[kk][1] = __ldcg(reinterpret_cast<const unsigned int*>(q1 + kk * 16));
+      qf[kk][2] = __ldcg(reinterpret_cast<const unsigned int*>(q0 + kk * 16 + 8));
+      qf[kk][3] = __ldcg(reinterpret_cast<const unsigned int*>(q1 + kk * 16 + 8));
     }
   }
   __syncthreads();
-  if (warp * 16 >= rows) return;
-
+  const bool active = warp * 16 < rows;
   float o[D / 8][4];
 #pragma unroll
   for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
   float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-  const uint32_t bk = smem_u32(blk);
-  attend_tile<D, kKTB, SPLIT, SPLIT>(bk, bk + kBlkB, bk + 2 * kBlkB, bk + 3 * kBlkB, a.S, qh, ql, o, m0, m1, l0, l1,
-                                     a.scale_log2, lane);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
-  l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
-  l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  if (active) {
+    const uint32_t bk = smem_u32(blk);
+    attend_tile<D, kKTB, SPLIT, SPLIT>(bk, bk + kBlkB, bk + 2 * kBlkB, bk + 3 * kBlkB, a.S, qh, ql, o, m0, m1, l0,
+                                       l1, a.scale_log2, lane);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 1);
+    l0 += __shfl_xor_sync(0xffffffffu, l0, 2);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 1);
+    l1 += __shfl_xor_sync(0xffffffffu, l1, 2);
+  }
+  pdl_wait();  // the context partials come from the preceding kernel
+  pdl_launch_dependents();
+  if (!active) return;
+  const int n_ctx = attn_launch_splits(a, n_ctx_plan, *a.ctx_len);  // as the context kernel chose
 
   // fold in the context partials, one slot per round trip
   const long long pbase = (long long)(b * a.Hkv + kvh) * n_ctx * rows;
@@ -522,8 +533,8 @@ __global__ void __launch_bounds__(128) k_attn_merge_block(const AttnArgs a, int 
 // CTA, the block keys in fp32 on the CUDA cores (q, k, v rebuilt from head +
 // remainder).  Scores: lane = (key j = lane / 2, half of the head dim), so
 // each dot product is split over two lanes; the output: lane owns dims
-// lane + 32 k.  The row's context partials are loaded first, so their
-// latency overlaps the staging and the block keys' arithmetic.
+// lane + 32 k.  The block keys are staged and attended while the context
+// kernel still runs; only the fold of its partials waits for it.
 constexpr int kMergeBatch = 4;  // context partials per row held in registers
 
 template <int D>
@@ -534,8 +545,6 @@ __global__ void __launch_bounds__(256) k_attn_merge_rows(const AttnArgs a, int n
   __shared__ __align__(16) float ks[kKTB * KS];
   __shared__ __align__(16) float vs[kKTB * D];
   __shared__ __align__(16) float qs[8 * D];
-  pdl_wait();  // q|k|v and the context partials come from the preceding kernels
-  pdl_launch_dependents();
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int S = a.S, rows = a.G * S;
   const int ctas_per_bk = (rows + 7) / 8;
@@ -543,132 +552,130 @@ __global__ void __launch_bounds__(256) k_attn_merge_rows(const AttnArgs a, int n
   const int r0 = (blockIdx.x % ctas_per_bk) * 8;
   const int nq = min(8, rows - r0);
   const int kvh = bk % a.Hkv, b = bk / a.Hkv;
-  if (a.cmp && b >= a.cmp[1]) return;  // not an active sequence
-  const int n_ctx = attn_launch_splits(a, n_ctx_plan, *a.ctx_len);  // as the context kernel chose
   const long long R = (long long)a.B * S;
   const long long lo = a.split ? R * a.ld_qkv : 0;
   const __nv_bfloat16* qkv = reinterpret_cast<const __nv_bfloat16*>(a.qkv);
-
-  // context partials of this warp's row
   const int r = r0 + warp;
   const bool active = warp < nq;
-  const long long pbase = (long long)bk * n_ctx * rows + r;
-  float2 ml[kMergeBatch];
-  float po[kMergeBatch][P];
-#pragma unroll
-  for (int t = 0; t < kMergeBatch; ++t) {
-    if (active && t < n_ctx) {
-      const long long pr = pbase + (long long)t * rows;
-      ml[t] = a.part_ml[pr];
-#pragma unroll
-      for (int k = 0; k < P; ++k) po[t][k] = a.part_o[pr * D + lane + 32 * k];
-    }
-  }
-
-  // q rows of this CTA, block K and block V -> shared memory (fp32, head +
-  // remainder); every load of this thread is issued before its first store
-  constexpr int CPR = D / 8;                                // 16-byte chunks per row
-  constexpr int kPer = ((8 + 2 * kKTB) * CPR + 255) / 256;  // chunks per thread, at most
-  const int total = (nq + 2 * S) * CPR;
-  uint4 hv[kPer], lv[kPer];
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int c = threadIdx.x + u * 256;
-    if (c < total) {
-      const int row = c / CPR, col = (c % CPR) * 8;
-      long long off;
-      if (row < nq) {
-        const int rr = r0 + row;
-        off = (long long)(b * S + rr % S) * a.ld_qkv + (kvh * a.G + rr / S) * D + col;
-      } else {
-        const int kv = row - nq, which = kv >= S ? 1 : 0, j = kv - which * S;
-        off = (long long)(b * S + j) * a.ld_qkv + (a.Hq + which * a.Hkv + kvh) * D + col;
-      }
-      hv[u] = *reinterpret_cast<const uint4*>(qkv + off);
-      lv[u] = a.split ? *reinterpret_cast<const uint4*>(qkv + lo + off) : make_uint4(0, 0, 0, 0);
-    }
-  }
-#pragma unroll
-  for (int u = 0; u < kPer; ++u) {
-    const int c = threadIdx.x + u * 256;
-    if (c < total) {
-      const int row = c / CPR, col = (c % CPR) * 8;
-      float* dst;
-      if (row < nq) {
-        dst = qs + row * D + col;
-      } else {
-        const int kv = row - nq, which = kv >= S ? 1 : 0, j = kv - which * S;
-        dst = which ? vs + j * D + col : ks + j * KS + col;
-      }
-      const uint32_t hw[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
-      const uint32_t lw[4] = {lv[u].x, lv[u].y, lv[u].z, lv[u].w};
-      float v[8];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        v[2 * e] = __uint_as_float(hw[e] << 16) + __uint_as_float(lw[e] << 16);
-        v[2 * e + 1] = __uint_as_float(hw[e] & 0xffff0000u) + __uint_as_float(lw[e] & 0xffff0000u);
-      }
-      reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
-      reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
-    }
-  }
-  __syncthreads();
-  if (!active) return;
-
-  // scores of keys j = lane / 2 + 16 u (u = 0, 1; S <= 32), in base-2 units
-  const int half = lane & 1;
-  float sj[2];
-#pragma unroll
-  for (int u = 0; u < 2; ++u) {
-    const int j = (lane >> 1) + 16 * u;
-    float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
-    if (j < S) {
-      const float4* kr = reinterpret_cast<const float4*>(ks + j * KS);
-      const float4* qr = reinterpret_cast<const float4*>(qs + warp * D);
-#pragma unroll
-      for (int m = 0; m < H2 / 4; ++m) {
-        // interleaved 16-byte chunks: this half takes chunk 2m + half
-        const float4 kv = kr[2 * m + half], qv = qr[2 * m + half];
-        t0 = fmaf(qv.x, kv.x, t0);
-        t1 = fmaf(qv.y, kv.y, t1);
-        t2 = fmaf(qv.z, kv.z, t2);
-        t3 = fmaf(qv.w, kv.w, t3);
-      }
-    }
-    float t = (t0 + t1) + (t2 + t3);
-    t += __shfl_xor_sync(0xffffffffu, t, 1);
-    sj[u] = j < S ? t * a.scale_log2 : -INFINITY;
-  }
-  float mb = fmaxf(sj[0], sj[1]);
-#pragma unroll
-  for (int o = 2; o < 32; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
-  float pj[2];
-#pragma unroll
-  for (int u = 0; u < 2; ++u) pj[u] = sj[u] == -INFINITY ? 0.f : exp2f(sj[u] - mb);
-  float lb = half ? 0.f : pj[0] + pj[1];
-#pragma unroll
-  for (int o = 1; o < 32; o <<= 1) lb += __shfl_xor_sync(0xffffffffu, lb, o);
+  // The block's q|k|v were written by the kernel before the context kernel,
+  // which lets this kernel launch only after its own wait on that kernel:
+  // they are complete here, so the block keys are staged (through L2) and
+  // attended before waiting for the context partials.
+  const bool seq_on = !a.cmp || b < __ldcg(a.cmp + 1);  // an active sequence
   float acc[P];
+  float M = -INFINITY, L = 0.f;
+  if (seq_on) {
+    // q rows of this CTA, block K and block V -> shared memory (fp32, head +
+    // remainder); every load of this thread is issued before its first store
+    constexpr int CPR = D / 8;                                // 16-byte chunks per row
+    constexpr int kPer = ((8 + 2 * kKTB) * CPR + 255) / 256;  // chunks per thread, at most
+    const int total = (nq + 2 * S) * CPR;
+    uint4 hv[kPer], lv[kPer];
 #pragma unroll
-  for (int k = 0; k < P; ++k) acc[k] = 0.f;
-  for (int jj = 0; jj < S; ++jj) {
-    const float p = __shfl_sync(0xffffffffu, jj < 16 ? pj[0] : pj[1], 2 * (jj & 15));
-#pragma unroll
-    for (int k = 0; k < P; ++k) acc[k] = fmaf(p, vs[jj * D + lane + 32 * k], acc[k]);
-  }
-
-  // merge with the context partials (beyond the first kMergeBatch: loaded here)
-  float M = mb, L = lb;
-  for (int s0 = 0; s0 < n_ctx; s0 += kMergeBatch) {
-    if (s0 > 0) {
-#pragma unroll
-      for (int t = 0; t < kMergeBatch; ++t) {
-        if (s0 + t < n_ctx) {
-          const long long pr = pbase + (long long)(s0 + t) * rows;
-          ml[t] = a.part_ml[pr];
-#pragma unroll
-          for (int k = 0; k < P; ++k) po[t][k] = a.part_o[pr * D + lane + 32 * k];
+    for (int u = 0; u < kPer; ++u) {
+      const int c = threadIdx.x + u * 256;
+      if (c < total) {
+        const int row = c / CPR, col = (c % CPR) * 8;
+        long long off;
+        if (row < nq) {
+          const int rr = r0 + row;
+          off = (long long)(b * S + rr % S) * a.ld_qkv + (kvh * a.G + rr / S) * D + col;
+        } else {
+          const int kv = row - nq, which = kv >= S ? 1 : 0, j = kv - which * S;
+          off = (long long)(b * S + j) * a.ld_qkv + (a.Hq + which * a.Hkv + kvh) * D + col;
         }
+        hv[u] = __ldcg(reinterpret_cast<const uint4*>(qkv + off));
+        lv[u] = a.split ? __ldcg(reinterpret_cast<const uint4*>(qkv + lo + off)) : make_uint4(0, 0, 0, 0);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int c = threadIdx.x + u * 256;
+      if (c < total) {
+        const int row = c / CPR, col = (c % CPR) * 8;
+        float* dst;
+        if (row < nq) {
+          dst = qs + row * D + col;
+        } else {
+          const int kv = row - nq, which = kv >= S ? 1 : 0, j = kv - which * S;
+          dst = which ? vs + j * D + col : ks + j * KS + col;
+        }
+        const uint32_t hw[4] = {hv[u].x, hv[u].y, hv[u].z, hv[u].w};
+        const uint32_t lw[4] = {lv[u].x, lv[u].y, lv[u].z, lv[u].w};
+        float v[8];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          v[2 * e] = __uint_as_float(hw[e] << 16) + __uint_as_float(lw[e] << 16);
+          v[2 * e + 1] = __uint_as_float(hw[e] & 0xffff0000u) + __uint_as_float(lw[e] & 0xffff0000u);
+        }
+        reinterpret_cast<float4*>(dst)[0] = make_float4(v[0], v[1], v[2], v[3]);
+        reinterpret_cast<float4*>(dst)[1] = make_float4(v[4], v[5], v[6], v[7]);
+      }
+    }
+    __syncthreads();
+    if (active) {
+      // scores of keys j = lane / 2 + 16 u (u = 0, 1; S <= 32), in base-2 units
+      const int half = lane & 1;
+      float sj[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) {
+        const int j = (lane >> 1) + 16 * u;
+        float t0 = 0.f, t1 = 0.f, t2 = 0.f, t3 = 0.f;
+        if (j < S) {
+          const float4* kr = reinterpret_cast<const float4*>(ks + j * KS);
+          const float4* qr = reinterpret_cast<const float4*>(qs + warp * D);
+#pragma unroll
+          for (int m = 0; m < H2 / 4; ++m) {
+            // interleaved 16-byte chunks: this half takes chunk 2m + half
+            const float4 kv = kr[2 * m + half], qv = qr[2 * m + half];
+            t0 = fmaf(qv.x, kv.x, t0);
+            t1 = fmaf(qv.y, kv.y, t1);
+            t2 = fmaf(qv.z, kv.z, t2);
+            t3 = fmaf(qv.w, kv.w, t3);
+          }
+        }
+        float t = (t0 + t1) + (t2 + t3);
+        t += __shfl_xor_sync(0xffffffffu, t, 1);
+        sj[u] = j < S ? t * a.scale_log2 : -INFINITY;
+      }
+      float mb = fmaxf(sj[0], sj[1]);
+#pragma unroll
+      for (int o = 2; o < 32; o <<= 1) mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, o));
+      float pj[2];
+#pragma unroll
+      for (int u = 0; u < 2; ++u) pj[u] = sj[u] == -INFINITY ? 0.f : exp2f(sj[u] - mb);
+      float lb = half ? 0.f : pj[0] + pj[1];
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) lb += __shfl_xor_sync(0xffffffffu, lb, o);
+#pragma unroll
+      for (int k = 0; k < P; ++k) acc[k] = 0.f;
+      for (int jj = 0; jj < S; ++jj) {
+        const float p = __shfl_sync(0xffffffffu, jj < 16 ? pj[0] : pj[1], 2 * (jj & 15));
+#pragma unroll
+        for (int k = 0; k < P; ++k) acc[k] = fmaf(p, vs[jj * D + lane + 32 * k], acc[k]);
+      }
+      M = mb;
+      L = lb;
+    }
+  }
+  pdl_wait();  // the context partials come from the preceding kernel
+  pdl_launch_dependents();
+  if (!seq_on || !active) return;
+  const int n_ctx = attn_launch_splits(a, n_ctx_plan, *a.ctx_len);  // as the context kernel chose
+
+  // merge with the context partials of this warp's row, kMergeBatch slots
+  // per round trip
+  const long long pbase = (long long)bk * n_ctx * rows + r;
+  for (int s0 = 0; s0 < n_ctx; s0 += kMergeBatch) {
+    float2 ml[kMergeBatch];
+    float po[kMergeBatch][P];
+#pragma unroll
+    for (int t = 0; t < kMergeBatch; ++t) {
+      if (s0 + t < n_ctx) {
+        const long long pr = pbase + (long long)(s0 + t) * rows;
+        ml[t] = a.part_ml[pr];
+#pragma unroll
+        for (int k = 0; k < P; ++k) po[t][k] = a.part_o[pr * D + lane + 32 * k];
       }
     }
 #pragma unroll
