@@ -56,16 +56,17 @@ namespace dd {
 
 void set_error_message(const char* msg) { g_last_error = msg; }
 
-bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows) {
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                 uint32_t box_cols) {
   auto fn = encode_fn();
-  if (!fn) return false;
+  if (!fn || (box_cols != 64 && box_cols != 32)) return false;
   cuuint64_t dims[2] = {cols, rows};
   cuuint64_t strides[1] = {cols * 2};
-  cuuint32_t box[2] = {64, box_rows};
+  cuuint32_t box[2] = {box_cols, box_rows};
   cuuint32_t es[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, es,
-            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+            CU_TENSOR_MAP_INTERLEAVE_NONE, box_cols == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+            CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 // planes x rows x cols bf16 with planes `stride_rows` rows apart; rows at or
@@ -635,9 +636,9 @@ dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_byte
             dd::make_map_3d(&c->m_vc, c->ws + L.vc, planes, L.alloc_ctx, L.alloc_ctx, cf.head_dim, 64) &&
             dd::make_map_3d(&c->m_kc128, c->ws + L.kc, planes, L.alloc_ctx, L.alloc_ctx, cf.head_dim, 128) &&
             dd::make_map_3d(&c->m_vc128, c->ws + L.vc, planes, L.alloc_ctx, L.alloc_ctx, cf.head_dim, 128) &&
-            dd::make_map_2d(&c->m_y_b, c->ws + L.y, 2 * c->R, cf.hidden, L.p_qkv.BN) &&
-            dd::make_map_2d(&c->m_attn_b, c->ws + L.attn, 2 * c->R, c->HqD, L.p_o.BN) &&
-            dd::make_map_2d(&c->m_h_b, c->ws + L.hmid, 2 * c->R, cf.mlp, L.p_d.BN) &&
+            dd::make_map_2d(&c->m_y_b, c->ws + L.y, 2 * c->R, cf.hidden, L.p_qkv.BN, L.p_qkv.bk) &&
+            dd::make_map_2d(&c->m_attn_b, c->ws + L.attn, 2 * c->R, c->HqD, L.p_o.BN, L.p_o.bk) &&
+            dd::make_map_2d(&c->m_h_b, c->ws + L.hmid, 2 * c->R, cf.mlp, L.p_d.BN, L.p_d.bk) &&
             dd::make_map_2d(&c->m_y_a, c->ws + L.y, 2 * c->R, cf.hidden, 128) &&
             dd::make_map_2d(&c->m_yc_a, c->ws + L.yc, 2 * c->R, cf.hidden, 128) &&
             dd::make_map_q(&c->m_q, c->ws + L.qkv, 2 * c->R, c->qkvw, cf.n_q_heads, cf.head_dim, c->G, cf.block);
@@ -662,7 +663,8 @@ dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_byte
     c->f_gu = dd::plan_gemm_fused(dd::kOpSwiglu, c->R, 2 * cf.mlp, cf.hidden);
     c->f_d = dd::plan_gemm_fused(dd::kOpResidual, c->R, cf.hidden, cf.mlp);
     c->fused_ok = c->f_qkv.fused_op >= 0 && c->f_o.fused_op >= 0 && c->f_gu.fused_op >= 0 &&
-                  c->f_d.fused_op >= 0 && L.p_qkv.BN == c->R && L.p_o.BN == c->R && L.p_d.BN == c->R;
+                  c->f_d.fused_op >= 0 && L.p_qkv.BN == c->R && L.p_o.BN == c->R && L.p_d.BN == c->R &&
+                  L.p_qkv.bk == 64;  // the fused kernel reads 64-wide K blocks
   }
   // Measured on the small decode workload the fused layers lose to the
   // separate reduce kernels inside the step graph, so they are opt-in.
@@ -699,11 +701,11 @@ dd_status dd_init_weights(dd_ctx* c, const dd_weights* w) {
   c->m_wgu64.assign(cf.n_layers, CUtensorMap{});
   bool ok = true;
   for (int l = 0; l < cf.n_layers && ok; ++l) {
-    ok = dd::make_map_2d(&c->m_wqkv[l], (const uint8_t*)w->wqkv + (size_t)l * c->qkvw * H * 2, c->qkvw, H, 128) &&
-         dd::make_map_2d(&c->m_wo[l], (const uint8_t*)w->wo + (size_t)l * H * c->HqD * 2, H, c->HqD, 128) &&
-         dd::make_map_2d(&c->m_wgu[l], (const uint8_t*)w->wgu + (size_t)l * 2 * F * H * 2, 2 * F, H, 128) &&
+    ok = dd::make_map_2d(&c->m_wqkv[l], (const uint8_t*)w->wqkv + (size_t)l * c->qkvw * H * 2, c->qkvw, H, 128, c->L.p_qkv.bk) &&
+         dd::make_map_2d(&c->m_wo[l], (const uint8_t*)w->wo + (size_t)l * H * c->HqD * 2, H, c->HqD, 128, c->L.p_o.bk) &&
+         dd::make_map_2d(&c->m_wgu[l], (const uint8_t*)w->wgu + (size_t)l * 2 * F * H * 2, 2 * F, H, 128, c->L.p_gu.bk) &&
          dd::make_map_2d(&c->m_wgu64[l], (const uint8_t*)w->wgu + (size_t)l * 2 * F * H * 2, 2 * F, H, 64) &&
-         dd::make_map_2d(&c->m_wd[l], (const uint8_t*)w->wd + (size_t)l * H * F * 2, H, F, 128);
+         dd::make_map_2d(&c->m_wd[l], (const uint8_t*)w->wd + (size_t)l * H * F * 2, H, F, 128, c->L.p_d.bk);
   }
   ok = ok && dd::make_map_2d(&c->m_lm, w->lm_head, cf.vocab, H, c->L.p_lm.BN);
   if (!ok) return fail(DD_ERR_CUDA, "tensor map encoding failed for the weights");
@@ -748,10 +750,10 @@ dd_status dd_set_context_tower(dd_ctx* c, const dd_context_tower* t) {
   const uint64_t n = (uint64_t)cf.n_layers * 2 * W;
   if (n % 128 || (3 * W) % 128)
     return fail(DD_ERR_UNSUPPORTED, "n_layers*2*n_kv_heads*head_dim and 3*n_kv_heads*head_dim must be multiples of 128");
-  if (!dd::make_map_2d(&c->m_tower, t->wkv, n, cf.hidden, 128) ||
-      !dd::make_map_2d(&c->m_tower_qkv, t->wqkv, 3 * W, cf.hidden, 128) ||
-      !dd::make_map_2d(&c->m_tower_o, t->wo, cf.hidden, W, 128) ||
-      !dd::make_map_2d(&c->m_tower_a, c->ws + c->L.attn, 2 * c->R, W, c->L.p_to.BN))
+  if (!dd::make_map_2d(&c->m_tower, t->wkv, n, cf.hidden, 128, c->L.p_tower.bk) ||
+      !dd::make_map_2d(&c->m_tower_qkv, t->wqkv, 3 * W, cf.hidden, 128, c->L.p_tqkv.bk) ||
+      !dd::make_map_2d(&c->m_tower_o, t->wo, cf.hidden, W, 128, c->L.p_to.bk) ||
+      !dd::make_map_2d(&c->m_tower_a, c->ws + c->L.attn, 2 * c->R, W, c->L.p_to.BN, c->L.p_to.bk))
     return fail(DD_ERR_CUDA, "tensor map encoding failed for the context tower");
   c->tower = *t;
   return DD_OK;
@@ -1141,7 +1143,7 @@ dd_status dd_gemm(int32_t rows, int32_t n, int32_t k, const void* x, const void*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   dd::GemmPlan p = dd::plan_gemm(dd::kEpiPartial, rows, n, k);
   CUtensorMap mw, mx;
-  if (!dd::make_map_2d(&mw, w, n, k, 128) || !dd::make_map_2d(&mx, x, rows, k, p.BN))
+  if (!dd::make_map_2d(&mw, w, n, k, 128, p.bk) || !dd::make_map_2d(&mx, x, rows, k, p.BN, p.bk))
     return fail(DD_ERR_CUDA, "tensor map encoding failed");
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   dd::GemmOut o{};

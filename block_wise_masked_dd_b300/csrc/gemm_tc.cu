@@ -35,9 +35,8 @@ namespace dd {
 namespace {
 
 constexpr int kBM = 128;
-constexpr int kBK = 64;
+constexpr int kBK = 64;  // K elements per block, 128-byte swizzle (32: 64-byte swizzle)
 constexpr int kThreads = 192;
-constexpr int kStageA = kBM * kBK * 2;  // 16 KB
 constexpr float kLog2e = 1.4426950408889634f;
 
 struct KArgs {
@@ -52,10 +51,18 @@ struct KArgs {
 };
 
 // Bytes of one pipeline stage: A tile, B tile, and the activation remainder.
-__host__ __device__ inline int stage_bytes_of(int epi, int BN, int split) {
-  const int b = BN * kBK * 2;
-  const int act = (epi == kEpiPartial) ? b : kStageA;
-  return kStageA + b + (split ? act : 0);
+__host__ __device__ inline int stage_bytes_of(int epi, int BN, int split, int bk) {
+  const int a = kBM * bk * 2;
+  const int b = BN * bk * 2;
+  const int act = (epi == kEpiPartial) ? b : a;
+  return a + b + (split ? act : 0);
+}
+
+// Shared-memory descriptor of a K-major tile as TMA wrote it for K blocks of BK.
+template <int BK>
+__device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
+  static_assert(BK == 64 || BK == 32, "K blocks of 64 or 32");
+  return BK == 64 ? smem_desc_sw128(saddr) : smem_desc_sw64(saddr);
 }
 
 // One piece of work of a CTA: K blocks [kb0, kb1) of tile (mt, nt), whose
@@ -103,14 +110,16 @@ __device__ __forceinline__ bool seg_of(const KArgs& a, int epi, int i, Seg& g) {
 }
 
 // SPLIT is a template parameter: a run-time test inside the MMA issue loop
-// slowed the LM head by a sixth.
-template <int EPI, int SPLIT>
+// slowed the LM head by a sixth.  BK: K elements per block and stage (the
+// tensor maps' box width).
+template <int EPI, int SPLIT, int BK>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, const KArgs args) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const int stage_b = args.BN * kBK * 2;
-  const int stage_bytes = stage_bytes_of(EPI, args.BN, SPLIT);
+  constexpr int kA = kBM * BK * 2;  // bytes of a 128-row tile of one K block
+  const int stage_b = args.BN * BK * 2;
+  const int stage_bytes = stage_bytes_of(EPI, args.BN, SPLIT, BK);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + args.stages * stage_bytes);
   uint64_t* empty = full + args.stages;
   uint64_t* acc_full = empty + args.stages;
@@ -164,18 +173,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       // weight loads go out before waiting for it (programmatic dependent
       // launch), the activation loads of those stages right after the wait.
       auto load_w = [&](uint8_t* sa, int s, int kb, int mt, int nt) {
-        if (EPI == kEpiPartial) tma_load_2d(sa, &map_a, &full[s], kb * kBK, mt * kBM);
-        else tma_load_2d(sa + kStageA, &map_b, &full[s], kb * kBK, nt * args.BN);
+        if (EPI == kEpiPartial) tma_load_2d(sa, &map_a, &full[s], kb * BK, mt * kBM);
+        else tma_load_2d(sa + kA, &map_b, &full[s], kb * BK, nt * args.BN);
       };
       auto load_x = [&](uint8_t* sa, int s, int kb, int mt, int nt) {
         if (EPI == kEpiPartial) {
-          tma_load_2d(sa + kStageA, &map_b, &full[s], kb * kBK, nt * args.BN);
+          tma_load_2d(sa + kA, &map_b, &full[s], kb * BK, nt * args.BN);
           if (SPLIT)
-            tma_load_2d(sa + kStageA + stage_b, &map_b, &full[s], kb * kBK, args.split_rows + nt * args.BN);
+            tma_load_2d(sa + kA + stage_b, &map_b, &full[s], kb * BK, args.split_rows + nt * args.BN);
         } else {
-          tma_load_2d(sa, &map_a, &full[s], kb * kBK, mt * kBM);
+          tma_load_2d(sa, &map_a, &full[s], kb * BK, mt * kBM);
           if (SPLIT)
-            tma_load_2d(sa + kStageA + stage_b, &map_a, &full[s], kb * kBK, args.split_rows + mt * kBM);
+            tma_load_2d(sa + kA + stage_b, &map_a, &full[s], kb * BK, args.split_rows + mt * kBM);
         }
       };
       auto publish_rows = [&]() {
@@ -251,17 +260,17 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (!mbar_wait_bounded(&full[s], phase, args.timeout_ns, abort_flag, args.status)) { ok = false; break; }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + s * stage_bytes);
-          const uint32_t b_addr = a_addr + kStageA;
+          const uint32_t b_addr = a_addr + kA;
           const uint32_t lo_addr = b_addr + stage_b;
 #pragma unroll
-          for (int k = 0; k < kBK / 16; ++k) {
-            tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc,
+          for (int k = 0; k < BK / 16; ++k) {
+            tc_mma_bf16(d_tmem, smem_desc<BK>(a_addr + k * 32), smem_desc<BK>(b_addr + k * 32), idesc,
                         (kb > kb0 || k > 0) ? 1u : 0u);
             if (SPLIT) {
               if (EPI == kEpiPartial)
-                tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + k * 32), smem_desc_sw128(lo_addr + k * 32), idesc, 1u);
+                tc_mma_bf16(d_tmem, smem_desc<BK>(a_addr + k * 32), smem_desc<BK>(lo_addr + k * 32), idesc, 1u);
               else
-                tc_mma_bf16(d_tmem, smem_desc_sw128(lo_addr + k * 32), smem_desc_sw128(b_addr + k * 32), idesc, 1u);
+                tc_mma_bf16(d_tmem, smem_desc<BK>(lo_addr + k * 32), smem_desc<BK>(b_addr + k * 32), idesc, 1u);
             }
           }
           tc_commit(&empty[s]);
@@ -397,19 +406,24 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act) {
   p.epi = epi;
   p.split_act = split_act;
   p.split_rows = rows;
-  p.kb_total = K / kBK;
+  p.bk = kBK;
   if (epi == kEpiPartial) {
     // features on M, activation rows on N
     p.m_tiles = N / kBM;
     p.BN = rows <= 256 ? ((rows + 15) / 16) * 16 : 256;
     p.n_tiles = (rows + p.BN - 1) / p.BN;
+    // Wider activation tiles take K blocks of 32: a 256-row split stage of
+    // 64 would be 80 KB, two in flight, and the MMAs would wait on every
+    // refill; at 32 it is 40 KB and five are in flight.
+    if (p.BN > 128) p.bk = 32;
   } else {
     // activation rows on M, vocab on N (256 per tile)
     p.m_tiles = (rows + kBM - 1) / kBM;
     p.BN = 256;
     p.n_tiles = N / p.BN;
   }
-  const int stage_bytes = stage_bytes_of(epi, p.BN, split_act);
+  p.kb_total = K / p.bk;
+  const int stage_bytes = stage_bytes_of(epi, p.BN, split_act, p.bk);
   p.stages = (200 * 1024) / stage_bytes;
   if (p.stages > 8) p.stages = 8;
   if (p.stages < 2) p.stages = 2;
@@ -421,11 +435,11 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act) {
     // Persistent CTAs (at most one per SM) walk the tiles; split K so that
     // the busiest SM's K blocks are few, charging each split for the fp32
     // partial it writes and the reduce kernel reads back (in units of one
-    // K block of weights per SM).
+    // K block of weights per SM, bk wide).
     int best_s = 1;
     double best_cost = -1.0;
     const int max_s = p.kb_total < kMaxSplits ? p.kb_total : kMaxSplits;
-    const double partial_kb = 0.5 * (double)rows * N * 8.0 / ((double)kNumSMs * kStageA);
+    const double partial_kb = 0.5 * (double)rows * N * 8.0 / ((double)kNumSMs * kBM * p.bk * 2);
     for (int s = 1; s <= max_s; ++s) {
       const int kbps = (p.kb_total + s - 1) / s;
       const int real_s = (p.kb_total + kbps - 1) / kbps;
@@ -453,7 +467,7 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act) {
         const long long first = (long long)t * p.kb_total / L, last = ((long long)(t + 1) * p.kb_total - 1) / L;
         if (last - first + 1 > max_seg) max_seg = (int)(last - first + 1);
       }
-      const double cost_sk = L + partial_kb * max_seg + 2.0;
+      const double cost_sk = L + partial_kb * max_seg + 2.0 * kBK / p.bk;
       if (max_seg <= kMaxSplits && cost_sk < 0.95 * best_cost) {
         p.sk_units = L;
         p.sk_total = (int)total;
@@ -490,22 +504,26 @@ cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUten
   a.timeout_ns = timeout_ns;
   void (*k)(const CUtensorMap, const CUtensorMap, const KArgs) = nullptr;
   switch (p.epi) {
-    case kEpiPartial: k = p.split_act ? k_gemm_tc<kEpiPartial, 1> : k_gemm_tc<kEpiPartial, 0>; break;
-    case kEpiSelect: k = p.split_act ? k_gemm_tc<kEpiSelect, 1> : k_gemm_tc<kEpiSelect, 0>; break;
-    default: k = p.split_act ? k_gemm_tc<kEpiStore, 1> : k_gemm_tc<kEpiStore, 0>; break;
+    case kEpiPartial:
+      if (p.bk == 32) k = p.split_act ? k_gemm_tc<kEpiPartial, 1, 32> : k_gemm_tc<kEpiPartial, 0, 32>;
+      else k = p.split_act ? k_gemm_tc<kEpiPartial, 1, 64> : k_gemm_tc<kEpiPartial, 0, 64>;
+      break;
+    case kEpiSelect: k = p.split_act ? k_gemm_tc<kEpiSelect, 1, 64> : k_gemm_tc<kEpiSelect, 0, 64>; break;
+    default: k = p.split_act ? k_gemm_tc<kEpiStore, 1, 64> : k_gemm_tc<kEpiStore, 0, 64>; break;
   }
   return launch_k(k, p.grid, kThreads, p.smem_bytes, st, map_a, map_b, a);
 }
 
 cudaError_t prepare_gemm_kernels() {
   const int lim = 227 * 1024;
-  const void* ks[6] = {(const void*)k_gemm_tc<kEpiPartial, 0>, (const void*)k_gemm_tc<kEpiPartial, 1>,
-                       (const void*)k_gemm_tc<kEpiSelect, 0>,  (const void*)k_gemm_tc<kEpiSelect, 1>,
-                       (const void*)k_gemm_tc<kEpiStore, 0>,   (const void*)k_gemm_tc<kEpiStore, 1>};
+  const void* ks[8] = {(const void*)k_gemm_tc<kEpiPartial, 0, 64>, (const void*)k_gemm_tc<kEpiPartial, 1, 64>,
+                       (const void*)k_gemm_tc<kEpiPartial, 0, 32>, (const void*)k_gemm_tc<kEpiPartial, 1, 32>,
+                       (const void*)k_gemm_tc<kEpiSelect, 0, 64>,  (const void*)k_gemm_tc<kEpiSelect, 1, 64>,
+                       (const void*)k_gemm_tc<kEpiStore, 0, 64>,   (const void*)k_gemm_tc<kEpiStore, 1, 64>};
   cudaError_t e = cudaSuccess;
-  for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+  for (int i = 0; i < 8 && e == cudaSuccess; ++i)
     e = cudaFuncSetAttribute(ks[i], cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-  for (int i = 0; i < 6 && e == cudaSuccess; ++i)
+  for (int i = 0; i < 8 && e == cudaSuccess; ++i)
     e = cudaFuncSetAttribute(ks[i], cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   return e;
 }

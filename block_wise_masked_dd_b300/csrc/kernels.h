@@ -45,7 +45,8 @@ enum GemmEpi : int {
 struct GemmPlan {
   int epi;
   int m_tiles, n_tiles, splits;   // tile grid (M = 128 per tile)
-  int kb_total, kb_per_split;     // K blocks of 64
+  int kb_total, kb_per_split;     // K blocks of bk
+  int bk;                         // K elements per block: 64 (128-byte swizzle) or 32 (64-byte swizzle)
   int BN;                         // MMA N (multiple of 16, <= 256)
   int stages;
   int tiles_total;
@@ -307,8 +308,11 @@ void set_error_message(const char* msg);
 
 // ------------------------------------------------------------ tensor maps
 
-// 2D bf16 map over a row-major [rows][cols] matrix, box {64 cols, box_rows}.
-bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows);
+// 2D bf16 map over a row-major [rows][cols] matrix, box {box_cols, box_rows}:
+// box_cols 64 with the 128-byte swizzle, 32 with the 64-byte swizzle (a GEMM
+// plan's bk).
+bool make_map_2d(CUtensorMap* m, const void* base, uint64_t rows, uint64_t cols, uint32_t box_rows,
+                 uint32_t box_cols = 64);
 // 3D bf16 map over [planes][rows][cols] (cols = head dim), box {64, box_rows, 1};
 // planes lie stride_rows rows apart and rows >= `rows` read as zero.
 bool make_map_3d(CUtensorMap* m, const void* base, uint64_t planes, uint64_t rows, uint64_t stride_rows, uint64_t cols,

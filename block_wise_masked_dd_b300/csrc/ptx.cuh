@@ -184,6 +184,17 @@ DD_DEV uint64_t smem_desc_sw128(uint32_t saddr) {
   return d;
 }
 
+// The same for a K-major tile written by TMA with the 64-byte swizzle (rows
+// of 32 bf16): 8-row groups 512 B apart.
+DD_DEV uint64_t smem_desc_sw64(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);       // start address >> 4, bits [0,14)
+  d |= (uint64_t)(512u >> 4) << 32;               // stride-dim byte offset: 8 rows x 64 B
+  d |= (uint64_t)1 << 46;                         // descriptor version for tcgen05
+  d |= (uint64_t)4 << 61;                         // swizzle mode: 64-byte
+  return d;
+}
+
 // Instruction descriptor, kind::f16: bf16 A and B (both K-major), fp32 D.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                 // D format: f32
