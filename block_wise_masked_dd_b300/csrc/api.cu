@@ -210,17 +210,26 @@ Layout make_layout(const dd_config& c) {
   const int HqD = c.n_q_heads * c.head_dim;
   L.alloc_ctx = c.max_ctx < 128 ? 128 : c.max_ctx;  // at least one 128-position TMA box
   // Every activation operand of the step is split (bf16 head + remainder).
-  L.p_qkv = dd::plan_gemm(dd::kEpiPartial, R, qkvw, c.hidden, 1);
-  L.p_o = dd::plan_gemm(dd::kEpiPartial, R, c.hidden, HqD, 1);
-  L.p_gu = dd::plan_gemm(dd::kEpiPartial, R, 2 * c.mlp, c.hidden, 1);
-  L.p_d = dd::plan_gemm(dd::kEpiPartial, R, c.hidden, c.mlp, 1);
+  // The linear layers share activation maps, so they share one choice of CTA
+  // pairs: when one of them has an odd number of weight tiles none pairs.
+  for (int allow_pairs = 1; allow_pairs >= 0; --allow_pairs) {
+    L.p_qkv = dd::plan_gemm(dd::kEpiPartial, R, qkvw, c.hidden, 1, allow_pairs);
+    L.p_o = dd::plan_gemm(dd::kEpiPartial, R, c.hidden, HqD, 1, allow_pairs);
+    L.p_gu = dd::plan_gemm(dd::kEpiPartial, R, 2 * c.mlp, c.hidden, 1, allow_pairs);
+    L.p_d = dd::plan_gemm(dd::kEpiPartial, R, c.hidden, c.mlp, 1, allow_pairs);
+    L.p_tower = dd::plan_gemm(dd::kEpiPartial, R, c.n_layers * 2 * c.n_kv_heads * c.head_dim, c.hidden, 1,
+                              allow_pairs);
+    // context tower's attention layer: q|k|v projection and output projection
+    L.p_tqkv = dd::plan_gemm(dd::kEpiPartial, R, 3 * c.n_kv_heads * c.head_dim, c.hidden, 1, allow_pairs);
+    L.p_to = dd::plan_gemm(dd::kEpiPartial, R, c.hidden, c.n_kv_heads * c.head_dim, 1, allow_pairs);
+    const dd::GemmPlan* ps[] = {&L.p_qkv, &L.p_o, &L.p_gu, &L.p_d, &L.p_tower, &L.p_tqkv, &L.p_to};
+    bool same = true;
+    for (const dd::GemmPlan* q : ps) same = same && q->cluster == L.p_qkv.cluster;
+    if (same) break;
+  }
   L.p_lm = dd::plan_gemm(dd::kEpiSelect, R, c.vocab, c.hidden, 1);
   L.p_store = dd::plan_gemm(dd::kEpiStore, R, c.vocab, c.hidden, 1);
   L.p_attn = dd::plan_attention(c.batch, c.block, c.n_q_heads, c.n_kv_heads, c.head_dim, c.max_ctx);
-  L.p_tower = dd::plan_gemm(dd::kEpiPartial, R, c.n_layers * 2 * c.n_kv_heads * c.head_dim, c.hidden, 1);
-  // context tower's attention layer: q|k|v projection and output projection
-  L.p_tqkv = dd::plan_gemm(dd::kEpiPartial, R, 3 * c.n_kv_heads * c.head_dim, c.hidden, 1);
-  L.p_to = dd::plan_gemm(dd::kEpiPartial, R, c.hidden, c.n_kv_heads * c.head_dim, 1);
   size_t pe = 0;
   auto upd = [&](const dd::GemmPlan& p, int N) {
     size_t e = (size_t)p.splits * R * N;
@@ -636,9 +645,9 @@ dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_byte
             dd::make_map_3d(&c->m_vc, c->ws + L.vc, planes, L.alloc_ctx, L.alloc_ctx, cf.head_dim, 64) &&
             dd::make_map_3d(&c->m_kc128, c->ws + L.kc, planes, L.alloc_ctx, L.alloc_ctx, cf.head_dim, 128) &&
             dd::make_map_3d(&c->m_vc128, c->ws + L.vc, planes, L.alloc_ctx, L.alloc_ctx, cf.head_dim, 128) &&
-            dd::make_map_2d(&c->m_y_b, c->ws + L.y, 2 * c->R, cf.hidden, L.p_qkv.BN, L.p_qkv.bk) &&
-            dd::make_map_2d(&c->m_attn_b, c->ws + L.attn, 2 * c->R, c->HqD, L.p_o.BN, L.p_o.bk) &&
-            dd::make_map_2d(&c->m_h_b, c->ws + L.hmid, 2 * c->R, cf.mlp, L.p_d.BN, L.p_d.bk) &&
+            dd::make_map_2d(&c->m_y_b, c->ws + L.y, 2 * c->R, cf.hidden, L.p_qkv.box_rows_b, L.p_qkv.bk) &&
+            dd::make_map_2d(&c->m_attn_b, c->ws + L.attn, 2 * c->R, c->HqD, L.p_o.box_rows_b, L.p_o.bk) &&
+            dd::make_map_2d(&c->m_h_b, c->ws + L.hmid, 2 * c->R, cf.mlp, L.p_d.box_rows_b, L.p_d.bk) &&
             dd::make_map_2d(&c->m_y_a, c->ws + L.y, 2 * c->R, cf.hidden, 128) &&
             dd::make_map_2d(&c->m_yc_a, c->ws + L.yc, 2 * c->R, cf.hidden, 128) &&
             dd::make_map_q(&c->m_q, c->ws + L.qkv, 2 * c->R, c->qkvw, cf.n_q_heads, cf.head_dim, c->G, cf.block);
@@ -753,7 +762,7 @@ dd_status dd_set_context_tower(dd_ctx* c, const dd_context_tower* t) {
   if (!dd::make_map_2d(&c->m_tower, t->wkv, n, cf.hidden, 128, c->L.p_tower.bk) ||
       !dd::make_map_2d(&c->m_tower_qkv, t->wqkv, 3 * W, cf.hidden, 128, c->L.p_tqkv.bk) ||
       !dd::make_map_2d(&c->m_tower_o, t->wo, cf.hidden, W, 128, c->L.p_to.bk) ||
-      !dd::make_map_2d(&c->m_tower_a, c->ws + c->L.attn, 2 * c->R, W, c->L.p_to.BN, c->L.p_to.bk))
+      !dd::make_map_2d(&c->m_tower_a, c->ws + c->L.attn, 2 * c->R, W, c->L.p_to.box_rows_b, c->L.p_to.bk))
     return fail(DD_ERR_CUDA, "tensor map encoding failed for the context tower");
   c->tower = *t;
   return DD_OK;
@@ -1143,7 +1152,7 @@ dd_status dd_gemm(int32_t rows, int32_t n, int32_t k, const void* x, const void*
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   dd::GemmPlan p = dd::plan_gemm(dd::kEpiPartial, rows, n, k);
   CUtensorMap mw, mx;
-  if (!dd::make_map_2d(&mw, w, n, k, 128, p.bk) || !dd::make_map_2d(&mx, x, rows, k, p.BN, p.bk))
+  if (!dd::make_map_2d(&mw, w, n, k, 128, p.bk) || !dd::make_map_2d(&mx, x, rows, k, p.box_rows_b, p.bk))
     return fail(DD_ERR_CUDA, "tensor map encoding failed");
   uint8_t* ws = static_cast<uint8_t*>(workspace);
   dd::GemmOut o{};

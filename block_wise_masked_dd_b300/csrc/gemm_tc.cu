@@ -44,6 +44,7 @@ struct KArgs {
   int sk_units;    // > 0: stream-K, each CTA takes this many consecutive (tile, K block) units
   int sk_total;    // units of the whole GEMM (tiles x K blocks)
   int split_rows;  // row offset of the remainder half in the activation map
+  int cluster;     // 1, or 2: CTA pairs (ranks 0, 1) on weight tiles 2p, 2p + 1 share each activation tile
   uint32_t tmem_half;
   GemmOut out;
   int* status;
@@ -78,11 +79,19 @@ struct Seg {
   bool first;                             // the CTA's first piece (never skipped)
 };
 
+//
+// With CTA pairs (cluster 2) both CTAs of a pair take the same pieces of the
+// same pair tile (weight tiles 2p and 2p + 1, one activation tile): the pair
+// is the unit of the schedule, and the CTA's rank picks its weight tile.
 __device__ __forceinline__ bool seg_of(const KArgs& a, int epi, int i, Seg& g) {
-  const int per_split = a.m_tiles * a.n_tiles;
+  const int rank = a.cluster == 2 ? (int)(blockIdx.x & 1) : 0;
+  const int cid = a.cluster == 2 ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;  // the schedule's worker
+  const int workers = a.cluster == 2 ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  const int m_tiles = a.m_tiles / a.cluster;
+  const int per_split = m_tiles * a.n_tiles;
   int tile;
   if (a.sk_units > 0) {
-    const int u0 = blockIdx.x * a.sk_units;
+    const int u0 = cid * a.sk_units;
     const int u1 = min(u0 + a.sk_units, a.sk_total);
     const int start = i == 0 ? u0 : (u0 / a.kb_total + i) * a.kb_total;
     if (start >= u1) return false;
@@ -91,10 +100,10 @@ __device__ __forceinline__ bool seg_of(const KArgs& a, int epi, int i, Seg& g) {
     g.kb1 = min(a.kb_total, u1 - tile * a.kb_total);
     const int first_cta = tile * a.kb_total / a.sk_units;
     const int last_cta = ((tile + 1) * a.kb_total - 1) / a.sk_units;
-    g.slot = blockIdx.x - first_cta;
+    g.slot = cid - first_cta;
     g.zero_from = g.kb1 == a.kb_total ? last_cta - first_cta + 1 : a.splits;
   } else {
-    const int t = blockIdx.x + i * gridDim.x;
+    const int t = cid + i * workers;
     if (t >= a.tiles_total) return false;
     const int split = t / per_split;
     tile = t % per_split;
@@ -103,8 +112,8 @@ __device__ __forceinline__ bool seg_of(const KArgs& a, int epi, int i, Seg& g) {
     g.slot = split;
     g.zero_from = a.splits;
   }
-  if (epi == kEpiPartial) { g.nt = tile % a.n_tiles; g.mt = tile / a.n_tiles; }
-  else { g.mt = tile % a.m_tiles; g.nt = tile / a.m_tiles; }
+  if (epi == kEpiPartial) { g.nt = tile % a.n_tiles; g.mt = (tile / a.n_tiles) * a.cluster + rank; }
+  else { g.mt = tile % m_tiles; g.nt = tile / m_tiles; }
   g.first = i == 0;
   return true;
 }
@@ -144,7 +153,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < args.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], 1);
+      mbar_init(&empty[s], args.cluster);  // the MMAs of every CTA of the pair read the stage
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
@@ -164,6 +173,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  // A pair writes into both CTAs' stages and barriers: both are set up first.
+  const int rank = args.cluster == 2 ? (int)(blockIdx.x & 1) : 0;
+  if (args.cluster == 2) cluster_sync_all();
 
 
   if (warp == 0) {
@@ -177,7 +189,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         else tma_load_2d(sa + kA, &map_b, &full[s], kb * BK, nt * args.BN);
       };
       auto load_x = [&](uint8_t* sa, int s, int kb, int mt, int nt) {
-        if (EPI == kEpiPartial) {
+        if (EPI == kEpiPartial && args.cluster == 2) {
+          // this CTA's half of the activation rows, to both CTAs of the pair
+          const int half = args.BN / 2;
+          const int off = rank * half * BK * 2;
+          tma_load_2d_mc(sa + kA + off, &map_b, &full[s], kb * BK, nt * args.BN + rank * half, 0x3);
+          if (SPLIT)
+            tma_load_2d_mc(sa + kA + stage_b + off, &map_b, &full[s], kb * BK,
+                           args.split_rows + nt * args.BN + rank * half, 0x3);
+        } else if (EPI == kEpiPartial) {
           tma_load_2d(sa + kA, &map_b, &full[s], kb * BK, nt * args.BN);
           if (SPLIT)
             tma_load_2d(sa + kA + stage_b, &map_b, &full[s], kb * BK, args.split_rows + nt * args.BN);
@@ -229,6 +249,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         pdl_launch_dependents();
         publish_rows();
       }
+      // A pair: wait until both CTAs have released every stage, so no stage
+      // release of the peer is still on its way to this CTA when it leaves.
+      for (int i = 0; ok && args.cluster == 2 && i < args.stages; ++i) {
+        ok = mbar_wait_bounded(&empty[s], phase ^ 1, args.timeout_ns, abort_flag, args.status);
+        if (++s == args.stages) { s = 0; phase ^= 1; }
+      }
     }
     __syncwarp();
   } else if (warp == 1) {
@@ -273,7 +299,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tc_mma_bf16(d_tmem, smem_desc<BK>(lo_addr + k * 32), smem_desc<BK>(b_addr + k * 32), idesc, 1u);
             }
           }
-          tc_commit(&empty[s]);
+          if (args.cluster == 2) tc_commit_mc(&empty[s], 0x3);
+          else tc_commit(&empty[s]);
           if (++s == args.stages) { s = 0; phase ^= 1; }
         }
         if (ok) tc_commit(&acc_full[ab]);
@@ -387,6 +414,9 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   __syncthreads();
+  // The peer's last stage releases arrive on this CTA's barriers: neither CTA
+  // of a pair leaves before both are done.
+  if (args.cluster == 2) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, 2 * args.tmem_half);
@@ -401,12 +431,13 @@ uint32_t pow2_at_least(uint32_t v, uint32_t lo) {
 
 }  // namespace
 
-GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act) {
+GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act, int allow_pairs) {
   GemmPlan p{};
   p.epi = epi;
   p.split_act = split_act;
   p.split_rows = rows;
   p.bk = kBK;
+  p.cluster = 1;
   if (epi == kEpiPartial) {
     // features on M, activation rows on N
     p.m_tiles = N / kBM;
@@ -416,6 +447,10 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act) {
     // 64 would be 80 KB, two in flight, and the MMAs would wait on every
     // refill; at 32 it is 40 KB and five are in flight.
     if (p.BN > 128) p.bk = 32;
+    // Those 64-byte box rows double the TMA requests per byte: CTA pairs on
+    // adjacent weight tiles load half of each activation tile each and
+    // multicast it to both, halving every SM's activation requests.
+    if (allow_pairs && p.bk == 32 && p.m_tiles % 2 == 0) p.cluster = 2;
   } else {
     // activation rows on M, vocab on N (256 per tile)
     p.m_tiles = (rows + kBM - 1) / kBM;
@@ -429,8 +464,12 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act) {
   if (p.stages < 2) p.stages = 2;
   p.smem_bytes = 1024 + p.stages * stage_bytes + 256;
   p.tmem_half = pow2_at_least(p.BN, 32);
+  p.box_rows_b = p.BN / p.cluster;
 
-  const int base = p.m_tiles * p.n_tiles;
+  // The schedule's workers: CTAs, or CTA pairs each taking a pair of weight
+  // tiles (both CTAs of a pair do the same K blocks of their own tile).
+  const int workers = kNumSMs / p.cluster;
+  const int base = (p.m_tiles / p.cluster) * p.n_tiles;
   if (epi == kEpiPartial) {
     // Persistent CTAs (at most one per SM) walk the tiles; split K so that
     // the busiest SM's K blocks are few, charging each split for the fp32
@@ -445,14 +484,14 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act) {
       const int real_s = (p.kb_total + kbps - 1) / kbps;
       if (real_s != s) continue;
       const long long tiles = (long long)base * s;
-      const long long per_sm = (tiles + kNumSMs - 1) / kNumSMs;
+      const long long per_sm = (tiles + workers - 1) / workers;
       const double cost = (double)(per_sm * kbps) + partial_kb * s + 0.01 * s;
       if (best_cost < 0 || cost < best_cost) { best_cost = cost; best_s = s; }
     }
     p.kb_per_split = (p.kb_total + best_s - 1) / best_s;
     p.splits = best_s;
     p.tiles_total = base * p.splits;
-    p.grid = p.tiles_total < kNumSMs ? p.tiles_total : kNumSMs;
+    p.grid = (p.tiles_total < workers ? p.tiles_total : workers) * p.cluster;
     // Stream-K for the wide activation shapes (more than 128 rows): every CTA
     // an equal run of (tile, K block) units, a tile cut between CTAs reduced
     // through one slot per piece.  Taken when its estimate (the run, the
@@ -461,7 +500,7 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act) {
     // critical path of a latency-bound kernel, and it measured slower.)
     if (rows > 128) {
       const long long total = (long long)base * p.kb_total;
-      const int L = (int)((total + kNumSMs - 1) / kNumSMs);
+      const int L = (int)((total + workers - 1) / workers);
       int max_seg = 1;
       for (int t = 0; t < base; ++t) {
         const long long first = (long long)t * p.kb_total / L, last = ((long long)(t + 1) * p.kb_total - 1) / L;
@@ -472,7 +511,7 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act) {
         p.sk_units = L;
         p.sk_total = (int)total;
         p.splits = max_seg;
-        p.grid = (int)((total + L - 1) / L);
+        p.grid = (int)((total + L - 1) / L) * p.cluster;
       }
     }
   } else {
@@ -498,6 +537,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUten
   a.sk_units = p.sk_units;
   a.sk_total = p.sk_total;
   a.split_rows = p.split_rows;
+  a.cluster = p.cluster;
   a.tmem_half = p.tmem_half;
   a.out = out;
   a.status = status;
@@ -511,6 +551,7 @@ cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUten
     case kEpiSelect: k = p.split_act ? k_gemm_tc<kEpiSelect, 1, 64> : k_gemm_tc<kEpiSelect, 0, 64>; break;
     default: k = p.split_act ? k_gemm_tc<kEpiStore, 1, 64> : k_gemm_tc<kEpiStore, 0, 64>; break;
   }
+  if (p.cluster > 1) return launch_k_cluster(k, p.grid, kThreads, p.smem_bytes, st, p.cluster, map_a, map_b, a);
   return launch_k(k, p.grid, kThreads, p.smem_bytes, st, map_a, map_b, a);
 }
 

@@ -30,6 +30,27 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// launch_k with thread-block clusters of `cluster_x` CTAs along x.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_k_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                             int cluster_x, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  attr[1].id = cudaLaunchAttributeClusterDimension;
+  attr[1].val.clusterDim.x = cluster_x;
+  attr[1].val.clusterDim.y = 1;
+  attr[1].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 constexpr int kNumSMs = 148;
 constexpr int kMaxSplits = 16;  // split-K partials of one linear layer, at most
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s per bounded wait
@@ -57,6 +78,8 @@ struct GemmPlan {
   int split_rows;                 // R
   int fused_op;                   // fused plans (plan_gemm_fused): the epilogue op; splits = group size
   int sk_units, sk_total;         // stream-K (> 0): (tile, K block) units per CTA and in all; splits = slots
+  int cluster;                    // 2: CTA pairs on adjacent weight tiles share each activation tile (TMA multicast)
+  int box_rows_b;                 // rows of the activation operand's TMA box (BN / cluster)
 };
 
 struct GemmOut {
@@ -73,7 +96,8 @@ struct GemmOut {
 
 // Plan a GEMM over activations [rows][K] and weights [N][K].  With
 // split_act the activation map covers [2*rows][K]: bf16 heads then remainders.
-GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act = 0);
+// allow_pairs = 0: no CTA pairs (every activation map then has BN-row boxes).
+GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act = 0, int allow_pairs = 1);
 // Enqueue.  map_w / map_x: 2D bf16 tensor maps with 128-byte swizzle, box
 // {64, 128} for the operand on the MMA M side and {64, BN} for the other.
 cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmOut& out,
