@@ -449,8 +449,9 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act, int allow_pai
     if (p.BN > 128) p.bk = 32;
     // Those 64-byte box rows double the TMA requests per byte: CTA pairs on
     // adjacent weight tiles load half of each activation tile each and
-    // multicast it to both, halving every SM's activation requests.
-    if (allow_pairs && p.bk == 32 && p.m_tiles % 2 == 0) p.cluster = 2;
+    // multicast it to both, halving every SM's activation requests.  (Both
+    // halves start on a 1024-byte boundary: BN a multiple of 32.)
+    if (allow_pairs && p.bk == 32 && p.m_tiles % 2 == 0 && p.BN % 32 == 0) p.cluster = 2;
   } else {
     // activation rows on M, vocab on N (256 per tile)
     p.m_tiles = (rows + kBM - 1) / kBM;

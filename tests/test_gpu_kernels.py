@@ -21,7 +21,10 @@ def _gpu():
                                       (512, 1024, 1024), (272, 256, 640),
                                       (272, 5632, 4096),
                                       # stream-K schedules (tiles cut between CTAs, zero-filled slots):
-                                      (384, 7168, 4096), (512, 4096, 14336)])
+                                      (384, 7168, 4096), (512, 4096, 14336),
+                                      # K blocks of 32 without CTA pairs (three weight tiles; an N
+                                      # tile of 144 rows), and pairs with 80-row halves (N tile 160)
+                                      (272, 384, 1024), (144, 512, 512), (160, 512, 512)])
 def test_gemm_vs_oracle_linear(rows, n, k):
     from block_wise_masked_dd_b300.decoder import gemm
     x = synth.make_activations(rows, k, seed=rows + n)
