@@ -26,8 +26,6 @@ __device__ __forceinline__ float block_sum(float v, float* red) {
   return t;
 }
 
-__device__ __forceinline__ float bf(const __nv_bfloat16* p, long long i) { return __bfloat162float(p[i]); }
-
 // 8 bf16 (one 16-byte load) -> fp32
 __device__ __forceinline__ void load8_bf16(const __nv_bfloat16* p, float (&v)[8]) {
   const uint4 u = *reinterpret_cast<const uint4*>(p);
@@ -154,7 +152,7 @@ __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const 
                              int H, int V, float eps, float* sq, int* cmp, float2* rope_cs, float theta, int D,
                              const int* ctx_len) {
   __shared__ float red[32];
-  __shared__ int s_seq, s_nact;
+  __shared__ int s_seq;
   const int r = blockIdx.x, i = r % S, R = gridDim.x, B = R / S;
   const int passes = H / (8 * blockDim.x);
   float gv[kMaxRowPasses][8], pv[kMaxRowPasses][8];
@@ -177,7 +175,6 @@ __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const 
       kth_active(mask, B, r / S, seq, n_act);
       if (threadIdx.x == 0) {
         s_seq = seq;
-        s_nact = n_act;
         if (r == 0) {
           cmp[0] = n_act * S;
           cmp[1] = n_act;
