@@ -45,6 +45,7 @@ struct KArgs {
   int sk_total;    // units of the whole GEMM (tiles x K blocks)
   int split_rows;  // row offset of the remainder half in the activation map
   int cluster;     // 1, or 2: CTA pairs (ranks 0, 1) on weight tiles 2p, 2p + 1 share each activation tile
+                   // (by TMA multicast, or, in the cta_group::2 kernel, as the two halves of one MMA's B)
   uint32_t tmem_half;
   GemmOut out;
   int* status;
@@ -120,15 +121,19 @@ __device__ __forceinline__ bool seg_of(const KArgs& a, int epi, int i, Seg& g) {
 
 // SPLIT is a template parameter: a run-time test inside the MMA issue loop
 // slowed the LM head by a sixth.  BK: K elements per block and stage (the
-// tensor maps' box width).
-template <int EPI, int SPLIT, int BK>
+// tensor maps' box width).  CG = 2: the CTA pairs of a cluster run one MMA of
+// M = 256 (cta_group::2): each CTA stages its own weight tile and its half of
+// the activation rows (head and remainder), rank 0 issues the MMAs, and each
+// CTA's tensor memory holds its own weight tile's accumulator rows.
+template <int EPI, int SPLIT, int BK, int CG = 1>
 __global__ void __launch_bounds__(kThreads, 1)
     k_gemm_tc(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b, const KArgs args) {
+  static_assert(CG == 1 || (CG == 2 && EPI == kEpiPartial), "cta_group::2 for the linear layers only");
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   constexpr int kA = kBM * BK * 2;  // bytes of a 128-row tile of one K block
-  const int stage_b = args.BN * BK * 2;
-  const int stage_bytes = stage_bytes_of(EPI, args.BN, SPLIT, BK);
+  const int stage_b = args.BN / CG * BK * 2;  // this CTA's activation rows of one K block
+  const int stage_bytes = stage_bytes_of(EPI, args.BN / CG, SPLIT, BK);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + args.stages * stage_bytes);
   uint64_t* empty = full + args.stages;
   uint64_t* acc_full = empty + args.stages;
@@ -138,6 +143,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(ready + 1);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
   volatile int* rows_smem = abort_flag + 1;
+  uint32_t* tmem_slot2 = reinterpret_cast<uint32_t*>(const_cast<int*>(rows_smem + 1));  // CG 2: second buffer
   // Compacted activation rows (the LM head's masked rows, or the active
   // sequences' rows of a linear layer): the valid row count is known on the
   // device only.  A CTA never skips its first tile (its weights were
@@ -153,11 +159,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < args.stages; ++s) {
       mbar_init(&full[s], 1);
-      mbar_init(&empty[s], args.cluster);  // the MMAs of every CTA of the pair read the stage
+      // released by the MMAs of every CTA of a multicast pair; CG 2: by rank 0's
+      mbar_init(&empty[s], CG == 2 ? 1 : args.cluster);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
-      mbar_init(&acc_empty[a], 4);
+      mbar_init(&acc_empty[a], 4 * CG);  // CG 2: rank 0's, released by both CTAs' epilogue warps
     }
     mbar_init(drain, 1);
     mbar_init(ready, 1);
@@ -166,30 +173,70 @@ __global__ void __launch_bounds__(kThreads, 1)
     tma_prefetch_desc(&map_a);
     tma_prefetch_desc(&map_b);
   }
-  if (warp == 1) {
-    tmem_alloc(tmem_slot, 2 * args.tmem_half);
-    tc_fence_before();
-  }
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem_base = *tmem_slot;
-  // A pair writes into both CTAs' stages and barriers: both are set up first.
   const int rank = args.cluster == 2 ? (int)(blockIdx.x & 1) : 0;
-  if (args.cluster == 2) cluster_sync_all();
+  uint32_t tbuf[2];    // the two accumulator buffers
+  int tmem_held = 0;   // CG 2: buffers allocated
+  bool pair_ok = true;
+  if constexpr (CG == 1) {
+    if (warp == 1) {
+      tmem_alloc(tmem_slot, 2 * args.tmem_half);
+      tc_fence_before();
+    }
+    __syncthreads();
+    tc_fence_after();
+    tbuf[0] = *tmem_slot;
+    tbuf[1] = tbuf[0] + args.tmem_half;
+    // A pair writes into both CTAs' stages and barriers: both are set up first.
+    if (args.cluster == 2) cluster_sync_all();
+  } else {
+    // Each buffer is allocated for the pair in its own round of tmem_half
+    // (<= 256) columns, and the two CTAs compare the addresses they got: two
+    // rounds can never wait on each other, and a mismatch stops the kernel
+    // with kStatusPairTmem instead of running MMAs into foreign columns.
+    uint32_t* slots[2] = {tmem_slot, tmem_slot2};
+    for (int round = 0; round < 2 && pair_ok; ++round) {
+      if (warp == 1) {
+        tmem_alloc_pair(slots[round], args.tmem_half);
+        tc_fence_before();
+      }
+      __syncthreads();
+      tc_fence_after();
+      cluster_sync_all();  // (the first one also publishes both CTAs' barriers)
+      tbuf[round] = *slots[round];
+      tmem_held = round + 1;
+      pair_ok = tbuf[round] == ld_cluster_u32(cluster_addr(slots[round], rank ^ 1));
+    }
+    if (!pair_ok && threadIdx.x == 0) {
+      *abort_flag = 1;
+      atomicExch(args.status, kStatusPairTmem);
+    }
+    __syncthreads();
+  }
 
-
-  if (warp == 0) {
+  if (!pair_ok) {
+    // the pair's tensor memory did not match: no work (status recorded)
+  } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
+      // CG 2: both CTAs' loads are counted on rank 0's stage barriers
+      const uint32_t full_c = CG == 2 ? cluster_addr(&full[0], 0) : 0u;
       // Weight tiles do not depend on the preceding kernel: the first stages'
       // weight loads go out before waiting for it (programmatic dependent
       // launch), the activation loads of those stages right after the wait.
       auto load_w = [&](uint8_t* sa, int s, int kb, int mt, int nt) {
-        if (EPI == kEpiPartial) tma_load_2d(sa, &map_a, &full[s], kb * BK, mt * kBM);
+        if constexpr (CG == 2) tma_load_2d_pair(sa, &map_a, full_c + 8u * s, kb * BK, mt * kBM);
+        else if (EPI == kEpiPartial) tma_load_2d(sa, &map_a, &full[s], kb * BK, mt * kBM);
         else tma_load_2d(sa + kA, &map_b, &full[s], kb * BK, nt * args.BN);
       };
       auto load_x = [&](uint8_t* sa, int s, int kb, int mt, int nt) {
-        if (EPI == kEpiPartial && args.cluster == 2) {
+        if constexpr (CG == 2) {
+          // this CTA's half of the activation rows (the MMA's B reads both)
+          const int half = args.BN / 2;
+          tma_load_2d_pair(sa + kA, &map_b, full_c + 8u * s, kb * BK, nt * args.BN + rank * half);
+          if (SPLIT)
+            tma_load_2d_pair(sa + kA + stage_b, &map_b, full_c + 8u * s, kb * BK,
+                             args.split_rows + nt * args.BN + rank * half);
+        } else if (EPI == kEpiPartial && args.cluster == 2) {
           // this CTA's half of the activation rows, to both CTAs of the pair
           const int half = args.BN / 2;
           const int off = rank * half * BK * 2;
@@ -225,7 +272,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int kb = kb0 + i;
           if (!mbar_wait_bounded(&empty[s], phase ^ 1, args.timeout_ns, abort_flag, args.status)) { ok = false; break; }
           uint8_t* sa = smem + s * stage_bytes;
-          mbar_arrive_expect_tx(&full[s], stage_bytes);
+          if (CG == 1) mbar_arrive_expect_tx(&full[s], stage_bytes);
+          else if (rank == 0) mbar_arrive_expect_tx(&full[s], 2 * stage_bytes);  // both CTAs' bytes
           load_w(sa, s, kb, mt, nt);
           if (waited) {
             load_x(sa, s, kb, mt, nt);
@@ -259,7 +307,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA
-    if (lane == 0) {
+    if (lane == 0 && CG == 2 && rank == 1) {
+      // rank 0 issues the pair's MMAs: wait until they have all completed
+      // (they write this CTA's tensor memory) before it is released
+      mbar_wait_bounded(drain, 0, args.timeout_ns, abort_flag, args.status);
+    } else if (lane == 0) {
       bool ok = true;
       int rows = -1;  // read when the first skippable tile comes up
       int s = 0;
@@ -275,13 +327,13 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           if (first_row(mt, nt) >= rows) continue;
         }
-        const uint32_t idesc = idesc_bf16_f32(kBM, args.BN);
+        const uint32_t idesc = idesc_bf16_f32(kBM * CG, args.BN);
         const int kb0 = sg.kb0, kb1 = sg.kb1;
         const int ab = it & 1;
         const uint32_t aphase = (it >> 1) & 1;
         if (!mbar_wait_bounded(&acc_empty[ab], aphase ^ 1, args.timeout_ns, abort_flag, args.status)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + ab * args.tmem_half;
+        const uint32_t d_tmem = tbuf[ab];
         for (int kb = kb0; kb < kb1; ++kb) {  // stage order; the producer picks which K block fills it
           if (!mbar_wait_bounded(&full[s], phase, args.timeout_ns, abort_flag, args.status)) { ok = false; break; }
           tc_fence_after();
@@ -290,25 +342,37 @@ __global__ void __launch_bounds__(kThreads, 1)
           const uint32_t lo_addr = b_addr + stage_b;
 #pragma unroll
           for (int k = 0; k < BK / 16; ++k) {
-            tc_mma_bf16(d_tmem, smem_desc<BK>(a_addr + k * 32), smem_desc<BK>(b_addr + k * 32), idesc,
-                        (kb > kb0 || k > 0) ? 1u : 0u);
-            if (SPLIT) {
-              if (EPI == kEpiPartial)
-                tc_mma_bf16(d_tmem, smem_desc<BK>(a_addr + k * 32), smem_desc<BK>(lo_addr + k * 32), idesc, 1u);
-              else
-                tc_mma_bf16(d_tmem, smem_desc<BK>(lo_addr + k * 32), smem_desc<BK>(b_addr + k * 32), idesc, 1u);
+            if constexpr (CG == 2) {
+              tc_mma_bf16_pair(d_tmem, smem_desc<BK>(a_addr + k * 32), smem_desc<BK>(b_addr + k * 32), idesc,
+                               (kb > kb0 || k > 0) ? 1u : 0u);
+              if (SPLIT)
+                tc_mma_bf16_pair(d_tmem, smem_desc<BK>(a_addr + k * 32), smem_desc<BK>(lo_addr + k * 32), idesc, 1u);
+            } else {
+              tc_mma_bf16(d_tmem, smem_desc<BK>(a_addr + k * 32), smem_desc<BK>(b_addr + k * 32), idesc,
+                          (kb > kb0 || k > 0) ? 1u : 0u);
+              if (SPLIT) {
+                if (EPI == kEpiPartial)
+                  tc_mma_bf16(d_tmem, smem_desc<BK>(a_addr + k * 32), smem_desc<BK>(lo_addr + k * 32), idesc, 1u);
+                else
+                  tc_mma_bf16(d_tmem, smem_desc<BK>(lo_addr + k * 32), smem_desc<BK>(b_addr + k * 32), idesc, 1u);
+              }
             }
           }
-          if (args.cluster == 2) tc_commit_mc(&empty[s], 0x3);
+          if constexpr (CG == 2) tc_commit_pair_mc(&empty[s], 0x3);
+          else if (args.cluster == 2) tc_commit_mc(&empty[s], 0x3);
           else tc_commit(&empty[s]);
           if (++s == args.stages) { s = 0; phase ^= 1; }
         }
-        if (ok) tc_commit(&acc_full[ab]);
+        if (ok) {
+          if constexpr (CG == 2) tc_commit_pair_mc(&acc_full[ab], 0x3);
+          else tc_commit(&acc_full[ab]);
+        }
         ++it;
       }
       // Drain: wait until every MMA issued by this thread has completed, so
       // TMEM can be released safely on every exit path.
-      tc_commit(drain);
+      if constexpr (CG == 2) tc_commit_pair_mc(drain, 0x3);
+      else tc_commit(drain);
       mbar_wait_bounded(drain, 0, args.timeout_ns, abort_flag, args.status);
     }
     __syncwarp();
@@ -334,7 +398,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + ab * args.tmem_half;
+      const uint32_t tbase = tbuf[ab] + ((uint32_t)(q * 32) << 16);
       const int lrow = mt * kBM + q * 32 + lane;  // accumulator row owned by this thread
 
       if (EPI == kEpiPartial) {
@@ -409,7 +473,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(&acc_empty[ab]);
+      if (lane == 0) {
+        if constexpr (CG == 2) mbar_arrive_cluster(cluster_addr(&acc_empty[ab], 0));  // rank 0 issues the MMAs
+        else mbar_arrive(&acc_empty[ab]);
+      }
     }
   }
 
@@ -419,7 +486,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (args.cluster == 2) cluster_sync_all();
   if (warp == 1) {
     tc_fence_after();
-    tmem_dealloc(tmem_base, 2 * args.tmem_half);
+    if constexpr (CG == 2) {
+      for (int r = 0; r < tmem_held; ++r) tmem_dealloc_pair(tbuf[r], args.tmem_half);
+    } else {
+      tmem_dealloc(tbuf[0], 2 * args.tmem_half);
+    }
   }
 }
 
@@ -438,20 +509,28 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act, int allow_pai
   p.split_rows = rows;
   p.bk = kBK;
   p.cluster = 1;
+  p.cg = 1;
   if (epi == kEpiPartial) {
     // features on M, activation rows on N
     p.m_tiles = N / kBM;
     p.BN = rows <= 256 ? ((rows + 15) / 16) * 16 : 256;
     p.n_tiles = (rows + p.BN - 1) / p.BN;
-    // Wider activation tiles take K blocks of 32: a 256-row split stage of
-    // 64 would be 80 KB, two in flight, and the MMAs would wait on every
-    // refill; at 32 it is 40 KB and five are in flight.
-    if (p.BN > 128) p.bk = 32;
-    // Those 64-byte box rows double the TMA requests per byte: CTA pairs on
-    // adjacent weight tiles load half of each activation tile each and
-    // multicast it to both, halving every SM's activation requests.  (Both
-    // halves start on a 1024-byte boundary: BN a multiple of 32.)
-    if (allow_pairs && p.bk == 32 && p.m_tiles % 2 == 0 && p.BN % 32 == 0) p.cluster = 2;
+    // Wider activation tiles: a 256-row split stage of 64-wide K blocks is
+    // 80 KB, only two fit and the MMAs wait on every refill.  CTA pairs on
+    // adjacent weight tiles run one MMA of M = 256 (cta_group::2): each CTA
+    // stages its weight tile and half of the activation rows, a 48 KB stage,
+    // four in flight, with 128-byte TMA rows.  (Both halves of a stage's
+    // activation tile start on a 1024-byte boundary: BN a multiple of 32.)
+    // Shapes that cannot pair take K blocks of 32: 40 KB stages, five in
+    // flight, at twice the TMA requests per byte.
+    if (p.BN > 128) {
+      if (allow_pairs && p.m_tiles % 2 == 0 && p.BN % 32 == 0) {
+        p.cluster = 2;
+        p.cg = 2;
+      } else {
+        p.bk = 32;
+      }
+    }
   } else {
     // activation rows on M, vocab on N (256 per tile)
     p.m_tiles = (rows + kBM - 1) / kBM;
@@ -459,7 +538,7 @@ GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act, int allow_pai
     p.n_tiles = N / p.BN;
   }
   p.kb_total = K / p.bk;
-  const int stage_bytes = stage_bytes_of(epi, p.BN, split_act, p.bk);
+  const int stage_bytes = stage_bytes_of(epi, p.BN / p.cg, split_act, p.bk);
   p.stages = (200 * 1024) / stage_bytes;
   if (p.stages > 8) p.stages = 8;
   if (p.stages < 2) p.stages = 2;
@@ -546,7 +625,8 @@ cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUten
   void (*k)(const CUtensorMap, const CUtensorMap, const KArgs) = nullptr;
   switch (p.epi) {
     case kEpiPartial:
-      if (p.bk == 32) k = p.split_act ? k_gemm_tc<kEpiPartial, 1, 32> : k_gemm_tc<kEpiPartial, 0, 32>;
+      if (p.cg == 2) k = p.split_act ? k_gemm_tc<kEpiPartial, 1, 64, 2> : k_gemm_tc<kEpiPartial, 0, 64, 2>;
+      else if (p.bk == 32) k = p.split_act ? k_gemm_tc<kEpiPartial, 1, 32> : k_gemm_tc<kEpiPartial, 0, 32>;
       else k = p.split_act ? k_gemm_tc<kEpiPartial, 1, 64> : k_gemm_tc<kEpiPartial, 0, 64>;
       break;
     case kEpiSelect: k = p.split_act ? k_gemm_tc<kEpiSelect, 1, 64> : k_gemm_tc<kEpiSelect, 0, 64>; break;
@@ -558,14 +638,15 @@ cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUten
 
 cudaError_t prepare_gemm_kernels() {
   const int lim = 227 * 1024;
-  const void* ks[8] = {(const void*)k_gemm_tc<kEpiPartial, 0, 64>, (const void*)k_gemm_tc<kEpiPartial, 1, 64>,
-                       (const void*)k_gemm_tc<kEpiPartial, 0, 32>, (const void*)k_gemm_tc<kEpiPartial, 1, 32>,
-                       (const void*)k_gemm_tc<kEpiSelect, 0, 64>,  (const void*)k_gemm_tc<kEpiSelect, 1, 64>,
-                       (const void*)k_gemm_tc<kEpiStore, 0, 64>,   (const void*)k_gemm_tc<kEpiStore, 1, 64>};
+  const void* ks[10] = {(const void*)k_gemm_tc<kEpiPartial, 0, 64>,    (const void*)k_gemm_tc<kEpiPartial, 1, 64>,
+                        (const void*)k_gemm_tc<kEpiPartial, 0, 32>,    (const void*)k_gemm_tc<kEpiPartial, 1, 32>,
+                        (const void*)k_gemm_tc<kEpiPartial, 0, 64, 2>, (const void*)k_gemm_tc<kEpiPartial, 1, 64, 2>,
+                        (const void*)k_gemm_tc<kEpiSelect, 0, 64>,     (const void*)k_gemm_tc<kEpiSelect, 1, 64>,
+                        (const void*)k_gemm_tc<kEpiStore, 0, 64>,      (const void*)k_gemm_tc<kEpiStore, 1, 64>};
   cudaError_t e = cudaSuccess;
-  for (int i = 0; i < 8 && e == cudaSuccess; ++i)
+  for (int i = 0; i < 10 && e == cudaSuccess; ++i)
     e = cudaFuncSetAttribute(ks[i], cudaFuncAttributeMaxDynamicSharedMemorySize, lim);
-  for (int i = 0; i < 8 && e == cudaSuccess; ++i)
+  for (int i = 0; i < 10 && e == cudaSuccess; ++i)
     e = cudaFuncSetAttribute(ks[i], cudaFuncAttributePreferredSharedMemoryCarveout, 100);
   return e;
 }

@@ -11,7 +11,7 @@
 namespace dd {
 
 // Device status word values (shared with the host side).
-enum : int { kStatusOk = 0, kStatusTimeout = 1 };
+enum : int { kStatusOk = 0, kStatusTimeout = 1, kStatusPairTmem = 2 };  // status word values
 
 DD_DEV uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -228,6 +228,69 @@ DD_DEV void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// ------------------------------------------------ CTA pairs (cta_group::2)
+// A pair of CTAs (cluster ranks 0 and 1) shares one MMA: rank 0 issues it,
+// each CTA holds half of A (M rows) and half of B (N rows) in its own shared
+// memory and half of the accumulator in its own tensor memory.  Every
+// tcgen05 allocation, MMA and commit of such a kernel uses cta_group::2.
+
+// The shared::cluster address of `local`'s counterpart in cluster rank `rank`.
+DD_DEV uint32_t cluster_addr(const void* local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  return r;
+}
+
+DD_DEV uint32_t ld_cluster_u32(uint32_t caddr) {
+  uint32_t v;
+  asm volatile("ld.shared::cluster.u32 %0, [%1];" : "=r"(v) : "r"(caddr) : "memory");
+  return v;
+}
+
+// Arrive on a barrier of any CTA of the cluster (its shared::cluster address).
+DD_DEV void mbar_arrive_cluster(uint32_t caddr) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(caddr) : "memory");
+}
+
+DD_DEV void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+               "r"(ncols)
+               : "memory");
+}
+
+DD_DEV void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D (M = 256 across the pair) (+)= A * B^T, issued by rank 0.
+DD_DEV void tc_mma_bf16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on the barrier at `bar`'s offset in the CTAs of `cta_mask` once the
+// pair MMAs issued so far by this thread have completed.
+DD_DEV void tc_commit_pair_mc(uint64_t* bar, uint16_t cta_mask) {
+  asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                   smem_u32(bar)),
+               "h"(cta_mask)
+               : "memory");
+}
+
+// A 2D box into this CTA's shared memory whose bytes are counted on the
+// barrier at shared::cluster address `bar_caddr` (this CTA's or its peer's).
+DD_DEV void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, uint32_t bar_caddr, int c0, int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4}], "
+      "[%2];" ::"r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_caddr), "r"(c0), "r"(c1)
       : "memory");
 }
 
