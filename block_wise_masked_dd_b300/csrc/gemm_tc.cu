@@ -25,6 +25,13 @@
 // accumulator buffers let the epilogue of one tile overlap the MMAs of the
 // next.  Every mbarrier wait is bounded; on expiry the kernel records a
 // timeout in the status word and unwinds.
+//
+// Linear layers whose activation tile is wider than 128 rows run as CTA
+// pairs (clusters of two on weight tiles 2p and 2p + 1) sharing one MMA of
+// M = 256 (tcgen05 cta_group::2): each CTA stages its own weight tile and half
+// of the activation rows, rank 0 waits for both CTAs' bytes on its barrier
+// and issues the MMAs, and each CTA's tensor memory receives its own weight
+// tile's accumulator rows for all activation rows.
 #include <math.h>
 
 #include "kernels.h"
@@ -44,8 +51,7 @@ struct KArgs {
   int sk_units;    // > 0: stream-K, each CTA takes this many consecutive (tile, K block) units
   int sk_total;    // units of the whole GEMM (tiles x K blocks)
   int split_rows;  // row offset of the remainder half in the activation map
-  int cluster;     // 1, or 2: CTA pairs (ranks 0, 1) on weight tiles 2p, 2p + 1 share each activation tile
-                   // (by TMA multicast, or, in the cta_group::2 kernel, as the two halves of one MMA's B)
+  int cluster;     // 1, or 2: CTA pairs (ranks 0, 1) on weight tiles 2p, 2p + 1, one MMA of M = 256 (CG 2)
   uint32_t tmem_half;
   GemmOut out;
   int* status;
@@ -159,8 +165,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     for (int s = 0; s < args.stages; ++s) {
       mbar_init(&full[s], 1);
-      // released by the MMAs of every CTA of a multicast pair; CG 2: by rank 0's
-      mbar_init(&empty[s], CG == 2 ? 1 : args.cluster);
+      mbar_init(&empty[s], 1);  // released by this CTA's MMAs (CG 2: rank 0's, to both CTAs)
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&acc_full[a], 1);
@@ -186,8 +191,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     tbuf[0] = *tmem_slot;
     tbuf[1] = tbuf[0] + args.tmem_half;
-    // A pair writes into both CTAs' stages and barriers: both are set up first.
-    if (args.cluster == 2) cluster_sync_all();
   } else {
     // Each buffer is allocated for the pair in its own round of tmem_half
     // (<= 256) columns, and the two CTAs compare the addresses they got: two
@@ -236,14 +239,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           if (SPLIT)
             tma_load_2d_pair(sa + kA + stage_b, &map_b, full_c + 8u * s, kb * BK,
                              args.split_rows + nt * args.BN + rank * half);
-        } else if (EPI == kEpiPartial && args.cluster == 2) {
-          // this CTA's half of the activation rows, to both CTAs of the pair
-          const int half = args.BN / 2;
-          const int off = rank * half * BK * 2;
-          tma_load_2d_mc(sa + kA + off, &map_b, &full[s], kb * BK, nt * args.BN + rank * half, 0x3);
-          if (SPLIT)
-            tma_load_2d_mc(sa + kA + stage_b + off, &map_b, &full[s], kb * BK,
-                           args.split_rows + nt * args.BN + rank * half, 0x3);
         } else if (EPI == kEpiPartial) {
           tma_load_2d(sa + kA, &map_b, &full[s], kb * BK, nt * args.BN);
           if (SPLIT)
@@ -359,7 +354,6 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
           }
           if constexpr (CG == 2) tc_commit_pair_mc(&empty[s], 0x3);
-          else if (args.cluster == 2) tc_commit_mc(&empty[s], 0x3);
           else tc_commit(&empty[s]);
           if (++s == args.stages) { s = 0; phase ^= 1; }
         }

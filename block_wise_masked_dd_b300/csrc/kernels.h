@@ -78,8 +78,8 @@ struct GemmPlan {
   int split_rows;                 // R
   int fused_op;                   // fused plans (plan_gemm_fused): the epilogue op; splits = group size
   int sk_units, sk_total;         // stream-K (> 0): (tile, K block) units per CTA and in all; splits = slots
-  int cluster;                    // 2: CTA pairs on adjacent weight tiles share each activation tile
-  int cg;                         // 2: the pair runs one MMA of M = 256 (cta_group::2); 1: multicast or none
+  int cluster;                    // 2: CTA pairs on adjacent weight tiles (cluster of 2)
+  int cg;                         // 2: the pair runs one MMA of M = 256 (cta_group::2)
   int box_rows_b;                 // rows of the activation operand's TMA box (BN / cluster)
 };
 

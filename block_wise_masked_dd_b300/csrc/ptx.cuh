@@ -126,17 +126,6 @@ DD_DEV void tma_load_2d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, i
       : "memory");
 }
 
-// The same box written to `smem_dst`'s offset in every CTA of the cluster
-// named in `cta_mask`; each destination's barrier at `bar`'s offset receives
-// the bytes (this GPU's own memory only).
-DD_DEV void tma_load_2d_mc(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster [%0], [%1, {%3, "
-      "%4}], [%2], %5;" ::"r"(smem_u32(smem_dst)),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask)
-      : "memory");
-}
-
 DD_DEV void tma_load_3d(void* smem_dst, const CUtensorMap* map, uint64_t* bar, int c0, int c1, int c2) {
   asm volatile(
       "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%3, %4, %5}], "
@@ -292,15 +281,6 @@ DD_DEV void tma_load_2d_pair(void* smem_dst, const CUtensorMap* map, uint32_t ba
       "[%2];" ::"r"(smem_u32(smem_dst)),
       "l"(reinterpret_cast<uint64_t>(map)), "r"(bar_caddr), "r"(c0), "r"(c1)
       : "memory");
-}
-
-// The same arrival on the barrier at `bar`'s offset in every CTA of the
-// cluster named in `cta_mask`.
-DD_DEV void tc_commit_mc(uint64_t* bar, uint16_t cta_mask) {
-  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-                   smem_u32(bar)),
-               "h"(cta_mask)
-               : "memory");
 }
 
 // Arrive on `bar` once every MMA issued so far by this thread has completed.
