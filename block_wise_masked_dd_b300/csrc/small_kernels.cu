@@ -62,7 +62,10 @@ __device__ __forceinline__ void store8_split(__nv_bfloat16* hi, __nv_bfloat16* l
 
 // acc += p[s * stride .. + 8] for s = s0, s0 + 1, ..., s1 - 1 in that order.
 // The loads of up to MAXS partials are issued together before the first add,
-// so a reduce costs about one L2 round trip per MAXS splits.
+// so a reduce costs about one round trip per MAXS splits.  The reduce kernels
+// are compiled for MAXS = 2, 4 and 8 and launched with the smallest that
+// covers the layer's splits: registers held for unused slots would only cap
+// the resident warps, and with them the partial bytes in flight.
 template <int MAXS>
 __device__ __forceinline__ void add_partials(const float* p, int s0, int s1, long long stride, float (&acc)[8]) {
   for (int b = s0; b < s1; b += MAXS) {
@@ -211,7 +214,12 @@ __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const 
 // One CTA per row; the split partial loads of each pass are independent.
 // With cmp (the compaction record of k_embed_norm) rows past the active ones
 // do nothing, and row r belongs to sequence cmp[2 + r / S].
-__global__ void k_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
+// (With two slots, four 256-thread CTAs fit an SM: the large decode's 512
+// rows run in one wave.  Forcing four slots into the same registers spilled
+// and measured no faster.)
+template <int MAXS>
+__global__ void __launch_bounds__(256, MAXS == 2 ? 4 : 2)
+    k_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
                                        const __nv_bfloat16* g, __nv_bfloat16* y, int H, float eps,
                                        const uint32_t* mask, int S, __nv_bfloat16* y_c, int* row_index, int* count,
                                        const int* cmp) {
@@ -234,7 +242,7 @@ __global__ void k_reduce_residual_norm(const float* part, int splits, long long 
     if (p >= passes) break;
     const long long e = (long long)r * H + (p * blockDim.x + threadIdx.x) * 8;
     load8_f32(x + e, xv[p]);
-    add_partials<8>(part + e, 0, splits, split_stride, xv[p]);
+    add_partials<MAXS>(part + e, 0, splits, split_stride, xv[p]);
     store8_f32(x + e, xv[p]);
   }
   // With `mask`: the rows still masked are also written, in order, to y_c
@@ -269,6 +277,7 @@ __global__ void k_reduce_residual_norm(const float* part, int splits, long long 
 }
 
 // out[r][n] = sum over splits of part[s][r][n] (fp32; the standalone GEMM).
+template <int MAXS>
 __global__ void k_reduce(const float* part, int splits, long long split_stride, long long total, float* out) {
   pdl_wait();
   pdl_launch_dependents();
@@ -276,7 +285,7 @@ __global__ void k_reduce(const float* part, int splits, long long split_stride, 
        e += (long long)gridDim.x * blockDim.x * 8) {
     float acc[8];
     load8_f32(part + e, acc);
-    add_partials<8>(part + e, 1, splits, split_stride, acc);
+    add_partials<MAXS>(part + e, 1, splits, split_stride, acc);
     store8_f32(out + e, acc);
   }
 }
@@ -290,6 +299,7 @@ __global__ void k_reduce(const float* part, int splits, long long split_stride, 
 // sine and cosine, the rotation in fp32.  With rope_cs (the step's table of
 // those cosines and sines, [S][D/2], written by the embedding kernel) the
 // rotation reads them instead of recomputing them per element.
+template <int MAXS>
 __global__ void k_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N,
                              __nv_bfloat16* out, int S, int D, int qk_cols, const int* ctx_len, float theta,
                              const int* rows_dev, const float2* rope_cs) {
@@ -305,7 +315,7 @@ __global__ void k_reduce_qkv(const float* part, int splits, long long split_stri
        e += (long long)gridDim.x * blockDim.x * 8) {
     float acc[8];
     load8_f32(part + e, acc);
-    add_partials<8>(part + e, 1, splits, split_stride, acc);
+    add_partials<MAXS>(part + e, 1, splits, split_stride, acc);
     const int n = (int)(e % N);
     if (theta > 0.f && n < qk_cols) {
       const int d0 = n % D;
@@ -404,6 +414,7 @@ __global__ void k_tower_attention(const float* qkv, __nv_bfloat16* out, int rows
 // r = b*S + i is layer n / (2 Hkv D), K or V, kv head, dim) rounded to bf16
 // and stored at cache position T + i, T = *ctx_len; the last CTA to finish
 // then advances *ctx_len by S.
+template <int MAXS>
 __global__ void k_reduce_kv_append(const float* part, int splits, long long split_stride, int rows, int N, int S,
                                    int B, int Hkv, int D, int alloc_ctx, int* ctx_len, __nv_bfloat16* kc,
                                    __nv_bfloat16* vc, unsigned int* done) {
@@ -416,7 +427,7 @@ __global__ void k_reduce_kv_append(const float* part, int splits, long long spli
        e += (long long)gridDim.x * blockDim.x * 8) {
     float acc[8];
     load8_f32(part + e, acc);
-    add_partials<8>(part + e, 1, splits, split_stride, acc);
+    add_partials<MAXS>(part + e, 1, splits, split_stride, acc);
     const int r = (int)(e / N), n = (int)(e % N);
     const int l = n / (2 * kvw), rem = n % (2 * kvw);
     const int h = (rem % kvw) / D, d = rem % D;
@@ -443,6 +454,7 @@ __global__ void k_reduce_kv_append(const float* part, int splits, long long spli
 // h[r][f] = silu(gate) * up, gate = column f, up = column F + f of the
 // summed partials [rows][2F]; head + remainder (remainder at h + rows*F);
 // with rows_dev only the first *rows_dev rows.
+template <int MAXS>
 __global__ void k_reduce_swiglu(const float* part, int splits, long long split_stride, __nv_bfloat16* h, int rows,
                                 int F, const int* rows_dev) {
   pdl_wait();
@@ -457,8 +469,8 @@ __global__ void k_reduce_swiglu(const float* part, int splits, long long split_s
     float gt[8], up[8];
     load8_f32(part + gi, gt);
     load8_f32(part + gi + F, up);
-    add_partials<4>(part + gi, 1, splits, split_stride, gt);
-    add_partials<4>(part + gi + F, 1, splits, split_stride, up);
+    add_partials<MAXS>(part + gi, 1, splits, split_stride, gt);
+    add_partials<MAXS>(part + gi + F, 1, splits, split_stride, up);
     float hv[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) hv[k] = gt[k] / (1.f + expf(-gt[k])) * up[k];
@@ -649,6 +661,16 @@ int grid_for(long long work, int threads) {
   return (int)b;
 }
 
+// The reduce kernels' slot batch for `n` partial slots after the first.
+int slot_batch(int n) { return n <= 2 ? 2 : (n <= 4 ? 4 : 8); }
+
+// The instantiation of a reduce kernel for `n` partial slots after the first.
+template <typename K>
+K pick_batch(int n, K k2, K k4, K k8) {
+  const int b = slot_batch(n);
+  return b == 2 ? k2 : (b == 4 ? k4 : k8);
+}
+
 // threads per row for the row kernels: 8 elements per thread per pass
 int row_threads(int H) {
   int t = H / 8;
@@ -662,12 +684,16 @@ int row_threads(int H) {
 // one the tensor-core kernels need: an SM then never has to drain to change
 // its L1 / shared split before the next kernel's CTAs can join it.
 cudaError_t prepare_small_kernels() {
-  const void* fns[] = {(const void*)k_embed_norm,           (const void*)k_reduce_residual_norm,
-                       (const void*)k_reduce,
-                       (const void*)k_reduce_swiglu,         (const void*)k_select_combine,
-                       (const void*)k_reduce_qkv,
-                       (const void*)k_tower_embed_norm,      (const void*)k_reduce_kv_append,
-                       (const void*)k_tower_attention<64>,   (const void*)k_tower_attention<128>,
+  const void* fns[] = {(const void*)k_embed_norm,              (const void*)k_select_combine,
+                       (const void*)k_reduce_residual_norm<2>,  (const void*)k_reduce_residual_norm<4>,
+                       (const void*)k_reduce_residual_norm<8>,  (const void*)k_reduce<2>,
+                       (const void*)k_reduce<4>,                (const void*)k_reduce<8>,
+                       (const void*)k_reduce_swiglu<2>,         (const void*)k_reduce_swiglu<4>,
+                       (const void*)k_reduce_swiglu<8>,         (const void*)k_reduce_qkv<2>,
+                       (const void*)k_reduce_qkv<4>,            (const void*)k_reduce_qkv<8>,
+                       (const void*)k_reduce_kv_append<2>,      (const void*)k_reduce_kv_append<4>,
+                       (const void*)k_reduce_kv_append<8>,      (const void*)k_tower_embed_norm,
+                       (const void*)k_tower_attention<64>,      (const void*)k_tower_attention<128>,
                        (const void*)k_commit};
   cudaError_t e = cudaSuccess;
   for (const void* f : fns) {
@@ -688,8 +714,9 @@ cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const
 cudaError_t launch_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N, void* out, int S,
                               int D, int qk_cols, const int* ctx_len, float theta, cudaStream_t st,
                               const int* rows_dev, const float2* rope_cs) {
-  return launch_k(k_reduce_qkv, grid_for((long long)rows * N / 8, 256), 256, 0, st, part, splits, split_stride, rows,
-                  N, (__nv_bfloat16*)out, S, D, qk_cols, ctx_len, theta, rows_dev, rope_cs);
+  return launch_k(pick_batch(splits - 1, k_reduce_qkv<2>, k_reduce_qkv<4>, k_reduce_qkv<8>),
+                  grid_for((long long)rows * N / 8, 256), 256, 0, st, part, splits, split_stride, rows, N,
+                  (__nv_bfloat16*)out, S, D, qk_cols, ctx_len, theta, rows_dev, rope_cs);
 }
 
 cudaError_t launch_tower_embed_norm(const int32_t* tokens, const void* embed, const void* g, float* x, void* y,
@@ -709,29 +736,33 @@ cudaError_t launch_tower_attention(const float* qkv, void* out, int rows, int S,
 cudaError_t launch_reduce_kv_append(const float* part, int splits, long long split_stride, int rows, int N, int S,
                                     int B, int Hkv, int D, int alloc_ctx, int* ctx_len, unsigned int* done, void* kc,
                                     void* vc, cudaStream_t st) {
-  return launch_k(k_reduce_kv_append, grid_for((long long)rows * N / 8, 256), 256, 0, st, part, splits, split_stride,
-                  rows, N, S, B, Hkv, D, alloc_ctx, ctx_len, (__nv_bfloat16*)kc, (__nv_bfloat16*)vc, done);
+  return launch_k(pick_batch(splits - 1, k_reduce_kv_append<2>, k_reduce_kv_append<4>, k_reduce_kv_append<8>),
+                  grid_for((long long)rows * N / 8, 256), 256, 0, st, part, splits, split_stride, rows, N, S, B, Hkv,
+                  D, alloc_ctx, ctx_len, (__nv_bfloat16*)kc, (__nv_bfloat16*)vc, done);
 }
 
 cudaError_t launch_reduce_f32(const float* part, int splits, long long split_stride, int rows, int N, float* out,
                               cudaStream_t st) {
   const long long total = (long long)rows * N;
-  return launch_k(k_reduce, grid_for(total / 8, 256), 256, 0, st, part, splits, split_stride, total, out);
+  return launch_k(pick_batch(splits - 1, k_reduce<2>, k_reduce<4>, k_reduce<8>), grid_for(total / 8, 256), 256, 0,
+                  st, part, splits, split_stride, total, out);
 }
 
 cudaError_t launch_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
                                         const void* g, void* y, int rows, int H, float eps, cudaStream_t st,
                                         const uint32_t* mask, int S, void* y_c, int* row_index, int* count,
                                         const int* cmp) {
-  return launch_k(k_reduce_residual_norm, rows, row_threads(H), 0, st, part, splits, split_stride, x,
-                  (const __nv_bfloat16*)g, (__nv_bfloat16*)y, H, eps, mask, S, (__nv_bfloat16*)y_c, row_index, count,
-                  cmp);
+  // (its partial loads start at slot 0)
+  return launch_k(pick_batch(splits, k_reduce_residual_norm<2>, k_reduce_residual_norm<4>, k_reduce_residual_norm<8>),
+                  rows, row_threads(H), 0, st, part, splits, split_stride, x, (const __nv_bfloat16*)g,
+                  (__nv_bfloat16*)y, H, eps, mask, S, (__nv_bfloat16*)y_c, row_index, count, cmp);
 }
 
 cudaError_t launch_reduce_swiglu(const float* part, int splits, long long split_stride, void* h, int rows, int F,
                                  cudaStream_t st, const int* rows_dev) {
-  return launch_k(k_reduce_swiglu, grid_for((long long)rows * F / 8, 256), 256, 0, st, part, splits, split_stride,
-                  (__nv_bfloat16*)h, rows, F, rows_dev);
+  return launch_k(pick_batch(splits - 1, k_reduce_swiglu<2>, k_reduce_swiglu<4>, k_reduce_swiglu<8>),
+                  grid_for((long long)rows * F / 8, 256), 256, 0, st, part, splits, split_stride, (__nv_bfloat16*)h,
+                  rows, F, rows_dev);
 }
 
 cudaError_t launch_select_combine(const float* sel_m, const float* sel_s, const int* sel_a, int n_tiles, int rows,
