@@ -35,6 +35,7 @@ constexpr int kNQ = 64;                  // query rows (MMA M)
 constexpr int kD = 128;                  // head dim
 constexpr int kBox = kKT * 128;          // one [128 keys][64 d] TMA box: 16 KB
 constexpr int kKV = 2 * kBox;            // K or V tile: 32 KB
+constexpr float kRescaleLog2 = 8.f;      // stacked kernel: O' rescaled when a row maximum grows by > 2^8
 constexpr int kRowBox = kNQ * 128;       // one [64 rows][64 cols] box: 8 KB
 constexpr int kQ = 2 * kRowBox;          // Q head or remainder: 16 KB
 constexpr int kP = 2 * kRowBox;          // P head or remainder [64][128 keys]: 16 KB
@@ -87,6 +88,19 @@ __device__ __forceinline__ void tmem_ld_frag(uint32_t taddr, float (&v)[64]) {
       : "memory");
 #pragma unroll
   for (int i = 0; i < 64; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// The inverse of tmem_ld_frag: write the 64 values back to the same 16 rows x
+// 128 columns (same register order), then wait for the stores.
+__device__ __forceinline__ void tmem_st_frag(uint32_t taddr, const float (&v)[64]) {
+  uint32_t r[64];
+#pragma unroll
+  for (int i = 0; i < 64; ++i) r[i] = __float_as_uint(v[i]);
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32,%33,%34,%35,%36,%37,%38,%39,%40,%41,%42,%43,%44,%45,%46,%47,%48,%49,%50,%51,%52,%53,%54,%55,%56,%57,%58,%59,%60,%61,%62,%63,%64};\n\t"
+      "tcgen05.wait::st.sync.aligned;" ::"r"(taddr),
+      "r"(r[0]),"r"(r[1]),"r"(r[2]),"r"(r[3]),"r"(r[4]),"r"(r[5]),"r"(r[6]),"r"(r[7]),"r"(r[8]),"r"(r[9]),"r"(r[10]),"r"(r[11]),"r"(r[12]),"r"(r[13]),"r"(r[14]),"r"(r[15]),"r"(r[16]),"r"(r[17]),"r"(r[18]),"r"(r[19]),"r"(r[20]),"r"(r[21]),"r"(r[22]),"r"(r[23]),"r"(r[24]),"r"(r[25]),"r"(r[26]),"r"(r[27]),"r"(r[28]),"r"(r[29]),"r"(r[30]),"r"(r[31]),"r"(r[32]),"r"(r[33]),"r"(r[34]),"r"(r[35]),"r"(r[36]),"r"(r[37]),"r"(r[38]),"r"(r[39]),"r"(r[40]),"r"(r[41]),"r"(r[42]),"r"(r[43]),"r"(r[44]),"r"(r[45]),"r"(r[46]),"r"(r[47]),"r"(r[48]),"r"(r[49]),"r"(r[50]),"r"(r[51]),"r"(r[52]),"r"(r[53]),"r"(r[54]),"r"(r[55]),"r"(r[56]),"r"(r[57]),"r"(r[58]),"r"(r[59]),"r"(r[60]),"r"(r[61]),"r"(r[62]),"r"(r[63])
+      : "memory");
 }
 
 __device__ __forceinline__ void stmatrix_x4(uint32_t saddr, uint32_t r0, uint32_t r1, uint32_t r2, uint32_t r3) {
@@ -593,29 +607,39 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_pv = idesc_bf16_f32(128, kD) | (1u << 16);  // B (V) MN-major
       const uint32_t p_base = smem_u32(smem + kOffPh);                  // P' [128 rows][128 keys]
       bool ok = true;
-      auto issue_pv = [&](int u) {
+      // O' of an item accumulates over its tiles in one of two TMEM buffers
+      // (the non-empty items alternate); PV of tile u (global tile index) of
+      // the item with non-empty index oi, first/last: its place in the item.
+      auto issue_pv = [&](int u, int oi, bool first, bool last) {
         const int s = u & 1;
         const uint32_t ph = (u >> 1) & 1;
+        const int ob = oi & 1;
         if (!mbar_wait_bounded(&vfull[s], ph, a.timeout_ns, abort_flag, a.status)) return false;
         if (!mbar_wait_bounded(pfull, u & 1, a.timeout_ns, abort_flag, a.status)) return false;
-        if (!mbar_wait_bounded(&ofree[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) return false;
+        // the buffer's previous item has been read out
+        if (first && !mbar_wait_bounded(&ofree[ob], ((oi >> 1) & 1) ^ 1, a.timeout_ns, abort_flag, a.status))
+          return false;
         tc_fence_after();
         const uint32_t vb = smem_u32(smem + kOffV + s * kKV);
 #pragma unroll
         for (int j = 0; j < kKT / 16; ++j) {
           const uint32_t aoff = (j >> 2) * kAtom + (j & 3) * 32;
-          tc_mma_bf16(t_o + s * kD, desc_sw128(p_base + aoff, 0, 1024), desc_sw128(vb + j * 2048, kBox, 1024),
-                      idesc_pv, j > 0 ? 1u : 0u);
+          tc_mma_bf16(t_o + ob * kD, desc_sw128(p_base + aoff, 0, 1024), desc_sw128(vb + j * 2048, kBox, 1024),
+                      idesc_pv, (j > 0 || !first) ? 1u : 0u);
         }
-        tc_commit(&ofull[s]);
+        if (last) tc_commit(&ofull[ob]);
         tc_commit(&vempty[s]);
         tc_commit(pfree);
         return true;
       };
       int g = 0;
+      int oi = -1;                                       // non-empty items so far, minus one
+      int p_oi = 0;                                      // the pending PV's item and place in it
+      bool p_first = false, p_last = false;
       for (int w = blockIdx.x, it = 0; w < n_items && ok; w += gridDim.x, ++it) {
         int split, kvh, b, tile0, nt;
         item(w, split, kvh, b, tile0, nt);
+        if (nt >= 1) ++oi;
         const int qb = it & 1;
         if (!mbar_wait_bounded(&qfull[qb], (it >> 1) & 1, a.timeout_ns, abort_flag, a.status)) { ok = false; break; }
         const uint32_t qa = smem_u32(smem + kOffQ + qb * 2 * kAtom);
@@ -634,11 +658,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_commit(&sfull[s]);
           tc_commit(&kempty[s]);
-          if (g >= 1 && !issue_pv(g - 1)) { ok = false; break; }
+          if (g >= 1 && !issue_pv(g - 1, p_oi, p_first, p_last)) { ok = false; break; }
+          p_oi = oi;
+          p_first = t == 0;
+          p_last = t == nt - 1;
         }
         tc_commit(&qempty[qb]);  // this item's QK^T products are all issued
       }
-      if (ok && g >= 1) issue_pv(g - 1);
+      if (ok && g >= 1) issue_pv(g - 1, p_oi, p_first, p_last);
       tc_commit(drain);
       volatile int no_abort = 0;
       mbar_wait_bounded(drain, 0, a.timeout_ns, &no_abort, a.status);
@@ -681,30 +708,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     };
     bool ok = true;
     int g = 0;
+    int oi = -1;  // non-empty items so far, minus one (their O' buffers alternate)
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       int split, kvh, b, tile0, nt;
       item(w, split, kvh, b, tile0, nt);
-      float o[64];                                  // O rows r0/r1 in fragment order
-#pragma unroll
-      for (int j = 0; j < 64; ++j) o[j] = 0.f;
+      if (nt >= 1) ++oi;
+      const int ob = oi & 1;
+      // O' accumulates in TMEM over the item's tiles.  P is taken against a
+      // reference maximum per query (base-2 units) that moves only when a
+      // tile's maximum exceeds it by more than kRescaleLog2: then, once the
+      // previous PV has completed, the warp rescales its O' rows in TMEM.
+      // Otherwise P <= 2^kRescaleLog2, well inside fp32 and the split P.
       float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-      float al0 = 0.f, al1 = 0.f;                   // rescale of the previous tile
-      auto consume_o = [&](int u, float a0, float a1) {
-        const int s = u & 1;
-        bool wt = true;
-        if (lane == 0) wt = mbar_wait_bounded(&ofull[s], (u >> 1) & 1, a.timeout_ns, abort_flag, a.status);
-        wt = __shfl_sync(0xffffffffu, wt ? 1 : 0, 0) != 0;
-        if (!wt) return false;
-        tc_fence_after();
-        float pv[64];
-        load_sum(t_o + s * kD, pv);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ofree[s]);
-#pragma unroll
-        for (int j = 0; j < 64; ++j) o[j] = fmaf(o[j], (j & 2) ? a1 : a0, pv[j]);
-        return true;
-      };
       for (int t = 0; t < nt; ++t, ++g) {
         const int s = g & 1;
         bool wt = true;
@@ -735,19 +750,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        // running max in base-2 units (scores times c)
-        const float mn0 = fmaxf(m0, mx0 * c), mn1 = fmaxf(m1, mx1 * c);
-        const float a0 = m0 == -INFINITY ? 0.f : ex2(m0 - mn0);
-        const float a1 = m1 == -INFINITY ? 0.f : ex2(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
+        // move the reference (the first tile sets it; O' then starts afresh)
+        float a0 = 1.f, a1 = 1.f;
+        if (mx0 * c > m0 + kRescaleLog2) {
+          a0 = m0 == -INFINITY ? 0.f : ex2(m0 - mx0 * c);
+          m0 = mx0 * c;
+        }
+        if (mx1 * c > m1 + kRescaleLog2) {
+          a1 = m1 == -INFINITY ? 0.f : ex2(m1 - mx1 * c);
+          m1 = mx1 * c;
+        }
+        const bool rescale = t > 0 && __any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f);
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
         for (int j = 0; j < 64; j += 4) {
-          v[j] = ex2(fmaf(v[j], c, -mn0));
-          v[j + 1] = ex2(fmaf(v[j + 1], c, -mn0));
-          v[j + 2] = ex2(fmaf(v[j + 2], c, -mn1));
-          v[j + 3] = ex2(fmaf(v[j + 3], c, -mn1));
+          v[j] = ex2(fmaf(v[j], c, -m0));
+          v[j + 1] = ex2(fmaf(v[j + 1], c, -m0));
+          v[j + 2] = ex2(fmaf(v[j + 2], c, -m1));
+          v[j + 3] = ex2(fmaf(v[j + 3], c, -m1));
           s0 += v[j] + v[j + 1];
           s1 += v[j + 2] + v[j + 3];
         }
@@ -757,12 +777,27 @@ __global__ void __launch_bounds__(kThreads, 1)
         s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
         l0 = l0 * a0 + s0;
         l1 = l1 * a1 + s1;
-        // P' (heads, and remainders 8 rows further) once the previous PV is done
+        // P' (heads, and remainders 8 rows further) once the previous PV is
+        // done; with a moved reference, O' is rescaled first
         if (g >= 1) {
           bool pw = true;
           if (lane == 0) pw = mbar_wait_bounded(pfree, (g - 1) & 1, a.timeout_ns, abort_flag, a.status);
           pw = __shfl_sync(0xffffffffu, pw ? 1 : 0, 0) != 0;
           if (!pw) { ok = false; break; }
+        }
+        if (rescale) {
+          tc_fence_after();
+          float h[64];
+          const uint32_t to = t_o + ob * kD;
+          tmem_ld_frag(to + lane_a, h);  // head and remainder rows of query r0
+#pragma unroll
+          for (int j = 0; j < 64; ++j) h[j] *= a0;
+          tmem_st_frag(to + lane_a, h);
+          tmem_ld_frag(to + lane_b, h);  // ... of query r1
+#pragma unroll
+          for (int j = 0; j < 64; ++j) h[j] *= a1;
+          tmem_st_frag(to + lane_b, h);
+          tc_fence_before();
         }
         const uint32_t pbase = smem_u32(smem + kOffPh);
 #pragma unroll
@@ -779,11 +814,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(pfull);
-        if (t >= 1 && !consume_o(g - 1, al0, al1)) { ok = false; break; }
-        al0 = a0;
-        al1 = a1;
       }
-      if (ok && nt >= 1) ok = consume_o(g - 1, al0, al1);
+      // the item's O' once its last PV has completed
+      float o[64];                                  // O rows r0/r1 in fragment order
+#pragma unroll
+      for (int j = 0; j < 64; ++j) o[j] = 0.f;
+      if (ok && nt >= 1) {
+        bool wt = true;
+        if (lane == 0) wt = mbar_wait_bounded(&ofull[ob], (oi >> 1) & 1, a.timeout_ns, abort_flag, a.status);
+        wt = __shfl_sync(0xffffffffu, wt ? 1 : 0, 0) != 0;
+        if (!wt) { ok = false; }
+        else {
+          tc_fence_after();
+          load_sum(t_o + ob * kD, o);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ofree[ob]);
+        }
+      }
       // partial slot `split`: o (unnormalised, [q][d]), (m, l) per q
       const long long prow = ((long long)(b * a.Hkv + kvh) * n_ctx + split) * kNQ;
 #pragma unroll
