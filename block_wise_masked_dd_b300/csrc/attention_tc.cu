@@ -13,14 +13,17 @@
 // softmax warp owns 16 query rows: row maxima and sums are in-thread plus two
 // quad shuffles, and P (a bf16 head and a bf16 remainder) goes to shared
 // memory with stmatrix in the swizzled K-major layout the PV MMA reads.
-// Each tile's O lands in a fresh TMEM buffer and is folded into registers
-// with the running rescale.
+// O accumulates in TMEM over all tiles of a work item (two buffers, taken by
+// the non-empty items in turn).  P is taken against a reference maximum per
+// query that moves only when a tile's maximum exceeds it by more than 2^8;
+// then the softmax warp rescales its O rows in TMEM between the previous PV
+// and the next (the scheme published with FlashAttention-4), and otherwise
+// P <= 2^8.  Each item's O is read out once.
 //
 // Roles (192 threads): warp 0 streams Q (double-buffered, one per work item)
 // and the K and V tiles with TMA (two slots each; K released after QK^T, V
-// after PV), warp 1 owns TMEM and issues the MMAs, warps 2-5 run the softmax,
-// fold the outputs and write each item's partial.  Every mbarrier wait is
-// bounded.
+// after PV), warp 1 owns TMEM and issues the MMAs, warps 2-5 run the softmax
+// and write each item's partial.  Every mbarrier wait is bounded.
 #include <math.h>
 
 #include "kernels.h"
@@ -35,7 +38,7 @@ constexpr int kNQ = 64;                  // query rows (MMA M)
 constexpr int kD = 128;                  // head dim
 constexpr int kBox = kKT * 128;          // one [128 keys][64 d] TMA box: 16 KB
 constexpr int kKV = 2 * kBox;            // K or V tile: 32 KB
-constexpr float kRescaleLog2 = 8.f;      // stacked kernel: O' rescaled when a row maximum grows by > 2^8
+constexpr float kRescaleLog2 = 8.f;      // O rescaled in TMEM when a row maximum grows by more than 2^8
 constexpr int kRowBox = kNQ * 128;       // one [64 rows][64 cols] box: 8 KB
 constexpr int kQ = 2 * kRowBox;          // Q head or remainder: 16 KB
 constexpr int kP = 2 * kRowBox;          // P head or remainder [64][128 keys]: 16 KB
@@ -255,35 +258,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t idesc_pv = idesc_bf16_f32(kNQ, kD) | (1u << 16);  // B (V) MN-major
       const uint32_t p_h = smem_u32(smem + kOffPh), p_l = smem_u32(smem + kOffPl);
       bool ok = true;
-      auto issue_pv = [&](int u) {
+      // O of an item accumulates over its tiles in one of two TMEM buffers
+      // (the non-empty items alternate); PV of tile u (global tile index) of
+      // the item with non-empty index oi, first/last: its place in the item.
+      auto issue_pv = [&](int u, int oi, bool first, bool last) {
         const int s = u & 1;
         const uint32_t ph = (u >> 1) & 1;
+        const int ob = oi & 1;
         if (!mbar_wait_bounded(&vfull[s], ph, a.timeout_ns, abort_flag, a.status)) return false;
         if (!mbar_wait_bounded(pfull, u & 1, a.timeout_ns, abort_flag, a.status)) return false;
-        if (!mbar_wait_bounded(&ofree[s], ph ^ 1, a.timeout_ns, abort_flag, a.status)) return false;
+        // the buffer's previous item has been read out
+        if (first && !mbar_wait_bounded(&ofree[ob], ((oi >> 1) & 1) ^ 1, a.timeout_ns, abort_flag, a.status))
+          return false;
         tc_fence_after();
         const uint32_t vb = smem_u32(smem + kOffV + s * kKV);
 #pragma unroll
         for (int j = 0; j < kKT / 16; ++j) {
           const uint32_t aoff = (j >> 2) * kRowBox + (j & 3) * 32;
-          tc_mma_bf16(t_o + s * kD, desc_sw128(p_h + aoff, 0, 1024), desc_sw128(vb + j * 2048, kBox, 1024), idesc_pv,
-                      j > 0 ? 1u : 0u);
+          tc_mma_bf16(t_o + ob * kD, desc_sw128(p_h + aoff, 0, 1024), desc_sw128(vb + j * 2048, kBox, 1024),
+                      idesc_pv, (j > 0 || !first) ? 1u : 0u);
         }
 #pragma unroll
         for (int j = 0; j < kKT / 16; ++j) {
           const uint32_t aoff = (j >> 2) * kRowBox + (j & 3) * 32;
-          tc_mma_bf16(t_o + s * kD, desc_sw128(p_l + aoff, 0, 1024), desc_sw128(vb + j * 2048, kBox, 1024), idesc_pv,
-                      1u);
+          tc_mma_bf16(t_o + ob * kD, desc_sw128(p_l + aoff, 0, 1024), desc_sw128(vb + j * 2048, kBox, 1024),
+                      idesc_pv, 1u);
         }
-        tc_commit(&ofull[s]);
+        if (last) tc_commit(&ofull[ob]);
         tc_commit(&vempty[s]);
         tc_commit(pfree);
         return true;
       };
       int g = 0;
+      int oi = -1;                                       // non-empty items so far, minus one
+      int p_oi = 0;                                      // the pending PV's item and place in it
+      bool p_first = false, p_last = false;
       for (int w = blockIdx.x, it = 0; w < n_items && ok; w += gridDim.x, ++it) {
         int split, kvh, b, tile0, nt;
         item(w, split, kvh, b, tile0, nt);
+        if (nt >= 1) ++oi;
         const int qb = it & 1;
         if (!mbar_wait_bounded(&qfull[qb], (it >> 1) & 1, a.timeout_ns, abort_flag, a.status)) { ok = false; break; }
         const uint32_t qh = smem_u32(smem + kOffQ + qb * 2 * kQ), ql = qh + kQ;
@@ -310,11 +323,14 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           tc_commit(&sfull[s]);
           tc_commit(&kempty[s]);
-          if (g >= 1 && !issue_pv(g - 1)) { ok = false; break; }
+          if (g >= 1 && !issue_pv(g - 1, p_oi, p_first, p_last)) { ok = false; break; }
+          p_oi = oi;
+          p_first = t == 0;
+          p_last = t == nt - 1;
         }
         tc_commit(&qempty[qb]);  // this item's QK^T products are all issued
       }
-      if (ok && g >= 1) issue_pv(g - 1);
+      if (ok && g >= 1) issue_pv(g - 1, p_oi, p_first, p_last);
       tc_commit(drain);
       volatile int no_abort = 0;
       mbar_wait_bounded(drain, 0, a.timeout_ns, &no_abort, a.status);
@@ -337,30 +353,17 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int pr1 = (r1 % a.G) * a.S + r1 / a.G;
     bool ok = true;
     int g = 0;
+    int oi = -1;  // non-empty items so far, minus one (their O buffers alternate)
     for (int w = blockIdx.x; w < n_items && ok; w += gridDim.x) {
       int split, kvh, b, tile0, nt;
       item(w, split, kvh, b, tile0, nt);
-      float o[64];                                  // O rows r0/r1 in fragment order
-#pragma unroll
-      for (int j = 0; j < 64; ++j) o[j] = 0.f;
+      if (nt >= 1) ++oi;
+      const int ob = oi & 1;
+      // O accumulates in TMEM over the item's tiles against a reference
+      // maximum per query that moves only when a tile's maximum exceeds it by
+      // more than kRescaleLog2 (then the warp rescales its O rows in TMEM once
+      // the previous PV has completed); read out once per item.
       float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
-      float al0 = 0.f, al1 = 0.f;                   // rescale of the previous tile
-      auto consume_o = [&](int u, float a0, float a1) {
-        const int s = u & 1;
-        bool wt = true;
-        if (lane == 0) wt = mbar_wait_bounded(&ofull[s], (u >> 1) & 1, a.timeout_ns, abort_flag, a.status);
-        wt = __shfl_sync(0xffffffffu, wt ? 1 : 0, 0) != 0;
-        if (!wt) return false;
-        tc_fence_after();
-        float pv[64];
-        tmem_ld_frag(t_o + s * kD + lane_off, pv);
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&ofree[s]);
-#pragma unroll
-        for (int j = 0; j < 64; ++j) o[j] = fmaf(o[j], (j & 2) ? a1 : a0, pv[j]);
-        return true;
-      };
       for (int t = 0; t < nt; ++t, ++g) {
         const int s = g & 1;
         bool wt = true;
@@ -391,19 +394,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, 2));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 1));
         mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, 2));
-        // running max in base-2 units (scores times c)
-        const float mn0 = fmaxf(m0, mx0 * c), mn1 = fmaxf(m1, mx1 * c);
-        const float a0 = m0 == -INFINITY ? 0.f : ex2(m0 - mn0);
-        const float a1 = m1 == -INFINITY ? 0.f : ex2(m1 - mn1);
-        m0 = mn0;
-        m1 = mn1;
+        // move the reference (the first tile sets it; O then starts afresh)
+        float a0 = 1.f, a1 = 1.f;
+        if (mx0 * c > m0 + kRescaleLog2) {
+          a0 = m0 == -INFINITY ? 0.f : ex2(m0 - mx0 * c);
+          m0 = mx0 * c;
+        }
+        if (mx1 * c > m1 + kRescaleLog2) {
+          a1 = m1 == -INFINITY ? 0.f : ex2(m1 - mx1 * c);
+          m1 = mx1 * c;
+        }
+        const bool rescale = t > 0 && __any_sync(0xffffffffu, a0 != 1.f || a1 != 1.f);
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
         for (int j = 0; j < 64; j += 4) {
-          v[j] = ex2(fmaf(v[j], c, -mn0));
-          v[j + 1] = ex2(fmaf(v[j + 1], c, -mn0));
-          v[j + 2] = ex2(fmaf(v[j + 2], c, -mn1));
-          v[j + 3] = ex2(fmaf(v[j + 3], c, -mn1));
+          v[j] = ex2(fmaf(v[j], c, -m0));
+          v[j + 1] = ex2(fmaf(v[j + 1], c, -m0));
+          v[j + 2] = ex2(fmaf(v[j + 2], c, -m1));
+          v[j + 3] = ex2(fmaf(v[j + 3], c, -m1));
           s0 += v[j] + v[j + 1];
           s1 += v[j + 2] + v[j + 3];
         }
@@ -413,12 +421,22 @@ __global__ void __launch_bounds__(kThreads, 1)
         s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
         l0 = l0 * a0 + s0;
         l1 = l1 * a1 + s1;
-        // P (head, remainder) -> shared memory, once the previous PV is done
+        // P (head, remainder) -> shared memory, once the previous PV is done;
+        // with a moved reference, O is rescaled first
         if (g >= 1) {
           bool pw = true;
           if (lane == 0) pw = mbar_wait_bounded(pfree, (g - 1) & 1, a.timeout_ns, abort_flag, a.status);
           pw = __shfl_sync(0xffffffffu, pw ? 1 : 0, 0) != 0;
           if (!pw) { ok = false; break; }
+        }
+        if (rescale) {
+          tc_fence_after();
+          float h[64];
+          tmem_ld_frag(t_o + ob * kD + lane_off, h);
+#pragma unroll
+          for (int j = 0; j < 64; ++j) h[j] *= (j & 2) ? a1 : a0;
+          tmem_st_frag(t_o + ob * kD + lane_off, h);
+          tc_fence_before();
         }
 #pragma unroll
         for (int gg = 0; gg < kKT / 16; ++gg) {
@@ -435,11 +453,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(pfull);
-        if (t >= 1 && !consume_o(g - 1, al0, al1)) { ok = false; break; }
-        al0 = a0;
-        al1 = a1;
       }
-      if (ok && nt >= 1) ok = consume_o(g - 1, al0, al1);
+      // the item's O once its last PV has completed
+      float o[64];                                  // O rows r0/r1 in fragment order
+#pragma unroll
+      for (int j = 0; j < 64; ++j) o[j] = 0.f;
+      if (ok && nt >= 1) {
+        bool wt = true;
+        if (lane == 0) wt = mbar_wait_bounded(&ofull[ob], (oi >> 1) & 1, a.timeout_ns, abort_flag, a.status);
+        wt = __shfl_sync(0xffffffffu, wt ? 1 : 0, 0) != 0;
+        if (!wt) { ok = false; }
+        else {
+          tc_fence_after();
+          tmem_ld_frag(t_o + ob * kD + lane_off, o);
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ofree[ob]);
+        }
+      }
       // partial slot `split`: o (unnormalised, [q][d]), (m, l) per q
       const long long prow = ((long long)(b * a.Hkv + kvh) * n_ctx + split) * kNQ;
 #pragma unroll
