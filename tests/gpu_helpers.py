@@ -57,11 +57,19 @@ def close(got, want, tol, what="", rel_rms=None):
 class Problem:
     """A synthetic decoding problem on both sides."""
 
-    def __init__(self, cfg: synth.Config, seed: int = 0, device="cuda"):
+    def __init__(self, cfg: synth.Config, seed: int = 0, device="cuda", key_growth: float = 0.0):
+        """key_growth > 0 scales the context keys of 128-position tile t by
+        1 + key_growth * t (then rounds them to bf16 again, for both sides):
+        later tiles' scores then exceed the earlier maxima by far, which moves
+        the attention kernels' reference maxima after the first tile."""
         from block_wise_masked_dd_b300.decoder import Decoder, pack_weights
         self.cfg = cfg
         self.w_bits = synth.make_weights(cfg, seed)
         self.k_bits, self.v_bits = synth.make_context_kv(cfg, seed)
+        if key_growth:
+            k = synth.bf16_bits_to_f32(self.k_bits)  # [L][B][Hkv][T][D]
+            scale = 1.0 + key_growth * (np.arange(k.shape[3]) // 128)
+            self.k_bits = synth.to_bf16_bits((k * scale[:, None]).astype(np.float32))
         self.model = oracle.OracleModel.from_bits(cfg, self.w_bits, self.k_bits, self.v_bits,
                                                   synth.bf16_bits_to_f32)
         self.weights = pack_weights(cfg, self.w_bits, device)

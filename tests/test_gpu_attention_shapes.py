@@ -3,7 +3,9 @@ activations) at every query-group shape it takes (G query heads per kv head
 times S block positions = 64 rows): the stacked form (head and remainder rows
 of one M = 128 operand) at G = 2, 4 and 8, and the two-pass M = 64 form at
 G = 16, against the oracle, from the start of a block and from a partly
-committed state, with a context whose last key tile is ragged."""
+committed state, with a context whose last key tile is ragged; and with
+context keys that grow tile by tile, so that the kernels move their
+reference maxima (and rescale the accumulated outputs) after the first tile."""
 import pytest
 
 import synth
@@ -41,3 +43,19 @@ def test_first_step(prob):
 def test_partly_committed_step(prob):
     tok, mask = synth.make_tokens(prob.cfg, seed=41, masked_frac=0.5)
     compare_step(prob, tok, mask, 0.8, logits=False)
+
+
+# 64 (sequence, kv head) pairs and 5 context tiles: two context splits of
+# up to three tiles, so the reference maxima move inside a work item
+GROWING = {"G4_S16": _cfg(32, 16, 8, 2, ctx=640), "G16_S4": _cfg(64, 4, 16, 1, ctx=640)}
+
+
+@pytest.mark.parametrize("shape", list(GROWING))
+def test_first_step_with_growing_keys(shape):
+    require_gpu()
+    p = Problem(GROWING[shape], seed=3, key_growth=16.0)
+    try:
+        tok, mask = p.start_state()
+        compare_step(p, tok, mask, 0.8)
+    finally:
+        p.dec.close()

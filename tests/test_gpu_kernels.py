@@ -37,12 +37,15 @@ def test_gemm_vs_oracle_linear(rows, n, k):
 
 # -------------------------------------------------------------- attention
 
-def _attn_case(B, S, Hq, Hkv, D, T, stride, seed, nan_tail=False):
+def _attn_case(B, S, Hq, Hkv, D, T, stride, seed, nan_tail=False, key_growth=0.0):
     from block_wise_masked_dd_b300.decoder import block_attention
     qkvw = (Hq + 2 * Hkv) * D
     qkv = synth.make_activations(B * S, qkvw, seed=seed)
     rng = np.random.default_rng(seed + 1)
-    kc = synth.to_bf16_bits(rng.standard_normal((B, Hkv, stride, D), dtype=np.float32))
+    k = rng.standard_normal((B, Hkv, stride, D), dtype=np.float32)
+    if key_growth:  # keys of 128-position tile t scaled by 1 + key_growth * t
+        k *= (1.0 + key_growth * (np.arange(stride) // 128))[:, None].astype(np.float32)
+    kc = synth.to_bf16_bits(k)
     vc = synth.to_bf16_bits(rng.standard_normal((B, Hkv, stride, D), dtype=np.float32))
     if nan_tail:  # rows beyond the context length must never reach the output
         kc[:, :, T:, :] = 0x7FC0
@@ -79,6 +82,17 @@ def test_block_attention_ignores_rows_beyond_context(B, S, Hq, Hkv, D, T, stride
 ])
 def test_block_attention_vs_oracle(B, S, Hq, Hkv, D, T, stride):
     _attn_case(B, S, Hq, Hkv, D, T, stride, seed=T + 13 * B)
+
+
+@pytest.mark.parametrize("B,S,Hq,Hkv,D,T,stride", [
+    (32, 16, 8, 2, 128, 1000, 1024),  # tcgen05 path: 64 pairs, two context splits of four tiles
+    (3, 16, 4, 1, 64, 700, 768),      # mma.sync path
+])
+def test_block_attention_with_growing_keys(B, S, Hq, Hkv, D, T, stride):
+    # later tiles' scores exceed the earlier maxima by far: the kernels move
+    # their reference maxima and rescale what they accumulated (the tcgen05
+    # kernel only within a work item, hence enough pairs for multi-tile items)
+    _attn_case(B, S, Hq, Hkv, D, T, stride, seed=29, key_growth=4.0)
 
 
 def test_block_attention_microbench_size_sampled():
