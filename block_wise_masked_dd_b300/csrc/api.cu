@@ -379,7 +379,7 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
       o.split_stride = (long long)R * c->qkvw;
       DD_CUDA(dd::launch_gemm(L.p_qkv, c->m_wqkv[l], c->m_y_b, o, status, c->timeout_ns, st));
       mk(kKGemmQkv);
-      DD_CUDA(dd::launch_reduce_qkv(part, L.p_qkv.splits, o.split_stride, R, c->qkvw, ws + L.qkv, cf.block,
+      DD_CUDA(dd::launch_reduce_qkv(part, dd::slot_plan(L.p_qkv), o.split_stride, R, c->qkvw, ws + L.qkv, cf.block,
                                     cf.head_dim, fo.qk_cols, small_ptr(c) + 2, cf.rope_theta, st, cmp, rope_cs));
       mk(kKReduceQkv);
     }
@@ -437,7 +437,7 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
       o.split_stride = (long long)R * H;
       DD_CUDA(dd::launch_gemm(L.p_o, c->m_wo[l], c->m_attn_b, o, status, c->timeout_ns, st));
       mk(kKGemmO);
-      DD_CUDA(dd::launch_reduce_residual_norm(part, L.p_o.splits, o.split_stride, x, g_mlp + (size_t)l * H * 2, y, R,
+      DD_CUDA(dd::launch_reduce_residual_norm(part, dd::slot_plan(L.p_o), o.split_stride, x, g_mlp + (size_t)l * H * 2, y, R,
                                               H, cf.rms_eps, st, nullptr, cf.block, nullptr, nullptr, nullptr, cmp));
       mk(kKNormO);
       // h = silu(y Wg^T) * (y Wu^T)
@@ -445,7 +445,7 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
       o.split_stride = (long long)R * 2 * F;
       DD_CUDA(dd::launch_gemm(L.p_gu, c->m_wgu[l], c->m_y_b, o, status, c->timeout_ns, st));
       mk(kKGemmGu);
-      DD_CUDA(dd::launch_reduce_swiglu(part, L.p_gu.splits, o.split_stride, ws + L.hmid, R, F, st, cmp));
+      DD_CUDA(dd::launch_reduce_swiglu(part, dd::slot_plan(L.p_gu), o.split_stride, ws + L.hmid, R, F, st, cmp));
       mk(kKSwiglu);
     }
     const void* gn = (l + 1 < cf.n_layers) ? (const void*)(g_attn + (size_t)(l + 1) * H * 2) : c->w.g_final;
@@ -469,7 +469,7 @@ dd_status enqueue_step(dd_ctx* c, cudaStream_t st, const dd_probe* probe, Marker
     // (except on the probe path, which reports every row, and when the LM
     // head has one row tile, which no compaction can skip).
     const bool compact = lm_compact && l + 1 == cf.n_layers;
-    DD_CUDA(dd::launch_reduce_residual_norm(part, L.p_d.splits, o.split_stride, x, gn, y, R, H, cf.rms_eps, st,
+    DD_CUDA(dd::launch_reduce_residual_norm(part, dd::slot_plan(L.p_d), o.split_stride, x, gn, y, R, H, cf.rms_eps, st,
                                             compact ? at<uint32_t>(ws, L.mask) : nullptr, cf.block, ws + L.yc,
                                             at<int>(ws, L.row_index), small_ptr(c) + 6, cmp));
     mk(kKNormDown);
@@ -795,20 +795,20 @@ dd_status dd_append_block(dd_ctx* c, const int32_t* tokens, void* stream) {
   o.split_stride = (long long)R * 3 * W;
   float* tqkv = at<float>(ws, L.qkv);
   DD_CUDA(dd::launch_gemm(L.p_tqkv, c->m_tower_qkv, c->m_y_b, o, small + 1, c->timeout_ns, st));
-  DD_CUDA(dd::launch_reduce_f32(part, L.p_tqkv.splits, o.split_stride, R, 3 * W, tqkv, st));
+  DD_CUDA(dd::launch_reduce_f32(part, dd::slot_plan(L.p_tqkv), o.split_stride, R, 3 * W, tqkv, st));
   // causal self-attention over each committed block -> a (head + remainder)
   DD_CUDA(dd::launch_tower_attention(tqkv, ws + L.attn, R, cf.block, cf.n_kv_heads, cf.head_dim, st));
   // x = e + a Wo^T ; y = RMSNorm(x) g2
   o.ld = H;
   o.split_stride = (long long)R * H;
   DD_CUDA(dd::launch_gemm(L.p_to, c->m_tower_o, c->m_tower_a, o, small + 1, c->timeout_ns, st));
-  DD_CUDA(dd::launch_reduce_residual_norm(part, L.p_to.splits, o.split_stride, x, c->tower.g2, ws + L.y, R, H,
+  DD_CUDA(dd::launch_reduce_residual_norm(part, dd::slot_plan(L.p_to), o.split_stride, x, c->tower.g2, ws + L.y, R, H,
                                           cf.rms_eps, st));
   // K/V of every denoiser layer = y W_kv^T, appended at positions [T, T + S)
   o.ld = N;
   o.split_stride = (long long)R * N;
   DD_CUDA(dd::launch_gemm(L.p_tower, c->m_tower, c->m_y_b, o, small + 1, c->timeout_ns, st));
-  DD_CUDA(dd::launch_reduce_kv_append(o.partial, L.p_tower.splits, o.split_stride, R, N, cf.block, cf.batch,
+  DD_CUDA(dd::launch_reduce_kv_append(o.partial, dd::slot_plan(L.p_tower), o.split_stride, R, N, cf.block, cf.batch,
                                       cf.n_kv_heads, cf.head_dim, L.alloc_ctx, small + 2,
                                       reinterpret_cast<unsigned int*>(small + 5), ws + L.kc, ws + L.vc, st));
   c->ctx_len += cf.block;
@@ -1161,7 +1161,7 @@ dd_status dd_gemm(int32_t rows, int32_t n, int32_t k, const void* x, const void*
   o.ld = n;
   o.rows_valid = rows;
   DD_CUDA(dd::launch_gemm(p, mw, mx, o, reinterpret_cast<int*>(ws), dd::kDefaultTimeoutNs, st));
-  DD_CUDA(dd::launch_reduce_f32(o.partial, p.splits, o.split_stride, rows, n, y, st));
+  DD_CUDA(dd::launch_reduce_f32(o.partial, dd::slot_plan(p), o.split_stride, rows, n, y, st));
   return DD_OK;
 }
 

@@ -79,10 +79,10 @@ __device__ __forceinline__ uint64_t smem_desc(uint32_t saddr) {
 // (linear layers, sk_units > 0): the CTA takes units [c*L, (c+1)*L) of the
 // (tile, K block) sequence, tile by tile, so every CTA does the same number of
 // K blocks; a tile cut between CTAs gets one slot per piece (slot = the CTA's
-// place among the tile's CTAs), and the CTA finishing a tile zero-fills the
-// slots past its pieces so the reduce can sum `splits` slots everywhere.
+// place among the tile's CTAs); the reduce reads a tile's pieces only
+// (slots_of).
 struct Seg {
-  int mt, nt, kb0, kb1, slot, zero_from;  // zero_from: first slot to clear after this piece (splits: none)
+  int mt, nt, kb0, kb1, slot;
   bool first;                             // the CTA's first piece (never skipped)
 };
 
@@ -105,10 +105,7 @@ __device__ __forceinline__ bool seg_of(const KArgs& a, int epi, int i, Seg& g) {
     tile = start / a.kb_total;
     g.kb0 = start - tile * a.kb_total;
     g.kb1 = min(a.kb_total, u1 - tile * a.kb_total);
-    const int first_cta = tile * a.kb_total / a.sk_units;
-    const int last_cta = ((tile + 1) * a.kb_total - 1) / a.sk_units;
-    g.slot = cid - first_cta;
-    g.zero_from = g.kb1 == a.kb_total ? last_cta - first_cta + 1 : a.splits;
+    g.slot = cid - tile * a.kb_total / a.sk_units;  // this piece's place among the tile's workers
   } else {
     const int t = cid + i * workers;
     if (t >= a.tiles_total) return false;
@@ -117,7 +114,6 @@ __device__ __forceinline__ bool seg_of(const KArgs& a, int epi, int i, Seg& g) {
     g.kb0 = split * a.kb_per_split;
     g.kb1 = min(a.kb_total, g.kb0 + a.kb_per_split);
     g.slot = split;
-    g.zero_from = a.splits;
   }
   if (epi == kEpiPartial) { g.nt = tile % a.n_tiles; g.mt = (tile / a.n_tiles) * a.cluster + rank; }
   else { g.mt = tile % m_tiles; g.nt = tile / m_tiles; }
@@ -417,12 +413,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           for (int j = 0; j < 16; ++j) {
             if (row0 + j < args.out.rows_valid) dst[(long long)(row0 + j) * args.out.ld] = v[j];
           }
-        }
-        // stream-K: the tile's slots past its pieces hold zeros
-        for (int z = sg.zero_from; z < args.splits; ++z) {
-          float* zd = args.out.partial + (long long)z * args.out.split_stride + lrow;
-          for (int row = nt * args.BN; row < min((nt + 1) * args.BN, args.out.rows_valid); ++row)
-            zd[(long long)row * args.out.ld] = 0.f;
         }
       } else if (EPI == kEpiSelect) {
         // lrow = activation row, columns = vocab ids nt*BN + c.

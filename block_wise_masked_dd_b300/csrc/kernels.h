@@ -83,6 +83,27 @@ struct GemmPlan {
   int box_rows_b;                 // rows of the activation operand's TMA box (BN / cluster)
 };
 
+// Which partial slots of a linear layer's output hold data: with a uniform
+// K split every tile fills `splits` slots; with stream-K a tile fills one
+// slot per piece it was cut into (its run of K blocks over the workers).
+struct SlotPlan {
+  int splits;    // slots of the partial buffer
+  int sk_units;  // > 0: stream-K, K blocks per worker
+  int kb_total;  // K blocks per tile
+  int n_tiles;   // activation-row tiles
+  int BN;        // activation rows per tile
+  int cluster;   // weight tiles per schedule unit (CTA pairs: 2)
+};
+
+// The slots holding data at (activation row, output feature).
+__host__ __device__ inline int slots_of(const SlotPlan& p, int row, int feature) {
+  if (p.sk_units <= 0) return p.splits;
+  const long long t = (long long)(feature / 128 / p.cluster) * p.n_tiles + row / p.BN;
+  const long long first = t * p.kb_total / p.sk_units;
+  const long long last = ((t + 1) * p.kb_total - 1) / p.sk_units;
+  return (int)(last - first + 1);
+}
+
 struct GemmOut {
   float* partial;          // kEpiPartial: [splits][rows][ld]; kEpiStore: [rows][ld]
   long long split_stride;  // elements between splits
@@ -99,6 +120,9 @@ struct GemmOut {
 // split_act the activation map covers [2*rows][K]: bf16 heads then remainders.
 // allow_pairs = 0: no CTA pairs (every activation map then has BN-row boxes).
 GemmPlan plan_gemm(int epi, int rows, int N, int K, int split_act = 0, int allow_pairs = 1);
+inline SlotPlan slot_plan(const GemmPlan& p) {
+  return SlotPlan{p.splits, p.sk_units, p.kb_total, p.n_tiles, p.BN, p.cluster};
+}
 // Enqueue.  map_w / map_x: 2D bf16 tensor maps with 128-byte swizzle, box
 // {64, 128} for the operand on the MMA M side and {64, BN} for the other.
 cudaError_t launch_gemm(const GemmPlan& p, const CUtensorMap& map_a, const CUtensorMap& map_b, const GemmOut& out,
@@ -273,7 +297,7 @@ cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const
 // to position *ctx_len + r % S (see dd_config.rope_theta).
 // With rows_dev only the first *rows_dev rows (the active ones) are written;
 // with rope_cs the rotation reads the step's table instead of recomputing it.
-cudaError_t launch_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N, void* out, int S,
+cudaError_t launch_reduce_qkv(const float* part, const SlotPlan& sp, long long split_stride, int rows, int N, void* out, int S,
                               int D, int qk_cols, const int* ctx_len, float theta, cudaStream_t st,
                               const int* rows_dev = nullptr, const float2* rope_cs = nullptr);
 // Context tower (dd_append_block): e = embed[token] (fp32, to x) and
@@ -288,21 +312,21 @@ cudaError_t launch_tower_embed_norm(const int32_t* tokens, const void* embed, co
 cudaError_t launch_tower_attention(const float* qkv, void* out_split, int rows, int S, int heads, int D,
                                    cudaStream_t st);
 // `done` is a zeroed counter the kernel leaves zeroed again.
-cudaError_t launch_reduce_kv_append(const float* part, int splits, long long split_stride, int rows, int N, int S,
+cudaError_t launch_reduce_kv_append(const float* part, const SlotPlan& sp, long long split_stride, int rows, int N, int S,
                                     int B, int Hkv, int D, int alloc_ctx, int* ctx_len, unsigned int* done, void* kc,
                                     void* vc, cudaStream_t st);
-cudaError_t launch_reduce_f32(const float* part, int splits, long long split_stride, int rows, int N, float* out,
+cudaError_t launch_reduce_f32(const float* part, const SlotPlan& sp, long long split_stride, int rows, int N, float* out,
                               cudaStream_t st);
 // With mask != nullptr the rows still masked are also written, compacted, to
 // y_c (head rows [0, count), remainders [rows, rows + count)), with
 // row_index[k] = the original row (b*S + i) of compacted row k and *count
 // their number.  With cmp (active-sequence compaction) rows at or past cmp[0]
 // do nothing and row r belongs to sequence cmp[2 + r/S].
-cudaError_t launch_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
+cudaError_t launch_reduce_residual_norm(const float* part, const SlotPlan& sp, long long split_stride, float* x,
                                         const void* g, void* y_split, int rows, int H, float eps, cudaStream_t st,
                                         const uint32_t* mask = nullptr, int S = 1, void* y_c = nullptr,
                                         int* row_index = nullptr, int* count = nullptr, const int* cmp = nullptr);
-cudaError_t launch_reduce_swiglu(const float* part, int splits, long long split_stride, void* h_split, int rows,
+cudaError_t launch_reduce_swiglu(const float* part, const SlotPlan& sp, long long split_stride, void* h_split, int rows,
                                  int F, cudaStream_t st, const int* rows_dev = nullptr);
 // With count/row_index (compacted rows): rows r < *count, written to row_index[r].
 cudaError_t launch_select_combine(const float* sel_m, const float* sel_s, const int* sel_a, int n_tiles, int rows,

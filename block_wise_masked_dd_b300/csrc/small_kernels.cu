@@ -219,7 +219,7 @@ __global__ void k_embed_norm(const int32_t* tokens, const uint32_t* mask, const 
 // and measured no faster.)
 template <int MAXS>
 __global__ void __launch_bounds__(256, MAXS == 2 ? 4 : 2)
-    k_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
+    k_reduce_residual_norm(const float* part, const SlotPlan sp, long long split_stride, float* x,
                                        const __nv_bfloat16* g, __nv_bfloat16* y, int H, float eps,
                                        const uint32_t* mask, int S, __nv_bfloat16* y_c, int* row_index, int* count,
                                        const int* cmp) {
@@ -242,7 +242,7 @@ __global__ void __launch_bounds__(256, MAXS == 2 ? 4 : 2)
     if (p >= passes) break;
     const long long e = (long long)r * H + (p * blockDim.x + threadIdx.x) * 8;
     load8_f32(x + e, xv[p]);
-    add_partials<MAXS>(part + e, 0, splits, split_stride, xv[p]);
+    add_partials<MAXS>(part + e, 0, slots_of(sp, r, (p * blockDim.x + threadIdx.x) * 8), split_stride, xv[p]);
     store8_f32(x + e, xv[p]);
   }
   // With `mask`: the rows still masked are also written, in order, to y_c
@@ -278,14 +278,15 @@ __global__ void __launch_bounds__(256, MAXS == 2 ? 4 : 2)
 
 // out[r][n] = sum over splits of part[s][r][n] (fp32; the standalone GEMM).
 template <int MAXS>
-__global__ void k_reduce(const float* part, int splits, long long split_stride, long long total, float* out) {
+__global__ void k_reduce(const float* part, const SlotPlan sp, long long split_stride, long long total, int N,
+                         float* out) {
   pdl_wait();
   pdl_launch_dependents();
   for (long long e = ((long long)blockIdx.x * blockDim.x + threadIdx.x) * 8; e < total;
        e += (long long)gridDim.x * blockDim.x * 8) {
     float acc[8];
     load8_f32(part + e, acc);
-    add_partials<MAXS>(part + e, 1, splits, split_stride, acc);
+    add_partials<MAXS>(part + e, 1, slots_of(sp, (int)(e / N), (int)(e % N)), split_stride, acc);
     store8_f32(out + e, acc);
   }
 }
@@ -300,7 +301,7 @@ __global__ void k_reduce(const float* part, int splits, long long split_stride, 
 // those cosines and sines, [S][D/2], written by the embedding kernel) the
 // rotation reads them instead of recomputing them per element.
 template <int MAXS>
-__global__ void k_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N,
+__global__ void k_reduce_qkv(const float* part, const SlotPlan sp, long long split_stride, int rows, int N,
                              __nv_bfloat16* out, int S, int D, int qk_cols, const int* ctx_len, float theta,
                              const int* rows_dev, const float2* rope_cs) {
   __shared__ double freq[64];  // theta^(-2j/D), j < D/2 (D <= 128)
@@ -315,7 +316,7 @@ __global__ void k_reduce_qkv(const float* part, int splits, long long split_stri
        e += (long long)gridDim.x * blockDim.x * 8) {
     float acc[8];
     load8_f32(part + e, acc);
-    add_partials<MAXS>(part + e, 1, splits, split_stride, acc);
+    add_partials<MAXS>(part + e, 1, slots_of(sp, (int)(e / N), (int)(e % N)), split_stride, acc);
     const int n = (int)(e % N);
     if (theta > 0.f && n < qk_cols) {
       const int d0 = n % D;
@@ -415,7 +416,7 @@ __global__ void k_tower_attention(const float* qkv, __nv_bfloat16* out, int rows
 // and stored at cache position T + i, T = *ctx_len; the last CTA to finish
 // then advances *ctx_len by S.
 template <int MAXS>
-__global__ void k_reduce_kv_append(const float* part, int splits, long long split_stride, int rows, int N, int S,
+__global__ void k_reduce_kv_append(const float* part, const SlotPlan sp, long long split_stride, int rows, int N, int S,
                                    int B, int Hkv, int D, int alloc_ctx, int* ctx_len, __nv_bfloat16* kc,
                                    __nv_bfloat16* vc, unsigned int* done) {
   pdl_wait();
@@ -427,7 +428,7 @@ __global__ void k_reduce_kv_append(const float* part, int splits, long long spli
        e += (long long)gridDim.x * blockDim.x * 8) {
     float acc[8];
     load8_f32(part + e, acc);
-    add_partials<MAXS>(part + e, 1, splits, split_stride, acc);
+    add_partials<MAXS>(part + e, 1, slots_of(sp, (int)(e / N), (int)(e % N)), split_stride, acc);
     const int r = (int)(e / N), n = (int)(e % N);
     const int l = n / (2 * kvw), rem = n % (2 * kvw);
     const int h = (rem % kvw) / D, d = rem % D;
@@ -455,7 +456,7 @@ __global__ void k_reduce_kv_append(const float* part, int splits, long long spli
 // summed partials [rows][2F]; head + remainder (remainder at h + rows*F);
 // with rows_dev only the first *rows_dev rows.
 template <int MAXS>
-__global__ void k_reduce_swiglu(const float* part, int splits, long long split_stride, __nv_bfloat16* h, int rows,
+__global__ void k_reduce_swiglu(const float* part, const SlotPlan sp, long long split_stride, __nv_bfloat16* h, int rows,
                                 int F, const int* rows_dev) {
   pdl_wait();
   pdl_launch_dependents();
@@ -469,8 +470,8 @@ __global__ void k_reduce_swiglu(const float* part, int splits, long long split_s
     float gt[8], up[8];
     load8_f32(part + gi, gt);
     load8_f32(part + gi + F, up);
-    add_partials<MAXS>(part + gi, 1, splits, split_stride, gt);
-    add_partials<MAXS>(part + gi + F, 1, splits, split_stride, up);
+    add_partials<MAXS>(part + gi, 1, slots_of(sp, (int)r, f), split_stride, gt);
+    add_partials<MAXS>(part + gi + F, 1, slots_of(sp, (int)r, F + f), split_stride, up);
     float hv[8];
 #pragma unroll
     for (int k = 0; k < 8; ++k) hv[k] = gt[k] / (1.f + expf(-gt[k])) * up[k];
@@ -711,11 +712,11 @@ cudaError_t launch_embed_norm(const int32_t* tokens, const uint32_t* mask, const
                   rope_cs, theta, D, ctx_len);
 }
 
-cudaError_t launch_reduce_qkv(const float* part, int splits, long long split_stride, int rows, int N, void* out, int S,
+cudaError_t launch_reduce_qkv(const float* part, const SlotPlan& sp, long long split_stride, int rows, int N, void* out, int S,
                               int D, int qk_cols, const int* ctx_len, float theta, cudaStream_t st,
                               const int* rows_dev, const float2* rope_cs) {
-  return launch_k(pick_batch(splits - 1, k_reduce_qkv<2>, k_reduce_qkv<4>, k_reduce_qkv<8>),
-                  grid_for((long long)rows * N / 8, 256), 256, 0, st, part, splits, split_stride, rows, N,
+  return launch_k(pick_batch(sp.splits - 1, k_reduce_qkv<2>, k_reduce_qkv<4>, k_reduce_qkv<8>),
+                  grid_for((long long)rows * N / 8, 256), 256, 0, st, part, sp, split_stride, rows, N,
                   (__nv_bfloat16*)out, S, D, qk_cols, ctx_len, theta, rows_dev, rope_cs);
 }
 
@@ -733,35 +734,35 @@ cudaError_t launch_tower_attention(const float* qkv, void* out, int rows, int S,
   return launch_k(k_tower_attention<64>, blocks, S * 32, 0, st, qkv, (__nv_bfloat16*)out, rows, S, heads, scale);
 }
 
-cudaError_t launch_reduce_kv_append(const float* part, int splits, long long split_stride, int rows, int N, int S,
+cudaError_t launch_reduce_kv_append(const float* part, const SlotPlan& sp, long long split_stride, int rows, int N, int S,
                                     int B, int Hkv, int D, int alloc_ctx, int* ctx_len, unsigned int* done, void* kc,
                                     void* vc, cudaStream_t st) {
-  return launch_k(pick_batch(splits - 1, k_reduce_kv_append<2>, k_reduce_kv_append<4>, k_reduce_kv_append<8>),
-                  grid_for((long long)rows * N / 8, 256), 256, 0, st, part, splits, split_stride, rows, N, S, B, Hkv,
+  return launch_k(pick_batch(sp.splits - 1, k_reduce_kv_append<2>, k_reduce_kv_append<4>, k_reduce_kv_append<8>),
+                  grid_for((long long)rows * N / 8, 256), 256, 0, st, part, sp, split_stride, rows, N, S, B, Hkv,
                   D, alloc_ctx, ctx_len, (__nv_bfloat16*)kc, (__nv_bfloat16*)vc, done);
 }
 
-cudaError_t launch_reduce_f32(const float* part, int splits, long long split_stride, int rows, int N, float* out,
+cudaError_t launch_reduce_f32(const float* part, const SlotPlan& sp, long long split_stride, int rows, int N, float* out,
                               cudaStream_t st) {
   const long long total = (long long)rows * N;
-  return launch_k(pick_batch(splits - 1, k_reduce<2>, k_reduce<4>, k_reduce<8>), grid_for(total / 8, 256), 256, 0,
-                  st, part, splits, split_stride, total, out);
+  return launch_k(pick_batch(sp.splits - 1, k_reduce<2>, k_reduce<4>, k_reduce<8>), grid_for(total / 8, 256), 256, 0,
+                  st, part, sp, split_stride, total, N, out);
 }
 
-cudaError_t launch_reduce_residual_norm(const float* part, int splits, long long split_stride, float* x,
+cudaError_t launch_reduce_residual_norm(const float* part, const SlotPlan& sp, long long split_stride, float* x,
                                         const void* g, void* y, int rows, int H, float eps, cudaStream_t st,
                                         const uint32_t* mask, int S, void* y_c, int* row_index, int* count,
                                         const int* cmp) {
   // (its partial loads start at slot 0)
-  return launch_k(pick_batch(splits, k_reduce_residual_norm<2>, k_reduce_residual_norm<4>, k_reduce_residual_norm<8>),
-                  rows, row_threads(H), 0, st, part, splits, split_stride, x, (const __nv_bfloat16*)g,
+  return launch_k(pick_batch(sp.splits, k_reduce_residual_norm<2>, k_reduce_residual_norm<4>, k_reduce_residual_norm<8>),
+                  rows, row_threads(H), 0, st, part, sp, split_stride, x, (const __nv_bfloat16*)g,
                   (__nv_bfloat16*)y, H, eps, mask, S, (__nv_bfloat16*)y_c, row_index, count, cmp);
 }
 
-cudaError_t launch_reduce_swiglu(const float* part, int splits, long long split_stride, void* h, int rows, int F,
+cudaError_t launch_reduce_swiglu(const float* part, const SlotPlan& sp, long long split_stride, void* h, int rows, int F,
                                  cudaStream_t st, const int* rows_dev) {
-  return launch_k(pick_batch(splits - 1, k_reduce_swiglu<2>, k_reduce_swiglu<4>, k_reduce_swiglu<8>),
-                  grid_for((long long)rows * F / 8, 256), 256, 0, st, part, splits, split_stride, (__nv_bfloat16*)h,
+  return launch_k(pick_batch(sp.splits - 1, k_reduce_swiglu<2>, k_reduce_swiglu<4>, k_reduce_swiglu<8>),
+                  grid_for((long long)rows * F / 8, 256), 256, 0, st, part, sp, split_stride, (__nv_bfloat16*)h,
                   rows, F, rows_dev);
 }
 
