@@ -20,7 +20,7 @@ def _gpu():
 @pytest.mark.parametrize("rows,n,k", [(16, 768, 256), (48, 384, 192), (128, 3072, 2048), (128, 2048, 5632),
                                       (512, 1024, 1024), (272, 256, 640),
                                       (272, 5632, 4096),
-                                      # stream-K schedules (tiles cut between CTAs, zero-filled slots):
+                                      # stream-K schedules (tiles cut between CTAs, a slot per piece):
                                       (384, 7168, 4096), (512, 4096, 14336),
                                       # K blocks of 32 without CTA pairs (three weight tiles; an N
                                       # tile of 144 rows), and pairs with 80-row halves (N tile 160)
