@@ -859,6 +859,12 @@ dd_status dd_denoise_step_probe(dd_ctx* c, int32_t* tokens, uint32_t* mask, floa
   return DD_OK;
 }
 
+// What a non-zero device status word means (ptx.cuh kStatus*).
+const char* device_status_text(int v) {
+  return v == dd::kStatusPairTmem ? "a pair of GEMM CTAs was given different tensor memory columns"
+                                  : "a kernel's bounded wait expired";
+}
+
 dd_status dd_decode_block(dd_ctx* c, int32_t* tokens, float gamma, int32_t mode, int32_t max_steps,
                           int32_t* steps_out, void* stream) {
   dd_status s = check_ctx(c);
@@ -885,7 +891,7 @@ dd_status dd_decode_block(dd_ctx* c, int32_t* tokens, float gamma, int32_t mode,
     DD_CUDA(cudaStreamSynchronize(st));
     steps = c->hpin[3];
     if (steps_out) *steps_out = steps;
-    if (c->hpin[1] != 0) return fail(DD_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired during step %d", steps);
+    if (c->hpin[1] != 0) return fail(DD_ERR_DEVICE_TIMEOUT, "%s during step %d", device_status_text(c->hpin[1]), steps);
     if (c->hpin[0] != 0) return fail(DD_ERR_STEP_LIMIT, "%d steps without filling the block", max_steps);
     return DD_OK;
   }
@@ -896,7 +902,7 @@ dd_status dd_decode_block(dd_ctx* c, int32_t* tokens, float gamma, int32_t mode,
     DD_CUDA(cudaStreamSynchronize(st));
     if (c->hpin[1] != 0) {
       if (steps_out) *steps_out = steps;
-      return fail(DD_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired during step %d", steps);
+      return fail(DD_ERR_DEVICE_TIMEOUT, "%s during step %d", device_status_text(c->hpin[1]), steps);
     }
     if (c->hpin[0] == 0) {
       done = true;
@@ -915,9 +921,10 @@ dd_status dd_device_status(dd_ctx* c, void* stream) {
   DD_CUDA(cudaMemcpyAsync(c->hpin, small_ptr(c), 8, cudaMemcpyDeviceToHost, st));
   DD_CUDA(cudaStreamSynchronize(st));
   if (c->hpin[1] != 0) {
+    const int v = c->hpin[1];
     DD_CUDA(cudaMemsetAsync(small_ptr(c) + 1, 0, 4, st));
     DD_CUDA(cudaStreamSynchronize(st));
-    return fail(DD_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait expired");
+    return fail(DD_ERR_DEVICE_TIMEOUT, "%s", device_status_text(v));
   }
   return DD_OK;
 }

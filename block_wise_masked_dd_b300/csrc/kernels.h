@@ -7,6 +7,9 @@
 
 namespace dd {
 
+// Values of the device status word (0: ok), set by kernels and read by the host.
+enum : int { kStatusOk = 0, kStatusTimeout = 1, kStatusPairTmem = 2 };
+
 // Launch `kernel` on `st`, allowing programmatic dependent launch when
 // `pdl_enabled()`: the kernel may start while its predecessor drains and must
 // call pdl_wait() before touching the predecessor's outputs (every kernel of

@@ -6,12 +6,11 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "kernels.h"  // kStatus* (the device status word's values)
+
 #define DD_DEV __device__ __forceinline__
 
 namespace dd {
-
-// Device status word values (shared with the host side).
-enum : int { kStatusOk = 0, kStatusTimeout = 1, kStatusPairTmem = 2 };  // status word values
 
 DD_DEV uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

@@ -53,7 +53,8 @@ typedef enum dd_status {
   DD_ERR_CUDA = 2,           /* a CUDA runtime/driver call failed */
   DD_ERR_NOT_READY = 3,      /* weights not set */
   DD_ERR_STEP_LIMIT = 4,     /* dd_decode_block hit max_steps with positions still masked */
-  DD_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait expired; results are invalid */
+  DD_ERR_DEVICE_TIMEOUT = 5, /* a bounded device-side wait expired, or a device-side consistency check
+                                failed (dd_last_error() says which); results are invalid */
   DD_ERR_UNSUPPORTED = 6     /* shape outside what the kernels implement */
 } dd_status;
 
@@ -209,8 +210,9 @@ dd_status dd_decode_block(dd_ctx* ctx, int32_t* tokens, float gamma, int32_t mod
                           int32_t* steps_out, void* stream);
 
 /* Synchronise `stream` and return DD_ERR_DEVICE_TIMEOUT if any kernel of this
- * context recorded an expired wait since the last call (the flag is then
- * cleared), else DD_OK. */
+ * context recorded an expired wait (or a failed device-side check, such as a
+ * pair of GEMM CTAs given different tensor memory) since the last call (the
+ * flag is then cleared), else DD_OK. */
 dd_status dd_device_status(dd_ctx* ctx, void* stream);
 
 const char* dd_status_string(dd_status s);
