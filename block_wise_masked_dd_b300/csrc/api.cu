@@ -673,7 +673,7 @@ dd_status dd_create(const dd_config* cfg, void* workspace, size_t workspace_byte
     c->f_d = dd::plan_gemm_fused(dd::kOpResidual, c->R, cf.hidden, cf.mlp);
     c->fused_ok = c->f_qkv.fused_op >= 0 && c->f_o.fused_op >= 0 && c->f_gu.fused_op >= 0 &&
                   c->f_d.fused_op >= 0 && L.p_qkv.BN == c->R && L.p_o.BN == c->R && L.p_d.BN == c->R &&
-                  L.p_qkv.bk == 64;  // the fused kernel reads 64-wide K blocks
+                  L.p_qkv.bk == 64 && L.p_qkv.cluster == 1;  // 64-wide K blocks, BN-row activation boxes
   }
   // Measured on the small decode workload the fused layers lose to the
   // separate reduce kernels inside the step graph, so they are opt-in.
