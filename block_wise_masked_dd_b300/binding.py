@@ -94,6 +94,7 @@ _SIGS = {
                           c_void_p], c_int32),
     "dd_gemm_workspace_size": ([c_int32, c_int32, c_int32, ctypes.POINTER(c_size_t)], c_int32),
     "dd_gemm": ([c_int32, c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p], c_int32),
+    "dd_gemm_plan_query": ([c_int32, c_int32, c_int32, c_int32, c_void_p, c_int32], c_int32),
     "dd_commit": ([c_int32, c_int32, c_void_p, c_void_p, c_void_p, c_void_p, c_float, c_int32, c_void_p, c_void_p,
                    c_void_p], c_int32),
     "dd_test_wait_timeout": ([c_int32, c_void_p, c_void_p], c_int32),
@@ -235,6 +236,18 @@ def dd_gemm_workspace_size(rows: int, n: int, k: int) -> int:
     out = c_size_t(0)
     _check(load().dd_gemm_workspace_size(rows, n, k, ctypes.byref(out)))
     return out.value
+
+
+GEMM_PLAN_FIELDS = ("grid", "cluster", "cg", "bk", "BN", "m_tiles", "n_tiles", "kb_total", "splits", "kb_per_split",
+                    "sk_units", "sk_total", "stages", "smem_bytes")
+
+
+def dd_gemm_plan_query(rows: int, n: int, k: int, split_act: int = 1) -> dict:
+    """The tensor-core GEMM's plan for a linear layer (host only), as a dict
+    keyed by GEMM_PLAN_FIELDS (the order of dd.h)."""
+    out = (c_int32 * len(GEMM_PLAN_FIELDS))()
+    _check(load().dd_gemm_plan_query(rows, n, k, split_act, ctypes.cast(out, c_void_p), len(GEMM_PLAN_FIELDS)))
+    return dict(zip(GEMM_PLAN_FIELDS, list(out)))
 
 
 def dd_gemm(rows: int, n: int, k: int, x: int, w: int, y: int, workspace: int, workspace_bytes: int,

@@ -1147,6 +1147,18 @@ dd_status dd_gemm_workspace_size(int32_t rows, int32_t n, int32_t k, size_t* byt
   return DD_OK;
 }
 
+dd_status dd_gemm_plan_query(int32_t rows, int32_t n, int32_t k, int32_t split_act, int32_t* out, int32_t n_out) {
+  if (rows < 16 || rows % 16 || n < 128 || n % 128 || k < 64 || k % 64)
+    return fail(DD_ERR_UNSUPPORTED, "need rows %% 16 == 0, n %% 128 == 0, k %% 64 == 0");
+  if (!out || n_out < 0) return fail(DD_ERR_INVALID_ARG, "out is NULL or n_out < 0");
+  const dd::GemmPlan p = dd::plan_gemm(dd::kEpiPartial, rows, n, k, split_act ? 1 : 0);
+  const int32_t v[DD_GEMM_PLAN_FIELDS] = {p.grid,     p.cluster,  p.cg,           p.bk,       p.BN,
+                                          p.m_tiles,  p.n_tiles,  p.kb_total,     p.splits,   p.kb_per_split,
+                                          p.sk_units, p.sk_total, p.stages,       p.smem_bytes};
+  for (int i = 0; i < n_out && i < DD_GEMM_PLAN_FIELDS; ++i) out[i] = v[i];
+  return DD_OK;
+}
+
 dd_status dd_gemm(int32_t rows, int32_t n, int32_t k, const void* x, const void* w, float* y, void* workspace,
                   size_t workspace_bytes, void* stream) {
   size_t need = 0;

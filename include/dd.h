@@ -376,6 +376,18 @@ dd_status dd_gemm_workspace_size(int32_t rows, int32_t n, int32_t k, size_t* byt
 dd_status dd_gemm(int32_t rows, int32_t n, int32_t k, const void* x, const void* w, float* y,
                   void* workspace, size_t workspace_bytes, void* stream);
 
+/* The plan the tensor-core GEMM takes for a linear layer of `rows` activation
+ * rows (split_act != 0: bf16 head + remainder rows, as in the denoising step),
+ * n outputs and k inputs (rows % 16 == 0, n % 128 == 0, k % 64 == 0).  Host
+ * only: no device is touched.  Writes up to n_out of, in order: grid (CTAs),
+ * cluster (1, or 2 for CTA pairs), cg (2: one MMA of M = 256 per pair),
+ * bk (K elements per block), BN (activation rows per tile), m_tiles, n_tiles,
+ * kb_total (K blocks per tile), splits (partial slots), kb_per_split,
+ * sk_units (> 0: stream-K, K blocks per worker), sk_total, stages, smem_bytes.
+ * For tests and tuning. */
+enum { DD_GEMM_PLAN_FIELDS = 14 };
+dd_status dd_gemm_plan_query(int32_t rows, int32_t n, int32_t k, int32_t split_act, int32_t* out, int32_t n_out);
+
 /* The commit rule alone (explainer steps 3-4) on given confidences and ids.
  * conf: fp32 [B][S], arg: int32 [B][S], tokens: int32 [B][S] (updated),
  * mask: uint32 [B] (updated), n_committed: int32 [B], remaining: int32 [1]
