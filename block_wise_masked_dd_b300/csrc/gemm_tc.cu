@@ -213,7 +213,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   if (!pair_ok) {
-    // the pair's tensor memory did not match: no work (status recorded)
+    // the pair's tensor memory did not match: no work (status recorded); the
+    // grid still completes only after its predecessor, as every kernel does
+    if (threadIdx.x == 0) {
+      pdl_wait();
+      pdl_launch_dependents();
+    }
   } else if (warp == 0) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
