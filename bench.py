@@ -342,7 +342,7 @@ def oracle_sample(dec, model, cfg, T0, gamma, mode, dev, budget_s=ORACLE_SAMPLE_
 # units processed, so the ratio carries over); the line's `traffic` is this
 # ratio times the launch's algorithmic bytes.  Kinds and workloads not
 # captured report null.
-TRAFFIC = {("small", "gemm_gate_up"): ((47.246e6 + 0.167e6) / 49545216,
+TRAFFIC = {("small", "gemm_gate_up"): ((47.241e6 + 0.351e6) / 49545216,
                                        "ncu capture of the small workload's gate|up launch"),
            ("large", "attention_context"): ((4303.529e6 + 32.699e6) / (2 * 2 * 32 * 8 * 32768 * 128 + 2 * 512 * 10240),
                                             "ncu capture of k_attn_ctx_stk<4> at the large layer shapes "
