@@ -42,6 +42,19 @@ METRIC = "committed tokens/sec on 1 B300 (block 16, γ=0.8); block-attn HBM GB/s
 UNIT = "tokens/s"
 
 
+def oracle_threads() -> int:
+    """Threads the oracle's arithmetic runs on: the size of NumPy's BLAS
+    thread pool (its matrix products), else the CPUs this process may use."""
+    try:
+        from threadpoolctl import threadpool_info
+        n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
+        if n:
+            return int(max(n))
+    except Exception:  # threadpoolctl missing or the BLAS not introspectable
+        pass
+    return len(os.sched_getaffinity(0))
+
+
 def mode_arg(s: str) -> str:
     if s in ("threshold", "mock_ar"):
         return s
@@ -274,7 +287,7 @@ def run_reference(args, world, rank):
         committed += step()
     dt = time.perf_counter() - t0
     value = committed / dt
-    sample = (f"oracle (NumPy fp32, {os.cpu_count()} host threads): {args.steps} denoising steps of one sequence "
+    sample = (f"oracle (NumPy fp32, {oracle_threads()} host threads): {args.steps} denoising steps of one sequence "
               f"of the {cfg.name} workload after {args.warmup} untimed ones, walking a block's decode "
               f"({committed} positions committed in {dt:.1f} s); sequences are independent, so the batch's "
               f"rate is the same per-sequence rate (its work scales with the batch)")
@@ -283,9 +296,9 @@ def run_reference(args, world, rank):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
             "data": "synthetic",
             "config": {"workload": workload_desc(cfg, args.gamma, args.mode), "tokens_per_step": committed / args.steps,
-                       "parallelism": f"host cores ({os.cpu_count()} threads), rank 0 only",
+                       "parallelism": f"host cores ({oracle_threads()} threads), rank 0 only",
                        "sample": "one sequence of the workload, one denoising step per step"},
-            "cpu_baseline": {"value": value, "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -639,7 +652,7 @@ def measure_workload(args, cfg, dev, world, rank, local, peaks, steps, warmup, f
         o = oracle_sample(dec, model, cfg, T0, args.gamma, mode, dev)
         del model
         line["cpu_baseline"] = {
-            "value": o["value"], "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+            "value": o["value"], "unit": UNIT, "cores": oracle_threads(), "kind": "oracle",
             "sample": (f"oracle (NumPy fp32) on sequence 0 of the {cfg.name} workload at gamma {args.gamma}: "
                        f"{o['steps']} denoising steps of a block from the CUDA path's states, "
                        f"{o['committed']} positions committed in {o['seconds']:.1f} s "

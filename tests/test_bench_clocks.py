@@ -1,5 +1,6 @@
-"""bench.py's clock sampler: parsing of the nvidia-smi samples it records
-beside every measurement (no GPU: the sampler's process is faked)."""
+"""bench.py's host-side helpers: parsing of the nvidia-smi clock samples it
+records beside every measurement (no GPU: the sampler's process is faked),
+and the oracle's thread count it reports with the CPU baseline."""
 import os
 import sys
 
@@ -51,3 +52,13 @@ def test_no_samples_gives_none():
     s = bench.ClockSampler.__new__(bench.ClockSampler)
     s.proc = None
     assert s.stop() is None
+
+
+def test_oracle_thread_count_follows_the_blas_pool():
+    """`cpu_baseline.cores` reports the oracle's BLAS threads, not the CPU count."""
+    import subprocess
+    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
+    out = subprocess.run([sys.executable, "-c", "import bench; print(bench.oracle_threads())"], cwd=ROOT, env=env,
+                         capture_output=True, text=True, timeout=120, check=True).stdout
+    assert int(out.strip()) == 1
+    assert bench.oracle_threads() >= 1
