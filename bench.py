@@ -44,15 +44,36 @@ UNIT = "tokens/s"
 
 def oracle_threads() -> int:
     """Threads the oracle's arithmetic runs on: the size of NumPy's BLAS
-    thread pool (its matrix products), else the CPUs this process may use."""
+    thread pool (its matrix products).  Asked of threadpoolctl where it is
+    installed, else of the OpenBLAS that NumPy bundles; failing both, the
+    thread count OpenBLAS takes by default (its environment variables, else
+    the CPUs this process may use)."""
     try:
         from threadpoolctl import threadpool_info
         n = [i["num_threads"] for i in threadpool_info() if i.get("user_api") == "blas"]
         if n:
             return int(max(n))
-    except Exception:  # threadpoolctl missing or the BLAS not introspectable
+    except Exception:  # not installed, or the BLAS not introspectable
         pass
-    return len(os.sched_getaffinity(0))
+    import ctypes
+    import glob
+    libs = os.path.join(os.path.dirname(os.path.dirname(np.__file__)), "numpy.libs")
+    for path in sorted(glob.glob(os.path.join(libs, "*openblas*.so*"))):
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for sym in ("scipy_openblas_get_num_threads64_", "openblas_get_num_threads64_", "openblas_get_num_threads"):
+            f = getattr(lib, sym, None)
+            if f is not None:
+                f.restype = ctypes.c_int
+                return int(f())
+    cpus = len(os.sched_getaffinity(0))
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS"):
+        v = os.environ.get(var, "")
+        if v.isdigit() and int(v) > 0:
+            return min(int(v), cpus)
+    return cpus
 
 
 def mode_arg(s: str) -> str:

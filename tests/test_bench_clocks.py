@@ -54,11 +54,26 @@ def test_no_samples_gives_none():
     assert s.stop() is None
 
 
+_HIDE_THREADPOOLCTL = """
+import builtins
+real = builtins.__import__
+def imp(name, *a, **k):
+    if name.startswith("threadpoolctl"):
+        raise ImportError(name)
+    return real(name, *a, **k)
+builtins.__import__ = imp
+"""
+
+
 def test_oracle_thread_count_follows_the_blas_pool():
-    """`cpu_baseline.cores` reports the oracle's BLAS threads, not the CPU count."""
+    """`cpu_baseline.cores` reports the oracle's BLAS threads, not the CPU
+    count: through threadpoolctl, and without it (from NumPy's own OpenBLAS)."""
     import subprocess
-    env = dict(os.environ, OPENBLAS_NUM_THREADS="1", OMP_NUM_THREADS="1", MKL_NUM_THREADS="1")
-    out = subprocess.run([sys.executable, "-c", "import bench; print(bench.oracle_threads())"], cwd=ROOT, env=env,
-                         capture_output=True, text=True, timeout=120, check=True).stdout
-    assert int(out.strip()) == 1
+    for prelude in ("", _HIDE_THREADPOOLCTL):
+        for n in (1, 3):
+            env = dict(os.environ, OPENBLAS_NUM_THREADS=str(n), OMP_NUM_THREADS=str(n))
+            code = prelude + "import bench, oracle\nprint(bench.oracle_threads())\n"
+            out = subprocess.run([sys.executable, "-c", code], cwd=ROOT, env=env, capture_output=True, text=True,
+                                 timeout=120, check=True).stdout
+            assert int(out.strip()) == min(n, len(os.sched_getaffinity(0))), (prelude != "", n, out)
     assert bench.oracle_threads() >= 1
