@@ -910,6 +910,7 @@ dd_status dd_decode_block(dd_ctx* c, int32_t* tokens, float gamma, int32_t mode,
     }
   }
   DD_CUDA(cudaMemcpyAsync(tokens, ws + c->L.tok, (size_t)c->R * 4, cudaMemcpyDefault, st));
+  DD_CUDA(cudaStreamSynchronize(st));  // host `tokens` hold the ids on return, as on the graph path
   if (steps_out) *steps_out = steps;
   if (!done) return fail(DD_ERR_STEP_LIMIT, "%d steps without filling the block", max_steps);
   return DD_OK;
