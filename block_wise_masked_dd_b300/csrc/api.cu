@@ -573,6 +573,17 @@ bool ensure_loop_graph(dd_ctx* c) {
   return ok;
 }
 
+// Drop the captured graphs (the step's and the decode loop's): they hold the
+// weights' tensor maps and pointers and the options' kernel choices by value.
+// An executable graph still in flight is freed once it completes.
+void drop_graphs(dd_ctx* c) {
+  if (c->exec) cudaGraphExecDestroy(c->exec);
+  if (c->loop_exec) cudaGraphExecDestroy(c->loop_exec);
+  c->exec = nullptr;
+  c->loop_exec = nullptr;
+  c->loop_tried = false;
+}
+
 dd_status check_ctx(dd_ctx* c) {
   if (!c) return fail(DD_ERR_INVALID_ARG, "ctx is NULL");
   if (!c->have_weights) return fail(DD_ERR_NOT_READY, "weights not set (call dd_init_weights)");
@@ -720,10 +731,7 @@ dd_status dd_init_weights(dd_ctx* c, const dd_weights* w) {
   if (!ok) return fail(DD_ERR_CUDA, "tensor map encoding failed for the weights");
   c->w = *w;
   c->have_weights = true;
-  if (c->exec) {
-    cudaGraphExecDestroy(c->exec);
-    c->exec = nullptr;
-  }
+  drop_graphs(c);  // both graphs captured the previous weights
   return DD_OK;
 }
 
@@ -951,11 +959,7 @@ dd_status dd_set_option(dd_ctx* c, int32_t option, int32_t value) {
   if ((value != 0) != flag) {
     // the captured graphs hold the other path
     DD_CUDA(cudaDeviceSynchronize());
-    if (c->exec) cudaGraphExecDestroy(c->exec);
-    if (c->loop_exec) cudaGraphExecDestroy(c->loop_exec);
-    c->exec = nullptr;
-    c->loop_exec = nullptr;
-    c->loop_tried = false;
+    drop_graphs(c);
     flag = value != 0;
   }
   return DD_OK;

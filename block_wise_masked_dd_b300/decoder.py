@@ -81,6 +81,12 @@ class Decoder:
             self.ctx = B.dd_create(self.cstruct, _ptr(self.workspace), nbytes)
             B.dd_init_weights(self.ctx, weights_struct(weights))
 
+    def set_weights(self, weights: dict):
+        """Point the context at another set of packed weights (kept alive here)."""
+        with torch.cuda.device(self.device):
+            B.dd_init_weights(self.ctx, weights_struct(weights))
+        self.weights = weights
+
     def close(self):
         if getattr(self, "ctx", None):
             B.dd_destroy(self.ctx)

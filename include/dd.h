@@ -133,7 +133,10 @@ void dd_destroy(dd_ctx* ctx);
  * and 16-byte aligned.  The decoder weights follow the pre-norm dense
  * transformer reading of the TwoTower denoising tower (attention, then
  * SwiGLU MLP, per layer; final RMSNorm; untied LM head).  Synchronous on the
- * host; enqueues nothing. */
+ * host; enqueues nothing.  May be called again with other weights: the calls
+ * after it use the new ones (the step and decode-loop graphs are captured
+ * anew); work already enqueued still reads the previous weights, which must
+ * stay valid until it completes. */
 dd_status dd_init_weights(dd_ctx* ctx, const dd_weights* w);
 
 /* Write context K/V for positions [t0, t0+n) of every layer and sequence and

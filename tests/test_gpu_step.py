@@ -316,3 +316,36 @@ def test_compacted_lm_head_small(small, masked_frac):
     compaction, since the single tile always runs)."""
     tok, mask = synth.make_tokens(small.cfg, seed=int(masked_frac * 100) + 1, masked_frac=masked_frac)
     _graph_step_vs_oracle(small, tok, mask)
+
+
+def test_weights_set_again_reach_both_graphs():
+    """dd_init_weights with another weight set after both graphs were captured:
+    the single-step graph and the decode-loop graph then run the new weights,
+    bit for bit as a context created with them (the previous weights stay
+    allocated meanwhile)."""
+    require_gpu()
+    from block_wise_masked_dd_b300.decoder import Decoder, pack_weights
+    cfg = synth.TINY
+    a = Problem(cfg, seed=0)
+    w_b = pack_weights(cfg, synth.make_weights(cfg, 1), "cuda")
+    fresh = Decoder(cfg, w_b, "cuda")
+    fresh.set_context_kv(a.k_dev, a.v_dev, 0)
+    ref_block, ref_steps = fresh.decode_block(0.8)
+    tok, mask = a.start_state()
+    t_ref, m_ref = a.gpu_state(tok, mask)
+    fresh.denoise_step(t_ref, m_ref, 0.8)
+    old_block, _ = a.dec.decode_block(0.8)  # captures both graphs with the first weights
+    t0, m0 = a.gpu_state(tok, mask)
+    a.dec.denoise_step(t0, m0, 0.8)
+    keep = a.dec.weights
+    a.dec.set_weights(w_b)
+    new_block, new_steps = a.dec.decode_block(0.8)
+    t1, m1 = a.gpu_state(tok, mask)
+    a.dec.denoise_step(t1, m1, 0.8)
+    torch.cuda.synchronize()
+    assert new_steps == ref_steps and torch.equal(new_block, ref_block)
+    assert torch.equal(t1, t_ref) and torch.equal(m1, m_ref)
+    assert not torch.equal(old_block, new_block)  # the two weight sets decode differently
+    fresh.close()
+    a.dec.close()
+    del keep
