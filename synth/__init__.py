@@ -82,14 +82,11 @@ class Config:
     def replace(self, **kw) -> "Config":
         return dataclasses.replace(self, **kw)
 
-    def n_params(self) -> int:
-        H, D, F, V = self.hidden, self.head_dim, self.mlp, self.vocab
-        per_layer = (self.qkv_width * H + H * self.n_q_heads * D + 3 * F * H + 2 * H)
-        return (V + 1) * H + self.block * H + self.n_layers * per_layer + H + V * H
-
 
 # The five workloads of the decoding study.  TINY is the case the oracle
-# finishes in seconds; SMALL is the decode workload throughput is quoted on.
+# finishes in seconds; SMALL a mid-size decode workload; LARGE the largest
+# decode workload one GPU holds, the one throughput is quoted on; the two
+# microbenchmarks time the block attention and the LM head + select alone.
 TINY = Config("tiny", batch=1, block=16, hidden=256, n_q_heads=4, n_kv_heads=4,
               head_dim=64, n_layers=2, mlp=1024, vocab=4096, ctx_len=256, max_ctx=256)
 SMALL = Config("small", batch=8, block=16, hidden=2048, n_q_heads=16, n_kv_heads=4,
@@ -254,11 +251,6 @@ def make_activations(rows: int, width: int, seed: int = 0, std: float = 1.0) -> 
     """A bf16 activation matrix [rows, width] ~ N(0, std^2) (bits)."""
     rng = np.random.default_rng(np.random.SeedSequence([seed, 0x414354, rows, width]))
     return _normal_bf16(rng, (rows, width), std)
-
-
-def make_qkv(cfg: Config, seed: int = 0) -> np.ndarray:
-    """Block-attention inputs: the packed q|k|v rows [B*S, (Hq+2Hkv)*D] ~ N(0,1) (bits)."""
-    return make_activations(cfg.rows, cfg.qkv_width, seed, 1.0)
 
 
 # ---------------------------------------------------------------------------
