@@ -893,7 +893,6 @@ int attention_tc_splits(int B, int Hkv, int max_ctx) {
   return attn_ctx_splits(B * Hkv, (max_ctx + kKT - 1) / kKT, 32);
 }
 
-int attention_tc_smem_bytes() { return kSmemBytes; }
 
 bool attention_tc_stacked_supported(int G, int S) { return (G == 2 || G == 4 || G == 8) && G * S == kNQ; }
 

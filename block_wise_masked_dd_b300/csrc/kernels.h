@@ -10,12 +10,10 @@ namespace dd {
 // Values of the device status word (0: ok), set by kernels and read by the host.
 enum : int { kStatusOk = 0, kStatusTimeout = 1, kStatusPairTmem = 2 };
 
-// Launch `kernel` on `st`, allowing programmatic dependent launch when
-// `pdl_enabled()`: the kernel may start while its predecessor drains and must
-// call pdl_wait() before touching the predecessor's outputs (every kernel of
-// this library does).
-bool pdl_enabled();
-void set_pdl_enabled(bool on);
+// Launch `kernel` on `st` with programmatic dependent launch allowed: the
+// kernel may start while its predecessor drains and must call pdl_wait()
+// before touching the predecessor's outputs (every kernel of this library
+// does).
 
 template <typename... KArgs, typename... Args>
 cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
@@ -27,7 +25,7 @@ cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t sme
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
@@ -44,7 +42,7 @@ cudaError_t launch_k_cluster(void (*kernel)(KArgs...), dim3 grid, dim3 block, si
   cfg.stream = st;
   cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = pdl_enabled() ? 1 : 0;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
   attr[1].id = cudaLaunchAttributeClusterDimension;
   attr[1].val.clusterDim.x = cluster_x;
   attr[1].val.clusterDim.y = 1;
@@ -262,7 +260,6 @@ cudaError_t launch_attention(const AttnPlan& p, const AttnArgs& a, const CUtenso
 // tcgen05 context attention (attention_tc.cu)
 bool attention_tc_supported(int D, int rows);
 int attention_tc_splits(int B, int Hkv, int max_ctx);
-int attention_tc_smem_bytes();
 bool attention_tc_stacked_supported(int G, int S);
 cudaError_t launch_attention_tc(const AttnArgs& a, int n_ctx, const CUtensorMap& map_k128,
                                 const CUtensorMap& map_v128, const CUtensorMap& map_q, cudaStream_t st,
@@ -352,7 +349,6 @@ cudaError_t launch_set_int(int* dst, int value, cudaStream_t st);
 cudaError_t launch_loop_init(int32_t* small, int max_steps, cudaStream_t st);
 cudaError_t launch_loop_control(int32_t* small, cudaGraphConditionalHandle handle, cudaStream_t st);
 cudaError_t launch_init_block(int32_t* tokens, uint32_t* mask, int B, int S, int V, cudaStream_t st);
-cudaError_t launch_copy_i32(int32_t* dst, const int32_t* src, int n, cudaStream_t st);
 cudaError_t launch_wait_forever_bounded(int* status, uint64_t timeout_ns, cudaStream_t st);
 
 // Set the thread-local message dd_last_error() returns.

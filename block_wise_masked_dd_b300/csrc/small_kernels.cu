@@ -636,11 +636,6 @@ __global__ void k_init_block(int32_t* tokens, uint32_t* mask, int B, int S, int 
   if (e < B) mask[e] = S == 32 ? 0xffffffffu : ((1u << S) - 1u);
 }
 
-__global__ void k_copy_i32(int32_t* dst, const int32_t* src, int n) {
-  const int e = blockIdx.x * blockDim.x + threadIdx.x;
-  if (e < n) dst[e] = src[e];
-}
-
 // Waits on a barrier that nothing completes, bounded by timeout_ns: the
 // timeout path of every pipelined kernel, in isolation.
 __global__ void k_wait_forever_bounded(int* status, uint64_t timeout_ns) {
@@ -806,21 +801,9 @@ cudaError_t launch_init_block(int32_t* tokens, uint32_t* mask, int B, int S, int
   return cudaGetLastError();
 }
 
-cudaError_t launch_copy_i32(int32_t* dst, const int32_t* src, int n, cudaStream_t st) {
-  k_copy_i32<<<(n + 255) / 256, 256, 0, st>>>(dst, src, n);
-  return cudaGetLastError();
-}
-
 cudaError_t launch_wait_forever_bounded(int* status, uint64_t timeout_ns, cudaStream_t st) {
   k_wait_forever_bounded<<<1, 32, 0, st>>>(status, timeout_ns);
   return cudaGetLastError();
 }
-
-namespace {
-bool g_pdl = true;
-}
-
-bool pdl_enabled() { return g_pdl; }
-void set_pdl_enabled(bool on) { g_pdl = on; }
 
 }  // namespace dd
