@@ -60,6 +60,17 @@ def test_workspace_size_host_only(lib):
     (dict(hidden=200), B.DD_ERR_UNSUPPORTED),
     (dict(batch=1, block=8), B.DD_ERR_UNSUPPORTED),
     (dict(max_ctx=-1), B.DD_ERR_INVALID_ARG),
+    (dict(batch=0), B.DD_ERR_INVALID_ARG),
+    (dict(n_q_heads=32, n_kv_heads=1), B.DD_ERR_UNSUPPORTED),          # 32 query rows per key head x 16 > 128
+    (dict(hidden=3072), B.DD_ERR_UNSUPPORTED),                         # above 2048 only 4096
+    (dict(hidden=8192), B.DD_ERR_UNSUPPORTED),
+    (dict(mlp=100), B.DD_ERR_UNSUPPORTED),
+    (dict(n_q_heads=1, n_kv_heads=1), B.DD_ERR_UNSUPPORTED),           # q|k|v width 192, not a multiple of 128
+    (dict(n_layers=0), B.DD_ERR_INVALID_ARG),
+    (dict(rms_eps=-1.0), B.DD_ERR_INVALID_ARG),
+    (dict(rms_eps=float("nan")), B.DD_ERR_INVALID_ARG),
+    (dict(rope_theta=-1.0), B.DD_ERR_INVALID_ARG),
+    (dict(rope_theta=float("inf")), B.DD_ERR_INVALID_ARG),
 ])
 def test_bad_configs_rejected(lib, bad, code):
     cfg = synth.TINY.replace(**bad)
@@ -67,6 +78,18 @@ def test_bad_configs_rejected(lib, bad, code):
         B.dd_workspace_size(config_struct(cfg))
     assert e.value.status == code
     assert B.dd_last_error()
+
+
+@pytest.mark.parametrize("edge", [
+    dict(block=32),                                   # the widest block the mask word holds
+    dict(batch=1, block=16, max_ctx=0),               # no context at all
+    dict(hidden=4096),
+    dict(hidden=128, mlp=128, vocab=256),             # the smallest widths
+    dict(n_q_heads=8, n_kv_heads=1),                  # 8 query heads per key head x 16 = 128 rows
+    dict(rope_theta=10000.0),
+])
+def test_edge_configs_accepted(lib, edge):
+    assert B.dd_workspace_size(config_struct(synth.TINY.replace(**edge))) > 0
 
 
 def test_null_pointers_rejected_before_cuda(lib):
