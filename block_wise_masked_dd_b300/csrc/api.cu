@@ -186,8 +186,10 @@ dd_status check_config(const dd_config* c) {
   if ((G * c->block) % 16 || G * c->block > 128)
     return fail(DD_ERR_UNSUPPORTED, "(n_q_heads/n_kv_heads)*block must be a multiple of 16 and <= 128 (got %d)",
                 G * c->block);
-  if (c->hidden < 128 || c->hidden % 128)
-    return fail(DD_ERR_UNSUPPORTED, "hidden must be a multiple of 128 (got %d)", c->hidden);
+  // The row kernels (embedding, norms) give a row hidden/8 threads, which
+  // must be whole warps for their warp-wide reductions.
+  if (c->hidden < 256 || c->hidden % 256)
+    return fail(DD_ERR_UNSUPPORTED, "hidden must be a multiple of 256 (got %d)", c->hidden);
   if (c->hidden > 4096 || (c->hidden > 2048 && c->hidden % 2048))
     return fail(DD_ERR_UNSUPPORTED, "hidden must be <= 2048, or 4096 (got %d)", c->hidden);
   if (c->mlp < 128 || c->mlp % 128) return fail(DD_ERR_UNSUPPORTED, "mlp must be a multiple of 128 (got %d)", c->mlp);

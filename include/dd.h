@@ -75,9 +75,11 @@ enum {
 
 /* Model and batch shape.  Supported: 1 <= block <= 32 with batch*block a
  * multiple of 16; head_dim 64 or 128; (n_q_heads/n_kv_heads)*block a multiple
- * of 16 and at most 128; hidden, mlp and (n_q_heads+2*n_kv_heads)*head_dim
- * multiples of 128; n_q_heads*head_dim a multiple of 64; vocab a multiple of
- * 256; max_ctx >= 0. */
+ * of 16 and at most 128; hidden a multiple of 256 and at most 2048, or 4096
+ * (the row kernels give each row hidden/8 threads, whole warps); mlp and
+ * (n_q_heads+2*n_kv_heads)*head_dim multiples of 128; n_q_heads*head_dim a
+ * multiple of 64; vocab a multiple of 256; max_ctx >= 0.  Other shapes are
+ * refused with DD_ERR_UNSUPPORTED (or DD_ERR_INVALID_ARG). */
 typedef struct dd_config {
   int32_t batch;      /* B: sequences decoded together */
   int32_t block;      /* S: positions per block */

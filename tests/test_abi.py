@@ -58,6 +58,8 @@ def test_workspace_size_host_only(lib):
     (dict(n_kv_heads=3), B.DD_ERR_INVALID_ARG),
     (dict(vocab=1000), B.DD_ERR_UNSUPPORTED),
     (dict(hidden=200), B.DD_ERR_UNSUPPORTED),
+    (dict(hidden=128), B.DD_ERR_UNSUPPORTED),                          # hidden/8 = 16 threads: half a warp
+    (dict(hidden=640), B.DD_ERR_UNSUPPORTED),                          # 80 threads: 2.5 warps
     (dict(batch=1, block=8), B.DD_ERR_UNSUPPORTED),
     (dict(max_ctx=-1), B.DD_ERR_INVALID_ARG),
     (dict(batch=0), B.DD_ERR_INVALID_ARG),
@@ -84,7 +86,8 @@ def test_bad_configs_rejected(lib, bad, code):
     dict(block=32),                                   # the widest block the mask word holds
     dict(batch=1, block=16, max_ctx=0),               # no context at all
     dict(hidden=4096),
-    dict(hidden=128, mlp=128, vocab=256),             # the smallest widths
+    dict(hidden=256, mlp=128, vocab=256),             # the smallest widths
+    dict(hidden=768),                                 # 96 threads per row: three warps
     dict(n_q_heads=8, n_kv_heads=1),                  # 8 query heads per key head x 16 = 128 rows
     dict(rope_theta=10000.0),
 ])
