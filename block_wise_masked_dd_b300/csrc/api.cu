@@ -1068,6 +1068,7 @@ dd_status dd_block_attention(const dd_attn_problem* p, void* stream) {
   dd::AttnPlan plan;
   const size_t need = attn_ws_bytes(p, &plan);
   if (p->workspace_bytes < need) return fail(DD_ERR_INVALID_ARG, "workspace too small: %zu < %zu", p->workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(p->workspace) % 256) return fail(DD_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   if (!encode_fn()) return fail(DD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   DD_CUDA(dd::prepare_kernels());
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1081,8 +1082,9 @@ dd_status dd_block_attention(const dd_attn_problem* p, void* stream) {
       !dd::make_map_3d(&mk128, p->k_ctx, planes, ext, p->ctx_stride, p->head_dim, 128) ||
       !dd::make_map_3d(&mv128, p->v_ctx, planes, ext, p->ctx_stride, p->head_dim, 128))
     return fail(DD_ERR_CUDA, "tensor map encoding failed for k_ctx/v_ctx");
-  int* small = reinterpret_cast<int*>(ws);  // [0] ctx_len, [1] status
-  DD_CUDA(dd::launch_set_int(small, p->ctx_len, st));
+  int* small = reinterpret_cast<int*>(ws);  // [0] status (the caller may read it), [1] ctx_len
+  DD_CUDA(cudaMemsetAsync(small, 0, 4, st));
+  DD_CUDA(dd::launch_set_int(small + 1, p->ctx_len, st));
   dd::AttnArgs a{};
   a.qkv = p->qkv;
   a.ld_qkv = (p->n_q_heads + 2 * p->n_kv_heads) * p->head_dim;
@@ -1091,7 +1093,7 @@ dd_status dd_block_attention(const dd_attn_problem* p, void* stream) {
   a.Hq = p->n_q_heads;
   a.Hkv = p->n_kv_heads;
   a.G = p->n_q_heads / p->n_kv_heads;
-  a.ctx_len = small;
+  a.ctx_len = small + 1;
   a.z0 = 0;
   a.out = p->out;
   a.ld_out = p->n_q_heads * p->head_dim;
@@ -1099,7 +1101,7 @@ dd_status dd_block_attention(const dd_attn_problem* p, void* stream) {
   a.part_ml = reinterpret_cast<float2*>(
       ws + 256 + align_up((size_t)p->batch * p->n_kv_heads * plan.n_splits * plan.rows * p->head_dim * 4, 16));
   a.scale_log2 = 1.4426950408889634f / sqrtf((float)p->head_dim);
-  a.status = small + 1;
+  a.status = small;
   a.timeout_ns = dd::kDefaultTimeoutNs;
   a.max_pair_splits = p->batch * p->n_kv_heads * plan.n_splits;
   CUtensorMap mq;
@@ -1126,6 +1128,7 @@ dd_status dd_lmhead_select(int32_t rows, int32_t hidden, int32_t vocab, const vo
   if (s != DD_OK) return s;
   if (!x || !w || !conf || !arg || !workspace) return fail(DD_ERR_INVALID_ARG, "null pointer");
   if (workspace_bytes < need) return fail(DD_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) % 256) return fail(DD_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   if (!encode_fn()) return fail(DD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   DD_CUDA(dd::prepare_kernels());
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1140,6 +1143,7 @@ dd_status dd_lmhead_select(int32_t rows, int32_t hidden, int32_t vocab, const vo
   o.sel_m = reinterpret_cast<float*>(ws + 256);
   o.sel_s = reinterpret_cast<float*>(ws + 256 + n);
   o.sel_a = reinterpret_cast<int*>(ws + 256 + 2 * n);
+  DD_CUDA(cudaMemsetAsync(ws, 0, 4, st));  // the call's status word
   DD_CUDA(dd::launch_gemm(p, mx, mw, o, reinterpret_cast<int*>(ws), dd::kDefaultTimeoutNs, st));
   DD_CUDA(dd::launch_select_combine(o.sel_m, o.sel_s, o.sel_a, p.n_tiles, rows, conf, arg, st));
   return DD_OK;
@@ -1173,6 +1177,7 @@ dd_status dd_gemm(int32_t rows, int32_t n, int32_t k, const void* x, const void*
   if (s != DD_OK) return s;
   if (!x || !w || !y || !workspace) return fail(DD_ERR_INVALID_ARG, "null pointer");
   if (workspace_bytes < need) return fail(DD_ERR_INVALID_ARG, "workspace too small: %zu < %zu", workspace_bytes, need);
+  if (reinterpret_cast<uintptr_t>(workspace) % 256) return fail(DD_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   if (!encode_fn()) return fail(DD_ERR_CUDA, "cuTensorMapEncodeTiled is not available");
   DD_CUDA(dd::prepare_kernels());
   cudaStream_t st = static_cast<cudaStream_t>(stream);
@@ -1186,6 +1191,7 @@ dd_status dd_gemm(int32_t rows, int32_t n, int32_t k, const void* x, const void*
   o.split_stride = (long long)rows * n;
   o.ld = n;
   o.rows_valid = rows;
+  DD_CUDA(cudaMemsetAsync(ws, 0, 4, st));  // the call's status word
   DD_CUDA(dd::launch_gemm(p, mw, mx, o, reinterpret_cast<int*>(ws), dd::kDefaultTimeoutNs, st));
   DD_CUDA(dd::launch_reduce_f32(o.partial, dd::slot_plan(p), o.split_stride, rows, n, y, st));
   return DD_OK;

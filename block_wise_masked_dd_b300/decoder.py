@@ -205,6 +205,13 @@ def join_split(t: torch.Tensor) -> torch.Tensor:
 
 # ------------------------------------------------------------- single kernels
 
+def workspace_status(ws: torch.Tensor) -> int:
+    """The status word a single-kernel call leaves in the first 4 bytes of its
+    workspace: 0, or non-zero if a bounded wait inside a kernel expired."""
+    torch.cuda.synchronize(ws.device)
+    return int(ws[:4].view(torch.int32).item())
+
+
 class BlockAttention:
     """dd_block_attention with a persistent workspace (for repeated launches)."""
 
@@ -220,6 +227,10 @@ class BlockAttention:
         self.p.qkv, self.p.k_ctx, self.p.v_ctx, self.p.out = _ptr(qkv), _ptr(k_ctx), _ptr(v_ctx), _ptr(out)
         B.dd_block_attention(self.p, _stream(stream))
         return out
+
+    def status(self) -> int:
+        """The last call's status word (0, or non-zero if a bounded wait expired); synchronises."""
+        return workspace_status(self.workspace)
 
 
 def block_attention(qkv, k_ctx, v_ctx, ctx_len, batch, block, n_q_heads, n_kv_heads, head_dim, stream=None):
@@ -239,6 +250,10 @@ class LmHeadSelect:
         B.dd_lmhead_select(self.rows, self.hidden, self.vocab, _ptr(x), _ptr(w), _ptr(conf), _ptr(arg),
                            _ptr(self.workspace), self.workspace.numel(), _stream(stream))
         return conf, arg
+
+    def status(self) -> int:
+        """The last call's status word (0, or non-zero if a bounded wait expired); synchronises."""
+        return workspace_status(self.workspace)
 
 
 def lmhead_select(x, w, stream=None):

@@ -318,12 +318,15 @@ dd_status dd_profile_step(dd_ctx* ctx, int32_t* tokens, uint32_t* mask, float ga
  * ctx_len context keys and the S block keys of kv head h/(Hq/Hkv), scale
  * 1/sqrt(D), no mask.
  *   qkv:   bf16 [B*S][(Hq+2*Hkv)*D], row b*S+i holds q (Hq heads), k, v of position i
- *   k_ctx, v_ctx: bf16 [B][Hkv][ctx_stride][D] (positions >= ctx_len not read
- *          for their values; they must hold finite numbers)
+ *   k_ctx, v_ctx: bf16 [B][Hkv][ctx_stride][D] (positions >= ctx_len are
+ *          never used: they may hold anything, NaN included)
  *   out:   bf16 [B*S][Hq*D]
  *   workspace: device scratch of dd_block_attention_workspace_size() bytes
- *          (split-context partials), 256-byte aligned.
- * All pointers device memory, 16-byte aligned. */
+ *          (split-context partials), 256-byte aligned.  Its first 4 bytes are
+ *          the call's status word (int32): the call clears it, and a kernel
+ *          whose bounded wait expires sets it non-zero, in which case `out`
+ *          is not valid.  Read it once the stream has completed the call.
+ * All pointers device memory, 16-byte aligned.  Asynchronous on `stream`. */
 typedef struct dd_attn_problem {
   int32_t batch, block, n_q_heads, n_kv_heads, head_dim;
   int32_t ctx_len, ctx_stride;
@@ -342,8 +345,13 @@ dd_status dd_block_attention(const dd_attn_problem* p, void* stream);
  * the tensor cores, never written to memory), then per row conf = 1/sum_v
  * exp(l_v - max) and arg = the lowest id of the maximum logit.
  *   x: bf16 [rows][hidden], w: bf16 [vocab][hidden], conf: fp32 [rows], arg: int32 [rows]
- *   workspace: dd_lmhead_select_workspace_size() bytes (per-tile partials).
- * hidden a multiple of 64, vocab a multiple of 256, rows >= 1. */
+ *   workspace: dd_lmhead_select_workspace_size() bytes (per-tile partials),
+ *   256-byte aligned; its first 4 bytes are the call's status word (int32),
+ *   cleared by the call and set non-zero by a kernel whose bounded wait
+ *   expires, in which case conf and arg are not valid (read it once the
+ *   stream has completed the call).
+ * hidden a multiple of 64, vocab a multiple of 256, rows >= 1.  Device
+ * memory; asynchronous on `stream`. */
 dd_status dd_lmhead_select_workspace_size(int32_t rows, int32_t hidden, int32_t vocab, size_t* bytes);
 dd_status dd_lmhead_select(int32_t rows, int32_t hidden, int32_t vocab, const void* x, const void* w,
                            float* conf, int32_t* arg, void* workspace, size_t workspace_bytes, void* stream);
@@ -376,7 +384,11 @@ dd_status dd_lmhead_select_noalloc(int32_t rows, int32_t hidden, int32_t vocab, 
 /* Plain tensor-core GEMM y = x w^T with fp32 output, through the same kernel
  * the linear layers use.  x: bf16 [rows][k], w: bf16 [n][k], y: fp32 [rows][n].
  * n a multiple of 128, k a multiple of 64, rows a multiple of 16.  workspace:
- * dd_gemm_workspace_size() bytes (split-K partials). */
+ * dd_gemm_workspace_size() bytes (split-K partials), 256-byte aligned; its
+ * first 4 bytes are the call's status word (int32), cleared by the call and
+ * set non-zero by a kernel whose bounded wait expires, in which case y is not
+ * valid (read it once the stream has completed the call).  Device memory;
+ * asynchronous on `stream`. */
 dd_status dd_gemm_workspace_size(int32_t rows, int32_t n, int32_t k, size_t* bytes);
 dd_status dd_gemm(int32_t rows, int32_t n, int32_t k, const void* x, const void* w, float* y,
                   void* workspace, size_t workspace_bytes, void* stream);

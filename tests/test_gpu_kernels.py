@@ -229,3 +229,43 @@ def test_bounded_wait_reports_timeout():
     # the context is still usable afterwards
     x = torch.ones(4, device="cuda")
     assert float((x * 2).sum()) == 8.0
+
+
+def test_single_kernel_calls_clear_their_status_word():
+    """dd_block_attention, dd_lmhead_select and dd_gemm clear the status word
+    in the first 4 bytes of their workspace, and no wait expires on these
+    inputs, so each leaves it 0 (a stale non-zero word is planted first)."""
+    from block_wise_masked_dd_b300 import binding as B
+    from block_wise_masked_dd_b300.decoder import BlockAttention, LmHeadSelect, workspace_status
+    dev = "cuda"
+    g = torch.Generator(device=dev).manual_seed(7)
+    nb, S, Hq, Hkv, D, T, stride = 2, 16, 8, 2, 128, 300, 384  # the tcgen05 context path and its merge
+    op = BlockAttention(nb, S, Hq, Hkv, D, T, stride, dev)
+    op.workspace[:4].fill_(0xFF)
+    qkv = torch.randn(nb * S, (Hq + 2 * Hkv) * D, device=dev, generator=g).bfloat16()
+    kc = torch.randn(nb, Hkv, stride, D, device=dev, generator=g).bfloat16()
+    vc = torch.randn(nb, Hkv, stride, D, device=dev, generator=g).bfloat16()
+    out = torch.empty(nb * S, Hq * D, dtype=torch.bfloat16, device=dev)
+    op(qkv, kc, vc, out)
+    assert op.status() == 0 and torch.isfinite(out.float()).all()
+
+    rows, H, V = 128, 256, 4096
+    lm = LmHeadSelect(rows, H, V, dev)
+    lm.workspace[:4].fill_(0xFF)
+    x = torch.randn(rows, H, device=dev, generator=g).bfloat16()
+    w = torch.randn(V, H, device=dev, generator=g).bfloat16()
+    conf = torch.empty(rows, dtype=torch.float32, device=dev)
+    arg = torch.empty(rows, dtype=torch.int32, device=dev)
+    lm(x, w, conf, arg)
+    assert lm.status() == 0 and bool(((arg >= 0) & (arg < V)).all())
+
+    n, k = 256, 256
+    ws_bytes = B.dd_gemm_workspace_size(rows, n, k)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    ws[:4].fill_(0xFF)
+    wg = torch.randn(n, k, device=dev, generator=g).bfloat16()
+    y = torch.empty(rows, n, dtype=torch.float32, device=dev)
+    B.dd_gemm(rows, n, k, x.data_ptr(), wg.data_ptr(), y.data_ptr(), ws.data_ptr(), ws_bytes,
+              torch.cuda.current_stream().cuda_stream)
+    assert workspace_status(ws) == 0
+    torch.testing.assert_close(y, x.float() @ wg.float().t(), rtol=1e-2, atol=1e-2)
